@@ -1,0 +1,29 @@
+"""CPU oracle for the mixed prefill+decode layer step.
+
+TEST INFRASTRUCTURE ONLY.  Nothing in the product path may import, call or
+execute this package: only the tests, ``__graft_entry__.smoke()`` and the
+``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` use it.  It shares
+no code with the CUDA library; both are fed from the seeded generator in
+``mixed_prefill_decode_gb300.workload``.
+
+Modules
+  layer       the layer step in float64 NumPy, KV read through the block table
+  packer      the token-budget packer
+  step_model  the roofline step-time model of the pofe.ai "Chunked prefill" page
+
+Parity status (what pins each part, tests in ``tests/test_oracle_*.py``):
+  attention   torch SDPA (float64, explicit mask) on gathered KV; kv = 1 gives
+              o = v; identical keys give mean(v); chunked == unchunked prefill;
+              decode == last row of prefill; page permutation invariance
+  rope        complex-multiplication form; position 0 is the identity; norm
+              preservation; relative-position invariance
+  rms_norm    torch.nn.functional.rms_norm; scale invariance; constant rows
+  linear      one-hot weights select the expected input column
+  swiglu      silu closed form at 0 and large |x|; gate/up half order
+  layer       all-zero weights give y = x; composition of the pinned parts
+              (the pages print no worked layer output: beyond that, parity
+              unpinned)
+  packer      the worked example of the pofe.ai page (8 x (64 + 512) at budget
+              576) and brute-force invariants
+  step_model  every number the pofe.ai page prints from its model
+"""

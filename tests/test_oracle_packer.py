@@ -1,0 +1,137 @@
+"""Pins for the oracle packer: the worked example of the pofe.ai "Chunked
+prefill" page and brute-force invariants over seeded random request streams.
+CPU only."""
+
+import json
+import os
+
+import numpy as np
+import pytest
+
+from oracle.packer import Packer, NoSpace, pages_for, rows_to_csr
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden", "pofe_packer_example.json")
+
+
+def test_worked_example_eight_mixed_iterations():
+    g = json.load(open(GOLD))
+    pk = Packer(budget=g["budget"], max_seqs=1000, chunk_cap=0, free_order=range(100000))
+    for i in range(g["running_decodes"]):
+        pk.add(i, prompt_len=g["decode_context"], computed=g["decode_context"])
+    pk.add(9999, prompt_len=g["prompt_len"])
+    for it in range(g["mixed_iterations"]):
+        rows = pk.pack()
+        dec = [r for r in rows if r[1] == 1]
+        pre = [r for r in rows if r[0] == 9999]
+        assert len(dec) == g["running_decodes"]
+        assert len(pre) == 1 and pre[0][1] == g["chunk_tokens_per_iteration"]
+        assert pre[0][2] == (it + 1) * g["chunk_tokens_per_iteration"]
+        assert sum(r[1] for r in rows) == g["budget"]
+    rows = pk.pack()
+    assert len(rows) == g["decodes_in_iteration_after_prompt"]
+    assert all(r[1] == 1 for r in rows)
+    assert rows[-1][0] == 9999 and rows[-1][2] == g["prompt_len"] + 1
+
+
+def test_decodes_first_then_partials_then_admissions_fifo():
+    pk = Packer(budget=20, max_seqs=10, chunk_cap=0, free_order=range(100))
+    pk.add(1, 5, computed=5)      # running
+    pk.add(2, 30, computed=10)    # partial
+    pk.add(3, 4)                  # waiting
+    pk.add(4, 100)                # waiting
+    rows = pk.pack()
+    assert [(r[0], r[1]) for r in rows] == [(1, 1), (2, 19)]
+    rows = pk.pack()
+    assert [(r[0], r[1]) for r in rows] == [(1, 1), (2, 1), (3, 4), (4, 14)]
+    rows = pk.pack()   # 2 and 3 are decoding now
+    assert [(r[0], r[1]) for r in rows] == [(1, 1), (2, 1), (3, 1), (4, 17)]
+
+
+def test_decodes_never_exceed_budget():
+    pk = Packer(budget=3, max_seqs=10, chunk_cap=0, free_order=range(100))
+    for i in range(5):
+        pk.add(i, 7, computed=7)
+    rows = pk.pack()
+    assert [r[0] for r in rows] == [0, 1, 2]
+
+
+def test_chunk_cap_and_max_seqs_and_page_exhaustion():
+    pk = Packer(budget=100, max_seqs=2, chunk_cap=30, free_order=range(4))
+    pk.add(1, 50)
+    pk.add(2, 50)
+    pk.add(3, 50)
+    rows = pk.pack()
+    # cap 30 each; the third is refused by max_seqs; 2 + 2 pages used
+    assert [(r[0], r[1]) for r in rows] == [(1, 30), (2, 30)]
+    rows = pk.pack()
+    # no page left: each partial keeps to its pages (32 tokens) -> 2 more each
+    assert [(r[0], r[1], r[2]) for r in rows] == [(1, 2, 32), (2, 2, 32)]
+    rows = pk.pack()
+    assert rows == []
+    pk.finish(1)
+    rows = pk.pack()
+    # 1's two pages go to 2 (which completes); 3 finds no page left for its chunk
+    assert [(r[0], r[1], r[2]) for r in rows] == [(2, 18, 50)]
+    rows = pk.pack()
+    assert [(r[0], r[1], r[2]) for r in rows] == [(2, 1, 51)]
+    pk.finish(2)
+    rows = pk.pack()
+    assert [(r[0], r[1], r[2], r[3]) for r in rows] == [(3, 30, 30, [2, 3])]
+
+
+def test_admission_stops_at_first_failure():
+    pk = Packer(budget=64, max_seqs=8, chunk_cap=0, free_order=range(2))
+    pk.add(1, 40)   # needs 3 pages for 40 tokens -> refused, and blocks 2
+    pk.add(2, 5)
+    assert pk.pack() == []
+
+
+def test_add_running_needs_pages():
+    pk = Packer(budget=8, max_seqs=8, chunk_cap=0, free_order=range(2))
+    with pytest.raises(NoSpace):
+        pk.add(1, 40, computed=40)
+
+
+def _random_stream(seed, steps=60):
+    rng = np.random.default_rng(seed)
+    P = int(rng.integers(8, 200))
+    pk = Packer(budget=int(rng.integers(1, 300)), max_seqs=int(rng.integers(1, 12)),
+                chunk_cap=int(rng.choice([0, 0, 16, 100])), free_order=rng.permutation(P))
+    nid = 0
+    for _ in range(steps):
+        if rng.random() < 0.5:
+            pk.add(nid, int(rng.integers(1, 400)))
+            nid += 1
+        if pk.reqs and rng.random() < 0.2:
+            pk.finish(int(rng.choice(sorted(pk.reqs))))
+        before = {rid: r.computed for rid, r in pk.reqs.items()}
+        running_before = [r.rid for r in pk.running]
+        rows = pk.pack()
+        yield pk, P, rows, before, running_before
+
+
+@pytest.mark.parametrize("seed", range(25))
+def test_invariants_random_streams(seed):
+    for pk, P, rows, before, running_before in _random_stream(seed):
+        total = sum(r[1] for r in rows)
+        assert total <= pk.budget
+        ids = [r[0] for r in rows]
+        assert len(set(ids)) == len(ids)
+        # decodes come first, in running order
+        nd = sum(1 for rid in ids if rid in running_before)
+        assert ids[:nd] == [rid for rid in running_before if rid in ids]
+        # budget ran out before any running decode was skipped for budget
+        if nd < len(running_before) and pk.budget >= len(running_before):
+            assert len(pk.free) == 0 or any(
+                pages_for(before[rid] + 1) - pages_for(before[rid]) > 0 for rid in running_before if rid not in ids)
+        all_pages = []
+        for rid, qo, kv, table in rows:
+            assert qo >= 1 and kv == before[rid] + qo
+            assert len(table) == pages_for(kv)
+            all_pages.extend(table)
+        assert len(set(all_pages)) == len(all_pages)
+        # conservation of pages: held + free == pool
+        held = [p for r in pk.reqs.values() for p in r.pages]
+        assert sorted(held + list(pk.free)) == list(range(P))
+        q, kvl, bti, bt, rid = rows_to_csr(rows)
+        assert q[-1] == total and len(bt) == bti[-1]
