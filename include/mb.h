@@ -1,0 +1,237 @@
+/*
+ * mb.h -- one transformer-layer step over a mixed prefill+decode batch, on one
+ * GB300 (sm_103a).  C ABI: plain pointers and sizes only.
+ *
+ * The operation.  A mixed batch holds, per request r, qo_len[r] new tokens and
+ * a KV cache that holds kv_len[r] = cached prefix + qo_len[r] tokens once this
+ * step has appended its own.  Prefill chunks (qo_len > 1) and decodes
+ * (qo_len = 1) share one token-batched pass through the linear layers, then
+ * split into a ragged attention over a 16-token paged KV cache:
+ *   - ConfluxServe summary (paper-daily.com), "Why can linear layers be batched
+ *     but attention cannot?": tokens of both phases form one matrix multiply,
+ *     weights are read once; attention splits per request.
+ *   - pofe.ai "Chunked prefill", "How it works, step by step", step 4: one
+ *     forward pass over the flattened tokens; prompt chunks write their K/V into
+ *     the cache and attend causally to everything cached so far; decodes append
+ *     one token.
+ *   - llm-stack-book 7.8, "Attention on Partial KV Caches": a query at position
+ *     T_past + i sees keys 0 .. T_past + i.
+ *   - Perplexity "Disaggregated Prefill and Decode", "Prefill versus
+ *     Decode-prestaties": qo_len / kv_len framing of prefill and decode rows.
+ *
+ * The layer (pre-norm, no biases; the pages never write one out, this is the
+ * plainest Llama-3 / Qwen3 reading):
+ *   xn = RMSNorm(x) g_attn;  [q k v] = xn W_qkv^T;  (Qwen3) q,k = RMSNorm_hd(.) g_q,g_k
+ *   q,k = RoPE(rotate-half, pos = cached + i, theta);  append k,v;  o = attention
+ *   h = x + o W_o^T;  a = silu(RMSNorm(h) g_ffn W_gate^T) * (RMSNorm(h) g_ffn W_up^T)
+ *   y = h + a W_down^T
+ *
+ * Conventions for every call:
+ *   - Return value is an mb_status; on failure mb_last_error() gives a message
+ *     (thread-local, valid until the next failing call on that thread).
+ *   - "device" pointers are CUDA device addresses on the current device; "host"
+ *     pointers are ordinary CPU memory.  Nothing here takes ownership of a
+ *     caller pointer unless stated.
+ *   - Asynchronous calls run on the given stream (a cudaStream_t passed as
+ *     void*; NULL = the legacy default stream).  Argument and descriptor
+ *     errors are returned before anything is launched.  A device-side check
+ *     that fails records an error word that mb_device_status() reports.
+ *   - There is no CPU fallback: without a usable sm_103a device every compute
+ *     call returns MB_ECUDA or MB_EUNSUPPORTED.
+ */
+#ifndef MB_H_
+#define MB_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MB_OK = 0,
+  MB_EINVAL = -1,        /* bad argument or malformed batch descriptor */
+  MB_ENOMEM = -2,        /* device or pinned-host allocation failed */
+  MB_ENOSPACE = -3,      /* KV pages exhausted (scheduler) */
+  MB_ECUDA = -4,         /* a CUDA runtime / driver call failed */
+  MB_EUNSUPPORTED = -5,  /* shape or device the kernels do not handle */
+  MB_EDEVICE = -6        /* a kernel recorded an error (bounds, wait limit) */
+} mb_status;
+
+#define MB_PAGE_TOKENS 16
+
+/* Model shape of one layer.  Supported: head_dim in {64, 128}; n_q_heads a
+ * multiple of n_kv_heads (GQA group = n_q_heads / n_kv_heads, any value up to
+ * 8); d_model, n_q_heads*head_dim and d_ff multiples of 128; max_tokens >= 1. */
+typedef struct {
+  int32_t d_model;
+  int32_t n_q_heads;
+  int32_t n_kv_heads;
+  int32_t head_dim;
+  int32_t d_ff;
+  float rms_eps;
+  float rope_theta;
+  int32_t qk_norm;      /* 1: per-head RMSNorm on q and k before RoPE (Qwen3) */
+  int32_t max_tokens;   /* largest T = sum(qo_len) any step will pass */
+} mb_layer_desc;
+
+/* Device bf16 weights, caller-owned, must outlive the layer.  Linear weights
+ * are row-major [N][K] (y = x W^T), rows 16-byte aligned:
+ *   w_qkv     [(Hq + 2 Hkv) hd][d]   rows: Q heads, then K heads, then V heads
+ *   w_o       [d][Hq hd]
+ *   w_gate_up [2 F][d]               rows: gate (F), then up (F)
+ *   w_down    [d][F]
+ *   g_attn, g_ffn [d];  g_q, g_k [hd] (may be NULL when qk_norm == 0). */
+typedef struct {
+  const void *g_attn, *w_qkv, *g_q, *g_k, *w_o, *g_ffn, *w_gate_up, *w_down;
+} mb_layer_weights;
+
+/* Batch descriptor, HOST int32 arrays (CSR).  Request r owns step tokens
+ * [qo_indptr[r], qo_indptr[r+1]) (so T = qo_indptr[num_reqs]), holds
+ * kv_len[r] keys once this step's tokens are appended, and its KV pages are
+ * bt[bt_indptr[r] .. bt_indptr[r+1]).  Token p of request r lives in page
+ * bt[bt_indptr[r] + p / 16], slot p % 16.  Rules, checked on the host:
+ * qo_indptr[0] = 0; 1 <= qo_len <= kv_len; table length >= ceil(kv_len / 16);
+ * page ids in [0, num_pages) and distinct across the whole batch;
+ * T <= max_tokens.  A request with qo_len = 1 is a decode row. */
+typedef struct {
+  int32_t num_reqs;
+  const int32_t *qo_indptr;
+  const int32_t *kv_len;
+  const int32_t *bt_indptr;
+  const int32_t *bt;
+} mb_batch;
+
+typedef struct mb_layer mb_layer;
+typedef struct mb_kv mb_kv;
+
+/* Create a layer: validates the shape, keeps the weight pointers, allocates
+ * the library-owned workspaces for max_tokens tokens on the current device.
+ * Errors: MB_EINVAL (shape), MB_EUNSUPPORTED (shape or device not sm_103),
+ * MB_ENOMEM, MB_ECUDA. */
+mb_status mb_layer_create(const mb_layer_desc *desc, const mb_layer_weights *w, mb_layer **out);
+
+/* Free a layer and its workspaces (synchronises the device first). */
+mb_status mb_destroy(mb_layer *layer);
+
+/* A paged KV pool for this layer: num_pages pages of
+ * [2 (K, V)][n_kv_heads][16 slots][head_dim] bf16 (the HND layout of the
+ * Perplexity page, "Gesharcde KV Cache Transfers": each head of a page is one
+ * contiguous 16 x hd block).  dev_buf: caller device memory of
+ * num_pages * 2 * Hkv * 16 * hd * 2 bytes, 128-byte aligned, or NULL to let
+ * the library allocate (contents then undefined).  Errors: MB_EINVAL,
+ * MB_ENOMEM, MB_ECUDA. */
+mb_status mb_kv_alloc(mb_layer *layer, int32_t num_pages, void *dev_buf, mb_kv **out);
+
+/* Element strides of the pool as [page][kv][head][slot][dim] and its base. */
+mb_status mb_kv_layout(const mb_kv *kv, int64_t strides[5], void **base);
+
+/* Release a pool (frees the memory only if the library allocated it). */
+mb_status mb_kv_free(mb_kv *kv);
+
+/* One layer step, asynchronous on `stream`.
+ *   x_in  device bf16 [T][d_model], read only
+ *   x_out device bf16 [T][d_model], written; must not alias x_in
+ * K/V of every new token are written into `kv` before attention reads it.
+ * The descriptor is copied during the call; the caller may reuse its arrays
+ * on return.  Workspaces are shared by successive steps of one layer, so
+ * steps of one layer must be issued on one stream (or otherwise ordered).
+ * T = 0 is a no-op.  Errors: MB_EINVAL (descriptor), MB_ECUDA. */
+mb_status mb_step(mb_layer *layer, mb_kv *kv, const mb_batch *batch, const void *x_in,
+                  void *x_out, void *stream);
+
+/* Check a batch descriptor against the rules above, on the host only (no
+ * device work; usable without a GPU).  num_pages: pool size; max_tokens: the
+ * layer's limit on T.  Errors: MB_EINVAL with a message naming the first
+ * violated rule. */
+mb_status mb_batch_validate(const mb_batch *batch, int32_t num_pages, int32_t max_tokens);
+
+/* Synchronise `stream` and report any error word the kernels recorded since
+ * the last call (then clears it).  MB_EDEVICE if one was set. */
+mb_status mb_device_status(mb_layer *layer, void *stream);
+
+/* Device pointer and byte size of an intermediate of the last step, for
+ * inspection: valid once the step's stream has completed and until the next
+ * mb_step.  which: 0 xn, 1 qkv, 2 q (rotated, [T][Hq][hd]), 3 o, 4 h, 5 hn,
+ * 6 a.  Errors: MB_EINVAL. */
+mb_status mb_layer_buffer(const mb_layer *layer, int32_t which, void **ptr, int64_t *bytes);
+
+/* Per-kernel timing of subsequent steps (CUDA events on the step's stream).
+ * mb_layer_timing returns the accumulated milliseconds of each launch kind
+ * since enable, in the order: rmsnorm_attn, gemm_qkv, rope_append, attention,
+ * attn_merge, gemm_o, rmsnorm_ffn, gemm_gate_up, gemm_down (n <= 9), and the
+ * number of steps timed.  It synchronises the stream of the last step. */
+mb_status mb_layer_set_timing(mb_layer *layer, int32_t enable);
+mb_status mb_layer_timing(mb_layer *layer, double *ms, int32_t n, int64_t *steps);
+
+/* Number of kernel launches the last mb_step issued. */
+int32_t mb_layer_last_launches(const mb_layer *layer);
+
+/* Standalone token-batched GEMM D = A B^T on the tcgen05 tensor cores (the
+ * linear layers of the step; ConfluxServe summary, "Why can linear layers be
+ * batched"). A device bf16 [M][K], B device bf16 [N][K], both row-major with
+ * K % 64 == 0 and 16-byte aligned rows.  epilogue:
+ *   0  D[M][N] = A B^T                          (bf16)
+ *   1  D[M][N] = A B^T + R[M][N]                (bf16 residual R, may not alias D)
+ *   2  N = 2F, B rows = [gate F; up F], F % 128 == 0:
+ *      D[M][F] = silu(A Bg^T) * (A Bu^T)        (bf16)
+ * Accumulation is fp32.  workspace: device memory of mb_gemm_workspace_bytes()
+ * bytes (fp32 partial tiles and tile tickets), or NULL to use the library's
+ * own (allocated once per device on first use).  Errors: MB_EINVAL,
+ * MB_EUNSUPPORTED, MB_ECUDA. */
+mb_status mb_gemm(const void *A, const void *B, void *D, const void *R, int32_t M, int32_t N,
+                  int32_t K, int32_t epilogue, void *workspace, void *stream);
+int64_t mb_gemm_workspace_bytes(void);
+
+/* ---------------- scheduler side (host only, no device work) ---------------
+ * The token-budget packer of the pofe.ai "Chunked prefill" page, "How it works,
+ * step by step" (steps 1-3) and its schedule() sketch: every step takes one
+ * token per running decode, then continues partial prefills min(C_left,
+ * p - p_done), then admits waiting prompts in arrival order while budget,
+ * sequence slots and KV pages remain, each with as many tokens as fit.
+ * Readings where the pages differ or are silent: decodes never drive the
+ * budget below zero (llm-stack-book 7.8 scheduler, budget >= 1); chunk_cap > 0
+ * caps every prefill chunk (pofe.ai, head-of-line blocking); admission stops
+ * at the first prompt refused for sequence slots or pages; pages are handed
+ * out FIFO from free_order at pack time, exactly ceil(kv_len / 16) per
+ * request; a decode that needs a page when none is free is skipped this
+ * step; a partial chunk shrinks to what its pages plus free pages hold;
+ * finishing a request appends its pages to the free list in table order. */
+typedef struct {
+  int32_t budget;     /* token budget C per step, >= 1 */
+  int32_t max_seqs;   /* running + partially prefilled requests, >= 1 */
+  int32_t chunk_cap;  /* per-request prefill chunk cap, 0 = none */
+} mb_pack_cfg;
+
+typedef struct {
+  mb_batch batch;          /* host arrays owned by the scheduler */
+  const int64_t *req_ids;  /* request id of each row */
+} mb_sched_batch;
+
+typedef struct mb_sched mb_sched;
+
+/* free_order: host int32[num_pages], a permutation of 0..num_pages-1 giving
+ * the initial free-list order (copied). */
+mb_status mb_sched_create(const mb_pack_cfg *cfg, int32_t num_pages, const int32_t *free_order,
+                          mb_sched **out);
+/* Add a request.  computed = tokens already in the cache: 0 for a new
+ * prompt, 0 < computed < prompt_len for a partial prefill, computed >=
+ * prompt_len for a running decode.  Pages for `computed` tokens are taken at
+ * once.  Errors: MB_EINVAL (duplicate id, bad lengths), MB_ENOSPACE. */
+mb_status mb_sched_add(mb_sched *s, int64_t req_id, int32_t prompt_len, int32_t computed);
+/* Build the next step's batch and advance the state as if it ran.  The
+ * output arrays stay valid until the next mb_sched_* call on `s`. */
+mb_status mb_sched_pack(mb_sched *s, mb_sched_batch *out);
+/* Remove a request and return its pages.  Errors: MB_EINVAL (unknown id). */
+mb_status mb_sched_finish(mb_sched *s, int64_t req_id);
+/* Counts: free pages, running, partial, waiting. */
+mb_status mb_sched_counts(const mb_sched *s, int32_t counts[4]);
+mb_status mb_sched_destroy(mb_sched *s);
+
+const char *mb_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MB_H_ */

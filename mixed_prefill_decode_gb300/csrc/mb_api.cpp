@@ -1,0 +1,799 @@
+// C-ABI of the mixed prefill+decode layer step: argument and descriptor
+// validation, work-list construction, descriptor upload and the launch
+// sequence.  See include/mb.h for the contract of every entry point.
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <string>
+#include <vector>
+
+#include "mb.h"
+#include "mb_internal.h"
+#include "mb_kernels.h"
+
+namespace mb {
+
+static thread_local std::string g_last_error;
+
+mb_status fail(mb_status st, const char *fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
+static mb_status cuda_fail(cudaError_t e, const char *where) {
+  return fail(e == cudaErrorMemoryAllocation ? MB_ENOMEM : MB_ECUDA, "%s: %s (%s)", where, cudaGetErrorName(e),
+              cudaGetErrorString(e));
+}
+
+// ------------------------------------------------------------ tensor maps
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+cudaError_t encode_tmap_2d(CUtensorMap *map, const void *base, uint64_t inner, uint64_t outer,
+                           uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return cudaErrorNotSupported;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_stride_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t encode_tmap_3d(CUtensorMap *map, const void *base, uint64_t d0, uint64_t d1, uint64_t d2,
+                           uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t b0, uint32_t b1, uint32_t b2) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return cudaErrorNotSupported;
+  cuuint64_t dims[3] = {d0, d1, d2};
+  cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
+  cuuint32_t box[3] = {b0, b1, b2};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+// ------------------------------------------------------ per-device context
+struct DeviceCtx {
+  int sms = 0;
+  int cc_major = 0, cc_minor = 0;
+  void *gemm_ws = nullptr;  // shared GEMM partial workspace
+  int *err = nullptr;       // error word for standalone calls
+};
+static std::mutex g_dev_mu;
+static DeviceCtx g_dev[64];
+
+static mb_status device_ctx(DeviceCtx **out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 64) return fail(MB_EUNSUPPORTED, "device index %d out of range", dev);
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DeviceCtx &c = g_dev[dev];
+  if (c.sms == 0) {
+    cudaDeviceProp prop;
+    e = cudaGetDeviceProperties(&prop, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDeviceProperties");
+    if (prop.major != 10 || (prop.minor != 3 && prop.minor != 0))
+      return fail(MB_EUNSUPPORTED, "device %d is sm_%d%d; these kernels are built for sm_103a", dev, prop.major,
+                  prop.minor);
+    c.cc_major = prop.major;
+    c.cc_minor = prop.minor;
+    c.sms = prop.multiProcessorCount;
+  }
+  if (!c.gemm_ws) {
+    e = cudaMalloc(&c.gemm_ws, gemm_workspace_bytes());
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(gemm workspace)");
+    e = cudaMemset(c.gemm_ws, 0, gemm_workspace_bytes());
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemset(gemm workspace)");
+    e = cudaMalloc(&c.err, 16);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(error word)");
+    e = cudaMemset(c.err, 0, 16);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemset(error word)");
+  }
+  *out = &c;
+  return MB_OK;
+}
+
+int device_sm_count() {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  return g_dev[dev].sms > 0 ? g_dev[dev].sms : 148;
+}
+
+}  // namespace mb
+
+using mb::fail;
+
+// ===================================================================== layer
+namespace {
+
+constexpr int kNumTimed = 9;
+constexpr int kRing = 4;
+
+struct EventSet {
+  cudaEvent_t ev[kNumTimed + 1];
+};
+
+struct StagingSlot {
+  int32_t *host = nullptr;
+  size_t cap = 0;  // int32 elements
+  cudaEvent_t done = nullptr;
+  bool used = false;
+};
+
+int32_t pages_for(int64_t n) { return static_cast<int32_t>((n + MB_PAGE_TOKENS - 1) / MB_PAGE_TOKENS); }
+
+}  // namespace
+
+struct mb_kv {
+  mb_layer *layer = nullptr;
+  void *base = nullptr;
+  bool owned = false;
+  int32_t num_pages = 0;
+  CUtensorMap tmap;
+  std::vector<uint32_t> stamp;  // page -> last step that referenced it (duplicate check)
+  uint32_t stamp_gen = 0;
+};
+
+struct mb_layer {
+  mb_layer_desc d;
+  mb_layer_weights w;
+  int device = 0;
+  int qkv_dim = 0;
+  // workspaces (bf16)
+  void *xn = nullptr, *qkv = nullptr, *q = nullptr, *o = nullptr, *h = nullptr, *hn = nullptr, *a = nullptr;
+  size_t bytes_x = 0, bytes_qkv = 0, bytes_q = 0, bytes_a = 0;
+  int *err = nullptr;
+  mb::GemmWorkspace gws{};
+  CUtensorMap tm_wqkv, tm_wo, tm_wgu, tm_wd;
+  // descriptor upload
+  StagingSlot ring[kRing];
+  int ring_next = 0;
+  int32_t *dblob = nullptr;
+  size_t dblob_cap = 0;
+  float *part = nullptr;
+  size_t part_cap = 0;  // floats
+  // last step
+  int32_t last_T = 0;
+  int32_t last_launches = 0;
+  // timing
+  bool timing = false;
+  std::vector<EventSet> ev_pool;
+  size_t ev_used = 0;
+  double ms[kNumTimed] = {0};
+  int64_t steps_timed = 0;
+  cudaStream_t last_stream = nullptr;
+  // host scratch
+  std::vector<int32_t> hbuf;
+};
+
+namespace {
+
+mb_status alloc_dev(void **p, size_t bytes, const char *what) {
+  cudaError_t e = cudaMalloc(p, bytes);
+  if (e != cudaSuccess) return mb::fail(e == cudaErrorMemoryAllocation ? MB_ENOMEM : MB_ECUDA, "cudaMalloc(%s, %zu bytes): %s", what, bytes, cudaGetErrorString(e));
+  return MB_OK;
+}
+
+void free_layer_mem(mb_layer *L) {
+  void *ptrs[] = {L->xn, L->qkv, L->q, L->o, L->h, L->hn, L->a, L->err, L->dblob, L->part};
+  for (void *p : ptrs)
+    if (p) cudaFree(p);
+  for (auto &s : L->ring) {
+    if (s.host) cudaFreeHost(s.host);
+    if (s.done) cudaEventDestroy(s.done);
+  }
+  for (auto &es : L->ev_pool)
+    for (auto &e : es.ev) cudaEventDestroy(e);
+}
+
+mb_status flush_timing(mb_layer *L) {
+  if (L->ev_used == 0) return MB_OK;
+  for (size_t i = 0; i < L->ev_used; ++i) {
+    EventSet &es = L->ev_pool[i];
+    cudaError_t e = cudaEventSynchronize(es.ev[kNumTimed]);
+    if (e != cudaSuccess) return mb::fail(MB_ECUDA, "cudaEventSynchronize: %s", cudaGetErrorString(e));
+    for (int k = 0; k < kNumTimed; ++k) {
+      float t = 0.f;
+      e = cudaEventElapsedTime(&t, es.ev[k], es.ev[k + 1]);
+      if (e != cudaSuccess) return mb::fail(MB_ECUDA, "cudaEventElapsedTime: %s", cudaGetErrorString(e));
+      L->ms[k] += t;
+    }
+    L->steps_timed += 1;
+  }
+  L->ev_used = 0;
+  return MB_OK;
+}
+
+
+// Descriptor rules of include/mb.h; `stamp` (num_pages entries) marks pages
+// already seen with `gen` to catch a page used twice.
+mb_status validate_batch(const mb_batch *b, int32_t num_pages, int32_t max_tokens, uint32_t *stamp, uint32_t gen,
+                         int64_t *T_out) {
+  const int n = b->num_reqs;
+  if (n < 0) return mb::fail(MB_EINVAL, "batch: num_reqs < 0");
+  if (n == 0) {
+    *T_out = 0;
+    return MB_OK;
+  }
+  if (!b->qo_indptr || !b->kv_len || !b->bt_indptr || !b->bt) return mb::fail(MB_EINVAL, "batch: null descriptor array");
+  if (b->qo_indptr[0] != 0) return mb::fail(MB_EINVAL, "batch: qo_indptr[0] must be 0");
+  int64_t T = 0;
+  for (int r = 0; r < n; ++r) {
+    const int64_t qo = static_cast<int64_t>(b->qo_indptr[r + 1]) - b->qo_indptr[r];
+    const int64_t kvl = b->kv_len[r];
+    if (qo < 1) return mb::fail(MB_EINVAL, "batch: request %d has qo_len %lld < 1", r, (long long)qo);
+    if (kvl < qo)
+      return mb::fail(MB_EINVAL, "batch: request %d has kv_len %lld < qo_len %lld", r, (long long)kvl, (long long)qo);
+    if (kvl > (1 << 24)) return mb::fail(MB_EUNSUPPORTED, "batch: request %d kv_len > 2^24", r);
+    const int64_t tl = static_cast<int64_t>(b->bt_indptr[r + 1]) - b->bt_indptr[r];
+    if (b->bt_indptr[r] < 0 || tl < pages_for(kvl))
+      return mb::fail(MB_EINVAL, "batch: request %d block table has %lld pages, needs %d", r, (long long)tl,
+                      pages_for(kvl));
+    for (int64_t i = 0; i < pages_for(kvl); ++i) {
+      const int32_t pg = b->bt[b->bt_indptr[r] + i];
+      if (pg < 0 || pg >= num_pages)
+        return mb::fail(MB_EINVAL, "batch: request %d page id %d outside [0, %d)", r, pg, num_pages);
+      if (stamp[pg] == gen) return mb::fail(MB_EINVAL, "batch: page %d referenced twice in one batch", pg);
+      stamp[pg] = gen;
+    }
+    T += qo;
+  }
+  if (T > max_tokens) return mb::fail(MB_EINVAL, "batch: T = %lld exceeds max_tokens %d", (long long)T, max_tokens);
+  *T_out = T;
+  return MB_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+mb_status mb_batch_validate(const mb_batch *b, int32_t num_pages, int32_t max_tokens) {
+  if (!b || num_pages < 0) return mb::fail(MB_EINVAL, "mb_batch_validate: null batch or negative num_pages");
+  std::vector<uint32_t> stamp(static_cast<size_t>(num_pages), 0u);
+  int64_t T = 0;
+  return validate_batch(b, num_pages, max_tokens, stamp.data(), 1u, &T);
+}
+
+const char *mb_last_error(void) { return mb::g_last_error.c_str(); }
+
+int64_t mb_gemm_workspace_bytes(void) { return static_cast<int64_t>(mb::gemm_workspace_bytes()); }
+
+mb_status mb_layer_create(const mb_layer_desc *desc, const mb_layer_weights *w, mb_layer **out) {
+  if (!desc || !w || !out) return fail(MB_EINVAL, "mb_layer_create: null argument");
+  const mb_layer_desc &d = *desc;
+  if (d.d_model <= 0 || d.n_q_heads <= 0 || d.n_kv_heads <= 0 || d.head_dim <= 0 || d.d_ff <= 0 ||
+      d.max_tokens <= 0 || !(d.rms_eps >= 0.f) || !(d.rope_theta > 0.f))
+    return fail(MB_EINVAL, "mb_layer_create: sizes must be positive, eps >= 0, theta > 0");
+  if (d.n_q_heads % d.n_kv_heads != 0)
+    return fail(MB_EINVAL, "mb_layer_create: n_q_heads must be a multiple of n_kv_heads");
+  if (d.head_dim != 64 && d.head_dim != 128)
+    return fail(MB_EUNSUPPORTED, "mb_layer_create: head_dim %d (supported: 64, 128)", d.head_dim);
+  if (d.n_q_heads / d.n_kv_heads > 8)
+    return fail(MB_EUNSUPPORTED, "mb_layer_create: GQA group %d > 8", d.n_q_heads / d.n_kv_heads);
+  if (d.d_model % 128 || (d.n_q_heads * d.head_dim) % 128 || d.d_ff % 128)
+    return fail(MB_EUNSUPPORTED, "mb_layer_create: d_model, n_q_heads*head_dim and d_ff must be multiples of 128");
+  if (d.d_model > 8192) return fail(MB_EUNSUPPORTED, "mb_layer_create: d_model > 8192");
+  if (!w->g_attn || !w->w_qkv || !w->w_o || !w->g_ffn || !w->w_gate_up || !w->w_down ||
+      (d.qk_norm && (!w->g_q || !w->g_k)))
+    return fail(MB_EINVAL, "mb_layer_create: missing weight pointer");
+  const void *wp[] = {w->g_attn, w->w_qkv, w->w_o, w->g_ffn, w->w_gate_up, w->w_down};
+  for (const void *p : wp)
+    if (reinterpret_cast<uintptr_t>(p) % 16)
+      return fail(MB_EINVAL, "mb_layer_create: weight pointers must be 16-byte aligned");
+
+  mb::DeviceCtx *ctx = nullptr;
+  mb_status st = mb::device_ctx(&ctx);
+  if (st != MB_OK) return st;
+
+  mb_layer *L = new (std::nothrow) mb_layer();
+  if (!L) return fail(MB_ENOMEM, "mb_layer_create: out of host memory");
+  L->d = d;
+  L->w = *w;
+  cudaGetDevice(&L->device);
+  L->qkv_dim = (d.n_q_heads + 2 * d.n_kv_heads) * d.head_dim;
+  const size_t T = static_cast<size_t>(d.max_tokens);
+  L->bytes_x = T * d.d_model * 2;
+  L->bytes_qkv = T * L->qkv_dim * 2;
+  L->bytes_q = T * d.n_q_heads * d.head_dim * 2;
+  L->bytes_a = T * d.d_ff * 2;
+  struct {
+    void **p;
+    size_t n;
+    const char *what;
+  } allocs[] = {{&L->xn, L->bytes_x, "xn"}, {&L->qkv, L->bytes_qkv, "qkv"}, {&L->q, L->bytes_q, "q"},
+                {&L->o, L->bytes_q, "o"},   {&L->h, L->bytes_x, "h"},       {&L->hn, L->bytes_x, "hn"},
+                {&L->a, L->bytes_a, "a"}};
+  for (auto &al : allocs) {
+    st = alloc_dev(al.p, al.n, al.what);
+    if (st != MB_OK) {
+      free_layer_mem(L);
+      delete L;
+      return st;
+    }
+  }
+  st = alloc_dev(reinterpret_cast<void **>(&L->err), 16, "error word");
+  if (st == MB_OK && cudaMemset(L->err, 0, 16) != cudaSuccess) st = fail(MB_ECUDA, "cudaMemset(error word)");
+  if (st != MB_OK) {
+    free_layer_mem(L);
+    delete L;
+    return st;
+  }
+  L->gws = mb::gemm_workspace_carve(ctx->gemm_ws);
+  const int hq = d.n_q_heads * d.head_dim;
+  cudaError_t e = mb::encode_tmap_2d(&L->tm_wqkv, w->w_qkv, d.d_model, L->qkv_dim, d.d_model * 2ull, 64, 128);
+  if (e == cudaSuccess) e = mb::encode_tmap_2d(&L->tm_wo, w->w_o, hq, d.d_model, hq * 2ull, 64, 128);
+  if (e == cudaSuccess) e = mb::encode_tmap_2d(&L->tm_wgu, w->w_gate_up, d.d_model, 2ull * d.d_ff, d.d_model * 2ull, 64, 128);
+  if (e == cudaSuccess) e = mb::encode_tmap_2d(&L->tm_wd, w->w_down, d.d_ff, d.d_model, d.d_ff * 2ull, 64, 128);
+  if (e != cudaSuccess) {
+    free_layer_mem(L);
+    delete L;
+    return fail(MB_ECUDA, "mb_layer_create: tensor map encoding failed (%s)", cudaGetErrorString(e));
+  }
+  for (auto &s : L->ring) {
+    if (cudaEventCreateWithFlags(&s.done, cudaEventDisableTiming) != cudaSuccess) {
+      free_layer_mem(L);
+      delete L;
+      return fail(MB_ECUDA, "mb_layer_create: cudaEventCreate failed");
+    }
+  }
+  *out = L;
+  return MB_OK;
+}
+
+mb_status mb_destroy(mb_layer *L) {
+  if (!L) return MB_OK;
+  cudaDeviceSynchronize();
+  free_layer_mem(L);
+  delete L;
+  return MB_OK;
+}
+
+mb_status mb_kv_alloc(mb_layer *L, int32_t num_pages, void *dev_buf, mb_kv **out) {
+  if (!L || !out || num_pages <= 0) return fail(MB_EINVAL, "mb_kv_alloc: null layer/out or num_pages <= 0");
+  if (dev_buf && reinterpret_cast<uintptr_t>(dev_buf) % 128)
+    return fail(MB_EINVAL, "mb_kv_alloc: dev_buf must be 128-byte aligned");
+  const int64_t Hkv = L->d.n_kv_heads, hd = L->d.head_dim;
+  const int64_t z = static_cast<int64_t>(num_pages) * 2 * Hkv;
+  if (z > INT32_MAX) return fail(MB_EUNSUPPORTED, "mb_kv_alloc: pool too large for 32-bit TMA coordinates");
+  mb_kv *kv = new (std::nothrow) mb_kv();
+  if (!kv) return fail(MB_ENOMEM, "mb_kv_alloc: out of host memory");
+  kv->layer = L;
+  kv->num_pages = num_pages;
+  const size_t bytes = static_cast<size_t>(z) * MB_PAGE_TOKENS * hd * 2;
+  if (dev_buf) {
+    kv->base = dev_buf;
+  } else {
+    mb_status st = alloc_dev(&kv->base, bytes, "kv pool");
+    if (st != MB_OK) {
+      delete kv;
+      return st;
+    }
+    kv->owned = true;
+  }
+  cudaError_t e = mb::encode_tmap_3d(&kv->tmap, kv->base, hd, MB_PAGE_TOKENS, z, hd * 2, MB_PAGE_TOKENS * hd * 2,
+                                     64, MB_PAGE_TOKENS, 1);
+  if (e != cudaSuccess) {
+    if (kv->owned) cudaFree(kv->base);
+    delete kv;
+    return fail(MB_ECUDA, "mb_kv_alloc: tensor map encoding failed");
+  }
+  kv->stamp.assign(static_cast<size_t>(num_pages), 0);
+  *out = kv;
+  return MB_OK;
+}
+
+mb_status mb_kv_layout(const mb_kv *kv, int64_t strides[5], void **base) {
+  if (!kv || !strides || !base) return fail(MB_EINVAL, "mb_kv_layout: null argument");
+  const int64_t Hkv = kv->layer->d.n_kv_heads, hd = kv->layer->d.head_dim;
+  strides[4] = 1;
+  strides[3] = hd;
+  strides[2] = MB_PAGE_TOKENS * hd;
+  strides[1] = Hkv * MB_PAGE_TOKENS * hd;
+  strides[0] = 2 * Hkv * MB_PAGE_TOKENS * hd;
+  *base = kv->base;
+  return MB_OK;
+}
+
+mb_status mb_kv_free(mb_kv *kv) {
+  if (!kv) return MB_OK;
+  if (kv->owned) {
+    cudaDeviceSynchronize();
+    cudaFree(kv->base);
+  }
+  delete kv;
+  return MB_OK;
+}
+
+mb_status mb_layer_buffer(const mb_layer *L, int32_t which, void **ptr, int64_t *bytes) {
+  if (!L || !ptr || !bytes) return fail(MB_EINVAL, "mb_layer_buffer: null argument");
+  const int64_t T = L->last_T;
+  const int64_t d = L->d.d_model, hq = L->d.n_q_heads * L->d.head_dim;
+  switch (which) {
+    case 0: *ptr = L->xn; *bytes = T * d * 2; break;
+    case 1: *ptr = L->qkv; *bytes = T * L->qkv_dim * 2; break;
+    case 2: *ptr = L->q; *bytes = T * hq * 2; break;
+    case 3: *ptr = L->o; *bytes = T * hq * 2; break;
+    case 4: *ptr = L->h; *bytes = T * d * 2; break;
+    case 5: *ptr = L->hn; *bytes = T * d * 2; break;
+    case 6: *ptr = L->a; *bytes = T * L->d.d_ff * 2; break;
+    default: return fail(MB_EINVAL, "mb_layer_buffer: unknown buffer %d", which);
+  }
+  return MB_OK;
+}
+
+mb_status mb_layer_set_timing(mb_layer *L, int32_t enable) {
+  if (!L) return fail(MB_EINVAL, "mb_layer_set_timing: null layer");
+  mb_status st = flush_timing(L);
+  if (st != MB_OK) return st;
+  L->timing = enable != 0;
+  std::fill(L->ms, L->ms + kNumTimed, 0.0);
+  L->steps_timed = 0;
+  return MB_OK;
+}
+
+mb_status mb_layer_timing(mb_layer *L, double *ms, int32_t n, int64_t *steps) {
+  if (!L || (n > 0 && !ms)) return fail(MB_EINVAL, "mb_layer_timing: null argument");
+  mb_status st = flush_timing(L);
+  if (st != MB_OK) return st;
+  for (int i = 0; i < n && i < kNumTimed; ++i) ms[i] = L->ms[i];
+  if (steps) *steps = L->steps_timed;
+  return MB_OK;
+}
+
+int32_t mb_layer_last_launches(const mb_layer *L) { return L ? L->last_launches : 0; }
+
+mb_status mb_device_status(mb_layer *L, void *stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return fail(MB_ECUDA, "mb_device_status: %s", cudaGetErrorString(e));
+  int *errp = nullptr;
+  mb::DeviceCtx *ctx = nullptr;
+  mb_status st = mb::device_ctx(&ctx);
+  if (st != MB_OK) return st;
+  errp = L ? L->err : ctx->err;
+  int code = 0;
+  e = cudaMemcpy(&code, errp, sizeof code, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return fail(MB_ECUDA, "mb_device_status: %s", cudaGetErrorString(e));
+  if (code != 0) {
+    cudaMemset(errp, 0, 16);
+    // a kernel that unwound early may leave stream-K tickets raised
+    cudaMemset(ctx->gemm_ws, 0, mb::gemm_workspace_bytes());
+    return fail(MB_EDEVICE, "mb_device_status: kernel error code %d", code);
+  }
+  return MB_OK;
+}
+
+// ------------------------------------------------------------------ GEMM
+mb_status mb_gemm(const void *A, const void *B, void *D, const void *R, int32_t M, int32_t N, int32_t K,
+                  int32_t epilogue, void *workspace, void *stream) {
+  if (!A || !B || !D || M < 0 || N <= 0 || K <= 0) return fail(MB_EINVAL, "mb_gemm: bad argument");
+  if (epilogue < 0 || epilogue > 2) return fail(MB_EINVAL, "mb_gemm: epilogue must be 0, 1 or 2");
+  if (epilogue == 1 && (!R || R == D)) return fail(MB_EINVAL, "mb_gemm: residual epilogue needs R != D");
+  if (K % 64) return fail(MB_EUNSUPPORTED, "mb_gemm: K must be a multiple of 64");
+  if (epilogue == 2 && N % 128) return fail(MB_EUNSUPPORTED, "mb_gemm: SwiGLU needs F = N %% 128 == 0");
+  if (N % 32) return fail(MB_EUNSUPPORTED, "mb_gemm: N must be a multiple of 32");
+  for (const void *p : {A, B, static_cast<const void *>(D), R})
+    if (p && reinterpret_cast<uintptr_t>(p) % 16) return fail(MB_EINVAL, "mb_gemm: pointers must be 16-byte aligned");
+  if (M == 0) return MB_OK;
+  mb::DeviceCtx *ctx = nullptr;
+  mb_status st = mb::device_ctx(&ctx);
+  if (st != MB_OK) return st;
+  mb::GemmWorkspace ws = mb::gemm_workspace_carve(workspace ? workspace : ctx->gemm_ws);
+  cudaError_t e = mb::gemm_run(A, B, nullptr, D, R, M, N, K, epilogue, ws, ctx->err, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return mb::cuda_fail(e, "mb_gemm");
+  return MB_OK;
+}
+
+// ------------------------------------------------------------------ step
+mb_status mb_step(mb_layer *L, mb_kv *kv, const mb_batch *b, const void *x_in, void *x_out, void *stream) {
+  if (!L || !kv || !b || !x_in || !x_out) return fail(MB_EINVAL, "mb_step: null argument");
+  if (kv->layer != L) return fail(MB_EINVAL, "mb_step: kv pool belongs to another layer");
+  if (x_in == x_out) return fail(MB_EINVAL, "mb_step: x_out must not alias x_in");
+  if (reinterpret_cast<uintptr_t>(x_in) % 16 || reinterpret_cast<uintptr_t>(x_out) % 16)
+    return fail(MB_EINVAL, "mb_step: x_in and x_out must be 16-byte aligned");
+  const int n = b->num_reqs;
+  if (n < 0) return fail(MB_EINVAL, "mb_step: num_reqs < 0");
+  L->last_launches = 0;
+  if (n == 0) {
+    L->last_T = 0;
+    return MB_OK;
+  }
+  if (!b->qo_indptr || !b->kv_len || !b->bt_indptr || !b->bt) return fail(MB_EINVAL, "mb_step: null descriptor array");
+  const mb_layer_desc &d = L->d;
+  // ---- validate the descriptor
+  if (++kv->stamp_gen == 0) {
+    std::fill(kv->stamp.begin(), kv->stamp.end(), 0u);
+    kv->stamp_gen = 1;
+  }
+  int64_t T = 0;
+  {
+    mb_status vst = validate_batch(b, kv->num_pages, d.max_tokens, kv->stamp.data(), kv->stamp_gen, &T);
+    if (vst != MB_OK) return vst;
+  }
+
+  mb::DeviceCtx *ctx = nullptr;
+  mb_status st = mb::device_ctx(&ctx);
+  if (st != MB_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  // ---- work lists
+  const int Hq = d.n_q_heads, Hkv = d.n_kv_heads, hd = d.head_dim, G = Hq / Hkv;
+  int64_t nb = b->bt_indptr[n];
+  std::vector<int32_t> &hb = L->hbuf;
+  hb.clear();
+  auto sec = [&](size_t count) {
+    size_t off = hb.size();
+    hb.resize(off + ((count + 3) & ~size_t(3)), 0);
+    return off;
+  };
+  const size_t o_qo = sec(n + 1), o_kv = sec(n), o_bti = sec(n + 1), o_bt = sec(static_cast<size_t>(nb));
+  const size_t o_treq = sec(T), o_tpos = sec(T);
+  std::copy(b->qo_indptr, b->qo_indptr + n + 1, hb.begin() + o_qo);
+  std::copy(b->kv_len, b->kv_len + n, hb.begin() + o_kv);
+  std::copy(b->bt_indptr, b->bt_indptr + n + 1, hb.begin() + o_bti);
+  std::copy(b->bt, b->bt + nb, hb.begin() + o_bt);
+  for (int r = 0; r < n; ++r) {
+    const int32_t t0 = b->qo_indptr[r], t1 = b->qo_indptr[r + 1];
+    const int32_t c = b->kv_len[r] - (t1 - t0);
+    for (int32_t t = t0; t1 > t; ++t) {
+      hb[o_treq + t] = r;
+      hb[o_tpos + t] = c + (t - t0);
+    }
+  }
+  // chunk tiles, heaviest first (rows x visible keys)
+  struct Tile {
+    int32_t r, i0, h;
+    int64_t work;
+  };
+  std::vector<Tile> tiles;
+  int64_t dec_pages = 0;
+  for (int r = 0; r < n; ++r) {
+    const int32_t qo = b->qo_indptr[r + 1] - b->qo_indptr[r];
+    if (qo > 1) {
+      const int32_t c = b->kv_len[r] - qo;
+      for (int32_t i0 = 0; i0 < qo; i0 += 128)
+        for (int32_t hh = 0; hh < Hq; ++hh) tiles.push_back({r, i0, hh, static_cast<int64_t>(c + i0 + 128)});
+    } else {
+      dec_pages += pages_for(b->kv_len[r]);
+    }
+  }
+  std::stable_sort(tiles.begin(), tiles.end(), [](const Tile &x, const Tile &y) { return x.work > y.work; });
+  const size_t o_tiles = sec(tiles.size() * 4);
+  for (size_t i = 0; i < tiles.size(); ++i) {
+    hb[o_tiles + 4 * i + 0] = tiles[i].r;
+    hb[o_tiles + 4 * i + 1] = tiles[i].i0;
+    hb[o_tiles + 4 * i + 2] = tiles[i].h;
+  }
+  // decode splits: enough warps to keep every SM streaming K/V
+  const int64_t target_items = static_cast<int64_t>(ctx->sms) * 32;
+  int64_t pps = (dec_pages * Hkv + target_items - 1) / std::max<int64_t>(1, target_items);
+  pps = std::max<int64_t>(pps, 4);
+  std::vector<int32_t> items, merges;
+  for (int r = 0; r < n; ++r) {
+    const int32_t qo = b->qo_indptr[r + 1] - b->qo_indptr[r];
+    if (qo != 1) continue;
+    const int32_t np = pages_for(b->kv_len[r]);
+    const int32_t ns = static_cast<int32_t>((np + pps - 1) / pps);
+    for (int32_t hk = 0; hk < Hkv; ++hk) {
+      const int32_t first = static_cast<int32_t>(items.size() / 8);
+      for (int32_t sidx = 0; sidx < ns; ++sidx) {
+        const int32_t pb = static_cast<int32_t>(sidx * pps);
+        const int32_t pe = static_cast<int32_t>(std::min<int64_t>(np, (sidx + 1) * pps));
+        items.insert(items.end(), {r, hk, pb, pe, sidx, ns, 0, 0});
+      }
+      if (ns > 1) merges.insert(merges.end(), {r, hk, first, ns});
+    }
+  }
+  const size_t o_items = sec(items.size()), o_merge = sec(merges.size());
+  std::copy(items.begin(), items.end(), hb.begin() + o_items);
+  std::copy(merges.begin(), merges.end(), hb.begin() + o_merge);
+  const int n_items = static_cast<int>(items.size() / 8);
+  const int n_merge = static_cast<int>(merges.size() / 4);
+
+  // ---- upload through a pinned ring slot
+  StagingSlot &slot = L->ring[L->ring_next];
+  L->ring_next = (L->ring_next + 1) % kRing;
+  cudaError_t e;
+  if (slot.used) {
+    e = cudaEventSynchronize(slot.done);
+    if (e != cudaSuccess) return mb::fail(MB_ECUDA, "mb_step: %s", cudaGetErrorString(e));
+  }
+  if (slot.cap < hb.size()) {
+    if (slot.host) cudaFreeHost(slot.host);
+    slot.host = nullptr;
+    size_t cap = std::max<size_t>(hb.size() * 2, 4096);
+    e = cudaHostAlloc(reinterpret_cast<void **>(&slot.host), cap * 4, cudaHostAllocDefault);
+    if (e != cudaSuccess) {
+      slot.cap = 0;
+      return mb::fail(MB_ENOMEM, "mb_step: cudaHostAlloc: %s", cudaGetErrorString(e));
+    }
+    slot.cap = cap;
+  }
+  if (L->dblob_cap < hb.size()) {
+    cudaStreamSynchronize(s);
+    if (L->dblob) cudaFree(L->dblob);
+    L->dblob = nullptr;
+    size_t cap = std::max<size_t>(hb.size() * 2, 4096);
+    st = alloc_dev(reinterpret_cast<void **>(&L->dblob), cap * 4, "descriptor");
+    if (st != MB_OK) {
+      L->dblob_cap = 0;
+      return st;
+    }
+    L->dblob_cap = cap;
+  }
+  const size_t part_need = static_cast<size_t>(n_items) * G * (hd + 4);  // rows of hd + 4 floats
+  if (L->part_cap < part_need) {
+    cudaStreamSynchronize(s);
+    if (L->part) cudaFree(L->part);
+    L->part = nullptr;
+    size_t cap = part_need * 2;
+    st = alloc_dev(reinterpret_cast<void **>(&L->part), cap * 4, "decode partials");
+    if (st != MB_OK) {
+      L->part_cap = 0;
+      return st;
+    }
+    L->part_cap = cap;
+  }
+  std::memcpy(slot.host, hb.data(), hb.size() * 4);
+  e = cudaMemcpyAsync(L->dblob, slot.host, hb.size() * 4, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return mb::fail(MB_ECUDA, "mb_step: descriptor upload: %s", cudaGetErrorString(e));
+  e = cudaEventRecord(slot.done, s);
+  if (e != cudaSuccess) return mb::fail(MB_ECUDA, "mb_step: %s", cudaGetErrorString(e));
+  slot.used = true;
+  const int32_t *db = L->dblob;
+
+  // ---- timing events
+  EventSet *es = nullptr;
+  if (L->timing) {
+    if (L->ev_used == 64) {
+      st = flush_timing(L);
+      if (st != MB_OK) return st;
+    }
+    if (L->ev_used == L->ev_pool.size()) {
+      EventSet ns;
+      for (auto &ev : ns.ev) cudaEventCreate(&ev);
+      L->ev_pool.push_back(ns);
+    }
+    es = &L->ev_pool[L->ev_used++];
+  }
+  auto mark = [&](int k) {
+    if (es) cudaEventRecord(es->ev[k], s);
+  };
+
+  // ---- launches
+  const int Ti = static_cast<int>(T);
+  const int hqd = Hq * hd;
+  int launches = 0;
+  auto chk = [&](cudaError_t err, const char *what) -> mb_status {
+    if (err != cudaSuccess) return mb::fail(MB_ECUDA, "mb_step: %s: %s", what, cudaGetErrorString(err));
+    return MB_OK;
+  };
+  mark(0);
+  if ((st = chk(mb::rmsnorm_run(x_in, L->w.g_attn, L->xn, Ti, d.d_model, d.rms_eps, s), "rmsnorm")) != MB_OK) return st;
+  ++launches;
+  mark(1);
+  if ((st = chk(mb::gemm_run(L->xn, L->w.w_qkv, &L->tm_wqkv, L->qkv, nullptr, Ti, L->qkv_dim, d.d_model, mb::kEpiStore,
+                             L->gws, L->err, s), "gemm qkv")) != MB_OK)
+    return st;
+  ++launches;
+  mark(2);
+  mb::RopeArgs ra;
+  ra.qkv = L->qkv;
+  ra.q_out = L->q;
+  ra.pool = kv->base;
+  ra.tok_req = db + o_treq;
+  ra.tok_pos = db + o_tpos;
+  ra.bt_indptr = db + o_bti;
+  ra.bt = db + o_bt;
+  ra.g_q = L->w.g_q;
+  ra.g_k = L->w.g_k;
+  ra.T = Ti;
+  ra.Hq = Hq;
+  ra.Hkv = Hkv;
+  ra.hd = hd;
+  ra.qk_norm = d.qk_norm;
+  ra.num_pages = kv->num_pages;
+  ra.eps = d.rms_eps;
+  ra.theta = d.rope_theta;
+  ra.err = L->err;
+  if ((st = chk(mb::rope_append_run(ra, s), "rope/append")) != MB_OK) return st;
+  ++launches;
+  mark(3);
+  CUtensorMap tm_q;
+  e = mb::encode_tmap_2d(&tm_q, L->q, hqd, Ti, hqd * 2ull, 64, 128);
+  if (e != cudaSuccess) return mb::fail(MB_ECUDA, "mb_step: Q tensor map");
+  mb::AttnArgs aa;
+  aa.q = L->q;
+  aa.pool = kv->base;
+  aa.o = L->o;
+  aa.qo_indptr = db + o_qo;
+  aa.kv_len = db + o_kv;
+  aa.bt_indptr = db + o_bti;
+  aa.bt = db + o_bt;
+  aa.tiles = db + o_tiles;
+  aa.items = db + o_items;
+  aa.part = L->part;
+  aa.n_tiles = static_cast<int>(tiles.size());
+  aa.n_items = n_items;
+  aa.T = Ti;
+  aa.Hq = Hq;
+  aa.Hkv = Hkv;
+  aa.hd = hd;
+  aa.num_pages = kv->num_pages;
+  aa.err = L->err;
+  aa.tm_q = &tm_q;
+  aa.tm_kv = &kv->tmap;
+  if ((st = chk(mb::attention_run(aa, s), "attention")) != MB_OK) return st;
+  launches += (aa.n_tiles > 0) + (aa.n_items > 0);
+  mark(4);
+  mb::MergeArgs ma;
+  ma.part = L->part;
+  ma.merge_list = db + o_merge;
+  ma.n_merge = n_merge;
+  ma.o = L->o;
+  ma.qo_indptr = db + o_qo;
+  ma.Hq = Hq;
+  ma.Hkv = Hkv;
+  ma.hd = hd;
+  if ((st = chk(mb::attn_merge_run(ma, s), "merge")) != MB_OK) return st;
+  launches += n_merge > 0;
+  mark(5);
+  if ((st = chk(mb::gemm_run(L->o, L->w.w_o, &L->tm_wo, L->h, x_in, Ti, d.d_model, hqd, mb::kEpiResidual, L->gws,
+                             L->err, s), "gemm o")) != MB_OK)
+    return st;
+  ++launches;
+  mark(6);
+  if ((st = chk(mb::rmsnorm_run(L->h, L->w.g_ffn, L->hn, Ti, d.d_model, d.rms_eps, s), "rmsnorm ffn")) != MB_OK) return st;
+  ++launches;
+  mark(7);
+  if ((st = chk(mb::gemm_run(L->hn, L->w.w_gate_up, &L->tm_wgu, L->a, nullptr, Ti, d.d_ff, d.d_model, mb::kEpiSwiGLU,
+                             L->gws, L->err, s), "gemm gate/up")) != MB_OK)
+    return st;
+  ++launches;
+  mark(8);
+  if ((st = chk(mb::gemm_run(L->a, L->w.w_down, &L->tm_wd, x_out, L->h, Ti, d.d_model, d.d_ff, mb::kEpiResidual, L->gws,
+                             L->err, s), "gemm down")) != MB_OK)
+    return st;
+  ++launches;
+  mark(9);
+  L->last_T = static_cast<int32_t>(T);
+  L->last_launches = launches;
+  L->last_stream = s;
+  return MB_OK;
+}
+
+}  // extern "C"

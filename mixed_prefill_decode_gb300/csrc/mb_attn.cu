@@ -1,0 +1,631 @@
+// Ragged paged attention of the mixed step.
+//
+// After the token-batched linear layers the batch splits (ConfluxServe
+// summary, "Why can linear layers be batched but attention cannot?"; Perplexity
+// "Disaggregated Prefill and Decode": prefill rows have large qo_len, decode
+// rows qo_len = 1 against long kv_len):
+//
+//  * chunk tiles: 128 query rows x one q-head of a prefill chunk.  A query at
+//    position c + i sees keys 0 .. c + i (llm-stack-book 7.8, "Attention on
+//    Partial KV Caches"); keys and values are read page by page through the
+//    block table with TMA (one 16 x 64 box per page, head and 64-wide half,
+//    from the HND pool), S = Q K^T and O_blk = P V run on tcgen05 with fp32
+//    accumulators in TMEM, the online softmax runs in registers (one thread
+//    per query row).  S is double-buffered in TMEM so the next block's Q K^T
+//    overlaps this block's softmax.
+//  * decode rows: split-KV.  One warp per (request, KV head, page range)
+//    serves all q-heads of the GQA group from one read of K and V (16-byte
+//    loads, 8 bf16 per lane), keeps (m, l, o) per head, and either writes the
+//    normalised output (single split) or a partial that the merge pass
+//    combines by log-sum-exp.
+//
+// GQA: q head h reads KV head h / (Hq / Hkv) (llm-stack-book 7.8, exercise 5).
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "mb_kernels.h"
+#include "mb_ptx.cuh"
+
+namespace mb {
+namespace {
+
+using namespace dev;
+
+constexpr float kLog2e = 1.4426950408889634f;
+// decode partial row: o[hd], m, l, padding to a 16-byte multiple
+template <int HD>
+__host__ __device__ constexpr int part_stride() { return HD + 4; }
+
+// ============================================================ chunk tiles
+template <int HD>
+struct ChunkCfg {
+  static constexpr int NH = HD / 64;              // 64-wide swizzle chunks along hd
+  static constexpr int TILE_BYTES = 128 * 128;    // [128 rows][64 bf16]
+  static constexpr int Q_BYTES = NH * TILE_BYTES;
+  static constexpr int KV_BYTES = NH * TILE_BYTES;
+  static constexpr int P_BYTES = 2 * TILE_BYTES;  // 128 x 128 keys
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_K = OFF_Q + Q_BYTES;
+  static constexpr int OFF_V = OFF_K + 2 * KV_BYTES;
+  static constexpr int OFF_P = OFF_V + 2 * KV_BYTES;
+  static constexpr int OFF_BAR = OFF_P + P_BYTES;
+  static constexpr int SMEM = OFF_BAR + 128 + 1024;
+  static constexpr uint32_t IDESC_S = idesc_bf16(128, 128, false);
+  static constexpr uint32_t IDESC_PV = idesc_bf16(128, HD, true);
+  static constexpr uint32_t TMEM_COLS = 512;      // S0 [0,128), S1 [128,256), O [256, 256+HD)
+};
+
+struct ChunkParams {
+  __nv_bfloat16 *o;
+  const int32_t *qo_indptr, *kv_len, *bt_indptr, *bt, *tiles;
+  int Hq, Hkv, num_pages;
+  float scale_log2;
+  int *err;
+};
+
+template <int HD>
+__global__ void __launch_bounds__(192, 1)
+    chunk_attn_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmKV,
+                      const ChunkParams p) {
+  using C = ChunkCfg<HD>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = align1024(smem_raw);
+  uint8_t *sQ = smem + C::OFF_Q;
+  uint8_t *sK = smem + C::OFF_K;
+  uint8_t *sV = smem + C::OFF_V;
+  uint8_t *sP = smem + C::OFF_P;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
+  uint64_t *q_full = bars + 0;
+  uint64_t *kv_full = bars + 1;   // [2]
+  uint64_t *kv_empty = bars + 3;  // [2]
+  uint64_t *s_full = bars + 5;    // [2]
+  uint64_t *p_full = bars + 7;
+  uint64_t *o_full = bars + 8;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 9);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  const int req = p.tiles[blockIdx.x * 4 + 0];
+  const int i0 = p.tiles[blockIdx.x * 4 + 1];
+  const int h = p.tiles[blockIdx.x * 4 + 2];
+  const int t0 = p.qo_indptr[req];
+  const int qo = p.qo_indptr[req + 1] - t0;
+  const int kv = p.kv_len[req];
+  const int cached = kv - qo;
+  const int rows_valid = min(128, qo - i0);
+  const int last_pos = cached + i0 + rows_valid - 1;
+  const int n_kb = (last_pos + 1 + 127) / 128;
+  const int hk = h / (p.Hq / p.Hkv);
+  const int32_t *table = p.bt + p.bt_indptr[req];
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
+      mbar_init(&s_full[s], 1);
+    }
+    mbar_init(p_full, 128);
+    mbar_init(o_full, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tmQ);
+    prefetch_tmap(&tmKV);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------ TMA producer
+      mbar_arrive_expect_tx(q_full, C::Q_BYTES);
+      for (int c = 0; c < C::NH; ++c) tma_load_2d(sQ + c * C::TILE_BYTES, &tmQ, q_full, h * HD + c * 64, t0 + i0);
+      uint32_t issued = 0, issued_ph = 0;
+      bool ok = true;
+      for (int j = 0; j < n_kb && ok; ++j) {
+        const int s = j & 1;
+        const uint32_t ph = (j >> 1) & 1;
+        if (!mbar_wait(&kv_empty[s], ph ^ 1, abort_flag, p.err, kErrWaitProducer)) {
+          ok = false;
+          break;
+        }
+        const int key0 = 128 * j;
+        const int key_end = min(key0 + 128, last_pos + 1);
+        const int np = (key_end - key0 + 15) / 16;
+        mbar_arrive_expect_tx(&kv_full[s], np * 2 * C::NH * 2048);
+        for (int pg = 0; pg < np; ++pg) {
+          int page = table[key0 / 16 + pg];
+          if (page < 0 || page >= p.num_pages) {
+            atomicExch(p.err, kErrBounds);
+            page = 0;
+          }
+          const int zk = (page * 2 + 0) * p.Hkv + hk;
+          const int zv = (page * 2 + 1) * p.Hkv + hk;
+          for (int c = 0; c < C::NH; ++c) {
+            tma_load_3d(sK + s * C::KV_BYTES + c * C::TILE_BYTES + pg * 2048, &tmKV, &kv_full[s], c * 64, 0, zk);
+            tma_load_3d(sV + s * C::KV_BYTES + c * C::TILE_BYTES + pg * 2048, &tmKV, &kv_full[s], c * 64, 0, zv);
+          }
+        }
+        issued |= 1u << s;
+        issued_ph = (issued_ph & ~(1u << s)) | (ph << s);
+      }
+      if (!ok) {
+        for (int s = 0; s < 2; ++s)
+          if (issued & (1u << s)) {
+            const uint64_t t_start = globaltimer();
+            while (!mbar_try_wait(smem_u32(&kv_full[s]), (issued_ph >> s) & 1u) &&
+                   globaltimer() - t_start < kWaitLimitNs) {
+            }
+          }
+      }
+      // the Q load is always in flight once issued; make sure it landed
+      {
+        const uint64_t t_start = globaltimer();
+        while (!mbar_try_wait(smem_u32(q_full), 0) && globaltimer() - t_start < kWaitLimitNs) {
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------------- MMA issuer
+      auto issue_s = [&](int j) {
+        const int s = j & 1;
+        const uint32_t d = tmem + s * 128;
+        const uint32_t q0 = smem_u32(sQ);
+        const uint32_t k0 = smem_u32(sK + s * C::KV_BYTES);
+#pragma unroll
+        for (int c = 0; c < C::NH; ++c)
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t ad = sdesc_sw128(q0 + c * C::TILE_BYTES + kk * 32, 16, 1024);
+            const uint64_t bd = sdesc_sw128(k0 + c * C::TILE_BYTES + kk * 32, 16, 1024);
+            mma_bf16(d, ad, bd, C::IDESC_S, (c > 0 || kk > 0) ? 1u : 0u);
+          }
+        mma_commit(&s_full[s]);
+      };
+      bool ok = mbar_wait(q_full, 0, abort_flag, p.err, kErrWaitMma);
+      if (ok) ok = mbar_wait(&kv_full[0], 0, abort_flag, p.err, kErrWaitMma);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0);
+      }
+      for (int j = 0; j < n_kb && ok; ++j) {
+        if (j + 1 < n_kb) {
+          if (!mbar_wait(&kv_full[(j + 1) & 1], ((j + 1) >> 1) & 1, abort_flag, p.err, kErrWaitMma)) break;
+          tc_fence_after();
+          issue_s(j + 1);
+        }
+        if (!mbar_wait(p_full, j & 1, abort_flag, p.err, kErrWaitMma)) break;
+        tc_fence_after();
+        const int s = j & 1;
+        const uint32_t pbase = smem_u32(sP);
+        const uint32_t vbase = smem_u32(sV + s * C::KV_BYTES);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {  // 16 keys per MMA
+          const uint64_t ad = sdesc_sw128(pbase + (ks >> 2) * C::TILE_BYTES + (ks & 3) * 32, 16, 1024);
+          const uint64_t bd = sdesc_sw128(vbase + ks * 2048, C::TILE_BYTES, 1024);
+          mma_bf16(tmem + 256, ad, bd, C::IDESC_PV, ks > 0 ? 1u : 0u);
+        }
+        mma_commit(o_full);
+        mma_commit(&kv_empty[s]);
+      }
+    }
+  } else {
+    // ------------------------------------------------- softmax / epilogue
+    const int q = warp & 3;
+    const int r = q * 32 + lane;
+    const int q_pos = cached + i0 + r;
+    const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+    float o_acc[HD];
+#pragma unroll
+    for (int d = 0; d < HD; ++d) o_acc[d] = 0.f;
+    float m = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_kb; ++j) {
+      const int b = j & 1;
+      if (!mbar_wait(&s_full[b], (j >> 1) & 1, abort_flag, p.err, kErrWaitSoftmax)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const int key0 = 128 * j;
+      // pass 1: row maximum of the visible scores
+      float mx = -INFINITY;
+#pragma unroll 1
+      for (int cc = 0; cc < 4; ++cc) {
+        float v[32];
+        tmem_ld32(tmem + lane_base + b * 128 + cc * 32, v);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int key = key0 + cc * 32 + i;
+          if (key <= q_pos && key < kv) mx = fmaxf(mx, v[i] * p.scale_log2);
+        }
+      }
+      const float m_new = fmaxf(m, mx);
+      const float alpha = (m == -INFINITY) ? 0.f : exp2f(m - m_new);
+      if (j > 0) {
+        if (!mbar_wait(o_full, (j - 1) & 1, abort_flag, p.err, kErrWaitSoftmax)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int cc = 0; cc < HD / 32; ++cc) {
+          float v[32];
+          tmem_ld32(tmem + lane_base + 256 + cc * 32, v);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o_acc[cc * 32 + i] += v[i];
+        }
+      }
+#pragma unroll
+      for (int d = 0; d < HD; ++d) o_acc[d] *= alpha;
+      l *= alpha;
+      // pass 2: probabilities -> bf16 P tile (A operand, K-major, swizzled)
+#pragma unroll 1
+      for (int cc = 0; cc < 4; ++cc) {
+        float v[32];
+        tmem_ld32(tmem + lane_base + b * 128 + cc * 32, v);
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          const int key = key0 + cc * 32 + i;
+          const float p0 = (key <= q_pos && key < kv) ? exp2f(v[i] * p.scale_log2 - m_new) : 0.f;
+          const float p1 = (key + 1 <= q_pos && key + 1 < kv) ? exp2f(v[i + 1] * p.scale_log2 - m_new) : 0.f;
+          l += p0 + p1;
+          pk[i / 2] = pack_bf16x2(p0, p1);
+        }
+        // keys cc*32 .. cc*32+31 live in P chunk (cc / 2), 16-byte groups
+        uint8_t *prow = sP + (cc >> 1) * C::TILE_BYTES + (r >> 3) * 1024 + (r & 7) * 128;
+#pragma unroll
+        for (int g4 = 0; g4 < 4; ++g4) {
+          const int grp = (cc & 1) * 4 + g4;  // 8-key group within the 64-key chunk
+          *reinterpret_cast<uint4 *>(prow + ((grp ^ (r & 7)) * 16)) =
+              make_uint4(pk[4 * g4], pk[4 * g4 + 1], pk[4 * g4 + 2], pk[4 * g4 + 3]);
+        }
+      }
+      if (j == n_kb - 1 && key0 + r > last_pos) {
+        // rows past the last visible key may hold stale or non-finite data:
+        // zero them so that P = 0 rows contribute exactly nothing
+        uint8_t *vrow = sV + b * C::KV_BYTES + (r >> 3) * 1024 + (r & 7) * 128;
+#pragma unroll
+        for (int c = 0; c < C::NH; ++c)
+#pragma unroll
+          for (int k = 0; k < 8; ++k) *reinterpret_cast<uint4 *>(vrow + c * C::TILE_BYTES + k * 16) = make_uint4(0, 0, 0, 0);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(p_full);
+      m = m_new;
+    }
+    if (ok && mbar_wait(o_full, (n_kb - 1) & 1, abort_flag, p.err, kErrWaitSoftmax)) {
+      tc_fence_after();
+#pragma unroll
+      for (int cc = 0; cc < HD / 32; ++cc) {
+        float v[32];
+        tmem_ld32(tmem + lane_base + 256 + cc * 32, v);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o_acc[cc * 32 + i] += v[i];
+      }
+      if (i0 + r < qo) {
+        const float inv = 1.f / l;
+        uint4 *dst = reinterpret_cast<uint4 *>(p.o + static_cast<size_t>(t0 + i0 + r) * (p.Hq * HD) + h * HD);
+#pragma unroll
+        for (int v8 = 0; v8 < HD / 8; ++v8)
+          dst[v8] = make_uint4(pack_bf16x2(o_acc[8 * v8] * inv, o_acc[8 * v8 + 1] * inv),
+                               pack_bf16x2(o_acc[8 * v8 + 2] * inv, o_acc[8 * v8 + 3] * inv),
+                               pack_bf16x2(o_acc[8 * v8 + 4] * inv, o_acc[8 * v8 + 5] * inv),
+                               pack_bf16x2(o_acc[8 * v8 + 6] * inv, o_acc[8 * v8 + 7] * inv));
+      }
+    }
+    tc_fence_before();
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+// ============================================================ decode rows
+struct DecodeParams {
+  const __nv_bfloat16 *q;
+  const __nv_bfloat16 *pool;
+  __nv_bfloat16 *o;
+  float *part;
+  const int32_t *qo_indptr, *kv_len, *bt_indptr, *bt, *items;
+  int n_items, Hq, Hkv, num_pages;
+  float scale_log2;
+  int *err;
+};
+
+__device__ __forceinline__ uint4 ldg_nc_v4(const void *ptr) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(ptr));
+  return v;
+}
+
+// One warp per work item.  HD / 8 lanes share one key (8 bf16 each), so a
+// warp covers KPS keys per 16-byte load instruction.
+template <int HD, int G>
+__global__ void __launch_bounds__(128) decode_attn_kernel(const DecodeParams p) {
+  constexpr int LPK = HD / 8;
+  constexpr int KPS = 32 / LPK;
+  constexpr int STEPS = 16 / KPS;
+  const int warp_global = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (warp_global >= p.n_items) return;
+  const int lane = threadIdx.x & 31;
+  const int32_t *it = p.items + warp_global * 8;
+  const int req = it[0], hk = it[1], pb = it[2], pe = it[3], n_splits = it[5];
+  const int t = p.qo_indptr[req];
+  const int kv = p.kv_len[req];
+  const int32_t *table = p.bt + p.bt_indptr[req];
+  const int sub = lane % LPK;   // which 8-element slice of hd
+  const int kk = lane / LPK;    // which key of a step
+  const int d0 = sub * 8;
+
+  float qf[G][8];
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    const uint4 raw = *reinterpret_cast<const uint4 *>(p.q + (static_cast<size_t>(t) * p.Hq + hk * G + g) * HD + d0);
+    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      qf[g][2 * e] = bf16lo(w[e]) * p.scale_log2;
+      qf[g][2 * e + 1] = bf16hi(w[e]) * p.scale_log2;
+    }
+  }
+  float m[G], l[G], acc[G][8];
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    m[g] = -INFINITY;
+    l[g] = 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[g][e] = 0.f;
+  }
+  const size_t head_stride = static_cast<size_t>(16) * HD;
+  for (int pg = pb; pg < pe; ++pg) {
+    int page = table[pg];
+    if (page < 0 || page >= p.num_pages) {
+      atomicExch(p.err, kErrBounds);
+      page = 0;
+    }
+    const __nv_bfloat16 *kb = p.pool + ((static_cast<size_t>(page) * 2 + 0) * p.Hkv + hk) * head_stride;
+    const __nv_bfloat16 *vb = kb + static_cast<size_t>(p.Hkv) * head_stride;
+    uint4 kr[STEPS], vr[STEPS];
+#pragma unroll
+    for (int st = 0; st < STEPS; ++st) {
+      const int slot = st * KPS + kk;
+      kr[st] = ldg_nc_v4(kb + slot * HD + d0);
+      vr[st] = ldg_nc_v4(vb + slot * HD + d0);
+    }
+    float s[STEPS][G];
+#pragma unroll
+    for (int st = 0; st < STEPS; ++st) {
+      const uint32_t w[4] = {kr[st].x, kr[st].y, kr[st].z, kr[st].w};
+      float kf[8];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        kf[2 * e] = bf16lo(w[e]);
+        kf[2 * e + 1] = bf16hi(w[e]);
+      }
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        float a = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) a = fmaf(qf[g][e], kf[e], a);
+#pragma unroll
+        for (int off = 1; off < LPK; off <<= 1) a += __shfl_xor_sync(0xffffffffu, a, off);
+        s[st][g] = a;
+      }
+      const int key = pg * 16 + st * KPS + kk;
+      if (key >= kv) {
+#pragma unroll
+        for (int g = 0; g < G; ++g) s[st][g] = -INFINITY;
+        vr[st] = make_uint4(0, 0, 0, 0);
+      }
+    }
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      float pm = -INFINITY;
+#pragma unroll
+      for (int st = 0; st < STEPS; ++st) pm = fmaxf(pm, s[st][g]);
+#pragma unroll
+      for (int off = LPK; off < 32; off <<= 1) pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, off));
+      const float m_new = fmaxf(m[g], pm);
+      const float alpha = (m[g] == -INFINITY) ? 0.f : exp2f(m[g] - m_new);
+      l[g] *= alpha;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[g][e] *= alpha;
+#pragma unroll
+      for (int st = 0; st < STEPS; ++st) {
+        const float pr = (s[st][g] == -INFINITY) ? 0.f : exp2f(s[st][g] - m_new);
+        l[g] += pr;
+        const uint32_t w[4] = {vr[st].x, vr[st].y, vr[st].z, vr[st].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          acc[g][2 * e] = fmaf(pr, bf16lo(w[e]), acc[g][2 * e]);
+          acc[g][2 * e + 1] = fmaf(pr, bf16hi(w[e]), acc[g][2 * e + 1]);
+        }
+      }
+      m[g] = m_new;
+    }
+  }
+  // combine the KPS key lanes that share an hd slice
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+#pragma unroll
+    for (int off = LPK; off < 32; off <<= 1) {
+      l[g] += __shfl_xor_sync(0xffffffffu, l[g], off);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[g][e] += __shfl_xor_sync(0xffffffffu, acc[g][e], off);
+    }
+  }
+  if (kk != 0) return;
+  if (n_splits == 1) {
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const float inv = 1.f / l[g];
+      uint4 out = make_uint4(pack_bf16x2(acc[g][0] * inv, acc[g][1] * inv), pack_bf16x2(acc[g][2] * inv, acc[g][3] * inv),
+                             pack_bf16x2(acc[g][4] * inv, acc[g][5] * inv), pack_bf16x2(acc[g][6] * inv, acc[g][7] * inv));
+      *reinterpret_cast<uint4 *>(p.o + (static_cast<size_t>(t) * p.Hq + hk * G + g) * HD + d0) = out;
+    }
+  } else {
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      float *dst = p.part + (static_cast<size_t>(warp_global) * G + g) * part_stride<HD>();
+      float4 *d4 = reinterpret_cast<float4 *>(dst + d0);
+      d4[0] = make_float4(acc[g][0], acc[g][1], acc[g][2], acc[g][3]);
+      d4[1] = make_float4(acc[g][4], acc[g][5], acc[g][6], acc[g][7]);
+      if (sub == 0) {
+        dst[HD] = m[g];
+        dst[HD + 1] = l[g];
+      }
+    }
+  }
+}
+
+// ============================================================ merge pass
+// One warp per (request, q head) with several splits: o = sum_s w_s o_s /
+// sum_s w_s l_s with w_s = 2^(m_s - max m).
+template <int HD>
+__global__ void __launch_bounds__(128) merge_kernel(const float *part, const int32_t *list, int n, __nv_bfloat16 *o,
+                                                    const int32_t *qo_indptr, int Hq, int G) {
+  const int w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (w >= n * G) return;
+  const int lane = threadIdx.x & 31;
+  const int idx = w / G, g = w % G;
+  const int req = list[idx * 4 + 0], hk = list[idx * 4 + 1], first = list[idx * 4 + 2], ns = list[idx * 4 + 3];
+  float mmax = -INFINITY;
+  for (int s = 0; s < ns; ++s) mmax = fmaxf(mmax, part[(static_cast<size_t>(first + s) * G + g) * part_stride<HD>() + HD]);
+  constexpr int PER = HD / 32;
+  float acc[PER];
+#pragma unroll
+  for (int e = 0; e < PER; ++e) acc[e] = 0.f;
+  float L = 0.f;
+  for (int s = 0; s < ns; ++s) {
+    const float *src = part + (static_cast<size_t>(first + s) * G + g) * part_stride<HD>();
+    const float ms = src[HD];
+    const float wgt = (ms == -INFINITY) ? 0.f : exp2f(ms - mmax);
+    L += wgt * src[HD + 1];
+#pragma unroll
+    for (int e = 0; e < PER; ++e) acc[e] += wgt * src[lane * PER + e];
+  }
+  const float inv = 1.f / L;
+  const int t = qo_indptr[req];
+  __nv_bfloat16 *dst = o + (static_cast<size_t>(t) * Hq + hk * G + g) * HD + lane * PER;
+#pragma unroll
+  for (int e = 0; e < PER; ++e) dst[e] = __float2bfloat16_rn(acc[e] * inv);
+}
+
+template <int HD, int G>
+cudaError_t launch_decode(const DecodeParams &dp, cudaStream_t st) {
+  const int blocks = (dp.n_items + 3) / 4;
+  decode_attn_kernel<HD, G><<<blocks, 128, 0, st>>>(dp);
+  return cudaGetLastError();
+}
+
+template <int HD>
+cudaError_t launch_decode_g(const DecodeParams &dp, int G, cudaStream_t st) {
+  switch (G) {
+    case 1: return launch_decode<HD, 1>(dp, st);
+    case 2: return launch_decode<HD, 2>(dp, st);
+    case 3: return launch_decode<HD, 3>(dp, st);
+    case 4: return launch_decode<HD, 4>(dp, st);
+    case 5: return launch_decode<HD, 5>(dp, st);
+    case 6: return launch_decode<HD, 6>(dp, st);
+    case 7: return launch_decode<HD, 7>(dp, st);
+    case 8: return launch_decode<HD, 8>(dp, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <int HD>
+cudaError_t launch_chunk(const CUtensorMap &tq, const CUtensorMap &tkv, const ChunkParams &cp, int n_tiles,
+                         cudaStream_t st) {
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(chunk_attn_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    ChunkCfg<HD>::SMEM);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  chunk_attn_kernel<HD><<<n_tiles, 192, ChunkCfg<HD>::SMEM, st>>>(tq, tkv, cp);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t attention_run(const AttnArgs &a, cudaStream_t st) {
+  const float scale_log2 = kLog2e / sqrtf(static_cast<float>(a.hd));
+  const int G = a.Hq / a.Hkv;
+  cudaError_t e = cudaSuccess;
+  if (a.n_tiles > 0) {
+    ChunkParams cp;
+    cp.o = static_cast<__nv_bfloat16 *>(a.o);
+    cp.qo_indptr = a.qo_indptr;
+    cp.kv_len = a.kv_len;
+    cp.bt_indptr = a.bt_indptr;
+    cp.bt = a.bt;
+    cp.tiles = a.tiles;
+    cp.Hq = a.Hq;
+    cp.Hkv = a.Hkv;
+    cp.num_pages = a.num_pages;
+    cp.scale_log2 = scale_log2;
+    cp.err = a.err;
+    e = a.hd == 128 ? launch_chunk<128>(*a.tm_q, *a.tm_kv, cp, a.n_tiles, st)
+                    : launch_chunk<64>(*a.tm_q, *a.tm_kv, cp, a.n_tiles, st);
+    if (e != cudaSuccess) return e;
+  }
+  if (a.n_items > 0) {
+    DecodeParams dp;
+    dp.q = static_cast<const __nv_bfloat16 *>(a.q);
+    dp.pool = static_cast<const __nv_bfloat16 *>(a.pool);
+    dp.o = static_cast<__nv_bfloat16 *>(a.o);
+    dp.part = a.part;
+    dp.qo_indptr = a.qo_indptr;
+    dp.kv_len = a.kv_len;
+    dp.bt_indptr = a.bt_indptr;
+    dp.bt = a.bt;
+    dp.items = a.items;
+    dp.n_items = a.n_items;
+    dp.Hq = a.Hq;
+    dp.Hkv = a.Hkv;
+    dp.num_pages = a.num_pages;
+    dp.scale_log2 = scale_log2;
+    dp.err = a.err;
+    e = a.hd == 128 ? launch_decode_g<128>(dp, G, st) : launch_decode_g<64>(dp, G, st);
+  }
+  return e;
+}
+
+cudaError_t attn_merge_run(const MergeArgs &m, cudaStream_t st) {
+  if (m.n_merge <= 0) return cudaSuccess;
+  const int G = m.Hq / m.Hkv;
+  const int warps = m.n_merge * G;
+  const int blocks = (warps + 3) / 4;
+  if (m.hd == 128)
+    merge_kernel<128><<<blocks, 128, 0, st>>>(m.part, m.merge_list, m.n_merge, static_cast<__nv_bfloat16 *>(m.o),
+                                              m.qo_indptr, m.Hq, G);
+  else
+    merge_kernel<64><<<blocks, 128, 0, st>>>(m.part, m.merge_list, m.n_merge, static_cast<__nv_bfloat16 *>(m.o),
+                                             m.qo_indptr, m.Hq, G);
+  return cudaGetLastError();
+}
+
+}  // namespace mb

@@ -1,0 +1,225 @@
+// Bandwidth-bound kernels of the step: RMSNorm, and the fused
+// (q/k RMSNorm) + RoPE + KV-append that writes this step's keys and values
+// into their 16-token pages before attention reads them (pofe.ai "Chunked
+// prefill", "How it works, step by step", step 4: chunks write their K/V into
+// the cache, then attend).
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "mb_kernels.h"
+#include "mb_ptx.cuh"
+
+namespace mb {
+namespace {
+
+using namespace dev;
+
+// ------------------------------------------------------------------ RMSNorm
+// y = x / sqrt(mean(x^2) + eps) * g, one CTA per row, 16-byte vectors.
+constexpr int kNormThreads = 128;
+constexpr int kNormMaxVec = 8;  // d <= 128 * 8 * 8 = 8192
+
+__global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const __nv_bfloat16 *__restrict__ x,
+                                                               const __nv_bfloat16 *__restrict__ g,
+                                                               __nv_bfloat16 *__restrict__ y, int d, float eps) {
+  const int row = blockIdx.x;
+  const int nv = d / 8;
+  const uint4 *xr = reinterpret_cast<const uint4 *>(x + static_cast<size_t>(row) * d);
+  const uint4 *gr = reinterpret_cast<const uint4 *>(g);
+  uint4 buf[kNormMaxVec];
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < kNormMaxVec; ++i) {
+    const int v = threadIdx.x + i * kNormThreads;
+    if (v < nv) {
+      buf[i] = xr[v];
+      const uint32_t w[4] = {buf[i].x, buf[i].y, buf[i].z, buf[i].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float a = bf16lo(w[e]), b = bf16hi(w[e]);
+        ss = fmaf(a, a, ss);
+        ss = fmaf(b, b, ss);
+      }
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+  __shared__ float red[kNormThreads / 32];
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  float tot = 0.f;
+#pragma unroll
+  for (int i = 0; i < kNormThreads / 32; ++i) tot += red[i];
+  const float inv = rsqrtf(tot / static_cast<float>(d) + eps);
+  uint4 *yr = reinterpret_cast<uint4 *>(y + static_cast<size_t>(row) * d);
+#pragma unroll
+  for (int i = 0; i < kNormMaxVec; ++i) {
+    const int v = threadIdx.x + i * kNormThreads;
+    if (v < nv) {
+      const uint4 gv = gr[v];
+      const uint32_t w[4] = {buf[i].x, buf[i].y, buf[i].z, buf[i].w};
+      const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+      uint32_t o[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        o[e] = pack_bf16x2(bf16lo(w[e]) * inv * bf16lo(gw[e]), bf16hi(w[e]) * inv * bf16hi(gw[e]));
+      yr[v] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+  }
+}
+
+// ------------------------------------------------------- RoPE + KV append
+// One CTA per token; warp w handles heads w, w + 8, ... of
+// [Q heads | K heads | V heads].  Rotate-half pairing (i, i + hd/2) with
+// frequency theta^(-2i/hd) at the token's absolute position.  The angle is
+// pos * f with f split into a float head and tail (pos is exact in fp32), and
+// reduced modulo 2 pi with a two-constant Cody-Waite step before sincosf, so
+// it keeps ~1e-6 rad accuracy at positions in the tens of thousands.
+constexpr int kRopeThreads = 256;
+constexpr float kTwoPiHi = 6.28318548202514648f;         // fp32(2 pi)
+constexpr float kTwoPiLo = -1.7484556000744893e-07f;     // 2 pi - kTwoPiHi
+
+struct RopeParams {
+  const __nv_bfloat16 *qkv;
+  __nv_bfloat16 *q_out;
+  __nv_bfloat16 *pool;
+  const int32_t *tok_req, *tok_pos, *bt_indptr, *bt;
+  const __nv_bfloat16 *g_q, *g_k;
+  int Hq, Hkv, qk_norm, num_pages;
+  float eps;
+  int *err;
+  float f_hi[64], f_lo[64];
+};
+
+template <int HD>
+__global__ void __launch_bounds__(kRopeThreads) rope_append_kernel(const RopeParams p) {
+  constexpr int HALF = HD / 2;
+  constexpr int PAIRS = HALF / 32;  // pairs per lane
+  __shared__ float cs[HALF], sn[HALF];
+  const int t = blockIdx.x;
+  const int pos = p.tok_pos[t];
+  for (int i = threadIdx.x; i < HALF; i += kRopeThreads) {
+    const float fp = static_cast<float>(pos);
+    const float hi = fp * p.f_hi[i];
+    const float lo = fmaf(fp, p.f_hi[i], -hi) + fp * p.f_lo[i];
+    const float k = rintf(hi * 0.15915494309189535f);
+    float r = fmaf(-k, kTwoPiHi, hi);
+    r = fmaf(-k, kTwoPiLo, r) + lo;
+    float s, c;
+    sincosf(r, &s, &c);
+    cs[i] = c;
+    sn[i] = s;
+  }
+  __syncthreads();
+
+  const int req = p.tok_req[t];
+  int page = p.bt[p.bt_indptr[req] + pos / kPage];
+  const int slot = pos % kPage;
+  if (page < 0 || page >= p.num_pages) {
+    if (threadIdx.x == 0) atomicExch(p.err, kErrBounds);
+    return;
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int heads = p.Hq + 2 * p.Hkv;
+  const int row_len = heads * HD;
+  for (int hh = warp; hh < heads; hh += kRopeThreads / 32) {
+    const __nv_bfloat16 *src = p.qkv + static_cast<size_t>(t) * row_len + hh * HD;
+    float x1[PAIRS], x2[PAIRS];
+#pragma unroll
+    for (int j = 0; j < PAIRS; ++j) {
+      const int i = lane * PAIRS + j;
+      x1[j] = __bfloat162float(src[i]);
+      x2[j] = __bfloat162float(src[i + HALF]);
+    }
+    const bool is_q = hh < p.Hq;
+    const bool is_k = !is_q && hh < p.Hq + p.Hkv;
+    if (is_q || is_k) {
+      if (p.qk_norm) {
+        float ss = 0.f;
+#pragma unroll
+        for (int j = 0; j < PAIRS; ++j) ss += x1[j] * x1[j] + x2[j] * x2[j];
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+        const float inv = rsqrtf(ss / static_cast<float>(HD) + p.eps);
+        const __nv_bfloat16 *g = is_q ? p.g_q : p.g_k;
+#pragma unroll
+        for (int j = 0; j < PAIRS; ++j) {
+          const int i = lane * PAIRS + j;
+          x1[j] = x1[j] * inv * __bfloat162float(g[i]);
+          x2[j] = x2[j] * inv * __bfloat162float(g[i + HALF]);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < PAIRS; ++j) {
+        const int i = lane * PAIRS + j;
+        const float a = x1[j], b = x2[j];
+        x1[j] = a * cs[i] - b * sn[i];
+        x2[j] = b * cs[i] + a * sn[i];
+      }
+    }
+    __nv_bfloat16 *dst;
+    if (is_q) {
+      dst = p.q_out + (static_cast<size_t>(t) * p.Hq + hh) * HD;
+    } else {
+      const int kvsel = is_k ? 0 : 1;
+      const int hk = is_k ? hh - p.Hq : hh - p.Hq - p.Hkv;
+      dst = p.pool + (((static_cast<size_t>(page) * 2 + kvsel) * p.Hkv + hk) * kPage + slot) * HD;
+    }
+#pragma unroll
+    for (int j = 0; j < PAIRS; ++j) {
+      const int i = lane * PAIRS + j;
+      dst[i] = __float2bfloat16_rn(x1[j]);
+      dst[i + HALF] = __float2bfloat16_rn(x2[j]);
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t rmsnorm_run(const void *x, const void *g, void *y, int rows, int d, float eps, cudaStream_t st) {
+  if (rows <= 0) return cudaSuccess;
+  if (d % 8 != 0 || d > kNormThreads * kNormMaxVec * 8) return cudaErrorInvalidValue;
+  rmsnorm_kernel<<<rows, kNormThreads, 0, st>>>(static_cast<const __nv_bfloat16 *>(x),
+                                                static_cast<const __nv_bfloat16 *>(g),
+                                                static_cast<__nv_bfloat16 *>(y), d, eps);
+  return cudaGetLastError();
+}
+
+cudaError_t rope_append_run(const RopeArgs &a, cudaStream_t st) {
+  if (a.T <= 0) return cudaSuccess;
+  RopeParams p;
+  p.qkv = static_cast<const __nv_bfloat16 *>(a.qkv);
+  p.q_out = static_cast<__nv_bfloat16 *>(a.q_out);
+  p.pool = static_cast<__nv_bfloat16 *>(a.pool);
+  p.tok_req = a.tok_req;
+  p.tok_pos = a.tok_pos;
+  p.bt_indptr = a.bt_indptr;
+  p.bt = a.bt;
+  p.g_q = static_cast<const __nv_bfloat16 *>(a.g_q);
+  p.g_k = static_cast<const __nv_bfloat16 *>(a.g_k);
+  p.Hq = a.Hq;
+  p.Hkv = a.Hkv;
+  p.qk_norm = a.qk_norm;
+  p.num_pages = a.num_pages;
+  p.eps = a.eps;
+  p.err = a.err;
+  const int half = a.hd / 2;
+  for (int i = 0; i < 64; ++i) {
+    double f = i < half ? std::pow(static_cast<double>(a.theta), -2.0 * i / a.hd) : 0.0;
+    p.f_hi[i] = static_cast<float>(f);
+    p.f_lo[i] = static_cast<float>(f - static_cast<double>(p.f_hi[i]));
+  }
+  if (a.hd == 128)
+    rope_append_kernel<128><<<a.T, kRopeThreads, 0, st>>>(p);
+  else if (a.hd == 64)
+    rope_append_kernel<64><<<a.T, kRopeThreads, 0, st>>>(p);
+  else
+    return cudaErrorInvalidValue;
+  return cudaGetLastError();
+}
+
+}  // namespace mb

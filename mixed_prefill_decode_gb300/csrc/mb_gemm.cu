@@ -1,0 +1,493 @@
+// Token-batched linear layers of the mixed step on the tcgen05 tensor cores.
+//
+// Prefill-chunk rows and decode rows are rows of one GEMM, so every weight
+// tile is read once for all of them (ConfluxServe summary, "Why can linear
+// layers be batched but attention cannot?"; pofe.ai "Chunked prefill": decodes
+// "are 64 more rows in a 4,160-row matrix multiply").
+//
+// D[M][N] = A[M][K] B[N][K]^T, bf16 in, fp32 accumulate in TMEM.
+//   tile      128 (tokens) x 256 (weight rows), K step 64 (one 128-byte
+//             swizzle atom), 4-stage TMA ring (48 KB per stage)
+//   warps     0: TMA producer, 1: MMA issuer (+ TMEM owner), 2-5: epilogue
+//   TMEM      two 256-column fp32 accumulators, so the epilogue of one tile
+//             overlaps the main loop of the next
+//   schedule  persistent; whole tiles data-parallel while there are several
+//             waves, the last one to two waves split along K evenly over all
+//             CTAs (stream-K).  A split tile's pieces go to fp32 partial slots;
+//             the CTA that takes the last ticket of the tile sums the pieces in
+//             CTA order (deterministic) and runs the epilogue.  No CTA waits on
+//             another.
+//   epilogues store | + residual | SwiGLU (B rows [gate F; up F]: a tile loads
+//             128 gate rows and the matching 128 up rows and writes
+//             silu(g) * u for 128 output features)
+//
+// The partial tile quantisation the pofe.ai page warns about (chunk 257 vs
+// 256, "Tile quantisation") is what the stream-K tail removes along N x K; a
+// ragged M tail still costs a full 128-row MMA.
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstdio>
+#include <mutex>
+
+#include "mb_kernels.h"
+#include "mb_ptx.cuh"
+
+namespace mb {
+namespace {
+
+using namespace dev;
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;
+constexpr int STAGES = 4;
+constexpr int A_STAGE = BM * BK * 2;   // 16 KB
+constexpr int B_STAGE = BN * BK * 2;   // 32 KB
+constexpr int SMEM_TILES = STAGES * (A_STAGE + B_STAGE);
+constexpr int SMEM_BYTES = SMEM_TILES + 1024 /*align*/ + 256 /*barriers*/;
+constexpr int THREADS = 192;
+constexpr uint32_t IDESC = idesc_bf16(BM, BN, false);
+
+struct Params {
+  int M, N, K;          // N: output width (F for SwiGLU)
+  int k_iters;
+  int tiles_m;
+  int dp_tiles, sk_tiles;
+  int grid;
+  __nv_bfloat16 *D;
+  int ldd;
+  const __nv_bfloat16 *R;
+  int ldr;
+  int F;                // SwiGLU: row offset of the up half in B
+  float *partials;
+  int *tickets;
+  int *err;
+};
+
+struct Seg {
+  int tile, k0, k1;
+  int partial;  // 0: whole K range; 1: a piece of a split tile
+  int slot;     // partial slot of this piece
+  int tl;       // stream-K local tile index
+};
+
+// Segment enumerator: every role of a CTA walks the same sequence.
+struct SegIter {
+  const Params &p;
+  int b;
+  int dp_next;
+  long long it, it_end;
+  long long total;
+  __device__ SegIter(const Params &pp) : p(pp), b(blockIdx.x) {
+    dp_next = b;
+    total = static_cast<long long>(p.sk_tiles) * p.k_iters;
+    it = total * b / p.grid;
+    it_end = total * (b + 1) / p.grid;
+  }
+  __device__ bool next(Seg &s) {
+    if (dp_next < p.dp_tiles) {
+      s.tile = dp_next;
+      s.k0 = 0;
+      s.k1 = p.k_iters;
+      s.partial = 0;
+      s.slot = 0;
+      s.tl = -1;
+      dp_next += p.grid;
+      return true;
+    }
+    if (it >= it_end) return false;
+    const int tl = static_cast<int>(it / p.k_iters);
+    const int k0 = static_cast<int>(it % p.k_iters);
+    long long rem = it_end - it;
+    const int k1 = static_cast<int>(min(static_cast<long long>(p.k_iters), k0 + rem));
+    s.tile = p.dp_tiles + tl;
+    s.k0 = k0;
+    s.k1 = k1;
+    s.partial = !(k0 == 0 && k1 == p.k_iters);
+    const long long first_it = total * b / p.grid;
+    s.slot = 2 * b + (tl == static_cast<int>(first_it / p.k_iters) ? 0 : 1);
+    s.tl = tl;
+    it += k1 - k0;
+    return true;
+  }
+};
+
+// CTAs whose stream-K ranges overlap local tile tl: [c_first, c_last].
+__device__ void tile_contributors(const Params &p, int tl, int &c_first, int &c_last) {
+  const long long total = static_cast<long long>(p.sk_tiles) * p.k_iters;
+  const long long lo = static_cast<long long>(tl) * p.k_iters;
+  const long long hi = lo + p.k_iters - 1;
+  // CTA c covers [total*c/grid, total*(c+1)/grid); invert with a search.
+  auto owner = [&](long long x) {
+    int c = static_cast<int>((x * p.grid) / total);
+    while (c > 0 && total * c / p.grid > x) --c;
+    while (c + 1 < p.grid && total * (c + 1) / p.grid <= x) ++c;
+    return c;
+  };
+  c_first = owner(lo);
+  c_last = owner(hi);
+}
+
+__device__ __forceinline__ float silu(float x) { return x / (1.0f + expf(-x)); }
+
+template <int EPI>
+__device__ __forceinline__ void store_chunk(const Params &p, int row, int col, const float (&v)[32],
+                                            const float (*u)[32]) {
+  // col: first output column of this 32-wide chunk
+  if (row >= p.M || col >= p.N) return;
+  uint32_t packed[16];
+  if (EPI == kEpiSwiGLU) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      packed[i] = pack_bf16x2(silu(v[2 * i]) * (*u)[2 * i], silu(v[2 * i + 1]) * (*u)[2 * i + 1]);
+  } else if (EPI == kEpiResidual) {
+    const uint4 *rp = reinterpret_cast<const uint4 *>(p.R + static_cast<size_t>(row) * p.ldr + col);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint4 r = rp[q];
+      uint32_t rr[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int i = q * 4 + j;
+        packed[i] = pack_bf16x2(v[2 * i] + bf16lo(rr[j]), v[2 * i + 1] + bf16hi(rr[j]));
+      }
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) packed[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+  }
+  uint4 *dp = reinterpret_cast<uint4 *>(p.D + static_cast<size_t>(row) * p.ldd + col);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) dp[q] = make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(THREADS, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = align1024(smem_raw);
+  uint8_t *sA = smem;
+  uint8_t *sB = smem + STAGES * A_STAGE;
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + SMEM_TILES);
+  uint64_t *empty = full + STAGES;
+  uint64_t *tfull = empty + STAGES;
+  uint64_t *tempty = tfull + 2;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tempty + 2);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  volatile int *bcast = abort_flag + 1;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 128);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------- TMA producer
+      SegIter segs(p);
+      Seg sg;
+      int s = 0;
+      uint32_t ph = 0;
+      uint32_t issued_mask = 0, issued_ph = 0;
+      bool ok = true;
+      while (ok && segs.next(sg)) {
+        const int m0 = (sg.tile % p.tiles_m) * BM;
+        const int nt = sg.tile / p.tiles_m;
+        const int rows0 = EPI == kEpiSwiGLU ? nt * 128 : nt * BN;
+        const int rows1 = EPI == kEpiSwiGLU ? p.F + nt * 128 : nt * BN + 128;
+        for (int kb = sg.k0; kb < sg.k1; ++kb) {
+          if (!mbar_wait(&empty[s], ph ^ 1, abort_flag, p.err, kErrWaitProducer)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[s], A_STAGE + B_STAGE);
+          tma_load_2d(sA + s * A_STAGE, &tmA, &full[s], kb * BK, m0);
+          tma_load_2d(sB + s * B_STAGE, &tmB, &full[s], kb * BK, rows0);
+          tma_load_2d(sB + s * B_STAGE + B_STAGE / 2, &tmB, &full[s], kb * BK, rows1);
+          issued_mask |= 1u << s;
+          issued_ph = (issued_ph & ~(1u << s)) | (ph << s);
+          if (++s == STAGES) {
+            s = 0;
+            ph ^= 1;
+          }
+        }
+      }
+      if (!ok) {
+        // let copies already in flight land before the CTA exits
+        for (int i = 0; i < STAGES; ++i)
+          if (issued_mask & (1u << i)) {
+            int dummy = 0;
+            volatile int never = 0;
+            const uint32_t a = smem_u32(&full[i]);
+            const uint64_t t0 = globaltimer();
+            while (!mbar_try_wait(a, (issued_ph >> i) & 1u) && globaltimer() - t0 < kWaitLimitNs && !never) {
+              ++dummy;
+            }
+          }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------------------------------------------------- MMA issuer
+      SegIter segs(p);
+      Seg sg;
+      int s = 0;
+      uint32_t ph = 0;
+      int acc = 0;
+      uint32_t acc_ph = 0;
+      bool ok = true;
+      while (ok && segs.next(sg)) {
+        if (!mbar_wait(&tempty[acc], acc_ph ^ 1, abort_flag, p.err, kErrWaitMma)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + acc * BN;
+        for (int kb = sg.k0; kb < sg.k1; ++kb) {
+          if (!mbar_wait(&full[s], ph, abort_flag, p.err, kErrWaitMma)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(sA + s * A_STAGE);
+          const uint32_t b0 = smem_u32(sB + s * B_STAGE);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t ad = sdesc_sw128(a0 + kk * 32, 16, 1024);
+            const uint64_t bd = sdesc_sw128(b0 + kk * 32, 16, 1024);
+            mma_bf16(d, ad, bd, IDESC, (kb > sg.k0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(&empty[s]);
+          if (++s == STAGES) {
+            s = 0;
+            ph ^= 1;
+          }
+        }
+        if (!ok) break;
+        mma_commit(&tfull[acc]);
+        acc ^= 1;
+        if (acc == 0) acc_ph ^= 1;
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;            // TMEM lane quarter this warp may read
+    const int r = q * 32 + lane;       // row within the tile
+    const int ep = threadIdx.x - 64;   // 0..127
+    SegIter segs(p);
+    Seg sg;
+    int acc = 0;
+    uint32_t acc_ph = 0;
+    while (segs.next(sg)) {
+      if (!mbar_wait(&tfull[acc], acc_ph, abort_flag, p.err, kErrWaitEpilogue)) break;
+      tc_fence_after();
+      const uint32_t tbase = tmem + acc * BN + (static_cast<uint32_t>(q * 32) << 16);
+      const int m0 = (sg.tile % p.tiles_m) * BM;
+      const int nt = sg.tile / p.tiles_m;
+      const int row = m0 + r;
+      if (!sg.partial) {
+        if (EPI == kEpiSwiGLU) {
+#pragma unroll 1
+          for (int j = 0; j < 4; ++j) {
+            float g[32], u[32];
+            tmem_ld32(tbase + 32 * j, g);
+            tmem_ld32(tbase + 128 + 32 * j, u);
+            store_chunk<EPI>(p, row, nt * 128 + 32 * j, g, &u);
+          }
+        } else {
+#pragma unroll 1
+          for (int j = 0; j < BN / 32; ++j) {
+            float v[32];
+            tmem_ld32(tbase + 32 * j, v);
+            store_chunk<EPI>(p, row, nt * BN + 32 * j, v, nullptr);
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(&tempty[acc]);
+      } else {
+        float *ws = p.partials + (static_cast<size_t>(sg.slot) * BM + r) * BN;
+#pragma unroll 1
+        for (int j = 0; j < BN / 32; ++j) {
+          float v[32];
+          tmem_ld32(tbase + 32 * j, v);
+          float4 *w4 = reinterpret_cast<float4 *>(ws + 32 * j);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) w4[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+        }
+        tc_fence_before();
+        mbar_arrive(&tempty[acc]);
+        __threadfence();
+        named_bar_sync(1, 128);
+        int c_first, c_last;
+        tile_contributors(p, sg.tl, c_first, c_last);
+        if (ep == 0) {
+          const int n = c_last - c_first + 1;
+          const int old = atomicAdd(&p.tickets[sg.tl], 1);
+          const int last = (old == n - 1);
+          if (last) p.tickets[sg.tl] = 0;
+          *bcast = last;
+        }
+        named_bar_sync(1, 128);
+        if (*bcast) {
+          __threadfence();
+          const long long total = static_cast<long long>(p.sk_tiles) * p.k_iters;
+          auto slot_of = [&](int c) {
+            const long long first_it = total * c / p.grid;
+            return 2 * c + (sg.tl == static_cast<int>(first_it / p.k_iters) ? 0 : 1);
+          };
+          if (EPI == kEpiSwiGLU) {
+#pragma unroll 1
+            for (int j = 0; j < 4; ++j) {
+              float g[32], u[32];
+#pragma unroll
+              for (int i = 0; i < 32; ++i) g[i] = u[i] = 0.f;
+              for (int c = c_first; c <= c_last; ++c) {
+                const float *src = p.partials + (static_cast<size_t>(slot_of(c)) * BM + r) * BN;
+                const float4 *g4 = reinterpret_cast<const float4 *>(src + 32 * j);
+                const float4 *u4 = reinterpret_cast<const float4 *>(src + 128 + 32 * j);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                  float4 a = __ldcg(g4 + i), b = __ldcg(u4 + i);
+                  g[4 * i] += a.x; g[4 * i + 1] += a.y; g[4 * i + 2] += a.z; g[4 * i + 3] += a.w;
+                  u[4 * i] += b.x; u[4 * i + 1] += b.y; u[4 * i + 2] += b.z; u[4 * i + 3] += b.w;
+                }
+              }
+              store_chunk<EPI>(p, row, nt * 128 + 32 * j, g, &u);
+            }
+          } else {
+#pragma unroll 1
+            for (int j = 0; j < BN / 32; ++j) {
+              float v[32];
+#pragma unroll
+              for (int i = 0; i < 32; ++i) v[i] = 0.f;
+              for (int c = c_first; c <= c_last; ++c) {
+                const float4 *s4 = reinterpret_cast<const float4 *>(
+                    p.partials + (static_cast<size_t>(slot_of(c)) * BM + r) * BN + 32 * j);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                  float4 a = __ldcg(s4 + i);
+                  v[4 * i] += a.x; v[4 * i + 1] += a.y; v[4 * i + 2] += a.z; v[4 * i + 3] += a.w;
+                }
+              }
+              store_chunk<EPI>(p, row, nt * BN + 32 * j, v, nullptr);
+            }
+          }
+        }
+      }
+      acc ^= 1;
+      if (acc == 0) acc_ph ^= 1;
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int EPI>
+cudaError_t launch(const CUtensorMap &tmA, const CUtensorMap &tmB, const Params &p, cudaStream_t st) {
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  gemm_kernel<EPI><<<p.grid, THREADS, SMEM_BYTES, st>>>(tmA, tmB, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t gemm_workspace_bytes() {
+  return static_cast<size_t>(2 * kMaxGemmGrid) * BM * BN * sizeof(float) + 2 * kMaxGemmGrid * sizeof(int);
+}
+
+GemmWorkspace gemm_workspace_carve(void *base) {
+  GemmWorkspace w;
+  w.partials = static_cast<float *>(base);
+  w.tickets = reinterpret_cast<int *>(static_cast<char *>(base) +
+                                      static_cast<size_t>(2 * kMaxGemmGrid) * BM * BN * sizeof(float));
+  return w;
+}
+
+cudaError_t gemm_run(const void *A, const void *B, const CUtensorMap *tmB_pre, void *D, const void *R, int M, int N,
+                     int K, int epi, const GemmWorkspace &ws, int *err, cudaStream_t st) {
+  if (M <= 0) return cudaSuccess;
+  const int b_rows = epi == kEpiSwiGLU ? 2 * N : N;
+  CUtensorMap tmA, tmB;
+  cudaError_t e = encode_tmap_2d(&tmA, A, K, M, static_cast<uint64_t>(K) * 2, BK, BM);
+  if (e != cudaSuccess) return e;
+  if (tmB_pre) {
+    tmB = *tmB_pre;
+  } else {
+    e = encode_tmap_2d(&tmB, B, K, b_rows, static_cast<uint64_t>(K) * 2, BK, 128);
+    if (e != cudaSuccess) return e;
+  }
+  Params p{};
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.k_iters = K / BK;
+  p.tiles_m = (M + BM - 1) / BM;
+  const int tiles_n = epi == kEpiSwiGLU ? N / 128 : (N + BN - 1) / BN;
+  const int tiles = p.tiles_m * tiles_n;
+  const int sms = device_sm_count() < kMaxGemmGrid ? device_sm_count() : kMaxGemmGrid;
+  // Whole waves run data-parallel; the last one to two waves are spread along
+  // K over every SM.  A tile count that is a multiple of the SM count needs no
+  // split.
+  if (tiles % sms == 0) {
+    p.dp_tiles = tiles;
+    p.sk_tiles = 0;
+    p.grid = sms;
+  } else {
+    const int waves = tiles / sms;
+    p.dp_tiles = waves >= 2 ? (waves - 1) * sms : 0;
+    p.sk_tiles = tiles - p.dp_tiles;
+    const long long sk_iters = static_cast<long long>(p.sk_tiles) * p.k_iters;
+    long long g = sms;
+    if (sk_iters < 2LL * g) g = sk_iters / 2 > 0 ? sk_iters / 2 : 1;  // at least two K steps per CTA
+    if (p.dp_tiles > 0 && g < sms) g = sms;
+    p.grid = static_cast<int>(g);
+    if (p.dp_tiles > 0 && p.grid != sms) return cudaErrorInvalidValue;
+  }
+  p.D = static_cast<__nv_bfloat16 *>(D);
+  p.ldd = N;
+  p.R = static_cast<const __nv_bfloat16 *>(R);
+  p.ldr = N;
+  p.F = epi == kEpiSwiGLU ? N : 0;
+  p.partials = ws.partials;
+  p.tickets = ws.tickets;
+  p.err = err;
+  switch (epi) {
+    case kEpiStore: return launch<kEpiStore>(tmA, tmB, p, st);
+    case kEpiResidual: return launch<kEpiResidual>(tmA, tmB, p, st);
+    case kEpiSwiGLU: return launch<kEpiSwiGLU>(tmA, tmB, p, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace mb

@@ -1,0 +1,86 @@
+// Host-side launchers of the device kernels (internal to the library).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace mb {
+
+constexpr int kPage = 16;
+
+// ---- tensor maps (driver entry point fetched at run time; the library does
+// not link libcuda, so it loads on machines without a driver) ----
+cudaError_t encode_tmap_2d(CUtensorMap *map, const void *base, uint64_t inner, uint64_t outer,
+                           uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer);
+cudaError_t encode_tmap_3d(CUtensorMap *map, const void *base, uint64_t d0, uint64_t d1, uint64_t d2,
+                           uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t b0, uint32_t b1, uint32_t b2);
+
+int device_sm_count();
+
+// ---- token-batched GEMM on tcgen05 ----
+enum GemmEpilogue : int { kEpiStore = 0, kEpiResidual = 1, kEpiSwiGLU = 2 };
+
+struct GemmWorkspace {
+  float *partials;  // [2 * kMaxGemmGrid][128][256] fp32
+  int *tickets;     // [2 * kMaxGemmGrid]
+};
+constexpr int kMaxGemmGrid = 256;
+size_t gemm_workspace_bytes();
+GemmWorkspace gemm_workspace_carve(void *base);
+
+// D = A B^T (+ R) or SwiGLU; A [M][K], B [Nb][K] (Nb = N, or 2F for SwiGLU
+// where N = F is the output width).  tmB may be a pre-encoded map of B (box
+// 64 x 128) or nullptr.
+cudaError_t gemm_run(const void *A, const void *B, const CUtensorMap *tmB, void *D, const void *R, int M, int N,
+                     int K, int epi, const GemmWorkspace &ws, int *err, cudaStream_t st);
+
+// ---- element-wise kernels ----
+cudaError_t rmsnorm_run(const void *x, const void *g, void *y, int rows, int d, float eps, cudaStream_t st);
+
+struct RopeArgs {
+  const void *qkv;          // [T][(Hq + 2 Hkv) hd] bf16
+  void *q_out;              // [T][Hq][hd] bf16
+  void *pool;               // [P][2][Hkv][16][hd] bf16
+  const int32_t *tok_req;   // [T] request of each token
+  const int32_t *tok_pos;   // [T] absolute position of each token
+  const int32_t *bt_indptr; // [n+1]
+  const int32_t *bt;        // block tables
+  const void *g_q, *g_k;    // [hd] bf16 or null
+  int T, Hq, Hkv, hd, qk_norm, num_pages;
+  float eps, theta;
+  int *err;
+};
+cudaError_t rope_append_run(const RopeArgs &a, cudaStream_t st);
+
+// ---- attention ----
+// Work lists (device int32, built on the host per step):
+//   chunk tiles:   {req, q_row0, q_head, 0} x n_tiles   (128 query rows each)
+//   decode items:  {req, kv_head, page_begin, page_end, split, n_splits, 0, 0} x n_items
+struct AttnArgs {
+  const void *q;            // [T][Hq][hd] bf16 (rotated)
+  const void *pool;         // [P][2][Hkv][16][hd]
+  void *o;                  // [T][Hq hd] bf16
+  const int32_t *qo_indptr, *kv_len, *bt_indptr, *bt;
+  const int32_t *tiles;     // chunk tile list
+  const int32_t *items;     // decode item list
+  float *part;              // decode split partials [n_items][Hq/Hkv group][hd + 4]: o, m, l, pad
+  int n_tiles, n_items;
+  int T, Hq, Hkv, hd, num_pages;
+  int *err;
+  const CUtensorMap *tm_q;  // Q map [T][Hq hd], box 64 x 128 (host pointer; copied into launch)
+  const CUtensorMap *tm_kv; // pool map [P*2*Hkv][16][hd], box 64 x 16 x 1
+};
+cudaError_t attention_run(const AttnArgs &a, cudaStream_t st);
+
+struct MergeArgs {
+  const float *part;
+  const int32_t *merge_list;  // per merged (req, kv_head): {req, kv_head, first_slot, n_splits}
+  int n_merge;
+  void *o;
+  const int32_t *qo_indptr;
+  int Hq, Hkv, hd;
+};
+cudaError_t attn_merge_run(const MergeArgs &m, cudaStream_t st);
+
+}  // namespace mb

@@ -1,0 +1,153 @@
+"""Host-side checks of the C-ABI library that need no GPU: the library loads
+and exports every entry point include/mb.h declares, the native packer agrees
+bit for bit with the oracle packer, and descriptor validation rejects every
+malformed batch before any device work."""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle.packer import Packer, rows_to_csr
+from mixed_prefill_decode_gb300 import workload as W
+
+
+def test_exports_every_declared_symbol(mb):
+    syms = mb.header_symbols()
+    assert len(syms) >= 20
+    missing = [s for s in syms if not hasattr(mb.lib(), s)]
+    assert missing == []
+
+
+def _drive_both(seed, steps=80):
+    rng = np.random.default_rng(seed)
+    P = int(rng.integers(4, 300))
+    budget = int(rng.integers(1, 600))
+    max_seqs = int(rng.integers(1, 20))
+    cap = int(rng.choice([0, 0, 8, 64, 256]))
+    order = rng.permutation(P)
+    return rng, P, budget, max_seqs, cap, order
+
+
+@pytest.mark.parametrize("seed", range(30))
+def test_native_packer_matches_oracle_bit_exactly(mb, seed):
+    rng, P, budget, max_seqs, cap, order = _drive_both(seed)
+    py = Packer(budget, max_seqs, cap, order)
+    s = mb.mb_sched_create(budget, max_seqs, cap, order)
+    try:
+        nid = 0
+        for step in range(80):
+            if rng.random() < 0.45:
+                plen = int(rng.integers(1, 500))
+                comp = int(rng.choice([0, 0, 0, int(rng.integers(0, plen + 40))]))
+                try:
+                    py.add(nid, plen, comp)
+                    ok_py = True
+                except Exception:
+                    ok_py = False
+                try:
+                    mb.mb_sched_add(s, nid, plen, comp)
+                    ok_c = True
+                except mb.MbError as e:
+                    ok_c = False
+                    assert e.status == mb.MB_ENOSPACE
+                assert ok_py == ok_c
+                nid += 1
+            if py.reqs and rng.random() < 0.25:
+                rid = int(rng.choice(sorted(py.reqs)))
+                py.finish(rid)
+                mb.mb_sched_finish(s, rid)
+            rows = py.pack()
+            qo, kv, bti, bt, ids = rows_to_csr(rows)
+            cqo, ckv, cbti, cbt, cids = mb.mb_sched_pack(s)
+            assert list(cqo) == qo
+            assert list(ckv) == kv
+            assert list(cbti) == bti
+            assert list(cbt) == bt
+            assert list(cids) == ids
+            fr, run, par, wait = mb.mb_sched_counts(s)
+            assert (fr, run, par, wait) == (len(py.free), len(py.running), len(py.partial), len(py.waiting))
+    finally:
+        mb.mb_sched_destroy(s)
+
+
+def test_native_packer_worked_example(mb):
+    s = mb.mb_sched_create(576, 1000, 0, np.arange(20000))
+    for i in range(64):
+        mb.mb_sched_add(s, i, 1125, 1125)
+    mb.mb_sched_add(s, 9999, 4096, 0)
+    for it in range(8):
+        qo, kv, bti, bt, ids = mb.mb_sched_pack(s)
+        assert qo[-1] == 576 and len(ids) == 65 and ids[-1] == 9999
+        assert kv[-1] == 512 * (it + 1)
+    qo, kv, bti, bt, ids = mb.mb_sched_pack(s)
+    assert len(ids) == 65 and qo[-1] == 65 and kv[-1] == 4097
+    mb.mb_sched_destroy(s)
+
+
+def test_sched_rejects_bad_config(mb):
+    with pytest.raises(mb.MbError) as e:
+        mb.mb_sched_create(0, 4, 0, np.arange(4))
+    assert e.value.status == mb.MB_EINVAL
+    with pytest.raises(mb.MbError):
+        mb.mb_sched_create(8, 4, 0, [0, 0, 1])   # not a permutation
+    s = mb.mb_sched_create(8, 4, 0, np.arange(2))
+    with pytest.raises(mb.MbError) as e:
+        mb.mb_sched_add(s, 1, 100, 100)          # needs 7 pages
+    assert e.value.status == mb.MB_ENOSPACE
+    mb.mb_sched_add(s, 1, 10, 0)
+    with pytest.raises(mb.MbError):
+        mb.mb_sched_add(s, 1, 10, 0)             # duplicate id
+    with pytest.raises(mb.MbError):
+        mb.mb_sched_finish(s, 77)
+    mb.mb_sched_destroy(s)
+
+
+def _good():
+    b, P = W.make_batch([(30, 1), (0, 70), (5, 11)], seed=5)
+    return b, P
+
+
+def test_batch_validate_accepts_good_and_empty(mb):
+    b, P = _good()
+    mb.mb_batch_validate(mb.Batch.of(b), P, 1000)
+    mb.mb_batch_validate(mb.Batch([0], [], [0], []), P, 1)
+
+
+@pytest.mark.parametrize("bad", ["qo0", "qo_zero", "kv_lt_qo", "short_table", "page_range", "page_dup",
+                                 "too_many_tokens", "neg_page"])
+def test_batch_validate_rejects(mb, bad):
+    b, P = _good()
+    qo, kv, bti, bt = b.qo_indptr.copy(), b.kv_len.copy(), b.bt_indptr.copy(), b.bt.copy()
+    maxT = 1000
+    if bad == "qo0":
+        qo = qo + 1
+    elif bad == "qo_zero":
+        qo[2] = qo[1]
+    elif bad == "kv_lt_qo":
+        kv[1] = 69
+    elif bad == "short_table":
+        bti[2] -= 1
+        bt = np.delete(bt, bti[2])
+        bti[3] -= 1
+    elif bad == "page_range":
+        bt[0] = P
+    elif bad == "page_dup":
+        bt[1] = bt[0]
+    elif bad == "too_many_tokens":
+        maxT = int(qo[-1]) - 1
+    elif bad == "neg_page":
+        bt[3] = -1
+    with pytest.raises(mb.MbError) as e:
+        mb.mb_batch_validate(mb.Batch(qo, kv, bti, bt), P, maxT)
+    assert e.value.status == mb.MB_EINVAL
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks behaviour without a GPU")
+def test_compute_calls_fail_loudly_without_gpu(mb):
+    with pytest.raises(mb.MbError) as e:
+        mb.mb_gemm(16, 16, 16, None, 128, 128, 64, 0)
+    assert e.value.status in (mb.MB_ECUDA, mb.MB_EUNSUPPORTED)
+    sh = W.TINY.as_dict()
+    with pytest.raises(mb.MbError) as e:
+        mb.Layer(sh, {k: 16 for k in ("g_attn", "w_qkv", "w_o", "g_ffn", "w_gate_up", "w_down")}, 64, 8)
+    assert e.value.status in (mb.MB_ECUDA, mb.MB_EUNSUPPORTED)

@@ -1,0 +1,63 @@
+"""GPU parity of the token-batched tcgen05 GEMM (all three epilogues) against
+the oracle's float64 linear layer, over shapes that span several tiles, ragged
+M tails, stream-K splits and the layer shapes of the pages' workloads."""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import layer as OL
+from mixed_prefill_decode_gb300 import workload as W
+from gpu_util import to_dev, from_dev, assert_close, f64
+
+pytestmark = pytest.mark.gpu
+
+SHAPES = [
+    # M, N, K
+    (1, 256, 64), (68, 768, 256), (68, 256, 1024), (129, 640, 512), (200, 1536, 512),
+    (300, 512, 1536), (576, 6144, 4096), (576, 4096, 4096), (16, 7168, 5120), (1040, 5120, 5120),
+    (2216, 512, 128),
+]
+
+
+def _inputs(M, N, K, seed):
+    rng = np.random.default_rng(seed)
+    A = W.f32_to_bf16_bits(rng.standard_normal((M, K), dtype=np.float32))
+    B = W.f32_to_bf16_bits(rng.standard_normal((N, K), dtype=np.float32) * np.float32(0.02))
+    R = W.f32_to_bf16_bits(rng.standard_normal((M, N), dtype=np.float32))
+    return A, B, R
+
+
+@pytest.mark.parametrize("M,N,K", SHAPES)
+@pytest.mark.parametrize("epi", [0, 1])
+def test_gemm_store_and_residual(mb, M, N, K, epi):
+    A, B, R = _inputs(M, N, K, M * 7 + N + K + epi)
+    dA, dB, dR = to_dev(A), to_dev(B), to_dev(R)
+    dD = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    for rep in range(2):   # twice: stream-K tickets must reset themselves
+        dD.fill_(float("nan"))
+        mb.mb_gemm(dA, dB, dD, dR if epi == 1 else None, M, N, K, epi, None, torch.cuda.current_stream().cuda_stream)
+        mb.mb_device_status(None, torch.cuda.current_stream().cuda_stream)
+        ref = OL.linear(f64(A), f64(B)) + (f64(R) if epi == 1 else 0.0)
+        assert_close(f"gemm{epi} {M}x{N}x{K}", f64(from_dev(dD)), ref)
+
+
+@pytest.mark.parametrize("M,F,K", [(68, 1024, 256), (200, 1536, 512), (576, 14336, 4096), (16, 17408, 5120),
+                                   (130, 128, 64)])
+def test_gemm_swiglu(mb, M, F, K):
+    A, B, _ = _inputs(M, 2 * F, K, M + F + K)
+    dA, dB = to_dev(A), to_dev(B)
+    dD = torch.empty((M, F), dtype=torch.bfloat16, device="cuda")
+    dD.fill_(float("nan"))
+    mb.mb_gemm(dA, dB, dD, None, M, F, K, 2, None, torch.cuda.current_stream().cuda_stream)
+    mb.mb_device_status(None, torch.cuda.current_stream().cuda_stream)
+    gu = OL.linear(f64(A), f64(B))
+    ref = OL.silu(gu[:, :F]) * gu[:, F:]
+    assert_close(f"swiglu {M}x{F}x{K}", f64(from_dev(dD)), ref)
+
+
+def test_gemm_rejects_bad_shapes(mb):
+    with pytest.raises(mb.MbError):
+        mb.mb_gemm(16, 16, 16, None, 128, 128, 60, 0)      # K % 64
+    with pytest.raises(mb.MbError):
+        mb.mb_gemm(16, 16, 16, None, 128, 100, 64, 2)      # F % 128
