@@ -1,0 +1,453 @@
+#!/usr/bin/env python
+"""Benchmark of the mixed prefill+decode layer step on GB300.
+
+One step = one mb_step call: the whole hot path (RMSNorm, QKV GEMM, q/k-norm +
+RoPE + KV append, prefill-chunk attention tiles, split-KV decode rows + merge,
+O GEMM + residual, RMSNorm, gate/up GEMM + SwiGLU, down GEMM + residual) over
+one mixed batch.  Default workload: the Llama-3-8B-shaped layer with 64
+decodes at 1,125-token contexts plus one 512-token chunk on a U[0, 4096]
+prefix (T = 576 tokens), synthetic seeded data, random-init weights.
+
+Prints ONE JSON line (rank 0).  ``--impl reference`` times the CPU oracle
+instead (the reference arm: a plain float64 restatement of the method).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl mine|reference]
+                    [--workload llama3_8b_T576|qwen3_14b_P0|qwen3_14b_P1024|qwen3_14b_P2200|tiny_T68]
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from mixed_prefill_decode_gb300 import workload as W  # noqa: E402
+
+METRIC = "mixed prefill+decode step tokens/s; decode-attn HBM GB/s; GEMM TFLOP/s % peak"
+UNIT = "tokens/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 256 << 20
+
+
+def workload_by_name(name: str) -> W.Workload:
+    if name == "llama3_8b_T576":
+        return W.llama3_8b_mixed()
+    if name.startswith("qwen3_14b_P"):
+        return W.qwen3_14b_mixed(int(name.split("P")[1]))
+    if name == "tiny_T68":
+        return W.tiny_mixed()
+    raise SystemExit(f"unknown workload {name}")
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {k: float(d[k]) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained")}, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# --------------------------------------------------------------- accounting
+def algorithmic(shape: W.LayerShape, batch: W.Batch) -> dict:
+    """Per-launch algorithmic work of each kernel (what the method must do)."""
+    T = batch.num_tokens
+    d, hd, F = shape.d_model, shape.head_dim, shape.d_ff
+    Hq, Hkv = shape.n_q_heads, shape.n_kv_heads
+    qo = batch.qo_len()
+    c = batch.cached()
+    dec = qo == 1
+    pairs = float(np.sum(qo[~dec] * c[~dec] + qo[~dec] * (qo[~dec] + 1) / 2))
+    return {
+        "rmsnorm_attn": ("hbm", 2.0 * T * d * 2),
+        "gemm_qkv": ("tensor", 2.0 * T * shape.qkv_dim * d),
+        "rope_append": ("hbm", 2.0 * T * shape.qkv_dim * 2),
+        "attn_chunk": ("tensor", 4.0 * hd * Hq * pairs),
+        "attn_decode": ("hbm", float(np.sum(batch.kv_len[dec])) * Hkv * hd * 2 * 2),
+        "attn_merge": ("hbm", 0.0),
+        "gemm_o": ("tensor", 2.0 * T * d * Hq * hd),
+        "rmsnorm_ffn": ("hbm", 2.0 * T * d * 2),
+        "gemm_gate_up": ("tensor", 2.0 * T * 2 * F * d),
+        "gemm_down": ("tensor", 2.0 * T * d * F),
+    }
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi sampled every 100 ms while running (read-only queries)."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.path = tempfile.mktemp(suffix=".csv")
+        self.proc = None
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        self.t0 = time.time()
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------- distributed
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+        pg = dist
+    return rank, world, local, pg
+
+
+def reduce_max(pg, v: float) -> float:
+    if pg is None:
+        return v
+    import torch
+    t = torch.tensor([v], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(pg):
+    if pg is not None:
+        pg.barrier()
+
+
+# ----------------------------------------------------------- CPU oracle
+def oracle_inputs(wl: W.Workload):
+    from oracle import layer as OL
+    wb, x, batch, pool = W.materialize(wl, unit_gains=True)
+    return OL, OL.weights_to_f64(wb), OL.bf16_bits_to_f64(x), batch, OL.bf16_bits_to_f64(pool)
+
+
+def sub_batch(batch: W.Batch, x: np.ndarray, n_dec: int, n_chunk: int):
+    """First n_dec decode rows and the first n_chunk rows of the chunk (same
+    prefix), as a batch of their own: a bounded sample of the workload."""
+    qo = batch.qo_len()
+    rows, xs = [], []
+    kept_dec = 0
+    for r in range(batch.num_reqs):
+        t0 = batch.qo_indptr[r]
+        table = batch.bt[batch.bt_indptr[r]:batch.bt_indptr[r + 1]]
+        c = int(batch.kv_len[r] - qo[r])
+        if qo[r] == 1 and kept_dec < n_dec:
+            rows.append((1, c + 1, table))
+            xs.append(x[t0:t0 + 1])
+            kept_dec += 1
+        elif qo[r] > 1 and n_chunk > 0:
+            n = min(n_chunk, int(qo[r]))
+            rows.append((n, c + n, table[:W.pages_for(c + n)]))
+            xs.append(x[t0:t0 + n])
+    qo_indptr = np.cumsum([0] + [r[0] for r in rows])
+    kv = np.array([r[1] for r in rows])
+    bti = np.cumsum([0] + [len(r[2]) for r in rows])
+    bt = np.concatenate([r[2] for r in rows])
+    return qo_indptr, kv, bti, bt, np.concatenate(xs)
+
+
+def time_oracle_step(OL, shape, w, pool, qo_indptr, kv, bti, bt, x) -> float:
+    p = pool.copy() if pool.size < (1 << 27) else pool   # appends rewrite the same slots each step
+    t = time.perf_counter()
+    OL.layer_step(shape.as_dict(), w, p, qo_indptr, kv, bti, bt, x)
+    return time.perf_counter() - t
+
+
+def cpu_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def calibrate_sample(OL, wl, w, x, batch, pool, target_s: float):
+    """Pick (n_dec, n_chunk), a fixed fraction of the workload's decode and
+    chunk rows, so that one oracle step takes about target_s."""
+    n_dec_all = int(np.sum(batch.qo_len() == 1))
+    n_chunk_all = int(np.max(batch.qo_len())) if np.any(batch.qo_len() > 1) else 0
+    frac = 1.0 / 64
+    while True:
+        nd = max(1, int(round(n_dec_all * frac)))
+        nc = int(round(n_chunk_all * frac))
+        dt = time_oracle_step(OL, wl.shape, w, pool, *sub_batch(batch, x, nd, nc))
+        if dt >= 0.5 * target_s or frac >= 1.0:
+            return nd, nc
+        frac = min(1.0, frac * min(4.0, max(1.5, target_s / max(dt, 1e-6))))
+
+
+def run_reference(args, rank: int, world: int):
+    if rank != 0:
+        return
+    wl = workload_by_name(args.workload)
+    OL, w, x, batch, pool = oracle_inputs(wl)
+    budget_s = 150.0
+    per_step = budget_s / max(1, args.steps + args.warmup)
+    nd, nc = calibrate_sample(OL, wl, w, x, batch, pool, per_step)
+    sample = sub_batch(batch, x, nd, nc)
+    tokens = int(sample[0][-1])
+    for _ in range(args.warmup):
+        time_oracle_step(OL, wl.shape, w, pool, *sample)
+    times = [time_oracle_step(OL, wl.shape, w, pool, *sample) for _ in range(args.steps)]
+    t = sum(times) / len(times)
+    value = tokens / t
+    desc = (f"each step: oracle layer step over {nd} of the decode rows and the first {nc} rows of the "
+            f"chunk ({tokens} tokens) of workload {wl.name}, float64 NumPy")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+            "config": {"workload": wl.name, "tokens_per_step": tokens, "sample": desc},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle", "sample": desc},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------- GPU arm
+def to_dev(bits, torch):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16).copy()).view(torch.bfloat16).cuda()
+
+
+def run_mine(args, rank: int, world: int, local: int, pg):
+    import torch
+    from mixed_prefill_decode_gb300 import build as B
+    from mixed_prefill_decode_gb300 import binding as mb
+
+    torch.cuda.set_device(local)
+    if rank == 0 or world == 1:
+        B.build()
+    barrier(pg)
+    B.build()
+    peaks, peak_kind = load_peaks()
+    wl = workload_by_name(args.workload)
+    wb, x, batch, pool = W.materialize(wl, unit_gains=True)
+    T = batch.num_tokens
+    dw = {k: to_dev(v, torch) for k, v in wb.items()}
+    dpool = to_dev(pool.reshape(-1), torch)
+    layer = mb.Layer(wl.shape.as_dict(), dw, T, pool.shape[0], kv_buf=dpool)
+    cb = mb.Batch.of(batch)
+    dx = to_dev(x, torch)
+    dy = torch.empty_like(dx)
+    stream = torch.cuda.current_stream()
+    s = stream.cuda_stream
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        layer.step(cb, dx, dy, s)
+    mb.mb_device_status(layer.handle, s)
+    launches_per_step = mb.mb_layer_last_launches(layer.handle)
+
+    # ---- timed region: K steps, L2 flushed between steps, per-step events
+    mb.mb_layer_set_timing(layer.handle, True)
+    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier(pg)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local) if rank == 0 else None
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        ev0[i].record(stream)
+        layer.step(cb, dx, dy, s)
+        ev1[i].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    barrier(pg)
+    clk = clocks.stop() if clocks else None
+    mb.mb_device_status(layer.handle, s)
+    step_ms_local = sum(a.elapsed_time(b) for a, b in zip(ev0, ev1)) / args.steps
+    kern_ms, ksteps = mb.mb_layer_timing(layer.handle)
+    mb.mb_layer_set_timing(layer.handle, False)
+    step_ms = reduce_max(pg, step_ms_local)
+    value = world * T / (step_ms / 1e3)
+
+    # ---- per-kernel rooflines from the live events of the timed region
+    alg = algorithmic(wl.shape, batch)
+    kernels = {}
+    for name, total in kern_ms.items():
+        ms = total / max(1, ksteps)
+        bound, work = alg[name]
+        if ms <= 0 or work <= 0:
+            kernels[name] = {"ms": round(ms, 5)}
+            continue
+        if bound == "tensor":
+            ach = work / (ms / 1e3) / 1e12
+            kernels[name] = {"ms": round(ms, 5), "tflops": round(ach, 1),
+                             "frac_burst": round(ach / peaks["bf16_tflops"], 4),
+                             "frac_sustained": round(ach / peaks["bf16_tflops_sustained"], 4)}
+        else:
+            ach = work / (ms / 1e3) / 1e9
+            kernels[name] = {"ms": round(ms, 5), "gbs": round(ach, 1), "frac": round(ach / peaks["hbm_gbs"], 4)}
+    dom = max(kern_ms, key=lambda k: kern_ms[k])
+    bound, work = alg[dom]
+    dom_ms = kern_ms[dom] / max(1, ksteps)
+    if bound == "tensor":
+        achieved = work / (dom_ms / 1e3) / 1e12
+        roofline = {"kernel": dom, "bound": "tensor", "achieved": round(achieved, 2),
+                    "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                    "frac": round(achieved / peaks["bf16_tflops"], 4), "traffic": None,
+                    "algorithmic_per_launch": work, "peak_kind": f"{peak_kind} bf16 burst"}
+    else:
+        achieved = work / (dom_ms / 1e3) / 1e9
+        roofline = {"kernel": dom, "bound": "hbm", "achieved": round(achieved, 2), "peak": peaks["hbm_gbs"],
+                    "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
+                    "algorithmic_per_launch": work, "peak_kind": f"{peak_kind} HBM copy"}
+    gemm_names = ("gemm_qkv", "gemm_o", "gemm_gate_up", "gemm_down")
+    gemm_flops = sum(alg[n][1] for n in gemm_names)
+    gemm_ms = sum(kern_ms[n] for n in gemm_names) / max(1, ksteps)
+    roof_ms = 0.0
+    for name, (bnd, wk) in alg.items():
+        if bnd == "tensor":
+            roof_ms += wk / (peaks["bf16_tflops"] * 1e12) * 1e3
+        else:
+            roof_ms += wk / (peaks["hbm_gbs"] * 1e9) * 1e3
+    weight_bytes = 2.0 * sum(int(np.prod(v.shape)) for v in wb.values())
+    roof_ms = max(roof_ms, weight_bytes / (peaks["hbm_gbs"] * 1e9) * 1e3)
+
+    # ---- end to end through the public API with host buffers
+    n_e2e = max(1, min(args.steps, 200))
+    xh = torch.from_numpy(x.view(np.int16).copy()).view(torch.bfloat16).pin_memory()
+    yh = torch.empty_like(xh).pin_memory()
+    e0 = [torch.cuda.Event(enable_timing=True) for _ in range(n_e2e)]
+    e1 = [torch.cuda.Event(enable_timing=True) for _ in range(n_e2e)]
+    torch.cuda.synchronize()
+    for i in range(n_e2e):
+        flush.fill_(i & 0xFF)
+        e0[i].record(stream)
+        dx.copy_(xh, non_blocking=True)
+        layer.step(cb, dx, dy, s)
+        yh.copy_(dy, non_blocking=True)
+        e1[i].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = reduce_max(pg, sum(a.elapsed_time(b) for a, b in zip(e0, e1)) / n_e2e)
+    upload = mb.mb_layer_last_upload_bytes(layer.handle)
+
+    # ---- CPU baseline: the oracle on a bounded sample (rank 0, one GPU only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        OL, w64, x64, b2, pool64 = oracle_inputs(wl)
+        nd, nc = calibrate_sample(OL, wl, w64, x64, b2, pool64, 15.0)
+        smp = sub_batch(b2, x64, nd, nc)
+        tok = int(smp[0][-1])
+        dt = time_oracle_step(OL, wl.shape, w64, pool64, *smp)
+        cpu = {"value": tok / dt, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+               "sample": f"one oracle layer step over {nd} decode rows and {nc} chunk rows ({tok} tokens) of "
+                         f"{wl.name}, float64 NumPy, {dt:.1f} s"}
+
+    # ---- P3 step-time model with GB300 peaks, as an analytic comparator
+    from oracle import step_model as SM
+    sh = wl.shape
+    n_params = sum(int(np.prod(v.shape)) for k, v in wb.items() if k.startswith("w_"))
+    gb300 = SM.Machine(flops=peaks["bf16_tflops_sustained"] * 1e12, bandwidth=peaks["hbm_gbs"] * 1e9, t_iter=0.0)
+    model = SM.Model(n_params=n_params, kappa=sh.kv_bytes_per_token, d_model=sh.d_model, n_layers=1)
+    qo = batch.qo_len()
+    c = batch.cached()
+    chunks = [(int(qo[r]), int(c[r])) for r in range(batch.num_reqs) if qo[r] > 1]
+    decs = [int(c[r]) for r in range(batch.num_reqs) if qo[r] == 1]
+    model_ms = SM.iteration_time(gb300, model, chunks, decs) * 1e3
+
+    layer.close()
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(step_ms, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) embeddings and KV prefix, "
+                                                      "N(0,0.02) random-init weights)",
+        "config": {"workload": wl.name, "tokens_per_step": T, "requests": batch.num_reqs,
+                   "decodes": int(np.sum(batch.qo_len() == 1)),
+                   "chunk_rows": int(np.sum(batch.qo_len()[batch.qo_len() > 1])),
+                   "chunk_prefix": [int(v) for v in batch.cached()[batch.qo_len() > 1]],
+                   "parallelism": f"replicas{world}" if world > 1 else "single GPU",
+                   "l2": "flushed between timed steps (256 MiB write); step time = per-step CUDA events",
+                   "wall_s_timed_region": round(wall, 4)},
+        "roofline": roofline,
+        "kernels": kernels,
+        "gemm": {"tflops": round(gemm_flops / (gemm_ms / 1e3) / 1e12, 1),
+                 "frac_burst": round(gemm_flops / (gemm_ms / 1e3) / 1e12 / peaks["bf16_tflops"], 4),
+                 "frac_sustained": round(gemm_flops / (gemm_ms / 1e3) / 1e12 / peaks["bf16_tflops_sustained"], 4)},
+        "decode_attn": kernels.get("attn_decode"),
+        "roofline_step_ms": round(roof_ms, 5),
+        "step_model_ms": round(model_ms, 5),
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(world * T / (e2e_ms / 1e3), 1), "unit": UNIT,
+                "h2d_bytes_per_step": int(x.nbytes + upload), "d2h_bytes_per_step": int(x.nbytes),
+                "ms_per_step": round(e2e_ms, 5)},
+        "gpu_launches": int(launches_per_step * args.steps),
+        "clocks": clk,
+        "peaks": {"kind": peak_kind, **peaks},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["mine", "reference"], default="mine")
+    ap.add_argument("--workload", default="llama3_8b_T576")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+    rank, world, local, pg = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_mine(args, rank, world, local, pg)
+    if pg is not None:
+        pg.barrier()
+        pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

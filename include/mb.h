@@ -158,14 +158,17 @@ mb_status mb_layer_buffer(const mb_layer *layer, int32_t which, void **ptr, int6
 
 /* Per-kernel timing of subsequent steps (CUDA events on the step's stream).
  * mb_layer_timing returns the accumulated milliseconds of each launch kind
- * since enable, in the order: rmsnorm_attn, gemm_qkv, rope_append, attention,
- * attn_merge, gemm_o, rmsnorm_ffn, gemm_gate_up, gemm_down (n <= 9), and the
- * number of steps timed.  It synchronises the stream of the last step. */
+ * since enable, in the order: rmsnorm_attn, gemm_qkv, rope_append,
+ * attn_chunk, attn_decode, attn_merge, gemm_o, rmsnorm_ffn, gemm_gate_up,
+ * gemm_down (n <= 10), and the number of steps timed.  It synchronises on the
+ * recorded events. */
 mb_status mb_layer_set_timing(mb_layer *layer, int32_t enable);
 mb_status mb_layer_timing(mb_layer *layer, double *ms, int32_t n, int64_t *steps);
 
-/* Number of kernel launches the last mb_step issued. */
+/* Number of kernel launches the last mb_step issued, and the bytes it copied
+ * host to device (the descriptor and its work lists). */
 int32_t mb_layer_last_launches(const mb_layer *layer);
+int64_t mb_layer_last_upload_bytes(const mb_layer *layer);
 
 /* Standalone token-batched GEMM D = A B^T on the tcgen05 tensor cores (the
  * linear layers of the step; ConfluxServe summary, "Why can linear layers be

@@ -22,7 +22,7 @@ from . import build as _build
 MB_OK, MB_EINVAL, MB_ENOMEM, MB_ENOSPACE, MB_ECUDA, MB_EUNSUPPORTED, MB_EDEVICE = 0, -1, -2, -3, -4, -5, -6
 STATUS_NAMES = {0: "MB_OK", -1: "MB_EINVAL", -2: "MB_ENOMEM", -3: "MB_ENOSPACE", -4: "MB_ECUDA",
                 -5: "MB_EUNSUPPORTED", -6: "MB_EDEVICE"}
-TIMED_KERNELS = ("rmsnorm_attn", "gemm_qkv", "rope_append", "attention", "attn_merge", "gemm_o",
+TIMED_KERNELS = ("rmsnorm_attn", "gemm_qkv", "rope_append", "attn_chunk", "attn_decode", "attn_merge", "gemm_o",
                  "rmsnorm_ffn", "gemm_gate_up", "gemm_down")
 BUF_XN, BUF_QKV, BUF_Q, BUF_O, BUF_H, BUF_HN, BUF_A = range(7)
 
@@ -78,6 +78,7 @@ _SIGS = {
     "mb_layer_set_timing": (_I32, [_VP, _I32]),
     "mb_layer_timing": (_I32, [_VP, ctypes.POINTER(ctypes.c_double), _I32, c_int64_p]),
     "mb_layer_last_launches": (_I32, [_VP]),
+    "mb_layer_last_upload_bytes": (_I64, [_VP]),
     "mb_gemm": (_I32, [_VP, _VP, _VP, _VP, _I32, _I32, _I32, _I32, _VP, _VP]),
     "mb_gemm_workspace_bytes": (_I64, []),
     "mb_sched_create": (_I32, [ctypes.POINTER(mb_pack_cfg), _I32, c_int32_p, ctypes.POINTER(_VP)]),
@@ -215,6 +216,10 @@ def mb_layer_timing(layer: int):
 
 def mb_layer_last_launches(layer: int) -> int:
     return int(lib().mb_layer_last_launches(layer))
+
+
+def mb_layer_last_upload_bytes(layer: int) -> int:
+    return int(lib().mb_layer_last_upload_bytes(layer))
 
 
 def mb_gemm(A, B, D, R, M: int, N: int, K: int, epilogue: int, workspace=None, stream=None) -> None:

@@ -140,7 +140,7 @@ using mb::fail;
 // ===================================================================== layer
 namespace {
 
-constexpr int kNumTimed = 9;
+constexpr int kNumTimed = 10;
 constexpr int kRing = 4;
 
 struct EventSet {
@@ -189,6 +189,7 @@ struct mb_layer {
   // last step
   int32_t last_T = 0;
   int32_t last_launches = 0;
+  int64_t last_upload = 0;
   // timing
   bool timing = false;
   std::vector<EventSet> ev_pool;
@@ -476,6 +477,8 @@ mb_status mb_layer_timing(mb_layer *L, double *ms, int32_t n, int64_t *steps) {
 
 int32_t mb_layer_last_launches(const mb_layer *L) { return L ? L->last_launches : 0; }
 
+int64_t mb_layer_last_upload_bytes(const mb_layer *L) { return L ? L->last_upload : 0; }
+
 mb_status mb_device_status(mb_layer *L, void *stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaStreamSynchronize(s);
@@ -679,7 +682,7 @@ mb_status mb_step(mb_layer *L, mb_kv *kv, const mb_batch *b, const void *x_in, v
   // ---- timing events
   EventSet *es = nullptr;
   if (L->timing) {
-    if (L->ev_used == 64) {
+    if (L->ev_used == 4096) {
       st = flush_timing(L);
       if (st != MB_OK) return st;
     }
@@ -757,9 +760,12 @@ mb_status mb_step(mb_layer *L, mb_kv *kv, const mb_batch *b, const void *x_in, v
   aa.err = L->err;
   aa.tm_q = &tm_q;
   aa.tm_kv = &kv->tmap;
-  if ((st = chk(mb::attention_run(aa, s), "attention")) != MB_OK) return st;
-  launches += (aa.n_tiles > 0) + (aa.n_items > 0);
+  if ((st = chk(mb::attn_chunk_run(aa, s), "chunk attention")) != MB_OK) return st;
+  launches += aa.n_tiles > 0;
   mark(4);
+  if ((st = chk(mb::attn_decode_run(aa, s), "decode attention")) != MB_OK) return st;
+  launches += aa.n_items > 0;
+  mark(5);
   mb::MergeArgs ma;
   ma.part = L->part;
   ma.merge_list = db + o_merge;
@@ -771,27 +777,28 @@ mb_status mb_step(mb_layer *L, mb_kv *kv, const mb_batch *b, const void *x_in, v
   ma.hd = hd;
   if ((st = chk(mb::attn_merge_run(ma, s), "merge")) != MB_OK) return st;
   launches += n_merge > 0;
-  mark(5);
+  mark(6);
   if ((st = chk(mb::gemm_run(L->o, L->w.w_o, &L->tm_wo, L->h, x_in, Ti, d.d_model, hqd, mb::kEpiResidual, L->gws,
                              L->err, s), "gemm o")) != MB_OK)
     return st;
   ++launches;
-  mark(6);
+  mark(7);
   if ((st = chk(mb::rmsnorm_run(L->h, L->w.g_ffn, L->hn, Ti, d.d_model, d.rms_eps, s), "rmsnorm ffn")) != MB_OK) return st;
   ++launches;
-  mark(7);
+  mark(8);
   if ((st = chk(mb::gemm_run(L->hn, L->w.w_gate_up, &L->tm_wgu, L->a, nullptr, Ti, d.d_ff, d.d_model, mb::kEpiSwiGLU,
                              L->gws, L->err, s), "gemm gate/up")) != MB_OK)
     return st;
   ++launches;
-  mark(8);
+  mark(9);
   if ((st = chk(mb::gemm_run(L->a, L->w.w_down, &L->tm_wd, x_out, L->h, Ti, d.d_model, d.d_ff, mb::kEpiResidual, L->gws,
                              L->err, s), "gemm down")) != MB_OK)
     return st;
   ++launches;
-  mark(9);
+  mark(10);
   L->last_T = static_cast<int32_t>(T);
   L->last_launches = launches;
+  L->last_upload = static_cast<int64_t>(hb.size()) * 4;
   L->last_stream = s;
   return MB_OK;
 }

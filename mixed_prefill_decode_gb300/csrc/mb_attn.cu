@@ -571,47 +571,44 @@ cudaError_t launch_chunk(const CUtensorMap &tq, const CUtensorMap &tkv, const Ch
 
 }  // namespace
 
-cudaError_t attention_run(const AttnArgs &a, cudaStream_t st) {
-  const float scale_log2 = kLog2e / sqrtf(static_cast<float>(a.hd));
+cudaError_t attn_chunk_run(const AttnArgs &a, cudaStream_t st) {
+  if (a.n_tiles <= 0) return cudaSuccess;
+  ChunkParams cp;
+  cp.o = static_cast<__nv_bfloat16 *>(a.o);
+  cp.qo_indptr = a.qo_indptr;
+  cp.kv_len = a.kv_len;
+  cp.bt_indptr = a.bt_indptr;
+  cp.bt = a.bt;
+  cp.tiles = a.tiles;
+  cp.Hq = a.Hq;
+  cp.Hkv = a.Hkv;
+  cp.num_pages = a.num_pages;
+  cp.scale_log2 = kLog2e / sqrtf(static_cast<float>(a.hd));
+  cp.err = a.err;
+  return a.hd == 128 ? launch_chunk<128>(*a.tm_q, *a.tm_kv, cp, a.n_tiles, st)
+                     : launch_chunk<64>(*a.tm_q, *a.tm_kv, cp, a.n_tiles, st);
+}
+
+cudaError_t attn_decode_run(const AttnArgs &a, cudaStream_t st) {
+  if (a.n_items <= 0) return cudaSuccess;
+  DecodeParams dp;
+  dp.q = static_cast<const __nv_bfloat16 *>(a.q);
+  dp.pool = static_cast<const __nv_bfloat16 *>(a.pool);
+  dp.o = static_cast<__nv_bfloat16 *>(a.o);
+  dp.part = a.part;
+  dp.qo_indptr = a.qo_indptr;
+  dp.kv_len = a.kv_len;
+  dp.bt_indptr = a.bt_indptr;
+  dp.bt = a.bt;
+  dp.items = a.items;
+  dp.n_items = a.n_items;
+  dp.Hq = a.Hq;
+  dp.Hkv = a.Hkv;
+  dp.num_pages = a.num_pages;
+  dp.scale_log2 = kLog2e / sqrtf(static_cast<float>(a.hd));
+  dp.err = a.err;
   const int G = a.Hq / a.Hkv;
-  cudaError_t e = cudaSuccess;
-  if (a.n_tiles > 0) {
-    ChunkParams cp;
-    cp.o = static_cast<__nv_bfloat16 *>(a.o);
-    cp.qo_indptr = a.qo_indptr;
-    cp.kv_len = a.kv_len;
-    cp.bt_indptr = a.bt_indptr;
-    cp.bt = a.bt;
-    cp.tiles = a.tiles;
-    cp.Hq = a.Hq;
-    cp.Hkv = a.Hkv;
-    cp.num_pages = a.num_pages;
-    cp.scale_log2 = scale_log2;
-    cp.err = a.err;
-    e = a.hd == 128 ? launch_chunk<128>(*a.tm_q, *a.tm_kv, cp, a.n_tiles, st)
-                    : launch_chunk<64>(*a.tm_q, *a.tm_kv, cp, a.n_tiles, st);
-    if (e != cudaSuccess) return e;
-  }
-  if (a.n_items > 0) {
-    DecodeParams dp;
-    dp.q = static_cast<const __nv_bfloat16 *>(a.q);
-    dp.pool = static_cast<const __nv_bfloat16 *>(a.pool);
-    dp.o = static_cast<__nv_bfloat16 *>(a.o);
-    dp.part = a.part;
-    dp.qo_indptr = a.qo_indptr;
-    dp.kv_len = a.kv_len;
-    dp.bt_indptr = a.bt_indptr;
-    dp.bt = a.bt;
-    dp.items = a.items;
-    dp.n_items = a.n_items;
-    dp.Hq = a.Hq;
-    dp.Hkv = a.Hkv;
-    dp.num_pages = a.num_pages;
-    dp.scale_log2 = scale_log2;
-    dp.err = a.err;
-    e = a.hd == 128 ? launch_decode_g<128>(dp, G, st) : launch_decode_g<64>(dp, G, st);
-  }
-  return e;
+  return a.hd == 128 ? launch_decode_g<128>(dp, G, st) : launch_decode_g<64>(dp, G, st);
 }
 
 cudaError_t attn_merge_run(const MergeArgs &m, cudaStream_t st) {
