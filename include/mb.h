@@ -186,6 +186,24 @@ mb_status mb_gemm(const void *A, const void *B, void *D, const void *R, int32_t 
                   int32_t K, int32_t epilogue, void *workspace, void *stream);
 int64_t mb_gemm_workspace_bytes(void);
 
+/* The same GEMM for callers that cannot allocate device memory (code inside
+ * an allocator's own hooks or out-of-memory path, processes whose device
+ * memory is all handed out in advance, plugins limited to the buffers their
+ * host passes in).  The pages have no counterpart: this is a deployment
+ * convenience, not part of the method.  Arguments, layouts and epilogues are
+ * those of mb_gemm; there is no workspace argument.  It calls no cudaMalloc,
+ * cudaFree or allocating library routine: its scratch (stream-K partial
+ * tiles, tile tickets, error word) is a file-scope device array of
+ * 16 MiB + 4 KiB that every GPU loading the library holds until exit.  The
+ * first call on a device looks the array's address up (once per device, with
+ * that device current); make that first call before any stream capture.
+ * Every call shares the array and clears its tickets on `stream` first, so
+ * calls that overlap on the GPU (unordered streams) race.  Shapes whose split
+ * would need more scratch than the array holds are rejected with
+ * MB_EUNSUPPORTED and a message giving both sizes.  Errors: as mb_gemm. */
+mb_status mb_gemm_noalloc(const void *A, const void *B, void *D, const void *R, int32_t M, int32_t N,
+                          int32_t K, int32_t epilogue, void *stream);
+
 /* ---------------- scheduler side (host only, no device work) ---------------
  * The token-budget packer of the pofe.ai "Chunked prefill" page, "How it works,
  * step by step" (steps 1-3) and its schedule() sketch: every step takes one

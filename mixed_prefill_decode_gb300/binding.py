@@ -81,6 +81,7 @@ _SIGS = {
     "mb_layer_last_upload_bytes": (_I64, [_VP]),
     "mb_gemm": (_I32, [_VP, _VP, _VP, _VP, _I32, _I32, _I32, _I32, _VP, _VP]),
     "mb_gemm_workspace_bytes": (_I64, []),
+    "mb_gemm_noalloc": (_I32, [_VP, _VP, _VP, _VP, _I32, _I32, _I32, _I32, _VP]),
     "mb_sched_create": (_I32, [ctypes.POINTER(mb_pack_cfg), _I32, c_int32_p, ctypes.POINTER(_VP)]),
     "mb_sched_add": (_I32, [_VP, _I64, _I32, _I32]),
     "mb_sched_pack": (_I32, [_VP, ctypes.POINTER(mb_sched_batch)]),
@@ -224,6 +225,10 @@ def mb_layer_last_upload_bytes(layer: int) -> int:
 
 def mb_gemm(A, B, D, R, M: int, N: int, K: int, epilogue: int, workspace=None, stream=None) -> None:
     _check(lib().mb_gemm(_ptr(A), _ptr(B), _ptr(D), _ptr(R), M, N, K, epilogue, _ptr(workspace), _ptr(stream)))
+
+
+def mb_gemm_noalloc(A, B, D, R, M: int, N: int, K: int, epilogue: int, stream=None) -> None:
+    _check(lib().mb_gemm_noalloc(_ptr(A), _ptr(B), _ptr(D), _ptr(R), M, N, K, epilogue, _ptr(stream)))
 
 
 def mb_gemm_workspace_bytes() -> int:

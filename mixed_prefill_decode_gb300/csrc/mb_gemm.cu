@@ -32,6 +32,8 @@
 #include <cstdio>
 #include <mutex>
 
+#include "mb.h"
+#include "mb_internal.h"
 #include "mb_kernels.h"
 #include "mb_ptx.cuh"
 
@@ -491,3 +493,135 @@ cudaError_t gemm_run(const void *A, const void *B, const CUtensorMap *tmB_pre, v
 }
 
 }  // namespace mb
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant of the GEMM entry point.
+//
+// Some callers cannot call cudaMalloc: code running under an allocator that
+// must not be re-entered (a memory pool's own hooks, an out-of-memory
+// handler), processes whose device memory is fully handed out up front, or
+// plugins that may only touch buffers their host gives them.  For them,
+// mb_gemm_noalloc keeps the stream-K scratch (fp32 partial tiles, tile tickets
+// and the error word) in the file-scope device array below instead of a
+// cudaMalloc'ed workspace.  Every GPU that loads this library holds the array
+// (16 MiB + 4 KiB) until the process exits.  All calls on a device share it:
+// calls that overlap on the GPU (different streams without ordering) race.
+// The tickets are cleared on the call's stream before every launch; the
+// partial tiles need no clearing (every slot is written before it is read).
+// The stream-K part runs on at most kNoAllocGrid CTAs so that its partial
+// tiles fit; problems with at least one tile per SM run without any split.
+
+static __device__ __align__(256) uint8_t g_gemm_noalloc_scratch[(2u * 64u * 128u * 256u * 4u) + 4096u];
+
+namespace mb {
+namespace {
+
+constexpr int kNoAllocGrid = 64;
+constexpr size_t kNoAllocPartialBytes = static_cast<size_t>(2 * kNoAllocGrid) * BM * BN * sizeof(float);
+constexpr size_t kNoAllocTailBytes = 4096;  // tickets, then the error word in the last 16 bytes
+static_assert(sizeof(g_gemm_noalloc_scratch) == kNoAllocPartialBytes + kNoAllocTailBytes, "scratch layout");
+
+std::mutex g_noalloc_mu;
+void *g_noalloc_addr[64] = {};
+
+// Device address of the scratch array on the current device, looked up once
+// per device (host code only has a stand-in for the symbol).
+cudaError_t noalloc_scratch(void **out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (!g_noalloc_addr[dev]) {
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_gemm_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    g_noalloc_addr[dev] = p;
+  }
+  *out = g_noalloc_addr[dev];
+  return cudaSuccess;
+}
+
+}  // namespace
+}  // namespace mb
+
+extern "C" mb_status mb_gemm_noalloc(const void *A, const void *B, void *D, const void *R, int32_t M, int32_t N,
+                                     int32_t K, int32_t epilogue, void *stream) {
+  using namespace mb;
+  if (!A || !B || !D || M < 0 || N <= 0 || K <= 0) return fail(MB_EINVAL, "mb_gemm_noalloc: bad argument");
+  if (epilogue < 0 || epilogue > 2) return fail(MB_EINVAL, "mb_gemm_noalloc: epilogue must be 0, 1 or 2");
+  if (epilogue == 1 && (!R || R == D)) return fail(MB_EINVAL, "mb_gemm_noalloc: residual epilogue needs R != D");
+  if (K % 64) return fail(MB_EUNSUPPORTED, "mb_gemm_noalloc: K must be a multiple of 64");
+  if (epilogue == 2 && N % 128) return fail(MB_EUNSUPPORTED, "mb_gemm_noalloc: SwiGLU needs F = N %% 128 == 0");
+  if (N % 32) return fail(MB_EUNSUPPORTED, "mb_gemm_noalloc: N must be a multiple of 32");
+  for (const void *p : {A, B, static_cast<const void *>(D), R})
+    if (p && reinterpret_cast<uintptr_t>(p) % 16)
+      return fail(MB_EINVAL, "mb_gemm_noalloc: pointers must be 16-byte aligned");
+  if (M == 0) return MB_OK;
+  int dev = 0, sms = 0, major = 0, minor = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  if (e != cudaSuccess) return fail(MB_ECUDA, "mb_gemm_noalloc: %s", cudaGetErrorString(e));
+  if (major != 10 || (minor != 3 && minor != 0))
+    return fail(MB_EUNSUPPORTED, "mb_gemm_noalloc: device is sm_%d%d; these kernels are built for sm_103a", major,
+                minor);
+
+  Params p{};
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.k_iters = K / BK;
+  p.tiles_m = (M + BM - 1) / BM;
+  const int tiles_n = epilogue == kEpiSwiGLU ? N / 128 : (N + BN - 1) / BN;
+  const long long tiles = static_cast<long long>(p.tiles_m) * tiles_n;
+  if (tiles >= sms) {
+    p.dp_tiles = static_cast<int>(tiles);
+    p.sk_tiles = 0;
+    p.grid = sms;
+  } else {
+    p.dp_tiles = 0;
+    p.sk_tiles = static_cast<int>(tiles);
+    const long long sk_iters = tiles * p.k_iters;
+    long long g = kNoAllocGrid;
+    if (sk_iters < 2LL * g) g = sk_iters / 2 > 0 ? sk_iters / 2 : 1;
+    p.grid = static_cast<int>(g);
+  }
+  const size_t need_partials = p.sk_tiles ? static_cast<size_t>(2 * p.grid) * BM * BN * sizeof(float) : 0;
+  const size_t need_tickets = static_cast<size_t>(p.sk_tiles) * sizeof(int);
+  if (need_partials > kNoAllocPartialBytes || need_tickets > kNoAllocTailBytes - 16)
+    return fail(MB_EUNSUPPORTED,
+                "mb_gemm_noalloc: this shape needs %zu bytes of partial tiles and %zu of tickets; the static "
+                "scratch holds %zu and %zu",
+                need_partials, need_tickets, kNoAllocPartialBytes, kNoAllocTailBytes - 16);
+
+  void *scratch = nullptr;
+  e = noalloc_scratch(&scratch);
+  if (e != cudaSuccess) return fail(MB_ECUDA, "mb_gemm_noalloc: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+  uint8_t *base = static_cast<uint8_t *>(scratch);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  e = cudaMemsetAsync(base + kNoAllocPartialBytes, 0, kNoAllocTailBytes, st);
+  if (e != cudaSuccess) return fail(MB_ECUDA, "mb_gemm_noalloc: cudaMemsetAsync: %s", cudaGetErrorString(e));
+
+  const int b_rows = epilogue == kEpiSwiGLU ? 2 * N : N;
+  CUtensorMap tmA, tmB;
+  e = encode_tmap_2d(&tmA, A, K, M, static_cast<uint64_t>(K) * 2, BK, BM);
+  if (e == cudaSuccess) e = encode_tmap_2d(&tmB, B, K, b_rows, static_cast<uint64_t>(K) * 2, BK, 128);
+  if (e != cudaSuccess) return fail(MB_ECUDA, "mb_gemm_noalloc: tensor map encoding failed");
+  p.D = static_cast<__nv_bfloat16 *>(D);
+  p.ldd = N;
+  p.R = static_cast<const __nv_bfloat16 *>(R);
+  p.ldr = N;
+  p.F = epilogue == kEpiSwiGLU ? N : 0;
+  p.partials = reinterpret_cast<float *>(base);
+  p.tickets = reinterpret_cast<int *>(base + kNoAllocPartialBytes);
+  p.err = reinterpret_cast<int *>(base + kNoAllocPartialBytes + kNoAllocTailBytes - 16);
+  switch (epilogue) {
+    case kEpiStore: e = launch<kEpiStore>(tmA, tmB, p, st); break;
+    case kEpiResidual: e = launch<kEpiResidual>(tmA, tmB, p, st); break;
+    default: e = launch<kEpiSwiGLU>(tmA, tmB, p, st); break;
+  }
+  if (e != cudaSuccess) return fail(MB_ECUDA, "mb_gemm_noalloc: launch: %s", cudaGetErrorString(e));
+  return MB_OK;
+}
