@@ -601,21 +601,22 @@ mb_status mb_step(mb_layer *L, mb_kv *kv, const mb_batch *b, const void *x_in, v
     hb[o_tiles + 4 * i + 1] = tiles[i].i0;
     hb[o_tiles + 4 * i + 2] = tiles[i].h;
   }
-  // decode splits: enough warps to keep every SM streaming K/V
-  const int64_t target_items = static_cast<int64_t>(ctx->sms) * 32;
+  // decode splits: about four CTAs per SM in total (two resident per SM),
+  // each request's pages divided evenly among its splits
+  const int64_t target_items = static_cast<int64_t>(ctx->sms) * 4;
   int64_t pps = (dec_pages * Hkv + target_items - 1) / std::max<int64_t>(1, target_items);
-  pps = std::max<int64_t>(pps, 4);
+  pps = std::max<int64_t>(pps, 8);
   std::vector<int32_t> items, merges;
   for (int r = 0; r < n; ++r) {
     const int32_t qo = b->qo_indptr[r + 1] - b->qo_indptr[r];
     if (qo != 1) continue;
     const int32_t np = pages_for(b->kv_len[r]);
-    const int32_t ns = static_cast<int32_t>((np + pps - 1) / pps);
+    const int32_t ns = static_cast<int32_t>(std::max<int64_t>(1, (np + pps / 2) / pps));
     for (int32_t hk = 0; hk < Hkv; ++hk) {
       const int32_t first = static_cast<int32_t>(items.size() / 8);
       for (int32_t sidx = 0; sidx < ns; ++sidx) {
-        const int32_t pb = static_cast<int32_t>(sidx * pps);
-        const int32_t pe = static_cast<int32_t>(std::min<int64_t>(np, (sidx + 1) * pps));
+        const int32_t pb = static_cast<int32_t>(static_cast<int64_t>(np) * sidx / ns);
+        const int32_t pe = static_cast<int32_t>(static_cast<int64_t>(np) * (sidx + 1) / ns);
         items.insert(items.end(), {r, hk, pb, pe, sidx, ns, 0, 0});
       }
       if (ns > 1) merges.insert(merges.end(), {r, hk, first, ns});

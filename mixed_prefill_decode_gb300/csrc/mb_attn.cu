@@ -352,149 +352,263 @@ struct DecodeParams {
   int *err;
 };
 
-__device__ __forceinline__ uint4 ldg_nc_v4(const void *ptr) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(ptr));
-  return v;
+// One CTA per work item {request, KV head, page range}.  Warp 4 streams the
+// K and V blocks of each (page, head) -- contiguous 16 x hd bf16 in the HND
+// pool -- into a ring of shared-memory slots with bulk copies; warps 0-3 take
+// every fourth page.  A warp serves all G q-heads of the GQA group: HD/8
+// lanes share a key (8 bf16 = one 16-byte shared load each), scores are
+// reduced across those lanes with a transposed butterfly (each lane ends with
+// the score of one key), and each key costs one exp2 per head.  The warps'
+// (m, l, o) are merged in shared memory at the end.
+template <int HD>
+struct DecCfg {
+  static constexpr int NW = 4;                  // consumer warps
+  static constexpr int THREADS = (NW + 1) * 32;
+  static constexpr int NSLOT = 8;
+  static constexpr int PAGE_BYTES = 16 * HD * 2;
+  static constexpr int SLOT_BYTES = 2 * PAGE_BYTES;
+  static constexpr int LPK = HD / 8;            // lanes per key
+  static constexpr int KPS = 32 / LPK;          // keys per step
+  static constexpr int STEPS = 16 / KPS;
+  static constexpr int RING = NSLOT * SLOT_BYTES;
+};
+
+template <int HD, int G>
+constexpr int dec_smem() {
+  // ring + barriers; the final merge reuses the ring
+  return DecCfg<HD>::RING + 256;
 }
 
-// One warp per work item.  HD / 8 lanes share one key (8 bf16 each), so a
-// warp covers KPS keys per 16-byte load instruction.
+__device__ __forceinline__ uint4 lds128(const uint8_t *p) { return *reinterpret_cast<const uint4 *>(p); }
+
+__device__ __forceinline__ float2 bf2(uint32_t w) { return make_float2(bf16lo(w), bf16hi(w)); }
+
 template <int HD, int G>
-__global__ void __launch_bounds__(128) decode_attn_kernel(const DecodeParams p) {
-  constexpr int LPK = HD / 8;
-  constexpr int KPS = 32 / LPK;
-  constexpr int STEPS = 16 / KPS;
-  const int warp_global = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  if (warp_global >= p.n_items) return;
-  const int lane = threadIdx.x & 31;
-  const int32_t *it = p.items + warp_global * 8;
+__global__ void __launch_bounds__(DecCfg<HD>::THREADS, 2) decode_attn_kernel(const DecodeParams p) {
+  using C = DecCfg<HD>;
+  extern __shared__ __align__(128) uint8_t dsm[];
+  uint8_t *ring = dsm;
+  uint64_t *full = reinterpret_cast<uint64_t *>(dsm + C::RING);
+  uint64_t *empty = full + C::NSLOT;
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(empty + C::NSLOT);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int32_t *it = p.items + blockIdx.x * 8;
   const int req = it[0], hk = it[1], pb = it[2], pe = it[3], n_splits = it[5];
+  const int np = pe - pb;
   const int t = p.qo_indptr[req];
   const int kv = p.kv_len[req];
   const int32_t *table = p.bt + p.bt_indptr[req];
-  const int sub = lane % LPK;   // which 8-element slice of hd
-  const int kk = lane / LPK;    // which key of a step
-  const int d0 = sub * 8;
 
-  float qf[G][8];
-#pragma unroll
-  for (int g = 0; g < G; ++g) {
-    const uint4 raw = *reinterpret_cast<const uint4 *>(p.q + (static_cast<size_t>(t) * p.Hq + hk * G + g) * HD + d0);
-    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      qf[g][2 * e] = bf16lo(w[e]) * p.scale_log2;
-      qf[g][2 * e + 1] = bf16hi(w[e]) * p.scale_log2;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::NSLOT; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
     }
+    *abort_flag = 0;
+    fence_mbar_init();
   }
-  float m[G], l[G], acc[G][8];
-#pragma unroll
-  for (int g = 0; g < G; ++g) {
-    m[g] = -INFINITY;
-    l[g] = 0.f;
-#pragma unroll
-    for (int e = 0; e < 8; ++e) acc[g][e] = 0.f;
-  }
-  const size_t head_stride = static_cast<size_t>(16) * HD;
-  for (int pg = pb; pg < pe; ++pg) {
-    int page = table[pg];
-    if (page < 0 || page >= p.num_pages) {
-      atomicExch(p.err, kErrBounds);
-      page = 0;
-    }
-    const __nv_bfloat16 *kb = p.pool + ((static_cast<size_t>(page) * 2 + 0) * p.Hkv + hk) * head_stride;
-    const __nv_bfloat16 *vb = kb + static_cast<size_t>(p.Hkv) * head_stride;
-    uint4 kr[STEPS], vr[STEPS];
-#pragma unroll
-    for (int st = 0; st < STEPS; ++st) {
-      const int slot = st * KPS + kk;
-      kr[st] = ldg_nc_v4(kb + slot * HD + d0);
-      vr[st] = ldg_nc_v4(vb + slot * HD + d0);
-    }
-    float s[STEPS][G];
-#pragma unroll
-    for (int st = 0; st < STEPS; ++st) {
-      const uint32_t w[4] = {kr[st].x, kr[st].y, kr[st].z, kr[st].w};
-      float kf[8];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        kf[2 * e] = bf16lo(w[e]);
-        kf[2 * e + 1] = bf16hi(w[e]);
+  __syncthreads();
+
+  if (warp == C::NW) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const size_t head_stride = static_cast<size_t>(16) * HD;
+      int last_slot_issued = -1;
+      for (int i = 0; i < np; ++i) {
+        const int slot = i % C::NSLOT;
+        if (i >= C::NSLOT &&
+            !mbar_wait(&empty[slot], ((i / C::NSLOT) - 1) & 1, abort_flag, p.err, kErrWaitProducer))
+          break;
+        int page = table[pb + i];
+        if (page < 0 || page >= p.num_pages) {
+          atomicExch(p.err, kErrBounds);
+          page = 0;
+        }
+        const __nv_bfloat16 *kb = p.pool + ((static_cast<size_t>(page) * 2 + 0) * p.Hkv + hk) * head_stride;
+        const __nv_bfloat16 *vb = kb + static_cast<size_t>(p.Hkv) * head_stride;
+        mbar_arrive_expect_tx(&full[slot], 2 * C::PAGE_BYTES);
+        bulk_load(ring + slot * C::SLOT_BYTES, kb, C::PAGE_BYTES, &full[slot]);
+        bulk_load(ring + slot * C::SLOT_BYTES + C::PAGE_BYTES, vb, C::PAGE_BYTES, &full[slot]);
+        last_slot_issued = i;
       }
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        float a = 0.f;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) a = fmaf(qf[g][e], kf[e], a);
-#pragma unroll
-        for (int off = 1; off < LPK; off <<= 1) a += __shfl_xor_sync(0xffffffffu, a, off);
-        s[st][g] = a;
-      }
-      const int key = pg * 16 + st * KPS + kk;
-      if (key >= kv) {
-#pragma unroll
-        for (int g = 0; g < G; ++g) s[st][g] = -INFINITY;
-        vr[st] = make_uint4(0, 0, 0, 0);
-      }
-    }
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      float pm = -INFINITY;
-#pragma unroll
-      for (int st = 0; st < STEPS; ++st) pm = fmaxf(pm, s[st][g]);
-#pragma unroll
-      for (int off = LPK; off < 32; off <<= 1) pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, off));
-      const float m_new = fmaxf(m[g], pm);
-      const float alpha = (m[g] == -INFINITY) ? 0.f : exp2f(m[g] - m_new);
-      l[g] *= alpha;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) acc[g][e] *= alpha;
-#pragma unroll
-      for (int st = 0; st < STEPS; ++st) {
-        const float pr = (s[st][g] == -INFINITY) ? 0.f : exp2f(s[st][g] - m_new);
-        l[g] += pr;
-        const uint32_t w[4] = {vr[st].x, vr[st].y, vr[st].z, vr[st].w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          acc[g][2 * e] = fmaf(pr, bf16lo(w[e]), acc[g][2 * e]);
-          acc[g][2 * e + 1] = fmaf(pr, bf16hi(w[e]), acc[g][2 * e + 1]);
+      // every issued copy is waited on by a consumer; if consumers gave up,
+      // wait here (bounded) for the last copies to land
+      if (*abort_flag) {
+        for (int i = (last_slot_issued - C::NSLOT + 1 > 0 ? last_slot_issued - C::NSLOT + 1 : 0);
+             i <= last_slot_issued; ++i) {
+          const uint64_t t0 = globaltimer();
+          while (!mbar_try_wait(smem_u32(&full[i % C::NSLOT]), (i / C::NSLOT) & 1) &&
+                 globaltimer() - t0 < kWaitLimitNs) {
+          }
         }
       }
-      m[g] = m_new;
-    }
-  }
-  // combine the KPS key lanes that share an hd slice
-#pragma unroll
-  for (int g = 0; g < G; ++g) {
-#pragma unroll
-    for (int off = LPK; off < 32; off <<= 1) {
-      l[g] += __shfl_xor_sync(0xffffffffu, l[g], off);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) acc[g][e] += __shfl_xor_sync(0xffffffffu, acc[g][e], off);
-    }
-  }
-  if (kk != 0) return;
-  if (n_splits == 1) {
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      const float inv = 1.f / l[g];
-      uint4 out = make_uint4(pack_bf16x2(acc[g][0] * inv, acc[g][1] * inv), pack_bf16x2(acc[g][2] * inv, acc[g][3] * inv),
-                             pack_bf16x2(acc[g][4] * inv, acc[g][5] * inv), pack_bf16x2(acc[g][6] * inv, acc[g][7] * inv));
-      *reinterpret_cast<uint4 *>(p.o + (static_cast<size_t>(t) * p.Hq + hk * G + g) * HD + d0) = out;
     }
   } else {
+    // ----------------------------------------------------------- consumers
+    const int sub = lane % C::LPK;   // 8-element slice of hd
+    const int kk = lane / C::LPK;    // key within a step
+    const int my_st = sub >> 1;      // step whose score this lane ends up holding
+    float2 qf[G][4];
 #pragma unroll
     for (int g = 0; g < G; ++g) {
-      float *dst = p.part + (static_cast<size_t>(warp_global) * G + g) * part_stride<HD>();
-      float4 *d4 = reinterpret_cast<float4 *>(dst + d0);
-      d4[0] = make_float4(acc[g][0], acc[g][1], acc[g][2], acc[g][3]);
-      d4[1] = make_float4(acc[g][4], acc[g][5], acc[g][6], acc[g][7]);
-      if (sub == 0) {
-        dst[HD] = m[g];
-        dst[HD + 1] = l[g];
+      const uint4 raw = *reinterpret_cast<const uint4 *>(p.q + (static_cast<size_t>(t) * p.Hq + hk * G + g) * HD + sub * 8);
+      const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = bf2(w[e]);
+        qf[g][e] = make_float2(f.x * p.scale_log2, f.y * p.scale_log2);
+      }
+    }
+    float m[G], l[G];
+    float2 acc[G][4];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      m[g] = -INFINITY;
+      l[g] = 0.f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[g][e] = make_float2(0.f, 0.f);
+    }
+    for (int i = warp; i < np; i += C::NW) {
+      const int slot = i % C::NSLOT;
+      if (!mbar_wait(&full[slot], (i / C::NSLOT) & 1, abort_flag, p.err, kErrWaitSoftmax)) break;
+      const uint8_t *ks = ring + slot * C::SLOT_BYTES;
+      const uint8_t *vs = ks + C::PAGE_BYTES;
+      const int key_base = (pb + i) * 16;
+      // partial dot products of this lane's 8 dims with each step's key
+      float part[G][C::STEPS];
+#pragma unroll
+      for (int st = 0; st < C::STEPS; ++st) {
+        const uint4 kr = lds128(ks + (st * C::KPS + kk) * HD * 2 + sub * 16);
+        const float2 k0 = bf2(kr.x), k1 = bf2(kr.y), k2 = bf2(kr.z), k3 = bf2(kr.w);
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          float2 a = __fmul2_rn(qf[g][0], k0);
+          a = __ffma2_rn(qf[g][1], k1, a);
+          a = __ffma2_rn(qf[g][2], k2, a);
+          a = __ffma2_rn(qf[g][3], k3, a);
+          part[g][st] = a.x + a.y;
+        }
+      }
+      // transposed butterfly: each lane ends with the full score of step my_st
+      float s[G];
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        float v[C::STEPS];
+#pragma unroll
+        for (int st = 0; st < C::STEPS; ++st) v[st] = part[g][st];
+        int n = C::STEPS;
+#pragma unroll
+        for (int o = C::LPK / 2; o >= 2; o >>= 1) {
+          const bool upper = (lane & o) != 0;
+          const int half = n / 2;
+#pragma unroll
+          for (int i2 = 0; i2 < C::STEPS / 2; ++i2) {
+            if (i2 < half) {
+              const float send = upper ? v[i2] : v[i2 + half];
+              const float keep = upper ? v[i2 + half] : v[i2];
+              v[i2] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+            }
+          }
+          n = half;
+        }
+        s[g] = v[0] + __shfl_xor_sync(0xffffffffu, v[0], 1);
+      }
+      const int my_key = key_base + my_st * C::KPS + kk;
+      const bool my_valid = my_key < kv;
+      float pv[G];
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        float mx = my_valid ? s[g] : -INFINITY;
+#pragma unroll
+        for (int o = 16; o >= 2; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        const float m_new = fmaxf(m[g], mx);
+        const float alpha = (m[g] == -INFINITY) ? 0.f : exp2f(m[g] - m_new);
+        m[g] = m_new;
+        pv[g] = my_valid ? exp2f(s[g] - m_new) : 0.f;
+        l[g] = l[g] * alpha + ((sub & 1) ? 0.f : pv[g]);
+        const float2 a2 = make_float2(alpha, alpha);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[g][e] = __fmul2_rn(acc[g][e], a2);
+      }
+      // o += p v over this lane's keys (step st, key st*KPS + kk)
+#pragma unroll
+      for (int st = 0; st < C::STEPS; ++st) {
+        const int src = kk * C::LPK + 2 * st;
+        const bool valid = key_base + st * C::KPS + kk < kv;
+        uint4 vr = lds128(vs + (st * C::KPS + kk) * HD * 2 + sub * 16);
+        if (!valid) vr = make_uint4(0, 0, 0, 0);
+        const float2 v0 = bf2(vr.x), v1 = bf2(vr.y), v2 = bf2(vr.z), v3 = bf2(vr.w);
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          const float pr = __shfl_sync(0xffffffffu, pv[g], src);
+          const float2 p2 = make_float2(pr, pr);
+          acc[g][0] = __ffma2_rn(p2, v0, acc[g][0]);
+          acc[g][1] = __ffma2_rn(p2, v1, acc[g][1]);
+          acc[g][2] = __ffma2_rn(p2, v2, acc[g][2]);
+          acc[g][3] = __ffma2_rn(p2, v3, acc[g][3]);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[slot]);
+    }
+    // fold the KPS key lanes that share an hd slice, and the l partials
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+#pragma unroll
+      for (int o = C::LPK; o < 32; o <<= 1)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          acc[g][e].x += __shfl_xor_sync(0xffffffffu, acc[g][e].x, o);
+          acc[g][e].y += __shfl_xor_sync(0xffffffffu, acc[g][e].y, o);
+        }
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) l[g] += __shfl_xor_sync(0xffffffffu, l[g], o);
+    }
+    // stash this warp's (m, l, o) for the CTA merge; the ring is free once
+    // every consumer is past its last page (barrier below)
+    named_bar_sync(1, C::NW * 32);
+    float *stash = reinterpret_cast<float *>(ring) + warp * G * (HD + 2);
+    if (kk == 0) {
+#pragma unroll
+      for (int g = 0; g < G; ++g)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          stash[g * (HD + 2) + sub * 8 + 2 * e] = acc[g][e].x;
+          stash[g * (HD + 2) + sub * 8 + 2 * e + 1] = acc[g][e].y;
+        }
+    }
+    if (lane == 0) {
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        stash[g * (HD + 2) + HD] = m[g];
+        stash[g * (HD + 2) + HD + 1] = l[g];
+      }
+    }
+    named_bar_sync(1, C::NW * 32);
+    const float *all = reinterpret_cast<const float *>(ring);
+    for (int idx = threadIdx.x; idx < G * HD; idx += C::NW * 32) {
+      const int g = idx / HD, d = idx % HD;
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < C::NW; ++w) M = fmaxf(M, all[(w * G + g) * (HD + 2) + HD]);
+      float L = 0.f, O = 0.f;
+#pragma unroll
+      for (int w = 0; w < C::NW; ++w) {
+        const float* base = all + (w * G + g) * (HD + 2);
+        const float wt = base[HD] == -INFINITY ? 0.f : exp2f(base[HD] - M);
+        L += wt * base[HD + 1];
+        O += wt * base[d];
+      }
+      if (n_splits == 1) {
+        p.o[(static_cast<size_t>(t) * p.Hq + hk * G + g) * HD + d] = __float2bfloat16_rn(O / L);
+      } else {
+        float *dst = p.part + (static_cast<size_t>(blockIdx.x) * G + g) * part_stride<HD>();
+        dst[d] = O;
+        if (d == 0) {
+          dst[HD] = M;
+          dst[HD + 1] = L;
+        }
       }
     }
   }
@@ -535,8 +649,14 @@ __global__ void __launch_bounds__(128) merge_kernel(const float *part, const int
 
 template <int HD, int G>
 cudaError_t launch_decode(const DecodeParams &dp, cudaStream_t st) {
-  const int blocks = (dp.n_items + 3) / 4;
-  decode_attn_kernel<HD, G><<<blocks, 128, 0, st>>>(dp);
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(decode_attn_kernel<HD, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    dec_smem<HD, G>());
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  decode_attn_kernel<HD, G><<<dp.n_items, DecCfg<HD>::THREADS, dec_smem<HD, G>(), st>>>(dp);
   return cudaGetLastError();
 }
 

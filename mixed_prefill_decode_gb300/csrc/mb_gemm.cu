@@ -52,11 +52,14 @@ constexpr int SMEM_TILES = STAGES * (A_STAGE + B_STAGE);
 constexpr int SMEM_BYTES = SMEM_TILES + 1024 /*align*/ + 256 /*barriers*/;
 constexpr int THREADS = 192;
 constexpr uint32_t IDESC = idesc_bf16(BM, BN, false);
+constexpr int kMaxGroupedTilesM = 8;   // grouped schedule up to 1,024 tokens
 
 struct Params {
   int M, N, K;          // N: output width (F for SwiGLU)
   int k_iters;
-  int tiles_m;
+  int tiles_m, tiles_n;
+  int grouped;          // 1: CTA (g, m) streams weight tiles of group g for M-tile m
+  int n_groups;         // grouped: CTA groups (grid = n_groups * tiles_m)
   int dp_tiles, sk_tiles;
   int grid;
   __nv_bfloat16 *D;
@@ -64,30 +67,47 @@ struct Params {
   const __nv_bfloat16 *R;
   int ldr;
   int F;                // SwiGLU: row offset of the up half in B
-  float *partials;
+  float *partials;      // [2 grid][8 chunks][128 rows][32] fp32
   int *tickets;
   int *err;
 };
 
+// Work decomposition.  Two schedules share one iteration space of (unit, k)
+// pairs, split into contiguous ranges over "ranks":
+//  * grouped (few M-tiles): a unit is an N-tile, a rank is a group of
+//    tiles_m CTAs, one per M-tile, that walk the same weight tiles at the
+//    same time (each weight tile then streams from HBM once);
+//  * default: whole tiles round-robin over the grid, then the tail tiles'
+//    (tile, k) space split over all CTAs (stream-K); a unit is a tail tile.
+// A unit covered by several ranks is summed from fp32 partial tiles by the
+// rank that arrives last (deterministic order: rank order).
 struct Seg {
   int tile, k0, k1;
   int partial;  // 0: whole K range; 1: a piece of a split tile
   int slot;     // partial slot of this piece
-  int tl;       // stream-K local tile index
+  int unit;     // unit index of a split piece
 };
 
-// Segment enumerator: every role of a CTA walks the same sequence.
+__device__ __forceinline__ long long sk_total(const Params &p) {
+  return static_cast<long long>(p.grouped ? p.tiles_n : p.sk_tiles) * p.k_iters;
+}
+__device__ __forceinline__ int sk_ranks(const Params &p) { return p.grouped ? p.n_groups : p.grid; }
+__device__ __forceinline__ long long rank_lo(const Params &p, int rank) {
+  return sk_total(p) * rank / sk_ranks(p);
+}
+
 struct SegIter {
   const Params &p;
-  int b;
+  int b, rank, mi;
   int dp_next;
-  long long it, it_end;
-  long long total;
+  long long it, it_end, first_unit;
   __device__ SegIter(const Params &pp) : p(pp), b(blockIdx.x) {
-    dp_next = b;
-    total = static_cast<long long>(p.sk_tiles) * p.k_iters;
-    it = total * b / p.grid;
-    it_end = total * (b + 1) / p.grid;
+    rank = p.grouped ? b / p.tiles_m : b;
+    mi = p.grouped ? b % p.tiles_m : 0;
+    dp_next = p.grouped ? p.dp_tiles : b;
+    it = rank_lo(p, rank);
+    it_end = rank_lo(p, rank + 1);
+    first_unit = it / p.k_iters;
   }
   __device__ bool next(Seg &s) {
     if (dp_next < p.dp_tiles) {
@@ -96,61 +116,81 @@ struct SegIter {
       s.k1 = p.k_iters;
       s.partial = 0;
       s.slot = 0;
-      s.tl = -1;
+      s.unit = -1;
       dp_next += p.grid;
       return true;
     }
     if (it >= it_end) return false;
-    const int tl = static_cast<int>(it / p.k_iters);
+    const int u = static_cast<int>(it / p.k_iters);
     const int k0 = static_cast<int>(it % p.k_iters);
-    long long rem = it_end - it;
-    const int k1 = static_cast<int>(min(static_cast<long long>(p.k_iters), k0 + rem));
-    s.tile = p.dp_tiles + tl;
+    const int k1 = static_cast<int>(min(static_cast<long long>(p.k_iters), k0 + (it_end - it)));
+    s.tile = p.grouped ? u * p.tiles_m + mi : p.dp_tiles + u;
     s.k0 = k0;
     s.k1 = k1;
     s.partial = !(k0 == 0 && k1 == p.k_iters);
-    const long long first_it = total * b / p.grid;
-    s.slot = 2 * b + (tl == static_cast<int>(first_it / p.k_iters) ? 0 : 1);
-    s.tl = tl;
+    s.slot = 2 * b + (u == first_unit ? 0 : 1);
+    s.unit = u;
     it += k1 - k0;
     return true;
   }
 };
 
-// CTAs whose stream-K ranges overlap local tile tl: [c_first, c_last].
-__device__ void tile_contributors(const Params &p, int tl, int &c_first, int &c_last) {
-  const long long total = static_cast<long long>(p.sk_tiles) * p.k_iters;
-  const long long lo = static_cast<long long>(tl) * p.k_iters;
-  const long long hi = lo + p.k_iters - 1;
-  // CTA c covers [total*c/grid, total*(c+1)/grid); invert with a search.
+// Ranks whose ranges overlap unit u: [r_first, r_last].
+__device__ void unit_ranks(const Params &p, int u, int &r_first, int &r_last) {
+  const long long total = sk_total(p);
+  const int R = sk_ranks(p);
   auto owner = [&](long long x) {
-    int c = static_cast<int>((x * p.grid) / total);
-    while (c > 0 && total * c / p.grid > x) --c;
-    while (c + 1 < p.grid && total * (c + 1) / p.grid <= x) ++c;
+    int c = static_cast<int>((x * R) / total);
+    while (c > 0 && total * c / R > x) --c;
+    while (c + 1 < R && total * (c + 1) / R <= x) ++c;
     return c;
   };
-  c_first = owner(lo);
-  c_last = owner(hi);
+  const long long lo = static_cast<long long>(u) * p.k_iters;
+  r_first = owner(lo);
+  r_last = owner(lo + p.k_iters - 1);
+}
+
+// Partial slot that the CTA of `rank` (same M-tile) used for unit u.
+__device__ __forceinline__ int slot_of(const Params &p, int rank, int mi, int u) {
+  const int c = p.grouped ? rank * p.tiles_m + mi : rank;
+  return 2 * c + (u == static_cast<int>(rank_lo(p, rank) / p.k_iters) ? 0 : 1);
 }
 
 __device__ __forceinline__ float silu(float x) { return x / (1.0f + expf(-x)); }
 
+__device__ __forceinline__ float *part_chunk(const Params &p, int slot, int j, int r) {
+  return p.partials + ((static_cast<size_t>(slot) * 8 + j) * 128 + r) * 32;
+}
+// Within a partial row of 32 floats, 16-byte group q is stored at q ^ (row % 8)
+// so that the finisher's shared-memory reads of 128 rows spread over banks.
+__device__ __forceinline__ int part_swz(int q, int r) { return q ^ (r & 7); }
+
+// Residual for 4 chunks (128 columns) of one row, issued early.
+__device__ __forceinline__ void load_resid4(const Params &p, int row, int col, uint4 (&rb)[16]) {
+  if (row >= p.M) return;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const bool in = col + 32 * j < p.N;
+    const uint4 *rp = reinterpret_cast<const uint4 *>(p.R + static_cast<size_t>(row) * p.ldr + col + 32 * j);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) rb[4 * j + q] = in ? rp[q] : make_uint4(0, 0, 0, 0);
+  }
+}
+
+// Epilogue of one 32-column chunk: v (and u for SwiGLU) -> bf16 -> D.
 template <int EPI>
 __device__ __forceinline__ void store_chunk(const Params &p, int row, int col, const float (&v)[32],
-                                            const float (*u)[32]) {
-  // col: first output column of this 32-wide chunk
+                                            const float *u, const uint4 *rb) {
   if (row >= p.M || col >= p.N) return;
   uint32_t packed[16];
   if (EPI == kEpiSwiGLU) {
 #pragma unroll
     for (int i = 0; i < 16; ++i)
-      packed[i] = pack_bf16x2(silu(v[2 * i]) * (*u)[2 * i], silu(v[2 * i + 1]) * (*u)[2 * i + 1]);
+      packed[i] = pack_bf16x2(silu(v[2 * i]) * u[2 * i], silu(v[2 * i + 1]) * u[2 * i + 1]);
   } else if (EPI == kEpiResidual) {
-    const uint4 *rp = reinterpret_cast<const uint4 *>(p.R + static_cast<size_t>(row) * p.ldr + col);
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      uint4 r = rp[q];
-      uint32_t rr[4] = {r.x, r.y, r.z, r.w};
+      const uint32_t rr[4] = {rb[q].x, rb[q].y, rb[q].z, rb[q].w};
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int i = q * 4 + j;
@@ -177,9 +217,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t *empty = full + STAGES;
   uint64_t *tfull = empty + STAGES;
   uint64_t *tempty = tfull + 2;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tempty + 2);
+  uint64_t *fixbar = tempty + 2;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(fixbar + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-  volatile int *bcast = abort_flag + 1;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -193,6 +233,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(&tfull[a], 1);
       mbar_init(&tempty[a], 128);
     }
+    mbar_init(fixbar, 1);
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tmA);
@@ -242,12 +283,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         // let copies already in flight land before the CTA exits
         for (int i = 0; i < STAGES; ++i)
           if (issued_mask & (1u << i)) {
-            int dummy = 0;
-            volatile int never = 0;
             const uint32_t a = smem_u32(&full[i]);
             const uint64_t t0 = globaltimer();
-            while (!mbar_try_wait(a, (issued_ph >> i) & 1u) && globaltimer() - t0 < kWaitLimitNs && !never) {
-              ++dummy;
+            while (!mbar_try_wait(a, (issued_ph >> i) & 1u) && globaltimer() - t0 < kWaitLimitNs) {
             }
           }
       }
@@ -301,101 +339,134 @@ __global__ void __launch_bounds__(THREADS, 1)
     Seg sg;
     int acc = 0;
     uint32_t acc_ph = 0;
-    while (segs.next(sg)) {
+    uint32_t fix_ph = 0;
+    bool ok = true;
+    while (ok && segs.next(sg)) {
+      const int mi = sg.tile % p.tiles_m;
+      const int m0 = mi * BM;
+      const int nt = sg.tile / p.tiles_m;
+      const int row = m0 + r;
+      const int col0 = EPI == kEpiSwiGLU ? nt * 128 : nt * BN;
+      uint4 rb[16];
+      if (EPI == kEpiResidual) load_resid4(p, row, col0, rb);   // independent of the accumulator
       if (!mbar_wait(&tfull[acc], acc_ph, abort_flag, p.err, kErrWaitEpilogue)) break;
       tc_fence_after();
       const uint32_t tbase = tmem + acc * BN + (static_cast<uint32_t>(q * 32) << 16);
-      const int m0 = (sg.tile % p.tiles_m) * BM;
-      const int nt = sg.tile / p.tiles_m;
-      const int row = m0 + r;
-      if (!sg.partial) {
+      bool finish = !sg.partial;
+      if (sg.partial) {
+        int r_first, r_last;
+        unit_ranks(p, sg.unit, r_first, r_last);
+        const int my_rank = p.grouped ? blockIdx.x / p.tiles_m : blockIdx.x;
+        // A split unit is identified by its first rank (no other split unit
+        // starts there), so flags stay below the grid size.
+        int *flag = p.tickets + (p.grouped ? r_first * p.tiles_m + mi : r_first);
+        if (my_rank != r_first) {
+          // a later piece: hand the fp32 partial to the rank that covers the
+          // unit's head (for which this unit is its last segment)
+#pragma unroll 1
+          for (int j = 0; j < BN / 32; ++j) {
+            float v[32];
+            tmem_ld32(tbase + 32 * j, v);
+            float4 *w4 = reinterpret_cast<float4 *>(part_chunk(p, sg.slot, j, r));
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              w4[part_swz(i, r)] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+          }
+          tc_fence_before();
+          mbar_arrive(&tempty[acc]);
+          __threadfence();
+          named_bar_sync(1, 128);
+          if (ep == 0) atomicAdd(flag, 1);
+        } else {
+          // the head piece: wait for the other pieces (written early in their
+          // ranks' timelines), fold them into the accumulator in TMEM
+          if (ep == 0) {
+            const int want = r_last - r_first;
+            const uint64_t t0 = globaltimer();
+            int spins = 0;
+            while (ld_acquire_gpu(flag) < want) {
+              if ((++spins & 255) == 0 && globaltimer() - t0 > kWaitLimitNs) {
+                *abort_flag = 1;
+                atomicExch(p.err, kErrWaitEpilogue);
+                break;
+              }
+            }
+            *flag = 0;
+            fence_proxy_async_global();
+          }
+          named_bar_sync(1, 128);
+          if (*abort_flag) {
+            ok = false;
+          } else {
+            // this unit is the rank's last segment: the stage buffers are idle
+            uint8_t *stage = smem;
+#pragma unroll 1
+            for (int rk = r_first + 1; rk <= r_last && ok; ++rk) {
+              if (ep == 0) {
+                const int slot = slot_of(p, rk, mi, sg.unit);
+                mbar_arrive_expect_tx(fixbar, 8 * 16384);
+                for (int j = 0; j < 8; ++j) bulk_load(stage + j * 16384, part_chunk(p, slot, j, 0), 16384, fixbar);
+              }
+              if (!mbar_wait(fixbar, fix_ph, abort_flag, p.err, kErrWaitEpilogue)) {
+                ok = false;
+                break;
+              }
+              fix_ph ^= 1;
+#pragma unroll 1
+              for (int j = 0; j < 8; ++j) {
+                float v[32];
+                tmem_ld32(tbase + 32 * j, v);
+                const float4 *src = reinterpret_cast<const float4 *>(stage + j * 16384 + r * 128);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                  const float4 t = src[part_swz(i, r)];
+                  v[4 * i] += t.x;
+                  v[4 * i + 1] += t.y;
+                  v[4 * i + 2] += t.z;
+                  v[4 * i + 3] += t.w;
+                }
+                tmem_st32(tbase + 32 * j, v);
+              }
+              named_bar_sync(1, 128);   // the next copy overwrites the stage buffers
+            }
+            finish = ok;
+          }
+          if (!finish) {
+            tc_fence_before();
+            mbar_arrive(&tempty[acc]);
+          }
+        }
+      }
+      if (finish) {
         if (EPI == kEpiSwiGLU) {
 #pragma unroll 1
           for (int j = 0; j < 4; ++j) {
             float g[32], u[32];
             tmem_ld32(tbase + 32 * j, g);
             tmem_ld32(tbase + 128 + 32 * j, u);
-            store_chunk<EPI>(p, row, nt * 128 + 32 * j, g, &u);
+            store_chunk<EPI>(p, row, col0 + 32 * j, g, u, nullptr);
+          }
+        } else if (EPI == kEpiResidual) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            if (h == 1) load_resid4(p, row, col0 + 128, rb);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              float v[32];
+              tmem_ld32(tbase + 128 * h + 32 * j, v);
+              store_chunk<EPI>(p, row, col0 + 128 * h + 32 * j, v, nullptr, rb + 4 * j);
+            }
           }
         } else {
 #pragma unroll 1
           for (int j = 0; j < BN / 32; ++j) {
             float v[32];
             tmem_ld32(tbase + 32 * j, v);
-            store_chunk<EPI>(p, row, nt * BN + 32 * j, v, nullptr);
+            store_chunk<EPI>(p, row, col0 + 32 * j, v, nullptr, nullptr);
           }
         }
         tc_fence_before();
         mbar_arrive(&tempty[acc]);
-      } else {
-        float *ws = p.partials + (static_cast<size_t>(sg.slot) * BM + r) * BN;
-#pragma unroll 1
-        for (int j = 0; j < BN / 32; ++j) {
-          float v[32];
-          tmem_ld32(tbase + 32 * j, v);
-          float4 *w4 = reinterpret_cast<float4 *>(ws + 32 * j);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) w4[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-        }
-        tc_fence_before();
-        mbar_arrive(&tempty[acc]);
-        __threadfence();
-        named_bar_sync(1, 128);
-        int c_first, c_last;
-        tile_contributors(p, sg.tl, c_first, c_last);
-        if (ep == 0) {
-          const int n = c_last - c_first + 1;
-          const int old = atomicAdd(&p.tickets[sg.tl], 1);
-          const int last = (old == n - 1);
-          if (last) p.tickets[sg.tl] = 0;
-          *bcast = last;
-        }
-        named_bar_sync(1, 128);
-        if (*bcast) {
-          __threadfence();
-          const long long total = static_cast<long long>(p.sk_tiles) * p.k_iters;
-          auto slot_of = [&](int c) {
-            const long long first_it = total * c / p.grid;
-            return 2 * c + (sg.tl == static_cast<int>(first_it / p.k_iters) ? 0 : 1);
-          };
-          if (EPI == kEpiSwiGLU) {
-#pragma unroll 1
-            for (int j = 0; j < 4; ++j) {
-              float g[32], u[32];
-#pragma unroll
-              for (int i = 0; i < 32; ++i) g[i] = u[i] = 0.f;
-              for (int c = c_first; c <= c_last; ++c) {
-                const float *src = p.partials + (static_cast<size_t>(slot_of(c)) * BM + r) * BN;
-                const float4 *g4 = reinterpret_cast<const float4 *>(src + 32 * j);
-                const float4 *u4 = reinterpret_cast<const float4 *>(src + 128 + 32 * j);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                  float4 a = __ldcg(g4 + i), b = __ldcg(u4 + i);
-                  g[4 * i] += a.x; g[4 * i + 1] += a.y; g[4 * i + 2] += a.z; g[4 * i + 3] += a.w;
-                  u[4 * i] += b.x; u[4 * i + 1] += b.y; u[4 * i + 2] += b.z; u[4 * i + 3] += b.w;
-                }
-              }
-              store_chunk<EPI>(p, row, nt * 128 + 32 * j, g, &u);
-            }
-          } else {
-#pragma unroll 1
-            for (int j = 0; j < BN / 32; ++j) {
-              float v[32];
-#pragma unroll
-              for (int i = 0; i < 32; ++i) v[i] = 0.f;
-              for (int c = c_first; c <= c_last; ++c) {
-                const float4 *s4 = reinterpret_cast<const float4 *>(
-                    p.partials + (static_cast<size_t>(slot_of(c)) * BM + r) * BN + 32 * j);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                  float4 a = __ldcg(s4 + i);
-                  v[4 * i] += a.x; v[4 * i + 1] += a.y; v[4 * i + 2] += a.z; v[4 * i + 3] += a.w;
-                }
-              }
-              store_chunk<EPI>(p, row, nt * BN + 32 * j, v, nullptr);
-            }
-          }
-        }
       }
       acc ^= 1;
       if (acc == 0) acc_ph ^= 1;
@@ -455,23 +526,33 @@ cudaError_t gemm_run(const void *A, const void *B, const CUtensorMap *tmB_pre, v
   p.K = K;
   p.k_iters = K / BK;
   p.tiles_m = (M + BM - 1) / BM;
-  const int tiles_n = epi == kEpiSwiGLU ? N / 128 : (N + BN - 1) / BN;
-  const int tiles = p.tiles_m * tiles_n;
+  p.tiles_n = epi == kEpiSwiGLU ? N / 128 : (N + BN - 1) / BN;
+  const int tiles = p.tiles_m * p.tiles_n;
   const int sms = device_sm_count() < kMaxGemmGrid ? device_sm_count() : kMaxGemmGrid;
-  // Whole waves run data-parallel; the last one to two waves are spread along
-  // K over every SM.  A tile count that is a multiple of the SM count needs no
-  // split.
-  if (tiles % sms == 0) {
+  if (p.tiles_m <= kMaxGroupedTilesM && p.tiles_m <= sms) {
+    // Few token tiles: every weight tile is consumed by tiles_m CTAs running
+    // side by side, and the (N-tile, k) space is split evenly over the groups.
+    long long groups = sms / p.tiles_m;
+    const long long iters = static_cast<long long>(p.tiles_n) * p.k_iters;
+    if (iters < 2 * groups) groups = iters / 2 > 0 ? iters / 2 : 1;  // at least two K steps per CTA
+    p.grouped = 1;
+    p.n_groups = static_cast<int>(groups);
+    p.grid = p.n_groups * p.tiles_m;
+    p.dp_tiles = 0;
+    p.sk_tiles = 0;
+  } else if (tiles % sms == 0) {
     p.dp_tiles = tiles;
     p.sk_tiles = 0;
     p.grid = sms;
   } else {
+    // Whole waves run data-parallel; the last one to two waves are spread
+    // along K over every SM.
     const int waves = tiles / sms;
     p.dp_tiles = waves >= 2 ? (waves - 1) * sms : 0;
     p.sk_tiles = tiles - p.dp_tiles;
     const long long sk_iters = static_cast<long long>(p.sk_tiles) * p.k_iters;
     long long g = sms;
-    if (sk_iters < 2LL * g) g = sk_iters / 2 > 0 ? sk_iters / 2 : 1;  // at least two K steps per CTA
+    if (sk_iters < 2LL * g) g = sk_iters / 2 > 0 ? sk_iters / 2 : 1;
     if (p.dp_tiles > 0 && g < sms) g = sms;
     p.grid = static_cast<int>(g);
     if (p.dp_tiles > 0 && p.grid != sms) return cudaErrorInvalidValue;
@@ -574,8 +655,8 @@ extern "C" mb_status mb_gemm_noalloc(const void *A, const void *B, void *D, cons
   p.K = K;
   p.k_iters = K / BK;
   p.tiles_m = (M + BM - 1) / BM;
-  const int tiles_n = epilogue == kEpiSwiGLU ? N / 128 : (N + BN - 1) / BN;
-  const long long tiles = static_cast<long long>(p.tiles_m) * tiles_n;
+  p.tiles_n = epilogue == kEpiSwiGLU ? N / 128 : (N + BN - 1) / BN;
+  const long long tiles = static_cast<long long>(p.tiles_m) * p.tiles_n;
   if (tiles >= sms) {
     p.dp_tiles = static_cast<int>(tiles);
     p.sk_tiles = 0;
