@@ -53,7 +53,9 @@ struct ChunkCfg {
   static constexpr int OFF_V = OFF_K + 2 * KV_BYTES;
   static constexpr int OFF_P = OFF_V + 2 * KV_BYTES;
   static constexpr int OFF_BAR = OFF_P + P_BYTES;
-  static constexpr int SMEM = OFF_BAR + 128 + 1024;
+  static constexpr int OFF_RED = OFF_BAR + 128;   // softmax row max / sum exchange
+  static constexpr int SMEM = OFF_RED + 6 * 128 * 4 + 1024;
+  static constexpr int THREADS = 320;             // TMA, MMA, 8 softmax warps
   static constexpr uint32_t IDESC_S = idesc_bf16(128, 128, false);
   static constexpr uint32_t IDESC_PV = idesc_bf16(128, HD, true);
   static constexpr uint32_t TMEM_COLS = 512;      // S0 [0,128), S1 [128,256), O [256, 256+HD)
@@ -68,7 +70,7 @@ struct ChunkParams {
 };
 
 template <int HD>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(ChunkCfg<HD>::THREADS, 1)
     chunk_attn_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmKV,
                       const ChunkParams p) {
   using C = ChunkCfg<HD>;
@@ -111,7 +113,7 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(&kv_empty[s], 1);
       mbar_init(&s_full[s], 1);
     }
-    mbar_init(p_full, 128);
+    mbar_init(p_full, 256);
     mbar_init(o_full, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -224,105 +226,140 @@ __global__ void __launch_bounds__(192, 1)
     }
   } else {
     // ------------------------------------------------- softmax / epilogue
+    // 8 warps: two per TMEM lane quarter, splitting the 128 key columns of S
+    // (and the hd columns of O) in halves; a row's max and sum are combined
+    // through shared memory once per key block.
     const int q = warp & 3;
+    const int hh = (warp - 2) >> 2;          // column half
     const int r = q * 32 + lane;
     const int q_pos = cached + i0 + r;
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
-    float o_acc[HD];
+    constexpr int OH = HD / 2;               // O columns per half
+    float *red = reinterpret_cast<float *>(smem + C::OFF_RED);  // [2 bufs][2 halves][128]
+    float o_acc[OH];
 #pragma unroll
-    for (int d = 0; d < HD; ++d) o_acc[d] = 0.f;
+    for (int d = 0; d < OH; ++d) o_acc[d] = 0.f;
     float m = -INFINITY, l = 0.f;
     bool ok = true;
+    // A wait that gives up marks the thread `bad`; the decision to leave is
+    // taken jointly at the per-block barrier so no warp is left waiting there.
+    bool bad = false;
     for (int j = 0; j < n_kb; ++j) {
       const int b = j & 1;
-      if (!mbar_wait(&s_full[b], (j >> 1) & 1, abort_flag, p.err, kErrWaitSoftmax)) {
+      bad = !ok || !mbar_wait(&s_full[b], (j >> 1) & 1, abort_flag, p.err, kErrWaitSoftmax);
+      bad = __any_sync(0xffffffffu, bad);   // tcgen05.ld below is warp-collective
+      tc_fence_after();
+      const int key0 = 128 * j + hh * 64;   // first key of this thread's half
+      const bool full = (key0 + 63 <= q_pos) && (key0 + 63 < kv);
+      const uint32_t scol = tmem + lane_base + b * 128 + hh * 64;
+      // pass 1: maximum of the visible scores of this half row
+      float mx = -INFINITY;
+#pragma unroll
+      for (int cc = 0; cc < 2 && !bad; ++cc) {
+        float v[32];
+        tmem_ld32(scol + cc * 32, v);
+        if (full) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) mx = fmaxf(mx, v[i]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int key = key0 + cc * 32 + i;
+            if (key <= q_pos && key < kv) mx = fmaxf(mx, v[i]);
+          }
+        }
+      }
+      mx *= p.scale_log2;
+      red[(b * 2 + hh) * 128 + r] = mx;
+      if (named_bar_or(2, 256, bad)) {
         ok = false;
         break;
       }
-      tc_fence_after();
-      const int key0 = 128 * j;
-      // pass 1: row maximum of the visible scores
-      float mx = -INFINITY;
-#pragma unroll 1
-      for (int cc = 0; cc < 4; ++cc) {
-        float v[32];
-        tmem_ld32(tmem + lane_base + b * 128 + cc * 32, v);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int key = key0 + cc * 32 + i;
-          if (key <= q_pos && key < kv) mx = fmaxf(mx, v[i] * p.scale_log2);
-        }
-      }
+      mx = fmaxf(mx, red[(b * 2 + (hh ^ 1)) * 128 + r]);
       const float m_new = fmaxf(m, mx);
       const float alpha = (m == -INFINITY) ? 0.f : exp2f(m - m_new);
       if (j > 0) {
-        if (!mbar_wait(o_full, (j - 1) & 1, abort_flag, p.err, kErrWaitSoftmax)) {
+        bad = !mbar_wait(o_full, (j - 1) & 1, abort_flag, p.err, kErrWaitSoftmax);
+        bad = __any_sync(0xffffffffu, bad);
+        if (bad) {
+          // reported at the next barrier (or after the loop); skip the work
           ok = false;
-          break;
+          continue;
         }
         tc_fence_after();
 #pragma unroll
-        for (int cc = 0; cc < HD / 32; ++cc) {
+        for (int cc = 0; cc < OH / 32; ++cc) {
           float v[32];
-          tmem_ld32(tmem + lane_base + 256 + cc * 32, v);
+          tmem_ld32(tmem + lane_base + 256 + hh * OH + cc * 32, v);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o_acc[cc * 32 + i] += v[i];
+          for (int i = 0; i < 32; ++i) o_acc[cc * 32 + i] = (o_acc[cc * 32 + i] + v[i]) * alpha;
         }
-      }
+      } else {
 #pragma unroll
-      for (int d = 0; d < HD; ++d) o_acc[d] *= alpha;
+        for (int d = 0; d < OH; ++d) o_acc[d] *= alpha;
+      }
       l *= alpha;
-      // pass 2: probabilities -> bf16 P tile (A operand, K-major, swizzled)
-#pragma unroll 1
-      for (int cc = 0; cc < 4; ++cc) {
+      // pass 2: probabilities -> bf16 P half row (A operand, K-major, swizzled)
+      uint8_t *prow = sP + hh * C::TILE_BYTES + (r >> 3) * 1024 + (r & 7) * 128;
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
         float v[32];
-        tmem_ld32(tmem + lane_base + b * 128 + cc * 32, v);
+        tmem_ld32(scol + cc * 32, v);
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
-          const int key = key0 + cc * 32 + i;
-          const float p0 = (key <= q_pos && key < kv) ? exp2f(v[i] * p.scale_log2 - m_new) : 0.f;
-          const float p1 = (key + 1 <= q_pos && key + 1 < kv) ? exp2f(v[i + 1] * p.scale_log2 - m_new) : 0.f;
+          float p0 = exp2f(fmaf(v[i], p.scale_log2, -m_new));
+          float p1 = exp2f(fmaf(v[i + 1], p.scale_log2, -m_new));
+          if (!full) {
+            const int key = key0 + cc * 32 + i;
+            if (!(key <= q_pos && key < kv)) p0 = 0.f;
+            if (!(key + 1 <= q_pos && key + 1 < kv)) p1 = 0.f;
+          }
           l += p0 + p1;
           pk[i / 2] = pack_bf16x2(p0, p1);
         }
-        // keys cc*32 .. cc*32+31 live in P chunk (cc / 2), 16-byte groups
-        uint8_t *prow = sP + (cc >> 1) * C::TILE_BYTES + (r >> 3) * 1024 + (r & 7) * 128;
 #pragma unroll
         for (int g4 = 0; g4 < 4; ++g4) {
-          const int grp = (cc & 1) * 4 + g4;  // 8-key group within the 64-key chunk
+          const int grp = cc * 4 + g4;  // 8-key group within this 64-key chunk
           *reinterpret_cast<uint4 *>(prow + ((grp ^ (r & 7)) * 16)) =
               make_uint4(pk[4 * g4], pk[4 * g4 + 1], pk[4 * g4 + 2], pk[4 * g4 + 3]);
         }
       }
-      if (j == n_kb - 1 && key0 + r > last_pos) {
+      if (j == n_kb - 1 && 128 * j + r > last_pos) {
         // rows past the last visible key may hold stale or non-finite data:
         // zero them so that P = 0 rows contribute exactly nothing
         uint8_t *vrow = sV + b * C::KV_BYTES + (r >> 3) * 1024 + (r & 7) * 128;
 #pragma unroll
         for (int c = 0; c < C::NH; ++c)
+          if ((c & 1) == hh)
 #pragma unroll
-          for (int k = 0; k < 8; ++k) *reinterpret_cast<uint4 *>(vrow + c * C::TILE_BYTES + k * 16) = make_uint4(0, 0, 0, 0);
+            for (int k = 0; k < 8; ++k)
+              *reinterpret_cast<uint4 *>(vrow + c * C::TILE_BYTES + k * 16) = make_uint4(0, 0, 0, 0);
       }
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(p_full);
       m = m_new;
     }
+    // row sum over both halves
+    float *lsum = red + 4 * 128;
+    lsum[hh * 128 + r] = l;
+    named_bar_sync(2, 256);
+    l += lsum[(hh ^ 1) * 128 + r];
     if (ok && mbar_wait(o_full, (n_kb - 1) & 1, abort_flag, p.err, kErrWaitSoftmax)) {
       tc_fence_after();
 #pragma unroll
-      for (int cc = 0; cc < HD / 32; ++cc) {
+      for (int cc = 0; cc < OH / 32; ++cc) {
         float v[32];
-        tmem_ld32(tmem + lane_base + 256 + cc * 32, v);
+        tmem_ld32(tmem + lane_base + 256 + hh * OH + cc * 32, v);
 #pragma unroll
         for (int i = 0; i < 32; ++i) o_acc[cc * 32 + i] += v[i];
       }
       if (i0 + r < qo) {
         const float inv = 1.f / l;
-        uint4 *dst = reinterpret_cast<uint4 *>(p.o + static_cast<size_t>(t0 + i0 + r) * (p.Hq * HD) + h * HD);
+        uint4 *dst = reinterpret_cast<uint4 *>(p.o + static_cast<size_t>(t0 + i0 + r) * (p.Hq * HD) + h * HD + hh * OH);
 #pragma unroll
-        for (int v8 = 0; v8 < HD / 8; ++v8)
+        for (int v8 = 0; v8 < OH / 8; ++v8)
           dst[v8] = make_uint4(pack_bf16x2(o_acc[8 * v8] * inv, o_acc[8 * v8 + 1] * inv),
                                pack_bf16x2(o_acc[8 * v8 + 2] * inv, o_acc[8 * v8 + 3] * inv),
                                pack_bf16x2(o_acc[8 * v8 + 4] * inv, o_acc[8 * v8 + 5] * inv),
@@ -685,7 +722,7 @@ cudaError_t launch_chunk(const CUtensorMap &tq, const CUtensorMap &tkv, const Ch
                                     ChunkCfg<HD>::SMEM);
   });
   if (attr_err != cudaSuccess) return attr_err;
-  chunk_attn_kernel<HD><<<n_tiles, 192, ChunkCfg<HD>::SMEM, st>>>(tq, tkv, cp);
+  chunk_attn_kernel<HD><<<n_tiles, ChunkCfg<HD>::THREADS, ChunkCfg<HD>::SMEM, st>>>(tq, tkv, cp);
   return cudaGetLastError();
 }
 

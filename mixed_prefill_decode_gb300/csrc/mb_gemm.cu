@@ -53,6 +53,10 @@ constexpr int SMEM_BYTES = SMEM_TILES + 1024 /*align*/ + 256 /*barriers*/;
 constexpr int THREADS = 192;
 constexpr uint32_t IDESC = idesc_bf16(BM, BN, false);
 constexpr int kMaxGroupedTilesM = 8;   // grouped schedule up to 1,024 tokens
+constexpr int kPrefetchAhead = 8;      // weight k-blocks fetched into L2 ahead of the ring
+#ifndef MB_GEMM_MULTICAST
+#define MB_GEMM_MULTICAST 1            // 1: a group's CTAs form a cluster and share weight tiles by multicast
+#endif
 
 struct Params {
   int M, N, K;          // N: output width (F for SwiGLU)
@@ -60,6 +64,7 @@ struct Params {
   int tiles_m, tiles_n;
   int grouped;          // 1: CTA (g, m) streams weight tiles of group g for M-tile m
   int n_groups;         // grouped: CTA groups (grid = n_groups * tiles_m)
+  int cluster;          // grouped with tiles_m > 1: a group is one cluster; B is multicast
   int dp_tiles, sk_tiles;
   int grid;
   __nv_bfloat16 *D;
@@ -227,7 +232,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], p.cluster);   // every CTA of the cluster releases the stage
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
@@ -247,6 +252,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // peers multicast into this CTA's stages and arrive on its barriers
+  if (p.cluster > 1) cluster_sync();
+  const uint32_t crank = p.cluster > 1 ? cluster_ctarank() : 0;
+  const uint16_t cmask = static_cast<uint16_t>((1u << p.cluster) - 1u);
 
   if (warp == 0) {
     if (lane == 0) {
@@ -262,15 +271,34 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int nt = sg.tile / p.tiles_m;
         const int rows0 = EPI == kEpiSwiGLU ? nt * 128 : nt * BN;
         const int rows1 = EPI == kEpiSwiGLU ? p.F + nt * 128 : nt * BN + 128;
+        // one CTA per group warms L2 with the weight k-blocks ahead of the ring
+        const bool prefetcher = p.grouped ? (blockIdx.x % p.tiles_m) == 0 : true;
+        if (prefetcher) {
+          for (int kb = sg.k0; kb < sg.k1 && kb < sg.k0 + kPrefetchAhead; ++kb) {
+            tma_prefetch_2d(&tmB, kb * BK, rows0);
+            tma_prefetch_2d(&tmB, kb * BK, rows1);
+          }
+        }
         for (int kb = sg.k0; kb < sg.k1; ++kb) {
+          if (prefetcher && kb + kPrefetchAhead < sg.k1) {
+            tma_prefetch_2d(&tmB, (kb + kPrefetchAhead) * BK, rows0);
+            tma_prefetch_2d(&tmB, (kb + kPrefetchAhead) * BK, rows1);
+          }
           if (!mbar_wait(&empty[s], ph ^ 1, abort_flag, p.err, kErrWaitProducer)) {
             ok = false;
             break;
           }
           mbar_arrive_expect_tx(&full[s], A_STAGE + B_STAGE);
           tma_load_2d(sA + s * A_STAGE, &tmA, &full[s], kb * BK, m0);
-          tma_load_2d(sB + s * B_STAGE, &tmB, &full[s], kb * BK, rows0);
-          tma_load_2d(sB + s * B_STAGE + B_STAGE / 2, &tmB, &full[s], kb * BK, rows1);
+          if (p.cluster == 1) {
+            tma_load_2d(sB + s * B_STAGE, &tmB, &full[s], kb * BK, rows0);
+            tma_load_2d(sB + s * B_STAGE + B_STAGE / 2, &tmB, &full[s], kb * BK, rows1);
+          } else if (crank == 0) {
+            // the group's M-tiles share the weight tile: one read, delivered to all
+            tma_load_2d_mc(sB + s * B_STAGE, &tmB, &full[s], kb * BK, rows0, cmask);
+          } else if (crank == 1) {
+            tma_load_2d_mc(sB + s * B_STAGE + B_STAGE / 2, &tmB, &full[s], kb * BK, rows1, cmask);
+          }
           issued_mask |= 1u << s;
           issued_ph = (issued_ph & ~(1u << s)) | (ph << s);
           if (++s == STAGES) {
@@ -318,7 +346,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             const uint64_t bd = sdesc_sw128(b0 + kk * 32, 16, 1024);
             mma_bf16(d, ad, bd, IDESC, (kb > sg.k0 || kk > 0) ? 1u : 0u);
           }
-          mma_commit(&empty[s]);
+          if (p.cluster > 1)
+            mma_commit_mc(&empty[s], cmask);
+          else
+            mma_commit(&empty[s]);
           if (++s == STAGES) {
             s = 0;
             ph ^= 1;
@@ -401,17 +432,19 @@ __global__ void __launch_bounds__(THREADS, 1)
             // this unit is the rank's last segment: the stage buffers are idle
             uint8_t *stage = smem;
 #pragma unroll 1
-            for (int rk = r_first + 1; rk <= r_last && ok; ++rk) {
+            for (int rk = r_first + 1; rk <= r_last; ++rk) {
               if (ep == 0) {
                 const int slot = slot_of(p, rk, mi, sg.unit);
                 mbar_arrive_expect_tx(fixbar, 8 * 16384);
                 for (int j = 0; j < 8; ++j) bulk_load(stage + j * 16384, part_chunk(p, slot, j, 0), 16384, fixbar);
               }
-              if (!mbar_wait(fixbar, fix_ph, abort_flag, p.err, kErrWaitEpilogue)) {
+              const bool got = __all_sync(0xffffffffu, mbar_wait(fixbar, fix_ph, abort_flag, p.err, kErrWaitEpilogue));
+              fix_ph ^= 1;
+              // leave together: the barrier at the end of each pass is shared
+              if (named_bar_or(1, 128, !got)) {
                 ok = false;
                 break;
               }
-              fix_ph ^= 1;
 #pragma unroll 1
               for (int j = 0; j < 8; ++j) {
                 float v[32];
@@ -474,6 +507,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 
   __syncthreads();
+  // no CTA leaves while a peer may still multicast into it or arrive on it
+  if (p.cluster > 1) cluster_sync();
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
@@ -489,8 +524,55 @@ cudaError_t launch(const CUtensorMap &tmA, const CUtensorMap &tmB, const Params 
     attr_err = cudaFuncSetAttribute(gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   });
   if (attr_err != cudaSuccess) return attr_err;
-  gemm_kernel<EPI><<<p.grid, THREADS, SMEM_BYTES, st>>>(tmA, tmB, p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.grid);
+  cfg.blockDim = dim3(THREADS);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = p.cluster > 1 ? p.cluster : 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gemm_kernel<EPI>, tmA, tmB, p);
+}
+
+// Clusters of `size` CTAs of this kernel that can be resident at once (the
+// split fix-up waits on other CTAs, so the whole grid must be co-resident).
+template <int EPI>
+int max_clusters(int size) {
+  static std::mutex mu;
+  static int cache[9] = {0};
+  std::lock_guard<std::mutex> lk(mu);
+  if (size < 1 || size > 8) return 0;
+  if (cache[size] == 0) {
+    cudaFuncSetAttribute(gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(size * 64);
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = size;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_kernel<EPI>, &cfg) != cudaSuccess || n <= 0) n = -1;
+    cache[size] = n;
+  }
+  return cache[size];
+}
+
+int max_clusters_for(int epi, int size) {
+  switch (epi) {
+    case kEpiStore: return max_clusters<kEpiStore>(size);
+    case kEpiResidual: return max_clusters<kEpiResidual>(size);
+    default: return max_clusters<kEpiSwiGLU>(size);
+  }
 }
 
 }  // namespace
@@ -533,6 +615,14 @@ cudaError_t gemm_run(const void *A, const void *B, const CUtensorMap *tmB_pre, v
     // Few token tiles: every weight tile is consumed by tiles_m CTAs running
     // side by side, and the (N-tile, k) space is split evenly over the groups.
     long long groups = sms / p.tiles_m;
+    p.cluster = 1;
+    if (MB_GEMM_MULTICAST && p.tiles_m > 1) {
+      const int mc = max_clusters_for(epi, p.tiles_m);
+      if (mc > 0) {
+        p.cluster = p.tiles_m;
+        if (groups > mc) groups = mc;
+      }
+    }
     const long long iters = static_cast<long long>(p.tiles_n) * p.k_iters;
     if (iters < 2 * groups) groups = iters / 2 > 0 ? iters / 2 : 1;  // at least two K steps per CTA
     p.grouped = 1;
@@ -541,10 +631,12 @@ cudaError_t gemm_run(const void *A, const void *B, const CUtensorMap *tmB_pre, v
     p.dp_tiles = 0;
     p.sk_tiles = 0;
   } else if (tiles % sms == 0) {
+    p.cluster = 1;
     p.dp_tiles = tiles;
     p.sk_tiles = 0;
     p.grid = sms;
   } else {
+    p.cluster = 1;
     // Whole waves run data-parallel; the last one to two waves are spread
     // along K over every SM.
     const int waves = tiles / sms;
@@ -657,6 +749,7 @@ extern "C" mb_status mb_gemm_noalloc(const void *A, const void *B, void *D, cons
   p.tiles_m = (M + BM - 1) / BM;
   p.tiles_n = epilogue == kEpiSwiGLU ? N / 128 : (N + BN - 1) / BN;
   const long long tiles = static_cast<long long>(p.tiles_m) * p.tiles_n;
+  p.cluster = 1;
   if (tiles >= sms) {
     p.dp_tiles = static_cast<int>(tiles);
     p.sk_tiles = 0;
