@@ -159,8 +159,9 @@ mb_status mb_layer_buffer(const mb_layer *layer, int32_t which, void **ptr, int6
 /* Per-kernel timing of subsequent steps (CUDA events on the step's stream).
  * mb_layer_timing returns the accumulated milliseconds of each launch kind
  * since enable, in the order: rmsnorm_attn, gemm_qkv, rope_append,
- * attn_chunk, attn_decode, attn_merge, gemm_o, rmsnorm_ffn, gemm_gate_up,
- * gemm_down (n <= 10), and the number of steps timed.  It synchronises on the
+ * attention (prefill-chunk tiles and decode rows, one grid), attn_merge,
+ * gemm_o, rmsnorm_ffn, gemm_gate_up, gemm_down (n <= 9), and the number of
+ * steps timed.  It synchronises on the
  * recorded events. */
 mb_status mb_layer_set_timing(mb_layer *layer, int32_t enable);
 mb_status mb_layer_timing(mb_layer *layer, double *ms, int32_t n, int64_t *steps);

@@ -22,7 +22,7 @@ from . import build as _build
 MB_OK, MB_EINVAL, MB_ENOMEM, MB_ENOSPACE, MB_ECUDA, MB_EUNSUPPORTED, MB_EDEVICE = 0, -1, -2, -3, -4, -5, -6
 STATUS_NAMES = {0: "MB_OK", -1: "MB_EINVAL", -2: "MB_ENOMEM", -3: "MB_ENOSPACE", -4: "MB_ECUDA",
                 -5: "MB_EUNSUPPORTED", -6: "MB_EDEVICE"}
-TIMED_KERNELS = ("rmsnorm_attn", "gemm_qkv", "rope_append", "attn_chunk", "attn_decode", "attn_merge", "gemm_o",
+TIMED_KERNELS = ("rmsnorm_attn", "gemm_qkv", "rope_append", "attention", "attn_merge", "gemm_o",
                  "rmsnorm_ffn", "gemm_gate_up", "gemm_down")
 BUF_XN, BUF_QKV, BUF_Q, BUF_O, BUF_H, BUF_HN, BUF_A = range(7)
 

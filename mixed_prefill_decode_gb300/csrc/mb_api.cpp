@@ -140,7 +140,7 @@ using mb::fail;
 // ===================================================================== layer
 namespace {
 
-constexpr int kNumTimed = 10;
+constexpr int kNumTimed = 9;
 constexpr int kRing = 4;
 
 struct EventSet {
@@ -601,8 +601,8 @@ mb_status mb_step(mb_layer *L, mb_kv *kv, const mb_batch *b, const void *x_in, v
     hb[o_tiles + 4 * i + 1] = tiles[i].i0;
     hb[o_tiles + 4 * i + 2] = tiles[i].h;
   }
-  // decode splits: about four CTAs per SM in total (two resident per SM),
-  // each request's pages divided evenly among its splits
+  // decode splits: about four items per SM (two per resident CTA of the
+  // attention grid), each request's pages divided evenly among its splits
   const int64_t target_items = static_cast<int64_t>(ctx->sms) * 4;
   int64_t pps = (dec_pages * Hkv + target_items - 1) / std::max<int64_t>(1, target_items);
   pps = std::max<int64_t>(pps, 8);
@@ -761,12 +761,9 @@ mb_status mb_step(mb_layer *L, mb_kv *kv, const mb_batch *b, const void *x_in, v
   aa.err = L->err;
   aa.tm_q = &tm_q;
   aa.tm_kv = &kv->tmap;
-  if ((st = chk(mb::attn_chunk_run(aa, s), "chunk attention")) != MB_OK) return st;
-  launches += aa.n_tiles > 0;
+  if ((st = chk(mb::attention_run(aa, s), "attention")) != MB_OK) return st;
+  launches += (aa.n_tiles + aa.n_items) > 0;
   mark(4);
-  if ((st = chk(mb::attn_decode_run(aa, s), "decode attention")) != MB_OK) return st;
-  launches += aa.n_items > 0;
-  mark(5);
   mb::MergeArgs ma;
   ma.part = L->part;
   ma.merge_list = db + o_merge;
@@ -778,25 +775,25 @@ mb_status mb_step(mb_layer *L, mb_kv *kv, const mb_batch *b, const void *x_in, v
   ma.hd = hd;
   if ((st = chk(mb::attn_merge_run(ma, s), "merge")) != MB_OK) return st;
   launches += n_merge > 0;
-  mark(6);
+  mark(5);
   if ((st = chk(mb::gemm_run(L->o, L->w.w_o, &L->tm_wo, L->h, x_in, Ti, d.d_model, hqd, mb::kEpiResidual, L->gws,
                              L->err, s), "gemm o")) != MB_OK)
     return st;
   ++launches;
-  mark(7);
+  mark(6);
   if ((st = chk(mb::rmsnorm_run(L->h, L->w.g_ffn, L->hn, Ti, d.d_model, d.rms_eps, s), "rmsnorm ffn")) != MB_OK) return st;
   ++launches;
-  mark(8);
+  mark(7);
   if ((st = chk(mb::gemm_run(L->hn, L->w.w_gate_up, &L->tm_wgu, L->a, nullptr, Ti, d.d_ff, d.d_model, mb::kEpiSwiGLU,
                              L->gws, L->err, s), "gemm gate/up")) != MB_OK)
     return st;
   ++launches;
-  mark(9);
+  mark(8);
   if ((st = chk(mb::gemm_run(L->a, L->w.w_down, &L->tm_wd, x_out, L->h, Ti, d.d_model, d.d_ff, mb::kEpiResidual, L->gws,
                              L->err, s), "gemm down")) != MB_OK)
     return st;
   ++launches;
-  mark(10);
+  mark(9);
   L->last_T = static_cast<int32_t>(T);
   L->last_launches = launches;
   L->last_upload = static_cast<int64_t>(hb.size()) * 4;

@@ -69,12 +69,12 @@ struct ChunkParams {
   int *err;
 };
 
+// One prefill-chunk tile (128 query rows x one q-head); needs
+// ChunkCfg<HD>::THREADS threads and ChunkCfg<HD>::SMEM bytes of shared memory.
 template <int HD>
-__global__ void __launch_bounds__(ChunkCfg<HD>::THREADS, 1)
-    chunk_attn_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmKV,
-                      const ChunkParams p) {
+__device__ __forceinline__ void chunk_tile(const CUtensorMap &tmQ, const CUtensorMap &tmKV, const ChunkParams &p,
+                                           int tile, uint8_t *smem_raw) {
   using C = ChunkCfg<HD>;
-  extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = align1024(smem_raw);
   uint8_t *sQ = smem + C::OFF_Q;
   uint8_t *sK = smem + C::OFF_K;
@@ -93,9 +93,9 @@ __global__ void __launch_bounds__(ChunkCfg<HD>::THREADS, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  const int req = p.tiles[blockIdx.x * 4 + 0];
-  const int i0 = p.tiles[blockIdx.x * 4 + 1];
-  const int h = p.tiles[blockIdx.x * 4 + 2];
+  const int req = p.tiles[tile * 4 + 0];
+  const int i0 = p.tiles[tile * 4 + 1];
+  const int h = p.tiles[tile * 4 + 2];
   const int t0 = p.qo_indptr[req];
   const int qo = p.qo_indptr[req + 1] - t0;
   const int kv = p.kv_len[req];
@@ -399,63 +399,58 @@ struct DecodeParams {
 // (m, l, o) are merged in shared memory at the end.
 template <int HD>
 struct DecCfg {
-  static constexpr int NW = 4;                  // consumer warps
-  static constexpr int THREADS = (NW + 1) * 32;
-  static constexpr int NSLOT = 8;
   static constexpr int PAGE_BYTES = 16 * HD * 2;
   static constexpr int SLOT_BYTES = 2 * PAGE_BYTES;
   static constexpr int LPK = HD / 8;            // lanes per key
   static constexpr int KPS = 32 / LPK;          // keys per step
   static constexpr int STEPS = 16 / KPS;
-  static constexpr int RING = NSLOT * SLOT_BYTES;
 };
-
-template <int HD, int G>
-constexpr int dec_smem() {
-  // ring + barriers; the final merge reuses the ring
-  return DecCfg<HD>::RING + 256;
-}
 
 __device__ __forceinline__ uint4 lds128(const uint8_t *p) { return *reinterpret_cast<const uint4 *>(p); }
 
 __device__ __forceinline__ float2 bf2(uint32_t w) { return make_float2(bf16lo(w), bf16hi(w)); }
 
-template <int HD, int G>
-__global__ void __launch_bounds__(DecCfg<HD>::THREADS, 2) decode_attn_kernel(const DecodeParams p) {
+// NW consumer warps (warps 0 .. NW-1) and one producer warp (warp NW);
+// further warps of the CTA idle.  `dsm` holds NSLOT ring slots, then the
+// barriers.
+template <int HD, int G, int NW, int NSLOT>
+__device__ __forceinline__ void decode_item(const DecodeParams &p, int item, uint8_t *dsm, int warp_base,
+                                            int bar_id) {
   using C = DecCfg<HD>;
-  extern __shared__ __align__(128) uint8_t dsm[];
+  constexpr int RING = NSLOT * C::SLOT_BYTES;
   uint8_t *ring = dsm;
-  uint64_t *full = reinterpret_cast<uint64_t *>(dsm + C::RING);
-  uint64_t *empty = full + C::NSLOT;
-  volatile int *abort_flag = reinterpret_cast<volatile int *>(empty + C::NSLOT);
+  uint64_t *full = reinterpret_cast<uint64_t *>(dsm + RING);
+  uint64_t *empty = full + NSLOT;
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(empty + NSLOT);
 
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int32_t *it = p.items + blockIdx.x * 8;
+  const int warp = (threadIdx.x >> 5) - warp_base, lane = threadIdx.x & 31;
+  const int tid = threadIdx.x - warp_base * 32;   // 0 .. (NW + 1) * 32 - 1
+  const int32_t *it = p.items + item * 8;
   const int req = it[0], hk = it[1], pb = it[2], pe = it[3], n_splits = it[5];
   const int np = pe - pb;
   const int t = p.qo_indptr[req];
   const int kv = p.kv_len[req];
   const int32_t *table = p.bt + p.bt_indptr[req];
 
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < C::NSLOT; ++i) {
+  if (tid == 0) {
+    for (int i = 0; i < NSLOT; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], 1);
     }
     *abort_flag = 0;
     fence_mbar_init();
   }
-  __syncthreads();
+  named_bar_sync(bar_id, (NW + 1) * 32);
 
-  if (warp == C::NW) {
+  if (warp == NW) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       const size_t head_stride = static_cast<size_t>(16) * HD;
       int last_slot_issued = -1;
       for (int i = 0; i < np; ++i) {
-        const int slot = i % C::NSLOT;
-        if (i >= C::NSLOT &&
-            !mbar_wait(&empty[slot], ((i / C::NSLOT) - 1) & 1, abort_flag, p.err, kErrWaitProducer))
+        const int slot = i % NSLOT;
+        if (i >= NSLOT &&
+            !mbar_wait(&empty[slot], ((i / NSLOT) - 1) & 1, abort_flag, p.err, kErrWaitProducer))
           break;
         int page = table[pb + i];
         if (page < 0 || page >= p.num_pages) {
@@ -472,10 +467,10 @@ __global__ void __launch_bounds__(DecCfg<HD>::THREADS, 2) decode_attn_kernel(con
       // every issued copy is waited on by a consumer; if consumers gave up,
       // wait here (bounded) for the last copies to land
       if (*abort_flag) {
-        for (int i = (last_slot_issued - C::NSLOT + 1 > 0 ? last_slot_issued - C::NSLOT + 1 : 0);
+        for (int i = (last_slot_issued - NSLOT + 1 > 0 ? last_slot_issued - NSLOT + 1 : 0);
              i <= last_slot_issued; ++i) {
           const uint64_t t0 = globaltimer();
-          while (!mbar_try_wait(smem_u32(&full[i % C::NSLOT]), (i / C::NSLOT) & 1) &&
+          while (!mbar_try_wait(smem_u32(&full[i % NSLOT]), (i / NSLOT) & 1) &&
                  globaltimer() - t0 < kWaitLimitNs) {
           }
         }
@@ -506,9 +501,9 @@ __global__ void __launch_bounds__(DecCfg<HD>::THREADS, 2) decode_attn_kernel(con
 #pragma unroll
       for (int e = 0; e < 4; ++e) acc[g][e] = make_float2(0.f, 0.f);
     }
-    for (int i = warp; i < np; i += C::NW) {
-      const int slot = i % C::NSLOT;
-      if (!mbar_wait(&full[slot], (i / C::NSLOT) & 1, abort_flag, p.err, kErrWaitSoftmax)) break;
+    for (int i = warp; i < np; i += NW) {
+      const int slot = i % NSLOT;
+      if (!mbar_wait(&full[slot], (i / NSLOT) & 1, abort_flag, p.err, kErrWaitSoftmax)) break;
       const uint8_t *ks = ring + slot * C::SLOT_BYTES;
       const uint8_t *vs = ks + C::PAGE_BYTES;
       const int key_base = (pb + i) * 16;
@@ -604,7 +599,7 @@ __global__ void __launch_bounds__(DecCfg<HD>::THREADS, 2) decode_attn_kernel(con
     }
     // stash this warp's (m, l, o) for the CTA merge; the ring is free once
     // every consumer is past its last page (barrier below)
-    named_bar_sync(1, C::NW * 32);
+    named_bar_sync(bar_id + 1, NW * 32);
     float *stash = reinterpret_cast<float *>(ring) + warp * G * (HD + 2);
     if (kk == 0) {
 #pragma unroll
@@ -622,16 +617,16 @@ __global__ void __launch_bounds__(DecCfg<HD>::THREADS, 2) decode_attn_kernel(con
         stash[g * (HD + 2) + HD + 1] = l[g];
       }
     }
-    named_bar_sync(1, C::NW * 32);
+    named_bar_sync(bar_id + 1, NW * 32);
     const float *all = reinterpret_cast<const float *>(ring);
-    for (int idx = threadIdx.x; idx < G * HD; idx += C::NW * 32) {
+    for (int idx = tid; idx < G * HD; idx += NW * 32) {
       const int g = idx / HD, d = idx % HD;
       float M = -INFINITY;
 #pragma unroll
-      for (int w = 0; w < C::NW; ++w) M = fmaxf(M, all[(w * G + g) * (HD + 2) + HD]);
+      for (int w = 0; w < NW; ++w) M = fmaxf(M, all[(w * G + g) * (HD + 2) + HD]);
       float L = 0.f, O = 0.f;
 #pragma unroll
-      for (int w = 0; w < C::NW; ++w) {
+      for (int w = 0; w < NW; ++w) {
         const float* base = all + (w * G + g) * (HD + 2);
         const float wt = base[HD] == -INFINITY ? 0.f : exp2f(base[HD] - M);
         L += wt * base[HD + 1];
@@ -640,7 +635,7 @@ __global__ void __launch_bounds__(DecCfg<HD>::THREADS, 2) decode_attn_kernel(con
       if (n_splits == 1) {
         p.o[(static_cast<size_t>(t) * p.Hq + hk * G + g) * HD + d] = __float2bfloat16_rn(O / L);
       } else {
-        float *dst = p.part + (static_cast<size_t>(blockIdx.x) * G + g) * part_stride<HD>();
+        float *dst = p.part + (static_cast<size_t>(item) * G + g) * part_stride<HD>();
         dst[d] = O;
         if (d == 0) {
           dst[HD] = M;
@@ -684,52 +679,79 @@ __global__ void __launch_bounds__(128) merge_kernel(const float *part, const int
   for (int e = 0; e < PER; ++e) dst[e] = __float2bfloat16_rn(acc[e] * inv);
 }
 
+// ============================================================ one grid
+// The ragged attention of a step is ONE launch: blocks [0, n_tiles) run a
+// prefill-chunk tile (tensor cores), the rest run a decode item (HBM stream),
+// so the two kinds share the GPU instead of running back to back.  Tiles come
+// first, heaviest first; decode items fill SMs as they free up.  The decode
+// part uses 9 consumer warps and a ring carved from the tile's shared memory.
+template <int HD>
+struct FusedCfg {
+  static constexpr int THREADS = ChunkCfg<HD>::THREADS;          // 10 warps
+  static constexpr int DEC_NW = 4;                                // consumers per decode item
+  static constexpr int SMEM = ChunkCfg<HD>::SMEM;
+  // two decode items per CTA, each with half of the shared memory
+  static constexpr int HALF = ((SMEM - 1024) / 2) & ~1023;
+  static constexpr int NSLOT = ((HALF - 256) / DecCfg<HD>::SLOT_BYTES) < 16
+                                   ? ((HALF - 256) / DecCfg<HD>::SLOT_BYTES)
+                                   : 16;
+  static_assert(2 * (DEC_NW + 1) * 32 == THREADS, "two decode items fill the CTA");
+};
+
 template <int HD, int G>
-cudaError_t launch_decode(const DecodeParams &dp, cudaStream_t st) {
+__global__ void __launch_bounds__(FusedCfg<HD>::THREADS, 1)
+    attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmKV,
+                     const ChunkParams cp, const DecodeParams dp, int n_tiles) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  if (static_cast<int>(blockIdx.x) < n_tiles) {
+    chunk_tile<HD>(tmQ, tmKV, cp, blockIdx.x, smem_raw);
+  } else {
+    // warps 0-4 take item 2k, warps 5-9 item 2k + 1 (if it exists)
+    using F = FusedCfg<HD>;
+    const int half = threadIdx.x >= (F::DEC_NW + 1) * 32;
+    const int item = 2 * (blockIdx.x - n_tiles) + half;
+    if (item < dp.n_items)
+      decode_item<HD, G, F::DEC_NW, F::NSLOT>(dp, item, align1024(smem_raw) + half * F::HALF,
+                                              half * (F::DEC_NW + 1), 1 + 2 * half);
+  }
+}
+
+template <int HD, int G>
+cudaError_t launch_attention(const CUtensorMap &tq, const CUtensorMap &tkv, const ChunkParams &cp,
+                             const DecodeParams &dp, int n_tiles, int n_items, cudaStream_t st) {
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(decode_attn_kernel<HD, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    dec_smem<HD, G>());
+    attr_err = cudaFuncSetAttribute(attention_kernel<HD, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    FusedCfg<HD>::SMEM);
   });
   if (attr_err != cudaSuccess) return attr_err;
-  decode_attn_kernel<HD, G><<<dp.n_items, DecCfg<HD>::THREADS, dec_smem<HD, G>(), st>>>(dp);
+  attention_kernel<HD, G><<<n_tiles + (n_items + 1) / 2, FusedCfg<HD>::THREADS, FusedCfg<HD>::SMEM, st>>>(
+      tq, tkv, cp, dp, n_tiles);
   return cudaGetLastError();
 }
 
 template <int HD>
-cudaError_t launch_decode_g(const DecodeParams &dp, int G, cudaStream_t st) {
+cudaError_t launch_attention_g(const CUtensorMap &tq, const CUtensorMap &tkv, const ChunkParams &cp,
+                               const DecodeParams &dp, int n_tiles, int n_items, int G, cudaStream_t st) {
   switch (G) {
-    case 1: return launch_decode<HD, 1>(dp, st);
-    case 2: return launch_decode<HD, 2>(dp, st);
-    case 3: return launch_decode<HD, 3>(dp, st);
-    case 4: return launch_decode<HD, 4>(dp, st);
-    case 5: return launch_decode<HD, 5>(dp, st);
-    case 6: return launch_decode<HD, 6>(dp, st);
-    case 7: return launch_decode<HD, 7>(dp, st);
-    case 8: return launch_decode<HD, 8>(dp, st);
+    case 1: return launch_attention<HD, 1>(tq, tkv, cp, dp, n_tiles, n_items, st);
+    case 2: return launch_attention<HD, 2>(tq, tkv, cp, dp, n_tiles, n_items, st);
+    case 3: return launch_attention<HD, 3>(tq, tkv, cp, dp, n_tiles, n_items, st);
+    case 4: return launch_attention<HD, 4>(tq, tkv, cp, dp, n_tiles, n_items, st);
+    case 5: return launch_attention<HD, 5>(tq, tkv, cp, dp, n_tiles, n_items, st);
+    case 6: return launch_attention<HD, 6>(tq, tkv, cp, dp, n_tiles, n_items, st);
+    case 7: return launch_attention<HD, 7>(tq, tkv, cp, dp, n_tiles, n_items, st);
+    case 8: return launch_attention<HD, 8>(tq, tkv, cp, dp, n_tiles, n_items, st);
     default: return cudaErrorInvalidValue;
   }
 }
 
-template <int HD>
-cudaError_t launch_chunk(const CUtensorMap &tq, const CUtensorMap &tkv, const ChunkParams &cp, int n_tiles,
-                         cudaStream_t st) {
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(chunk_attn_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    ChunkCfg<HD>::SMEM);
-  });
-  if (attr_err != cudaSuccess) return attr_err;
-  chunk_attn_kernel<HD><<<n_tiles, ChunkCfg<HD>::THREADS, ChunkCfg<HD>::SMEM, st>>>(tq, tkv, cp);
-  return cudaGetLastError();
-}
-
 }  // namespace
 
-cudaError_t attn_chunk_run(const AttnArgs &a, cudaStream_t st) {
-  if (a.n_tiles <= 0) return cudaSuccess;
+cudaError_t attention_run(const AttnArgs &a, cudaStream_t st) {
+  if (a.n_tiles + a.n_items <= 0) return cudaSuccess;
+  const float scale_log2 = kLog2e / sqrtf(static_cast<float>(a.hd));
   ChunkParams cp;
   cp.o = static_cast<__nv_bfloat16 *>(a.o);
   cp.qo_indptr = a.qo_indptr;
@@ -740,14 +762,8 @@ cudaError_t attn_chunk_run(const AttnArgs &a, cudaStream_t st) {
   cp.Hq = a.Hq;
   cp.Hkv = a.Hkv;
   cp.num_pages = a.num_pages;
-  cp.scale_log2 = kLog2e / sqrtf(static_cast<float>(a.hd));
+  cp.scale_log2 = scale_log2;
   cp.err = a.err;
-  return a.hd == 128 ? launch_chunk<128>(*a.tm_q, *a.tm_kv, cp, a.n_tiles, st)
-                     : launch_chunk<64>(*a.tm_q, *a.tm_kv, cp, a.n_tiles, st);
-}
-
-cudaError_t attn_decode_run(const AttnArgs &a, cudaStream_t st) {
-  if (a.n_items <= 0) return cudaSuccess;
   DecodeParams dp;
   dp.q = static_cast<const __nv_bfloat16 *>(a.q);
   dp.pool = static_cast<const __nv_bfloat16 *>(a.pool);
@@ -762,10 +778,11 @@ cudaError_t attn_decode_run(const AttnArgs &a, cudaStream_t st) {
   dp.Hq = a.Hq;
   dp.Hkv = a.Hkv;
   dp.num_pages = a.num_pages;
-  dp.scale_log2 = kLog2e / sqrtf(static_cast<float>(a.hd));
+  dp.scale_log2 = scale_log2;
   dp.err = a.err;
   const int G = a.Hq / a.Hkv;
-  return a.hd == 128 ? launch_decode_g<128>(dp, G, st) : launch_decode_g<64>(dp, G, st);
+  return a.hd == 128 ? launch_attention_g<128>(*a.tm_q, *a.tm_kv, cp, dp, a.n_tiles, a.n_items, G, st)
+                     : launch_attention_g<64>(*a.tm_q, *a.tm_kv, cp, dp, a.n_tiles, a.n_items, G, st);
 }
 
 cudaError_t attn_merge_run(const MergeArgs &m, cudaStream_t st) {

@@ -71,8 +71,8 @@ struct AttnArgs {
   const CUtensorMap *tm_q;  // Q map [T][Hq hd], box 64 x 128 (host pointer; copied into launch)
   const CUtensorMap *tm_kv; // pool map [P*2*Hkv][16][hd], box 64 x 16 x 1
 };
-cudaError_t attn_chunk_run(const AttnArgs &a, cudaStream_t st);   // prefill-chunk tiles (tcgen05)
-cudaError_t attn_decode_run(const AttnArgs &a, cudaStream_t st);  // decode rows (split-KV)
+// Prefill-chunk tiles (tcgen05) and decode rows (split-KV) in one launch.
+cudaError_t attention_run(const AttnArgs &a, cudaStream_t st);
 
 struct MergeArgs {
   const float *part;
