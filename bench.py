@@ -281,6 +281,58 @@ def decode_only_attention(mb, torch, peaks, steps: int = 30) -> dict:
             "frac": round(gbs / peaks["hbm_gbs"], 4), "includes": "attention launch + merge"}
 
 
+def stack_step_time(mb, torch, wl, n_layers, steps: int = 10, warmup: int = 3, share_pool_bytes: float = 0.0,
+                    weights=None) -> dict:
+    """Device time of one step of an n_layers stack (one descriptor, CUDA
+    graph replay), L2 flushed between steps.  Weights and KV are drawn on the
+    device.  If the layers' KV would exceed `share_pool_bytes` (> 0), all
+    layers use one physical pool: timing-equivalent, since every layer's KV is
+    far larger than L2 and layers run one after another."""
+    sh = wl.shape
+    batch, num_pages = W.make_batch(wl.reqs, wl.seed + 1, spare_pages=4)
+    x = W.make_embeddings(batch.num_tokens, sh.d_model, wl.seed + 2)
+    pool_bytes = num_pages * 2 * sh.n_kv_heads * 16 * sh.head_dim * 2
+    shared = share_pool_bytes > 0 and pool_bytes * n_layers > share_pool_bytes
+    layers, keep = [], []
+    shared_pool = W.device_kv_pool(sh, num_pages, wl.seed + 200) if shared else None
+    for l in range(n_layers):
+        dw = weights[l] if weights is not None else W.device_weights(sh, wl.seed + 100 + l)
+        dpool = shared_pool if shared else W.device_kv_pool(sh, num_pages, wl.seed + 200 + l)
+        layers.append(mb.Layer(sh.as_dict(), dw, batch.num_tokens, num_pages, kv_buf=dpool))
+        keep.append((dw, dpool))
+    stack = mb.mb_stack_create([L.handle for L in layers], True)
+    cb = mb.Batch.of(batch)
+    dx = to_dev(x, torch)
+    dy = torch.empty_like(dx)
+    stream = torch.cuda.current_stream()
+    s = stream.cuda_stream
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    kvs = [L.kv for L in layers]
+    for _ in range(warmup):
+        mb.mb_stack_step(stack, kvs, cb, dx, dy, s)
+    e0 = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    e1 = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    torch.cuda.synchronize()
+    for i in range(steps):
+        flush.fill_(i & 0xFF)
+        e0[i].record(stream)
+        mb.mb_stack_step(stack, kvs, cb, dx, dy, s)
+        e1[i].record(stream)
+    torch.cuda.synchronize()
+    mb.mb_device_status(layers[0].handle, s)
+    ms = sum(a.elapsed_time(b) for a, b in zip(e0, e1)) / steps
+    launches = mb.mb_stack_last_launches(stack)
+    mb.mb_stack_destroy(stack)
+    for L in layers:
+        L.close()
+    del keep, shared_pool
+    torch.cuda.empty_cache()
+    T = batch.num_tokens
+    return {"workload": wl.name, "layers": n_layers, "tokens_per_step": T, "ms_per_step": round(ms, 4),
+            "tokens_per_s": round(T / (ms / 1e3), 1), "launches_per_step": launches,
+            "kv_pool": "one physical pool shared by all layers" if shared else "one pool per layer"}
+
+
 def to_dev(bits, torch):
     return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16).copy()).view(torch.bfloat16).cuda()
 
@@ -424,8 +476,12 @@ def run_mine(args, rank: int, world: int, local: int, pg):
                "sample": f"one oracle layer step over {nd} decode rows and {nc} chunk rows ({tok} tokens) of "
                          f"{wl.name}, float64 NumPy, {dt:.1f} s"}
 
-    # ---- decode rows alone (no chunk tiles in the grid)
+    # ---- decode rows alone (no chunk tiles in the grid), and the 40-layer stack
     dec_only = decode_only_attention(mb, torch, peaks) if rank == 0 and not args.no_aux else None
+    stack40 = None
+    if rank == 0 and not args.no_aux:
+        swl, nl = W.qwen3_14b_stack(prefix=30720)
+        stack40 = stack_step_time(mb, torch, swl, nl)
 
     # ---- P3 step-time model with GB300 peaks, as an analytic comparator
     from oracle import step_model as SM
@@ -460,6 +516,7 @@ def run_mine(args, rank: int, world: int, local: int, pg):
                  "frac_burst": round(gemm_flops / (gemm_ms / 1e3) / 1e12 / peaks["bf16_tflops"], 4),
                  "frac_sustained": round(gemm_flops / (gemm_ms / 1e3) / 1e12 / peaks["bf16_tflops_sustained"], 4)},
         "decode_attn": dec_only,
+        "stack_qwen3_14b_40": stack40,
         "roofline_step_ms": round(roof_ms, 5),
         "step_model_ms": round(model_ms, 5),
         "cpu_baseline": cpu,
@@ -473,6 +530,38 @@ def run_mine(args, rank: int, world: int, local: int, pg):
     print(json.dumps(line), flush=True)
 
 
+def run_sweep(args):
+    """Token budget C x decode batch b on the 32-layer Llama-3-8B-shaped stack
+    (compute/bandwidth crossover): tokens/s per point, with the pofe.ai step
+    model (GB300 peaks) beside each."""
+    import torch
+    from mixed_prefill_decode_gb300 import build as B
+    from mixed_prefill_decode_gb300 import binding as mb
+    from oracle import step_model as SM
+    B.build()
+    peaks, _ = load_peaks()
+    sh = W.LLAMA3_8B
+    weights = [W.device_weights(sh, 5100 + l) for l in range(32)]
+    n_params = 32 * (sh.qkv_dim * sh.d_model + sh.d_model * sh.n_q_heads * sh.head_dim + 3 * sh.d_ff * sh.d_model)
+    gb300 = SM.Machine(flops=peaks["bf16_tflops_sustained"] * 1e12, bandwidth=peaks["hbm_gbs"] * 1e9, t_iter=0.0)
+    model = SM.Model(n_params=n_params, kappa=32 * sh.kv_bytes_per_token, d_model=sh.d_model, n_layers=32)
+    free_budget = torch.cuda.mem_get_info()[0] - (24 << 30)
+    for C in (256, 512, 1024, 2048, 4096, 8192):
+        for b in (1, 16, 64, 256):
+            if C <= b:
+                continue
+            wl, nl = W.llama3_8b_stack(C, b)
+            r = stack_step_time(mb, torch, wl, nl, steps=5, warmup=2, share_pool_bytes=free_budget,
+                                weights=weights)
+            qo = np.array([q for _, q in wl.reqs])
+            cs = np.array([c for c, _ in wl.reqs])
+            chunks = [(int(q), int(c)) for c, q in wl.reqs if q > 1]
+            decs = [int(c) for c, q in wl.reqs if q == 1]
+            r.update({"budget": C, "decodes": b,
+                      "step_model_ms": round(SM.iteration_time(gb300, model, chunks, decs) * 1e3, 4)})
+            print(json.dumps(r), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -481,11 +570,16 @@ def main():
     ap.add_argument("--impl", choices=["mine", "reference"], default="mine")
     ap.add_argument("--workload", default="llama3_8b_T576")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-aux", action="store_true", help="skip the decode-only attention measurement")
+    ap.add_argument("--no-aux", action="store_true", help="skip the decode-only and 40-layer stack measurements")
+    ap.add_argument("--sweep", action="store_true",
+                    help="token-budget sweep on the 32-layer Llama-3-8B stack: one JSON line per point")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
     rank, world, local, pg = dist_setup()
+    if args.sweep:
+        run_sweep(args)
+        return
     if args.impl == "reference":
         run_reference(args, rank, world)
     else:

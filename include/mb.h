@@ -140,6 +140,30 @@ mb_status mb_kv_free(mb_kv *kv);
 mb_status mb_step(mb_layer *layer, mb_kv *kv, const mb_batch *batch, const void *x_in,
                   void *x_out, void *stream);
 
+/* ---------------- stacks (several layers, one descriptor per step) ---------
+ * A model is L layers applied in turn to the same mixed batch; every layer
+ * has its own weights and KV pool, and the batch descriptor is the same for
+ * all of them.  A stack uploads the descriptor and builds the work lists once
+ * per step and runs the L layers back to back on `stream`, with activations
+ * ping-ponging between two library-owned buffers.  All layers must share the
+ * model shape, max_tokens and device; they also share the first layer's
+ * workspaces, so the layers of a stack must not be stepped concurrently on
+ * their own.  With use_graphs != 0 the L layers' launches are captured once
+ * into a CUDA graph per batch geometry (T, work-list sizes, buffers) and
+ * replayed (the same geometry recurs across steps of a fixed batch shape; the
+ * descriptor's contents may change).  Capture happens inside mb_stack_step,
+ * so `stream` must not already be capturing.  layers: host array of n_layers
+ * handles (not owned).  Errors: MB_EINVAL, MB_ENOMEM, MB_ECUDA. */
+typedef struct mb_stack mb_stack;
+mb_status mb_stack_create(mb_layer *const *layers, int32_t n_layers, int32_t use_graphs, mb_stack **out);
+/* One step of all layers: kvs is a host array of the n_layers pools (pool i
+ * belongs to layer i); x_in / x_out device bf16 [T][d_model], not aliased.
+ * The descriptor is checked against the smallest pool. */
+mb_status mb_stack_step(mb_stack *stack, mb_kv *const *kvs, const mb_batch *batch, const void *x_in,
+                        void *x_out, void *stream);
+int32_t mb_stack_last_launches(const mb_stack *stack);
+mb_status mb_stack_destroy(mb_stack *stack);
+
 /* Check a batch descriptor against the rules above, on the host only (no
  * device work; usable without a GPU).  num_pages: pool size; max_tokens: the
  * layer's limit on T.  Errors: MB_EINVAL with a message naming the first

@@ -82,6 +82,10 @@ _SIGS = {
     "mb_gemm": (_I32, [_VP, _VP, _VP, _VP, _I32, _I32, _I32, _I32, _VP, _VP]),
     "mb_gemm_workspace_bytes": (_I64, []),
     "mb_gemm_noalloc": (_I32, [_VP, _VP, _VP, _VP, _I32, _I32, _I32, _I32, _VP]),
+    "mb_stack_create": (_I32, [ctypes.POINTER(_VP), _I32, _I32, ctypes.POINTER(_VP)]),
+    "mb_stack_step": (_I32, [_VP, ctypes.POINTER(_VP), ctypes.POINTER(mb_batch), _VP, _VP, _VP]),
+    "mb_stack_last_launches": (_I32, [_VP]),
+    "mb_stack_destroy": (_I32, [_VP]),
     "mb_sched_create": (_I32, [ctypes.POINTER(mb_pack_cfg), _I32, c_int32_p, ctypes.POINTER(_VP)]),
     "mb_sched_add": (_I32, [_VP, _I64, _I32, _I32]),
     "mb_sched_pack": (_I32, [_VP, ctypes.POINTER(mb_sched_batch)]),
@@ -233,6 +237,27 @@ def mb_gemm_noalloc(A, B, D, R, M: int, N: int, K: int, epilogue: int, stream=No
 
 def mb_gemm_workspace_bytes() -> int:
     return int(lib().mb_gemm_workspace_bytes())
+
+
+# ----------------------------------------------------------------- stack
+def mb_stack_create(layers: Sequence[int], use_graphs: bool = True) -> int:
+    arr = (_VP * len(layers))(*layers)
+    h = _VP()
+    _check(lib().mb_stack_create(arr, len(layers), 1 if use_graphs else 0, ctypes.byref(h)))
+    return h.value
+
+
+def mb_stack_step(stack: int, kvs: Sequence[int], batch: Batch, x_in, x_out, stream=None) -> None:
+    arr = (_VP * len(kvs))(*kvs)
+    _check(lib().mb_stack_step(stack, arr, ctypes.byref(batch.c), _ptr(x_in), _ptr(x_out), _ptr(stream)))
+
+
+def mb_stack_last_launches(stack: int) -> int:
+    return int(lib().mb_stack_last_launches(stack))
+
+
+def mb_stack_destroy(stack: int) -> None:
+    _check(lib().mb_stack_destroy(stack))
 
 
 # ------------------------------------------------------------- scheduler

@@ -201,6 +201,41 @@ struct mb_layer {
   std::vector<int32_t> hbuf;
 };
 
+
+// A stack of layers that share one batch descriptor per step.
+struct GraphKey {
+  int64_t T;
+  int n_tiles, n_items, n_merge;
+  const void *db, *part, *x_in, *x_out, *kv0;
+  bool operator==(const GraphKey &o) const {
+    return T == o.T && n_tiles == o.n_tiles && n_items == o.n_items && n_merge == o.n_merge && db == o.db &&
+           part == o.part && x_in == o.x_in && x_out == o.x_out && kv0 == o.kv0;
+  }
+};
+
+struct mb_stack {
+  std::vector<mb_layer *> layers;
+  void *act[2] = {nullptr, nullptr};  // ping-pong activations between layers
+  std::vector<uint32_t> stamp;
+  uint32_t stamp_gen = 0;
+  bool use_graphs = true;
+  struct Entry {
+    GraphKey key;
+    cudaGraphExec_t exec;
+    int launches;
+  };
+  std::vector<Entry> graphs;
+  std::vector<mb_kv *> graph_kvs;
+  cudaStream_t cap_stream = nullptr;
+  int32_t last_launches = 0;
+  int32_t last_T = 0;
+  void drop_graphs() {
+    for (auto &g : graphs) cudaGraphExecDestroy(g.exec);
+    graphs.clear();
+    graph_kvs.clear();
+  }
+};
+
 namespace {
 
 mb_status alloc_dev(void **p, size_t bytes, const char *what) {
@@ -277,6 +312,273 @@ mb_status validate_batch(const mb_batch *b, int32_t num_pages, int32_t max_token
   *T_out = T;
   return MB_OK;
 }
+
+
+// Device-side plan of one step: where the descriptor, per-token tables and
+// work lists live in the uploaded blob, and their sizes.
+struct StepPlan {
+  int64_t T = 0;
+  size_t o_qo = 0, o_kv = 0, o_bti = 0, o_bt = 0, o_treq = 0, o_tpos = 0, o_tiles = 0, o_items = 0, o_merge = 0;
+  int n_tiles = 0, n_items = 0, n_merge = 0;
+  const int32_t *db = nullptr;
+  int64_t upload_bytes = 0;
+};
+
+// Host part of a step: per-token tables, attention work lists (chunk tiles,
+// decode splits, merge list), one upload through `L`'s pinned ring into its
+// device blob.  The batch has been validated.
+mb_status prepare_step(mb_layer *L, const mb_batch *b, int64_t T, cudaStream_t s, StepPlan *plan) {
+  mb::DeviceCtx *ctx = nullptr;
+  mb_status st = mb::device_ctx(&ctx);
+  if (st != MB_OK) return st;
+  const mb_layer_desc &d = L->d;
+  const int n = b->num_reqs;
+  const int Hq = d.n_q_heads, Hkv = d.n_kv_heads, hd = d.head_dim, G = Hq / Hkv;
+  const int64_t nb = b->bt_indptr[n];
+  std::vector<int32_t> &hb = L->hbuf;
+  hb.clear();
+  auto sec = [&](size_t count) {
+    size_t off = hb.size();
+    hb.resize(off + ((count + 3) & ~size_t(3)), 0);
+    return off;
+  };
+  StepPlan &P = *plan;
+  P.T = T;
+  P.o_qo = sec(n + 1);
+  P.o_kv = sec(n);
+  P.o_bti = sec(n + 1);
+  P.o_bt = sec(static_cast<size_t>(nb));
+  P.o_treq = sec(T);
+  P.o_tpos = sec(T);
+  std::copy(b->qo_indptr, b->qo_indptr + n + 1, hb.begin() + P.o_qo);
+  std::copy(b->kv_len, b->kv_len + n, hb.begin() + P.o_kv);
+  std::copy(b->bt_indptr, b->bt_indptr + n + 1, hb.begin() + P.o_bti);
+  std::copy(b->bt, b->bt + nb, hb.begin() + P.o_bt);
+  for (int r = 0; r < n; ++r) {
+    const int32_t t0 = b->qo_indptr[r], t1 = b->qo_indptr[r + 1];
+    const int32_t c = b->kv_len[r] - (t1 - t0);
+    for (int32_t t = t0; t1 > t; ++t) {
+      hb[P.o_treq + t] = r;
+      hb[P.o_tpos + t] = c + (t - t0);
+    }
+  }
+  // chunk tiles, heaviest first (rows x visible keys)
+  struct Tile {
+    int32_t r, i0, h;
+    int64_t work;
+  };
+  std::vector<Tile> tiles;
+  int64_t dec_pages = 0;
+  for (int r = 0; r < n; ++r) {
+    const int32_t qo = b->qo_indptr[r + 1] - b->qo_indptr[r];
+    if (qo > 1) {
+      const int32_t c = b->kv_len[r] - qo;
+      for (int32_t i0 = 0; i0 < qo; i0 += 128)
+        for (int32_t hh = 0; hh < Hq; ++hh) tiles.push_back({r, i0, hh, static_cast<int64_t>(c + i0 + 128)});
+    } else {
+      dec_pages += pages_for(b->kv_len[r]);
+    }
+  }
+  std::stable_sort(tiles.begin(), tiles.end(), [](const Tile &x, const Tile &y) { return x.work > y.work; });
+  P.o_tiles = sec(tiles.size() * 4);
+  for (size_t i = 0; i < tiles.size(); ++i) {
+    hb[P.o_tiles + 4 * i + 0] = tiles[i].r;
+    hb[P.o_tiles + 4 * i + 1] = tiles[i].i0;
+    hb[P.o_tiles + 4 * i + 2] = tiles[i].h;
+  }
+  // decode splits: about four items per SM (two per resident CTA of the
+  // attention grid), each request's pages divided evenly among its splits
+  const int64_t target_items = static_cast<int64_t>(ctx->sms) * 4;
+  int64_t pps = (dec_pages * Hkv + target_items - 1) / std::max<int64_t>(1, target_items);
+  pps = std::max<int64_t>(pps, 8);
+  std::vector<int32_t> items, merges;
+  for (int r = 0; r < n; ++r) {
+    const int32_t qo = b->qo_indptr[r + 1] - b->qo_indptr[r];
+    if (qo != 1) continue;
+    const int32_t np = pages_for(b->kv_len[r]);
+    const int32_t ns = static_cast<int32_t>(std::max<int64_t>(1, (np + pps / 2) / pps));
+    for (int32_t hk = 0; hk < Hkv; ++hk) {
+      const int32_t first = static_cast<int32_t>(items.size() / 8);
+      for (int32_t sidx = 0; sidx < ns; ++sidx) {
+        const int32_t pb = static_cast<int32_t>(static_cast<int64_t>(np) * sidx / ns);
+        const int32_t pe = static_cast<int32_t>(static_cast<int64_t>(np) * (sidx + 1) / ns);
+        items.insert(items.end(), {r, hk, pb, pe, sidx, ns, 0, 0});
+      }
+      if (ns > 1) merges.insert(merges.end(), {r, hk, first, ns});
+    }
+  }
+  P.o_items = sec(items.size());
+  P.o_merge = sec(merges.size());
+  std::copy(items.begin(), items.end(), hb.begin() + P.o_items);
+  std::copy(merges.begin(), merges.end(), hb.begin() + P.o_merge);
+  P.n_tiles = static_cast<int>(tiles.size());
+  P.n_items = static_cast<int>(items.size() / 8);
+  P.n_merge = static_cast<int>(merges.size() / 4);
+
+  // ---- upload through a pinned ring slot
+  StagingSlot &slot = L->ring[L->ring_next];
+  L->ring_next = (L->ring_next + 1) % kRing;
+  cudaError_t e;
+  if (slot.used) {
+    e = cudaEventSynchronize(slot.done);
+    if (e != cudaSuccess) return mb::fail(MB_ECUDA, "step: %s", cudaGetErrorString(e));
+  }
+  if (slot.cap < hb.size()) {
+    if (slot.host) cudaFreeHost(slot.host);
+    slot.host = nullptr;
+    size_t cap = std::max<size_t>(hb.size() * 2, 4096);
+    e = cudaHostAlloc(reinterpret_cast<void **>(&slot.host), cap * 4, cudaHostAllocDefault);
+    if (e != cudaSuccess) {
+      slot.cap = 0;
+      return mb::fail(MB_ENOMEM, "step: cudaHostAlloc: %s", cudaGetErrorString(e));
+    }
+    slot.cap = cap;
+  }
+  if (L->dblob_cap < hb.size()) {
+    cudaStreamSynchronize(s);
+    if (L->dblob) cudaFree(L->dblob);
+    L->dblob = nullptr;
+    size_t cap = std::max<size_t>(hb.size() * 2, 4096);
+    st = alloc_dev(reinterpret_cast<void **>(&L->dblob), cap * 4, "descriptor");
+    if (st != MB_OK) {
+      L->dblob_cap = 0;
+      return st;
+    }
+    L->dblob_cap = cap;
+  }
+  const size_t part_need = static_cast<size_t>(P.n_items) * G * (hd + 4);  // rows of hd + 4 floats
+  if (L->part_cap < part_need) {
+    cudaStreamSynchronize(s);
+    if (L->part) cudaFree(L->part);
+    L->part = nullptr;
+    size_t cap = part_need * 2;
+    st = alloc_dev(reinterpret_cast<void **>(&L->part), cap * 4, "decode partials");
+    if (st != MB_OK) {
+      L->part_cap = 0;
+      return st;
+    }
+    L->part_cap = cap;
+  }
+  std::memcpy(slot.host, hb.data(), hb.size() * 4);
+  e = cudaMemcpyAsync(L->dblob, slot.host, hb.size() * 4, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return mb::fail(MB_ECUDA, "step: descriptor upload: %s", cudaGetErrorString(e));
+  e = cudaEventRecord(slot.done, s);
+  if (e != cudaSuccess) return mb::fail(MB_ECUDA, "step: %s", cudaGetErrorString(e));
+  slot.used = true;
+  P.db = L->dblob;
+  P.upload_bytes = static_cast<int64_t>(hb.size()) * 4;
+  return MB_OK;
+}
+
+// The launches of one layer: weights and tensor maps of `L`, workspaces of
+// `W` (the layer itself, or the first layer of a stack), KV pool `kv`.
+mb_status launch_layer(mb_layer *L, mb_layer *W, mb_kv *kv, const StepPlan &P, const void *x_in, void *x_out,
+                       cudaStream_t s, EventSet *es, int *launches) {
+  const mb_layer_desc &d = L->d;
+  const int Hq = d.n_q_heads, Hkv = d.n_kv_heads, hd = d.head_dim;
+  const int Ti = static_cast<int>(P.T);
+  const int hqd = Hq * hd;
+  const int32_t *db = P.db;
+  auto mark = [&](int k) {
+    if (es) cudaEventRecord(es->ev[k], s);
+  };
+  auto chk = [&](cudaError_t err, const char *what) -> mb_status {
+    if (err != cudaSuccess) return mb::fail(MB_ECUDA, "step: %s: %s", what, cudaGetErrorString(err));
+    return MB_OK;
+  };
+  mb_status st;
+  mark(0);
+  if ((st = chk(mb::rmsnorm_run(x_in, L->w.g_attn, W->xn, Ti, d.d_model, d.rms_eps, s), "rmsnorm")) != MB_OK) return st;
+  ++*launches;
+  mark(1);
+  if ((st = chk(mb::gemm_run(W->xn, L->w.w_qkv, &L->tm_wqkv, W->qkv, nullptr, Ti, L->qkv_dim, d.d_model,
+                             mb::kEpiStore, W->gws, W->err, s), "gemm qkv")) != MB_OK)
+    return st;
+  ++*launches;
+  mark(2);
+  mb::RopeArgs ra;
+  ra.qkv = W->qkv;
+  ra.q_out = W->q;
+  ra.pool = kv->base;
+  ra.tok_req = db + P.o_treq;
+  ra.tok_pos = db + P.o_tpos;
+  ra.bt_indptr = db + P.o_bti;
+  ra.bt = db + P.o_bt;
+  ra.g_q = L->w.g_q;
+  ra.g_k = L->w.g_k;
+  ra.T = Ti;
+  ra.Hq = Hq;
+  ra.Hkv = Hkv;
+  ra.hd = hd;
+  ra.qk_norm = d.qk_norm;
+  ra.num_pages = kv->num_pages;
+  ra.eps = d.rms_eps;
+  ra.theta = d.rope_theta;
+  ra.err = W->err;
+  if ((st = chk(mb::rope_append_run(ra, s), "rope/append")) != MB_OK) return st;
+  ++*launches;
+  mark(3);
+  CUtensorMap tm_q;
+  cudaError_t e = mb::encode_tmap_2d(&tm_q, W->q, hqd, Ti, hqd * 2ull, 64, 128);
+  if (e != cudaSuccess) return mb::fail(MB_ECUDA, "step: Q tensor map");
+  mb::AttnArgs aa;
+  aa.q = W->q;
+  aa.pool = kv->base;
+  aa.o = W->o;
+  aa.qo_indptr = db + P.o_qo;
+  aa.kv_len = db + P.o_kv;
+  aa.bt_indptr = db + P.o_bti;
+  aa.bt = db + P.o_bt;
+  aa.tiles = db + P.o_tiles;
+  aa.items = db + P.o_items;
+  aa.part = W->part;
+  aa.n_tiles = P.n_tiles;
+  aa.n_items = P.n_items;
+  aa.T = Ti;
+  aa.Hq = Hq;
+  aa.Hkv = Hkv;
+  aa.hd = hd;
+  aa.num_pages = kv->num_pages;
+  aa.err = W->err;
+  aa.tm_q = &tm_q;
+  aa.tm_kv = &kv->tmap;
+  if ((st = chk(mb::attention_run(aa, s), "attention")) != MB_OK) return st;
+  *launches += (aa.n_tiles + aa.n_items) > 0;
+  mark(4);
+  mb::MergeArgs ma;
+  ma.part = W->part;
+  ma.merge_list = db + P.o_merge;
+  ma.n_merge = P.n_merge;
+  ma.o = W->o;
+  ma.qo_indptr = db + P.o_qo;
+  ma.Hq = Hq;
+  ma.Hkv = Hkv;
+  ma.hd = hd;
+  if ((st = chk(mb::attn_merge_run(ma, s), "merge")) != MB_OK) return st;
+  *launches += P.n_merge > 0;
+  mark(5);
+  if ((st = chk(mb::gemm_run(W->o, L->w.w_o, &L->tm_wo, W->h, x_in, Ti, d.d_model, hqd, mb::kEpiResidual, W->gws,
+                             W->err, s), "gemm o")) != MB_OK)
+    return st;
+  ++*launches;
+  mark(6);
+  if ((st = chk(mb::rmsnorm_run(W->h, L->w.g_ffn, W->hn, Ti, d.d_model, d.rms_eps, s), "rmsnorm ffn")) != MB_OK)
+    return st;
+  ++*launches;
+  mark(7);
+  if ((st = chk(mb::gemm_run(W->hn, L->w.w_gate_up, &L->tm_wgu, W->a, nullptr, Ti, d.d_ff, d.d_model,
+                             mb::kEpiSwiGLU, W->gws, W->err, s), "gemm gate/up")) != MB_OK)
+    return st;
+  ++*launches;
+  mark(8);
+  if ((st = chk(mb::gemm_run(W->a, L->w.w_down, &L->tm_wd, x_out, W->h, Ti, d.d_model, d.d_ff, mb::kEpiResidual,
+                             W->gws, W->err, s), "gemm down")) != MB_OK)
+    return st;
+  ++*launches;
+  mark(9);
+  return MB_OK;
+}
+
 
 }  // namespace
 
@@ -528,165 +830,25 @@ mb_status mb_step(mb_layer *L, mb_kv *kv, const mb_batch *b, const void *x_in, v
   if (x_in == x_out) return fail(MB_EINVAL, "mb_step: x_out must not alias x_in");
   if (reinterpret_cast<uintptr_t>(x_in) % 16 || reinterpret_cast<uintptr_t>(x_out) % 16)
     return fail(MB_EINVAL, "mb_step: x_in and x_out must be 16-byte aligned");
-  const int n = b->num_reqs;
-  if (n < 0) return fail(MB_EINVAL, "mb_step: num_reqs < 0");
+  if (b->num_reqs < 0) return fail(MB_EINVAL, "mb_step: num_reqs < 0");
   L->last_launches = 0;
-  if (n == 0) {
+  if (b->num_reqs == 0) {
     L->last_T = 0;
     return MB_OK;
   }
-  if (!b->qo_indptr || !b->kv_len || !b->bt_indptr || !b->bt) return fail(MB_EINVAL, "mb_step: null descriptor array");
-  const mb_layer_desc &d = L->d;
-  // ---- validate the descriptor
   if (++kv->stamp_gen == 0) {
     std::fill(kv->stamp.begin(), kv->stamp.end(), 0u);
     kv->stamp_gen = 1;
   }
   int64_t T = 0;
-  {
-    mb_status vst = validate_batch(b, kv->num_pages, d.max_tokens, kv->stamp.data(), kv->stamp_gen, &T);
-    if (vst != MB_OK) return vst;
-  }
-
-  mb::DeviceCtx *ctx = nullptr;
-  mb_status st = mb::device_ctx(&ctx);
+  mb_status st = validate_batch(b, kv->num_pages, L->d.max_tokens, kv->stamp.data(), kv->stamp_gen, &T);
   if (st != MB_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-
-  // ---- work lists
-  const int Hq = d.n_q_heads, Hkv = d.n_kv_heads, hd = d.head_dim, G = Hq / Hkv;
-  int64_t nb = b->bt_indptr[n];
-  std::vector<int32_t> &hb = L->hbuf;
-  hb.clear();
-  auto sec = [&](size_t count) {
-    size_t off = hb.size();
-    hb.resize(off + ((count + 3) & ~size_t(3)), 0);
-    return off;
-  };
-  const size_t o_qo = sec(n + 1), o_kv = sec(n), o_bti = sec(n + 1), o_bt = sec(static_cast<size_t>(nb));
-  const size_t o_treq = sec(T), o_tpos = sec(T);
-  std::copy(b->qo_indptr, b->qo_indptr + n + 1, hb.begin() + o_qo);
-  std::copy(b->kv_len, b->kv_len + n, hb.begin() + o_kv);
-  std::copy(b->bt_indptr, b->bt_indptr + n + 1, hb.begin() + o_bti);
-  std::copy(b->bt, b->bt + nb, hb.begin() + o_bt);
-  for (int r = 0; r < n; ++r) {
-    const int32_t t0 = b->qo_indptr[r], t1 = b->qo_indptr[r + 1];
-    const int32_t c = b->kv_len[r] - (t1 - t0);
-    for (int32_t t = t0; t1 > t; ++t) {
-      hb[o_treq + t] = r;
-      hb[o_tpos + t] = c + (t - t0);
-    }
-  }
-  // chunk tiles, heaviest first (rows x visible keys)
-  struct Tile {
-    int32_t r, i0, h;
-    int64_t work;
-  };
-  std::vector<Tile> tiles;
-  int64_t dec_pages = 0;
-  for (int r = 0; r < n; ++r) {
-    const int32_t qo = b->qo_indptr[r + 1] - b->qo_indptr[r];
-    if (qo > 1) {
-      const int32_t c = b->kv_len[r] - qo;
-      for (int32_t i0 = 0; i0 < qo; i0 += 128)
-        for (int32_t hh = 0; hh < Hq; ++hh) tiles.push_back({r, i0, hh, static_cast<int64_t>(c + i0 + 128)});
-    } else {
-      dec_pages += pages_for(b->kv_len[r]);
-    }
-  }
-  std::stable_sort(tiles.begin(), tiles.end(), [](const Tile &x, const Tile &y) { return x.work > y.work; });
-  const size_t o_tiles = sec(tiles.size() * 4);
-  for (size_t i = 0; i < tiles.size(); ++i) {
-    hb[o_tiles + 4 * i + 0] = tiles[i].r;
-    hb[o_tiles + 4 * i + 1] = tiles[i].i0;
-    hb[o_tiles + 4 * i + 2] = tiles[i].h;
-  }
-  // decode splits: about four items per SM (two per resident CTA of the
-  // attention grid), each request's pages divided evenly among its splits
-  const int64_t target_items = static_cast<int64_t>(ctx->sms) * 4;
-  int64_t pps = (dec_pages * Hkv + target_items - 1) / std::max<int64_t>(1, target_items);
-  pps = std::max<int64_t>(pps, 8);
-  std::vector<int32_t> items, merges;
-  for (int r = 0; r < n; ++r) {
-    const int32_t qo = b->qo_indptr[r + 1] - b->qo_indptr[r];
-    if (qo != 1) continue;
-    const int32_t np = pages_for(b->kv_len[r]);
-    const int32_t ns = static_cast<int32_t>(std::max<int64_t>(1, (np + pps / 2) / pps));
-    for (int32_t hk = 0; hk < Hkv; ++hk) {
-      const int32_t first = static_cast<int32_t>(items.size() / 8);
-      for (int32_t sidx = 0; sidx < ns; ++sidx) {
-        const int32_t pb = static_cast<int32_t>(static_cast<int64_t>(np) * sidx / ns);
-        const int32_t pe = static_cast<int32_t>(static_cast<int64_t>(np) * (sidx + 1) / ns);
-        items.insert(items.end(), {r, hk, pb, pe, sidx, ns, 0, 0});
-      }
-      if (ns > 1) merges.insert(merges.end(), {r, hk, first, ns});
-    }
-  }
-  const size_t o_items = sec(items.size()), o_merge = sec(merges.size());
-  std::copy(items.begin(), items.end(), hb.begin() + o_items);
-  std::copy(merges.begin(), merges.end(), hb.begin() + o_merge);
-  const int n_items = static_cast<int>(items.size() / 8);
-  const int n_merge = static_cast<int>(merges.size() / 4);
-
-  // ---- upload through a pinned ring slot
-  StagingSlot &slot = L->ring[L->ring_next];
-  L->ring_next = (L->ring_next + 1) % kRing;
-  cudaError_t e;
-  if (slot.used) {
-    e = cudaEventSynchronize(slot.done);
-    if (e != cudaSuccess) return mb::fail(MB_ECUDA, "mb_step: %s", cudaGetErrorString(e));
-  }
-  if (slot.cap < hb.size()) {
-    if (slot.host) cudaFreeHost(slot.host);
-    slot.host = nullptr;
-    size_t cap = std::max<size_t>(hb.size() * 2, 4096);
-    e = cudaHostAlloc(reinterpret_cast<void **>(&slot.host), cap * 4, cudaHostAllocDefault);
-    if (e != cudaSuccess) {
-      slot.cap = 0;
-      return mb::fail(MB_ENOMEM, "mb_step: cudaHostAlloc: %s", cudaGetErrorString(e));
-    }
-    slot.cap = cap;
-  }
-  if (L->dblob_cap < hb.size()) {
-    cudaStreamSynchronize(s);
-    if (L->dblob) cudaFree(L->dblob);
-    L->dblob = nullptr;
-    size_t cap = std::max<size_t>(hb.size() * 2, 4096);
-    st = alloc_dev(reinterpret_cast<void **>(&L->dblob), cap * 4, "descriptor");
-    if (st != MB_OK) {
-      L->dblob_cap = 0;
-      return st;
-    }
-    L->dblob_cap = cap;
-  }
-  const size_t part_need = static_cast<size_t>(n_items) * G * (hd + 4);  // rows of hd + 4 floats
-  if (L->part_cap < part_need) {
-    cudaStreamSynchronize(s);
-    if (L->part) cudaFree(L->part);
-    L->part = nullptr;
-    size_t cap = part_need * 2;
-    st = alloc_dev(reinterpret_cast<void **>(&L->part), cap * 4, "decode partials");
-    if (st != MB_OK) {
-      L->part_cap = 0;
-      return st;
-    }
-    L->part_cap = cap;
-  }
-  std::memcpy(slot.host, hb.data(), hb.size() * 4);
-  e = cudaMemcpyAsync(L->dblob, slot.host, hb.size() * 4, cudaMemcpyHostToDevice, s);
-  if (e != cudaSuccess) return mb::fail(MB_ECUDA, "mb_step: descriptor upload: %s", cudaGetErrorString(e));
-  e = cudaEventRecord(slot.done, s);
-  if (e != cudaSuccess) return mb::fail(MB_ECUDA, "mb_step: %s", cudaGetErrorString(e));
-  slot.used = true;
-  const int32_t *db = L->dblob;
-
-  // ---- timing events
+  StepPlan plan;
+  if ((st = prepare_step(L, b, T, s, &plan)) != MB_OK) return st;
   EventSet *es = nullptr;
   if (L->timing) {
-    if (L->ev_used == 4096) {
-      st = flush_timing(L);
-      if (st != MB_OK) return st;
-    }
+    if (L->ev_used == 4096 && (st = flush_timing(L)) != MB_OK) return st;
     if (L->ev_used == L->ev_pool.size()) {
       EventSet ns;
       for (auto &ev : ns.ev) cudaEventCreate(&ev);
@@ -694,110 +856,143 @@ mb_status mb_step(mb_layer *L, mb_kv *kv, const mb_batch *b, const void *x_in, v
     }
     es = &L->ev_pool[L->ev_used++];
   }
-  auto mark = [&](int k) {
-    if (es) cudaEventRecord(es->ev[k], s);
-  };
-
-  // ---- launches
-  const int Ti = static_cast<int>(T);
-  const int hqd = Hq * hd;
   int launches = 0;
-  auto chk = [&](cudaError_t err, const char *what) -> mb_status {
-    if (err != cudaSuccess) return mb::fail(MB_ECUDA, "mb_step: %s: %s", what, cudaGetErrorString(err));
-    return MB_OK;
-  };
-  mark(0);
-  if ((st = chk(mb::rmsnorm_run(x_in, L->w.g_attn, L->xn, Ti, d.d_model, d.rms_eps, s), "rmsnorm")) != MB_OK) return st;
-  ++launches;
-  mark(1);
-  if ((st = chk(mb::gemm_run(L->xn, L->w.w_qkv, &L->tm_wqkv, L->qkv, nullptr, Ti, L->qkv_dim, d.d_model, mb::kEpiStore,
-                             L->gws, L->err, s), "gemm qkv")) != MB_OK)
-    return st;
-  ++launches;
-  mark(2);
-  mb::RopeArgs ra;
-  ra.qkv = L->qkv;
-  ra.q_out = L->q;
-  ra.pool = kv->base;
-  ra.tok_req = db + o_treq;
-  ra.tok_pos = db + o_tpos;
-  ra.bt_indptr = db + o_bti;
-  ra.bt = db + o_bt;
-  ra.g_q = L->w.g_q;
-  ra.g_k = L->w.g_k;
-  ra.T = Ti;
-  ra.Hq = Hq;
-  ra.Hkv = Hkv;
-  ra.hd = hd;
-  ra.qk_norm = d.qk_norm;
-  ra.num_pages = kv->num_pages;
-  ra.eps = d.rms_eps;
-  ra.theta = d.rope_theta;
-  ra.err = L->err;
-  if ((st = chk(mb::rope_append_run(ra, s), "rope/append")) != MB_OK) return st;
-  ++launches;
-  mark(3);
-  CUtensorMap tm_q;
-  e = mb::encode_tmap_2d(&tm_q, L->q, hqd, Ti, hqd * 2ull, 64, 128);
-  if (e != cudaSuccess) return mb::fail(MB_ECUDA, "mb_step: Q tensor map");
-  mb::AttnArgs aa;
-  aa.q = L->q;
-  aa.pool = kv->base;
-  aa.o = L->o;
-  aa.qo_indptr = db + o_qo;
-  aa.kv_len = db + o_kv;
-  aa.bt_indptr = db + o_bti;
-  aa.bt = db + o_bt;
-  aa.tiles = db + o_tiles;
-  aa.items = db + o_items;
-  aa.part = L->part;
-  aa.n_tiles = static_cast<int>(tiles.size());
-  aa.n_items = n_items;
-  aa.T = Ti;
-  aa.Hq = Hq;
-  aa.Hkv = Hkv;
-  aa.hd = hd;
-  aa.num_pages = kv->num_pages;
-  aa.err = L->err;
-  aa.tm_q = &tm_q;
-  aa.tm_kv = &kv->tmap;
-  if ((st = chk(mb::attention_run(aa, s), "attention")) != MB_OK) return st;
-  launches += (aa.n_tiles + aa.n_items) > 0;
-  mark(4);
-  mb::MergeArgs ma;
-  ma.part = L->part;
-  ma.merge_list = db + o_merge;
-  ma.n_merge = n_merge;
-  ma.o = L->o;
-  ma.qo_indptr = db + o_qo;
-  ma.Hq = Hq;
-  ma.Hkv = Hkv;
-  ma.hd = hd;
-  if ((st = chk(mb::attn_merge_run(ma, s), "merge")) != MB_OK) return st;
-  launches += n_merge > 0;
-  mark(5);
-  if ((st = chk(mb::gemm_run(L->o, L->w.w_o, &L->tm_wo, L->h, x_in, Ti, d.d_model, hqd, mb::kEpiResidual, L->gws,
-                             L->err, s), "gemm o")) != MB_OK)
-    return st;
-  ++launches;
-  mark(6);
-  if ((st = chk(mb::rmsnorm_run(L->h, L->w.g_ffn, L->hn, Ti, d.d_model, d.rms_eps, s), "rmsnorm ffn")) != MB_OK) return st;
-  ++launches;
-  mark(7);
-  if ((st = chk(mb::gemm_run(L->hn, L->w.w_gate_up, &L->tm_wgu, L->a, nullptr, Ti, d.d_ff, d.d_model, mb::kEpiSwiGLU,
-                             L->gws, L->err, s), "gemm gate/up")) != MB_OK)
-    return st;
-  ++launches;
-  mark(8);
-  if ((st = chk(mb::gemm_run(L->a, L->w.w_down, &L->tm_wd, x_out, L->h, Ti, d.d_model, d.d_ff, mb::kEpiResidual, L->gws,
-                             L->err, s), "gemm down")) != MB_OK)
-    return st;
-  ++launches;
-  mark(9);
+  if ((st = launch_layer(L, L, kv, plan, x_in, x_out, s, es, &launches)) != MB_OK) return st;
   L->last_T = static_cast<int32_t>(T);
   L->last_launches = launches;
-  L->last_upload = static_cast<int64_t>(hb.size()) * 4;
+  L->last_upload = plan.upload_bytes;
   L->last_stream = s;
+  return MB_OK;
+}
+
+// ------------------------------------------------------------------ stack
+mb_status mb_stack_create(mb_layer *const *layers, int32_t n_layers, int32_t use_graphs, mb_stack **out) {
+  if (!layers || n_layers <= 0 || !out) return fail(MB_EINVAL, "mb_stack_create: need layers and n_layers > 0");
+  const mb_layer_desc &d0 = layers[0]->d;
+  for (int i = 0; i < n_layers; ++i) {
+    const mb_layer *L = layers[i];
+    if (!L) return fail(MB_EINVAL, "mb_stack_create: layer %d is null", i);
+    const mb_layer_desc &d = L->d;
+    if (d.d_model != d0.d_model || d.n_q_heads != d0.n_q_heads || d.n_kv_heads != d0.n_kv_heads ||
+        d.head_dim != d0.head_dim || d.d_ff != d0.d_ff || d.max_tokens != d0.max_tokens ||
+        d.qk_norm != d0.qk_norm || L->device != layers[0]->device)
+      return fail(MB_EINVAL, "mb_stack_create: layer %d differs in shape, max_tokens or device from layer 0", i);
+  }
+  mb_stack *S = new (std::nothrow) mb_stack();
+  if (!S) return fail(MB_ENOMEM, "mb_stack_create: out of host memory");
+  S->layers.assign(layers, layers + n_layers);
+  S->use_graphs = use_graphs != 0;
+  if (cudaStreamCreateWithFlags(&S->cap_stream, cudaStreamNonBlocking) != cudaSuccess) {
+    delete S;
+    return fail(MB_ECUDA, "mb_stack_create: cudaStreamCreate failed");
+  }
+  const size_t bytes = static_cast<size_t>(d0.max_tokens) * d0.d_model * 2;
+  for (int i = 0; i < 2; ++i) {
+    mb_status st = alloc_dev(&S->act[i], bytes, "stack activations");
+    if (st != MB_OK) {
+      mb_stack_destroy(S);
+      return st;
+    }
+  }
+  *out = S;
+  return MB_OK;
+}
+
+mb_status mb_stack_step(mb_stack *S, mb_kv *const *kvs, const mb_batch *b, const void *x_in, void *x_out,
+                        void *stream) {
+  if (!S || !kvs || !b || !x_in || !x_out) return fail(MB_EINVAL, "mb_stack_step: null argument");
+  if (x_in == x_out) return fail(MB_EINVAL, "mb_stack_step: x_out must not alias x_in");
+  if (reinterpret_cast<uintptr_t>(x_in) % 16 || reinterpret_cast<uintptr_t>(x_out) % 16)
+    return fail(MB_EINVAL, "mb_stack_step: x_in and x_out must be 16-byte aligned");
+  const int nl = static_cast<int>(S->layers.size());
+  int32_t min_pages = INT32_MAX;
+  for (int i = 0; i < nl; ++i) {
+    if (!kvs[i] || kvs[i]->layer != S->layers[i])
+      return fail(MB_EINVAL, "mb_stack_step: kv pool %d is missing or belongs to another layer", i);
+    min_pages = std::min(min_pages, kvs[i]->num_pages);
+  }
+  if (b->num_reqs < 0) return fail(MB_EINVAL, "mb_stack_step: num_reqs < 0");
+  S->last_launches = 0;
+  if (b->num_reqs == 0) return MB_OK;
+  mb_layer *L0 = S->layers[0];
+  if (S->stamp.size() < static_cast<size_t>(min_pages)) S->stamp.assign(static_cast<size_t>(min_pages), 0u);
+  if (++S->stamp_gen == 0) {
+    std::fill(S->stamp.begin(), S->stamp.end(), 0u);
+    S->stamp_gen = 1;
+  }
+  int64_t T = 0;
+  mb_status st = validate_batch(b, min_pages, L0->d.max_tokens, S->stamp.data(), S->stamp_gen, &T);
+  if (st != MB_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  StepPlan plan;
+  if ((st = prepare_step(L0, b, T, s, &plan)) != MB_OK) return st;
+
+  // Every launch of the L layers depends on the batch only through the
+  // plan's sizes and the (fixed) buffers, so one captured graph serves every
+  // step with the same geometry.
+  GraphKey key{T, plan.n_tiles, plan.n_items, plan.n_merge, plan.db, L0->part, x_in, x_out, kvs[0]};
+  auto enqueue = [&](int *launches) -> mb_status {
+    for (int i = 0; i < nl; ++i) {
+      const void *in = i == 0 ? x_in : S->act[(i - 1) & 1];
+      void *outp = i == nl - 1 ? x_out : S->act[i & 1];
+      mb_status st2 = launch_layer(S->layers[i], L0, kvs[i], plan, in, outp, s, nullptr, launches);
+      if (st2 != MB_OK) return st2;
+    }
+    return MB_OK;
+  };
+  int launches = 0;
+  if (!S->use_graphs) {
+    if ((st = enqueue(&launches)) != MB_OK) return st;
+  } else {
+    // graphs hold every layer's pool: a different set of pools invalidates them
+    if (!S->graph_kvs.empty() && !std::equal(kvs, kvs + nl, S->graph_kvs.begin())) S->drop_graphs();
+    cudaGraphExec_t exec = nullptr;
+    for (auto &g : S->graphs)
+      if (g.key == key) exec = g.exec;
+    if (!exec) {
+      // capture on the stack's own stream (capturing the legacy default
+      // stream is not allowed); the graph is then launched on `s`
+      cudaStream_t cs = S->cap_stream;
+      s = cs;
+      cudaGraph_t graph = nullptr;
+      cudaError_t e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal);
+      if (e != cudaSuccess) return mb::fail(MB_ECUDA, "mb_stack_step: begin capture: %s", cudaGetErrorString(e));
+      st = enqueue(&launches);
+      e = cudaStreamEndCapture(cs, &graph);
+      s = static_cast<cudaStream_t>(stream);
+      if (st != MB_OK) {
+        if (graph) cudaGraphDestroy(graph);
+        return st;
+      }
+      if (e != cudaSuccess) return mb::fail(MB_ECUDA, "mb_stack_step: end capture: %s", cudaGetErrorString(e));
+      e = cudaGraphInstantiate(&exec, graph, 0);
+      cudaGraphDestroy(graph);
+      if (e != cudaSuccess) return mb::fail(MB_ECUDA, "mb_stack_step: instantiate: %s", cudaGetErrorString(e));
+      if (S->graphs.size() == 8) S->drop_graphs();
+      S->graphs.push_back({key, exec, launches});
+      S->graph_kvs.assign(kvs, kvs + nl);
+    } else {
+      for (auto &g : S->graphs)
+        if (g.key == key) launches = g.launches;
+    }
+    cudaError_t e = cudaGraphLaunch(exec, s);
+    if (e != cudaSuccess) return mb::fail(MB_ECUDA, "mb_stack_step: graph launch: %s", cudaGetErrorString(e));
+  }
+  S->last_launches = launches;
+  S->last_T = static_cast<int32_t>(T);
+  return MB_OK;
+}
+
+int32_t mb_stack_last_launches(const mb_stack *S) { return S ? S->last_launches : 0; }
+
+mb_status mb_stack_destroy(mb_stack *S) {
+  if (!S) return MB_OK;
+  cudaDeviceSynchronize();
+  S->drop_graphs();
+  for (void *p : S->act)
+    if (p) cudaFree(p);
+  if (S->cap_stream) cudaStreamDestroy(S->cap_stream);
+  delete S;
   return MB_OK;
 }
 

@@ -270,3 +270,69 @@ def materialize(w: Workload, unit_gains: bool = False, fill_all_kv: bool = False
     x = make_embeddings(batch.num_tokens, w.shape.d_model, w.seed + 3)
     pool = make_kv_pool(w.shape, num_pages, batch, w.seed + 4, fill_all=fill_all_kv)
     return weights, x, batch, pool
+
+
+# --------------------------------------------------------------------------
+# Stacks (many layers): generated on the device with torch's seeded CUDA
+# generator, since tens of GB of random weights would take minutes on the
+# host.  Returned as torch bf16 tensors; a test copies back the layers the
+# oracle checks.
+# --------------------------------------------------------------------------
+
+def qwen3_14b_stack(prefix: int = 30720, seed: int = 4000, n_decodes: int = 96):
+    """40-layer Qwen3-14B-shaped stack: one 2,048-token chunk after `prefix`
+    cached tokens of a 32,768-token prompt, plus decodes with contexts
+    log-uniform in [1024, 8192]."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    ctx = np.exp(rng.uniform(np.log(1024), np.log(8192), size=n_decodes)).astype(np.int64)
+    reqs = [(int(c), 1) for c in ctx] + [(prefix, 2048)]
+    return Workload(f"qwen3_14b_stack40_P{prefix}", QWEN3_14B, reqs, seed + prefix), 40
+
+
+def llama3_8b_stack(budget: int, n_decodes: int, seed: int = 5000):
+    """32-layer Llama-3-8B-shaped stack for the token-budget sweep: n_decodes
+    decodes with contexts log-uniform in [512, 32768] and one prefill chunk of
+    budget - n_decodes tokens with a prefix uniform in [0, 16384] (no chunk if
+    the decodes use the whole budget)."""
+    rng = np.random.Generator(np.random.PCG64(seed + 31 * budget + n_decodes))
+    ctx = np.exp(rng.uniform(np.log(512), np.log(32768), size=n_decodes)).astype(np.int64)
+    reqs = [(int(c), 1) for c in ctx]
+    if budget > n_decodes:
+        reqs.append((int(rng.integers(0, 16384, endpoint=True)), budget - n_decodes))
+    return Workload(f"llama3_8b_stack32_C{budget}_b{n_decodes}", LLAMA3_8B, reqs,
+                    seed + 31 * budget + n_decodes), 32
+
+
+def device_weights(shape: LayerShape, seed: int, device="cuda", unit_gains: bool = True):
+    """Random-init layer weights drawn on the device (torch, seeded): linear
+    weights N(0, 0.02), gains 1 (or 1 + N(0, 0.1)); bf16 tensors with the
+    layouts of make_weights."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    d, hd, F = shape.d_model, shape.head_dim, shape.d_ff
+    Hq, Hkv = shape.n_q_heads, shape.n_kv_heads
+
+    def lin(n, k):
+        return (torch.randn((n, k), generator=g, device=device, dtype=torch.float32) * 0.02).to(torch.bfloat16)
+
+    def gain(n):
+        if unit_gains:
+            return torch.ones(n, device=device, dtype=torch.bfloat16)
+        return (1 + 0.1 * torch.randn(n, generator=g, device=device, dtype=torch.float32)).to(torch.bfloat16)
+
+    w = {"g_attn": gain(d), "w_qkv": lin((Hq + 2 * Hkv) * hd, d), "w_o": lin(d, Hq * hd), "g_ffn": gain(d),
+         "w_gate_up": lin(2 * F, d), "w_down": lin(d, F)}
+    if shape.qk_norm:
+        w["g_q"] = gain(hd)
+        w["g_k"] = gain(hd)
+    return w
+
+
+def device_kv_pool(shape: LayerShape, num_pages: int, seed: int, device="cuda"):
+    """A KV pool [P][2][Hkv][16][hd] bf16 filled with N(0, 1), on the device."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    return torch.randn((num_pages, 2, shape.n_kv_heads, PAGE_TOKENS, shape.head_dim), generator=g,
+                       device=device, dtype=torch.float32).to(torch.bfloat16)
