@@ -79,15 +79,14 @@ __device__ __forceinline__ void chunk_tile(const CUtensorMap &tmQ, const CUtenso
   uint8_t *sQ = smem + C::OFF_Q;
   uint8_t *sK = smem + C::OFF_K;
   uint8_t *sV = smem + C::OFF_V;
-  uint8_t *sP = smem + C::OFF_P;
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
   uint64_t *q_full = bars + 0;
   uint64_t *kv_full = bars + 1;   // [2]
   uint64_t *kv_empty = bars + 3;  // [2]
   uint64_t *s_full = bars + 5;    // [2]
-  uint64_t *p_full = bars + 7;
-  uint64_t *o_full = bars + 8;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 9);
+  uint64_t *p_full = bars + 7;    // [2]
+  uint64_t *o_full = bars + 9;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 10);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -113,7 +112,8 @@ __device__ __forceinline__ void chunk_tile(const CUtensorMap &tmQ, const CUtenso
       mbar_init(&kv_empty[s], 1);
       mbar_init(&s_full[s], 1);
     }
-    mbar_init(p_full, 256);
+    mbar_init(&p_full[0], 256);
+    mbar_init(&p_full[1], 256);
     mbar_init(o_full, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -209,16 +209,16 @@ __device__ __forceinline__ void chunk_tile(const CUtensorMap &tmQ, const CUtenso
           tc_fence_after();
           issue_s(j + 1);
         }
-        if (!mbar_wait(p_full, j & 1, abort_flag, p.err, kErrWaitMma)) break;
+        if (!mbar_wait(&p_full[j & 1], (j >> 1) & 1, abort_flag, p.err, kErrWaitMma)) break;
         tc_fence_after();
         const int s = j & 1;
-        const uint32_t pbase = smem_u32(sP);
         const uint32_t vbase = smem_u32(sV + s * C::KV_BYTES);
+        // P(j) sits in TMEM over S(j): 128 keys as 64 columns of bf16 pairs
+        const uint32_t pcol = tmem + s * 128;
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {  // 16 keys per MMA
-          const uint64_t ad = sdesc_sw128(pbase + (ks >> 2) * C::TILE_BYTES + (ks & 3) * 32, 16, 1024);
           const uint64_t bd = sdesc_sw128(vbase + ks * 2048, C::TILE_BYTES, 1024);
-          mma_bf16(tmem + 256, ad, bd, C::IDESC_PV, ks > 0 ? 1u : 0u);
+          mma_bf16_ts(tmem + 256, pcol + ks * 8, bd, C::IDESC_PV, (j > 0 || ks > 0) ? 1u : 0u);
         }
         mma_commit(o_full);
         mma_commit(&kv_empty[s]);
@@ -228,21 +228,20 @@ __device__ __forceinline__ void chunk_tile(const CUtensorMap &tmQ, const CUtenso
     // ------------------------------------------------- softmax / epilogue
     // 8 warps: two per TMEM lane quarter, splitting the 128 key columns of S
     // (and the hd columns of O) in halves; a row's max and sum are combined
-    // through shared memory once per key block.
+    // through shared memory once per key block.  O accumulates in TMEM (the
+    // PV MMA adds each block); a row is rescaled only when its maximum grows
+    // by more than 2^8 over the reference it uses, so probabilities stay
+    // <= 256 and most blocks never wait for the previous PV.
     const int q = warp & 3;
     const int hh = (warp - 2) >> 2;          // column half
     const int r = q * 32 + lane;
     const int q_pos = cached + i0 + r;
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     constexpr int OH = HD / 2;               // O columns per half
+    constexpr float kRescaleAbove = 8.f;     // log2 units
     float *red = reinterpret_cast<float *>(smem + C::OFF_RED);  // [2 bufs][2 halves][128]
-    float o_acc[OH];
-#pragma unroll
-    for (int d = 0; d < OH; ++d) o_acc[d] = 0.f;
-    float m = -INFINITY, l = 0.f;
+    float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
-    // A wait that gives up marks the thread `bad`; the decision to leave is
-    // taken jointly at the per-block barrier so no warp is left waiting there.
     bool bad = false;
     for (int j = 0; j < n_kb; ++j) {
       const int b = j & 1;
@@ -252,79 +251,61 @@ __device__ __forceinline__ void chunk_tile(const CUtensorMap &tmQ, const CUtenso
       const int key0 = 128 * j + hh * 64;   // first key of this thread's half
       const bool full = (key0 + 63 <= q_pos) && (key0 + 63 < kv);
       const uint32_t scol = tmem + lane_base + b * 128 + hh * 64;
-      // pass 1: maximum of the visible scores of this half row
+      // pass 1: this half row of S into registers, and its visible maximum
+      float sv[64];
       float mx = -INFINITY;
+      if (!bad) {
+        tmem_ld32(scol, *reinterpret_cast<float(*)[32]>(&sv[0]));
+        tmem_ld32(scol + 32, *reinterpret_cast<float(*)[32]>(&sv[32]));
 #pragma unroll
-      for (int cc = 0; cc < 2 && !bad; ++cc) {
-        float v[32];
-        tmem_ld32(scol + cc * 32, v);
-        if (full) {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) mx = fmaxf(mx, v[i]);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int key = key0 + cc * 32 + i;
-            if (key <= q_pos && key < kv) mx = fmaxf(mx, v[i]);
+        for (int i = 0; i < 64; ++i) {
+          sv[i] *= p.scale_log2;
+          if (!full) {
+            const int key = key0 + i;
+            if (!(key <= q_pos && key < kv)) sv[i] = -INFINITY;
           }
+          mx = fmaxf(mx, sv[i]);
         }
       }
-      mx *= p.scale_log2;
       red[(b * 2 + hh) * 128 + r] = mx;
+      // every thread is past its reads of S(j) here, so P(j) may overwrite it
       if (named_bar_or(2, 256, bad)) {
         ok = false;
         break;
       }
       mx = fmaxf(mx, red[(b * 2 + (hh ^ 1)) * 128 + r]);
-      const float m_new = fmaxf(m, mx);
-      const float alpha = (m == -INFINITY) ? 0.f : exp2f(m - m_new);
-      if (j > 0) {
+      const bool grow = (m_ref == -INFINITY) || (mx > m_ref + kRescaleAbove);
+      if (j > 0 && __any_sync(0xffffffffu, grow)) {
+        // O holds blocks < j relative to m_ref: finish PV(j-1), then rescale
         bad = !mbar_wait(o_full, (j - 1) & 1, abort_flag, p.err, kErrWaitSoftmax);
         bad = __any_sync(0xffffffffu, bad);
         if (bad) {
-          // reported at the next barrier (or after the loop); skip the work
           ok = false;
           continue;
         }
         tc_fence_after();
+        const float alpha = grow ? exp2f(m_ref - mx) : 1.f;
 #pragma unroll
         for (int cc = 0; cc < OH / 32; ++cc) {
           float v[32];
           tmem_ld32(tmem + lane_base + 256 + hh * OH + cc * 32, v);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o_acc[cc * 32 + i] = (o_acc[cc * 32 + i] + v[i]) * alpha;
+          for (int i = 0; i < 32; ++i) v[i] *= alpha;
+          tmem_st32(tmem + lane_base + 256 + hh * OH + cc * 32, v);
         }
-      } else {
-#pragma unroll
-        for (int d = 0; d < OH; ++d) o_acc[d] *= alpha;
+        if (grow) l *= alpha;
       }
-      l *= alpha;
-      // pass 2: probabilities -> bf16 P half row (A operand, K-major, swizzled)
-      uint8_t *prow = sP + hh * C::TILE_BYTES + (r >> 3) * 1024 + (r & 7) * 128;
+      if (grow) m_ref = mx;
+      // pass 2: probabilities relative to m_ref -> bf16 pairs into TMEM over S(j)
+      float pk[32];
 #pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        float v[32];
-        tmem_ld32(scol + cc * 32, v);
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          float p0 = exp2f(fmaf(v[i], p.scale_log2, -m_new));
-          float p1 = exp2f(fmaf(v[i + 1], p.scale_log2, -m_new));
-          if (!full) {
-            const int key = key0 + cc * 32 + i;
-            if (!(key <= q_pos && key < kv)) p0 = 0.f;
-            if (!(key + 1 <= q_pos && key + 1 < kv)) p1 = 0.f;
-          }
-          l += p0 + p1;
-          pk[i / 2] = pack_bf16x2(p0, p1);
-        }
-#pragma unroll
-        for (int g4 = 0; g4 < 4; ++g4) {
-          const int grp = cc * 4 + g4;  // 8-key group within this 64-key chunk
-          *reinterpret_cast<uint4 *>(prow + ((grp ^ (r & 7)) * 16)) =
-              make_uint4(pk[4 * g4], pk[4 * g4 + 1], pk[4 * g4 + 2], pk[4 * g4 + 3]);
-        }
+      for (int i = 0; i < 64; i += 2) {
+        const float p0 = exp2f(sv[i] - m_ref);
+        const float p1 = exp2f(sv[i + 1] - m_ref);
+        l += p0 + p1;
+        pk[i / 2] = __uint_as_float(pack_bf16x2(p0, p1));
       }
+      tmem_st32(tmem + lane_base + b * 128 + hh * 32, pk);
       if (j == n_kb - 1 && 128 * j + r > last_pos) {
         // rows past the last visible key may hold stale or non-finite data:
         // zero them so that P = 0 rows contribute exactly nothing
@@ -335,11 +316,10 @@ __device__ __forceinline__ void chunk_tile(const CUtensorMap &tmQ, const CUtenso
 #pragma unroll
             for (int k = 0; k < 8; ++k)
               *reinterpret_cast<uint4 *>(vrow + c * C::TILE_BYTES + k * 16) = make_uint4(0, 0, 0, 0);
+        fence_proxy_async_smem();
       }
-      fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(p_full);
-      m = m_new;
+      mbar_arrive(&p_full[b]);
     }
     // row sum over both halves
     float *lsum = red + 4 * 128;
@@ -348,13 +328,10 @@ __device__ __forceinline__ void chunk_tile(const CUtensorMap &tmQ, const CUtenso
     l += lsum[(hh ^ 1) * 128 + r];
     if (ok && mbar_wait(o_full, (n_kb - 1) & 1, abort_flag, p.err, kErrWaitSoftmax)) {
       tc_fence_after();
+      float o_acc[OH];
 #pragma unroll
-      for (int cc = 0; cc < OH / 32; ++cc) {
-        float v[32];
-        tmem_ld32(tmem + lane_base + 256 + hh * OH + cc * 32, v);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) o_acc[cc * 32 + i] += v[i];
-      }
+      for (int cc = 0; cc < OH / 32; ++cc)
+        tmem_ld32(tmem + lane_base + 256 + hh * OH + cc * 32, *reinterpret_cast<float(*)[32]>(&o_acc[cc * 32]));
       if (i0 + r < qo) {
         const float inv = 1.f / l;
         uint4 *dst = reinterpret_cast<uint4 *>(p.o + static_cast<size_t>(t0 + i0 + r) * (p.Hq * HD) + h * HD + hh * OH);
