@@ -47,14 +47,15 @@ struct ChunkCfg {
   static constexpr int TILE_BYTES = 128 * 128;    // [128 rows][64 bf16]
   static constexpr int Q_BYTES = NH * TILE_BYTES;
   static constexpr int KV_BYTES = NH * TILE_BYTES;
-  static constexpr int P_BYTES = 2 * TILE_BYTES;  // 128 x 128 keys
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + Q_BYTES;
-  static constexpr int OFF_V = OFF_K + 2 * KV_BYTES;
-  static constexpr int OFF_P = OFF_V + 2 * KV_BYTES;
-  static constexpr int OFF_BAR = OFF_P + P_BYTES;
+  static constexpr int NKV = 3;                   // K/V stages
+  static constexpr int OFF_V = OFF_K + NKV * KV_BYTES;
+  static constexpr int OFF_BAR = OFF_V + NKV * KV_BYTES;
   static constexpr int OFF_RED = OFF_BAR + 128;   // softmax row max / sum exchange
-  static constexpr int SMEM = OFF_RED + 6 * 128 * 4 + 1024;
+  // The kernel checks that the dynamic shared memory starts 1024-aligned, so
+  // no alignment slack is reserved (it would not fit beside three stages).
+  static constexpr int SMEM = OFF_RED + 4 * 128 * 4;
   static constexpr int THREADS = 320;             // TMA, MMA, 8 softmax warps
   static constexpr uint32_t IDESC_S = idesc_bf16(128, 128, false);
   static constexpr uint32_t IDESC_PV = idesc_bf16(128, HD, true);
@@ -81,12 +82,13 @@ __device__ __forceinline__ void chunk_tile(const CUtensorMap &tmQ, const CUtenso
   uint8_t *sV = smem + C::OFF_V;
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
   uint64_t *q_full = bars + 0;
-  uint64_t *kv_full = bars + 1;   // [2]
-  uint64_t *kv_empty = bars + 3;  // [2]
-  uint64_t *s_full = bars + 5;    // [2]
-  uint64_t *p_full = bars + 7;    // [2]
-  uint64_t *o_full = bars + 9;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 10);
+  uint64_t *kv_full = bars + 1;   // [NKV]
+  uint64_t *kv_empty = bars + 4;  // [NKV]
+  uint64_t *s_full = bars + 7;    // [2]
+  uint64_t *p_full = bars + 9;    // [2]
+  uint64_t *o_full = bars + 11;   // PV(j) done, j < n_kb - 1
+  uint64_t *o_last = bars + 12;   // every MMA of the tile done (committed once)
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 13);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -107,14 +109,16 @@ __device__ __forceinline__ void chunk_tile(const CUtensorMap &tmQ, const CUtenso
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < C::NKV; ++s) {
       mbar_init(&kv_full[s], 1);
       mbar_init(&kv_empty[s], 1);
-      mbar_init(&s_full[s], 1);
     }
+    mbar_init(&s_full[0], 1);
+    mbar_init(&s_full[1], 1);
     mbar_init(&p_full[0], 256);
     mbar_init(&p_full[1], 256);
     mbar_init(o_full, 1);
+    mbar_init(o_last, 1);
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tmQ);
@@ -137,8 +141,8 @@ __device__ __forceinline__ void chunk_tile(const CUtensorMap &tmQ, const CUtenso
       uint32_t issued = 0, issued_ph = 0;
       bool ok = true;
       for (int j = 0; j < n_kb && ok; ++j) {
-        const int s = j & 1;
-        const uint32_t ph = (j >> 1) & 1;
+        const int s = j % C::NKV;
+        const uint32_t ph = (j / C::NKV) & 1;
         if (!mbar_wait(&kv_empty[s], ph ^ 1, abort_flag, p.err, kErrWaitProducer)) {
           ok = false;
           break;
@@ -164,7 +168,7 @@ __device__ __forceinline__ void chunk_tile(const CUtensorMap &tmQ, const CUtenso
         issued_ph = (issued_ph & ~(1u << s)) | (ph << s);
       }
       if (!ok) {
-        for (int s = 0; s < 2; ++s)
+        for (int s = 0; s < C::NKV; ++s)
           if (issued & (1u << s)) {
             const uint64_t t_start = globaltimer();
             while (!mbar_try_wait(smem_u32(&kv_full[s]), (issued_ph >> s) & 1u) &&
@@ -183,8 +187,9 @@ __device__ __forceinline__ void chunk_tile(const CUtensorMap &tmQ, const CUtenso
     if (lane == 0) {
       // ------------------------------------------------------- MMA issuer
       auto issue_s = [&](int j) {
-        const int s = j & 1;
-        const uint32_t d = tmem + s * 128;
+        const int b = j & 1;                 // S buffer in TMEM
+        const int s = j % C::NKV;            // K/V stage
+        const uint32_t d = tmem + b * 128;
         const uint32_t q0 = smem_u32(sQ);
         const uint32_t k0 = smem_u32(sK + s * C::KV_BYTES);
 #pragma unroll
@@ -195,7 +200,23 @@ __device__ __forceinline__ void chunk_tile(const CUtensorMap &tmQ, const CUtenso
             const uint64_t bd = sdesc_sw128(k0 + c * C::TILE_BYTES + kk * 32, 16, 1024);
             mma_bf16(d, ad, bd, C::IDESC_S, (c > 0 || kk > 0) ? 1u : 0u);
           }
-        mma_commit(&s_full[s]);
+        mma_commit(&s_full[b]);
+      };
+      auto issue_pv = [&](int j) {
+        const int b = j & 1;
+        const int s = j % C::NKV;
+        const uint32_t vbase = smem_u32(sV + s * C::KV_BYTES);
+        // P(j) sits in TMEM over S(j): 128 keys as 64 columns of bf16 pairs
+        const uint32_t pcol = tmem + b * 128;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {  // 16 keys per MMA
+          const uint64_t bd = sdesc_sw128(vbase + ks * 2048, C::TILE_BYTES, 1024);
+          mma_bf16_ts(tmem + 256, pcol + ks * 8, bd, C::IDESC_PV, (j > 0 || ks > 0) ? 1u : 0u);
+        }
+        // the last PV is covered by the o_last commit after the loop; stages
+        // the producer will not refill get no release (nothing waits on it)
+        if (j + 1 < n_kb) mma_commit(o_full);
+        if (j + C::NKV < n_kb) mma_commit(&kv_empty[s]);
       };
       bool ok = mbar_wait(q_full, 0, abort_flag, p.err, kErrWaitMma);
       if (ok) ok = mbar_wait(&kv_full[0], 0, abort_flag, p.err, kErrWaitMma);
@@ -203,25 +224,45 @@ __device__ __forceinline__ void chunk_tile(const CUtensorMap &tmQ, const CUtenso
         tc_fence_after();
         issue_s(0);
       }
+      // Block j: S(j+1) as soon as its K/V landed, PV(j) as soon as P(j) is
+      // ready, in whichever order they come (neither waits on the other).
       for (int j = 0; j < n_kb && ok; ++j) {
-        if (j + 1 < n_kb) {
-          if (!mbar_wait(&kv_full[(j + 1) & 1], ((j + 1) >> 1) & 1, abort_flag, p.err, kErrWaitMma)) break;
-          tc_fence_after();
-          issue_s(j + 1);
+        bool s_done = j + 1 >= n_kb, pv_done = false;
+        const uint32_t kv_bar = smem_u32(&kv_full[(j + 1) % C::NKV]);
+        const uint32_t kv_par = ((j + 1) / C::NKV) & 1;
+        const uint32_t p_bar = smem_u32(&p_full[j & 1]);
+        const uint32_t p_par = (j >> 1) & 1;
+        const uint64_t t_start = globaltimer();
+        for (uint32_t spin = 0; !(s_done && pv_done); ++spin) {
+          if (!s_done && mbar_test_wait(kv_bar, kv_par)) {
+            tc_fence_after();
+            issue_s(j + 1);
+            s_done = true;
+          }
+          if (!pv_done && mbar_test_wait(p_bar, p_par)) {
+            tc_fence_after();
+            issue_pv(j);
+            pv_done = true;
+          }
+          if ((spin & 63u) == 63u) {
+            if (*abort_flag) {
+              ok = false;
+              break;
+            }
+            if (globaltimer() - t_start > kWaitLimitNs) {
+              *abort_flag = 1;
+              atomicExch(p.err, kErrWaitMma);
+              ok = false;
+              break;
+            }
+          }
         }
-        if (!mbar_wait(&p_full[j & 1], (j >> 1) & 1, abort_flag, p.err, kErrWaitMma)) break;
-        tc_fence_after();
-        const int s = j & 1;
-        const uint32_t vbase = smem_u32(sV + s * C::KV_BYTES);
-        // P(j) sits in TMEM over S(j): 128 keys as 64 columns of bf16 pairs
-        const uint32_t pcol = tmem + s * 128;
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {  // 16 keys per MMA
-          const uint64_t bd = sdesc_sw128(vbase + ks * 2048, C::TILE_BYTES, 1024);
-          mma_bf16_ts(tmem + 256, pcol + ks * 8, bd, C::IDESC_PV, (j > 0 || ks > 0) ? 1u : 0u);
-        }
-        mma_commit(o_full);
-        mma_commit(&kv_empty[s]);
+      }
+      // One commit for all MMAs issued above (on every path), waited on here
+      // too, so no MMA is in flight when the tile frees its TMEM.
+      mma_commit(o_last);
+      const uint64_t t_end = globaltimer();
+      while (!mbar_try_wait(smem_u32(o_last), 0) && globaltimer() - t_end < kWaitLimitNs) {
       }
     }
   } else {
@@ -255,8 +296,7 @@ __device__ __forceinline__ void chunk_tile(const CUtensorMap &tmQ, const CUtenso
       float sv[64];
       float mx = -INFINITY;
       if (!bad) {
-        tmem_ld32(scol, *reinterpret_cast<float(*)[32]>(&sv[0]));
-        tmem_ld32(scol + 32, *reinterpret_cast<float(*)[32]>(&sv[32]));
+        tmem_ld64(scol, sv);
 #pragma unroll
         for (int i = 0; i < 64; ++i) {
           sv[i] *= p.scale_log2;
@@ -309,7 +349,7 @@ __device__ __forceinline__ void chunk_tile(const CUtensorMap &tmQ, const CUtenso
       if (j == n_kb - 1 && 128 * j + r > last_pos) {
         // rows past the last visible key may hold stale or non-finite data:
         // zero them so that P = 0 rows contribute exactly nothing
-        uint8_t *vrow = sV + b * C::KV_BYTES + (r >> 3) * 1024 + (r & 7) * 128;
+        uint8_t *vrow = sV + (j % C::NKV) * C::KV_BYTES + (r >> 3) * 1024 + (r & 7) * 128;
 #pragma unroll
         for (int c = 0; c < C::NH; ++c)
           if ((c & 1) == hh)
@@ -321,12 +361,13 @@ __device__ __forceinline__ void chunk_tile(const CUtensorMap &tmQ, const CUtenso
       tc_fence_before();
       mbar_arrive(&p_full[b]);
     }
-    // row sum over both halves
-    float *lsum = red + 4 * 128;
+    // row sum over both halves (reuses the exchange buffer of the parity the
+    // last block did not use, so no reader of the last maxima is overtaken)
+    float *lsum = red + (((n_kb - 1) & 1) ^ 1) * 256;
     lsum[hh * 128 + r] = l;
     named_bar_sync(2, 256);
     l += lsum[(hh ^ 1) * 128 + r];
-    if (ok && mbar_wait(o_full, (n_kb - 1) & 1, abort_flag, p.err, kErrWaitSoftmax)) {
+    if (ok && mbar_wait(o_last, 0, abort_flag, p.err, kErrWaitSoftmax) && !*abort_flag) {
       tc_fence_after();
       float o_acc[OH];
 #pragma unroll
@@ -660,19 +701,28 @@ __global__ void __launch_bounds__(128) merge_kernel(const float *part, const int
 // The ragged attention of a step is ONE launch: blocks [0, n_tiles) run a
 // prefill-chunk tile (tensor cores), the rest run a decode item (HBM stream),
 // so the two kinds share the GPU instead of running back to back.  Tiles come
-// first, heaviest first; decode items fill SMs as they free up.  The decode
-// part uses 9 consumer warps and a ring carved from the tile's shared memory.
+// first, heaviest first; decode items fill SMs as they free up.  A decode CTA
+// runs two items side by side, each with 4 consumer warps, a producer warp and
+// a ring in its half of the tile's shared memory.
 template <int HD>
 struct FusedCfg {
   static constexpr int THREADS = ChunkCfg<HD>::THREADS;          // 10 warps
   static constexpr int DEC_NW = 4;                                // consumers per decode item
   static constexpr int SMEM = ChunkCfg<HD>::SMEM;
   // two decode items per CTA, each with half of the shared memory
-  static constexpr int HALF = ((SMEM - 1024) / 2) & ~1023;
-  static constexpr int NSLOT = ((HALF - 256) / DecCfg<HD>::SLOT_BYTES) < 16
-                                   ? ((HALF - 256) / DecCfg<HD>::SLOT_BYTES)
-                                   : 16;
+  static constexpr int HALF = (SMEM / 2) & ~1023;
+  // Page i lives in slot i % NSLOT and is consumed by warp i % DEC_NW; with
+  // NSLOT a multiple of DEC_NW every slot has a single consumer warp, which
+  // takes its pages in order, so a parity wait on a slot can never match a
+  // phase two copies ahead.
+  static constexpr int FIT = (HALF - 256) / DecCfg<HD>::SLOT_BYTES;
+  static constexpr int NSLOT = ((FIT < 16 ? FIT : 16) / DEC_NW) * DEC_NW;
   static_assert(2 * (DEC_NW + 1) * 32 == THREADS, "two decode items fill the CTA");
+  static_assert(NSLOT >= DEC_NW && NSLOT % DEC_NW == 0, "one consumer warp per ring slot");
+  // ring, full/empty barriers and the abort word of one item fit its half
+  static_assert(NSLOT * DecCfg<HD>::SLOT_BYTES + 16 * NSLOT + 4 <= HALF, "decode item exceeds its half");
+  // the end-of-item merge stash (8 q-heads at most) reuses the ring
+  static_assert(DEC_NW * 8 * (HD + 2) * 4 <= NSLOT * DecCfg<HD>::SLOT_BYTES, "merge stash exceeds the ring");
 };
 
 template <int HD, int G>
@@ -680,6 +730,11 @@ __global__ void __launch_bounds__(FusedCfg<HD>::THREADS, 1)
     attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmKV,
                      const ChunkParams cp, const DecodeParams dp, int n_tiles) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
+  if (smem_u32(smem_raw) & 1023u) {
+    // the layouts above need a 1024-aligned base and reserve no slack
+    if (threadIdx.x == 0) atomicExch(cp.err, kErrBounds);
+    return;
+  }
   if (static_cast<int>(blockIdx.x) < n_tiles) {
     chunk_tile<HD>(tmQ, tmKV, cp, blockIdx.x, smem_raw);
   } else {

@@ -249,3 +249,30 @@ def test_step_rejects_malformed_descriptor_before_launch(mb):
             layer.step(mb.Batch([0, 17], [17], [0, 2], [0, 1]), x, y, _stream())  # T > max_tokens
     finally:
         layer.close()
+
+
+@pytest.mark.parametrize("name", ["llama3_8b_T576", "qwen3_14b_P0", "qwen3_14b_P2200"])
+def test_many_repeats_bit_identical(mb, name):
+    """Several hundred back-to-back steps on one input: every output equals the
+    first bit for bit and no kernel reports an error.  Rare pipeline races
+    (a ring slot read before its copy lands, TMEM freed under an MMA) show up
+    here as a mismatch or an error word long before a single step would."""
+    wl = W.llama3_8b_mixed() if name.startswith("llama") else W.qwen3_14b_mixed(int(name.split("P")[1]))
+    wb, x, batch, pool = W.materialize(wl, unit_gains=True)
+    dw = {k: to_dev(v) for k, v in wb.items()}
+    dpool = to_dev(pool.reshape(-1))
+    layer = mb.Layer(wl.shape.as_dict(), dw, batch.num_tokens, pool.shape[0], kv_buf=dpool)
+    try:
+        cb = mb.Batch.of(batch)
+        dx = to_dev(x)
+        first = torch.empty_like(dx)
+        dy = torch.empty_like(dx)
+        layer.step(cb, dx, first, _stream())
+        mismatches = torch.zeros((), dtype=torch.int64, device=dx.device)
+        for _ in range(400):
+            layer.step(cb, dx, dy, _stream())
+            mismatches += (dy.view(torch.int16) != first.view(torch.int16)).any().to(torch.int64)
+        mb.mb_device_status(layer.handle, _stream())
+        assert int(mismatches) == 0, f"{int(mismatches)} of 400 repeated steps differ from the first"
+    finally:
+        layer.close()
