@@ -163,6 +163,13 @@ def barrier(pg):
         pg.barrier()
 
 
+def replica_throughput(pg, world: int, tokens_per_step: int, ms_local: float):
+    """Replicas only: every rank runs the same step on its own GPU.  The job's
+    step time is the slowest rank's; the value counts the tokens of all ranks."""
+    ms = reduce_max(pg, ms_local)
+    return ms, world * tokens_per_step / (ms / 1e3)
+
+
 # ----------------------------------------------------------- CPU oracle
 def oracle_inputs(wl: W.Workload):
     from oracle import layer as OL
@@ -388,8 +395,7 @@ def run_mine(args, rank: int, world: int, local: int, pg):
     step_ms_local = sum(a.elapsed_time(b) for a, b in zip(ev0, ev1)) / args.steps
     kern_ms, ksteps = mb.mb_layer_timing(layer.handle)
     mb.mb_layer_set_timing(layer.handle, False)
-    step_ms = reduce_max(pg, step_ms_local)
-    value = world * T / (step_ms / 1e3)
+    step_ms, value = replica_throughput(pg, world, T, step_ms_local)
 
     # ---- per-kernel rooflines from the live events of the timed region
     alg = algorithmic(wl.shape, batch)
@@ -461,7 +467,7 @@ def run_mine(args, rank: int, world: int, local: int, pg):
         yh.copy_(dy, non_blocking=True)
         e1[i].record(stream)
     torch.cuda.synchronize()
-    e2e_ms = reduce_max(pg, sum(a.elapsed_time(b) for a, b in zip(e0, e1)) / n_e2e)
+    e2e_ms, e2e_value = replica_throughput(pg, world, T, sum(a.elapsed_time(b) for a, b in zip(e0, e1)) / n_e2e)
     upload = mb.mb_layer_last_upload_bytes(layer.handle)
 
     # ---- CPU baseline: the oracle on a bounded sample (rank 0, one GPU only)
@@ -520,7 +526,7 @@ def run_mine(args, rank: int, world: int, local: int, pg):
         "roofline_step_ms": round(roof_ms, 5),
         "step_model_ms": round(model_ms, 5),
         "cpu_baseline": cpu,
-        "e2e": {"value": round(world * T / (e2e_ms / 1e3), 1), "unit": UNIT,
+        "e2e": {"value": round(e2e_value, 1), "unit": UNIT,
                 "h2d_bytes_per_step": int(x.nbytes + upload), "d2h_bytes_per_step": int(x.nbytes),
                 "ms_per_step": round(e2e_ms, 5)},
         "gpu_launches": int(launches_per_step * args.steps),
