@@ -51,6 +51,28 @@ def workload_by_name(name: str) -> W.Workload:
     raise SystemExit(f"unknown workload {name}")
 
 
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu
+# capture, keyed by kernel; each is valid only for the sources it was captured on
+# and reads as null once any of them changes.
+NCU_TRAFFIC = {
+    "gemm_gate_up": {"bytes": 255.82e6, "sha256_16": "958065fbe514e176",
+                     "sources": ("csrc/mb_gemm.cu", "csrc/mb_ptx.cuh", "csrc/mb_kernels.h"),
+                     "capture": "profiles/gemm_llama3_8b_T576.md (llama3_8b_T576, second warm-up step)"},
+}
+
+
+def ncu_traffic(kernel: str):
+    import hashlib
+    rec = NCU_TRAFFIC.get(kernel)
+    if rec is None:
+        return None
+    h = hashlib.sha256()
+    for f in rec["sources"]:
+        with open(os.path.join(ROOT, "mixed_prefill_decode_gb300", f), "rb") as fh:
+            h.update(fh.read())
+    return rec["bytes"] if h.hexdigest()[:16] == rec["sha256_16"] else None
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -431,12 +453,12 @@ def run_mine(args, rank: int, world: int, local: int, pg):
         achieved = work / (dom_ms / 1e3) / 1e12
         roofline = {"kernel": dom, "bound": "tensor", "achieved": round(achieved, 2),
                     "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                    "frac": round(achieved / peaks["bf16_tflops"], 4), "traffic": None,
+                    "frac": round(achieved / peaks["bf16_tflops"], 4), "traffic": ncu_traffic(dom),
                     "algorithmic_per_launch": work, "peak_kind": f"{peak_kind} bf16 burst"}
     else:
         achieved = work / (dom_ms / 1e3) / 1e9
         roofline = {"kernel": dom, "bound": "hbm", "achieved": round(achieved, 2), "peak": peaks["hbm_gbs"],
-                    "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
+                    "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": ncu_traffic(dom),
                     "algorithmic_per_launch": work, "peak_kind": f"{peak_kind} HBM copy"}
     gemm_names = ("gemm_qkv", "gemm_o", "gemm_gate_up", "gemm_down")
     gemm_flops = sum(alg[n][1] for n in gemm_names)
