@@ -6,17 +6,23 @@
 // "are 64 more rows in a 4,160-row matrix multiply").
 //
 // D[M][N] = A[M][K] B[N][K]^T, bf16 in, fp32 accumulate in TMEM.
-//   tile      128 (tokens) x 256 (weight rows), K step 64 (one 128-byte
-//             swizzle atom), 4-stage TMA ring (48 KB per stage)
-//   warps     0: TMA producer, 1: MMA issuer (+ TMEM owner), 2-5: epilogue
-//   TMEM      two 256-column fp32 accumulators, so the epilogue of one tile
-//             overlaps the main loop of the next
+//   tile      256 (tokens) x 256 (weight rows), K step 64 (one 128-byte
+//             swizzle atom): two M = 128 MMAs per K step share the B tile, so a
+//             64 KB stage feeds 1,024 tensor cycles (a 128-row tile would need
+//             48 KB per 512).  A tile whose second half lies past M issues and
+//             loads only the first.  3-stage TMA ring (64 KB per stage).
+//   warps     0: TMA producer, 1: MMA issuer (+ TMEM owner), 2-9: epilogue
+//             (warp w reads TMEM lane quarter w % 4 of half (w - 2) / 4)
+//   TMEM      the two halves' 256-column fp32 accumulators fill all 512
+//             columns; the epilogue drains a tile before the next one starts
 //   schedule  persistent; whole tiles data-parallel while there are several
 //             waves, the last one to two waves split along K evenly over all
-//             CTAs (stream-K).  A split tile's pieces go to fp32 partial slots;
-//             the CTA that takes the last ticket of the tile sums the pieces in
-//             CTA order (deterministic) and runs the epilogue.  No CTA waits on
-//             another.
+//             CTAs (stream-K).  A split tile's later pieces go to fp32 partial
+//             slots; the CTA that holds the tile's first piece waits (bounded)
+//             for them, adds them in rank order (deterministic) and runs the
+//             epilogue.  That wait needs every CTA of the grid resident at
+//             once: the grid never exceeds the SM count, or the number of
+//             clusters the occupancy query says fit.
 //   epilogues store | + residual | SwiGLU (B rows [gate F; up F]: a tile loads
 //             128 gate rows and the matching 128 up rows and writes
 //             silu(g) * u for 128 output features)
@@ -42,18 +48,43 @@ namespace {
 
 using namespace dev;
 
-constexpr int BM = 128;
+constexpr int HM = 128;                // rows of a half (the MMA's M)
 constexpr int BN = 256;
 constexpr int BK = 64;
-constexpr int STAGES = 4;
-constexpr int A_STAGE = BM * BK * 2;   // 16 KB
+constexpr int A_HALF = HM * BK * 2;    // 16 KB
 constexpr int B_STAGE = BN * BK * 2;   // 32 KB
-constexpr int SMEM_TILES = STAGES * (A_STAGE + B_STAGE);
-constexpr int SMEM_BYTES = SMEM_TILES + 1024 /*align*/ + 256 /*barriers*/;
-constexpr int THREADS = 192;
-constexpr uint32_t IDESC = idesc_bf16(BM, BN, false);
-constexpr int kMaxGroupedTilesM = 8;   // grouped schedule up to 1,024 tokens
-constexpr int kPrefetchAhead = 8;      // weight k-blocks fetched into L2 ahead of the ring
+constexpr int CHUNK = 128 * 32 * 4;    // one fp32 partial chunk: 128 rows x 32 columns
+constexpr uint32_t IDESC = idesc_bf16(HM, BN, false);
+constexpr int kMaxHalves = 2;
+constexpr int kMaxGroupedTilesM = 8;   // grouped schedule up to 8 M-tiles
+constexpr int kWideMinRows = 1024;     // from this many tokens on, tiles have two halves
+
+// Tile configurations: NH halves of 128 rows per tile.
+//  NH = 1: 128 x 256 tiles, 4 stages of 48 KB, two TMEM accumulators, so the
+//          epilogue of one tile overlaps the main loop of the next;
+//  NH = 2: 256 x 256 tiles, 3 stages of 64 KB (1.5x the MMA work per staged
+//          byte), one accumulator pair that fills TMEM.
+// Measured on GB300, NH = 1 is faster up to ~600 tokens (its double-buffered
+// epilogue and lighter split fix-up win), NH = 2 from ~2,000 tokens on (its
+// main loop runs at the MMA rate).
+template <int NH>
+struct TileCfg {
+  static constexpr int BM = HM * NH;
+  static constexpr int STAGES = NH == 1 ? 4 : 3;
+  static constexpr int A_STAGE = NH * A_HALF;
+  static constexpr int SMEM_TILES = STAGES * (A_STAGE + B_STAGE);
+  static constexpr int SMEM_BYTES = SMEM_TILES + 1024 /*align*/ + 256 /*barriers*/;
+  static constexpr int EPI_THREADS = 128 * NH;
+  static constexpr int THREADS = 64 + EPI_THREADS;     // TMA, MMA, 4 epilogue warps per half
+  static constexpr int NACC = NH == 1 ? 2 : 1;          // accumulator buffers in TMEM
+  static constexpr int FIX_CHUNKS = NH == 1 ? 8 : 4;    // partial chunks staged per fix-up round
+  static_assert(NACC * NH * BN <= 512, "TMEM holds 512 columns");
+  static_assert(NH * FIX_CHUNKS * CHUNK <= SMEM_TILES, "fix-up staging lives in the idle stage buffers");
+};
+#ifndef MB_GEMM_PREFETCH
+#define MB_GEMM_PREFETCH 8             // weight k-blocks fetched into L2 ahead of the ring
+#endif
+constexpr int kPrefetchAhead = MB_GEMM_PREFETCH;
 #ifndef MB_GEMM_MULTICAST
 #define MB_GEMM_MULTICAST 1            // 1: a group's CTAs form a cluster and share weight tiles by multicast
 #endif
@@ -72,7 +103,7 @@ struct Params {
   const __nv_bfloat16 *R;
   int ldr;
   int F;                // SwiGLU: row offset of the up half in B
-  float *partials;      // [2 grid][8 chunks][128 rows][32] fp32
+  float *partials;      // [2 grid][NH halves][8 chunks][128 rows][32] fp32
   int *tickets;
   int *err;
 };
@@ -163,9 +194,13 @@ __device__ __forceinline__ int slot_of(const Params &p, int rank, int mi, int u)
 
 __device__ __forceinline__ float silu(float x) { return x / (1.0f + expf(-x)); }
 
-__device__ __forceinline__ float *part_chunk(const Params &p, int slot, int j, int r) {
-  return p.partials + ((static_cast<size_t>(slot) * 8 + j) * 128 + r) * 32;
+template <int NH>
+__device__ __forceinline__ float *part_chunk(const Params &p, int slot, int h, int j, int r) {
+  return p.partials + (((static_cast<size_t>(slot) * NH + h) * 8 + j) * 128 + r) * 32;
 }
+// Halves of the tile at m0 that hold rows of A.
+template <int NH>
+__device__ __forceinline__ int halves_of(const Params &p, int m0) { return (NH == 2 && m0 + HM < p.M) ? 2 : 1; }
 // Within a partial row of 32 floats, 16-byte group q is stored at q ^ (row % 8)
 // so that the finisher's shared-memory reads of 128 rows spread over banks.
 __device__ __forceinline__ int part_swz(int q, int r) { return q ^ (r & 7); }
@@ -211,19 +246,21 @@ __device__ __forceinline__ void store_chunk(const Params &p, int row, int col, c
   for (int q = 0; q < 4; ++q) dp[q] = make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
 }
 
-template <int EPI>
-__global__ void __launch_bounds__(THREADS, 1)
+template <int EPI, int NH>
+__global__ void __launch_bounds__(TileCfg<NH>::THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const Params p) {
+  using C = TileCfg<NH>;
+  constexpr int BM = C::BM, STAGES = C::STAGES, A_STAGE = C::A_STAGE, EPI_THREADS = C::EPI_THREADS;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = align1024(smem_raw);
   uint8_t *sA = smem;
   uint8_t *sB = smem + STAGES * A_STAGE;
-  uint64_t *full = reinterpret_cast<uint64_t *>(smem + SMEM_TILES);
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::SMEM_TILES);
   uint64_t *empty = full + STAGES;
-  uint64_t *tfull = empty + STAGES;
-  uint64_t *tempty = tfull + 2;
-  uint64_t *fixbar = tempty + 2;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(fixbar + 1);
+  uint64_t *tfull = empty + STAGES;   // [NACC]
+  uint64_t *tempty = tfull + C::NACC; // [NACC]
+  uint64_t *fixbar = tempty + C::NACC;   // [NH], one per half
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(fixbar + 2);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -234,11 +271,11 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], p.cluster);   // every CTA of the cluster releases the stage
     }
-    for (int a = 0; a < 2; ++a) {
+    for (int a = 0; a < C::NACC; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 128);
+      mbar_init(&tempty[a], EPI_THREADS);
     }
-    mbar_init(fixbar, 1);
+    for (int h = 0; h < NH; ++h) mbar_init(&fixbar[h], 1);
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tmA);
@@ -268,6 +305,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       bool ok = true;
       while (ok && segs.next(sg)) {
         const int m0 = (sg.tile % p.tiles_m) * BM;
+        const int nh = halves_of<NH>(p, m0);
         const int nt = sg.tile / p.tiles_m;
         const int rows0 = EPI == kEpiSwiGLU ? nt * 128 : nt * BN;
         const int rows1 = EPI == kEpiSwiGLU ? p.F + nt * 128 : nt * BN + 128;
@@ -288,8 +326,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&full[s], A_STAGE + B_STAGE);
+          mbar_arrive_expect_tx(&full[s], nh * A_HALF + B_STAGE);
           tma_load_2d(sA + s * A_STAGE, &tmA, &full[s], kb * BK, m0);
+          if (nh == 2) tma_load_2d(sA + s * A_STAGE + A_HALF, &tmA, &full[s], kb * BK, m0 + HM);
           if (p.cluster == 1) {
             tma_load_2d(sB + s * B_STAGE, &tmB, &full[s], kb * BK, rows0);
             tma_load_2d(sB + s * B_STAGE + B_STAGE / 2, &tmB, &full[s], kb * BK, rows1);
@@ -329,9 +368,11 @@ __global__ void __launch_bounds__(THREADS, 1)
       uint32_t acc_ph = 0;
       bool ok = true;
       while (ok && segs.next(sg)) {
+        const int nh = halves_of<NH>(p, (sg.tile % p.tiles_m) * BM);
+        // the epilogue has drained this accumulator buffer's previous tile
         if (!mbar_wait(&tempty[acc], acc_ph ^ 1, abort_flag, p.err, kErrWaitMma)) break;
         tc_fence_after();
-        const uint32_t d = tmem + acc * BN;
+        const uint32_t d = tmem + acc * NH * BN;
         for (int kb = sg.k0; kb < sg.k1; ++kb) {
           if (!mbar_wait(&full[s], ph, abort_flag, p.err, kErrWaitMma)) {
             ok = false;
@@ -342,9 +383,10 @@ __global__ void __launch_bounds__(THREADS, 1)
           const uint32_t b0 = smem_u32(sB + s * B_STAGE);
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
-            const uint64_t ad = sdesc_sw128(a0 + kk * 32, 16, 1024);
             const uint64_t bd = sdesc_sw128(b0 + kk * 32, 16, 1024);
-            mma_bf16(d, ad, bd, IDESC, (kb > sg.k0 || kk > 0) ? 1u : 0u);
+            const uint32_t accum = (kb > sg.k0 || kk > 0) ? 1u : 0u;
+            mma_bf16(d, sdesc_sw128(a0 + kk * 32, 16, 1024), bd, IDESC, accum);
+            if (nh == 2) mma_bf16(d + BN, sdesc_sw128(a0 + A_HALF + kk * 32, 16, 1024), bd, IDESC, accum);
           }
           if (p.cluster > 1)
             mma_commit_mc(&empty[s], cmask);
@@ -357,15 +399,20 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         if (!ok) break;
         mma_commit(&tfull[acc]);
-        acc ^= 1;
-        if (acc == 0) acc_ph ^= 1;
+        if (++acc == C::NACC) {
+          acc = 0;
+          acc_ph ^= 1;
+        }
       }
     }
   } else {
     // ------------------------------------------------------------ epilogue
+    // Every branch below that contains a named barrier is taken by all 256
+    // epilogue threads or by none (decisions go through barrier ORs).
     const int q = warp & 3;            // TMEM lane quarter this warp may read
-    const int r = q * 32 + lane;       // row within the tile
-    const int ep = threadIdx.x - 64;   // 0..127
+    const int h = (warp - 2) >> 2;     // half of the tile (TMEM columns h*256 ..)
+    const int r = q * 32 + lane;       // row within the half
+    const int ep = threadIdx.x - 64;   // 0 .. EPI_THREADS-1
     SegIter segs(p);
     Seg sg;
     int acc = 0;
@@ -375,14 +422,18 @@ __global__ void __launch_bounds__(THREADS, 1)
     while (ok && segs.next(sg)) {
       const int mi = sg.tile % p.tiles_m;
       const int m0 = mi * BM;
+      const bool mine = h < halves_of<NH>(p, m0);   // this half holds rows of A
       const int nt = sg.tile / p.tiles_m;
-      const int row = m0 + r;
+      const int row = m0 + h * HM + r;
       const int col0 = EPI == kEpiSwiGLU ? nt * 128 : nt * BN;
       uint4 rb[16];
-      if (EPI == kEpiResidual) load_resid4(p, row, col0, rb);   // independent of the accumulator
-      if (!mbar_wait(&tfull[acc], acc_ph, abort_flag, p.err, kErrWaitEpilogue)) break;
+      // the residual does not depend on the accumulator: fetch it while the
+      // MMAs run (a split tile fetches it after its fix-up instead)
+      if (EPI == kEpiResidual && mine && !sg.partial) load_resid4(p, row, col0, rb);
+      const bool got = mbar_wait(&tfull[acc], acc_ph, abort_flag, p.err, kErrWaitEpilogue);
+      if (named_bar_or(1, EPI_THREADS, !got)) break;
       tc_fence_after();
-      const uint32_t tbase = tmem + acc * BN + (static_cast<uint32_t>(q * 32) << 16);
+      const uint32_t tbase = tmem + (acc * NH + h) * BN + (static_cast<uint32_t>(q * 32) << 16);
       bool finish = !sg.partial;
       if (sg.partial) {
         int r_first, r_last;
@@ -394,19 +445,21 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (my_rank != r_first) {
           // a later piece: hand the fp32 partial to the rank that covers the
           // unit's head (for which this unit is its last segment)
+          if (mine) {
 #pragma unroll 1
-          for (int j = 0; j < BN / 32; ++j) {
-            float v[32];
-            tmem_ld32(tbase + 32 * j, v);
-            float4 *w4 = reinterpret_cast<float4 *>(part_chunk(p, sg.slot, j, r));
+            for (int j = 0; j < BN / 32; ++j) {
+              float v[32];
+              tmem_ld32(tbase + 32 * j, v);
+              float4 *w4 = reinterpret_cast<float4 *>(part_chunk<NH>(p, sg.slot, h, j, r));
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              w4[part_swz(i, r)] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+              for (int i = 0; i < 8; ++i)
+                w4[part_swz(i, r)] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+            }
           }
           tc_fence_before();
           mbar_arrive(&tempty[acc]);
           __threadfence();
-          named_bar_sync(1, 128);
+          named_bar_sync(1, EPI_THREADS);
           if (ep == 0) atomicAdd(flag, 1);
         } else {
           // the head piece: wait for the other pieces (written early in their
@@ -425,42 +478,53 @@ __global__ void __launch_bounds__(THREADS, 1)
             *flag = 0;
             fence_proxy_async_global();
           }
-          named_bar_sync(1, 128);
-          if (*abort_flag) {
+          if (named_bar_or(1, EPI_THREADS, *abort_flag != 0)) {
             ok = false;
           } else {
-            // this unit is the rank's last segment: the stage buffers are idle
-            uint8_t *stage = smem;
+            // this unit is the rank's last segment: the stage buffers are idle;
+            // each half stages FIX_CHUNKS of its 8 chunks at a time in its own area
+            uint8_t *stage = smem + h * C::FIX_CHUNKS * CHUNK;
 #pragma unroll 1
-            for (int rk = r_first + 1; rk <= r_last; ++rk) {
-              if (ep == 0) {
-                const int slot = slot_of(p, rk, mi, sg.unit);
-                mbar_arrive_expect_tx(fixbar, 8 * 16384);
-                for (int j = 0; j < 8; ++j) bulk_load(stage + j * 16384, part_chunk(p, slot, j, 0), 16384, fixbar);
-              }
-              const bool got = __all_sync(0xffffffffu, mbar_wait(fixbar, fix_ph, abort_flag, p.err, kErrWaitEpilogue));
-              fix_ph ^= 1;
-              // leave together: the barrier at the end of each pass is shared
-              if (named_bar_or(1, 128, !got)) {
-                ok = false;
-                break;
-              }
+            for (int rk = r_first + 1; rk <= r_last && ok; ++rk) {
+              const int slot = slot_of(p, rk, mi, sg.unit);
 #pragma unroll 1
-              for (int j = 0; j < 8; ++j) {
-                float v[32];
-                tmem_ld32(tbase + 32 * j, v);
-                const float4 *src = reinterpret_cast<const float4 *>(stage + j * 16384 + r * 128);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                  const float4 t = src[part_swz(i, r)];
-                  v[4 * i] += t.x;
-                  v[4 * i + 1] += t.y;
-                  v[4 * i + 2] += t.z;
-                  v[4 * i + 3] += t.w;
+              for (int rr = 0; rr < 8 / C::FIX_CHUNKS; ++rr) {
+                bool fine = true;
+                if (mine) {
+                  if (q == 0 && lane == 0) {
+                    mbar_arrive_expect_tx(&fixbar[h], C::FIX_CHUNKS * CHUNK);
+                    for (int jj = 0; jj < C::FIX_CHUNKS; ++jj)
+                      bulk_load(stage + jj * CHUNK, part_chunk<NH>(p, slot, h, rr * C::FIX_CHUNKS + jj, 0), CHUNK,
+                                &fixbar[h]);
+                  }
+                  fine = __all_sync(0xffffffffu, mbar_wait(&fixbar[h], fix_ph, abort_flag, p.err, kErrWaitEpilogue));
+                  fix_ph ^= 1;
                 }
-                tmem_st32(tbase + 32 * j, v);
+                // leave together: the barrier at the end of each pass is shared
+                if (named_bar_or(1, EPI_THREADS, !fine)) {
+                  ok = false;
+                  break;
+                }
+                if (mine) {
+#pragma unroll 1
+                  for (int jj = 0; jj < C::FIX_CHUNKS; ++jj) {
+                    const int j = rr * C::FIX_CHUNKS + jj;
+                    float v[32];
+                    tmem_ld32(tbase + 32 * j, v);
+                    const float4 *src = reinterpret_cast<const float4 *>(stage + jj * CHUNK + r * 128);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                      const float4 t = src[part_swz(i, r)];
+                      v[4 * i] += t.x;
+                      v[4 * i + 1] += t.y;
+                      v[4 * i + 2] += t.z;
+                      v[4 * i + 3] += t.w;
+                    }
+                    tmem_st32(tbase + 32 * j, v);
+                  }
+                }
+                named_bar_sync(1, EPI_THREADS);   // the next copy overwrites the staging
               }
-              named_bar_sync(1, 128);   // the next copy overwrites the stage buffers
             }
             finish = ok;
           }
@@ -471,38 +535,43 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       }
       if (finish) {
-        if (EPI == kEpiSwiGLU) {
+        if (mine) {
+          if (EPI == kEpiSwiGLU) {
 #pragma unroll 1
-          for (int j = 0; j < 4; ++j) {
-            float g[32], u[32];
-            tmem_ld32(tbase + 32 * j, g);
-            tmem_ld32(tbase + 128 + 32 * j, u);
-            store_chunk<EPI>(p, row, col0 + 32 * j, g, u, nullptr);
-          }
-        } else if (EPI == kEpiResidual) {
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            if (h == 1) load_resid4(p, row, col0 + 128, rb);
-#pragma unroll
             for (int j = 0; j < 4; ++j) {
-              float v[32];
-              tmem_ld32(tbase + 128 * h + 32 * j, v);
-              store_chunk<EPI>(p, row, col0 + 128 * h + 32 * j, v, nullptr, rb + 4 * j);
+              float g[32], u[32];
+              tmem_ld32(tbase + 32 * j, g);
+              tmem_ld32(tbase + 128 + 32 * j, u);
+              store_chunk<EPI>(p, row, col0 + 32 * j, g, u, nullptr);
             }
-          }
-        } else {
+          } else if (EPI == kEpiResidual) {
+            if (sg.partial) load_resid4(p, row, col0, rb);
+#pragma unroll
+            for (int hc = 0; hc < 2; ++hc) {
+              if (hc == 1) load_resid4(p, row, col0 + 128, rb);
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                float v[32];
+                tmem_ld32(tbase + 128 * hc + 32 * j, v);
+                store_chunk<EPI>(p, row, col0 + 128 * hc + 32 * j, v, nullptr, rb + 4 * j);
+              }
+            }
+          } else {
 #pragma unroll 1
-          for (int j = 0; j < BN / 32; ++j) {
-            float v[32];
-            tmem_ld32(tbase + 32 * j, v);
-            store_chunk<EPI>(p, row, col0 + 32 * j, v, nullptr, nullptr);
+            for (int j = 0; j < BN / 32; ++j) {
+              float v[32];
+              tmem_ld32(tbase + 32 * j, v);
+              store_chunk<EPI>(p, row, col0 + 32 * j, v, nullptr, nullptr);
+            }
           }
         }
         tc_fence_before();
         mbar_arrive(&tempty[acc]);
       }
-      acc ^= 1;
-      if (acc == 0) acc_ph ^= 1;
+      if (++acc == C::NACC) {
+        acc = 0;
+        acc_ph ^= 1;
+      }
     }
   }
 
@@ -516,18 +585,19 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
-template <int EPI>
+template <int EPI, int NH>
 cudaError_t launch(const CUtensorMap &tmA, const CUtensorMap &tmB, const Params &p, cudaStream_t st) {
+  using C = TileCfg<NH>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    attr_err = cudaFuncSetAttribute(gemm_kernel<EPI, NH>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   });
   if (attr_err != cudaSuccess) return attr_err;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.grid);
-  cfg.blockDim = dim3(THREADS);
-  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.blockDim = dim3(C::THREADS);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -536,23 +606,42 @@ cudaError_t launch(const CUtensorMap &tmA, const CUtensorMap &tmB, const Params 
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemm_kernel<EPI>, tmA, tmB, p);
+  return cudaLaunchKernelEx(&cfg, gemm_kernel<EPI, NH>, tmA, tmB, p);
+}
+
+cudaError_t launch_for(int epi, int nh, const CUtensorMap &tmA, const CUtensorMap &tmB, const Params &p,
+                       cudaStream_t st) {
+  if (nh == 2) {
+    switch (epi) {
+      case kEpiStore: return launch<kEpiStore, 2>(tmA, tmB, p, st);
+      case kEpiResidual: return launch<kEpiResidual, 2>(tmA, tmB, p, st);
+      case kEpiSwiGLU: return launch<kEpiSwiGLU, 2>(tmA, tmB, p, st);
+      default: return cudaErrorInvalidValue;
+    }
+  }
+  switch (epi) {
+    case kEpiStore: return launch<kEpiStore, 1>(tmA, tmB, p, st);
+    case kEpiResidual: return launch<kEpiResidual, 1>(tmA, tmB, p, st);
+    case kEpiSwiGLU: return launch<kEpiSwiGLU, 1>(tmA, tmB, p, st);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 // Clusters of `size` CTAs of this kernel that can be resident at once (the
 // split fix-up waits on other CTAs, so the whole grid must be co-resident).
-template <int EPI>
+template <int EPI, int NH>
 int max_clusters(int size) {
+  using C = TileCfg<NH>;
   static std::mutex mu;
   static int cache[9] = {0};
   std::lock_guard<std::mutex> lk(mu);
   if (size < 1 || size > 8) return 0;
   if (cache[size] == 0) {
-    cudaFuncSetAttribute(gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    cudaFuncSetAttribute(gemm_kernel<EPI, NH>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(size * 64);
-    cfg.blockDim = dim3(THREADS);
-    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.blockDim = dim3(C::THREADS);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = size;
@@ -561,7 +650,7 @@ int max_clusters(int size) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, gemm_kernel<EPI>, &cfg) != cudaSuccess || n <= 0) n = -1;
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_kernel<EPI, NH>, &cfg) != cudaSuccess || n <= 0) n = -1;
     cache[size] = n;
   }
   return cache[size];
@@ -569,23 +658,24 @@ int max_clusters(int size) {
 
 int max_clusters_for(int epi, int size) {
   switch (epi) {
-    case kEpiStore: return max_clusters<kEpiStore>(size);
-    case kEpiResidual: return max_clusters<kEpiResidual>(size);
-    default: return max_clusters<kEpiSwiGLU>(size);
+    case kEpiStore: return max_clusters<kEpiStore, 1>(size);
+    case kEpiResidual: return max_clusters<kEpiResidual, 1>(size);
+    default: return max_clusters<kEpiSwiGLU, 1>(size);
   }
 }
 
 }  // namespace
 
+constexpr size_t kPartialSlotBytes = static_cast<size_t>(kMaxHalves) * HM * BN * sizeof(float);
+
 size_t gemm_workspace_bytes() {
-  return static_cast<size_t>(2 * kMaxGemmGrid) * BM * BN * sizeof(float) + 2 * kMaxGemmGrid * sizeof(int);
+  return static_cast<size_t>(2 * kMaxGemmGrid) * kPartialSlotBytes + 2 * kMaxGemmGrid * sizeof(int);
 }
 
 GemmWorkspace gemm_workspace_carve(void *base) {
   GemmWorkspace w;
   w.partials = static_cast<float *>(base);
-  w.tickets = reinterpret_cast<int *>(static_cast<char *>(base) +
-                                      static_cast<size_t>(2 * kMaxGemmGrid) * BM * BN * sizeof(float));
+  w.tickets = reinterpret_cast<int *>(static_cast<char *>(base) + static_cast<size_t>(2 * kMaxGemmGrid) * kPartialSlotBytes);
   return w;
 }
 
@@ -594,7 +684,7 @@ cudaError_t gemm_run(const void *A, const void *B, const CUtensorMap *tmB_pre, v
   if (M <= 0) return cudaSuccess;
   const int b_rows = epi == kEpiSwiGLU ? 2 * N : N;
   CUtensorMap tmA, tmB;
-  cudaError_t e = encode_tmap_2d(&tmA, A, K, M, static_cast<uint64_t>(K) * 2, BK, BM);
+  cudaError_t e = encode_tmap_2d(&tmA, A, K, M, static_cast<uint64_t>(K) * 2, BK, HM);
   if (e != cudaSuccess) return e;
   if (tmB_pre) {
     tmB = *tmB_pre;
@@ -607,7 +697,8 @@ cudaError_t gemm_run(const void *A, const void *B, const CUtensorMap *tmB_pre, v
   p.N = N;
   p.K = K;
   p.k_iters = K / BK;
-  p.tiles_m = (M + BM - 1) / BM;
+  const int nh = M >= kWideMinRows ? 2 : 1;
+  p.tiles_m = (M + nh * HM - 1) / (nh * HM);
   p.tiles_n = epi == kEpiSwiGLU ? N / 128 : (N + BN - 1) / BN;
   const int tiles = p.tiles_m * p.tiles_n;
   const int sms = device_sm_count() < kMaxGemmGrid ? device_sm_count() : kMaxGemmGrid;
@@ -616,7 +707,9 @@ cudaError_t gemm_run(const void *A, const void *B, const CUtensorMap *tmB_pre, v
     // side by side, and the (N-tile, k) space is split evenly over the groups.
     long long groups = sms / p.tiles_m;
     p.cluster = 1;
-    if (MB_GEMM_MULTICAST && p.tiles_m > 1) {
+    // multicast pays for 128-row tiles (more CTAs per weight tile); with
+    // 256-row tiles the cluster's lockstep costs more than it saves
+    if (MB_GEMM_MULTICAST && nh == 1 && p.tiles_m > 1) {
       const int mc = max_clusters_for(epi, p.tiles_m);
       if (mc > 0) {
         p.cluster = p.tiles_m;
@@ -657,12 +750,7 @@ cudaError_t gemm_run(const void *A, const void *B, const CUtensorMap *tmB_pre, v
   p.partials = ws.partials;
   p.tickets = ws.tickets;
   p.err = err;
-  switch (epi) {
-    case kEpiStore: return launch<kEpiStore>(tmA, tmB, p, st);
-    case kEpiResidual: return launch<kEpiResidual>(tmA, tmB, p, st);
-    case kEpiSwiGLU: return launch<kEpiSwiGLU>(tmA, tmB, p, st);
-    default: return cudaErrorInvalidValue;
-  }
+  return launch_for(epi, nh, tmA, tmB, p, st);
 }
 
 }  // namespace mb
@@ -690,7 +778,7 @@ namespace mb {
 namespace {
 
 constexpr int kNoAllocGrid = 64;
-constexpr size_t kNoAllocPartialBytes = static_cast<size_t>(2 * kNoAllocGrid) * BM * BN * sizeof(float);
+constexpr size_t kNoAllocPartialBytes = static_cast<size_t>(2 * kNoAllocGrid) * TileCfg<1>::BM * BN * sizeof(float);
 constexpr size_t kNoAllocTailBytes = 4096;  // tickets, then the error word in the last 16 bytes
 static_assert(sizeof(g_gemm_noalloc_scratch) == kNoAllocPartialBytes + kNoAllocTailBytes, "scratch layout");
 
@@ -746,7 +834,7 @@ extern "C" mb_status mb_gemm_noalloc(const void *A, const void *B, void *D, cons
   p.N = N;
   p.K = K;
   p.k_iters = K / BK;
-  p.tiles_m = (M + BM - 1) / BM;
+  p.tiles_m = (M + TileCfg<1>::BM - 1) / TileCfg<1>::BM;
   p.tiles_n = epilogue == kEpiSwiGLU ? N / 128 : (N + BN - 1) / BN;
   const long long tiles = static_cast<long long>(p.tiles_m) * p.tiles_n;
   p.cluster = 1;
@@ -762,7 +850,7 @@ extern "C" mb_status mb_gemm_noalloc(const void *A, const void *B, void *D, cons
     if (sk_iters < 2LL * g) g = sk_iters / 2 > 0 ? sk_iters / 2 : 1;
     p.grid = static_cast<int>(g);
   }
-  const size_t need_partials = p.sk_tiles ? static_cast<size_t>(2 * p.grid) * BM * BN * sizeof(float) : 0;
+  const size_t need_partials = p.sk_tiles ? static_cast<size_t>(2 * p.grid) * TileCfg<1>::BM * BN * sizeof(float) : 0;
   const size_t need_tickets = static_cast<size_t>(p.sk_tiles) * sizeof(int);
   if (need_partials > kNoAllocPartialBytes || need_tickets > kNoAllocTailBytes - 16)
     return fail(MB_EUNSUPPORTED,
@@ -780,7 +868,7 @@ extern "C" mb_status mb_gemm_noalloc(const void *A, const void *B, void *D, cons
 
   const int b_rows = epilogue == kEpiSwiGLU ? 2 * N : N;
   CUtensorMap tmA, tmB;
-  e = encode_tmap_2d(&tmA, A, K, M, static_cast<uint64_t>(K) * 2, BK, BM);
+  e = encode_tmap_2d(&tmA, A, K, M, static_cast<uint64_t>(K) * 2, BK, HM);
   if (e == cudaSuccess) e = encode_tmap_2d(&tmB, B, K, b_rows, static_cast<uint64_t>(K) * 2, BK, 128);
   if (e != cudaSuccess) return fail(MB_ECUDA, "mb_gemm_noalloc: tensor map encoding failed");
   p.D = static_cast<__nv_bfloat16 *>(D);
@@ -791,11 +879,7 @@ extern "C" mb_status mb_gemm_noalloc(const void *A, const void *B, void *D, cons
   p.partials = reinterpret_cast<float *>(base);
   p.tickets = reinterpret_cast<int *>(base + kNoAllocPartialBytes);
   p.err = reinterpret_cast<int *>(base + kNoAllocPartialBytes + kNoAllocTailBytes - 16);
-  switch (epilogue) {
-    case kEpiStore: e = launch<kEpiStore>(tmA, tmB, p, st); break;
-    case kEpiResidual: e = launch<kEpiResidual>(tmA, tmB, p, st); break;
-    default: e = launch<kEpiSwiGLU>(tmA, tmB, p, st); break;
-  }
+  e = launch_for(epilogue, 1, tmA, tmB, p, st);   // 128-row tiles: their partials fit the array
   if (e != cudaSuccess) return fail(MB_ECUDA, "mb_gemm_noalloc: launch: %s", cudaGetErrorString(e));
   return MB_OK;
 }

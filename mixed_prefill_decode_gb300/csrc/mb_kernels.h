@@ -22,7 +22,7 @@ int device_sm_count();
 enum GemmEpilogue : int { kEpiStore = 0, kEpiResidual = 1, kEpiSwiGLU = 2 };
 
 struct GemmWorkspace {
-  float *partials;  // [2 * kMaxGemmGrid][128][256] fp32
+  float *partials;  // [2 * kMaxGemmGrid][256][256] fp32
   int *tickets;     // [2 * kMaxGemmGrid]
 };
 constexpr int kMaxGemmGrid = 256;

@@ -17,6 +17,9 @@ SHAPES = [
     (1, 256, 64), (68, 768, 256), (68, 256, 1024), (129, 640, 512), (200, 1536, 512),
     (300, 512, 1536), (576, 6144, 4096), (576, 4096, 4096), (16, 7168, 5120), (1040, 5120, 5120),
     (2216, 512, 128),
+    # 256-row tiles (from 1,024 tokens on): a ragged last half, a tile with one
+    # half, split and data-parallel schedules
+    (1100, 1536, 512), (1300, 768, 1024), (2144, 2560, 2048), (4100, 512, 256),
 ]
 
 
@@ -43,7 +46,7 @@ def test_gemm_store_and_residual(mb, M, N, K, epi):
 
 
 @pytest.mark.parametrize("M,F,K", [(68, 1024, 256), (200, 1536, 512), (576, 14336, 4096), (16, 17408, 5120),
-                                   (130, 128, 64)])
+                                   (130, 128, 64), (1040, 1024, 512), (2216, 2048, 1024)])
 def test_gemm_swiglu(mb, M, F, K):
     A, B, _ = _inputs(M, 2 * F, K, M + F + K)
     dA, dB = to_dev(A), to_dev(B)
