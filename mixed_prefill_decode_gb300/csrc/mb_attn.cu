@@ -28,6 +28,7 @@
 #include <mutex>
 
 #include "mb_kernels.h"
+#include "mb_launch.cuh"
 #include "mb_ptx.cuh"
 
 namespace mb {
@@ -132,6 +133,7 @@ __device__ __forceinline__ void chunk_tile(const CUtensorMap &tmQ, const CUtenso
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_wait();   // q, the KV pool and o belong to earlier kernels of the stream
 
   if (warp == 0) {
     if (lane == 0) {
@@ -670,6 +672,7 @@ __device__ __forceinline__ void decode_item(const DecodeParams &p, int item, uin
 template <int HD>
 __global__ void __launch_bounds__(128) merge_kernel(const float *part, const int32_t *list, int n, __nv_bfloat16 *o,
                                                     const int32_t *qo_indptr, int Hq, int G) {
+  pdl_wait();
   const int w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   if (w >= n * G) return;
   const int lane = threadIdx.x & 31;
@@ -732,12 +735,14 @@ __global__ void __launch_bounds__(FusedCfg<HD>::THREADS, 1)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   if (smem_u32(smem_raw) & 1023u) {
     // the layouts above need a 1024-aligned base and reserve no slack
+    pdl_wait();
     if (threadIdx.x == 0) atomicExch(cp.err, kErrBounds);
     return;
   }
   if (static_cast<int>(blockIdx.x) < n_tiles) {
-    chunk_tile<HD>(tmQ, tmKV, cp, blockIdx.x, smem_raw);
+    chunk_tile<HD>(tmQ, tmKV, cp, blockIdx.x, smem_raw);   // waits after its set-up
   } else {
+    pdl_wait();
     // warps 0-4 take item 2k, warps 5-9 item 2k + 1 (if it exists)
     using F = FusedCfg<HD>;
     const int half = threadIdx.x >= (F::DEC_NW + 1) * 32;
@@ -758,9 +763,8 @@ cudaError_t launch_attention(const CUtensorMap &tq, const CUtensorMap &tkv, cons
                                     FusedCfg<HD>::SMEM);
   });
   if (attr_err != cudaSuccess) return attr_err;
-  attention_kernel<HD, G><<<n_tiles + (n_items + 1) / 2, FusedCfg<HD>::THREADS, FusedCfg<HD>::SMEM, st>>>(
-      tq, tkv, cp, dp, n_tiles);
-  return cudaGetLastError();
+  return launch_pdl(attention_kernel<HD, G>, dim3(n_tiles + (n_items + 1) / 2), dim3(FusedCfg<HD>::THREADS),
+                    FusedCfg<HD>::SMEM, st, 1, tq, tkv, cp, dp, n_tiles);
 }
 
 template <int HD>
@@ -822,13 +826,12 @@ cudaError_t attn_merge_run(const MergeArgs &m, cudaStream_t st) {
   const int G = m.Hq / m.Hkv;
   const int warps = m.n_merge * G;
   const int blocks = (warps + 3) / 4;
+  __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(m.o);
   if (m.hd == 128)
-    merge_kernel<128><<<blocks, 128, 0, st>>>(m.part, m.merge_list, m.n_merge, static_cast<__nv_bfloat16 *>(m.o),
-                                              m.qo_indptr, m.Hq, G);
-  else
-    merge_kernel<64><<<blocks, 128, 0, st>>>(m.part, m.merge_list, m.n_merge, static_cast<__nv_bfloat16 *>(m.o),
-                                             m.qo_indptr, m.Hq, G);
-  return cudaGetLastError();
+    return launch_pdl(merge_kernel<128>, dim3(blocks), dim3(128), 0, st, 1, m.part, m.merge_list, m.n_merge, o,
+                      m.qo_indptr, m.Hq, G);
+  return launch_pdl(merge_kernel<64>, dim3(blocks), dim3(128), 0, st, 1, m.part, m.merge_list, m.n_merge, o,
+                    m.qo_indptr, m.Hq, G);
 }
 
 }  // namespace mb

@@ -11,6 +11,7 @@
 #include <cstdint>
 
 #include "mb_kernels.h"
+#include "mb_launch.cuh"
 #include "mb_ptx.cuh"
 
 namespace mb {
@@ -26,6 +27,7 @@ constexpr int kNormMaxVec = 8;  // d <= 128 * 8 * 8 = 8192
 __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const __nv_bfloat16 *__restrict__ x,
                                                                const __nv_bfloat16 *__restrict__ g,
                                                                __nv_bfloat16 *__restrict__ y, int d, float eps) {
+  pdl_wait();
   const int row = blockIdx.x;
   const int nv = d / 8;
   const uint4 *xr = reinterpret_cast<const uint4 *>(x + static_cast<size_t>(row) * d);
@@ -100,6 +102,7 @@ __global__ void __launch_bounds__(kRopeThreads) rope_append_kernel(const RopePar
   constexpr int HALF = HD / 2;
   constexpr int PAIRS = HALF / 32;  // pairs per lane
   __shared__ float cs[HALF], sn[HALF];
+  pdl_wait();
   const int t = blockIdx.x;
   const int pos = p.tok_pos[t];
   for (int i = threadIdx.x; i < HALF; i += kRopeThreads) {
@@ -183,10 +186,8 @@ __global__ void __launch_bounds__(kRopeThreads) rope_append_kernel(const RopePar
 cudaError_t rmsnorm_run(const void *x, const void *g, void *y, int rows, int d, float eps, cudaStream_t st) {
   if (rows <= 0) return cudaSuccess;
   if (d % 8 != 0 || d > kNormThreads * kNormMaxVec * 8) return cudaErrorInvalidValue;
-  rmsnorm_kernel<<<rows, kNormThreads, 0, st>>>(static_cast<const __nv_bfloat16 *>(x),
-                                                static_cast<const __nv_bfloat16 *>(g),
-                                                static_cast<__nv_bfloat16 *>(y), d, eps);
-  return cudaGetLastError();
+  return launch_pdl(rmsnorm_kernel, dim3(rows), dim3(kNormThreads), 0, st, 1, static_cast<const __nv_bfloat16 *>(x),
+                    static_cast<const __nv_bfloat16 *>(g), static_cast<__nv_bfloat16 *>(y), d, eps);
 }
 
 cudaError_t rope_append_run(const RopeArgs &a, cudaStream_t st) {
@@ -213,13 +214,9 @@ cudaError_t rope_append_run(const RopeArgs &a, cudaStream_t st) {
     p.f_hi[i] = static_cast<float>(f);
     p.f_lo[i] = static_cast<float>(f - static_cast<double>(p.f_hi[i]));
   }
-  if (a.hd == 128)
-    rope_append_kernel<128><<<a.T, kRopeThreads, 0, st>>>(p);
-  else if (a.hd == 64)
-    rope_append_kernel<64><<<a.T, kRopeThreads, 0, st>>>(p);
-  else
-    return cudaErrorInvalidValue;
-  return cudaGetLastError();
+  if (a.hd == 128) return launch_pdl(rope_append_kernel<128>, dim3(a.T), dim3(kRopeThreads), 0, st, 1, p);
+  if (a.hd == 64) return launch_pdl(rope_append_kernel<64>, dim3(a.T), dim3(kRopeThreads), 0, st, 1, p);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace mb

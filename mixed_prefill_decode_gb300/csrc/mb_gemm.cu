@@ -41,6 +41,7 @@
 #include "mb.h"
 #include "mb_internal.h"
 #include "mb_kernels.h"
+#include "mb_launch.cuh"
 #include "mb_ptx.cuh"
 
 namespace mb {
@@ -293,6 +294,24 @@ __global__ void __launch_bounds__(TileCfg<NH>::THREADS, 1)
   if (p.cluster > 1) cluster_sync();
   const uint32_t crank = p.cluster > 1 ? cluster_ctarank() : 0;
   const uint16_t cmask = static_cast<uint16_t>((1u << p.cluster) - 1u);
+
+  if (warp == 0 && lane == 0) {
+    // The weights are read-only for the whole stream: start pulling this
+    // CTA's first weight k-blocks into L2 while earlier kernels finish.
+    SegIter first(p);
+    Seg s0;
+    const bool prefetcher = p.grouped ? (blockIdx.x % p.tiles_m) == 0 : true;
+    if (prefetcher && first.next(s0)) {
+      const int nt = s0.tile / p.tiles_m;
+      const int rows0 = EPI == kEpiSwiGLU ? nt * 128 : nt * BN;
+      const int rows1 = EPI == kEpiSwiGLU ? p.F + nt * 128 : nt * BN + 128;
+      for (int kb = s0.k0; kb < s0.k1 && kb < s0.k0 + kPrefetchAhead; ++kb) {
+        tma_prefetch_2d(&tmB, kb * BK, rows0);
+        tma_prefetch_2d(&tmB, kb * BK, rows1);
+      }
+    }
+  }
+  pdl_wait();   // A, R, D, the tickets and partials belong to earlier kernels of the stream
 
   if (warp == 0) {
     if (lane == 0) {
@@ -594,19 +613,7 @@ cudaError_t launch(const CUtensorMap &tmA, const CUtensorMap &tmB, const Params 
     attr_err = cudaFuncSetAttribute(gemm_kernel<EPI, NH>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   });
   if (attr_err != cudaSuccess) return attr_err;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.grid);
-  cfg.blockDim = dim3(C::THREADS);
-  cfg.dynamicSmemBytes = C::SMEM_BYTES;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = p.cluster > 1 ? p.cluster : 1;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemm_kernel<EPI, NH>, tmA, tmB, p);
+  return launch_pdl(gemm_kernel<EPI, NH>, dim3(p.grid), dim3(C::THREADS), C::SMEM_BYTES, st, p.cluster, tmA, tmB, p);
 }
 
 cudaError_t launch_for(int epi, int nh, const CUtensorMap &tmA, const CUtensorMap &tmB, const Params &p,

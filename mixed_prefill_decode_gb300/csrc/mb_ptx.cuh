@@ -60,6 +60,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Programmatic dependent launch (see mb_launch.cuh): wait until every earlier
+// kernel of the stream has finished and its writes are visible.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Non-blocking probe of a phase (try_wait may suspend the thread for a while;
 // a thread that polls two barriers must not sleep on either).
 __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
