@@ -19,6 +19,10 @@
 #include "mb_internal.h"
 #include "mb_kernels.h"
 
+#ifndef MB_DEC_ITEMS_PER_SM
+#define MB_DEC_ITEMS_PER_SM 8
+#endif
+
 namespace mb {
 
 static thread_local std::string g_last_error;
@@ -386,9 +390,10 @@ mb_status prepare_step(mb_layer *L, const mb_batch *b, int64_t T, cudaStream_t s
     hb[P.o_tiles + 4 * i + 1] = tiles[i].i0;
     hb[P.o_tiles + 4 * i + 2] = tiles[i].h;
   }
-  // decode splits: about four items per SM (two per resident CTA of the
-  // attention grid), each request's pages divided evenly among its splits
-  const int64_t target_items = static_cast<int64_t>(ctx->sms) * 4;
+  // decode splits: about MB_DEC_ITEMS_PER_SM items per SM, each request's
+  // pages divided evenly among its splits, at least one 128-key block per
+  // item.  Workers take items dynamically, so the tail is about one item long.
+  const int64_t target_items = static_cast<int64_t>(ctx->sms) * MB_DEC_ITEMS_PER_SM;
   int64_t pps = (dec_pages * Hkv + target_items - 1) / std::max<int64_t>(1, target_items);
   pps = std::max<int64_t>(pps, 8);
   std::vector<int32_t> items, merges;
@@ -518,8 +523,9 @@ mb_status launch_layer(mb_layer *L, mb_layer *W, mb_kv *kv, const StepPlan &P, c
   if ((st = chk(mb::rope_append_run(ra, s), "rope/append")) != MB_OK) return st;
   ++*launches;
   mark(3);
-  CUtensorMap tm_q;
+  CUtensorMap tm_q, tm_qd;
   cudaError_t e = mb::encode_tmap_2d(&tm_q, W->q, hqd, Ti, hqd * 2ull, 64, 128);
+  if (e == cudaSuccess) e = mb::encode_tmap_2d(&tm_qd, W->q, hd, static_cast<uint64_t>(Ti) * Hq, hd * 2ull, 64, 16);
   if (e != cudaSuccess) return mb::fail(MB_ECUDA, "step: Q tensor map");
   mb::AttnArgs aa;
   aa.q = W->q;
@@ -541,7 +547,9 @@ mb_status launch_layer(mb_layer *L, mb_layer *W, mb_kv *kv, const StepPlan &P, c
   aa.num_pages = kv->num_pages;
   aa.err = W->err;
   aa.tm_q = &tm_q;
+  aa.tm_qd = &tm_qd;
   aa.tm_kv = &kv->tmap;
+  aa.dec_ctr = W->err + 2;   // words 2-3 of the layer's error block
   if ((st = chk(mb::attention_run(aa, s), "attention")) != MB_OK) return st;
   *launches += (aa.n_tiles + aa.n_items) > 0;
   mark(4);

@@ -136,39 +136,49 @@ __device__ __forceinline__ void chunk_tile(const CUtensorMap &tmQ, const CUtenso
   pdl_wait();   // q, the KV pool and o belong to earlier kernels of the stream
 
   if (warp == 0) {
+    // -------------------------------------------------------- TMA producer
+    // Lane 0 waits and arms each stage; the block's 8 pages x (K, V) x hd
+    // chunks then go out as one TMA per lane (one thread issuing all of them
+    // would pace the ring at ~90 cycles a copy).  Page ids: one per lane,
+    // loaded a block ahead.
+    constexpr int OPS = 8 * 2 * C::NH;
+    const int my_pg = lane / (2 * C::NH), my_kv = (lane / C::NH) & 1, my_c = lane % C::NH;
     if (lane == 0) {
-      // ------------------------------------------------------ TMA producer
       mbar_arrive_expect_tx(q_full, C::Q_BYTES);
       for (int c = 0; c < C::NH; ++c) tma_load_2d(sQ + c * C::TILE_BYTES, &tmQ, q_full, h * HD + c * 64, t0 + i0);
-      uint32_t issued = 0, issued_ph = 0;
-      bool ok = true;
-      for (int j = 0; j < n_kb && ok; ++j) {
-        const int s = j % C::NKV;
-        const uint32_t ph = (j / C::NKV) & 1;
-        if (!mbar_wait(&kv_empty[s], ph ^ 1, abort_flag, p.err, kErrWaitProducer)) {
-          ok = false;
-          break;
-        }
-        const int key0 = 128 * j;
-        const int key_end = min(key0 + 128, last_pos + 1);
-        const int np = (key_end - key0 + 15) / 16;
-        mbar_arrive_expect_tx(&kv_full[s], np * 2 * C::NH * 2048);
-        for (int pg = 0; pg < np; ++pg) {
-          int page = table[key0 / 16 + pg];
-          if (page < 0 || page >= p.num_pages) {
-            atomicExch(p.err, kErrBounds);
-            page = 0;
-          }
-          const int zk = (page * 2 + 0) * p.Hkv + hk;
-          const int zv = (page * 2 + 1) * p.Hkv + hk;
-          for (int c = 0; c < C::NH; ++c) {
-            tma_load_3d(sK + s * C::KV_BYTES + c * C::TILE_BYTES + pg * 2048, &tmKV, &kv_full[s], c * 64, 0, zk);
-            tma_load_3d(sV + s * C::KV_BYTES + c * C::TILE_BYTES + pg * 2048, &tmKV, &kv_full[s], c * 64, 0, zv);
-          }
-        }
-        issued |= 1u << s;
-        issued_ph = (issued_ph & ~(1u << s)) | (ph << s);
+    }
+    uint32_t issued = 0, issued_ph = 0;
+    bool ok = true;
+    const int n_pages = (last_pos + 1 + 15) / 16;
+    int nxt = lane < 8 && lane < n_pages ? table[lane] : 0;
+    for (int j = 0; j < n_kb && ok; ++j) {
+      const int s = j % C::NKV;
+      const uint32_t ph = (j / C::NKV) & 1;
+      const int cur = nxt;
+      if (j + 1 < n_kb) nxt = lane < 8 && 8 * (j + 1) + lane < n_pages ? table[8 * (j + 1) + lane] : 0;
+      const int key0 = 128 * j;
+      const int key_end = min(key0 + 128, last_pos + 1);
+      const int np = (key_end - key0 + 15) / 16;
+      if (lane == 0) {
+        ok = mbar_wait(&kv_empty[s], ph ^ 1, abort_flag, p.err, kErrWaitProducer);
+        if (ok) mbar_arrive_expect_tx(&kv_full[s], np * 2 * C::NH * 2048);
       }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      int page = __shfl_sync(0xffffffffu, cur, my_pg & 7);
+      if (lane < OPS && my_pg < np) {
+        if (page < 0 || page >= p.num_pages) {
+          atomicExch(p.err, kErrBounds);
+          page = 0;
+        }
+        const int z = (page * 2 + my_kv) * p.Hkv + hk;
+        uint8_t *dst = (my_kv ? sV : sK) + s * C::KV_BYTES + my_c * C::TILE_BYTES + my_pg * 2048;
+        tma_load_3d(dst, &tmKV, &kv_full[s], my_c * 64, 0, z);
+      }
+      issued |= 1u << s;
+      issued_ph = (issued_ph & ~(1u << s)) | (ph << s);
+    }
+    if (lane == 0) {
       if (!ok) {
         for (int s = 0; s < C::NKV; ++s)
           if (issued & (1u << s)) {
@@ -179,10 +189,8 @@ __device__ __forceinline__ void chunk_tile(const CUtensorMap &tmQ, const CUtenso
           }
       }
       // the Q load is always in flight once issued; make sure it landed
-      {
-        const uint64_t t_start = globaltimer();
-        while (!mbar_try_wait(smem_u32(q_full), 0) && globaltimer() - t_start < kWaitLimitNs) {
-        }
+      const uint64_t t_start = globaltimer();
+      while (!mbar_try_wait(smem_u32(q_full), 0) && globaltimer() - t_start < kWaitLimitNs) {
       }
     }
   } else if (warp == 1) {
@@ -236,16 +244,19 @@ __device__ __forceinline__ void chunk_tile(const CUtensorMap &tmQ, const CUtenso
         const uint32_t p_par = (j >> 1) & 1;
         const uint64_t t_start = globaltimer();
         for (uint32_t spin = 0; !(s_done && pv_done); ++spin) {
+          bool progress = false;
           if (!s_done && mbar_test_wait(kv_bar, kv_par)) {
             tc_fence_after();
             issue_s(j + 1);
-            s_done = true;
+            s_done = progress = true;
           }
           if (!pv_done && mbar_test_wait(p_bar, p_par)) {
             tc_fence_after();
             issue_pv(j);
-            pv_done = true;
+            pv_done = progress = true;
           }
+          // back off: this thread shares a scheduler with a softmax warp
+          if (!progress) __nanosleep(64);
           if ((spin & 63u) == 63u) {
             if (*abort_flag) {
               ok = false;
@@ -398,270 +409,458 @@ __device__ __forceinline__ void chunk_tile(const CUtensorMap &tmQ, const CUtenso
 }
 
 // ============================================================ decode rows
+// Persistent decode workers on the tensor cores.  A work item is {request,
+// KV head, page range}; a worker CTA takes items from an atomic counter until
+// none are left, so workers that start late (behind chunk tiles) simply take
+// fewer.  For each 128-key block (8 pages) of an item:
+//
+//   S^T = K Q^T      M = 128 keys, N = 16 (the G q-heads of the group,
+//                    padded), K = hd: K is staged by TMA page by page exactly
+//                    as for the chunk tiles, Q^T is a 16-row tile of q
+//   softmax          one thread per key; each head's block maximum and sum
+//                    are reduced over the 128 threads, the running (m, l)
+//                    per head is updated online (exp2 domain)
+//   O^T_blk = V^T P^T  M = hd, N = 16, K = 128 keys: V is read as an
+//                    MN-major A operand straight from its TMA stage, P^T is
+//                    written by the softmax threads to shared memory
+//   o = o alpha + O_blk  per thread = one hd row, in registers
+//
+// A block moves 64 KB of KV (hd 128) through a 3-stage ring; the producer
+// runs on into the next item while the current one finishes, and the MMAs of
+// the next block's S overlap the softmax of this one.  The work per KV byte
+// on the CUDA cores is a few instructions per key, not G FMAs per element, so
+// the stream runs at HBM speed.  Keys past kv_len in the last block are
+// masked (their V rows are zeroed in shared memory so that P = 0 adds 0).
+// The items' results go straight to o (single split) or to a partial row
+// {o, m, l} for the merge pass.
 struct DecodeParams {
-  const __nv_bfloat16 *q;
-  const __nv_bfloat16 *pool;
   __nv_bfloat16 *o;
   float *part;
   const int32_t *qo_indptr, *kv_len, *bt_indptr, *bt, *items;
-  int n_items, Hq, Hkv, num_pages;
+  int n_items, Hq, Hkv, num_pages, n_workers;
   float scale_log2;
   int *err;
+  int *ctr;   // [0]: next item, [1]: workers done (the last one resets both)
 };
 
-// One CTA per work item {request, KV head, page range}.  Warp 4 streams the
-// K and V blocks of each (page, head) -- contiguous 16 x hd bf16 in the HND
-// pool -- into a ring of shared-memory slots with bulk copies; warps 0-3 take
-// every fourth page.  A warp serves all G q-heads of the GQA group: HD/8
-// lanes share a key (8 bf16 = one 16-byte shared load each), scores are
-// reduced across those lanes with a transposed butterfly (each lane ends with
-// the score of one key), and each key costs one exp2 per head.  The warps'
-// (m, l, o) are merged in shared memory at the end.
 template <int HD>
 struct DecCfg {
-  static constexpr int PAGE_BYTES = 16 * HD * 2;
-  static constexpr int SLOT_BYTES = 2 * PAGE_BYTES;
-  static constexpr int LPK = HD / 8;            // lanes per key
-  static constexpr int KPS = 32 / LPK;          // keys per step
-  static constexpr int STEPS = 16 / KPS;
+  static constexpr int NH = HD / 64;
+  static constexpr int TILE = 128 * 128;                 // [128 keys][64 bf16]
+  static constexpr int KV_STAGE = 2 * NH * TILE;         // K then V
+  static constexpr int STAGES = 3;
+  static constexpr int QT = NH * 16 * 128;               // Q^T: [NH][16 rows][128 B]
+  static constexpr int PT = 2 * 16 * 128;                // P^T: [2 key chunks][16 rows][128 B]
+  static constexpr int OFF_Q = STAGES * KV_STAGE;
+  static constexpr int OFF_P = OFF_Q + 2 * QT;
+  static constexpr int OFF_HDR = OFF_P + 2 * PT;
+  static constexpr int OFF_RED = OFF_HDR + STAGES * 32;
+  static constexpr int OFF_BAR = OFF_RED + 2 * 4 * 16 * 4;
+  static constexpr int SMEM = OFF_BAR + 256;
+  static constexpr uint32_t IDESC_S = idesc_bf16_ab(128, 16, false, false);
+  static constexpr uint32_t IDESC_PV = idesc_bf16_ab(128, 16, true, false);
 };
 
-__device__ __forceinline__ uint4 lds128(const uint8_t *p) { return *reinterpret_cast<const uint4 *>(p); }
+// Stage header written by the producer before it arms the stage.
+struct DecHdr {
+  int item;     // -1: no more items
+  int nvalid;   // keys of the block below kv_len
+  int flags;    // 1: first block of the item, 2: last block
+  int qb;       // Q^T buffer of the item
+};
 
-__device__ __forceinline__ float2 bf2(uint32_t w) { return make_float2(bf16lo(w), bf16hi(w)); }
-
-// NW consumer warps (warps 0 .. NW-1) and one producer warp (warp NW);
-// further warps of the CTA idle.  `dsm` holds NSLOT ring slots, then the
-// barriers.
-template <int HD, int G, int NW, int NSLOT>
-__device__ __forceinline__ void decode_item(const DecodeParams &p, int item, uint8_t *dsm, int warp_base,
-                                            int bar_id) {
+template <int HD, int G>
+__device__ __forceinline__ void decode_worker(const CUtensorMap &tmKV, const CUtensorMap &tmQd, const DecodeParams &p,
+                                              uint8_t *smem) {
   using C = DecCfg<HD>;
-  constexpr int RING = NSLOT * C::SLOT_BYTES;
-  uint8_t *ring = dsm;
-  uint64_t *full = reinterpret_cast<uint64_t *>(dsm + RING);
-  uint64_t *empty = full + NSLOT;
-  volatile int *abort_flag = reinterpret_cast<volatile int *>(empty + NSLOT);
+  static_assert(G >= 1 && G <= 16, "a GQA group fills at most the 16 columns");
+  uint8_t *sKV = smem;
+  uint8_t *sQ = smem + C::OFF_Q;
+  uint8_t *sP = smem + C::OFF_P;
+  DecHdr *hdr = reinterpret_cast<DecHdr *>(smem + C::OFF_HDR);
+  float *red = reinterpret_cast<float *>(smem + C::OFF_RED);     // [max | sum][4 warps][16]
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
+  uint64_t *kv_full = bars;                  // [STAGES]
+  uint64_t *kv_empty = bars + C::STAGES;     // [STAGES]
+  uint64_t *q_full = bars + 2 * C::STAGES;   // [2]
+  uint64_t *q_empty = q_full + 2;            // [2]
+  uint64_t *s_full = q_full + 4;             // [2]
+  uint64_t *s_empty = q_full + 6;            // [2]
+  uint64_t *p_full = q_full + 8;             // [2]
+  uint64_t *o_full = q_full + 10;            // [2]
+  uint64_t *o_empty = q_full + 12;           // [2]
+  uint64_t *mma_done = q_full + 14;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(q_full + 15);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
-  const int warp = (threadIdx.x >> 5) - warp_base, lane = threadIdx.x & 31;
-  const int tid = threadIdx.x - warp_base * 32;   // 0 .. (NW + 1) * 32 - 1
-  const int32_t *it = p.items + item * 8;
-  const int req = it[0], hk = it[1], pb = it[2], pe = it[3], n_splits = it[5];
-  const int np = pe - pb;
-  const int t = p.qo_indptr[req];
-  const int kv = p.kv_len[req];
-  const int32_t *table = p.bt + p.bt_indptr[req];
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
 
-  if (tid == 0) {
-    for (int i = 0; i < NSLOT; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 1);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
     }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&q_full[b], 1);
+      mbar_init(&q_empty[b], 1);
+      mbar_init(&s_full[b], 1);
+      mbar_init(&s_empty[b], 128);
+      mbar_init(&p_full[b], 128);
+      mbar_init(&o_full[b], 1);
+      mbar_init(&o_empty[b], 128);
+    }
+    mbar_init(mma_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
+    prefetch_tmap(&tmKV);
+    prefetch_tmap(&tmQd);
   }
-  named_bar_sync(bar_id, (NW + 1) * 32);
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 64);   // S^T x 2 (cols 0-31), O^T_blk x 2 (cols 32-63)
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  pdl_wait();   // q, the KV pool, o and the work counter belong to earlier kernels
 
-  if (warp == NW) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      const size_t head_stride = static_cast<size_t>(16) * HD;
-      int last_slot_issued = -1;
-      for (int i = 0; i < np; ++i) {
-        const int slot = i % NSLOT;
-        if (i >= NSLOT &&
-            !mbar_wait(&empty[slot], ((i / NSLOT) - 1) & 1, abort_flag, p.err, kErrWaitProducer))
-          break;
-        int page = table[pb + i];
-        if (page < 0 || page >= p.num_pages) {
-          atomicExch(p.err, kErrBounds);
-          page = 0;
-        }
-        const __nv_bfloat16 *kb = p.pool + ((static_cast<size_t>(page) * 2 + 0) * p.Hkv + hk) * head_stride;
-        const __nv_bfloat16 *vb = kb + static_cast<size_t>(p.Hkv) * head_stride;
-        mbar_arrive_expect_tx(&full[slot], 2 * C::PAGE_BYTES);
-        bulk_load(ring + slot * C::SLOT_BYTES, kb, C::PAGE_BYTES, &full[slot]);
-        bulk_load(ring + slot * C::SLOT_BYTES + C::PAGE_BYTES, vb, C::PAGE_BYTES, &full[slot]);
-        last_slot_issued = i;
-      }
-      // every issued copy is waited on by a consumer; if consumers gave up,
-      // wait here (bounded) for the last copies to land
-      if (*abort_flag) {
-        for (int i = (last_slot_issued - NSLOT + 1 > 0 ? last_slot_issued - NSLOT + 1 : 0);
-             i <= last_slot_issued; ++i) {
-          const uint64_t t0 = globaltimer();
-          while (!mbar_try_wait(smem_u32(&full[i % NSLOT]), (i / NSLOT) & 1) &&
-                 globaltimer() - t0 < kWaitLimitNs) {
+  if (warp == 0) {
+    // -------------------------------------------------------- TMA producer
+    // The whole warp: lane 0 waits, fetches work and arms each stage, then
+    // the block's 8 pages x (K, V) x hd chunks go out as one TMA per lane
+    // (a single thread needs ~90 cycles per copy, which would pace the ring).
+    // Global loads the producer depends on (the next item, the next block's
+    // page ids, one per lane) are issued a block ahead.
+    constexpr int OPS = 8 * 2 * C::NH;   // copies per full block
+    const int my_pg = lane / (2 * C::NH), my_kv = (lane / C::NH) & 1, my_c = lane % C::NH;
+    int seq = 0, k_local = 0;
+    bool ok = true;
+    int next_item = lane == 0 ? atomicAdd(&p.ctr[0], 1) : 0;
+    while (ok) {
+      const int item = __shfl_sync(0xffffffffu, next_item, 0);
+      if (item >= p.n_items) {
+        if (lane == 0) {
+          const int s = seq % C::STAGES;
+          if (mbar_wait(&kv_empty[s], ((seq / C::STAGES) & 1) ^ 1, abort_flag, p.err, kErrWaitProducer)) {
+            hdr[s].item = -1;
+            mbar_arrive(&kv_full[s]);
           }
         }
+        break;
       }
-    }
-  } else {
-    // ----------------------------------------------------------- consumers
-    const int sub = lane % C::LPK;   // 8-element slice of hd
-    const int kk = lane / C::LPK;    // key within a step
-    const int my_st = sub >> 1;      // step whose score this lane ends up holding
-    float2 qf[G][4];
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      const uint4 raw = *reinterpret_cast<const uint4 *>(p.q + (static_cast<size_t>(t) * p.Hq + hk * G + g) * HD + sub * 8);
-      const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float2 f = bf2(w[e]);
-        qf[g][e] = make_float2(f.x * p.scale_log2, f.y * p.scale_log2);
-      }
-    }
-    float m[G], l[G];
-    float2 acc[G][4];
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      m[g] = -INFINITY;
-      l[g] = 0.f;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) acc[g][e] = make_float2(0.f, 0.f);
-    }
-    for (int i = warp; i < np; i += NW) {
-      const int slot = i % NSLOT;
-      if (!mbar_wait(&full[slot], (i / NSLOT) & 1, abort_flag, p.err, kErrWaitSoftmax)) break;
-      const uint8_t *ks = ring + slot * C::SLOT_BYTES;
-      const uint8_t *vs = ks + C::PAGE_BYTES;
-      const int key_base = (pb + i) * 16;
-      // partial dot products of this lane's 8 dims with each step's key
-      float part[G][C::STEPS];
-#pragma unroll
-      for (int st = 0; st < C::STEPS; ++st) {
-        const uint4 kr = lds128(ks + (st * C::KPS + kk) * HD * 2 + sub * 16);
-        const float2 k0 = bf2(kr.x), k1 = bf2(kr.y), k2 = bf2(kr.z), k3 = bf2(kr.w);
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          float2 a = __fmul2_rn(qf[g][0], k0);
-          a = __ffma2_rn(qf[g][1], k1, a);
-          a = __ffma2_rn(qf[g][2], k2, a);
-          a = __ffma2_rn(qf[g][3], k3, a);
-          part[g][st] = a.x + a.y;
+      if (lane == 0) next_item = atomicAdd(&p.ctr[0], 1);   // used at the next item
+      const int32_t *it = p.items + item * 8;
+      const int req = it[0], hk = it[1], pb = it[2], pe = it[3];
+      const int t = p.qo_indptr[req];
+      const int kv = p.kv_len[req];
+      const int32_t *table = p.bt + p.bt_indptr[req];
+      const int nblk = (pe - pb + 7) / 8;
+      int nxt = lane < 8 && pb + lane < pe ? table[pb + lane] : 0;
+      const int qb = k_local & 1;
+      if (lane == 0) {
+        ok = mbar_wait(&q_empty[qb], ((k_local >> 1) & 1) ^ 1, abort_flag, p.err, kErrWaitProducer);
+        if (ok) {
+          mbar_arrive_expect_tx(&q_full[qb], C::QT);
+          for (int c = 0; c < C::NH; ++c)
+            tma_load_2d(sQ + qb * C::QT + c * 2048, &tmQd, &q_full[qb], c * 64, t * p.Hq + hk * G);
         }
       }
-      // transposed butterfly: each lane ends with the full score of step my_st
-      float s[G];
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      for (int b = 0; b < nblk && ok; ++b) {
+        const int pg0 = pb + 8 * b;
+        const int npg = min(8, pe - pg0);
+        const int cur = nxt;
+        if (b + 1 < nblk) nxt = lane < 8 && pg0 + 8 + lane < pe ? table[pg0 + 8 + lane] : 0;
+        const int s = seq % C::STAGES;
+        if (lane == 0) {
+          ok = mbar_wait(&kv_empty[s], ((seq / C::STAGES) & 1) ^ 1, abort_flag, p.err, kErrWaitProducer);
+          if (ok) {
+            hdr[s].item = item;
+            hdr[s].nvalid = min(npg * 16, kv - pg0 * 16);
+            hdr[s].flags = (b == 0 ? 1 : 0) | (b == nblk - 1 ? 2 : 0);
+            hdr[s].qb = qb;
+            mbar_arrive_expect_tx(&kv_full[s], npg * 2 * C::NH * 2048);
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        int page = __shfl_sync(0xffffffffu, cur, my_pg & 7);
+        if (lane < OPS && my_pg < npg) {
+          if (page < 0 || page >= p.num_pages) {
+            atomicExch(p.err, kErrBounds);
+            page = 0;
+          }
+          const int z = (page * 2 + my_kv) * p.Hkv + hk;
+          tma_load_3d(sKV + s * C::KV_STAGE + (my_kv * C::NH + my_c) * C::TILE + my_pg * 2048, &tmKV, &kv_full[s],
+                      my_c * 64, 0, z);
+        }
+        ++seq;
+      }
+      ++k_local;
+    }
+    // on an abort, let copies in flight land before the CTA exits
+    if (lane == 0 && (!ok || *abort_flag)) {
+      for (int i = max(0, seq - C::STAGES); i < seq; ++i) {
+        const uint64_t t0 = globaltimer();
+        while (!mbar_try_wait(smem_u32(&kv_full[i % C::STAGES]), (i / C::STAGES) & 1) &&
+               globaltimer() - t0 < kWaitLimitNs) {
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------------- MMA issuer
+      // Block j: S(j+1) as soon as its K (and Q) landed and S buffer (j+1)&1
+      // is free; PV(j) as soon as P(j) is written and O_blk buffer j&1 is free.
+      auto issue_s = [&](int j, int s, int qb) {
+        const uint32_t d = tmem + (j & 1) * 16;
+        const uint32_t k0 = smem_u32(sKV + s * C::KV_STAGE);
+        const uint32_t q0 = smem_u32(sQ + qb * C::QT);
 #pragma unroll
-      for (int g = 0; g < G; ++g) {
-        float v[C::STEPS];
+        for (int c = 0; c < C::NH; ++c)
 #pragma unroll
-        for (int st = 0; st < C::STEPS; ++st) v[st] = part[g][st];
-        int n = C::STEPS;
+          for (int kk = 0; kk < 4; ++kk)
+            mma_bf16(d, sdesc_sw128(k0 + c * C::TILE + kk * 32, 16, 1024),
+                     sdesc_sw128(q0 + c * 2048 + kk * 32, 16, 1024), C::IDESC_S, (c > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&s_full[j & 1]);
+      };
+      auto issue_pv = [&](int j, int s) {
+        const uint32_t d = tmem + 32 + (j & 1) * 16;
+        const uint32_t v0 = smem_u32(sKV + s * C::KV_STAGE + C::NH * C::TILE);
+        const uint32_t p0 = smem_u32(sP + (j & 1) * C::PT);
 #pragma unroll
-        for (int o = C::LPK / 2; o >= 2; o >>= 1) {
-          const bool upper = (lane & o) != 0;
-          const int half = n / 2;
-#pragma unroll
-          for (int i2 = 0; i2 < C::STEPS / 2; ++i2) {
-            if (i2 < half) {
-              const float send = upper ? v[i2] : v[i2 + half];
-              const float keep = upper ? v[i2 + half] : v[i2];
-              v[i2] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        for (int ks = 0; ks < 8; ++ks)   // 16 keys per MMA
+          mma_bf16(d, sdesc_sw128(v0 + ks * 2048, C::TILE, 1024),
+                   sdesc_sw128(p0 + (ks >> 2) * 2048 + (ks & 3) * 32, 16, 1024), C::IDESC_PV, ks > 0 ? 1u : 0u);
+        mma_commit(&o_full[j & 1]);
+        mma_commit(&kv_empty[s]);
+      };
+      int qcount = 0;   // items whose Q^T the S MMAs have used
+      // block 0
+      bool ok = mbar_wait(&kv_full[0], 0, abort_flag, p.err, kErrWaitMma);
+      bool done = !ok || hdr[0].item < 0;
+      if (!done) {
+        ok = mbar_wait(&q_full[0], 0, abort_flag, p.err, kErrWaitMma);
+        if (ok) {
+          tc_fence_after();
+          issue_s(0, 0, 0);
+          if (hdr[0].flags & 2) {
+            mma_commit(&q_empty[0]);
+            ++qcount;
+          }
+        }
+        done = !ok;
+      }
+      for (int j = 0; !done; ++j) {
+        const int s = j % C::STAGES, s1 = (j + 1) % C::STAGES;
+        bool s_done = false, pv_done = false, last = false;
+        const uint64_t t_start = globaltimer();
+        for (uint32_t spin = 0; !(s_done && pv_done); ++spin) {
+          const bool was = s_done || pv_done;
+          if (!s_done && mbar_test_wait(smem_u32(&kv_full[s1]), ((j + 1) / C::STAGES) & 1)) {
+            if (hdr[s1].item < 0) {
+              s_done = true;
+              last = true;
+            } else {
+              const int qb = hdr[s1].qb;
+              const bool need_q = hdr[s1].flags & 1;
+              if ((!need_q || mbar_test_wait(smem_u32(&q_full[qb]), (qcount >> 1) & 1)) &&
+                  mbar_test_wait(smem_u32(&s_empty[(j + 1) & 1]), (((j + 1) >> 1) & 1) ^ 1)) {
+                tc_fence_after();
+                issue_s(j + 1, s1, qb);
+                if (hdr[s1].flags & 2) {
+                  mma_commit(&q_empty[qb]);
+                  ++qcount;
+                }
+                s_done = true;
+              }
             }
           }
-          n = half;
+          bool progress = false;
+          if (!pv_done && mbar_test_wait(smem_u32(&p_full[j & 1]), (j >> 1) & 1) &&
+              mbar_test_wait(smem_u32(&o_empty[j & 1]), ((j >> 1) & 1) ^ 1)) {
+            tc_fence_after();
+            issue_pv(j, s);
+            pv_done = progress = true;
+          }
+          // back off: this thread shares a scheduler with a softmax warp
+          if (!progress && was == (s_done || pv_done)) __nanosleep(64);
+          if ((spin & 63u) == 63u) {
+            if (*abort_flag) {
+              ok = false;
+              break;
+            }
+            if (globaltimer() - t_start > kWaitLimitNs) {
+              *abort_flag = 1;
+              atomicExch(p.err, kErrWaitMma);
+              ok = false;
+              break;
+            }
+          }
         }
-        s[g] = v[0] + __shfl_xor_sync(0xffffffffu, v[0], 1);
+        done = !ok || last;
       }
-      const int my_key = key_base + my_st * C::KPS + kk;
-      const bool my_valid = my_key < kv;
-      float pv[G];
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        float mx = my_valid ? s[g] : -INFINITY;
-#pragma unroll
-        for (int o = 16; o >= 2; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        const float m_new = fmaxf(m[g], mx);
-        const float alpha = (m[g] == -INFINITY) ? 0.f : exp2f(m[g] - m_new);
-        m[g] = m_new;
-        pv[g] = my_valid ? exp2f(s[g] - m_new) : 0.f;
-        l[g] = l[g] * alpha + ((sub & 1) ? 0.f : pv[g]);
-        const float2 a2 = make_float2(alpha, alpha);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) acc[g][e] = __fmul2_rn(acc[g][e], a2);
+      // every MMA issued above has completed before TMEM is freed
+      mma_commit(mma_done);
+      const uint64_t t_end = globaltimer();
+      while (!mbar_try_wait(smem_u32(mma_done), 0) && globaltimer() - t_end < kWaitLimitNs) {
       }
-      // o += p v over this lane's keys (step st, key st*KPS + kk)
-#pragma unroll
-      for (int st = 0; st < C::STEPS; ++st) {
-        const int src = kk * C::LPK + 2 * st;
-        const bool valid = key_base + st * C::KPS + kk < kv;
-        uint4 vr = lds128(vs + (st * C::KPS + kk) * HD * 2 + sub * 16);
-        if (!valid) vr = make_uint4(0, 0, 0, 0);
-        const float2 v0 = bf2(vr.x), v1 = bf2(vr.y), v2 = bf2(vr.z), v3 = bf2(vr.w);
+    }
+  } else if (warp < 6) {
+    // ---------------------------------------------- softmax / accumulation
+    const int q = warp & 3;
+    const int t = q * 32 + lane;             // key of the block (S^T lane) and hd row (O^T lane)
+    const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+    float m[G], l[G], o[G], alpha_prev[G];
+    bool ok = true;
+    for (int j = 0;; ++j) {
+      const int s = j % C::STAGES;
+      bool bad = !ok || !mbar_wait(&kv_full[s], (j / C::STAGES) & 1, abort_flag, p.err, kErrWaitSoftmax);
+      const DecHdr h = hdr[s];
+      if (named_bar_or(1, 128, bad) || h.item < 0) break;
+      bad = !mbar_wait(&s_full[j & 1], (j >> 1) & 1, abort_flag, p.err, kErrWaitSoftmax);
+      bad = __any_sync(0xffffffffu, bad);
+      float sv[16];
+      if (!bad) {
+        tc_fence_after();
+        tmem_ld16(tmem + lane_base + (j & 1) * 16, sv);
+      }
+      tc_fence_before();
+      mbar_arrive(&s_empty[j & 1]);
+      if (h.flags & 1) {
 #pragma unroll
         for (int g = 0; g < G; ++g) {
-          const float pr = __shfl_sync(0xffffffffu, pv[g], src);
-          const float2 p2 = make_float2(pr, pr);
-          acc[g][0] = __ffma2_rn(p2, v0, acc[g][0]);
-          acc[g][1] = __ffma2_rn(p2, v1, acc[g][1]);
-          acc[g][2] = __ffma2_rn(p2, v2, acc[g][2]);
-          acc[g][3] = __ffma2_rn(p2, v3, acc[g][3]);
+          m[g] = -INFINITY;
+          l[g] = 0.f;
+          o[g] = 0.f;
         }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[slot]);
-    }
-    // fold the KPS key lanes that share an hd slice, and the l partials
+      const bool valid = t < h.nvalid;
+      float sc[G], mx[G];
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-#pragma unroll
-      for (int o = C::LPK; o < 32; o <<= 1)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          acc[g][e].x += __shfl_xor_sync(0xffffffffu, acc[g][e].x, o);
-          acc[g][e].y += __shfl_xor_sync(0xffffffffu, acc[g][e].y, o);
-        }
-#pragma unroll
-      for (int o = 16; o >= 1; o >>= 1) l[g] += __shfl_xor_sync(0xffffffffu, l[g], o);
-    }
-    // stash this warp's (m, l, o) for the CTA merge; the ring is free once
-    // every consumer is past its last page (barrier below)
-    named_bar_sync(bar_id + 1, NW * 32);
-    float *stash = reinterpret_cast<float *>(ring) + warp * G * (HD + 2);
-    if (kk == 0) {
+      for (int g = 0; g < G; ++g) {
+        sc[g] = valid ? sv[g] * p.scale_log2 : -INFINITY;
+        mx[g] = sc[g];
+      }
 #pragma unroll
       for (int g = 0; g < G; ++g)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          stash[g * (HD + 2) + sub * 8 + 2 * e] = acc[g][e].x;
-          stash[g * (HD + 2) + sub * 8 + 2 * e + 1] = acc[g][e].y;
-        }
-    }
-    if (lane == 0) {
+        for (int off = 16; off > 0; off >>= 1) mx[g] = fmaxf(mx[g], __shfl_xor_sync(0xffffffffu, mx[g], off));
+      if (lane == 0)
+#pragma unroll
+        for (int g = 0; g < G; ++g) red[q * 16 + g] = mx[g];
+      if (named_bar_or(1, 128, bad)) {
+        ok = false;
+        break;
+      }
+      float alpha[G], pr[G];
 #pragma unroll
       for (int g = 0; g < G; ++g) {
-        stash[g * (HD + 2) + HD] = m[g];
-        stash[g * (HD + 2) + HD + 1] = l[g];
+        const float bm = fmaxf(fmaxf(red[g], red[16 + g]), fmaxf(red[32 + g], red[48 + g]));
+        const float mn = fmaxf(m[g], bm);
+        alpha[g] = (m[g] == -INFINITY) ? 0.f : exp2f(m[g] - mn);
+        m[g] = mn;
+        pr[g] = exp2f(sc[g] - mn);   // 0 for masked keys
       }
-    }
-    named_bar_sync(bar_id + 1, NW * 32);
-    const float *all = reinterpret_cast<const float *>(ring);
-    for (int idx = tid; idx < G * HD; idx += NW * 32) {
-      const int g = idx / HD, d = idx % HD;
-      float M = -INFINITY;
+      // P^T[g][t] into the K-major 128-byte-swizzled B tile (two 64-key chunks)
+      uint8_t *pt = sP + (j & 1) * C::PT + (t >> 6) * 2048;
 #pragma unroll
-      for (int w = 0; w < NW; ++w) M = fmaxf(M, all[(w * G + g) * (HD + 2) + HD]);
-      float L = 0.f, O = 0.f;
+      for (int g = 0; g < G; ++g)
+        *reinterpret_cast<__nv_bfloat16 *>(pt + sw128_offset(g, t & 63)) = __float2bfloat16_rn(pr[g]);
+      if (!valid) {
+        // a key past kv_len: its V row may hold anything; make it exactly 0
+        uint8_t *vrow = sKV + s * C::KV_STAGE + C::NH * C::TILE + (t >> 3) * 1024 + (t & 7) * 128;
 #pragma unroll
-      for (int w = 0; w < NW; ++w) {
-        const float* base = all + (w * G + g) * (HD + 2);
-        const float wt = base[HD] == -INFINITY ? 0.f : exp2f(base[HD] - M);
-        L += wt * base[HD + 1];
-        O += wt * base[d];
+        for (int c = 0; c < C::NH; ++c)
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            *reinterpret_cast<uint4 *>(vrow + c * C::TILE + k * 16) = make_uint4(0, 0, 0, 0);
       }
-      if (n_splits == 1) {
-        p.o[(static_cast<size_t>(t) * p.Hq + hk * G + g) * HD + d] = __float2bfloat16_rn(O / L);
-      } else {
-        float *dst = p.part + (static_cast<size_t>(item) * G + g) * part_stride<HD>();
-        dst[d] = O;
-        if (d == 0) {
-          dst[HD] = M;
-          dst[HD + 1] = L;
+      fence_proxy_async_smem();
+      mbar_arrive(&p_full[j & 1]);
+      // block sums per head
+      float sm[G];
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        sm[g] = pr[g];
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) sm[g] += __shfl_xor_sync(0xffffffffu, sm[g], off);
+      }
+      if (lane == 0)
+#pragma unroll
+        for (int g = 0; g < G; ++g) red[64 + q * 16 + g] = sm[g];
+      named_bar_sync(1, 128);
+#pragma unroll
+      for (int g = 0; g < G; ++g)
+        l[g] = l[g] * alpha[g] + ((red[64 + g] + red[80 + g]) + (red[96 + g] + red[112 + g]));
+      // O^T_blk(i): row t = hd element t, column g = head.  Block j-1 is
+      // folded in here, after this block's softmax, so that PV(j-1) ran
+      // meanwhile; an item's last block is folded at once.
+      auto fold = [&](int i, const float (&al)[G]) -> bool {
+        const bool b = __any_sync(0xffffffffu, !mbar_wait(&o_full[i & 1], (i >> 1) & 1, abort_flag, p.err,
+                                                          kErrWaitSoftmax));
+        float ob[16];
+        if (!b) {
+          tc_fence_after();
+          tmem_ld16(tmem + lane_base + 32 + (i & 1) * 16, ob);
+        }
+        tc_fence_before();
+        mbar_arrive(&o_empty[i & 1]);
+        if (!b)
+#pragma unroll
+          for (int g = 0; g < G; ++g) o[g] = fmaf(o[g], al[g], ob[g]);
+        return !b;
+      };
+      if (!(h.flags & 1) && !fold(j - 1, alpha_prev)) {
+        ok = false;
+        continue;   // the next block's first barrier-OR takes every thread out
+      }
+#pragma unroll
+      for (int g = 0; g < G; ++g) alpha_prev[g] = alpha[g];
+      if (!(h.flags & 2)) continue;
+      if (!fold(j, alpha)) {
+        ok = false;
+        continue;
+      }
+      if (t < HD) {
+        const int32_t *it = p.items + h.item * 8;
+        const int req = it[0], hk = it[1], n_splits = it[5];
+        if (n_splits == 1) {
+          const size_t tok = static_cast<size_t>(p.qo_indptr[req]);
+#pragma unroll
+          for (int g = 0; g < G; ++g)
+            p.o[(tok * p.Hq + hk * G + g) * HD + t] = __float2bfloat16_rn(o[g] / l[g]);
+        } else {
+#pragma unroll
+          for (int g = 0; g < G; ++g) {
+            float *dst = p.part + (static_cast<size_t>(h.item) * G + g) * part_stride<HD>();
+            dst[t] = o[g];
+            if (t == 0) {
+              dst[HD] = m[g];
+              dst[HD + 1] = l[g];
+            }
+          }
         }
       }
+    }
+    tc_fence_before();
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 64);
+  }
+  if (threadIdx.x == 0) {
+    // the last worker out resets the counter for the next launch
+    __threadfence();
+    if (atomicAdd(&p.ctr[1], 1) == p.n_workers - 1) {
+      p.ctr[0] = 0;
+      p.ctr[1] = 0;
+      __threadfence();
     }
   }
 }
@@ -702,36 +901,26 @@ __global__ void __launch_bounds__(128) merge_kernel(const float *part, const int
 
 // ============================================================ one grid
 // The ragged attention of a step is ONE launch: blocks [0, n_tiles) run a
-// prefill-chunk tile (tensor cores), the rest run a decode item (HBM stream),
-// so the two kinds share the GPU instead of running back to back.  Tiles come
-// first, heaviest first; decode items fill SMs as they free up.  A decode CTA
-// runs two items side by side, each with 4 consumer warps, a producer warp and
-// a ring in its half of the tile's shared memory.
+// prefill-chunk tile (tensor cores, compute-heavy), the rest are persistent
+// decode workers (tensor cores, HBM stream) that take decode items until none
+// are left, so the two kinds share the GPU instead of running back to back.
+// Tiles come first, heaviest first; workers fill SMs as they free up.
 template <int HD>
 struct FusedCfg {
-  static constexpr int THREADS = ChunkCfg<HD>::THREADS;          // 10 warps
-  static constexpr int DEC_NW = 4;                                // consumers per decode item
-  static constexpr int SMEM = ChunkCfg<HD>::SMEM;
-  // two decode items per CTA, each with half of the shared memory
-  static constexpr int HALF = (SMEM / 2) & ~1023;
-  // Page i lives in slot i % NSLOT and is consumed by warp i % DEC_NW; with
-  // NSLOT a multiple of DEC_NW every slot has a single consumer warp, which
-  // takes its pages in order, so a parity wait on a slot can never match a
-  // phase two copies ahead.
-  static constexpr int FIT = (HALF - 256) / DecCfg<HD>::SLOT_BYTES;
-  static constexpr int NSLOT = ((FIT < 16 ? FIT : 16) / DEC_NW) * DEC_NW;
-  static_assert(2 * (DEC_NW + 1) * 32 == THREADS, "two decode items fill the CTA");
-  static_assert(NSLOT >= DEC_NW && NSLOT % DEC_NW == 0, "one consumer warp per ring slot");
-  // ring, full/empty barriers and the abort word of one item fit its half
-  static_assert(NSLOT * DecCfg<HD>::SLOT_BYTES + 16 * NSLOT + 4 <= HALF, "decode item exceeds its half");
-  // the end-of-item merge stash (8 q-heads at most) reuses the ring
-  static_assert(DEC_NW * 8 * (HD + 2) * 4 <= NSLOT * DecCfg<HD>::SLOT_BYTES, "merge stash exceeds the ring");
+  static constexpr int THREADS = ChunkCfg<HD>::THREADS;   // 10 warps
+  static constexpr int SMEM = ChunkCfg<HD>::SMEM > DecCfg<HD>::SMEM ? ChunkCfg<HD>::SMEM : DecCfg<HD>::SMEM;
+  using D = DecCfg<HD>;
+  // the decode worker's V^T operand reads 128 hd rows; for hd 64 the upper 64
+  // (ignored) rows of the last stage lie past it and must stay in this CTA
+  static_assert((D::STAGES - 1) * D::KV_STAGE + D::NH * D::TILE + 2 * D::TILE <= SMEM, "V^T over-read");
+  static_assert(THREADS >= 6 * 32, "the decode worker uses warps 0-5");
 };
 
 template <int HD, int G>
 __global__ void __launch_bounds__(FusedCfg<HD>::THREADS, 1)
     attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmKV,
-                     const ChunkParams cp, const DecodeParams dp, int n_tiles) {
+                     const __grid_constant__ CUtensorMap tmQd, const ChunkParams cp, const DecodeParams dp,
+                     int n_tiles) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   if (smem_u32(smem_raw) & 1023u) {
     // the layouts above need a 1024-aligned base and reserve no slack
@@ -739,23 +928,15 @@ __global__ void __launch_bounds__(FusedCfg<HD>::THREADS, 1)
     if (threadIdx.x == 0) atomicExch(cp.err, kErrBounds);
     return;
   }
-  if (static_cast<int>(blockIdx.x) < n_tiles) {
-    chunk_tile<HD>(tmQ, tmKV, cp, blockIdx.x, smem_raw);   // waits after its set-up
-  } else {
-    pdl_wait();
-    // warps 0-4 take item 2k, warps 5-9 item 2k + 1 (if it exists)
-    using F = FusedCfg<HD>;
-    const int half = threadIdx.x >= (F::DEC_NW + 1) * 32;
-    const int item = 2 * (blockIdx.x - n_tiles) + half;
-    if (item < dp.n_items)
-      decode_item<HD, G, F::DEC_NW, F::NSLOT>(dp, item, align1024(smem_raw) + half * F::HALF,
-                                              half * (F::DEC_NW + 1), 1 + 2 * half);
-  }
+  if (static_cast<int>(blockIdx.x) < n_tiles)
+    chunk_tile<HD>(tmQ, tmKV, cp, blockIdx.x, smem_raw);   // waits for earlier kernels after its set-up
+  else
+    decode_worker<HD, G>(tmKV, tmQd, dp, smem_raw);       // likewise
 }
 
 template <int HD, int G>
-cudaError_t launch_attention(const CUtensorMap &tq, const CUtensorMap &tkv, const ChunkParams &cp,
-                             const DecodeParams &dp, int n_tiles, int n_items, cudaStream_t st) {
+cudaError_t launch_attention(const CUtensorMap &tq, const CUtensorMap &tkv, const CUtensorMap &tqd,
+                             const ChunkParams &cp, const DecodeParams &dp, int n_tiles, cudaStream_t st) {
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
@@ -763,22 +944,22 @@ cudaError_t launch_attention(const CUtensorMap &tq, const CUtensorMap &tkv, cons
                                     FusedCfg<HD>::SMEM);
   });
   if (attr_err != cudaSuccess) return attr_err;
-  return launch_pdl(attention_kernel<HD, G>, dim3(n_tiles + (n_items + 1) / 2), dim3(FusedCfg<HD>::THREADS),
-                    FusedCfg<HD>::SMEM, st, 1, tq, tkv, cp, dp, n_tiles);
+  return launch_pdl(attention_kernel<HD, G>, dim3(n_tiles + dp.n_workers), dim3(FusedCfg<HD>::THREADS),
+                    FusedCfg<HD>::SMEM, st, 1, tq, tkv, tqd, cp, dp, n_tiles);
 }
 
 template <int HD>
-cudaError_t launch_attention_g(const CUtensorMap &tq, const CUtensorMap &tkv, const ChunkParams &cp,
-                               const DecodeParams &dp, int n_tiles, int n_items, int G, cudaStream_t st) {
+cudaError_t launch_attention_g(const CUtensorMap &tq, const CUtensorMap &tkv, const CUtensorMap &tqd,
+                               const ChunkParams &cp, const DecodeParams &dp, int n_tiles, int G, cudaStream_t st) {
   switch (G) {
-    case 1: return launch_attention<HD, 1>(tq, tkv, cp, dp, n_tiles, n_items, st);
-    case 2: return launch_attention<HD, 2>(tq, tkv, cp, dp, n_tiles, n_items, st);
-    case 3: return launch_attention<HD, 3>(tq, tkv, cp, dp, n_tiles, n_items, st);
-    case 4: return launch_attention<HD, 4>(tq, tkv, cp, dp, n_tiles, n_items, st);
-    case 5: return launch_attention<HD, 5>(tq, tkv, cp, dp, n_tiles, n_items, st);
-    case 6: return launch_attention<HD, 6>(tq, tkv, cp, dp, n_tiles, n_items, st);
-    case 7: return launch_attention<HD, 7>(tq, tkv, cp, dp, n_tiles, n_items, st);
-    case 8: return launch_attention<HD, 8>(tq, tkv, cp, dp, n_tiles, n_items, st);
+    case 1: return launch_attention<HD, 1>(tq, tkv, tqd, cp, dp, n_tiles, st);
+    case 2: return launch_attention<HD, 2>(tq, tkv, tqd, cp, dp, n_tiles, st);
+    case 3: return launch_attention<HD, 3>(tq, tkv, tqd, cp, dp, n_tiles, st);
+    case 4: return launch_attention<HD, 4>(tq, tkv, tqd, cp, dp, n_tiles, st);
+    case 5: return launch_attention<HD, 5>(tq, tkv, tqd, cp, dp, n_tiles, st);
+    case 6: return launch_attention<HD, 6>(tq, tkv, tqd, cp, dp, n_tiles, st);
+    case 7: return launch_attention<HD, 7>(tq, tkv, tqd, cp, dp, n_tiles, st);
+    case 8: return launch_attention<HD, 8>(tq, tkv, tqd, cp, dp, n_tiles, st);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -801,8 +982,6 @@ cudaError_t attention_run(const AttnArgs &a, cudaStream_t st) {
   cp.scale_log2 = scale_log2;
   cp.err = a.err;
   DecodeParams dp;
-  dp.q = static_cast<const __nv_bfloat16 *>(a.q);
-  dp.pool = static_cast<const __nv_bfloat16 *>(a.pool);
   dp.o = static_cast<__nv_bfloat16 *>(a.o);
   dp.part = a.part;
   dp.qo_indptr = a.qo_indptr;
@@ -816,9 +995,11 @@ cudaError_t attention_run(const AttnArgs &a, cudaStream_t st) {
   dp.num_pages = a.num_pages;
   dp.scale_log2 = scale_log2;
   dp.err = a.err;
+  dp.ctr = a.dec_ctr;
+  dp.n_workers = a.n_items < device_sm_count() ? a.n_items : device_sm_count();
   const int G = a.Hq / a.Hkv;
-  return a.hd == 128 ? launch_attention_g<128>(*a.tm_q, *a.tm_kv, cp, dp, a.n_tiles, a.n_items, G, st)
-                     : launch_attention_g<64>(*a.tm_q, *a.tm_kv, cp, dp, a.n_tiles, a.n_items, G, st);
+  return a.hd == 128 ? launch_attention_g<128>(*a.tm_q, *a.tm_kv, *a.tm_qd, cp, dp, a.n_tiles, G, st)
+                     : launch_attention_g<64>(*a.tm_q, *a.tm_kv, *a.tm_qd, cp, dp, a.n_tiles, G, st);
 }
 
 cudaError_t attn_merge_run(const MergeArgs &m, cudaStream_t st) {

@@ -69,9 +69,11 @@ struct AttnArgs {
   int T, Hq, Hkv, hd, num_pages;
   int *err;
   const CUtensorMap *tm_q;  // Q map [T][Hq hd], box 64 x 128 (host pointer; copied into launch)
+  const CUtensorMap *tm_qd; // Q map [T Hq][hd], box 64 x 16: the G q-heads of one decode row (and padding)
   const CUtensorMap *tm_kv; // pool map [P*2*Hkv][16][hd], box 64 x 16 x 1
+  int *dec_ctr;             // two ints, zero between launches: decode work counter
 };
-// Prefill-chunk tiles (tcgen05) and decode rows (split-KV) in one launch.
+// Prefill-chunk tiles and persistent decode workers (both tcgen05) in one launch.
 cudaError_t attention_run(const AttnArgs &a, cudaStream_t st);
 
 struct MergeArgs {
