@@ -75,15 +75,18 @@ cudaError_t encode_tmap_2d(CUtensorMap *map, const void *base, uint64_t inner, u
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-cudaError_t encode_tmap_3d(CUtensorMap *map, const void *base, uint64_t d0, uint64_t d1, uint64_t d2,
-                           uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t b0, uint32_t b1, uint32_t b2) {
+cudaError_t encode_tmap_5d(CUtensorMap *map, const void *base, const uint64_t dims[5], const uint64_t strides_bytes[4],
+                           const uint32_t box[5]) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return cudaErrorNotSupported;
-  cuuint64_t dims[3] = {d0, d1, d2};
-  cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
-  cuuint32_t box[3] = {b0, b1, b2};
-  cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+  cuuint64_t d[5], st[4];
+  cuuint32_t b[5], estr[5] = {1, 1, 1, 1, 1};
+  for (int i = 0; i < 5; ++i) {
+    d[i] = dims[i];
+    b[i] = box[i];
+  }
+  for (int i = 0; i < 4; ++i) st[i] = strides_bytes[i];
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(base), d, st, b, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
@@ -715,8 +718,17 @@ mb_status mb_kv_alloc(mb_layer *L, int32_t num_pages, void *dev_buf, mb_kv **out
     }
     kv->owned = true;
   }
-  cudaError_t e = mb::encode_tmap_3d(&kv->tmap, kv->base, hd, MB_PAGE_TOKENS, z, hd * 2, MB_PAGE_TOKENS * hd * 2,
-                                     64, MB_PAGE_TOKENS, 1);
+  // The attention kernels fetch one (page, K or V, head) block of 16 x hd per
+  // copy, as a 5-D view: (64 hd elements, 8 slots, hd/64 halves, 2 slot
+  // groups, page*2*Hkv + kv*Hkv + head).  In shared memory that lands as
+  // [slot group][hd half][8 slots][128 B], 128-byte swizzled: every 8 keys of
+  // one hd half form a swizzle atom, and consecutive atoms of a half sit
+  // hd/64 KB apart, which the tensor-core descriptors step over uniformly.
+  const uint64_t nh = static_cast<uint64_t>(hd) / 64;
+  const uint64_t dims5[5] = {64, 8, nh, MB_PAGE_TOKENS / 8, z};
+  const uint64_t strides5[4] = {static_cast<uint64_t>(hd) * 2, 128, 8ull * hd * 2, MB_PAGE_TOKENS * hd * 2ull};
+  const uint32_t box5[5] = {64, 8, static_cast<uint32_t>(nh), MB_PAGE_TOKENS / 8, 1};
+  cudaError_t e = mb::encode_tmap_5d(&kv->tmap, kv->base, dims5, strides5, box5);
   if (e != cudaSuccess) {
     if (kv->owned) cudaFree(kv->base);
     delete kv;

@@ -51,6 +51,10 @@ struct ChunkCfg {
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + Q_BYTES;
   static constexpr int NKV = 3;                   // K/V stages
+  // A K or V stage holds 128 keys as [8-key group][hd half][8 keys][128 B]
+  // (what one copy per page delivers): atoms of a half are ATOM_STRIDE apart.
+  static constexpr int ATOM_STRIDE = NH * 1024;
+  static constexpr int PAGE_BYTES = 2 * ATOM_STRIDE;
   static constexpr int OFF_V = OFF_K + NKV * KV_BYTES;
   static constexpr int OFF_BAR = OFF_V + NKV * KV_BYTES;
   static constexpr int OFF_RED = OFF_BAR + 128;   // softmax row max / sum exchange
@@ -141,8 +145,8 @@ __device__ __forceinline__ void chunk_tile(const CUtensorMap &tmQ, const CUtenso
     // chunks then go out as one TMA per lane (one thread issuing all of them
     // would pace the ring at ~90 cycles a copy).  Page ids: one per lane,
     // loaded a block ahead.
-    constexpr int OPS = 8 * 2 * C::NH;
-    const int my_pg = lane / (2 * C::NH), my_kv = (lane / C::NH) & 1, my_c = lane % C::NH;
+    // one copy per (page, K or V): 16 per block, lanes 0-15
+    const int my_pg = lane >> 1, my_kv = lane & 1;
     if (lane == 0) {
       mbar_arrive_expect_tx(q_full, C::Q_BYTES);
       for (int c = 0; c < C::NH; ++c) tma_load_2d(sQ + c * C::TILE_BYTES, &tmQ, q_full, h * HD + c * 64, t0 + i0);
@@ -166,14 +170,14 @@ __device__ __forceinline__ void chunk_tile(const CUtensorMap &tmQ, const CUtenso
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       int page = __shfl_sync(0xffffffffu, cur, my_pg & 7);
-      if (lane < OPS && my_pg < np) {
+      if (lane < 16 && my_pg < np) {
         if (page < 0 || page >= p.num_pages) {
           atomicExch(p.err, kErrBounds);
           page = 0;
         }
         const int z = (page * 2 + my_kv) * p.Hkv + hk;
-        uint8_t *dst = (my_kv ? sV : sK) + s * C::KV_BYTES + my_c * C::TILE_BYTES + my_pg * 2048;
-        tma_load_3d(dst, &tmKV, &kv_full[s], my_c * 64, 0, z);
+        uint8_t *dst = (my_kv ? sV : sK) + s * C::KV_BYTES + my_pg * C::PAGE_BYTES;
+        tma_load_5d(dst, &tmKV, &kv_full[s], 0, 0, 0, 0, z);
       }
       issued |= 1u << s;
       issued_ph = (issued_ph & ~(1u << s)) | (ph << s);
@@ -207,7 +211,7 @@ __device__ __forceinline__ void chunk_tile(const CUtensorMap &tmQ, const CUtenso
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             const uint64_t ad = sdesc_sw128(q0 + c * C::TILE_BYTES + kk * 32, 16, 1024);
-            const uint64_t bd = sdesc_sw128(k0 + c * C::TILE_BYTES + kk * 32, 16, 1024);
+            const uint64_t bd = sdesc_sw128(k0 + c * 1024 + kk * 32, 16, C::ATOM_STRIDE);
             mma_bf16(d, ad, bd, C::IDESC_S, (c > 0 || kk > 0) ? 1u : 0u);
           }
         mma_commit(&s_full[b]);
@@ -219,8 +223,8 @@ __device__ __forceinline__ void chunk_tile(const CUtensorMap &tmQ, const CUtenso
         // P(j) sits in TMEM over S(j): 128 keys as 64 columns of bf16 pairs
         const uint32_t pcol = tmem + b * 128;
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {  // 16 keys per MMA
-          const uint64_t bd = sdesc_sw128(vbase + ks * 2048, C::TILE_BYTES, 1024);
+        for (int ks = 0; ks < 8; ++ks) {  // 16 keys (two atoms) per MMA; hd halves 1 KB apart
+          const uint64_t bd = sdesc_sw128(vbase + ks * 2 * C::ATOM_STRIDE, 1024, C::ATOM_STRIDE);
           mma_bf16_ts(tmem + 256, pcol + ks * 8, bd, C::IDESC_PV, (j > 0 || ks > 0) ? 1u : 0u);
         }
         // the last PV is covered by the o_last commit after the loop; stages
@@ -362,13 +366,13 @@ __device__ __forceinline__ void chunk_tile(const CUtensorMap &tmQ, const CUtenso
       if (j == n_kb - 1 && 128 * j + r > last_pos) {
         // rows past the last visible key may hold stale or non-finite data:
         // zero them so that P = 0 rows contribute exactly nothing
-        uint8_t *vrow = sV + (j % C::NKV) * C::KV_BYTES + (r >> 3) * 1024 + (r & 7) * 128;
+        uint8_t *vrow = sV + (j % C::NKV) * C::KV_BYTES + (r >> 3) * C::ATOM_STRIDE + (r & 7) * 128;
 #pragma unroll
         for (int c = 0; c < C::NH; ++c)
           if ((c & 1) == hh)
 #pragma unroll
             for (int k = 0; k < 8; ++k)
-              *reinterpret_cast<uint4 *>(vrow + c * C::TILE_BYTES + k * 16) = make_uint4(0, 0, 0, 0);
+              *reinterpret_cast<uint4 *>(vrow + c * 1024 + k * 16) = make_uint4(0, 0, 0, 0);
         fence_proxy_async_smem();
       }
       tc_fence_before();
@@ -446,8 +450,11 @@ struct DecodeParams {
 template <int HD>
 struct DecCfg {
   static constexpr int NH = HD / 64;
-  static constexpr int TILE = 128 * 128;                 // [128 keys][64 bf16]
+  static constexpr int TILE = 128 * 128;                 // 128 keys x 64 bf16
   static constexpr int KV_STAGE = 2 * NH * TILE;         // K then V
+  // K and V each as [8-key group][hd half][8 keys][128 B] (one copy per page)
+  static constexpr int ATOM_STRIDE = NH * 1024;
+  static constexpr int PAGE_BYTES = 2 * ATOM_STRIDE;
   static constexpr int STAGES = 3;
   static constexpr int QT = NH * 16 * 128;               // Q^T: [NH][16 rows][128 B]
   static constexpr int PT = 2 * 16 * 128;                // P^T: [2 key chunks][16 rows][128 B]
@@ -533,8 +540,7 @@ __device__ __forceinline__ void decode_worker(const CUtensorMap &tmKV, const CUt
     // (a single thread needs ~90 cycles per copy, which would pace the ring).
     // Global loads the producer depends on (the next item, the next block's
     // page ids, one per lane) are issued a block ahead.
-    constexpr int OPS = 8 * 2 * C::NH;   // copies per full block
-    const int my_pg = lane / (2 * C::NH), my_kv = (lane / C::NH) & 1, my_c = lane % C::NH;
+    const int my_pg = lane >> 1, my_kv = lane & 1;   // one copy per (page, K or V): lanes 0-15
     int seq = 0, k_local = 0;
     bool ok = true;
     int next_item = lane == 0 ? atomicAdd(&p.ctr[0], 1) : 0;
@@ -587,14 +593,14 @@ __device__ __forceinline__ void decode_worker(const CUtensorMap &tmKV, const CUt
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
         int page = __shfl_sync(0xffffffffu, cur, my_pg & 7);
-        if (lane < OPS && my_pg < npg) {
+        if (lane < 16 && my_pg < npg) {
           if (page < 0 || page >= p.num_pages) {
             atomicExch(p.err, kErrBounds);
             page = 0;
           }
           const int z = (page * 2 + my_kv) * p.Hkv + hk;
-          tma_load_3d(sKV + s * C::KV_STAGE + (my_kv * C::NH + my_c) * C::TILE + my_pg * 2048, &tmKV, &kv_full[s],
-                      my_c * 64, 0, z);
+          tma_load_5d(sKV + s * C::KV_STAGE + my_kv * C::NH * C::TILE + my_pg * C::PAGE_BYTES, &tmKV, &kv_full[s], 0,
+                      0, 0, 0, z);
         }
         ++seq;
       }
@@ -622,7 +628,7 @@ __device__ __forceinline__ void decode_worker(const CUtensorMap &tmKV, const CUt
         for (int c = 0; c < C::NH; ++c)
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_bf16(d, sdesc_sw128(k0 + c * C::TILE + kk * 32, 16, 1024),
+            mma_bf16(d, sdesc_sw128(k0 + c * 1024 + kk * 32, 16, C::ATOM_STRIDE),
                      sdesc_sw128(q0 + c * 2048 + kk * 32, 16, 1024), C::IDESC_S, (c > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&s_full[j & 1]);
       };
@@ -631,8 +637,10 @@ __device__ __forceinline__ void decode_worker(const CUtensorMap &tmKV, const CUt
         const uint32_t v0 = smem_u32(sKV + s * C::KV_STAGE + C::NH * C::TILE);
         const uint32_t p0 = smem_u32(sP + (j & 1) * C::PT);
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks)   // 16 keys per MMA
-          mma_bf16(d, sdesc_sw128(v0 + ks * 2048, C::TILE, 1024),
+        // 16 keys (two atoms) per MMA; the hd halves are 1 KB apart (hd 64: the
+        // ignored upper 64 rows are read 16 KB on)
+        for (int ks = 0; ks < 8; ++ks)
+          mma_bf16(d, sdesc_sw128(v0 + ks * 2 * C::ATOM_STRIDE, C::NH == 2 ? 1024 : C::TILE, C::ATOM_STRIDE),
                    sdesc_sw128(p0 + (ks >> 2) * 2048 + (ks & 3) * 32, 16, 1024), C::IDESC_PV, ks > 0 ? 1u : 0u);
         mma_commit(&o_full[j & 1]);
         mma_commit(&kv_empty[s]);
@@ -771,12 +779,12 @@ __device__ __forceinline__ void decode_worker(const CUtensorMap &tmKV, const CUt
         *reinterpret_cast<__nv_bfloat16 *>(pt + sw128_offset(g, t & 63)) = __float2bfloat16_rn(pr[g]);
       if (!valid) {
         // a key past kv_len: its V row may hold anything; make it exactly 0
-        uint8_t *vrow = sKV + s * C::KV_STAGE + C::NH * C::TILE + (t >> 3) * 1024 + (t & 7) * 128;
+        uint8_t *vrow = sKV + s * C::KV_STAGE + C::NH * C::TILE + (t >> 3) * C::ATOM_STRIDE + (t & 7) * 128;
 #pragma unroll
         for (int c = 0; c < C::NH; ++c)
 #pragma unroll
           for (int k = 0; k < 8; ++k)
-            *reinterpret_cast<uint4 *>(vrow + c * C::TILE + k * 16) = make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4 *>(vrow + c * 1024 + k * 16) = make_uint4(0, 0, 0, 0);
       }
       fence_proxy_async_smem();
       mbar_arrive(&p_full[j & 1]);

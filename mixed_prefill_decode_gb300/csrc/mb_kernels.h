@@ -13,9 +13,8 @@ constexpr int kPage = 16;
 // not link libcuda, so it loads on machines without a driver) ----
 cudaError_t encode_tmap_2d(CUtensorMap *map, const void *base, uint64_t inner, uint64_t outer,
                            uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer);
-cudaError_t encode_tmap_3d(CUtensorMap *map, const void *base, uint64_t d0, uint64_t d1, uint64_t d2,
-                           uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t b0, uint32_t b1, uint32_t b2);
-
+cudaError_t encode_tmap_5d(CUtensorMap *map, const void *base, const uint64_t dims[5], const uint64_t strides_bytes[4],
+                           const uint32_t box[5]);
 int device_sm_count();
 
 // ---- token-batched GEMM on tcgen05 ----
@@ -70,7 +69,7 @@ struct AttnArgs {
   int *err;
   const CUtensorMap *tm_q;  // Q map [T][Hq hd], box 64 x 128 (host pointer; copied into launch)
   const CUtensorMap *tm_qd; // Q map [T Hq][hd], box 64 x 16: the G q-heads of one decode row (and padding)
-  const CUtensorMap *tm_kv; // pool map [P*2*Hkv][16][hd], box 64 x 16 x 1
+  const CUtensorMap *tm_kv; // pool map, 5-D view of [P*2*Hkv][16][hd]: one (page, K/V, head) block per copy
   int *dec_ctr;             // two ints, zero between launches: decode work counter
 };
 // Prefill-chunk tiles and persistent decode workers (both tcgen05) in one launch.
