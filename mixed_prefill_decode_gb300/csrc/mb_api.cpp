@@ -20,7 +20,7 @@
 #include "mb_kernels.h"
 
 #ifndef MB_DEC_ITEMS_PER_SM
-#define MB_DEC_ITEMS_PER_SM 8
+#define MB_DEC_ITEMS_PER_SM 4
 #endif
 
 namespace mb {
@@ -325,8 +325,9 @@ mb_status validate_batch(const mb_batch *b, int32_t num_pages, int32_t max_token
 // work lists live in the uploaded blob, and their sizes.
 struct StepPlan {
   int64_t T = 0;
-  size_t o_qo = 0, o_kv = 0, o_bti = 0, o_bt = 0, o_treq = 0, o_tpos = 0, o_tiles = 0, o_items = 0, o_merge = 0;
-  int n_tiles = 0, n_items = 0, n_merge = 0;
+  size_t o_qo = 0, o_kv = 0, o_bti = 0, o_bt = 0, o_treq = 0, o_tpos = 0, o_tiles = 0, o_items = 0;
+  int n_tiles = 0, n_items = 0, n_merge = 0;   // n_merge: (request, KV head) groups with several splits
+  size_t merge_off = 0;                        // their counters, in floats from the partials' base
   const int32_t *db = nullptr;
   int64_t upload_bytes = 0;
 };
@@ -393,35 +394,39 @@ mb_status prepare_step(mb_layer *L, const mb_batch *b, int64_t T, cudaStream_t s
     hb[P.o_tiles + 4 * i + 1] = tiles[i].i0;
     hb[P.o_tiles + 4 * i + 2] = tiles[i].h;
   }
-  // decode splits: about MB_DEC_ITEMS_PER_SM items per SM, each request's
-  // pages divided evenly among its splits, at least one 128-key block per
-  // item.  Workers take items dynamically, so the tail is about one item long.
+  // decode splits: about MB_DEC_ITEMS_PER_SM items per SM.  A request's
+  // 128-key blocks (8 pages) are divided evenly among its splits, so only its
+  // last block can be partial.  Workers take items dynamically, so the tail
+  // is about one item long; the splits of one (request, KV head) are
+  // consecutive items {req, kv_head, page_begin, page_end, split, n_splits,
+  // group, 0}, and the last one to finish merges them (group = its counter).
   const int64_t target_items = static_cast<int64_t>(ctx->sms) * MB_DEC_ITEMS_PER_SM;
-  int64_t pps = (dec_pages * Hkv + target_items - 1) / std::max<int64_t>(1, target_items);
-  pps = std::max<int64_t>(pps, 8);
-  std::vector<int32_t> items, merges;
+  const int64_t dec_blocks = (dec_pages + 7) / 8;   // upper bound per KV head, summed over requests
+  const int64_t bps = std::max<int64_t>(1, (dec_blocks * Hkv + target_items - 1) / std::max<int64_t>(1, target_items));
+  std::vector<int32_t> items;
+  int32_t n_groups = 0;
   for (int r = 0; r < n; ++r) {
     const int32_t qo = b->qo_indptr[r + 1] - b->qo_indptr[r];
     if (qo != 1) continue;
     const int32_t np = pages_for(b->kv_len[r]);
-    const int32_t ns = static_cast<int32_t>(std::max<int64_t>(1, (np + pps / 2) / pps));
+    const int32_t nblk = (np + 7) / 8;
+    // at most 32 splits: the merge holds one split per lane
+    const int32_t ns = static_cast<int32_t>(
+        std::max<int64_t>(1, std::min<int64_t>({nblk, (nblk + bps / 2) / bps, 32})));
     for (int32_t hk = 0; hk < Hkv; ++hk) {
-      const int32_t first = static_cast<int32_t>(items.size() / 8);
+      const int32_t grp = ns > 1 ? n_groups++ : -1;
       for (int32_t sidx = 0; sidx < ns; ++sidx) {
-        const int32_t pb = static_cast<int32_t>(static_cast<int64_t>(np) * sidx / ns);
-        const int32_t pe = static_cast<int32_t>(static_cast<int64_t>(np) * (sidx + 1) / ns);
-        items.insert(items.end(), {r, hk, pb, pe, sidx, ns, 0, 0});
+        const int32_t pb = 8 * static_cast<int32_t>(static_cast<int64_t>(nblk) * sidx / ns);
+        const int32_t pe = std::min(np, 8 * static_cast<int32_t>(static_cast<int64_t>(nblk) * (sidx + 1) / ns));
+        items.insert(items.end(), {r, hk, pb, pe, sidx, ns, grp, 0});
       }
-      if (ns > 1) merges.insert(merges.end(), {r, hk, first, ns});
     }
   }
   P.o_items = sec(items.size());
-  P.o_merge = sec(merges.size());
   std::copy(items.begin(), items.end(), hb.begin() + P.o_items);
-  std::copy(merges.begin(), merges.end(), hb.begin() + P.o_merge);
   P.n_tiles = static_cast<int>(tiles.size());
   P.n_items = static_cast<int>(items.size() / 8);
-  P.n_merge = static_cast<int>(merges.size() / 4);
+  P.n_merge = n_groups;
 
   // ---- upload through a pinned ring slot
   StagingSlot &slot = L->ring[L->ring_next];
@@ -454,19 +459,23 @@ mb_status prepare_step(mb_layer *L, const mb_batch *b, int64_t T, cudaStream_t s
     }
     L->dblob_cap = cap;
   }
-  const size_t part_need = static_cast<size_t>(P.n_items) * G * (hd + 4);  // rows of hd + 4 floats
+  // decode split partials (rows of hd + 4 floats: o, m, l, pad), then one
+  // merge counter per split group; counters must start at zero
+  const size_t part_need = static_cast<size_t>(P.n_items) * G * (hd + 4) + static_cast<size_t>(P.n_merge);
   if (L->part_cap < part_need) {
     cudaStreamSynchronize(s);
     if (L->part) cudaFree(L->part);
     L->part = nullptr;
     size_t cap = part_need * 2;
     st = alloc_dev(reinterpret_cast<void **>(&L->part), cap * 4, "decode partials");
+    if (st == MB_OK && cudaMemset(L->part, 0, cap * 4) != cudaSuccess) st = fail(MB_ECUDA, "cudaMemset(partials)");
     if (st != MB_OK) {
       L->part_cap = 0;
       return st;
     }
     L->part_cap = cap;
   }
+  P.merge_off = static_cast<size_t>(P.n_items) * G * (hd + 4);
   std::memcpy(slot.host, hb.data(), hb.size() * 4);
   e = cudaMemcpyAsync(L->dblob, slot.host, hb.size() * 4, cudaMemcpyHostToDevice, s);
   if (e != cudaSuccess) return mb::fail(MB_ECUDA, "step: descriptor upload: %s", cudaGetErrorString(e));
@@ -553,20 +562,11 @@ mb_status launch_layer(mb_layer *L, mb_layer *W, mb_kv *kv, const StepPlan &P, c
   aa.tm_qd = &tm_qd;
   aa.tm_kv = &kv->tmap;
   aa.dec_ctr = W->err + 2;   // words 2-3 of the layer's error block
+  aa.merge_ctr = reinterpret_cast<int *>(W->part + P.merge_off);
   if ((st = chk(mb::attention_run(aa, s), "attention")) != MB_OK) return st;
   *launches += (aa.n_tiles + aa.n_items) > 0;
   mark(4);
-  mb::MergeArgs ma;
-  ma.part = W->part;
-  ma.merge_list = db + P.o_merge;
-  ma.n_merge = P.n_merge;
-  ma.o = W->o;
-  ma.qo_indptr = db + P.o_qo;
-  ma.Hq = Hq;
-  ma.Hkv = Hkv;
-  ma.hd = hd;
-  if ((st = chk(mb::attn_merge_run(ma, s), "merge")) != MB_OK) return st;
-  *launches += P.n_merge > 0;
+  // (split merging happens inside the attention launch)
   mark(5);
   if ((st = chk(mb::gemm_run(W->o, L->w.w_o, &L->tm_wo, W->h, x_in, Ti, d.d_model, hqd, mb::kEpiResidual, W->gws,
                              W->err, s), "gemm o")) != MB_OK)
@@ -815,6 +815,8 @@ mb_status mb_device_status(mb_layer *L, void *stream) {
   if (e != cudaSuccess) return fail(MB_ECUDA, "mb_device_status: %s", cudaGetErrorString(e));
   if (code != 0) {
     cudaMemset(errp, 0, 16);
+    // a decode worker that gave up may leave split-merge counters raised
+    if (L && L->part) cudaMemset(L->part, 0, L->part_cap * 4);
     // a kernel that unwound early may leave stream-K tickets raised
     cudaMemset(ctx->gemm_ws, 0, mb::gemm_workspace_bytes());
     return fail(MB_EDEVICE, "mb_device_status: kernel error code %d", code);

@@ -445,6 +445,7 @@ struct DecodeParams {
   float scale_log2;
   int *err;
   int *ctr;   // [0]: next item, [1]: workers done (the last one resets both)
+  int *mctr;  // per split (request, KV head): splits finished (the merger resets it)
 };
 
 template <int HD>
@@ -462,7 +463,8 @@ struct DecCfg {
   static constexpr int OFF_P = OFF_Q + 2 * QT;
   static constexpr int OFF_HDR = OFF_P + 2 * PT;
   static constexpr int OFF_RED = OFF_HDR + STAGES * 32;
-  static constexpr int OFF_BAR = OFF_RED + 2 * 4 * 16 * 4;
+  static constexpr int OFF_FLAG = OFF_RED + 2 * 4 * 16 * 4;   // merge decision broadcast
+  static constexpr int OFF_BAR = OFF_FLAG + 16;
   static constexpr int SMEM = OFF_BAR + 256;
   static constexpr uint32_t IDESC_S = idesc_bf16_ab(128, 16, false, false);
   static constexpr uint32_t IDESC_PV = idesc_bf16_ab(128, 16, true, false);
@@ -486,6 +488,7 @@ __device__ __forceinline__ void decode_worker(const CUtensorMap &tmKV, const CUt
   uint8_t *sP = smem + C::OFF_P;
   DecHdr *hdr = reinterpret_cast<DecHdr *>(smem + C::OFF_HDR);
   float *red = reinterpret_cast<float *>(smem + C::OFF_RED);     // [max | sum][4 warps][16]
+  volatile int *merge_flag = reinterpret_cast<volatile int *>(smem + C::OFF_FLAG);
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
   uint64_t *kv_full = bars;                  // [STAGES]
   uint64_t *kv_empty = bars + C::STAGES;     // [STAGES]
@@ -645,71 +648,60 @@ __device__ __forceinline__ void decode_worker(const CUtensorMap &tmKV, const CUt
         mma_commit(&o_full[j & 1]);
         mma_commit(&kv_empty[s]);
       };
-      int qcount = 0;   // items whose Q^T the S MMAs have used
-      // block 0
-      bool ok = mbar_wait(&kv_full[0], 0, abort_flag, p.err, kErrWaitMma);
-      bool done = !ok || hdr[0].item < 0;
-      if (!done) {
-        ok = mbar_wait(&q_full[0], 0, abort_flag, p.err, kErrWaitMma);
-        if (ok) {
-          tc_fence_after();
-          issue_s(0, 0, 0);
-          if (hdr[0].flags & 2) {
-            mma_commit(&q_empty[0]);
-            ++qcount;
-          }
-        }
-        done = !ok;
-      }
-      for (int j = 0; !done; ++j) {
-        const int s = j % C::STAGES, s1 = (j + 1) % C::STAGES;
-        bool s_done = false, pv_done = false, last = false;
-        const uint64_t t_start = globaltimer();
-        for (uint32_t spin = 0; !(s_done && pv_done); ++spin) {
-          const bool was = s_done || pv_done;
-          if (!s_done && mbar_test_wait(smem_u32(&kv_full[s1]), ((j + 1) / C::STAGES) & 1)) {
-            if (hdr[s1].item < 0) {
-              s_done = true;
-              last = true;
+      // S and PV advance independently: S(ns) goes out as soon as its K (and
+      // the item's Q) landed and S buffer ns&1 is free, PV(np) as soon as P(np)
+      // is written and O_blk buffer np&1 is free.
+      int ns = 0, npv = 0, qcount = 0;   // qcount: items whose Q^T the S MMAs are done with
+      bool s_end = false, ok = true;
+      uint64_t t_idle = globaltimer();
+      for (uint32_t spin = 0;; ++spin) {
+        bool progress = false;
+        if (!s_end) {
+          const int s = ns % C::STAGES;
+          if (mbar_test_wait(smem_u32(&kv_full[s]), (ns / C::STAGES) & 1)) {
+            if (hdr[s].item < 0) {
+              s_end = progress = true;
             } else {
-              const int qb = hdr[s1].qb;
-              const bool need_q = hdr[s1].flags & 1;
+              const int qb = hdr[s].qb;
+              const bool need_q = hdr[s].flags & 1;
               if ((!need_q || mbar_test_wait(smem_u32(&q_full[qb]), (qcount >> 1) & 1)) &&
-                  mbar_test_wait(smem_u32(&s_empty[(j + 1) & 1]), (((j + 1) >> 1) & 1) ^ 1)) {
+                  mbar_test_wait(smem_u32(&s_empty[ns & 1]), ((ns >> 1) & 1) ^ 1)) {
                 tc_fence_after();
-                issue_s(j + 1, s1, qb);
-                if (hdr[s1].flags & 2) {
+                issue_s(ns, s, qb);
+                if (hdr[s].flags & 2) {
                   mma_commit(&q_empty[qb]);
                   ++qcount;
                 }
-                s_done = true;
+                ++ns;
+                progress = true;
               }
             }
           }
-          bool progress = false;
-          if (!pv_done && mbar_test_wait(smem_u32(&p_full[j & 1]), (j >> 1) & 1) &&
-              mbar_test_wait(smem_u32(&o_empty[j & 1]), ((j >> 1) & 1) ^ 1)) {
-            tc_fence_after();
-            issue_pv(j, s);
-            pv_done = progress = true;
+        }
+        if (npv < ns && mbar_test_wait(smem_u32(&p_full[npv & 1]), (npv >> 1) & 1) &&
+            mbar_test_wait(smem_u32(&o_empty[npv & 1]), ((npv >> 1) & 1) ^ 1)) {
+          tc_fence_after();
+          issue_pv(npv, npv % C::STAGES);
+          ++npv;
+          progress = true;
+        }
+        if (s_end && npv == ns) break;
+        if (progress) {
+          t_idle = globaltimer();
+        } else if ((spin & 15u) == 15u) {
+          if (*abort_flag) {
+            ok = false;
+            break;
           }
-          // back off: this thread shares a scheduler with a softmax warp
-          if (!progress && was == (s_done || pv_done)) __nanosleep(64);
-          if ((spin & 63u) == 63u) {
-            if (*abort_flag) {
-              ok = false;
-              break;
-            }
-            if (globaltimer() - t_start > kWaitLimitNs) {
-              *abort_flag = 1;
-              atomicExch(p.err, kErrWaitMma);
-              ok = false;
-              break;
-            }
+          if (globaltimer() - t_idle > kWaitLimitNs) {
+            *abort_flag = 1;
+            atomicExch(p.err, kErrWaitMma);
+            ok = false;
+            break;
           }
         }
-        done = !ok || last;
       }
+      (void)ok;
       // every MMA issued above has completed before TMEM is freed
       mma_commit(mma_done);
       const uint64_t t_end = globaltimer();
@@ -821,36 +813,78 @@ __device__ __forceinline__ void decode_worker(const CUtensorMap &tmKV, const CUt
           for (int g = 0; g < G; ++g) o[g] = fmaf(o[g], al[g], ob[g]);
         return !b;
       };
-      if (!(h.flags & 1) && !fold(j - 1, alpha_prev)) {
-        ok = false;
-        continue;   // the next block's first barrier-OR takes every thread out
-      }
+      // a failed wait leaves via the next block's first barrier-OR
+      if (!(h.flags & 1) && !fold(j - 1, alpha_prev)) ok = false;
 #pragma unroll
       for (int g = 0; g < G; ++g) alpha_prev[g] = alpha[g];
       if (!(h.flags & 2)) continue;
-      if (!fold(j, alpha)) {
-        ok = false;
-        continue;
-      }
-      if (t < HD) {
-        const int32_t *it = p.items + h.item * 8;
-        const int req = it[0], hk = it[1], n_splits = it[5];
-        if (n_splits == 1) {
-          const size_t tok = static_cast<size_t>(p.qo_indptr[req]);
+      if (ok && !fold(j, alpha)) ok = false;
+      if (named_bar_or(1, 128, !ok)) break;   // all or none enter the barriers below
+      // ---- the item is done: its output, or its split's partial
+      const int32_t *it = p.items + h.item * 8;
+      const int req = it[0], hk = it[1], sidx = it[4], n_splits = it[5], grp = it[6];
+      const size_t tok = static_cast<size_t>(p.qo_indptr[req]);
+      if (n_splits == 1) {
+        if (t < HD)
 #pragma unroll
           for (int g = 0; g < G; ++g)
             p.o[(tok * p.Hq + hk * G + g) * HD + t] = __float2bfloat16_rn(o[g] / l[g]);
-        } else {
+        continue;
+      }
+      if (t < HD)
 #pragma unroll
-          for (int g = 0; g < G; ++g) {
-            float *dst = p.part + (static_cast<size_t>(h.item) * G + g) * part_stride<HD>();
-            dst[t] = o[g];
-            if (t == 0) {
-              dst[HD] = m[g];
-              dst[HD + 1] = l[g];
-            }
+        for (int g = 0; g < G; ++g) {
+          float *dst = p.part + (static_cast<size_t>(h.item) * G + g) * part_stride<HD>();
+          dst[t] = o[g];
+          if (t == 0) {
+            dst[HD] = m[g];
+            dst[HD + 1] = l[g];
           }
         }
+      // The last split of the (request, KV head) to finish merges all of its
+      // partials by log-sum-exp: o = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s.
+      __threadfence();
+      named_bar_sync(1, 128);
+      if (t == 0) *merge_flag = atomicAdd(&p.mctr[grp], 1) == n_splits - 1;
+      named_bar_sync(1, 128);
+      if (*merge_flag) {
+        // warp q takes heads q, q + 4, ...; lane s holds split s's (m, l)
+        // (at most 32 splits), the hd row is spread over the lanes, and the
+        // loads of consecutive splits are independent, so a merge costs a few
+        // L2 round trips rather than one per split
+        __threadfence();
+        const float *first = p.part + static_cast<size_t>(h.item - sidx) * G * part_stride<HD>();
+        constexpr int PER = HD / 32;
+        for (int g = q; g < G; g += 4) {
+          float mv = -INFINITY, lv = 0.f;
+          if (lane < n_splits) {
+            const float *src = first + (static_cast<size_t>(lane) * G + g) * part_stride<HD>();
+            mv = src[HD];
+            lv = src[HD + 1];
+          }
+          float M = mv;
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+          const float w = lane < n_splits ? exp2f(mv - M) : 0.f;
+          float L = w * lv;
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+          float acc[PER];
+#pragma unroll
+          for (int k = 0; k < PER; ++k) acc[k] = 0.f;
+#pragma unroll 4
+          for (int sp = 0; sp < n_splits; ++sp) {
+            const float ws = __shfl_sync(0xffffffffu, w, sp);
+            const float *src = first + (static_cast<size_t>(sp) * G + g) * part_stride<HD>();
+#pragma unroll
+            for (int k = 0; k < PER; ++k) acc[k] = fmaf(ws, src[lane + 32 * k], acc[k]);
+          }
+          const float inv = 1.f / L;
+#pragma unroll
+          for (int k = 0; k < PER; ++k)
+            p.o[(tok * p.Hq + hk * G + g) * HD + lane + 32 * k] = __float2bfloat16_rn(acc[k] * inv);
+        }
+        if (t == 0) p.mctr[grp] = 0;   // ready for the next launch
       }
     }
     tc_fence_before();
@@ -871,40 +905,6 @@ __device__ __forceinline__ void decode_worker(const CUtensorMap &tmKV, const CUt
       __threadfence();
     }
   }
-}
-
-// ============================================================ merge pass
-// One warp per (request, q head) with several splits: o = sum_s w_s o_s /
-// sum_s w_s l_s with w_s = 2^(m_s - max m).
-template <int HD>
-__global__ void __launch_bounds__(128) merge_kernel(const float *part, const int32_t *list, int n, __nv_bfloat16 *o,
-                                                    const int32_t *qo_indptr, int Hq, int G) {
-  pdl_wait();
-  const int w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  if (w >= n * G) return;
-  const int lane = threadIdx.x & 31;
-  const int idx = w / G, g = w % G;
-  const int req = list[idx * 4 + 0], hk = list[idx * 4 + 1], first = list[idx * 4 + 2], ns = list[idx * 4 + 3];
-  float mmax = -INFINITY;
-  for (int s = 0; s < ns; ++s) mmax = fmaxf(mmax, part[(static_cast<size_t>(first + s) * G + g) * part_stride<HD>() + HD]);
-  constexpr int PER = HD / 32;
-  float acc[PER];
-#pragma unroll
-  for (int e = 0; e < PER; ++e) acc[e] = 0.f;
-  float L = 0.f;
-  for (int s = 0; s < ns; ++s) {
-    const float *src = part + (static_cast<size_t>(first + s) * G + g) * part_stride<HD>();
-    const float ms = src[HD];
-    const float wgt = (ms == -INFINITY) ? 0.f : exp2f(ms - mmax);
-    L += wgt * src[HD + 1];
-#pragma unroll
-    for (int e = 0; e < PER; ++e) acc[e] += wgt * src[lane * PER + e];
-  }
-  const float inv = 1.f / L;
-  const int t = qo_indptr[req];
-  __nv_bfloat16 *dst = o + (static_cast<size_t>(t) * Hq + hk * G + g) * HD + lane * PER;
-#pragma unroll
-  for (int e = 0; e < PER; ++e) dst[e] = __float2bfloat16_rn(acc[e] * inv);
 }
 
 // ============================================================ one grid
@@ -1004,23 +1004,11 @@ cudaError_t attention_run(const AttnArgs &a, cudaStream_t st) {
   dp.scale_log2 = scale_log2;
   dp.err = a.err;
   dp.ctr = a.dec_ctr;
+  dp.mctr = a.merge_ctr;
   dp.n_workers = a.n_items < device_sm_count() ? a.n_items : device_sm_count();
   const int G = a.Hq / a.Hkv;
   return a.hd == 128 ? launch_attention_g<128>(*a.tm_q, *a.tm_kv, *a.tm_qd, cp, dp, a.n_tiles, G, st)
                      : launch_attention_g<64>(*a.tm_q, *a.tm_kv, *a.tm_qd, cp, dp, a.n_tiles, G, st);
-}
-
-cudaError_t attn_merge_run(const MergeArgs &m, cudaStream_t st) {
-  if (m.n_merge <= 0) return cudaSuccess;
-  const int G = m.Hq / m.Hkv;
-  const int warps = m.n_merge * G;
-  const int blocks = (warps + 3) / 4;
-  __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(m.o);
-  if (m.hd == 128)
-    return launch_pdl(merge_kernel<128>, dim3(blocks), dim3(128), 0, st, 1, m.part, m.merge_list, m.n_merge, o,
-                      m.qo_indptr, m.Hq, G);
-  return launch_pdl(merge_kernel<64>, dim3(blocks), dim3(128), 0, st, 1, m.part, m.merge_list, m.n_merge, o,
-                    m.qo_indptr, m.Hq, G);
 }
 
 }  // namespace mb

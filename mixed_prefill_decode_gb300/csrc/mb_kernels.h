@@ -63,7 +63,7 @@ struct AttnArgs {
   const int32_t *qo_indptr, *kv_len, *bt_indptr, *bt;
   const int32_t *tiles;     // chunk tile list
   const int32_t *items;     // decode item list
-  float *part;              // decode split partials [n_items][Hq/Hkv group][hd + 4]: o, m, l, pad
+  float *part;              // decode split partials [n_items][Hq/Hkv group][hd + 4]: o, m, l, pad (merged in-kernel)
   int n_tiles, n_items;
   int T, Hq, Hkv, hd, num_pages;
   int *err;
@@ -71,18 +71,9 @@ struct AttnArgs {
   const CUtensorMap *tm_qd; // Q map [T Hq][hd], box 64 x 16: the G q-heads of one decode row (and padding)
   const CUtensorMap *tm_kv; // pool map, 5-D view of [P*2*Hkv][16][hd]: one (page, K/V, head) block per copy
   int *dec_ctr;             // two ints, zero between launches: decode work counter
+  int *merge_ctr;           // one int per split group, zero between launches
 };
 // Prefill-chunk tiles and persistent decode workers (both tcgen05) in one launch.
 cudaError_t attention_run(const AttnArgs &a, cudaStream_t st);
-
-struct MergeArgs {
-  const float *part;
-  const int32_t *merge_list;  // per merged (req, kv_head): {req, kv_head, first_slot, n_splits}
-  int n_merge;
-  void *o;
-  const int32_t *qo_indptr;
-  int Hq, Hkv, hd;
-};
-cudaError_t attn_merge_run(const MergeArgs &m, cudaStream_t st);
 
 }  // namespace mb
