@@ -725,7 +725,7 @@ mb_status mb_kv_alloc(mb_layer *L, int32_t num_pages, void *dev_buf, mb_kv **out
   // one hd half form a swizzle atom, and consecutive atoms of a half sit
   // hd/64 KB apart, which the tensor-core descriptors step over uniformly.
   const uint64_t nh = static_cast<uint64_t>(hd) / 64;
-  const uint64_t dims5[5] = {64, 8, nh, MB_PAGE_TOKENS / 8, z};
+  const uint64_t dims5[5] = {64, 8, nh, MB_PAGE_TOKENS / 8, static_cast<uint64_t>(z)};
   const uint64_t strides5[4] = {static_cast<uint64_t>(hd) * 2, 128, 8ull * hd * 2, MB_PAGE_TOKENS * hd * 2ull};
   const uint32_t box5[5] = {64, 8, static_cast<uint32_t>(nh), MB_PAGE_TOKENS / 8, 1};
   cudaError_t e = mb::encode_tmap_5d(&kv->tmap, kv->base, dims5, strides5, box5);

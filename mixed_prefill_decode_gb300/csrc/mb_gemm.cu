@@ -193,7 +193,9 @@ __device__ __forceinline__ int slot_of(const Params &p, int rank, int mi, int u)
   return 2 * c + (u == static_cast<int>(rank_lo(p, rank) / p.k_iters) ? 0 : 1);
 }
 
-__device__ __forceinline__ float silu(float x) { return x / (1.0f + expf(-x)); }
+// silu(x) = x / (1 + e^-x), with the fast exponential and reciprocal: their
+// relative error (~1e-6) is far below the bf16 rounding of the result.
+__device__ __forceinline__ float silu(float x) { return x * __frcp_rn(1.0f + __expf(-x)); }
 
 template <int NH>
 __device__ __forceinline__ float *part_chunk(const Params &p, int slot, int h, int j, int r) {
@@ -295,19 +297,34 @@ __global__ void __launch_bounds__(TileCfg<NH>::THREADS, 1)
   const uint32_t crank = p.cluster > 1 ? cluster_ctarank() : 0;
   const uint16_t cmask = static_cast<uint16_t>((1u << p.cluster) - 1u);
 
+  // The weights are read-only for the whole stream: while earlier kernels
+  // finish, arm the first stages and load their weight tiles (and warm L2
+  // with the next ones); only the activation tiles wait for those kernels.
+  int pre = 0;   // stages whose weight tiles are already on their way
   if (warp == 0 && lane == 0) {
-    // The weights are read-only for the whole stream: start pulling this
-    // CTA's first weight k-blocks into L2 while earlier kernels finish.
     SegIter first(p);
     Seg s0;
-    const bool prefetcher = p.grouped ? (blockIdx.x % p.tiles_m) == 0 : true;
-    if (prefetcher && first.next(s0)) {
+    if (first.next(s0)) {
+      const int nh = halves_of<NH>(p, (s0.tile % p.tiles_m) * BM);
       const int nt = s0.tile / p.tiles_m;
       const int rows0 = EPI == kEpiSwiGLU ? nt * 128 : nt * BN;
       const int rows1 = EPI == kEpiSwiGLU ? p.F + nt * 128 : nt * BN + 128;
-      for (int kb = s0.k0; kb < s0.k1 && kb < s0.k0 + kPrefetchAhead; ++kb) {
-        tma_prefetch_2d(&tmB, kb * BK, rows0);
-        tma_prefetch_2d(&tmB, kb * BK, rows1);
+      const bool prefetcher = p.grouped ? (blockIdx.x % p.tiles_m) == 0 : true;
+      if (prefetcher)
+        for (int kb = s0.k0 + STAGES; kb < s0.k1 && kb < s0.k0 + STAGES + kPrefetchAhead; ++kb) {
+          tma_prefetch_2d(&tmB, kb * BK, rows0);
+          tma_prefetch_2d(&tmB, kb * BK, rows1);
+        }
+      for (int kb = s0.k0; kb < s0.k1 && pre < STAGES; ++kb, ++pre) {
+        mbar_arrive_expect_tx(&full[pre], nh * A_HALF + B_STAGE);
+        if (p.cluster == 1) {
+          tma_load_2d(sB + pre * B_STAGE, &tmB, &full[pre], kb * BK, rows0);
+          tma_load_2d(sB + pre * B_STAGE + B_STAGE / 2, &tmB, &full[pre], kb * BK, rows1);
+        } else if (crank == 0) {
+          tma_load_2d_mc(sB + pre * B_STAGE, &tmB, &full[pre], kb * BK, rows0, cmask);
+        } else if (crank == 1) {
+          tma_load_2d_mc(sB + pre * B_STAGE + B_STAGE / 2, &tmB, &full[pre], kb * BK, rows1, cmask);
+        }
       }
     }
   }
@@ -321,6 +338,7 @@ __global__ void __launch_bounds__(TileCfg<NH>::THREADS, 1)
       int s = 0;
       uint32_t ph = 0;
       uint32_t issued_mask = 0, issued_ph = 0;
+      int n_issued = 0;   // k steps issued so far (the first `pre` have their weights in flight)
       bool ok = true;
       while (ok && segs.next(sg)) {
         const int m0 = (sg.tile % p.tiles_m) * BM;
@@ -345,10 +363,12 @@ __global__ void __launch_bounds__(TileCfg<NH>::THREADS, 1)
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&full[s], nh * A_HALF + B_STAGE);
+          const bool b_sent = n_issued++ < pre;
+          if (!b_sent) mbar_arrive_expect_tx(&full[s], nh * A_HALF + B_STAGE);
           tma_load_2d(sA + s * A_STAGE, &tmA, &full[s], kb * BK, m0);
           if (nh == 2) tma_load_2d(sA + s * A_STAGE + A_HALF, &tmA, &full[s], kb * BK, m0 + HM);
-          if (p.cluster == 1) {
+          if (b_sent) {
+          } else if (p.cluster == 1) {
             tma_load_2d(sB + s * B_STAGE, &tmB, &full[s], kb * BK, rows0);
             tma_load_2d(sB + s * B_STAGE + B_STAGE / 2, &tmB, &full[s], kb * BK, rows1);
           } else if (crank == 0) {
