@@ -20,6 +20,9 @@ SHAPES = [
     # 256-row tiles (from 1,024 tokens on): a ragged last half, a tile with one
     # half, split and data-parallel schedules
     (1100, 1536, 512), (1300, 768, 1024), (2144, 2560, 2048), (4100, 512, 256),
+    # 192-row tiles (385 to 1,023 tokens): a 16-row last tile, a 124-row one with a single
+    # half, six tiles with a 40-row tail
+    (400, 768, 512), (700, 1536, 1024), (1000, 512, 256),
 ]
 
 
@@ -46,7 +49,8 @@ def test_gemm_store_and_residual(mb, M, N, K, epi):
 
 
 @pytest.mark.parametrize("M,F,K", [(68, 1024, 256), (200, 1536, 512), (576, 14336, 4096), (16, 17408, 5120),
-                                   (130, 128, 64), (1040, 1024, 512), (2216, 2048, 1024)])
+                                   (130, 128, 64), (1040, 1024, 512), (2216, 2048, 1024),
+                                   (700, 1024, 512)])
 def test_gemm_swiglu(mb, M, F, K):
     A, B, _ = _inputs(M, 2 * F, K, M + F + K)
     dA, dB = to_dev(A), to_dev(B)
