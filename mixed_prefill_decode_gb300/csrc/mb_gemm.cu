@@ -6,15 +6,26 @@
 // "are 64 more rows in a 4,160-row matrix multiply").
 //
 // D[M][N] = A[M][K] B[N][K]^T, bf16 in, fp32 accumulate in TMEM.
-//   tile      256 (tokens) x 256 (weight rows), K step 64 (one 128-byte
-//             swizzle atom): two M = 128 MMAs per K step share the B tile, so a
-//             64 KB stage feeds 1,024 tensor cycles (a 128-row tile would need
-//             48 KB per 512).  A tile whose second half lies past M issues and
-//             loads only the first.  3-stage TMA ring (64 KB per stage).
-//   warps     0: TMA producer, 1: MMA issuer (+ TMEM owner), 2-9: epilogue
-//             (warp w reads TMEM lane quarter w % 4 of half (w - 2) / 4)
-//   TMEM      the two halves' 256-column fp32 accumulators fill all 512
-//             columns; the epilogue drains a tile before the next one starts
+//   tiles     by token count M (K step 64: one 128-byte swizzle atom):
+//             * M <= 128: 128 x 256 per CTA, 4 stages of 48 KB, two
+//               256-column accumulators (the epilogue of one tile overlaps
+//               the next tile's main loop);
+//             * otherwise 256 x 256 over a CTA pair (tcgen05 cta_group::2):
+//               each CTA stages its 128 rows of A and one 128-row half of B
+//               (32 KB a stage, 6 stages), rank 0 issues M = 256 MMAs that
+//               read both CTAs' stages, each CTA's TMEM holds its 128 rows in
+//               two 256-column accumulators;
+//             * below 1,024 tokens, where 128-row tiles pad M less (M mod 256
+//               in 1..128), 128 x 256 per CTA as for M <= 128.
+//             The main loop is bound by load latency: a stage takes ~1,700-
+//             2,900 cycles from its slot freeing to the MMA seeing it full,
+//             so throughput is stages x stage bytes in flight over that time;
+//             the pair's 32 KB stage per 512 MMA cycles (against 48 KB)
+//             is what lets 6 stages cover it.
+//   warps     0: TMA producer, 1: MMA issuer (+ TMEM owner), 2-5: epilogue
+//             (warp w reads TMEM lane quarter w % 4); the 256-row-per-CTA
+//             configuration (NH = 2, not used by the dispatcher) adds warps 6-9
+//   TMEM      all 512 columns
 //   schedule  persistent; whole tiles data-parallel while there are several
 //             waves, the last one to two waves split along K evenly over all
 //             CTAs (stream-K).  A split tile's later pieces go to fp32 partial
@@ -34,6 +45,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdint>
 #include <cstdio>
 #include <mutex>
@@ -56,24 +68,36 @@ constexpr int A_HALF = HM * BK * 2;    // 16 KB
 constexpr int B_STAGE = BN * BK * 2;   // 32 KB
 constexpr int CHUNK = 128 * 32 * 4;    // one fp32 partial chunk: 128 rows x 32 columns
 constexpr uint32_t IDESC = idesc_bf16(HM, BN, false);
+constexpr uint32_t IDESC_PAIR = idesc_bf16(2 * HM, BN, false);   // M = 256 over a CTA pair
 constexpr int kMaxHalves = 2;
 constexpr int kMaxGroupedTilesM = 8;   // grouped schedule up to 8 M-tiles
 constexpr int kWideMinRows = 1024;     // from this many tokens on, tiles have two halves
+#ifndef MB_GEMM_PAIRS
+#define MB_GEMM_PAIRS 1                // 0: no CTA pairs (128- and 256-row tiles per CTA)
+#endif
 
 // Tile configurations: NH halves of 128 rows per tile.
 //  NH = 1: 128 x 256 tiles, 4 stages of 48 KB, two TMEM accumulators, so the
 //          epilogue of one tile overlaps the main loop of the next;
 //  NH = 2: 256 x 256 tiles, 3 stages of 64 KB (1.5x the MMA work per staged
 //          byte), one accumulator pair that fills TMEM.
-// Measured on GB300, NH = 1 is faster up to ~600 tokens (its double-buffered
-// epilogue and lighter split fix-up win), NH = 2 from ~2,000 tokens on (its
-// main loop runs at the MMA rate).
-template <int NH>
+//  PAIR:   256 x 256 tiles over a CTA pair (2 SMs, one pair MMA of M = 256):
+//          each CTA stages its 128 rows of A and one 128-row half of B, so
+//          a 32 KB stage feeds 512 tensor cycles on each SM (64 B/cycle, as
+//          for NH = 2) while each SM keeps two 256-column accumulators;
+//          6 stages.
+// Measured on GB300 (standalone, L2 flushed): pairs beat NH = 2 at every
+// shape from 2,048 tokens (e.g. 2,144 x 5,120 x 17,408: 484 -> 322 us) and
+// NH = 1 where their padding is no larger; at 576 tokens (768 padded rows
+// against 640) NH = 1 stays faster.
+template <int NH, bool PAIR = false>
 struct TileCfg {
-  static constexpr int BM = HM * NH;
-  static constexpr int STAGES = NH == 1 ? 4 : 3;
+  static_assert(!PAIR || NH == 1, "a pair CTA holds one 128-row half");
+  static constexpr int BM = PAIR ? 2 * HM : HM * NH;   // rows of a tile
+  static constexpr int B_STG = PAIR ? B_STAGE / 2 : B_STAGE;
+  static constexpr int STAGES = PAIR ? 6 : NH == 1 ? 4 : 3;
   static constexpr int A_STAGE = NH * A_HALF;
-  static constexpr int SMEM_TILES = STAGES * (A_STAGE + B_STAGE);
+  static constexpr int SMEM_TILES = STAGES * (A_STAGE + B_STG);
   static constexpr int SMEM_BYTES = SMEM_TILES + 1024 /*align*/ + 256 /*barriers*/;
   static constexpr int EPI_THREADS = 128 * NH;
   static constexpr int THREADS = 64 + EPI_THREADS;     // TMA, MMA, 4 epilogue warps per half
@@ -138,7 +162,10 @@ struct SegIter {
   int b, rank, mi;
   int dp_next;
   long long it, it_end, first_unit;
-  __device__ SegIter(const Params &pp) : p(pp), b(blockIdx.x) {
+  // b: this CTA's place in the schedule (a pair's two CTAs share one);
+  // slot_cta: the CTA index that owns its partial slots
+  int slot_cta;
+  __device__ SegIter(const Params &pp, int bb, int sc) : p(pp), b(bb), slot_cta(sc) {
     rank = p.grouped ? b / p.tiles_m : b;
     mi = p.grouped ? b % p.tiles_m : 0;
     dp_next = p.grouped ? p.dp_tiles : b;
@@ -165,7 +192,7 @@ struct SegIter {
     s.k0 = k0;
     s.k1 = k1;
     s.partial = !(k0 == 0 && k1 == p.k_iters);
-    s.slot = 2 * b + (u == first_unit ? 0 : 1);
+    s.slot = 2 * slot_cta + (u == first_unit ? 0 : 1);
     s.unit = u;
     it += k1 - k0;
     return true;
@@ -187,10 +214,16 @@ __device__ void unit_ranks(const Params &p, int u, int &r_first, int &r_last) {
   r_last = owner(lo + p.k_iters - 1);
 }
 
-// Partial slot that the CTA of `rank` (same M-tile) used for unit u.
-__device__ __forceinline__ int slot_of(const Params &p, int rank, int mi, int u) {
-  const int c = p.grouped ? rank * p.tiles_m + mi : rank;
-  return 2 * c + (u == static_cast<int>(rank_lo(p, rank) / p.k_iters) ? 0 : 1);
+// Schedule index of rank `rank`'s CTA (or pair) for M-tile mi.
+__device__ __forceinline__ int sched_cta(const Params &p, int rank, int mi) {
+  return p.grouped ? rank * p.tiles_m + mi : rank;
+}
+// Partial slot that the CTA of `rank` (same M-tile; for pairs the CTA of the
+// same rank in the pair, `crank`) used for unit u.
+template <bool PAIR>
+__device__ __forceinline__ int slot_of(const Params &p, int rank, int mi, int crank, int u) {
+  const int c = sched_cta(p, rank, mi);
+  return 2 * (PAIR ? 2 * c + crank : c) + (u == static_cast<int>(rank_lo(p, rank) / p.k_iters) ? 0 : 1);
 }
 
 // silu(x) = x / (1 + e^-x), with the fast exponential and reciprocal: their
@@ -249,21 +282,27 @@ __device__ __forceinline__ void store_chunk(const Params &p, int row, int col, c
   for (int q = 0; q < 4; ++q) dp[q] = make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
 }
 
-template <int EPI, int NH>
-__global__ void __launch_bounds__(TileCfg<NH>::THREADS, 1)
+// PAIR: the grid is p.grid pairs (2 p.grid CTAs, clusters of 2).  Rank 0 of
+// a pair issues the pair MMAs, owns the stage-full and accumulator-empty
+// barriers both CTAs' copies and epilogues report to; each CTA loads, drains
+// and fixes up its own 128 rows.
+template <int EPI, int NH, bool PAIR>
+__global__ void __launch_bounds__(TileCfg<NH, PAIR>::THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const Params p) {
-  using C = TileCfg<NH>;
+  using C = TileCfg<NH, PAIR>;
   constexpr int BM = C::BM, STAGES = C::STAGES, A_STAGE = C::A_STAGE, EPI_THREADS = C::EPI_THREADS;
+  constexpr int B_STG = C::B_STG;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = align1024(smem_raw);
   uint8_t *sA = smem;
   uint8_t *sB = smem + STAGES * A_STAGE;
-  uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::SMEM_TILES);
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::SMEM_TILES);   // [STAGES] (a pair: rank 0's)
   uint64_t *empty = full + STAGES;
   uint64_t *tfull = empty + STAGES;   // [NACC]
   uint64_t *tempty = tfull + C::NACC; // [NACC]
   uint64_t *fixbar = tempty + C::NACC;   // [NH], one per half
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(fixbar + 2);
+  uint64_t *fin = fixbar + 2;            // a pair: all pair MMAs done (rank 0)
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(fin + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -272,21 +311,29 @@ __global__ void __launch_bounds__(TileCfg<NH>::THREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], p.cluster);   // every CTA of the cluster releases the stage
+      // every CTA of a multicast cluster releases the stage; a pair's one MMA
+      // commit releases both CTAs' stages
+      mbar_init(&empty[s], PAIR ? 1 : p.cluster);
     }
     for (int a = 0; a < C::NACC; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], EPI_THREADS);
+      mbar_init(&tempty[a], (PAIR ? 2 : 1) * EPI_THREADS);   // a pair: both CTAs' epilogues
     }
     for (int h = 0; h < NH; ++h) mbar_init(&fixbar[h], 1);
+    mbar_init(fin, 1);
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, 512);
-    tmem_relinquish();
+    if (PAIR) {
+      tmem_alloc_pair(tmem_slot, 512);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(tmem_slot, 512);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -296,34 +343,49 @@ __global__ void __launch_bounds__(TileCfg<NH>::THREADS, 1)
   if (p.cluster > 1) cluster_sync();
   const uint32_t crank = p.cluster > 1 ? cluster_ctarank() : 0;
   const uint16_t cmask = static_cast<uint16_t>((1u << p.cluster) - 1u);
+  const int sched_b = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  // a pair's stage-full barriers live in rank 0 (cluster addresses)
+  const uint32_t full_r0 = PAIR ? mapa_shared(smem_u32(full), 0) : 0u;
+  // bytes that land for one stage (a pair: both CTAs'; a pair CTA whose rows
+  // all lie past M loads no A)
+  auto stage_bytes = [&](int m0, int nh) -> uint32_t {
+    if (PAIR) return (m0 + HM < p.M ? 2 : 1) * A_HALF + 2 * B_STG;
+    return nh * A_HALF + B_STG;
+  };
 
   // The weights are read-only for the whole stream: while earlier kernels
   // finish, arm the first stages and load their weight tiles (and warm L2
   // with the next ones); only the activation tiles wait for those kernels.
   int pre = 0;   // stages whose weight tiles are already on their way
   if (warp == 0 && lane == 0) {
-    SegIter first(p);
+    SegIter first(p, sched_b, blockIdx.x);
     Seg s0;
     if (first.next(s0)) {
-      const int nh = halves_of<NH>(p, (s0.tile % p.tiles_m) * BM);
+      const int m0f = (s0.tile % p.tiles_m) * BM;
+      const int nh = halves_of<NH>(p, m0f);
       const int nt = s0.tile / p.tiles_m;
       const int rows0 = EPI == kEpiSwiGLU ? nt * 128 : nt * BN;
       const int rows1 = EPI == kEpiSwiGLU ? p.F + nt * 128 : nt * BN + 128;
-      const bool prefetcher = p.grouped ? (blockIdx.x % p.tiles_m) == 0 : true;
+      const bool prefetcher = (p.grouped ? (sched_b % p.tiles_m) == 0 : true) && crank == 0;
       if (prefetcher)
         for (int kb = s0.k0 + STAGES; kb < s0.k1 && kb < s0.k0 + STAGES + kPrefetchAhead; ++kb) {
           tma_prefetch_2d(&tmB, kb * BK, rows0);
           tma_prefetch_2d(&tmB, kb * BK, rows1);
         }
       for (int kb = s0.k0; kb < s0.k1 && pre < STAGES; ++kb, ++pre) {
-        mbar_arrive_expect_tx(&full[pre], nh * A_HALF + B_STAGE);
+        if (PAIR) {
+          if (crank == 0) mbar_arrive_expect_tx(&full[pre], stage_bytes(m0f, nh));
+          tma_load_2d_pair(sB + pre * B_STG, &tmB, full_r0 + 8 * pre, kb * BK, crank ? rows1 : rows0);
+          continue;
+        }
+        mbar_arrive_expect_tx(&full[pre], stage_bytes(m0f, nh));
         if (p.cluster == 1) {
-          tma_load_2d(sB + pre * B_STAGE, &tmB, &full[pre], kb * BK, rows0);
-          tma_load_2d(sB + pre * B_STAGE + B_STAGE / 2, &tmB, &full[pre], kb * BK, rows1);
+          tma_load_2d(sB + pre * B_STG, &tmB, &full[pre], kb * BK, rows0);
+          tma_load_2d(sB + pre * B_STG + B_STAGE / 2, &tmB, &full[pre], kb * BK, rows1);
         } else if (crank == 0) {
-          tma_load_2d_mc(sB + pre * B_STAGE, &tmB, &full[pre], kb * BK, rows0, cmask);
+          tma_load_2d_mc(sB + pre * B_STG, &tmB, &full[pre], kb * BK, rows0, cmask);
         } else if (crank == 1) {
-          tma_load_2d_mc(sB + pre * B_STAGE + B_STAGE / 2, &tmB, &full[pre], kb * BK, rows1, cmask);
+          tma_load_2d_mc(sB + pre * B_STG + B_STAGE / 2, &tmB, &full[pre], kb * BK, rows1, cmask);
         }
       }
     }
@@ -333,7 +395,7 @@ __global__ void __launch_bounds__(TileCfg<NH>::THREADS, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------- TMA producer
-      SegIter segs(p);
+      SegIter segs(p, sched_b, blockIdx.x);
       Seg sg;
       int s = 0;
       uint32_t ph = 0;
@@ -347,7 +409,7 @@ __global__ void __launch_bounds__(TileCfg<NH>::THREADS, 1)
         const int rows0 = EPI == kEpiSwiGLU ? nt * 128 : nt * BN;
         const int rows1 = EPI == kEpiSwiGLU ? p.F + nt * 128 : nt * BN + 128;
         // one CTA per group warms L2 with the weight k-blocks ahead of the ring
-        const bool prefetcher = p.grouped ? (blockIdx.x % p.tiles_m) == 0 : true;
+        const bool prefetcher = (p.grouped ? (sched_b % p.tiles_m) == 0 : true) && crank == 0;
         if (prefetcher) {
           for (int kb = sg.k0; kb < sg.k1 && kb < sg.k0 + kPrefetchAhead; ++kb) {
             tma_prefetch_2d(&tmB, kb * BK, rows0);
@@ -364,18 +426,34 @@ __global__ void __launch_bounds__(TileCfg<NH>::THREADS, 1)
             break;
           }
           const bool b_sent = n_issued++ < pre;
-          if (!b_sent) mbar_arrive_expect_tx(&full[s], nh * A_HALF + B_STAGE);
+          if (PAIR) {
+            // rank 0 arms its barrier for both CTAs' bytes; each CTA loads its
+            // rows of A and its half of B and reports to rank 0
+            if (crank == 0 && !b_sent) mbar_arrive_expect_tx(&full[s], stage_bytes(m0, nh));
+            const uint32_t fb = full_r0 + 8 * s;
+            if (m0 + static_cast<int>(crank) * HM < p.M)
+              tma_load_2d_pair(sA + s * A_STAGE, &tmA, fb, kb * BK, m0 + crank * HM);
+            if (!b_sent) tma_load_2d_pair(sB + s * B_STG, &tmB, fb, kb * BK, crank ? rows1 : rows0);
+            issued_mask |= 1u << s;
+            issued_ph = (issued_ph & ~(1u << s)) | (ph << s);
+            if (++s == STAGES) {
+              s = 0;
+              ph ^= 1;
+            }
+            continue;
+          }
+          if (!b_sent) mbar_arrive_expect_tx(&full[s], stage_bytes(m0, nh));
           tma_load_2d(sA + s * A_STAGE, &tmA, &full[s], kb * BK, m0);
           if (nh == 2) tma_load_2d(sA + s * A_STAGE + A_HALF, &tmA, &full[s], kb * BK, m0 + HM);
           if (b_sent) {
           } else if (p.cluster == 1) {
-            tma_load_2d(sB + s * B_STAGE, &tmB, &full[s], kb * BK, rows0);
-            tma_load_2d(sB + s * B_STAGE + B_STAGE / 2, &tmB, &full[s], kb * BK, rows1);
+            tma_load_2d(sB + s * B_STG, &tmB, &full[s], kb * BK, rows0);
+            tma_load_2d(sB + s * B_STG + B_STAGE / 2, &tmB, &full[s], kb * BK, rows1);
           } else if (crank == 0) {
             // the group's M-tiles share the weight tile: one read, delivered to all
-            tma_load_2d_mc(sB + s * B_STAGE, &tmB, &full[s], kb * BK, rows0, cmask);
+            tma_load_2d_mc(sB + s * B_STG, &tmB, &full[s], kb * BK, rows0, cmask);
           } else if (crank == 1) {
-            tma_load_2d_mc(sB + s * B_STAGE + B_STAGE / 2, &tmB, &full[s], kb * BK, rows1, cmask);
+            tma_load_2d_mc(sB + s * B_STG + B_STAGE / 2, &tmB, &full[s], kb * BK, rows1, cmask);
           }
           issued_mask |= 1u << s;
           issued_ph = (issued_ph & ~(1u << s)) | (ph << s);
@@ -386,7 +464,15 @@ __global__ void __launch_bounds__(TileCfg<NH>::THREADS, 1)
         }
       }
       if (!ok) {
-        // let copies already in flight land before the CTA exits
+        // let copies already in flight land before the CTA exits (rank 1 of a
+        // pair reports its copies to rank 0's barriers, which it cannot poll:
+        // it gives them a millisecond, far beyond a copy's latency)
+        if (PAIR && crank != 0) {
+          const uint64_t t0 = globaltimer();
+          while (globaltimer() - t0 < 1000000ull) {
+          }
+          issued_mask = 0;
+        }
         for (int i = 0; i < STAGES; ++i)
           if (issued_mask & (1u << i)) {
             const uint32_t a = smem_u32(&full[i]);
@@ -399,13 +485,14 @@ __global__ void __launch_bounds__(TileCfg<NH>::THREADS, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------------------------------------------------- MMA issuer
-      SegIter segs(p);
+      // (a pair: rank 0 only; the pair MMA writes both CTAs' TMEM)
+      SegIter segs(p, sched_b, blockIdx.x);
       Seg sg;
       int s = 0;
       uint32_t ph = 0;
       int acc = 0;
       uint32_t acc_ph = 0;
-      bool ok = true;
+      bool ok = !(PAIR && crank != 0);
       while (ok && segs.next(sg)) {
         const int nh = halves_of<NH>(p, (sg.tile % p.tiles_m) * BM);
         // the epilogue has drained this accumulator buffer's previous tile
@@ -419,15 +506,21 @@ __global__ void __launch_bounds__(TileCfg<NH>::THREADS, 1)
           }
           tc_fence_after();
           const uint32_t a0 = smem_u32(sA + s * A_STAGE);
-          const uint32_t b0 = smem_u32(sB + s * B_STAGE);
+          const uint32_t b0 = smem_u32(sB + s * B_STG);
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
             const uint64_t bd = sdesc_sw128(b0 + kk * 32, 16, 1024);
             const uint32_t accum = (kb > sg.k0 || kk > 0) ? 1u : 0u;
+            if (PAIR) {
+              mma_bf16_pair(d, sdesc_sw128(a0 + kk * 32, 16, 1024), bd, IDESC_PAIR, accum);
+              continue;
+            }
             mma_bf16(d, sdesc_sw128(a0 + kk * 32, 16, 1024), bd, IDESC, accum);
             if (nh == 2) mma_bf16(d + BN, sdesc_sw128(a0 + A_HALF + kk * 32, 16, 1024), bd, IDESC, accum);
           }
-          if (p.cluster > 1)
+          if (PAIR)
+            mma_commit_pair(&empty[s], 3);
+          else if (p.cluster > 1)
             mma_commit_mc(&empty[s], cmask);
           else
             mma_commit(&empty[s]);
@@ -437,10 +530,20 @@ __global__ void __launch_bounds__(TileCfg<NH>::THREADS, 1)
           }
         }
         if (!ok) break;
-        mma_commit(&tfull[acc]);
+        if (PAIR)
+          mma_commit_pair(&tfull[acc], 3);
+        else
+          mma_commit(&tfull[acc]);
         if (++acc == C::NACC) {
           acc = 0;
           acc_ph ^= 1;
+        }
+      }
+      if (PAIR && crank == 0) {
+        // no pair MMA may still write either CTA's TMEM when they free it
+        mma_commit_pair(fin, 1);
+        const uint64_t t0 = globaltimer();
+        while (!mbar_try_wait(smem_u32(fin), 0) && globaltimer() - t0 < kWaitLimitNs) {
         }
       }
     }
@@ -452,7 +555,16 @@ __global__ void __launch_bounds__(TileCfg<NH>::THREADS, 1)
     const int h = (warp - 2) >> 2;     // half of the tile (TMEM columns h*256 ..)
     const int r = q * 32 + lane;       // row within the half
     const int ep = threadIdx.x - 64;   // 0 .. EPI_THREADS-1
-    SegIter segs(p);
+    // a drained accumulator goes back to the MMA issuer (a pair: rank 0's barrier)
+    const uint32_t tempty_r0 = PAIR ? mapa_shared(smem_u32(tempty), 0) : 0u;
+    auto release_acc = [&](int a) {
+      tc_fence_before();
+      if (PAIR && crank != 0)
+        mbar_arrive_remote(tempty_r0 + 8 * a);
+      else
+        mbar_arrive(&tempty[a]);
+    };
+    SegIter segs(p, sched_b, blockIdx.x);
     Seg sg;
     int acc = 0;
     uint32_t acc_ph = 0;
@@ -461,9 +573,10 @@ __global__ void __launch_bounds__(TileCfg<NH>::THREADS, 1)
     while (ok && segs.next(sg)) {
       const int mi = sg.tile % p.tiles_m;
       const int m0 = mi * BM;
-      const bool mine = h < halves_of<NH>(p, m0);   // this half holds rows of A
+      // this half (a pair: this CTA's 128 rows) holds rows of A
+      const bool mine = PAIR ? m0 + static_cast<int>(crank) * HM < p.M : h < halves_of<NH>(p, m0);
       const int nt = sg.tile / p.tiles_m;
-      const int row = m0 + h * HM + r;
+      const int row = m0 + (PAIR ? static_cast<int>(crank) : h) * HM + r;
       const int col0 = EPI == kEpiSwiGLU ? nt * 128 : nt * BN;
       uint4 rb[16];
       // the residual does not depend on the accumulator: fetch it while the
@@ -477,10 +590,12 @@ __global__ void __launch_bounds__(TileCfg<NH>::THREADS, 1)
       if (sg.partial) {
         int r_first, r_last;
         unit_ranks(p, sg.unit, r_first, r_last);
-        const int my_rank = p.grouped ? blockIdx.x / p.tiles_m : blockIdx.x;
+        const int my_rank = p.grouped ? sched_b / p.tiles_m : sched_b;
         // A split unit is identified by its first rank (no other split unit
-        // starts there), so flags stay below the grid size.
-        int *flag = p.tickets + (p.grouped ? r_first * p.tiles_m + mi : r_first);
+        // starts there), so flags stay below the grid size.  The CTAs of a
+        // pair fix up their own rows: one flag each.
+        const int fidx = sched_cta(p, r_first, mi);
+        int *flag = p.tickets + (PAIR ? 2 * fidx + static_cast<int>(crank) : fidx);
         if (my_rank != r_first) {
           // a later piece: hand the fp32 partial to the rank that covers the
           // unit's head (for which this unit is its last segment)
@@ -495,8 +610,7 @@ __global__ void __launch_bounds__(TileCfg<NH>::THREADS, 1)
                 w4[part_swz(i, r)] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
             }
           }
-          tc_fence_before();
-          mbar_arrive(&tempty[acc]);
+          release_acc(acc);
           __threadfence();
           named_bar_sync(1, EPI_THREADS);
           if (ep == 0) atomicAdd(flag, 1);
@@ -525,7 +639,7 @@ __global__ void __launch_bounds__(TileCfg<NH>::THREADS, 1)
             uint8_t *stage = smem + h * C::FIX_CHUNKS * CHUNK;
 #pragma unroll 1
             for (int rk = r_first + 1; rk <= r_last && ok; ++rk) {
-              const int slot = slot_of(p, rk, mi, sg.unit);
+              const int slot = slot_of<PAIR>(p, rk, mi, static_cast<int>(crank), sg.unit);
 #pragma unroll 1
               for (int rr = 0; rr < 8 / C::FIX_CHUNKS; ++rr) {
                 bool fine = true;
@@ -567,10 +681,7 @@ __global__ void __launch_bounds__(TileCfg<NH>::THREADS, 1)
             }
             finish = ok;
           }
-          if (!finish) {
-            tc_fence_before();
-            mbar_arrive(&tempty[acc]);
-          }
+          if (!finish) release_acc(acc);
         }
       }
       if (finish) {
@@ -604,8 +715,7 @@ __global__ void __launch_bounds__(TileCfg<NH>::THREADS, 1)
             }
           }
         }
-        tc_fence_before();
-        mbar_arrive(&tempty[acc]);
+        release_acc(acc);
       }
       if (++acc == C::NACC) {
         acc = 0;
@@ -616,28 +726,46 @@ __global__ void __launch_bounds__(TileCfg<NH>::THREADS, 1)
 
   __syncthreads();
   // no CTA leaves while a peer may still multicast into it or arrive on it
+  // (a pair: rank 0's MMA issuer saw its last MMA complete before this)
   if (p.cluster > 1) cluster_sync();
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    if (PAIR)
+      tmem_dealloc_pair(tmem, 512);
+    else
+      tmem_dealloc(tmem, 512);
   }
 }
 
-template <int EPI, int NH>
+template <int EPI, int NH, bool PAIR = false>
 cudaError_t launch(const CUtensorMap &tmA, const CUtensorMap &tmB, const Params &p, cudaStream_t st) {
-  using C = TileCfg<NH>;
+  using C = TileCfg<NH, PAIR>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(gemm_kernel<EPI, NH>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    attr_err = cudaFuncSetAttribute(gemm_kernel<EPI, NH, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    C::SMEM_BYTES);
   });
   if (attr_err != cudaSuccess) return attr_err;
-  return launch_pdl(gemm_kernel<EPI, NH>, dim3(p.grid), dim3(C::THREADS), C::SMEM_BYTES, st, p.cluster, tmA, tmB, p);
+  // a pair schedule's p.grid counts pairs
+  return launch_pdl(gemm_kernel<EPI, NH, PAIR>, dim3(PAIR ? 2 * p.grid : p.grid), dim3(C::THREADS), C::SMEM_BYTES,
+                    st, p.cluster, tmA, tmB, p);
 }
+
+// mode: 1 = 128-row tiles, 2 = 256-row tiles, kModePair = 256-row tiles over CTA pairs
+constexpr int kModePair = 3;
 
 cudaError_t launch_for(int epi, int nh, const CUtensorMap &tmA, const CUtensorMap &tmB, const Params &p,
                        cudaStream_t st) {
+  if (nh == kModePair) {
+    switch (epi) {
+      case kEpiStore: return launch<kEpiStore, 1, true>(tmA, tmB, p, st);
+      case kEpiResidual: return launch<kEpiResidual, 1, true>(tmA, tmB, p, st);
+      case kEpiSwiGLU: return launch<kEpiSwiGLU, 1, true>(tmA, tmB, p, st);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   if (nh == 2) {
     switch (epi) {
       case kEpiStore: return launch<kEpiStore, 2>(tmA, tmB, p, st);
@@ -656,15 +784,15 @@ cudaError_t launch_for(int epi, int nh, const CUtensorMap &tmA, const CUtensorMa
 
 // Clusters of `size` CTAs of this kernel that can be resident at once (the
 // split fix-up waits on other CTAs, so the whole grid must be co-resident).
-template <int EPI, int NH>
+template <int EPI, int NH, bool PAIR = false>
 int max_clusters(int size) {
-  using C = TileCfg<NH>;
+  using C = TileCfg<NH, PAIR>;
   static std::mutex mu;
   static int cache[9] = {0};
   std::lock_guard<std::mutex> lk(mu);
   if (size < 1 || size > 8) return 0;
   if (cache[size] == 0) {
-    cudaFuncSetAttribute(gemm_kernel<EPI, NH>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    cudaFuncSetAttribute(gemm_kernel<EPI, NH, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(size * 64);
     cfg.blockDim = dim3(C::THREADS);
@@ -677,7 +805,7 @@ int max_clusters(int size) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, gemm_kernel<EPI, NH>, &cfg) != cudaSuccess || n <= 0) n = -1;
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_kernel<EPI, NH, PAIR>, &cfg) != cudaSuccess || n <= 0) n = -1;
     cache[size] = n;
   }
   return cache[size];
@@ -688,6 +816,15 @@ int max_clusters_for(int epi, int size) {
     case kEpiStore: return max_clusters<kEpiStore, 1>(size);
     case kEpiResidual: return max_clusters<kEpiResidual, 1>(size);
     default: return max_clusters<kEpiSwiGLU, 1>(size);
+  }
+}
+
+// CTA pairs of the pair kernel that can be resident at once.
+int max_pairs_for(int epi) {
+  switch (epi) {
+    case kEpiStore: return max_clusters<kEpiStore, 1, true>(2);
+    case kEpiResidual: return max_clusters<kEpiResidual, 1, true>(2);
+    default: return max_clusters<kEpiSwiGLU, 1, true>(2);
   }
 }
 
@@ -724,16 +861,29 @@ cudaError_t gemm_run(const void *A, const void *B, const CUtensorMap *tmB_pre, v
   p.N = N;
   p.K = K;
   p.k_iters = K / BK;
-  const int nh = M >= kWideMinRows ? 2 : 1;
-  p.tiles_m = (M + nh * HM - 1) / (nh * HM);
+  const int sm_count = device_sm_count() < kMaxGemmGrid ? device_sm_count() : kMaxGemmGrid;
+  // Tile shape.  Up to 128 tokens: one 128-row tile per CTA.  From
+  // kWideMinRows tokens on: 256-row tiles over CTA pairs.  In between, pairs
+  // where they pad M no more than 128-row tiles do (M mod 256 = 0 or > 128):
+  // at 576 tokens, 768 padded rows against 640 cost more than the pairs'
+  // faster main loop saves (measured on GB300).
+  const auto round_up = [](int x, int t) { return (x + t - 1) / t * t; };
+  const bool want_pairs =
+      MB_GEMM_PAIRS && M > HM && (M >= kWideMinRows || round_up(M, 2 * HM) == round_up(M, HM));
+  const int pairs = want_pairs ? std::min(sm_count / 2, max_pairs_for(epi)) : 0;
+  const int nh = pairs > 0 ? kModePair : M >= kWideMinRows ? 2 : 1;
+  const int tile_rows = nh == 1 ? HM : 2 * HM;
+  p.tiles_m = (M + tile_rows - 1) / tile_rows;
   p.tiles_n = epi == kEpiSwiGLU ? N / 128 : (N + BN - 1) / BN;
   const int tiles = p.tiles_m * p.tiles_n;
-  const int sms = device_sm_count() < kMaxGemmGrid ? device_sm_count() : kMaxGemmGrid;
+  // schedule units: CTAs, or CTA pairs
+  const int sms = pairs > 0 ? pairs : sm_count;
+  const int base_cluster = pairs > 0 ? 2 : 1;
   if (p.tiles_m <= kMaxGroupedTilesM && p.tiles_m <= sms) {
     // Few token tiles: every weight tile is consumed by tiles_m CTAs running
     // side by side, and the (N-tile, k) space is split evenly over the groups.
     long long groups = sms / p.tiles_m;
-    p.cluster = 1;
+    p.cluster = base_cluster;
     // multicast pays for 128-row tiles (more CTAs per weight tile); with
     // 256-row tiles the cluster's lockstep costs more than it saves
     if (MB_GEMM_MULTICAST && nh == 1 && p.tiles_m > 1) {
@@ -751,12 +901,12 @@ cudaError_t gemm_run(const void *A, const void *B, const CUtensorMap *tmB_pre, v
     p.dp_tiles = 0;
     p.sk_tiles = 0;
   } else if (tiles % sms == 0) {
-    p.cluster = 1;
+    p.cluster = base_cluster;
     p.dp_tiles = tiles;
     p.sk_tiles = 0;
     p.grid = sms;
   } else {
-    p.cluster = 1;
+    p.cluster = base_cluster;
     // Whole waves run data-parallel; the last one to two waves are spread
     // along K over every SM.
     const int waves = tiles / sms;
