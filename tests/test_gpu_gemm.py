@@ -1,6 +1,7 @@
 """GPU parity of the token-batched tcgen05 GEMM (all three epilogues) against
 the oracle's float64 linear layer, over shapes that span several tiles, ragged
-M tails, stream-K splits and the layer shapes of the pages' workloads."""
+M tails, stream-K splits and the layer shapes of the pages' workloads, in both
+tile configurations (128-row tiles per CTA; 256-row tiles over CTA pairs)."""
 
 import numpy as np
 import pytest
@@ -17,11 +18,12 @@ SHAPES = [
     (1, 256, 64), (68, 768, 256), (68, 256, 1024), (129, 640, 512), (200, 1536, 512),
     (300, 512, 1536), (576, 6144, 4096), (576, 4096, 4096), (16, 7168, 5120), (1040, 5120, 5120),
     (2216, 512, 128),
-    # 256-row tiles (from 1,024 tokens on): a ragged last half, a tile with one
-    # half, split and data-parallel schedules
+    # 256-row tiles over CTA pairs (from 1,024 tokens on): last pair tiles whose
+    # second CTA has no rows (1100, 1300, 2144, 4100), grouped, split and
+    # data-parallel schedules
     (1100, 1536, 512), (1300, 768, 1024), (2144, 2560, 2048), (4100, 512, 256),
-    # 192-row tiles (385 to 1,023 tokens): a 16-row last tile, a 124-row one with a single
-    # half, six tiles with a 40-row tail
+    # pairs below 1,024 tokens (M mod 256 > 128): the second CTA of the last pair
+    # tile holds 16, 60 and 104 rows
     (400, 768, 512), (700, 1536, 1024), (1000, 512, 256),
 ]
 
