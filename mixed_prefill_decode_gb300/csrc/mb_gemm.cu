@@ -131,6 +131,10 @@ struct Params {
   float *partials;      // [2 grid][NH halves][8 chunks][128 rows][32] fp32
   int *tickets;
   int *err;
+  // First (unit, k) iteration of each rank; rlo[ranks] = all iterations.
+  // Filled on the host (fill_rank_bounds) so that no CTA divides 64-bit
+  // numbers before its first load.
+  int rlo[kMaxGemmGrid + 1];
 };
 
 // Work decomposition.  Two schedules share one iteration space of (unit, k)
@@ -149,19 +153,24 @@ struct Seg {
   int unit;     // unit index of a split piece
 };
 
-__device__ __forceinline__ long long sk_total(const Params &p) {
-  return static_cast<long long>(p.grouped ? p.tiles_n : p.sk_tiles) * p.k_iters;
-}
-__device__ __forceinline__ int sk_ranks(const Params &p) { return p.grouped ? p.n_groups : p.grid; }
-__device__ __forceinline__ long long rank_lo(const Params &p, int rank) {
-  return sk_total(p) * rank / sk_ranks(p);
+__host__ __device__ __forceinline__ int sk_ranks(const Params &p) { return p.grouped ? p.n_groups : p.grid; }
+__device__ __forceinline__ int rank_lo(const Params &p, int rank) { return p.rlo[rank]; }
+
+// Rank boundaries: rank r covers iterations [total r / R, total (r + 1) / R)
+// of the (unit, k) space.  False if the space does not fit 32-bit indices.
+bool fill_rank_bounds(Params &p) {
+  const long long total = static_cast<long long>(p.grouped ? p.tiles_n : p.sk_tiles) * p.k_iters;
+  const int R = sk_ranks(p);
+  if (total >= (1ll << 31) || R < 1 || R > kMaxGemmGrid) return false;
+  for (int r = 0; r <= R; ++r) p.rlo[r] = static_cast<int>(total * r / R);
+  return true;
 }
 
 struct SegIter {
   const Params &p;
   int b, rank, mi;
   int dp_next;
-  long long it, it_end, first_unit;
+  int it, it_end, first_unit;
   // b: this CTA's place in the schedule (a pair's two CTAs share one);
   // slot_cta: the CTA index that owns its partial slots
   int slot_cta;
@@ -185,9 +194,9 @@ struct SegIter {
       return true;
     }
     if (it >= it_end) return false;
-    const int u = static_cast<int>(it / p.k_iters);
-    const int k0 = static_cast<int>(it % p.k_iters);
-    const int k1 = static_cast<int>(min(static_cast<long long>(p.k_iters), k0 + (it_end - it)));
+    const int u = it / p.k_iters;
+    const int k0 = it - u * p.k_iters;
+    const int k1 = min(p.k_iters, k0 + (it_end - it));
     s.tile = p.grouped ? u * p.tiles_m + mi : p.dp_tiles + u;
     s.k0 = k0;
     s.k1 = k1;
@@ -201,15 +210,19 @@ struct SegIter {
 
 // Ranks whose ranges overlap unit u: [r_first, r_last].
 __device__ void unit_ranks(const Params &p, int u, int &r_first, int &r_last) {
-  const long long total = sk_total(p);
   const int R = sk_ranks(p);
-  auto owner = [&](long long x) {
-    int c = static_cast<int>((x * R) / total);
-    while (c > 0 && total * c / R > x) --c;
-    while (c + 1 < R && total * (c + 1) / R <= x) ++c;
-    return c;
+  auto owner = [&](int x) {   // the last rank whose range starts at or before x
+    int lo = 0, hi = R - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (p.rlo[mid] <= x)
+        lo = mid;
+      else
+        hi = mid - 1;
+    }
+    return lo;
   };
-  const long long lo = static_cast<long long>(u) * p.k_iters;
+  const int lo = u * p.k_iters;
   r_first = owner(lo);
   r_last = owner(lo + p.k_iters - 1);
 }
@@ -223,12 +236,15 @@ __device__ __forceinline__ int sched_cta(const Params &p, int rank, int mi) {
 template <bool PAIR>
 __device__ __forceinline__ int slot_of(const Params &p, int rank, int mi, int crank, int u) {
   const int c = sched_cta(p, rank, mi);
-  return 2 * (PAIR ? 2 * c + crank : c) + (u == static_cast<int>(rank_lo(p, rank) / p.k_iters) ? 0 : 1);
+  return 2 * (PAIR ? 2 * c + crank : c) + (u == rank_lo(p, rank) / p.k_iters ? 0 : 1);
 }
 
-// silu(x) = x / (1 + e^-x), with the fast exponential and reciprocal: their
-// relative error (~1e-6) is far below the bf16 rounding of the result.
-__device__ __forceinline__ float silu(float x) { return x * __frcp_rn(1.0f + __expf(-x)); }
+// silu(x) = x / (1 + e^-x), with the fast exponential and division (relative
+// error ~1e-6, far below the bf16 rounding of the result; for x < -87 the
+// denominator overflows and the result is 0, as it rounds to in bf16 anyway).
+// A correctly rounded reciprocal has a special-case branch per element that
+// serialises the epilogue's 4 warps (measured: ~8 us per 128 x 128 tile).
+__device__ __forceinline__ float silu(float x) { return __fdividef(x, 1.0f + __expf(-x)); }
 
 template <int NH>
 __device__ __forceinline__ float *part_chunk(const Params &p, int slot, int h, int j, int r) {
@@ -927,6 +943,7 @@ cudaError_t gemm_run(const void *A, const void *B, const CUtensorMap *tmB_pre, v
   p.partials = ws.partials;
   p.tickets = ws.tickets;
   p.err = err;
+  if (!fill_rank_bounds(p)) return cudaErrorInvalidValue;
   return launch_for(epi, nh, tmA, tmB, p, st);
 }
 
@@ -1056,6 +1073,7 @@ extern "C" mb_status mb_gemm_noalloc(const void *A, const void *B, void *D, cons
   p.partials = reinterpret_cast<float *>(base);
   p.tickets = reinterpret_cast<int *>(base + kNoAllocPartialBytes);
   p.err = reinterpret_cast<int *>(base + kNoAllocPartialBytes + kNoAllocTailBytes - 16);
+  if (!fill_rank_bounds(p)) return fail(MB_EUNSUPPORTED, "mb_gemm_noalloc: too many (tile, K step) pairs");
   e = launch_for(epilogue, 1, tmA, tmB, p, st);   // 128-row tiles: their partials fit the array
   if (e != cudaSuccess) return fail(MB_ECUDA, "mb_gemm_noalloc: launch: %s", cudaGetErrorString(e));
   return MB_OK;
