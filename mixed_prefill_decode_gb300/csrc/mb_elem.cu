@@ -32,13 +32,21 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const __nv_bfloat
   const int nv = d / 8;
   const uint4 *xr = reinterpret_cast<const uint4 *>(x + static_cast<size_t>(row) * d);
   const uint4 *gr = reinterpret_cast<const uint4 *>(g);
-  uint4 buf[kNormMaxVec];
+  uint4 buf[kNormMaxVec], gbuf[kNormMaxVec];
   float ss = 0.f;
+  // the gains are requested with the row, not after the reduction
 #pragma unroll
   for (int i = 0; i < kNormMaxVec; ++i) {
     const int v = threadIdx.x + i * kNormThreads;
     if (v < nv) {
       buf[i] = xr[v];
+      gbuf[i] = gr[v];
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < kNormMaxVec; ++i) {
+    const int v = threadIdx.x + i * kNormThreads;
+    if (v < nv) {
       const uint32_t w[4] = {buf[i].x, buf[i].y, buf[i].z, buf[i].w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
@@ -62,7 +70,7 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const __nv_bfloat
   for (int i = 0; i < kNormMaxVec; ++i) {
     const int v = threadIdx.x + i * kNormThreads;
     if (v < nv) {
-      const uint4 gv = gr[v];
+      const uint4 gv = gbuf[i];
       const uint32_t w[4] = {buf[i].x, buf[i].y, buf[i].z, buf[i].w};
       const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
       uint32_t o[4];
@@ -97,13 +105,59 @@ struct RopeParams {
   float f_hi[64], f_lo[64];
 };
 
+// Element pairs of a head row, by lane: PAIRS consecutive elements of each
+// half (bf16x2 loads and stores for hd 128, single elements for hd 64).
+template <int PAIRS>
+struct HalfVec;
+template <>
+struct HalfVec<1> {
+  using T = uint16_t;
+  static __device__ __forceinline__ void unpack(T v, float (&x)[1]) { x[0] = __uint_as_float(static_cast<uint32_t>(v) << 16); }
+  static __device__ __forceinline__ T pack(const float (&x)[1]) {
+    return static_cast<uint16_t>(__bfloat16_as_ushort(__float2bfloat16_rn(x[0])));
+  }
+};
+template <>
+struct HalfVec<2> {
+  using T = uint32_t;
+  static __device__ __forceinline__ void unpack(T v, float (&x)[2]) {
+    x[0] = bf16lo(v);
+    x[1] = bf16hi(v);
+  }
+  static __device__ __forceinline__ T pack(const float (&x)[2]) { return pack_bf16x2(x[0], x[1]); }
+};
+
 template <int HD>
 __global__ void __launch_bounds__(kRopeThreads) rope_append_kernel(const RopeParams p) {
   constexpr int HALF = HD / 2;
-  constexpr int PAIRS = HALF / 32;  // pairs per lane
+  constexpr int PAIRS = HALF / 32;          // elements of each half per lane
+  constexpr int NW = kRopeThreads / 32;
+  constexpr int MAXH = 8;                   // heads a warp holds in registers per round
+  using V = HalfVec<PAIRS>;
+  using VT = typename V::T;
   __shared__ float cs[HALF], sn[HALF];
+  __shared__ int s_page;
   pdl_wait();
   const int t = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int heads = p.Hq + 2 * p.Hkv;
+  const int row_len = heads * HD;
+  const VT *src_row = reinterpret_cast<const VT *>(p.qkv + static_cast<size_t>(t) * row_len);
+  // Every load below is independent of the position and the page, so the
+  // first round's head rows are requested before the position, the sines and
+  // the page lookup (three dependent loads) are worked out.
+  VT a1[MAXH], a2[MAXH];
+  auto load_round = [&](int base) {
+#pragma unroll
+    for (int k = 0; k < MAXH; ++k) {
+      const int hh = base + warp + k * NW;
+      if (hh < heads) {
+        a1[k] = src_row[(hh * HD) / PAIRS + lane];
+        a2[k] = src_row[(hh * HD + HALF) / PAIRS + lane];
+      }
+    }
+  };
+  load_round(0);
   const int pos = p.tok_pos[t];
   for (int i = threadIdx.x; i < HALF; i += kRopeThreads) {
     const float fp = static_cast<float>(pos);
@@ -112,71 +166,68 @@ __global__ void __launch_bounds__(kRopeThreads) rope_append_kernel(const RopePar
     const float k = rintf(hi * 0.15915494309189535f);
     float r = fmaf(-k, kTwoPiHi, hi);
     r = fmaf(-k, kTwoPiLo, r) + lo;
-    float s, c;
-    sincosf(r, &s, &c);
-    cs[i] = c;
-    sn[i] = s;
+    float sv, cv;
+    sincosf(r, &sv, &cv);
+    cs[i] = cv;
+    sn[i] = sv;
+  }
+  if (threadIdx.x == kRopeThreads - 32) {   // the last warp looks the page up
+    const int req = p.tok_req[t];
+    const int page = p.bt[p.bt_indptr[req] + pos / kPage];
+    s_page = (page < 0 || page >= p.num_pages) ? -1 : page;
   }
   __syncthreads();
-
-  const int req = p.tok_req[t];
-  int page = p.bt[p.bt_indptr[req] + pos / kPage];
-  const int slot = pos % kPage;
-  if (page < 0 || page >= p.num_pages) {
+  const int page = s_page;
+  if (page < 0) {
     if (threadIdx.x == 0) atomicExch(p.err, kErrBounds);
     return;
   }
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int heads = p.Hq + 2 * p.Hkv;
-  const int row_len = heads * HD;
-  for (int hh = warp; hh < heads; hh += kRopeThreads / 32) {
-    const __nv_bfloat16 *src = p.qkv + static_cast<size_t>(t) * row_len + hh * HD;
-    float x1[PAIRS], x2[PAIRS];
+  const int slot = pos % kPage;
+  for (int base = 0; base < heads; base += NW * MAXH) {
+    if (base > 0) load_round(base);
 #pragma unroll
-    for (int j = 0; j < PAIRS; ++j) {
-      const int i = lane * PAIRS + j;
-      x1[j] = __bfloat162float(src[i]);
-      x2[j] = __bfloat162float(src[i + HALF]);
-    }
-    const bool is_q = hh < p.Hq;
-    const bool is_k = !is_q && hh < p.Hq + p.Hkv;
-    if (is_q || is_k) {
-      if (p.qk_norm) {
-        float ss = 0.f;
+    for (int k = 0; k < MAXH; ++k) {
+      const int hh = base + warp + k * NW;
+      if (hh >= heads) break;
+      float x1[PAIRS], x2[PAIRS];
+      V::unpack(a1[k], x1);
+      V::unpack(a2[k], x2);
+      const bool is_q = hh < p.Hq;
+      const bool is_k = !is_q && hh < p.Hq + p.Hkv;
+      if (is_q || is_k) {
+        if (p.qk_norm) {
+          float ss = 0.f;
 #pragma unroll
-        for (int j = 0; j < PAIRS; ++j) ss += x1[j] * x1[j] + x2[j] * x2[j];
+          for (int j = 0; j < PAIRS; ++j) ss += x1[j] * x1[j] + x2[j] * x2[j];
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-        const float inv = rsqrtf(ss / static_cast<float>(HD) + p.eps);
-        const __nv_bfloat16 *g = is_q ? p.g_q : p.g_k;
+          for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+          const float inv = rsqrtf(ss / static_cast<float>(HD) + p.eps);
+          const __nv_bfloat16 *g = is_q ? p.g_q : p.g_k;
+#pragma unroll
+          for (int j = 0; j < PAIRS; ++j) {
+            const int i = lane * PAIRS + j;
+            x1[j] = x1[j] * inv * __bfloat162float(g[i]);
+            x2[j] = x2[j] * inv * __bfloat162float(g[i + HALF]);
+          }
+        }
 #pragma unroll
         for (int j = 0; j < PAIRS; ++j) {
           const int i = lane * PAIRS + j;
-          x1[j] = x1[j] * inv * __bfloat162float(g[i]);
-          x2[j] = x2[j] * inv * __bfloat162float(g[i + HALF]);
+          const float a = x1[j], b = x2[j];
+          x1[j] = a * cs[i] - b * sn[i];
+          x2[j] = b * cs[i] + a * sn[i];
         }
       }
-#pragma unroll
-      for (int j = 0; j < PAIRS; ++j) {
-        const int i = lane * PAIRS + j;
-        const float a = x1[j], b = x2[j];
-        x1[j] = a * cs[i] - b * sn[i];
-        x2[j] = b * cs[i] + a * sn[i];
+      VT *dst;
+      if (is_q) {
+        dst = reinterpret_cast<VT *>(p.q_out + (static_cast<size_t>(t) * p.Hq + hh) * HD);
+      } else {
+        const int kvsel = is_k ? 0 : 1;
+        const int hk = is_k ? hh - p.Hq : hh - p.Hq - p.Hkv;
+        dst = reinterpret_cast<VT *>(p.pool + (((static_cast<size_t>(page) * 2 + kvsel) * p.Hkv + hk) * kPage + slot) * HD);
       }
-    }
-    __nv_bfloat16 *dst;
-    if (is_q) {
-      dst = p.q_out + (static_cast<size_t>(t) * p.Hq + hh) * HD;
-    } else {
-      const int kvsel = is_k ? 0 : 1;
-      const int hk = is_k ? hh - p.Hq : hh - p.Hq - p.Hkv;
-      dst = p.pool + (((static_cast<size_t>(page) * 2 + kvsel) * p.Hkv + hk) * kPage + slot) * HD;
-    }
-#pragma unroll
-    for (int j = 0; j < PAIRS; ++j) {
-      const int i = lane * PAIRS + j;
-      dst[i] = __float2bfloat16_rn(x1[j]);
-      dst[i + HALF] = __float2bfloat16_rn(x2[j]);
+      dst[lane] = V::pack(x1);
+      dst[HALF / PAIRS + lane] = V::pack(x2);
     }
   }
 }

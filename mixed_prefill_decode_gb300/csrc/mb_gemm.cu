@@ -73,7 +73,10 @@ constexpr int kMaxHalves = 2;
 constexpr int kMaxGroupedTilesM = 8;   // grouped schedule up to 8 M-tiles
 constexpr int kWideMinRows = 1024;     // from this many tokens on, tiles have two halves
 #ifndef MB_GEMM_PAIRS
-#define MB_GEMM_PAIRS 1                // 0: no CTA pairs (128- and 256-row tiles per CTA)
+#define MB_GEMM_PAIRS 1                // 0: no CTA pairs (128- and 256-row tiles per CTA); 2: pairs from 129 tokens
+#endif
+#ifndef MB_GEMM_PAIR_STAGES
+#define MB_GEMM_PAIR_STAGES 6
 #endif
 
 // Tile configurations: NH halves of 128 rows per tile.
@@ -95,7 +98,7 @@ struct TileCfg {
   static_assert(!PAIR || NH == 1, "a pair CTA holds one 128-row half");
   static constexpr int BM = PAIR ? 2 * HM : HM * NH;   // rows of a tile
   static constexpr int B_STG = PAIR ? B_STAGE / 2 : B_STAGE;
-  static constexpr int STAGES = PAIR ? 6 : NH == 1 ? 4 : 3;
+  static constexpr int STAGES = PAIR ? MB_GEMM_PAIR_STAGES : NH == 1 ? 4 : 3;
   static constexpr int A_STAGE = NH * A_HALF;
   static constexpr int SMEM_TILES = STAGES * (A_STAGE + B_STG);
   static constexpr int SMEM_BYTES = SMEM_TILES + 1024 /*align*/ + 256 /*barriers*/;
@@ -383,11 +386,6 @@ __global__ void __launch_bounds__(TileCfg<NH, PAIR>::THREADS, 1)
       const int rows0 = EPI == kEpiSwiGLU ? nt * 128 : nt * BN;
       const int rows1 = EPI == kEpiSwiGLU ? p.F + nt * 128 : nt * BN + 128;
       const bool prefetcher = (p.grouped ? (sched_b % p.tiles_m) == 0 : true) && crank == 0;
-      if (prefetcher)
-        for (int kb = s0.k0 + STAGES; kb < s0.k1 && kb < s0.k0 + STAGES + kPrefetchAhead; ++kb) {
-          tma_prefetch_2d(&tmB, kb * BK, rows0);
-          tma_prefetch_2d(&tmB, kb * BK, rows1);
-        }
       for (int kb = s0.k0; kb < s0.k1 && pre < STAGES; ++kb, ++pre) {
         if (PAIR) {
           if (crank == 0) mbar_arrive_expect_tx(&full[pre], stage_bytes(m0f, nh));
@@ -404,6 +402,13 @@ __global__ void __launch_bounds__(TileCfg<NH, PAIR>::THREADS, 1)
           tma_load_2d_mc(sB + pre * B_STG + B_STAGE / 2, &tmB, &full[pre], kb * BK, rows1, cmask);
         }
       }
+      // then warm L2 with the next k-blocks (a TMA instruction costs ~90
+      // cycles to issue: the stage loads go first)
+      if (prefetcher)
+        for (int kb = s0.k0 + STAGES; kb < s0.k1 && kb < s0.k0 + STAGES + kPrefetchAhead; ++kb) {
+          tma_prefetch_2d(&tmB, kb * BK, rows0);
+          tma_prefetch_2d(&tmB, kb * BK, rows1);
+        }
     }
   }
   pdl_wait();   // A, R, D, the tickets and partials belong to earlier kernels of the stream
@@ -418,6 +423,7 @@ __global__ void __launch_bounds__(TileCfg<NH, PAIR>::THREADS, 1)
       uint32_t issued_mask = 0, issued_ph = 0;
       int n_issued = 0;   // k steps issued so far (the first `pre` have their weights in flight)
       bool ok = true;
+      bool first_seg = true;
       while (ok && segs.next(sg)) {
         const int m0 = (sg.tile % p.tiles_m) * BM;
         const int nh = halves_of<NH>(p, m0);
@@ -425,15 +431,20 @@ __global__ void __launch_bounds__(TileCfg<NH, PAIR>::THREADS, 1)
         const int rows0 = EPI == kEpiSwiGLU ? nt * 128 : nt * BN;
         const int rows1 = EPI == kEpiSwiGLU ? p.F + nt * 128 : nt * BN + 128;
         // one CTA per group warms L2 with the weight k-blocks ahead of the ring
+        // (the first segment's first STAGES + kPrefetchAhead blocks were
+        // loaded or prefetched before the grid-dependency wait)
         const bool prefetcher = (p.grouped ? (sched_b % p.tiles_m) == 0 : true) && crank == 0;
-        if (prefetcher) {
+        const bool warmed = first_seg && pre > 0;
+        const int pf_from = warmed ? sg.k0 + STAGES + kPrefetchAhead : sg.k0 + kPrefetchAhead;
+        first_seg = false;
+        if (prefetcher && !warmed) {
           for (int kb = sg.k0; kb < sg.k1 && kb < sg.k0 + kPrefetchAhead; ++kb) {
             tma_prefetch_2d(&tmB, kb * BK, rows0);
             tma_prefetch_2d(&tmB, kb * BK, rows1);
           }
         }
         for (int kb = sg.k0; kb < sg.k1; ++kb) {
-          if (prefetcher && kb + kPrefetchAhead < sg.k1) {
+          if (prefetcher && kb + kPrefetchAhead < sg.k1 && kb + kPrefetchAhead >= pf_from) {
             tma_prefetch_2d(&tmB, (kb + kPrefetchAhead) * BK, rows0);
             tma_prefetch_2d(&tmB, (kb + kPrefetchAhead) * BK, rows1);
           }
@@ -884,8 +895,8 @@ cudaError_t gemm_run(const void *A, const void *B, const CUtensorMap *tmB_pre, v
   // at 576 tokens, 768 padded rows against 640 cost more than the pairs'
   // faster main loop saves (measured on GB300).
   const auto round_up = [](int x, int t) { return (x + t - 1) / t * t; };
-  const bool want_pairs =
-      MB_GEMM_PAIRS && M > HM && (M >= kWideMinRows || round_up(M, 2 * HM) == round_up(M, HM));
+  const bool want_pairs = MB_GEMM_PAIRS && M > HM &&
+                          (MB_GEMM_PAIRS == 2 || M >= kWideMinRows || round_up(M, 2 * HM) == round_up(M, HM));
   const int pairs = want_pairs ? std::min(sm_count / 2, max_pairs_for(epi)) : 0;
   const int nh = pairs > 0 ? kModePair : M >= kWideMinRows ? 2 : 1;
   const int tile_rows = nh == 1 ? HM : 2 * HM;
@@ -900,13 +911,18 @@ cudaError_t gemm_run(const void *A, const void *B, const CUtensorMap *tmB_pre, v
     // side by side, and the (N-tile, k) space is split evenly over the groups.
     long long groups = sms / p.tiles_m;
     p.cluster = base_cluster;
-    // multicast pays for 128-row tiles (more CTAs per weight tile); with
-    // 256-row tiles the cluster's lockstep costs more than it saves
+    // Multicast pays for 128-row tiles (more CTAs per weight tile), but
+    // clusters of tiles_m CTAs fit fewer groups on the GPCs (5-CTA clusters:
+    // 28 groups = 140 CTAs against 30).  Take it where those groups split the
+    // N-tiles evenly (no stream-K fix-up; Llama-3-8B gate/up at 576 tokens:
+    // 105 against 109 us), otherwise every SM without it (down: 70 against
+    // 74 us).  With 256-row tiles the cluster's lockstep costs more than it saves.
     if (MB_GEMM_MULTICAST && nh == 1 && p.tiles_m > 1) {
       const int mc = max_clusters_for(epi, p.tiles_m);
-      if (mc > 0) {
+      const long long mc_groups = groups > mc ? mc : groups;
+      if (mc > 0 && p.tiles_n % mc_groups == 0) {
         p.cluster = p.tiles_m;
-        if (groups > mc) groups = mc;
+        groups = mc_groups;
       }
     }
     const long long iters = static_cast<long long>(p.tiles_n) * p.k_iters;
