@@ -522,7 +522,7 @@ def run_mine(args, rank: int, world: int, local: int, pg):
         stack40 = stack_step_time(mb, torch, swl, nl)
 
     # ---- P3 step-time model with GB300 peaks, as an analytic comparator
-    from oracle import step_model as SM
+    from mixed_prefill_decode_gb300 import step_model as SM
     sh = wl.shape
     n_params = sum(int(np.prod(v.shape)) for k, v in wb.items() if k.startswith("w_"))
     gb300 = SM.Machine(flops=peaks["bf16_tflops_sustained"] * 1e12, bandwidth=peaks["hbm_gbs"] * 1e9, t_iter=0.0)
@@ -575,7 +575,7 @@ def run_sweep(args):
     import torch
     from mixed_prefill_decode_gb300 import build as B
     from mixed_prefill_decode_gb300 import binding as mb
-    from oracle import step_model as SM
+    from mixed_prefill_decode_gb300 import step_model as SM
     B.build()
     peaks, _ = load_peaks()
     sh = W.LLAMA3_8B
@@ -600,6 +600,53 @@ def run_sweep(args):
             print(json.dumps(r), flush=True)
 
 
+def run_budget(args):
+    """Budget selection on GB300 (pofe.ai "Chunked prefill", "Tuning knobs"):
+    time the 32-layer Llama-3-8B-shaped stack over token budgets and decode
+    counts, fit the step-time model t = t0 + a T + b KVd + c pairs, take the
+    largest budget within each TBT target, and replay seeded load through the
+    packer on the fitted model (p99 TBT / TTFT, goodput at p99 TBT <= 50 ms and
+    TTFT <= 1 s).  One JSON line per profiled point, then the fit, the choices
+    and the load tests."""
+    import torch
+    from mixed_prefill_decode_gb300 import build as B
+    from mixed_prefill_decode_gb300 import binding as mb
+    from mixed_prefill_decode_gb300 import budget as BU
+    B.build()
+    sh = W.LLAMA3_8B
+    weights = [W.device_weights(sh, 5100 + l) for l in range(32)]
+    free_budget = torch.cuda.mem_get_info()[0] - (24 << 30)
+    batches, secs, curve = [], [], {}
+    for C in (256, 512, 1024, 2048, 4096, 8192):
+        for b in (16, 64, 256):
+            if C <= b:
+                continue
+            wl, nl = W.llama3_8b_stack(C, b)
+            r = stack_step_time(mb, torch, wl, nl, steps=5, warmup=2, share_pool_bytes=free_budget, weights=weights)
+            rows = [(i, q, c + q) for i, (c, q) in enumerate(wl.reqs)]
+            batches.append(rows)
+            secs.append(r["ms_per_step"] / 1e3)
+            if b == 64:
+                curve[C] = r["ms_per_step"] / 1e3
+            r.update({"kind": "profile", "budget": C, "decodes": b})
+            print(json.dumps(r), flush=True)
+    fit = BU.StepTimeFit.fit(batches, secs)
+    resid = [abs(fit(rw) - t) / t for rw, t in zip(batches, secs)]
+    print(json.dumps({"kind": "fit", "t0_ms": round(fit.t0 * 1e3, 4), "a_us_per_token": round(fit.a * 1e6, 5),
+                      "b_ns_per_decode_key": round(fit.b * 1e9, 5), "c_ps_per_pair": round(fit.c * 1e12, 5),
+                      "max_rel_residual": round(max(resid), 4), "points": len(secs)}), flush=True)
+    choices = {}
+    for tbt in (0.025, 0.050, 0.100):
+        choices[tbt] = BU.select_budget(curve, tbt)
+        print(json.dumps({"kind": "select", "tbt_target_ms": tbt * 1e3, "decodes": 64,
+                          "curve_ms": {str(k): round(v * 1e3, 3) for k, v in sorted(curve.items())},
+                          "budget": choices[tbt]}), flush=True)
+    for C in sorted({256, 512, 1024, 2048, 4096, 8192} | {c for c in choices.values() if c}):
+        g, pts = BU.goodput(C, [5, 10, 15, 20, 25, 30, 40, 50, 60, 80], fit, n_requests=1000, seed=7)
+        print(json.dumps({"kind": "load_test", "budget": C, "step_time": "GB300 fit", "goodput_rps": g,
+                          "points": pts}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -611,12 +658,17 @@ def main():
     ap.add_argument("--no-aux", action="store_true", help="skip the decode-only and 40-layer stack measurements")
     ap.add_argument("--sweep", action="store_true",
                     help="token-budget sweep on the 32-layer Llama-3-8B stack: one JSON line per point")
+    ap.add_argument("--budget", action="store_true",
+                    help="budget selection: profile the stack, fit the step time, choose budgets, load-test them")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
     rank, world, local, pg = dist_setup()
     if args.sweep:
         run_sweep(args)
+        return
+    if args.budget:
+        run_budget(args)
         return
     if args.impl == "reference":
         run_reference(args, rank, world)

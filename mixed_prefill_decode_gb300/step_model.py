@@ -1,7 +1,8 @@
 """Roofline step-time model of one serving iteration.
 
-TEST INFRASTRUCTURE ONLY (see the package docstring); ``bench.py`` reports it
-beside the measured step as an analytic comparator.
+Host-side analytic model: ``bench.py`` reports it beside the measured step,
+and ``budget.py`` can drive its load test with it (the page's own simulator
+ran on it).  It holds none of the layer's arithmetic.
 
 The pofe.ai "Chunked prefill" page ("The bottleneck: prefill-decode
 interference" and "What chunking costs") models an iteration of P prompt tokens
@@ -73,6 +74,23 @@ def iteration_time(machine: Machine, model: Model, chunks: Sequence[Tuple[int, i
     flops = 2 * model.n_params * tokens + 4 * model.d_model * model.n_layers * pairs
     nbytes = 2 * model.n_params + model.kappa * kv_read
     return max(flops / machine.flops, nbytes / machine.bandwidth) + machine.t_iter
+
+
+def iteration_time_pessimistic(machine: Machine, model: Model, chunks: Sequence[Tuple[int, int]],
+                               decode_ctx: Iterable[int]) -> float:
+    """The page's second model ("Simulated numbers: choosing the budget"):
+    decode attention runs after the matrix multiplies and adds its full
+    memory time instead of overlapping, i.e. the decodes' KV bytes leave the
+    max() and are added on:  max(FLOPs / F, (2 N + kappa * chunk KV) / B_W)
+    + kappa * decode KV / B_W + t_iter."""
+    decode_ctx = list(decode_ctx)
+    tokens = sum(p for p, _ in chunks) + len(decode_ctx)
+    pairs = sum(p * c + p * (p + 1) / 2 for p, c in chunks) + sum(c + 1 for c in decode_ctx)
+    kv_chunk = sum(c for _, c in chunks)
+    kv_decode = sum(c + 1 for c in decode_ctx)
+    flops = 2 * model.n_params * tokens + 4 * model.d_model * model.n_layers * pairs
+    overlapped = max(flops / machine.flops, (2 * model.n_params + model.kappa * kv_chunk) / machine.bandwidth)
+    return overlapped + model.kappa * kv_decode / machine.bandwidth + machine.t_iter
 
 
 def chunked_prompt_time(machine: Machine, model: Model, prompt: int, chunk: int) -> float:

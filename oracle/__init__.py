@@ -9,7 +9,6 @@ no code with the CUDA library; both are fed from the seeded generator in
 Modules
   layer       the layer step in float64 NumPy, KV read through the block table
   packer      the token-budget packer
-  step_model  the roofline step-time model of the pofe.ai "Chunked prefill" page
 
 Parity status (what pins each part, tests in ``tests/test_oracle_*.py``):
   attention   torch SDPA (float64, explicit mask) on gathered KV; kv = 1 gives
@@ -25,5 +24,4 @@ Parity status (what pins each part, tests in ``tests/test_oracle_*.py``):
               unpinned)
   packer      the worked example of the pofe.ai page (8 x (64 + 512) at budget
               576) and brute-force invariants
-  step_model  every number the pofe.ai page prints from its model
 """

@@ -4,7 +4,7 @@ prefill" page prints from it (tests/golden/pofe_step_model.json)."""
 import json
 import os
 
-from oracle import step_model as S
+from mixed_prefill_decode_gb300 import step_model as S
 
 G = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "pofe_step_model.json")))
 M, MOD = S.H100_CLASS, S.LLAMA_8B
