@@ -381,8 +381,9 @@ mb_status prepare_step(mb_layer *L, const mb_batch *b, int64_t T, cudaStream_t s
     const int32_t qo = b->qo_indptr[r + 1] - b->qo_indptr[r];
     if (qo > 1) {
       const int32_t c = b->kv_len[r] - qo;
-      for (int32_t i0 = 0; i0 < qo; i0 += 128)
-        for (int32_t hh = 0; hh < Hq; ++hh) tiles.push_back({r, i0, hh, static_cast<int64_t>(c + i0 + 128)});
+      // 256 query rows (two 128-row tiles) per chunk tile
+      for (int32_t i0 = 0; i0 < qo; i0 += 256)
+        for (int32_t hh = 0; hh < Hq; ++hh) tiles.push_back({r, i0, hh, static_cast<int64_t>(c + i0 + 256)});
     } else {
       dec_pages += pages_for(b->kv_len[r]);
     }

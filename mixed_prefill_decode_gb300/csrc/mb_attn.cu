@@ -42,29 +42,50 @@ template <int HD>
 __host__ __device__ constexpr int part_stride() { return HD + 4; }
 
 // ============================================================ chunk tiles
+// A chunk tile is 256 query rows of one q-head of a prefill chunk, as two
+// 128-row query tiles t = 0, 1 that share every staged block of keys and
+// values.  Keys and values come through the block table in 128-key blocks
+// (8 pages, one TMA copy per page and K or V).  Per block j and tile t:
+//
+//   S_t = Q_t K^T     tcgen05, M = 128 rows, N = 128 keys, K = hd (TMEM)
+//   softmax           four warps per tile, one thread per query row, so a
+//                     row's maximum and sum need no exchange between threads
+//   O_t += P_t V      P_t (bf16) written over S_t in TMEM is the A operand,
+//                     V the MN-major B operand straight from its stage
+//
+// The MMA issuer alternates the tiles, PV_0(j), S_0(j+1), PV_1(j), S_1(j+1),
+// so the tensor cores run one tile's products while the other tile's softmax
+// runs (the FA4-style ping-pong).  O_t accumulates in TMEM; a row is rescaled
+// only when its maximum grows by more than 2^8 over the reference it uses,
+// so probabilities stay <= 256 and most blocks never wait for the previous PV.
 template <int HD>
 struct ChunkCfg {
-  static constexpr int NH = HD / 64;              // 64-wide swizzle chunks along hd
-  static constexpr int TILE_BYTES = 128 * 128;    // [128 rows][64 bf16]
-  static constexpr int Q_BYTES = NH * TILE_BYTES;
-  static constexpr int KV_BYTES = NH * TILE_BYTES;
-  static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K = OFF_Q + Q_BYTES;
-  static constexpr int NKV = 3;                   // K/V stages
+  static constexpr int NH = HD / 64;               // 64-wide swizzle chunks along hd
+  static constexpr int TILE_BYTES = 128 * 128;     // [128 rows][64 bf16]
+  static constexpr int QT_BYTES = NH * TILE_BYTES; // one query tile
+  static constexpr int KV_BYTES = NH * TILE_BYTES; // a block of K or of V
   // A K or V stage holds 128 keys as [8-key group][hd half][8 keys][128 B]
   // (what one copy per page delivers): atoms of a half are ATOM_STRIDE apart.
   static constexpr int ATOM_STRIDE = NH * 1024;
   static constexpr int PAGE_BYTES = 2 * ATOM_STRIDE;
-  static constexpr int OFF_V = OFF_K + NKV * KV_BYTES;
-  static constexpr int OFF_BAR = OFF_V + NKV * KV_BYTES;
-  static constexpr int OFF_RED = OFF_BAR + 128;   // softmax row max / sum exchange
+  // Separate K and V rings: a K block is free once both tiles' S products
+  // are done, a V block only after both PV products, a block period later.
+  // With 3 K and 2 V stages each load gets about two block periods of lead
+  // (two query tiles take the room a third V stage would need).
+  static constexpr int NK = HD == 128 ? 3 : 4;
+  static constexpr int NV = HD == 128 ? 2 : 4;
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_K = OFF_Q + 2 * QT_BYTES;
+  static constexpr int OFF_V = OFF_K + NK * KV_BYTES;
+  static constexpr int OFF_BAR = OFF_V + NV * KV_BYTES;
   // The kernel checks that the dynamic shared memory starts 1024-aligned, so
-  // no alignment slack is reserved (it would not fit beside three stages).
-  static constexpr int SMEM = OFF_RED + 4 * 128 * 4;
-  static constexpr int THREADS = 320;             // TMA, MMA, 8 softmax warps
+  // no alignment slack is reserved.
+  static constexpr int SMEM = OFF_BAR + 256;
+  static constexpr int THREADS = 320;              // TMA, MMA, 2 x 4 softmax warps
   static constexpr uint32_t IDESC_S = idesc_bf16(128, 128, false);
   static constexpr uint32_t IDESC_PV = idesc_bf16(128, HD, true);
-  static constexpr uint32_t TMEM_COLS = 512;      // S0 [0,128), S1 [128,256), O [256, 256+HD)
+  static constexpr uint32_t TMEM_COLS = 512;       // S_0 [0,128), S_1 [128,256), O_0, O_1 from 256
+  static constexpr uint32_t O_COL = 256;
 };
 
 struct ChunkParams {
@@ -75,7 +96,7 @@ struct ChunkParams {
   int *err;
 };
 
-// One prefill-chunk tile (128 query rows x one q-head); needs
+// One chunk tile (up to 256 query rows x one q-head); needs
 // ChunkCfg<HD>::THREADS threads and ChunkCfg<HD>::SMEM bytes of shared memory.
 template <int HD>
 __device__ __forceinline__ void chunk_tile(const CUtensorMap &tmQ, const CUtensorMap &tmKV, const ChunkParams &p,
@@ -87,14 +108,17 @@ __device__ __forceinline__ void chunk_tile(const CUtensorMap &tmQ, const CUtenso
   uint8_t *sV = smem + C::OFF_V;
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
   uint64_t *q_full = bars + 0;
-  uint64_t *kv_full = bars + 1;   // [NKV]
-  uint64_t *kv_empty = bars + 4;  // [NKV]
-  uint64_t *s_full = bars + 7;    // [2]
-  uint64_t *p_full = bars + 9;    // [2]
-  uint64_t *o_full = bars + 11;   // PV(j) done, j < n_kb - 1
-  uint64_t *o_last = bars + 12;   // every MMA of the tile done (committed once)
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 13);
+  uint64_t *k_full = bars + 1;             // [NK]
+  uint64_t *k_empty = k_full + C::NK;      // [NK]
+  uint64_t *v_full = k_empty + C::NK;      // [NV]
+  uint64_t *v_empty = v_full + C::NV;      // [NV]
+  uint64_t *s_full = v_empty + C::NV;      // [2 tiles]
+  uint64_t *p_full = s_full + 2;           // [2 tiles]
+  uint64_t *o_full = p_full + 2;           // [2 tiles]: PV_t(j) done, j < n_kb_t - 1
+  uint64_t *o_last = o_full + 2;           // every MMA of the tile done (committed once)
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(o_last + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  static_assert((1 + 2 * C::NK + 2 * C::NV + 7) * 8 + 8 <= 256, "barrier area");
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -106,23 +130,34 @@ __device__ __forceinline__ void chunk_tile(const CUtensorMap &tmQ, const CUtenso
   const int qo = p.qo_indptr[req + 1] - t0;
   const int kv = p.kv_len[req];
   const int cached = kv - qo;
-  const int rows_valid = min(128, qo - i0);
+  const int rows_valid = min(256, qo - i0);
   const int last_pos = cached + i0 + rows_valid - 1;
   const int n_kb = (last_pos + 1 + 127) / 128;
+  // blocks each query tile needs (0: the tile has no rows)
+  int nkb_t[2];
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const int rows = min(128, rows_valid - 128 * t);
+    nkb_t[t] = rows > 0 ? (cached + i0 + 128 * t + rows - 1 + 1 + 127) / 128 : 0;
+  }
   const int hk = h / (p.Hq / p.Hkv);
   const int32_t *table = p.bt + p.bt_indptr[req];
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int s = 0; s < C::NKV; ++s) {
-      mbar_init(&kv_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
+    for (int s = 0; s < C::NK; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
     }
-    mbar_init(&s_full[0], 1);
-    mbar_init(&s_full[1], 1);
-    mbar_init(&p_full[0], 256);
-    mbar_init(&p_full[1], 256);
-    mbar_init(o_full, 1);
+    for (int s = 0; s < C::NV; ++s) {
+      mbar_init(&v_full[s], 1);
+      mbar_init(&v_empty[s], 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&s_full[t], 1);
+      mbar_init(&p_full[t], 128);
+      mbar_init(&o_full[t], 1);
+    }
     mbar_init(o_last, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -141,71 +176,83 @@ __device__ __forceinline__ void chunk_tile(const CUtensorMap &tmQ, const CUtenso
 
   if (warp == 0) {
     // -------------------------------------------------------- TMA producer
-    // Lane 0 waits and arms each stage; the block's 8 pages x (K, V) x hd
-    // chunks then go out as one TMA per lane (one thread issuing all of them
-    // would pace the ring at ~90 cycles a copy).  Page ids: one per lane,
-    // loaded a block ahead.
-    // one copy per (page, K or V): 16 per block, lanes 0-15
-    const int my_pg = lane >> 1, my_kv = lane & 1;
+    // Lane 0 waits and arms each stage; the block's 8 pages go out as one
+    // TMA per lane (one thread issuing them all would pace the rings at ~90
+    // cycles a copy).  K runs NK - NV blocks ahead of V, the order in which
+    // their slots free up.  Page ids: one per lane, loaded a block ahead.
     if (lane == 0) {
-      mbar_arrive_expect_tx(q_full, C::Q_BYTES);
-      for (int c = 0; c < C::NH; ++c) tma_load_2d(sQ + c * C::TILE_BYTES, &tmQ, q_full, h * HD + c * 64, t0 + i0);
+      const int nq = nkb_t[1] > 0 ? 2 : 1;
+      mbar_arrive_expect_tx(q_full, nq * C::QT_BYTES);
+      for (int t = 0; t < nq; ++t)
+        for (int c = 0; c < C::NH; ++c)
+          tma_load_2d(sQ + t * C::QT_BYTES + c * C::TILE_BYTES, &tmQ, q_full, h * HD + c * 64, t0 + i0 + 128 * t);
     }
-    uint32_t issued = 0, issued_ph = 0;
-    bool ok = true;
+    constexpr int AHEAD = C::NK - C::NV;
     const int n_pages = (last_pos + 1 + 15) / 16;
-    int nxt = lane < 8 && lane < n_pages ? table[lane] : 0;
-    for (int j = 0; j < n_kb && ok; ++j) {
-      const int s = j % C::NKV;
-      const uint32_t ph = (j / C::NKV) & 1;
-      const int cur = nxt;
-      if (j + 1 < n_kb) nxt = lane < 8 && 8 * (j + 1) + lane < n_pages ? table[8 * (j + 1) + lane] : 0;
-      const int key0 = 128 * j;
-      const int key_end = min(key0 + 128, last_pos + 1);
-      const int np = (key_end - key0 + 15) / 16;
+    auto page_of = [&](int blk) { return lane < 8 && 8 * blk + lane < n_pages ? table[8 * blk + lane] : 0; };
+    // one ring: wait for the slot, arm it, 8 copies (lanes 0-7)
+    auto load_block = [&](bool is_v, int blk, int pg) -> bool {
+      const int ns = is_v ? C::NV : C::NK;
+      const int st = blk % ns;
+      uint64_t *full = (is_v ? v_full : k_full) + st;
+      uint64_t *empty = (is_v ? v_empty : k_empty) + st;
+      const int key0 = 128 * blk;
+      const int np = (min(key0 + 128, last_pos + 1) - key0 + 15) / 16;
+      bool ok = true;
       if (lane == 0) {
-        ok = mbar_wait(&kv_empty[s], ph ^ 1, abort_flag, p.err, kErrWaitProducer);
-        if (ok) mbar_arrive_expect_tx(&kv_full[s], np * 2 * C::NH * 2048);
+        ok = mbar_wait(empty, ((blk / ns) & 1) ^ 1, abort_flag, p.err, kErrWaitProducer);
+        if (ok) mbar_arrive_expect_tx(full, np * C::NH * 2048);
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
-      int page = __shfl_sync(0xffffffffu, cur, my_pg & 7);
-      if (lane < 16 && my_pg < np) {
-        if (page < 0 || page >= p.num_pages) {
+      if (!ok) return false;
+      if (lane < np) {
+        if (pg < 0 || pg >= p.num_pages) {
           atomicExch(p.err, kErrBounds);
-          page = 0;
+          pg = 0;
         }
-        const int z = (page * 2 + my_kv) * p.Hkv + hk;
-        uint8_t *dst = (my_kv ? sV : sK) + s * C::KV_BYTES + my_pg * C::PAGE_BYTES;
-        tma_load_5d(dst, &tmKV, &kv_full[s], 0, 0, 0, 0, z);
+        const int z = (pg * 2 + (is_v ? 1 : 0)) * p.Hkv + hk;
+        tma_load_5d((is_v ? sV : sK) + st * C::KV_BYTES + lane * C::PAGE_BYTES, &tmKV, full, 0, 0, 0, 0, z);
       }
-      issued |= 1u << s;
-      issued_ph = (issued_ph & ~(1u << s)) | (ph << s);
+      return true;
+    };
+    bool ok = true;
+    // each ring keeps its own page ids for its current and next block
+    int pk = page_of(0), pk_next = page_of(1), pv = pk, pv_next = pk_next;
+    int kb = 0, vb = 0;   // next K and V block to load
+    while (ok && vb < n_kb) {
+      if (kb < n_kb && kb <= vb + AHEAD) {
+        ok = load_block(false, kb, pk);
+        ++kb;
+        pk = pk_next;
+        pk_next = page_of(kb + 1);
+      } else {
+        ok = load_block(true, vb, pv);
+        ++vb;
+        pv = pv_next;
+        pv_next = page_of(vb + 1);
+      }
     }
     if (lane == 0) {
+      // let copies in flight land before the CTA exits (bounded), and the Q load
+      const uint64_t t_start = globaltimer();
       if (!ok) {
-        for (int s = 0; s < C::NKV; ++s)
-          if (issued & (1u << s)) {
-            const uint64_t t_start = globaltimer();
-            while (!mbar_try_wait(smem_u32(&kv_full[s]), (issued_ph >> s) & 1u) &&
-                   globaltimer() - t_start < kWaitLimitNs) {
-            }
+        for (int b = max(0, kb - C::NK); b < kb; ++b)
+          while (!mbar_try_wait(smem_u32(&k_full[b % C::NK]), (b / C::NK) & 1) && globaltimer() - t_start < kWaitLimitNs) {
+          }
+        for (int b = max(0, vb - C::NV); b < vb; ++b)
+          while (!mbar_try_wait(smem_u32(&v_full[b % C::NV]), (b / C::NV) & 1) && globaltimer() - t_start < kWaitLimitNs) {
           }
       }
-      // the Q load is always in flight once issued; make sure it landed
-      const uint64_t t_start = globaltimer();
       while (!mbar_try_wait(smem_u32(q_full), 0) && globaltimer() - t_start < kWaitLimitNs) {
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
       // ------------------------------------------------------- MMA issuer
-      auto issue_s = [&](int j) {
-        const int b = j & 1;                 // S buffer in TMEM
-        const int s = j % C::NKV;            // K/V stage
-        const uint32_t d = tmem + b * 128;
-        const uint32_t q0 = smem_u32(sQ);
-        const uint32_t k0 = smem_u32(sK + s * C::KV_BYTES);
+      auto issue_s = [&](int t, int j) {
+        const uint32_t d = tmem + 128 * t;
+        const uint32_t q0 = smem_u32(sQ + t * C::QT_BYTES);
+        const uint32_t k0 = smem_u32(sK + (j % C::NK) * C::KV_BYTES);
 #pragma unroll
         for (int c = 0; c < C::NH; ++c)
 #pragma unroll
@@ -214,64 +261,49 @@ __device__ __forceinline__ void chunk_tile(const CUtensorMap &tmQ, const CUtenso
             const uint64_t bd = sdesc_sw128(k0 + c * 1024 + kk * 32, 16, C::ATOM_STRIDE);
             mma_bf16(d, ad, bd, C::IDESC_S, (c > 0 || kk > 0) ? 1u : 0u);
           }
-        mma_commit(&s_full[b]);
+        mma_commit(&s_full[t]);
       };
-      auto issue_pv = [&](int j) {
-        const int b = j & 1;
-        const int s = j % C::NKV;
-        const uint32_t vbase = smem_u32(sV + s * C::KV_BYTES);
-        // P(j) sits in TMEM over S(j): 128 keys as 64 columns of bf16 pairs
-        const uint32_t pcol = tmem + b * 128;
+      auto issue_pv = [&](int t, int j) {
+        const uint32_t vbase = smem_u32(sV + (j % C::NV) * C::KV_BYTES);
+        // P_t(j) sits in TMEM over S_t(j): 128 keys as 64 columns of bf16 pairs
+        const uint32_t pcol = tmem + 128 * t;
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {  // 16 keys (two atoms) per MMA; hd halves 1 KB apart
           const uint64_t bd = sdesc_sw128(vbase + ks * 2 * C::ATOM_STRIDE, 1024, C::ATOM_STRIDE);
-          mma_bf16_ts(tmem + 256, pcol + ks * 8, bd, C::IDESC_PV, (j > 0 || ks > 0) ? 1u : 0u);
+          mma_bf16_ts(tmem + C::O_COL + HD * t, pcol + ks * 8, bd, C::IDESC_PV, (j > 0 || ks > 0) ? 1u : 0u);
         }
-        // the last PV is covered by the o_last commit after the loop; stages
-        // the producer will not refill get no release (nothing waits on it)
-        if (j + 1 < n_kb) mma_commit(o_full);
-        if (j + C::NKV < n_kb) mma_commit(&kv_empty[s]);
+        // the last PV of a tile is covered by the o_last commit after the loop
+        if (j + 1 < nkb_t[t]) mma_commit(&o_full[t]);
       };
-      bool ok = mbar_wait(q_full, 0, abort_flag, p.err, kErrWaitMma);
-      if (ok) ok = mbar_wait(&kv_full[0], 0, abort_flag, p.err, kErrWaitMma);
+      auto wait = [&](uint64_t *bar, uint32_t par) { return mbar_wait(bar, par, abort_flag, p.err, kErrWaitMma); };
+      // the last tile that reads block j (tile 1 reads every block it needs,
+      // and needs at least the blocks of tile 0 when it has rows)
+      auto last_tile = [&](int j) { return j < nkb_t[1] ? 1 : 0; };
+      bool ok = wait(q_full, 0) && wait(&k_full[0], 0);
       if (ok) {
         tc_fence_after();
-        issue_s(0);
+        for (int t = 0; t < 2; ++t)
+          if (nkb_t[t] > 0) issue_s(t, 0);
+        if (C::NK < n_kb) mma_commit(&k_empty[0]);
       }
-      // Block j: S(j+1) as soon as its K/V landed, PV(j) as soon as P(j) is
-      // ready, in whichever order they come (neither waits on the other).
+      // Block j: PV_0(j), S_0(j+1), PV_1(j), S_1(j+1); a tile that needs no
+      // more blocks drops out.  A K block is released after the last S that
+      // reads it, a V block after the last PV.
       for (int j = 0; j < n_kb && ok; ++j) {
-        bool s_done = j + 1 >= n_kb, pv_done = false;
-        const uint32_t kv_bar = smem_u32(&kv_full[(j + 1) % C::NKV]);
-        const uint32_t kv_par = ((j + 1) / C::NKV) & 1;
-        const uint32_t p_bar = smem_u32(&p_full[j & 1]);
-        const uint32_t p_par = (j >> 1) & 1;
-        const uint64_t t_start = globaltimer();
-        for (uint32_t spin = 0; !(s_done && pv_done); ++spin) {
-          bool progress = false;
-          if (!s_done && mbar_test_wait(kv_bar, kv_par)) {
+        ok = wait(&v_full[j % C::NV], (j / C::NV) & 1);
+        for (int t = 0; t < 2 && ok; ++t) {
+          if (j >= nkb_t[t]) continue;
+          ok = wait(&p_full[t], j & 1);
+          if (!ok) break;
+          tc_fence_after();
+          issue_pv(t, j);
+          if (t == last_tile(j) && j + C::NV < n_kb) mma_commit(&v_empty[j % C::NV]);
+          if (j + 1 < nkb_t[t]) {
+            ok = wait(&k_full[(j + 1) % C::NK], ((j + 1) / C::NK) & 1);
+            if (!ok) break;
             tc_fence_after();
-            issue_s(j + 1);
-            s_done = progress = true;
-          }
-          if (!pv_done && mbar_test_wait(p_bar, p_par)) {
-            tc_fence_after();
-            issue_pv(j);
-            pv_done = progress = true;
-          }
-          // back off: this thread shares a scheduler with a softmax warp
-          if (!progress) __nanosleep(64);
-          if ((spin & 63u) == 63u) {
-            if (*abort_flag) {
-              ok = false;
-              break;
-            }
-            if (globaltimer() - t_start > kWaitLimitNs) {
-              *abort_flag = 1;
-              atomicExch(p.err, kErrWaitMma);
-              ok = false;
-              break;
-            }
+            issue_s(t, j + 1);
+            if (t == last_tile(j + 1) && j + 1 + C::NK < n_kb) mma_commit(&k_empty[(j + 1) % C::NK]);
           }
         }
       }
@@ -284,121 +316,151 @@ __device__ __forceinline__ void chunk_tile(const CUtensorMap &tmQ, const CUtenso
     }
   } else {
     // ------------------------------------------------- softmax / epilogue
-    // 8 warps: two per TMEM lane quarter, splitting the 128 key columns of S
-    // (and the hd columns of O) in halves; a row's max and sum are combined
-    // through shared memory once per key block.  O accumulates in TMEM (the
-    // PV MMA adds each block); a row is rescaled only when its maximum grows
-    // by more than 2^8 over the reference it uses, so probabilities stay
-    // <= 256 and most blocks never wait for the previous PV.
-    const int q = warp & 3;
-    const int hh = (warp - 2) >> 2;          // column half
-    const int r = q * 32 + lane;
-    const int q_pos = cached + i0 + r;
+    const int t = (warp - 2) >> 2;          // query tile of this warp group
+    const int q = warp & 3;                 // TMEM lane quarter
+    const int r = q * 32 + lane;            // row within the tile
+    const int i = i0 + 128 * t + r;         // row within the chunk
+    const int q_pos = cached + i;
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
-    constexpr int OH = HD / 2;               // O columns per half
+    const uint32_t s_col = tmem + lane_base + 128 * t;
+    const uint32_t o_col = tmem + lane_base + C::O_COL + HD * t;
     constexpr float kRescaleAbove = 8.f;     // log2 units
-    float *red = reinterpret_cast<float *>(smem + C::OFF_RED);  // [2 bufs][2 halves][128]
+    const float scale = p.scale_log2;
+    const int zero_t = nkb_t[0] == n_kb ? 0 : 1;   // the tile whose WG zeroes stale V rows
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
-    bool bad = false;
-    for (int j = 0; j < n_kb; ++j) {
-      const int b = j & 1;
-      bad = !ok || !mbar_wait(&s_full[b], (j >> 1) & 1, abort_flag, p.err, kErrWaitSoftmax);
+    for (int j = 0; j < nkb_t[t]; ++j) {
+      bool bad = !ok || !mbar_wait(&s_full[t], j & 1, abort_flag, p.err, kErrWaitSoftmax);
       bad = __any_sync(0xffffffffu, bad);   // tcgen05.ld below is warp-collective
-      tc_fence_after();
-      const int key0 = 128 * j + hh * 64;   // first key of this thread's half
-      const bool full = (key0 + 63 <= q_pos) && (key0 + 63 < kv);
-      const uint32_t scol = tmem + lane_base + b * 128 + hh * 64;
-      // pass 1: this half row of S into registers, and its visible maximum
-      float sv[64];
-      float mx = -INFINITY;
-      if (!bad) {
-        tmem_ld64(scol, sv);
-#pragma unroll
-        for (int i = 0; i < 64; ++i) {
-          sv[i] *= p.scale_log2;
-          if (!full) {
-            const int key = key0 + i;
-            if (!(key <= q_pos && key < kv)) sv[i] = -INFINITY;
-          }
-          mx = fmaxf(mx, sv[i]);
-        }
-      }
-      red[(b * 2 + hh) * 128 + r] = mx;
-      // every thread is past its reads of S(j) here, so P(j) may overwrite it
-      if (named_bar_or(2, 256, bad)) {
+      if (bad) {
         ok = false;
         break;
       }
-      mx = fmaxf(mx, red[(b * 2 + (hh ^ 1)) * 128 + r]);
+      tc_fence_after();
+      const int key0 = 128 * j;
+      const bool full = key0 + 127 <= q_pos;   // every key of the block is visible to this row
+      const int vis = q_pos - key0;            // else keys key0 .. key0 + vis are (vis < 127)
+      // pass 1: the row's largest visible logit (raw; the scale is positive).
+      // The upper 64 keys are read twice (here and in pass 2) so that only
+      // 64 logits live in registers at a time.
+      float sa[64];
+      float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
+      {
+        float sb[64];
+        tmem_ld64(s_col + 64, sb);
+        if (!full)
+#pragma unroll
+          for (int c = 0; c < 64; ++c)
+            if (c + 64 > vis) sb[c] = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 64; c += 4) {
+          m0 = fmaxf(m0, sb[c]);
+          m1 = fmaxf(m1, sb[c + 1]);
+          m2 = fmaxf(m2, sb[c + 2]);
+          m3 = fmaxf(m3, sb[c + 3]);
+        }
+      }
+      tmem_ld64(s_col, sa);
+      if (!full)
+#pragma unroll
+        for (int c = 0; c < 64; ++c)
+          if (c > vis) sa[c] = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 64; c += 4) {
+        m0 = fmaxf(m0, sa[c]);
+        m1 = fmaxf(m1, sa[c + 1]);
+        m2 = fmaxf(m2, sa[c + 2]);
+        m3 = fmaxf(m3, sa[c + 3]);
+      }
+      const float mx = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3)) * scale;
       const bool grow = (m_ref == -INFINITY) || (mx > m_ref + kRescaleAbove);
       if (j > 0 && __any_sync(0xffffffffu, grow)) {
-        // O holds blocks < j relative to m_ref: finish PV(j-1), then rescale
-        bad = !mbar_wait(o_full, (j - 1) & 1, abort_flag, p.err, kErrWaitSoftmax);
+        // O_t holds blocks < j relative to m_ref: finish PV_t(j-1), then rescale
+        bad = !mbar_wait(&o_full[t], (j - 1) & 1, abort_flag, p.err, kErrWaitSoftmax);
         bad = __any_sync(0xffffffffu, bad);
         if (bad) {
           ok = false;
-          continue;
+          break;
         }
         tc_fence_after();
-        const float alpha = grow ? exp2f(m_ref - mx) : 1.f;
+        const float alpha = grow ? ex2_approx(m_ref - mx) : 1.f;
 #pragma unroll
-        for (int cc = 0; cc < OH / 32; ++cc) {
+        for (int cc = 0; cc < HD / 32; ++cc) {
           float v[32];
-          tmem_ld32(tmem + lane_base + 256 + hh * OH + cc * 32, v);
+          tmem_ld32(o_col + cc * 32, v);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] *= alpha;
-          tmem_st32(tmem + lane_base + 256 + hh * OH + cc * 32, v);
+          for (int k = 0; k < 32; ++k) v[k] *= alpha;
+          tmem_st32(o_col + cc * 32, v);
         }
         if (grow) l *= alpha;
       }
       if (grow) m_ref = mx;
-      // pass 2: probabilities relative to m_ref -> bf16 pairs into TMEM over S(j)
+      // pass 2: probabilities relative to m_ref -> bf16 pairs into TMEM over S_t
       float pk[32];
 #pragma unroll
-      for (int i = 0; i < 64; i += 2) {
-        const float p0 = exp2f(sv[i] - m_ref);
-        const float p1 = exp2f(sv[i + 1] - m_ref);
+      for (int c = 0; c < 64; c += 2) {
+        const float p0 = ex2_approx(fmaf(sa[c], scale, -m_ref));
+        const float p1 = ex2_approx(fmaf(sa[c + 1], scale, -m_ref));
         l += p0 + p1;
-        pk[i / 2] = __uint_as_float(pack_bf16x2(p0, p1));
+        pk[c / 2] = __uint_as_float(pack_bf16x2(p0, p1));
       }
-      tmem_st32(tmem + lane_base + b * 128 + hh * 32, pk);
-      if (j == n_kb - 1 && 128 * j + r > last_pos) {
-        // rows past the last visible key may hold stale or non-finite data:
-        // zero them so that P = 0 rows contribute exactly nothing
-        uint8_t *vrow = sV + (j % C::NKV) * C::KV_BYTES + (r >> 3) * C::ATOM_STRIDE + (r & 7) * 128;
+      tmem_st32(s_col, pk);   // columns 0-31: the upper logits (64-127) are still intact
+      {
+        float sb[64];
+        tmem_ld64(s_col + 64, sb);
+        if (!full)
+#pragma unroll
+          for (int c = 0; c < 64; ++c)
+            if (c + 64 > vis) sb[c] = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 64; c += 2) {
+          const float p0 = ex2_approx(fmaf(sb[c], scale, -m_ref));
+          const float p1 = ex2_approx(fmaf(sb[c + 1], scale, -m_ref));
+          l += p0 + p1;
+          pk[c / 2] = __uint_as_float(pack_bf16x2(p0, p1));
+        }
+      }
+      tmem_st32(s_col + 32, pk);
+      if (j == n_kb - 1 && t == zero_t) {
+        // the block's V copies must have landed before they are patched
+        bad = !mbar_wait(&v_full[j % C::NV], (j / C::NV) & 1, abort_flag, p.err, kErrWaitSoftmax);
+        if (__any_sync(0xffffffffu, bad)) {
+          ok = false;
+          break;
+        }
+      }
+      if (j == n_kb - 1 && t == zero_t && key0 + r > last_pos) {
+        // keys past the tile's last position may be stale or non-finite in the
+        // stage: zero their V rows so that P = 0 contributes exactly nothing.
+        // One warp group does it (tile 0 if it reads this block), before its
+        // P is ready; the other tile's PV is issued after this one's.
+        uint8_t *vrow = sV + (j % C::NV) * C::KV_BYTES + (r >> 3) * C::ATOM_STRIDE + (r & 7) * 128;
 #pragma unroll
         for (int c = 0; c < C::NH; ++c)
-          if ((c & 1) == hh)
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
-              *reinterpret_cast<uint4 *>(vrow + c * 1024 + k * 16) = make_uint4(0, 0, 0, 0);
+          for (int k = 0; k < 8; ++k)
+            *reinterpret_cast<uint4 *>(vrow + c * 1024 + k * 16) = make_uint4(0, 0, 0, 0);
         fence_proxy_async_smem();
       }
       tc_fence_before();
-      mbar_arrive(&p_full[b]);
+      mbar_arrive(&p_full[t]);
     }
-    // row sum over both halves (reuses the exchange buffer of the parity the
-    // last block did not use, so no reader of the last maxima is overtaken)
-    float *lsum = red + (((n_kb - 1) & 1) ^ 1) * 256;
-    lsum[hh * 128 + r] = l;
-    named_bar_sync(2, 256);
-    l += lsum[(hh ^ 1) * 128 + r];
-    if (ok && mbar_wait(o_last, 0, abort_flag, p.err, kErrWaitSoftmax) && !*abort_flag) {
+    if (nkb_t[t] > 0 && ok && mbar_wait(o_last, 0, abort_flag, p.err, kErrWaitSoftmax) && !*abort_flag) {
       tc_fence_after();
-      float o_acc[OH];
+      const bool valid = i < qo;
+      const float inv = 1.f / l;
+      uint4 *dst = reinterpret_cast<uint4 *>(p.o + static_cast<size_t>(t0 + i) * (p.Hq * HD) + h * HD);
 #pragma unroll
-      for (int cc = 0; cc < OH / 32; ++cc)
-        tmem_ld32(tmem + lane_base + 256 + hh * OH + cc * 32, *reinterpret_cast<float(*)[32]>(&o_acc[cc * 32]));
-      if (i0 + r < qo) {
-        const float inv = 1.f / l;
-        uint4 *dst = reinterpret_cast<uint4 *>(p.o + static_cast<size_t>(t0 + i0 + r) * (p.Hq * HD) + h * HD + hh * OH);
+      for (int cc = 0; cc < HD / 32; ++cc) {
+        float v[32];
+        tmem_ld32(o_col + cc * 32, v);
+        if (valid)
 #pragma unroll
-        for (int v8 = 0; v8 < OH / 8; ++v8)
-          dst[v8] = make_uint4(pack_bf16x2(o_acc[8 * v8] * inv, o_acc[8 * v8 + 1] * inv),
-                               pack_bf16x2(o_acc[8 * v8 + 2] * inv, o_acc[8 * v8 + 3] * inv),
-                               pack_bf16x2(o_acc[8 * v8 + 4] * inv, o_acc[8 * v8 + 5] * inv),
-                               pack_bf16x2(o_acc[8 * v8 + 6] * inv, o_acc[8 * v8 + 7] * inv));
+          for (int v8 = 0; v8 < 4; ++v8)
+            dst[cc * 4 + v8] = make_uint4(pack_bf16x2(v[8 * v8] * inv, v[8 * v8 + 1] * inv),
+                                          pack_bf16x2(v[8 * v8 + 2] * inv, v[8 * v8 + 3] * inv),
+                                          pack_bf16x2(v[8 * v8 + 4] * inv, v[8 * v8 + 5] * inv),
+                                          pack_bf16x2(v[8 * v8 + 6] * inv, v[8 * v8 + 7] * inv));
       }
     }
     tc_fence_before();

@@ -237,6 +237,14 @@ __device__ __forceinline__ void mma_commit_mc(uint64_t *bar, uint16_t mask) {
       : "memory");
 }
 
+// 2^x on the special-function unit (PTX ex2.approx.ftz.f32: relative error
+// ~2^-22, results below 2^-126 flushed to 0).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // ------------------------------------------------------- CTA pairs (2 SMs)
 // A cluster of two CTAs (ranks 0 and 1, on the two SMs of a TPC) can run one
 // MMA over both SMs: rank 0 issues it, A's M = 256 rows are 128 in each CTA's
