@@ -641,10 +641,19 @@ def run_budget(args):
         print(json.dumps({"kind": "select", "tbt_target_ms": tbt * 1e3, "decodes": 64,
                           "curve_ms": {str(k): round(v * 1e3, 3) for k, v in sorted(curve.items())},
                           "budget": choices[tbt]}), flush=True)
+    rates = [5, 10, 15, 20, 25, 30, 40, 50, 60, 80]
     for C in sorted({256, 512, 1024, 2048, 4096, 8192} | {c for c in choices.values() if c}):
-        g, pts = BU.goodput(C, [5, 10, 15, 20, 25, 30, 40, 50, 60, 80], fit, n_requests=1000, seed=7)
+        g, pts = BU.goodput(C, rates, fit, n_requests=1000, seed=7)
         print(json.dumps({"kind": "load_test", "budget": C, "step_time": "GB300 fit", "goodput_rps": g,
                           "points": pts}), flush=True)
+    # the chosen budget with a fixed per-request cap (head-of-line blocking)
+    # and with the adaptive per-step chunk size (min 128, base 512, max 4,096,
+    # pressure 16: the llm-stack-book defaults)
+    C50 = choices.get(0.050) or 2048
+    for label, kw in (("chunk_cap 512", {"chunk_cap": 512}), ("adaptive 128/512/4096/16", {"adaptive": (128, 512, 4096, 16)})):
+        g, pts = BU.goodput(C50, rates, fit, n_requests=1000, seed=7, **kw)
+        print(json.dumps({"kind": "load_test", "budget": C50, "policy": label, "step_time": "GB300 fit",
+                          "goodput_rps": g, "points": pts}), flush=True)
 
 
 def main():

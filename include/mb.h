@@ -270,6 +270,19 @@ mb_status mb_sched_add(mb_sched *s, int64_t req_id, int32_t prompt_len, int32_t 
 mb_status mb_sched_pack(mb_sched *s, mb_sched_batch *out);
 /* Remove a request and return its pages.  Errors: MB_EINVAL (unknown id). */
 mb_status mb_sched_finish(mb_sched *s, int64_t req_id);
+/* Adaptive chunk size (llm-stack-book 7.8, "Priority and Preemption Policies",
+ * adaptive_chunk_size, and its exercise 4, which applies it in schedule()):
+ * from the next mb_sched_pack on, every prefill chunk of a step is capped at
+ *   max_chunk                                    with no running decode,
+ *   min_chunk                                    with >= decode_pressure,
+ *   trunc(base - (d / pressure) (base - min))    with d running decodes between,
+ * clamped to [min_chunk, base_chunk], and at chunk_cap too if that is set
+ * (the fixed per-request cap against head-of-line blocking, pofe.ai "Failure
+ * modes and how to spot them").  The ratio is computed in double precision.
+ * min_chunk = 0 turns it off.  Errors: MB_EINVAL unless 1 <= min <= base <=
+ * max and decode_pressure >= 1. */
+mb_status mb_sched_set_adaptive(mb_sched *s, int32_t min_chunk, int32_t base_chunk, int32_t max_chunk,
+                                int32_t decode_pressure);
 /* Counts: free pages, running, partial, waiting. */
 mb_status mb_sched_counts(const mb_sched *s, int32_t counts[4]);
 mb_status mb_sched_destroy(mb_sched *s);

@@ -90,6 +90,7 @@ _SIGS = {
     "mb_sched_add": (_I32, [_VP, _I64, _I32, _I32]),
     "mb_sched_pack": (_I32, [_VP, ctypes.POINTER(mb_sched_batch)]),
     "mb_sched_finish": (_I32, [_VP, _I64]),
+    "mb_sched_set_adaptive": (_I32, [_VP, _I32, _I32, _I32, _I32]),
     "mb_sched_counts": (_I32, [_VP, c_int32_p]),
     "mb_sched_destroy": (_I32, [_VP]),
     "mb_last_error": (ctypes.c_char_p, []),
@@ -289,6 +290,11 @@ def mb_sched_pack(s: int):
 
 def mb_sched_finish(s: int, req_id: int) -> None:
     _check(lib().mb_sched_finish(s, req_id))
+
+
+def mb_sched_set_adaptive(s: int, min_chunk: int, base_chunk: int = 512, max_chunk: int = 4096,
+                          decode_pressure: int = 16) -> None:
+    _check(lib().mb_sched_set_adaptive(s, min_chunk, base_chunk, max_chunk, decode_pressure))
 
 
 def mb_sched_counts(s: int):

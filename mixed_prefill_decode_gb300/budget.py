@@ -158,14 +158,19 @@ class LoadResult:
 
 def simulate(budget: int, requests: Sequence[Tuple[float, int, int]], step_time: Callable[[Sequence[Row]], float],
              max_seqs: int = 256, chunk_cap: int = 0, num_pages: Optional[int] = None, rate: float = float("nan"),
-             log: Optional[list] = None) -> LoadResult:
+             log: Optional[list] = None, adaptive: Optional[Tuple[int, int, int, int]] = None) -> LoadResult:
     """Replay ``requests`` through the packer with the given budget; each
-    iteration takes ``step_time(rows)`` seconds.  ``log`` (if a list) receives
+    iteration takes ``step_time(rows)`` seconds.  ``chunk_cap`` caps every
+    prefill chunk (the head-of-line cap); ``adaptive`` = (min, base, max,
+    decode pressure) sets the per-step chunk size from the decode load
+    (``mb_sched_set_adaptive``).  ``log`` (if a list) receives
     the call sequence: ("add", id, prompt), ("pack", rows), ("finish", id)."""
     if num_pages is None:   # room for every request's whole context at once
         num_pages = sum((p + o + PAGE_TOKENS - 1) // PAGE_TOKENS + 1 for _, p, o in requests) + 1
     s = mb.mb_sched_create(budget, max_seqs, chunk_cap, list(range(num_pages)))
     try:
+        if adaptive:
+            mb.mb_sched_set_adaptive(s, *adaptive)
         n = len(requests)
         computed = [0] * n
         produced = [0] * n

@@ -36,6 +36,8 @@ struct Req {
 struct mb_sched {
   mb_pack_cfg cfg;
   int32_t num_pages;
+  // adaptive per-step chunk cap (mb_sched_set_adaptive); ad_min == 0: off
+  int32_t ad_min = 0, ad_base = 0, ad_max = 0, ad_pressure = 0;
   std::deque<int32_t> free_pages;
   std::unordered_map<int64_t, Req *> by_id;
   // Queues hold pointers into by_id's objects; std::list keeps FIFO order with
@@ -128,7 +130,25 @@ mb_status mb_sched_pack(mb_sched *s, mb_sched_batch *out) {
   };
   std::vector<Row> rows;
   int64_t left = s->cfg.budget;
-  const int64_t cap = s->cfg.chunk_cap;
+  int64_t cap = s->cfg.chunk_cap;
+  if (s->ad_min > 0) {
+    // this step's chunk size from the decode load (llm-stack-book 7.8,
+    // "Priority and Preemption Policies", adaptive_chunk_size): the largest
+    // chunks with no decode running, the smallest from `pressure` decodes
+    // on, linearly from base down to min in between (truncated)
+    const int64_t depth = static_cast<int64_t>(s->running.size());
+    int64_t eff;
+    if (depth == 0) {
+      eff = s->ad_max;
+    } else if (depth >= s->ad_pressure) {
+      eff = s->ad_min;
+    } else {
+      const double ratio = static_cast<double>(depth) / static_cast<double>(s->ad_pressure);
+      eff = static_cast<int64_t>(static_cast<double>(s->ad_base) - ratio * static_cast<double>(s->ad_base - s->ad_min));
+      eff = std::max<int64_t>(s->ad_min, std::min<int64_t>(eff, s->ad_base));
+    }
+    cap = cap ? std::min(cap, eff) : eff;
+  }
 
   // 1. one token per running decode, while a budget unit is left
   for (Req *r : s->running) {
@@ -193,6 +213,22 @@ mb_status mb_sched_pack(mb_sched *s, mb_sched_batch *out) {
   out->batch.bt_indptr = s->bt_indptr.data();
   out->batch.bt = s->bt.data();
   out->req_ids = s->ids.data();
+  return MB_OK;
+}
+
+mb_status mb_sched_set_adaptive(mb_sched *s, int32_t min_chunk, int32_t base_chunk, int32_t max_chunk,
+                                int32_t decode_pressure) {
+  if (!s) return mb::fail(MB_EINVAL, "mb_sched_set_adaptive: null scheduler");
+  if (min_chunk == 0) {
+    s->ad_min = s->ad_base = s->ad_max = s->ad_pressure = 0;
+    return MB_OK;
+  }
+  if (min_chunk < 1 || base_chunk < min_chunk || max_chunk < base_chunk || decode_pressure < 1)
+    return mb::fail(MB_EINVAL, "mb_sched_set_adaptive: need 1 <= min <= base <= max and decode_pressure >= 1");
+  s->ad_min = min_chunk;
+  s->ad_base = base_chunk;
+  s->ad_max = max_chunk;
+  s->ad_pressure = decode_pressure;
   return MB_OK;
 }
 

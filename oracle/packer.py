@@ -30,7 +30,13 @@ Readings where the pages are silent or disagree:
     this step; a partial prefill's chunk is shortened to what its pages plus
     the free pages can hold, and skipped if that is nothing;
   * finishing a request returns its pages to the tail of the free list in
-    block-table order.
+    block-table order;
+  * adaptive chunk size (optional; llm-stack-book 7.8, "Priority and
+    Preemption Policies", ``adaptive_chunk_size``, applied per step as in its
+    exercise 4): the step's chunk cap follows the number of running decodes d
+    at the start of the step: max with d = 0, min from d >= pressure on, else
+    the base-to-min line at d / pressure, truncated, kept in [min, base]; it
+    combines with ``chunk_cap`` by taking the smaller.
 
 Each scheduled row is (req_id, qo_len, kv_len, block_table); a row with
 qo_len = 1 is a decode row whatever the request's phase.  ``pack`` advances the
@@ -42,7 +48,7 @@ step on (pofe.ai step 5).
 from __future__ import annotations
 
 from collections import deque
-from typing import Dict, List, Sequence, Tuple
+from typing import Dict, List, Optional, Sequence, Tuple
 
 PAGE_TOKENS = 16
 
@@ -65,13 +71,26 @@ class _Req:
         self.pages: List[int] = []
 
 
+def adaptive_chunk(decodes: int, min_chunk: int, base_chunk: int, max_chunk: int, pressure: int) -> int:
+    """The step's chunk size from the number of running decodes
+    (llm-stack-book 7.8, ``adaptive_chunk_size``)."""
+    if decodes == 0:
+        return max_chunk
+    if decodes >= pressure:
+        return min_chunk
+    chunk = int(base_chunk - (decodes / pressure) * (base_chunk - min_chunk))
+    return max(min_chunk, min(chunk, base_chunk))
+
+
 class Packer:
-    def __init__(self, budget: int, max_seqs: int, chunk_cap: int, free_order: Sequence[int]):
+    def __init__(self, budget: int, max_seqs: int, chunk_cap: int, free_order: Sequence[int],
+                 adaptive: Optional[Tuple[int, int, int, int]] = None):
         if budget < 1 or max_seqs < 1 or chunk_cap < 0:
             raise ValueError("bad packer config")
         self.budget = budget
         self.max_seqs = max_seqs
         self.chunk_cap = chunk_cap
+        self.adaptive = adaptive        # (min, base, max, pressure) or None
         self.free = deque(int(p) for p in free_order)
         self.reqs: Dict[int, _Req] = {}
         self.running: List[_Req] = []
@@ -115,6 +134,10 @@ class Packer:
     def pack(self) -> List[Tuple[int, int, int, List[int]]]:
         left = self.budget
         sched: List[Tuple[_Req, int, bool]] = []   # (req, n, is_prefill)
+        cap = self.chunk_cap
+        if self.adaptive:
+            eff = adaptive_chunk(len(self.running), *self.adaptive)
+            cap = min(cap, eff) if cap else eff
 
         # 1. decodes first
         for r in self.running:
@@ -132,8 +155,8 @@ class Packer:
             if left <= 0:
                 break
             n = min(left, r.prompt_len - r.computed)
-            if self.chunk_cap:
-                n = min(n, self.chunk_cap)
+            if cap:
+                n = min(n, cap)
             room = (len(r.pages) + len(self.free)) * PAGE_TOKENS - r.computed
             n = min(n, room)
             if n <= 0:
@@ -148,8 +171,8 @@ class Packer:
             if len(self.running) + len(self.partial) >= self.max_seqs:
                 break
             n = min(left, r.prompt_len)
-            if self.chunk_cap:
-                n = min(n, self.chunk_cap)
+            if cap:
+                n = min(n, cap)
             if pages_for(n) > len(self.free):
                 break
             self.waiting.popleft()

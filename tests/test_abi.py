@@ -28,11 +28,19 @@ def _drive_both(seed, steps=80):
     return rng, P, budget, max_seqs, cap, order
 
 
-@pytest.mark.parametrize("seed", range(30))
+@pytest.mark.parametrize("seed", range(40))
 def test_native_packer_matches_oracle_bit_exactly(mb, seed):
     rng, P, budget, max_seqs, cap, order = _drive_both(seed)
-    py = Packer(budget, max_seqs, cap, order)
+    # seeds 30-39: adaptive chunk size on (min, base, max, pressure)
+    adaptive = None
+    if seed >= 30:
+        mn = int(rng.integers(1, 64))
+        base = mn + int(rng.integers(0, 300))
+        adaptive = (mn, base, base + int(rng.integers(0, 600)), int(rng.integers(1, 12)))
+    py = Packer(budget, max_seqs, cap, order, adaptive=adaptive)
     s = mb.mb_sched_create(budget, max_seqs, cap, order)
+    if adaptive:
+        mb.mb_sched_set_adaptive(s, *adaptive)
     try:
         nid = 0
         for step in range(80):

@@ -138,3 +138,31 @@ def test_page_goodput():
         assert g is not None and abs(g - want) <= 2, (C, g)
     g, pts = BU.goodput(2048, [8, 16, 24], OPT, **kw)
     assert g is None and all(p["p99_tbt_ms"] > slo["p99_tbt_ms"] for p in pts)
+
+
+def test_adaptive_policy_in_the_load_test_matches_oracle_packer():
+    log = []
+    reqs = BU.draw_requests(BU.LoadSpec(rate=25, n_requests=200, seed=21))
+    BU.simulate(1024, reqs, OPT, max_seqs=64, adaptive=(64, 256, 2048, 8), log=log)
+    num_pages = sum((p + o + 15) // 16 + 1 for _, p, o in reqs) + 1
+    ref = OP.Packer(1024, 64, 0, list(range(num_pages)), adaptive=(64, 256, 2048, 8))
+    for ev in log:
+        if ev[0] == "add":
+            ref.add(ev[1], ev[2])
+        elif ev[0] == "finish":
+            ref.finish(ev[1])
+        else:
+            assert [(r[0], r[1], r[2], list(r[3])) for r in ref.pack()] == ev[1]
+
+
+def test_head_of_line_cap_lets_short_prompts_in():
+    # a 100,000-token document arrives first, then short prompts: without a
+    # cap it takes the whole prefill share for ~50 iterations (pofe.ai "Failure
+    # modes and how to spot them"); with a per-request cap the short prompts
+    # are admitted beside it
+    reqs = [(0.0, 100000, 2)] + [(0.001 * i, 200, 2) for i in range(1, 21)]
+    t = 0.01
+    free = BU.simulate(2048, reqs, lambda rows: t)
+    capped = BU.simulate(2048, reqs, lambda rows: t, chunk_cap=512)
+    assert np.max(free.ttft_s[1:]) > 40 * t
+    assert np.max(capped.ttft_s[1:]) < 5 * t

@@ -135,3 +135,36 @@ def test_invariants_random_streams(seed):
         assert sorted(held + list(pk.free)) == list(range(P))
         q, kvl, bti, bt, rid = rows_to_csr(rows)
         assert q[-1] == total and len(bt) == bti[-1]
+
+
+def test_adaptive_chunk_closed_forms():
+    # llm-stack-book 7.8 "Priority and Preemption Policies": defaults min 128,
+    # base 512, max 4,096, pressure 16
+    from oracle.packer import adaptive_chunk
+    f = lambda d: adaptive_chunk(d, 128, 512, 4096, 16)
+    assert f(0) == 4096                   # no decode running: full large chunks
+    assert f(16) == 128 and f(500) == 128 # at and past the pressure threshold
+    assert f(8) == 320                    # halfway: 512 - 0.5 * 384
+    assert f(1) == 488                    # 512 - 384 / 16
+    assert f(15) == 152                   # 512 - 15 * 24
+    vals = [f(d) for d in range(1, 16)]
+    assert all(a >= b for a, b in zip(vals, vals[1:]))   # monotone in the decode load
+
+
+def test_adaptive_cap_bounds_every_prefill_chunk():
+    from oracle.packer import adaptive_chunk
+    rng = np.random.default_rng(77)
+    pk = Packer(budget=2048, max_seqs=64, chunk_cap=0, free_order=range(20000), adaptive=(64, 256, 1024, 8))
+    nid = 0
+    for _ in range(120):
+        if rng.random() < 0.6:
+            pk.add(nid, int(rng.integers(1, 3000)))
+            nid += 1
+        if pk.running and rng.random() < 0.3:
+            pk.finish(pk.running[0].rid)
+        d = len(pk.running)
+        cap = adaptive_chunk(d, 64, 256, 1024, 8)
+        running = {r.rid for r in pk.running}
+        for rid, qo, kv, table in pk.pack():
+            if rid not in running:
+                assert qo <= cap
