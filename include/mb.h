@@ -270,6 +270,29 @@ mb_status mb_sched_add(mb_sched *s, int64_t req_id, int32_t prompt_len, int32_t 
 mb_status mb_sched_pack(mb_sched *s, mb_sched_batch *out);
 /* Remove a request and return its pages.  Errors: MB_EINVAL (unknown id). */
 mb_status mb_sched_finish(mb_sched *s, int64_t req_id);
+/* Next tokens of a pass, greedy (pofe.ai "Chunked prefill", "How it works,
+ * step by step", step 5: every decode row, and the last row of a prompt
+ * whose last chunk ran in the pass, samples a token in that same pass; the
+ * pages leave the sampling rule open, this is the greedy one):
+ *   y_i      = RMSNorm(x[rows[i]]) * g_final                    (eps)
+ *   logits_i = y_i W_lm^T                    bf16, fp32 accumulation
+ *   ids[i]   = argmax_j logits_i[j], the lowest j among equal maxima
+ * x: device bf16 [T][d] (the last layer's output); rows: device int32
+ * [n_rows], each in [0, T); g_final: device bf16 [d]; w_lm: device bf16
+ * [vocab][d]; y_work: device bf16 [n_rows][d] and logits: device bf16
+ * [n_rows][vocab], caller-owned workspaces (logits holds the row logits
+ * afterwards); ids: device int32 [n_rows].  d % 64 == 0, d <= 8192, vocab %
+ * 32 == 0, pointers 16-byte aligned.  Asynchronous on `stream`; a row id out
+ * of range records MB_EDEVICE (mb_device_status with layer NULL). */
+mb_status mb_sample_greedy(const void *x, int32_t T, const int32_t *rows, int32_t n_rows, int32_t d, float eps,
+                           const void *g_final, const void *w_lm, int32_t vocab, void *y_work, void *logits,
+                           int32_t *ids, void *stream);
+/* Token embeddings for the next pass: out[i] = table[ids[i]] (device bf16
+ * [vocab][d] -> [n][d]; ids device int32 [n]).  An id out of range records
+ * MB_EDEVICE and gives a zero row.  d % 8 == 0. */
+mb_status mb_embed(const void *table, int32_t vocab, int32_t d, const int32_t *ids, int32_t n, void *out,
+                   void *stream);
+
 /* Adaptive chunk size (llm-stack-book 7.8, "Priority and Preemption Policies",
  * adaptive_chunk_size, and its exercise 4, which applies it in schedule()):
  * from the next mb_sched_pack on, every prefill chunk of a step is capped at

@@ -91,6 +91,8 @@ _SIGS = {
     "mb_sched_pack": (_I32, [_VP, ctypes.POINTER(mb_sched_batch)]),
     "mb_sched_finish": (_I32, [_VP, _I64]),
     "mb_sched_set_adaptive": (_I32, [_VP, _I32, _I32, _I32, _I32]),
+    "mb_sample_greedy": (_I32, [_VP, _I32, _VP, _I32, _I32, ctypes.c_float, _VP, _VP, _I32, _VP, _VP, _VP, _VP]),
+    "mb_embed": (_I32, [_VP, _I32, _I32, _VP, _I32, _VP, _VP]),
     "mb_sched_counts": (_I32, [_VP, c_int32_p]),
     "mb_sched_destroy": (_I32, [_VP]),
     "mb_last_error": (ctypes.c_char_p, []),
@@ -261,6 +263,17 @@ def mb_stack_destroy(stack: int) -> None:
     _check(lib().mb_stack_destroy(stack))
 
 
+# ----------------------------------------------------------- next tokens
+def mb_sample_greedy(x, T: int, rows, n_rows: int, d: int, eps: float, g_final, w_lm, vocab: int, y_work, logits,
+                     ids, stream=None) -> None:
+    _check(lib().mb_sample_greedy(_ptr(x), T, _ptr(rows), n_rows, d, eps, _ptr(g_final), _ptr(w_lm), vocab,
+                                  _ptr(y_work), _ptr(logits), _ptr(ids), stream))
+
+
+def mb_embed(table, vocab: int, d: int, ids, n: int, out, stream=None) -> None:
+    _check(lib().mb_embed(_ptr(table), vocab, d, _ptr(ids), n, _ptr(out), stream))
+
+
 # ------------------------------------------------------------- scheduler
 def mb_sched_create(budget: int, max_seqs: int, chunk_cap: int, free_order: Sequence[int]) -> int:
     fo = _i32(free_order)
@@ -317,7 +330,10 @@ class Layer:
                                   max_tokens)
         self.w = mb_layer_weights(*[_ptr(weights.get(k)) for k in
                                     ("g_attn", "w_qkv", "g_q", "g_k", "w_o", "g_ffn", "w_gate_up", "w_down")])
+        # the library holds raw device pointers: keep the caller's tensors
+        # (weights, and a KV buffer it hands in) alive as long as the layer
         self._keep = weights
+        self._kv_buf = kv_buf
         self.handle = mb_layer_create(self.desc, self.w)
         self.kv = mb_kv_alloc(self.handle, num_pages, kv_buf)
 

@@ -846,6 +846,47 @@ mb_status mb_gemm(const void *A, const void *B, void *D, const void *R, int32_t 
   return MB_OK;
 }
 
+// ------------------------------------------------------- next tokens
+mb_status mb_sample_greedy(const void *x, int32_t T, const int32_t *rows, int32_t n_rows, int32_t d, float eps,
+                           const void *g_final, const void *w_lm, int32_t vocab, void *y_work, void *logits,
+                           int32_t *ids, void *stream) {
+  if (!x || !rows || !g_final || !w_lm || !y_work || !logits || !ids || T < 0 || n_rows < 0 || d <= 0 || vocab <= 0)
+    return fail(MB_EINVAL, "mb_sample_greedy: bad argument");
+  if (d % 64) return fail(MB_EUNSUPPORTED, "mb_sample_greedy: d must be a multiple of 64");
+  if (vocab % 32) return fail(MB_EUNSUPPORTED, "mb_sample_greedy: vocab must be a multiple of 32");
+  if (d > 8192) return fail(MB_EUNSUPPORTED, "mb_sample_greedy: d must be at most 8192");
+  for (const void *p : {x, g_final, w_lm, static_cast<const void *>(y_work), static_cast<const void *>(logits)})
+    if (reinterpret_cast<uintptr_t>(p) % 16) return fail(MB_EINVAL, "mb_sample_greedy: pointers must be 16-byte aligned");
+  if (n_rows == 0) return MB_OK;
+  mb::DeviceCtx *ctx = nullptr;
+  mb_status st = mb::device_ctx(&ctx);
+  if (st != MB_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = mb::rmsnorm_rows_run(x, T, rows, n_rows, g_final, y_work, d, eps, ctx->err, s);
+  if (e != cudaSuccess) return mb::cuda_fail(e, "mb_sample_greedy: final norm");
+  e = mb::gemm_run(y_work, w_lm, nullptr, logits, nullptr, n_rows, vocab, d, mb::kEpiStore,
+                   mb::gemm_workspace_carve(ctx->gemm_ws), ctx->err, s);
+  if (e != cudaSuccess) return mb::cuda_fail(e, "mb_sample_greedy: LM head");
+  e = mb::argmax_rows_run(logits, n_rows, vocab, ids, s);
+  if (e != cudaSuccess) return mb::cuda_fail(e, "mb_sample_greedy: argmax");
+  return MB_OK;
+}
+
+mb_status mb_embed(const void *table, int32_t vocab, int32_t d, const int32_t *ids, int32_t n, void *out,
+                   void *stream) {
+  if (!table || !ids || !out || vocab <= 0 || d <= 0 || n < 0) return fail(MB_EINVAL, "mb_embed: bad argument");
+  if (d % 8) return fail(MB_EUNSUPPORTED, "mb_embed: d must be a multiple of 8");
+  if (reinterpret_cast<uintptr_t>(table) % 16 || reinterpret_cast<uintptr_t>(out) % 16)
+    return fail(MB_EINVAL, "mb_embed: table and out must be 16-byte aligned");
+  if (n == 0) return MB_OK;
+  mb::DeviceCtx *ctx = nullptr;
+  mb_status st = mb::device_ctx(&ctx);
+  if (st != MB_OK) return st;
+  cudaError_t e = mb::embed_rows_run(table, vocab, d, ids, n, out, ctx->err, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return mb::cuda_fail(e, "mb_embed");
+  return MB_OK;
+}
+
 // ------------------------------------------------------------------ step
 mb_status mb_step(mb_layer *L, mb_kv *kv, const mb_batch *b, const void *x_in, void *x_out, void *stream) {
   if (!L || !kv || !b || !x_in || !x_out) return fail(MB_EINVAL, "mb_step: null argument");

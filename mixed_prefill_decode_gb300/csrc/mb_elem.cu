@@ -24,13 +24,26 @@ using namespace dev;
 constexpr int kNormThreads = 128;
 constexpr int kNormMaxVec = 8;  // d <= 128 * 8 * 8 = 8192
 
+// rows (optional): output row i normalises input row rows[i] (each in
+// [0, n_src); an id out of range records kErrBounds and gives a zero row).
 __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const __nv_bfloat16 *__restrict__ x,
                                                                const __nv_bfloat16 *__restrict__ g,
-                                                               __nv_bfloat16 *__restrict__ y, int d, float eps) {
+                                                               __nv_bfloat16 *__restrict__ y, int d, float eps,
+                                                               const int32_t *__restrict__ rows, int n_src, int *err) {
   pdl_wait();
   const int row = blockIdx.x;
   const int nv = d / 8;
-  const uint4 *xr = reinterpret_cast<const uint4 *>(x + static_cast<size_t>(row) * d);
+  int src = row;
+  if (rows) {
+    src = rows[row];
+    if (src < 0 || src >= n_src) {
+      if (threadIdx.x == 0) atomicExch(err, kErrBounds);
+      uint4 *yr = reinterpret_cast<uint4 *>(y + static_cast<size_t>(row) * d);
+      for (int v = threadIdx.x; v < nv; v += kNormThreads) yr[v] = make_uint4(0, 0, 0, 0);
+      return;
+    }
+  }
+  const uint4 *xr = reinterpret_cast<const uint4 *>(x + static_cast<size_t>(src) * d);
   const uint4 *gr = reinterpret_cast<const uint4 *>(g);
   uint4 buf[kNormMaxVec], gbuf[kNormMaxVec];
   float ss = 0.f;
@@ -232,13 +245,101 @@ __global__ void __launch_bounds__(kRopeThreads) rope_append_kernel(const RopePar
   }
 }
 
+// ------------------------------------------------------- greedy sampling
+// One CTA per row: the largest logit and its index, the lowest index among
+// equal maxima (a NaN never wins).  16-byte loads of 8 bf16.
+constexpr int kArgmaxThreads = 256;
+
+__device__ __forceinline__ bool argmax_better(float v, int i, float bv, int bi) {
+  return v > bv || (v == bv && i < bi);
+}
+
+__global__ void __launch_bounds__(kArgmaxThreads) argmax_kernel(const __nv_bfloat16 *__restrict__ logits, int vocab,
+                                                                int32_t *__restrict__ ids) {
+  pdl_wait();
+  const int row = blockIdx.x;
+  const uint4 *lr = reinterpret_cast<const uint4 *>(logits + static_cast<size_t>(row) * vocab);
+  float bv = -INFINITY;
+  int bi = 0x7fffffff;
+  for (int v = threadIdx.x; v < vocab / 8; v += kArgmaxThreads) {
+    const uint4 q = lr[v];
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float a = bf16lo(w[e]), b = bf16hi(w[e]);
+      const int i = 8 * v + 2 * e;
+      if (argmax_better(a, i, bv, bi)) { bv = a; bi = i; }
+      if (argmax_better(b, i + 1, bv, bi)) { bv = b; bi = i + 1; }
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+    const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+    if (argmax_better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+  }
+  __shared__ float sv[kArgmaxThreads / 32];
+  __shared__ int si[kArgmaxThreads / 32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) { sv[warp] = bv; si[warp] = bi; }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < kArgmaxThreads / 32; ++w)
+      if (argmax_better(sv[w], si[w], bv, bi)) { bv = sv[w]; bi = si[w]; }
+    ids[row] = bi == 0x7fffffff ? 0 : bi;   // all NaN: token 0
+  }
+}
+
+// ------------------------------------------------------------ embeddings
+constexpr int kEmbedThreads = 128;
+
+__global__ void __launch_bounds__(kEmbedThreads) embed_kernel(const __nv_bfloat16 *__restrict__ table, int vocab, int d,
+                                                              const int32_t *__restrict__ ids,
+                                                              __nv_bfloat16 *__restrict__ out, int *err) {
+  pdl_wait();
+  const int row = blockIdx.x;
+  const int id = ids[row];
+  uint4 *o = reinterpret_cast<uint4 *>(out + static_cast<size_t>(row) * d);
+  if (id < 0 || id >= vocab) {
+    if (threadIdx.x == 0) atomicExch(err, kErrBounds);
+    for (int v = threadIdx.x; v < d / 8; v += kEmbedThreads) o[v] = make_uint4(0, 0, 0, 0);
+    return;
+  }
+  const uint4 *t = reinterpret_cast<const uint4 *>(table + static_cast<size_t>(id) * d);
+  for (int v = threadIdx.x; v < d / 8; v += kEmbedThreads) o[v] = t[v];
+}
+
 }  // namespace
 
 cudaError_t rmsnorm_run(const void *x, const void *g, void *y, int rows, int d, float eps, cudaStream_t st) {
   if (rows <= 0) return cudaSuccess;
   if (d % 8 != 0 || d > kNormThreads * kNormMaxVec * 8) return cudaErrorInvalidValue;
   return launch_pdl(rmsnorm_kernel, dim3(rows), dim3(kNormThreads), 0, st, 1, static_cast<const __nv_bfloat16 *>(x),
-                    static_cast<const __nv_bfloat16 *>(g), static_cast<__nv_bfloat16 *>(y), d, eps);
+                    static_cast<const __nv_bfloat16 *>(g), static_cast<__nv_bfloat16 *>(y), d, eps,
+                    static_cast<const int32_t *>(nullptr), 0, static_cast<int *>(nullptr));
+}
+
+cudaError_t rmsnorm_rows_run(const void *x, int n_src, const int32_t *rows, int n_rows, const void *g, void *y, int d,
+                             float eps, int *err, cudaStream_t st) {
+  if (n_rows <= 0) return cudaSuccess;
+  if (d % 8 != 0 || d > kNormThreads * kNormMaxVec * 8) return cudaErrorInvalidValue;
+  return launch_pdl(rmsnorm_kernel, dim3(n_rows), dim3(kNormThreads), 0, st, 1, static_cast<const __nv_bfloat16 *>(x),
+                    static_cast<const __nv_bfloat16 *>(g), static_cast<__nv_bfloat16 *>(y), d, eps, rows, n_src, err);
+}
+
+cudaError_t argmax_rows_run(const void *logits, int n_rows, int vocab, int32_t *ids, cudaStream_t st) {
+  if (n_rows <= 0) return cudaSuccess;
+  if (vocab <= 0 || vocab % 8 != 0) return cudaErrorInvalidValue;
+  return launch_pdl(argmax_kernel, dim3(n_rows), dim3(kArgmaxThreads), 0, st, 1,
+                    static_cast<const __nv_bfloat16 *>(logits), vocab, ids);
+}
+
+cudaError_t embed_rows_run(const void *table, int vocab, int d, const int32_t *ids, int n, void *out, int *err,
+                           cudaStream_t st) {
+  if (n <= 0) return cudaSuccess;
+  if (d % 8 != 0) return cudaErrorInvalidValue;
+  return launch_pdl(embed_kernel, dim3(n), dim3(kEmbedThreads), 0, st, 1, static_cast<const __nv_bfloat16 *>(table),
+                    vocab, d, ids, static_cast<__nv_bfloat16 *>(out), err);
 }
 
 cudaError_t rope_append_run(const RopeArgs &a, cudaStream_t st) {

@@ -36,6 +36,14 @@ cudaError_t gemm_run(const void *A, const void *B, const CUtensorMap *tmB, void 
 
 // ---- element-wise kernels ----
 cudaError_t rmsnorm_run(const void *x, const void *g, void *y, int rows, int d, float eps, cudaStream_t st);
+// y[i] = RMSNorm(x[rows[i]]) g for i < n_rows (rows: device int32, each in [0, n_src))
+cudaError_t rmsnorm_rows_run(const void *x, int n_src, const int32_t *rows, int n_rows, const void *g, void *y, int d,
+                             float eps, int *err, cudaStream_t st);
+// ids[i] = argmax of bf16 row i of logits [n_rows][vocab] (lowest index among equal maxima)
+cudaError_t argmax_rows_run(const void *logits, int n_rows, int vocab, int32_t *ids, cudaStream_t st);
+// out[i] = table[ids[i]] (bf16 [vocab][d] -> [n][d])
+cudaError_t embed_rows_run(const void *table, int vocab, int d, const int32_t *ids, int n, void *out, int *err,
+                           cudaStream_t st);
 
 struct RopeArgs {
   const void *qkv;          // [T][(Hq + 2 Hkv) hd] bf16

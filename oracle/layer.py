@@ -202,3 +202,15 @@ def layer_step(shape: Dict, w: Dict[str, np.ndarray], pool: np.ndarray, qo_indpt
 
 def weights_to_f64(w: Dict[str, np.ndarray]) -> Dict[str, np.ndarray]:
     return {kk: bf16_bits_to_f64(vv) for kk, vv in w.items()}
+
+
+def next_tokens_greedy(x: np.ndarray, rows, g_final: np.ndarray, w_lm: np.ndarray, eps: float):
+    """The tokens a pass samples (pofe.ai "Chunked prefill", "How it works,
+    step by step", step 5: each decode row and the last row of a prompt whose
+    last chunk ran sample in the same pass).  The pages leave the rule open;
+    the greedy one: logits = RMSNorm(x[rows]) g_final W_lm^T, token = the
+    argmax, the lowest index among equal maxima (NumPy's argmax returns the
+    first).  Returns (logits float64 [n, vocab], ids int64 [n])."""
+    y = rms_norm(np.asarray(x, dtype=np.float64)[np.asarray(rows, dtype=np.int64)], g_final, eps)
+    logits = linear(y, w_lm)
+    return logits, np.argmax(logits, axis=1)

@@ -1,0 +1,135 @@
+"""GPU parity of the next-token step (greedy sampling from the LM head, and the
+embedding of the sampled ids for the next pass) against the oracle.
+
+The argmax is an integer decided by floating point: the kernel decides on the
+bf16 logits it wrote, so the ids are compared bit-exactly with the argmax of
+those same logits (lowest index among equal maxima); the logits themselves
+are compared with the oracle's float64 ones within the acceptance tolerance,
+and where the oracle's own argmax differs, its top two must lie within that
+tolerance of each other."""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import layer as OL
+from mixed_prefill_decode_gb300 import workload as W
+from gpu_util import to_dev, from_dev, assert_close, f64, TOL
+
+pytestmark = pytest.mark.gpu
+
+
+def _argmax_lowest(logits_bits: np.ndarray) -> np.ndarray:
+    v = f64(logits_bits)
+    v = np.where(np.isnan(v), -np.inf, v)
+    return np.argmax(v, axis=1)
+
+
+@pytest.mark.parametrize("T,d,vocab,n_rows,seed", [(68, 256, 4096, 5, 1), (576, 4096, 32000, 65, 2),
+                                                    (300, 512, 1024, 300, 3), (17, 128, 96, 1, 4)])
+def test_sample_greedy_matches_oracle(mb, T, d, vocab, n_rows, seed):
+    rng = np.random.default_rng(seed)
+    x = W.f32_to_bf16_bits(rng.standard_normal((T, d), dtype=np.float32))
+    g = W.f32_to_bf16_bits(1.0 + 0.1 * rng.standard_normal(d).astype(np.float32))
+    w = W.f32_to_bf16_bits(0.02 * rng.standard_normal((vocab, d), dtype=np.float32))
+    w[vocab - 1] = w[vocab // 3]          # duplicated rows: ties go to the lower id
+    rows = np.sort(rng.choice(T, size=n_rows, replace=False)).astype(np.int32)
+    dx, dg, dw = to_dev(x), to_dev(g), to_dev(w)
+    drows = torch.from_numpy(rows).cuda()
+    y = torch.empty((n_rows, d), dtype=torch.bfloat16, device="cuda")
+    logits = torch.full((n_rows, vocab), float("nan"), dtype=torch.bfloat16, device="cuda")
+    ids = torch.full((n_rows,), -1, dtype=torch.int32, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    mb.mb_sample_greedy(dx, T, drows, n_rows, d, 1e-6, dg, dw, vocab, y, logits, ids, s)
+    mb.mb_device_status(None, s)
+    got_logits = from_dev(logits)
+    got_ids = ids.cpu().numpy()
+    # the decision, bit-exact on the kernel's own logits
+    assert np.array_equal(got_ids, _argmax_lowest(got_logits))
+    # the logits against the oracle's float64 ones
+    ref_logits, ref_ids = OL.next_tokens_greedy(f64(x), rows, f64(g), f64(w), 1e-6)
+    assert_close(f"logits {T}x{vocab}", f64(got_logits), ref_logits)
+    scale = np.max(np.abs(ref_logits))
+    for k in np.nonzero(got_ids != ref_ids)[0]:
+        # only a near tie may flip: the oracle's values at both ids agree within the tolerance
+        assert ref_logits[k, ref_ids[k]] - ref_logits[k, got_ids[k]] <= TOL * scale
+    assert np.mean(got_ids == ref_ids) >= 0.9
+
+
+def test_embed_is_exact_and_checks_ids(mb):
+    rng = np.random.default_rng(9)
+    vocab, d, n = 500, 384, 37
+    table = W.f32_to_bf16_bits(rng.standard_normal((vocab, d), dtype=np.float32))
+    ids = rng.integers(0, vocab, size=n).astype(np.int32)
+    dt = to_dev(table)
+    out = torch.full((n, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    mb.mb_embed(dt, vocab, d, torch.from_numpy(ids).cuda(), n, out, s)
+    mb.mb_device_status(None, s)
+    assert np.array_equal(from_dev(out), table[ids])
+    # an id out of range: a zero row and an error word (checked by the kernel)
+    bad = ids.copy()
+    bad[5] = vocab + 3
+    mb.mb_embed(dt, vocab, d, torch.from_numpy(bad).cuda(), n, out, s)
+    with pytest.raises(mb.MbError):
+        mb.mb_device_status(None, s)
+    got = from_dev(out)
+    assert np.all(got[5] == 0) and np.array_equal(np.delete(got, 5, 0), table[np.delete(bad, 5)])
+
+
+def test_generation_loop_on_a_layer(mb):
+    """Three passes of one layer where every decode row's next input is the
+    embedding of the token the previous pass sampled: each pass's ids equal
+    the argmax of its own logits, and its logits match the oracle fed the same
+    layer output."""
+    wl = W.small_mixed(W.SMALL_GQA, seed=31, n_dec=6, chunk=0)
+    weights, x, batch, pool = W.materialize(wl)
+    shape = wl.shape
+    P = pool.shape[0]
+    vocab = 2048
+    rng = np.random.default_rng(32)
+    table = W.f32_to_bf16_bits(rng.standard_normal((vocab, shape.d_model), dtype=np.float32))
+    w_lm = W.f32_to_bf16_bits(0.02 * rng.standard_normal((vocab, shape.d_model), dtype=np.float32))
+    g_f = W.f32_to_bf16_bits(np.ones(shape.d_model, dtype=np.float32))
+    dw = {k: to_dev(v) for k, v in weights.items()}
+    L = mb.Layer(shape.as_dict(), dw, batch.num_tokens + 8, pool.shape[0] + 64, kv_buf=to_dev(
+        np.concatenate([pool.reshape(-1), np.full(64 * pool[0].size, W.KV_SENTINEL, np.uint16)])))
+    s = torch.cuda.current_stream().cuda_stream
+    dt, dwl, dgf = to_dev(table), to_dev(w_lm), to_dev(g_f)
+    T = batch.num_tokens
+    dx = to_dev(x)
+    rows = torch.arange(T, dtype=torch.int32, device="cuda")
+    y = torch.empty((T, shape.d_model), dtype=torch.bfloat16, device="cuda")
+    logits = torch.empty((T, vocab), dtype=torch.bfloat16, device="cuda")
+    ids = torch.empty((T,), dtype=torch.int32, device="cuda")
+    yw = torch.empty((T, shape.d_model), dtype=torch.bfloat16, device="cuda")
+    kv_len = batch.kv_len.copy()
+    bt_indptr, bt = batch.bt_indptr.copy(), batch.bt.copy()
+    for step in range(3):
+        b = mb.Batch(batch.qo_indptr, kv_len, bt_indptr, bt)
+        L.step(b, dx, y, s)
+        mb.mb_sample_greedy(y, T, rows, T, shape.d_model, shape.rms_eps, dgf, dwl, vocab, yw, logits, ids, s)
+        mb.mb_device_status(L.handle, s)
+        mb.mb_device_status(None, s)
+        got_logits = from_dev(logits)
+        got_ids = ids.cpu().numpy()
+        assert np.array_equal(got_ids, _argmax_lowest(got_logits))
+        ref_logits, _ = OL.next_tokens_greedy(f64(from_dev(y)), np.arange(T), f64(g_f), f64(w_lm), shape.rms_eps)
+        assert_close(f"loop logits step {step}", f64(got_logits), ref_logits)
+        # next pass: every row decodes one more token, embedded from its sampled id
+        mb.mb_embed(dt, vocab, shape.d_model, ids, T, dx, s)
+        mb.mb_device_status(None, s)
+        assert np.array_equal(from_dev(dx), table[got_ids])
+        kv_len = kv_len + 1
+        # grow block tables where a row crosses a page boundary
+        new_bt, new_ind = [], [0]
+        nxt = P + 16 * step   # the fresh pages appended to the pool
+        for r in range(len(kv_len)):
+            tab = list(bt[bt_indptr[r]:bt_indptr[r + 1]])
+            while len(tab) * 16 < kv_len[r]:
+                tab.append(nxt)
+                nxt += 1
+            new_bt += tab
+            new_ind.append(len(new_bt))
+        bt, bt_indptr = np.array(new_bt, np.int32), np.array(new_ind, np.int32)
+    L.close()

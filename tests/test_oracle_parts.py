@@ -152,3 +152,26 @@ def test_single_token_attention_path_is_value_projection():
     v = xn @ w["w_qkv"][(Hq + Hkv) * hd:].T          # [1, Hkv*hd]
     assert Hq == Hkv       # group 1: q head h reads v head h
     np.testing.assert_allclose(r["h"], x + v @ w["w_o"].T, rtol=1e-10, atol=1e-12)
+
+
+def test_next_tokens_greedy_one_hot_and_ties():
+    # LM head rows that are one-hot in d pick the coordinate of the largest
+    # normalised activation; duplicated rows tie and the lower id wins
+    from oracle.layer import next_tokens_greedy
+    rng = np.random.default_rng(4)
+    d, vocab = 16, 40
+    x = rng.standard_normal((5, d))
+    g = np.ones(d)
+    W = np.zeros((vocab, d))
+    for v in range(d):
+        W[v, v] = 1.0
+    W[30] = W[3]                    # a duplicate of row 3
+    logits, ids = next_tokens_greedy(x, [4, 0, 2], g, W, 1e-6)
+    for k, r in enumerate([4, 0, 2]):
+        want = int(np.argmax(x[r]))
+        assert ids[k] == want
+        assert logits[k, 30] == logits[k, 3]
+    x2 = np.zeros((1, d))
+    x2[0, 3] = 5.0
+    _, ids2 = next_tokens_greedy(x2, [0], g, W, 1e-6)
+    assert ids2[0] == 3             # tie with row 30: the lower index
