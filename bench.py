@@ -362,6 +362,93 @@ def stack_step_time(mb, torch, wl, n_layers, steps: int = 10, warmup: int = 3, s
             "kv_pool": "one physical pool shared by all layers" if shared else "one pool per layer"}
 
 
+def generation_step_time(mb, torch, peaks, n_decodes: int = 64, vocab: int = 128256, steps: int = 8,
+                         warmup: int = 3) -> dict:
+    """Token generation on the 32-layer Llama-3-8B-shaped stack (pofe.ai
+    "Chunked prefill", step 5: the pass samples its next tokens): per step,
+    the stack over n_decodes decode rows, the final RMSNorm + LM head (vocab x
+    d, bf16) + greedy argmax of every row, and the embedding of the sampled ids
+    as the next step's input.  Weights, KV and the LM head are drawn on the
+    device; L2 flushed between steps.  Reports output tokens/s and the LM
+    head's share (its time also alone, against HBM: the weights are read once
+    per step)."""
+    sh = W.LLAMA3_8B
+    wl, nl = W.llama3_8b_stack(n_decodes, n_decodes)   # a budget of b: decodes only
+    batch, num_pages = W.make_batch(wl.reqs, wl.seed + 1, spare_pages=4 * n_decodes)
+    d = sh.d_model
+    free_budget = torch.cuda.mem_get_info()[0] - (24 << 30)
+    pool_bytes = num_pages * 2 * sh.n_kv_heads * 16 * sh.head_dim * 2
+    shared = pool_bytes * nl > free_budget
+    shared_pool = W.device_kv_pool(sh, num_pages, wl.seed + 200) if shared else None
+    layers, keep = [], []
+    for l in range(nl):
+        dw = W.device_weights(sh, 5100 + l)
+        dpool = shared_pool if shared else W.device_kv_pool(sh, num_pages, wl.seed + 200 + l)
+        layers.append(mb.Layer(sh.as_dict(), dw, batch.num_tokens, num_pages, kv_buf=dpool))
+        keep.append((dw, dpool))
+    stack = mb.mb_stack_create([L.handle for L in layers], True)
+    g = torch.Generator(device="cuda").manual_seed(wl.seed + 7)
+    w_lm = (torch.randn((vocab, d), generator=g, device="cuda") * 0.02).to(torch.bfloat16)
+    table = torch.randn((vocab, d), generator=g, device="cuda").to(torch.bfloat16)
+    g_final = torch.ones(d, dtype=torch.bfloat16, device="cuda")
+    T = batch.num_tokens
+    x = torch.randn((T, d), generator=g, device="cuda").to(torch.bfloat16)
+    y = torch.empty_like(x)
+    rows = torch.arange(T, dtype=torch.int32, device="cuda")
+    yw = torch.empty_like(x)
+    logits = torch.empty((T, vocab), dtype=torch.bfloat16, device="cuda")
+    ids = torch.empty((T,), dtype=torch.int32, device="cuda")
+    kvs = [L.kv for L in layers]
+    cb = mb.Batch.of(batch)
+    stream = torch.cuda.current_stream()
+    s = stream.cuda_stream
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+
+    def one_step():
+        mb.mb_stack_step(stack, kvs, cb, x, y, s)
+        mb.mb_sample_greedy(y, T, rows, T, d, sh.rms_eps, g_final, w_lm, vocab, yw, logits, ids, s)
+        mb.mb_embed(table, vocab, d, ids, T, x, s)
+
+    for _ in range(warmup):
+        one_step()
+    torch.cuda.synchronize()
+    e0 = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    e1 = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for i in range(steps):
+        flush.fill_(i & 0xFF)
+        e0[i].record(stream)
+        one_step()
+        e1[i].record(stream)
+    torch.cuda.synchronize()
+    mb.mb_device_status(layers[0].handle, s)
+    mb.mb_device_status(None, s)
+    ms = sum(a.elapsed_time(b) for a, b in zip(e0, e1)) / steps
+    # the sampling part alone (final norm + LM head + argmax), L2 flushed
+    h0 = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    h1 = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for i in range(steps):
+        flush.fill_(i & 0xFF)
+        h0[i].record(stream)
+        mb.mb_sample_greedy(y, T, rows, T, d, sh.rms_eps, g_final, w_lm, vocab, yw, logits, ids, s)
+        h1[i].record(stream)
+    torch.cuda.synchronize()
+    mb.mb_device_status(None, s)
+    head_ms = sum(a.elapsed_time(b) for a, b in zip(h0, h1)) / steps
+    head_bytes = vocab * d * 2 + T * vocab * 2
+    mb.mb_stack_destroy(stack)
+    for L in layers:
+        L.close()
+    del keep, shared_pool
+    torch.cuda.empty_cache()
+    return {"workload": f"llama3_8b_stack32_generate_b{n_decodes}", "layers": nl, "vocab": vocab,
+            "decodes": T, "ms_per_step": round(ms, 4), "output_tokens_per_s": round(T / (ms / 1e3), 1),
+            "sample_ms": round(head_ms, 4), "sample_share": round(head_ms / ms, 4),
+            "sample_gbs": round(head_bytes / (head_ms / 1e3) / 1e9, 1),
+            "sample_frac_hbm": round(head_bytes / (head_ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
+            "batch": "the same decode rows every step (positions held: timing-equivalent)",
+            "kv_pool": "one physical pool shared by all layers" if shared else "one pool per layer"}
+
+
 def to_dev(bits, torch):
     return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16).copy()).view(torch.bfloat16).cuda()
 
@@ -516,10 +603,11 @@ def run_mine(args, rank: int, world: int, local: int, pg):
 
     # ---- decode rows alone (no chunk tiles in the grid), and the 40-layer stack
     dec_only = decode_only_attention(mb, torch, peaks) if rank == 0 and not args.no_aux else None
-    stack40 = None
+    stack40 = gen = None
     if rank == 0 and not args.no_aux:
         swl, nl = W.qwen3_14b_stack(prefix=30720)
         stack40 = stack_step_time(mb, torch, swl, nl)
+        gen = generation_step_time(mb, torch, peaks)
 
     # ---- P3 step-time model with GB300 peaks, as an analytic comparator
     from mixed_prefill_decode_gb300 import step_model as SM
@@ -555,6 +643,7 @@ def run_mine(args, rank: int, world: int, local: int, pg):
                  "frac_sustained": round(gemm_flops / (gemm_ms / 1e3) / 1e12 / peaks["bf16_tflops_sustained"], 4)},
         "decode_attn": dec_only,
         "stack_qwen3_14b_40": stack40,
+        "generate_llama3_8b_32": gen,
         "roofline_step_ms": round(roof_ms, 5),
         "step_model_ms": round(model_ms, 5),
         "cpu_baseline": cpu,
