@@ -689,6 +689,79 @@ def run_sweep(args):
             print(json.dumps(r), flush=True)
 
 
+def run_partition(args):
+    """SM partition for decode attention (row f1: ConfluxServe gives decode
+    "just enough SMs" for most of its bandwidth).  (1) Decode-only attention
+    (Qwen3-14B-shaped, 16 x 8,192 tokens) against the cap on decode-worker
+    CTAs; (2) the Llama-3-8B-shaped step (T = 576) with each cap against the
+    one-grid default, where workers take every SM the chunk tiles leave.  One
+    JSON line per point."""
+    import torch
+    from mixed_prefill_decode_gb300 import build as B
+    from mixed_prefill_decode_gb300 import binding as mb
+    B.build()
+    peaks, _ = load_peaks()
+    s = torch.cuda.current_stream()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+
+    def make(wl):
+        wb, x, batch, pool = W.materialize(wl, unit_gains=True)
+        dw = {k: to_dev(v, torch) for k, v in wb.items()}
+        dpool = to_dev(pool.reshape(-1), torch)
+        layer = mb.Layer(wl.shape.as_dict(), dw, batch.num_tokens, pool.shape[0], kv_buf=dpool)
+        dx = to_dev(x, torch)
+        return layer, mb.Batch.of(batch), dx, torch.empty_like(dx), batch
+
+    def kernel_ms(layer, cb, dx, dy, n=20):
+        for _ in range(3):
+            layer.step(cb, dx, dy, s.cuda_stream)
+        mb.mb_layer_set_timing(layer.handle, True)
+        for i in range(n):
+            flush.fill_(i & 0xFF)
+            layer.step(cb, dx, dy, s.cuda_stream)
+        km, k = mb.mb_layer_timing(layer.handle)
+        mb.mb_layer_set_timing(layer.handle, False)
+        mb.mb_device_status(layer.handle, s.cuda_stream)
+        return {name: v / max(1, k) for name, v in km.items()}
+
+    wl = W.qwen3_14b_mixed(0)
+    layer, cb, dx, dy, batch = make(wl)
+    by = float(np.sum(batch.kv_len)) * wl.shape.n_kv_heads * wl.shape.head_dim * 4
+    for cap in (8, 16, 24, 32, 48, 64, 96, 128, 0):
+        mb.mb_layer_set_decode_sms(layer.handle, cap)
+        km = kernel_ms(layer, cb, dx, dy)
+        ms = km["attention"] + km["attn_merge"]
+        print(json.dumps({"kind": "decode_only", "workload": wl.name, "decode_sms": cap or "all",
+                          "ms": round(ms, 5), "gbs": round(by / (ms / 1e3) / 1e9, 1),
+                          "frac": round(by / (ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4)}), flush=True)
+    layer.close()
+
+    wl = W.llama3_8b_mixed()
+    layer, cb, dx, dy, batch = make(wl)
+    T = batch.num_tokens
+    for cap in (16, 24, 32, 48, 64, 88, 0):
+        mb.mb_layer_set_decode_sms(layer.handle, cap)
+        km = kernel_ms(layer, cb, dx, dy)
+        for _ in range(3):
+            layer.step(cb, dx, dy, s.cuda_stream)
+        n = 200
+        e0 = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        e1 = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        torch.cuda.synchronize()
+        for i in range(n):
+            flush.fill_(i & 0xFF)
+            e0[i].record(s)
+            layer.step(cb, dx, dy, s.cuda_stream)
+            e1[i].record(s)
+        torch.cuda.synchronize()
+        mb.mb_device_status(layer.handle, s.cuda_stream)
+        ms = sum(a.elapsed_time(b) for a, b in zip(e0, e1)) / n
+        print(json.dumps({"kind": "mixed_step", "workload": wl.name, "decode_sms": cap or "all (one grid)",
+                          "ms_per_step": round(ms, 5), "tokens_per_s": round(T / (ms / 1e3), 1),
+                          "attention_ms": round(km["attention"] + km["attn_merge"], 5)}), flush=True)
+    layer.close()
+
+
 def run_budget(args):
     """Budget selection on GB300 (pofe.ai "Chunked prefill", "Tuning knobs"):
     time the 32-layer Llama-3-8B-shaped stack over token budgets and decode
@@ -756,6 +829,8 @@ def main():
     ap.add_argument("--no-aux", action="store_true", help="skip the decode-only and 40-layer stack measurements")
     ap.add_argument("--sweep", action="store_true",
                     help="token-budget sweep on the 32-layer Llama-3-8B stack: one JSON line per point")
+    ap.add_argument("--partition", action="store_true",
+                    help="decode SM partition: decode-only bandwidth and the mixed step against the decode-SM cap")
     ap.add_argument("--budget", action="store_true",
                     help="budget selection: profile the stack, fit the step time, choose budgets, load-test them")
     args = ap.parse_args()
@@ -767,6 +842,9 @@ def main():
         return
     if args.budget:
         run_budget(args)
+        return
+    if args.partition:
+        run_partition(args)
         return
     if args.impl == "reference":
         run_reference(args, rank, world)

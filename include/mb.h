@@ -188,6 +188,14 @@ mb_status mb_layer_buffer(const mb_layer *layer, int32_t which, void **ptr, int6
  * steps timed.  It synchronises on the
  * recorded events. */
 mb_status mb_layer_set_timing(mb_layer *layer, int32_t enable);
+/* SM partition for decode attention: the attention launch runs at most n
+ * persistent decode-worker CTAs (one per SM), the prefill-chunk tiles and
+ * the rest of the GPU around them; 0 (the default) allows one per SM, so
+ * workers fill every SM the chunk tiles leave (ConfluxServe gives decode "just
+ * enough SMs" for most of its bandwidth; this is the knob that measures it).
+ * Takes effect at the next step (stacks re-capture their graphs).  Errors:
+ * MB_EINVAL for n < 0. */
+mb_status mb_layer_set_decode_sms(mb_layer *layer, int32_t n);
 mb_status mb_layer_timing(mb_layer *layer, double *ms, int32_t n, int64_t *steps);
 
 /* Number of kernel launches the last mb_step issued, and the bytes it copied

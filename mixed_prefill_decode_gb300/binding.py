@@ -91,6 +91,7 @@ _SIGS = {
     "mb_sched_pack": (_I32, [_VP, ctypes.POINTER(mb_sched_batch)]),
     "mb_sched_finish": (_I32, [_VP, _I64]),
     "mb_sched_set_adaptive": (_I32, [_VP, _I32, _I32, _I32, _I32]),
+    "mb_layer_set_decode_sms": (_I32, [_VP, _I32]),
     "mb_sample_greedy": (_I32, [_VP, _I32, _VP, _I32, _I32, ctypes.c_float, _VP, _VP, _I32, _VP, _VP, _VP, _VP]),
     "mb_embed": (_I32, [_VP, _I32, _I32, _VP, _I32, _VP, _VP]),
     "mb_sched_counts": (_I32, [_VP, c_int32_p]),
@@ -213,6 +214,10 @@ def mb_layer_buffer(layer: int, which: int):
 
 def mb_layer_set_timing(layer: int, enable: bool) -> None:
     _check(lib().mb_layer_set_timing(layer, 1 if enable else 0))
+
+
+def mb_layer_set_decode_sms(layer: int, n: int) -> None:
+    _check(lib().mb_layer_set_decode_sms(layer, n))
 
 
 def mb_layer_timing(layer: int):

@@ -199,6 +199,7 @@ struct mb_layer {
   int64_t last_upload = 0;
   // timing
   bool timing = false;
+  int32_t dec_sms = 0;   // decode worker CTAs at most (mb_layer_set_decode_sms; 0: one per SM)
   std::vector<EventSet> ev_pool;
   size_t ev_used = 0;
   double ms[kNumTimed] = {0};
@@ -214,9 +215,10 @@ struct GraphKey {
   int64_t T;
   int n_tiles, n_items, n_merge;
   const void *db, *part, *x_in, *x_out, *kv0;
+  int dec_sms;
   bool operator==(const GraphKey &o) const {
     return T == o.T && n_tiles == o.n_tiles && n_items == o.n_items && n_merge == o.n_merge && db == o.db &&
-           part == o.part && x_in == o.x_in && x_out == o.x_out && kv0 == o.kv0;
+           part == o.part && x_in == o.x_in && x_out == o.x_out && kv0 == o.kv0 && dec_sms == o.dec_sms;
   }
 };
 
@@ -553,6 +555,7 @@ mb_status launch_layer(mb_layer *L, mb_layer *W, mb_kv *kv, const StepPlan &P, c
   aa.part = W->part;
   aa.n_tiles = P.n_tiles;
   aa.n_items = P.n_items;
+  aa.max_workers = L->dec_sms;
   aa.T = Ti;
   aa.Hq = Hq;
   aa.Hkv = Hkv;
@@ -779,6 +782,13 @@ mb_status mb_layer_buffer(const mb_layer *L, int32_t which, void **ptr, int64_t 
   return MB_OK;
 }
 
+mb_status mb_layer_set_decode_sms(mb_layer *L, int32_t n) {
+  if (!L) return fail(MB_EINVAL, "mb_layer_set_decode_sms: null layer");
+  if (n < 0) return fail(MB_EINVAL, "mb_layer_set_decode_sms: n must be >= 0");
+  L->dec_sms = n;
+  return MB_OK;
+}
+
 mb_status mb_layer_set_timing(mb_layer *L, int32_t enable) {
   if (!L) return fail(MB_EINVAL, "mb_layer_set_timing: null layer");
   mb_status st = flush_timing(L);
@@ -994,7 +1004,10 @@ mb_status mb_stack_step(mb_stack *S, mb_kv *const *kvs, const mb_batch *b, const
   // Every launch of the L layers depends on the batch only through the
   // plan's sizes and the (fixed) buffers, so one captured graph serves every
   // step with the same geometry.
-  GraphKey key{T, plan.n_tiles, plan.n_items, plan.n_merge, plan.db, L0->part, x_in, x_out, kvs[0]};
+  uint32_t dec_sms_key = 0;   // every layer's decode SM cap (a change re-captures)
+  for (mb_layer *Li : S->layers) dec_sms_key = dec_sms_key * 31u + static_cast<uint32_t>(Li->dec_sms);
+  GraphKey key{T,  plan.n_tiles, plan.n_items, plan.n_merge, plan.db,           L0->part,
+               x_in, x_out,      kvs[0],       static_cast<int>(dec_sms_key)};
   auto enqueue = [&](int *launches) -> mb_status {
     for (int i = 0; i < nl; ++i) {
       const void *in = i == 0 ? x_in : S->act[(i - 1) & 1];

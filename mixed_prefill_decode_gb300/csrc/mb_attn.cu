@@ -1067,7 +1067,9 @@ cudaError_t attention_run(const AttnArgs &a, cudaStream_t st) {
   dp.err = a.err;
   dp.ctr = a.dec_ctr;
   dp.mctr = a.merge_ctr;
-  dp.n_workers = a.n_items < device_sm_count() ? a.n_items : device_sm_count();
+  const int sms = device_sm_count();
+  const int cap = a.max_workers > 0 && a.max_workers < sms ? a.max_workers : sms;
+  dp.n_workers = a.n_items < cap ? a.n_items : cap;
   const int G = a.Hq / a.Hkv;
   return a.hd == 128 ? launch_attention_g<128>(*a.tm_q, *a.tm_kv, *a.tm_qd, cp, dp, a.n_tiles, G, st)
                      : launch_attention_g<64>(*a.tm_q, *a.tm_kv, *a.tm_qd, cp, dp, a.n_tiles, G, st);

@@ -62,7 +62,7 @@ cudaError_t rope_append_run(const RopeArgs &a, cudaStream_t st);
 
 // ---- attention ----
 // Work lists (device int32, built on the host per step):
-//   chunk tiles:   {req, q_row0, q_head, 0} x n_tiles   (128 query rows each)
+//   chunk tiles:   {req, q_row0, q_head, 0} x n_tiles   (256 query rows each)
 //   decode items:  {req, kv_head, page_begin, page_end, split, n_splits, 0, 0} x n_items
 struct AttnArgs {
   const void *q;            // [T][Hq][hd] bf16 (rotated)
@@ -73,6 +73,7 @@ struct AttnArgs {
   const int32_t *items;     // decode item list
   float *part;              // decode split partials [n_items][Hq/Hkv group][hd + 4]: o, m, l, pad (merged in-kernel)
   int n_tiles, n_items;
+  int max_workers;          // decode worker CTAs at most (0: one per SM)
   int T, Hq, Hkv, hd, num_pages;
   int *err;
   const CUtensorMap *tm_q;  // Q map [T][Hq hd], box 64 x 128 (host pointer; copied into launch)

@@ -276,3 +276,31 @@ def test_many_repeats_bit_identical(mb, name):
         assert int(mismatches) == 0, f"{int(mismatches)} of 400 repeated steps differ from the first"
     finally:
         layer.close()
+
+
+@pytest.mark.parametrize("name,caps", [("llama3_8b_T576", (1, 5, 24, 0)), ("qwen3_14b_P2200", (3, 40, 0))])
+def test_decode_sm_cap_is_bit_identical(mb, name, caps):
+    """Capping the decode-worker CTAs (the decode SM partition) changes only
+    which worker takes which decode item, not what an item computes: every
+    cap gives the uncapped output bit for bit."""
+    wl = W.llama3_8b_mixed() if name.startswith("llama") else W.qwen3_14b_mixed(int(name.split("P")[1]))
+    wb, x, batch, pool = W.materialize(wl, unit_gains=True)
+    dw = {k: to_dev(v) for k, v in wb.items()}
+    dpool = to_dev(pool.reshape(-1))
+    layer = mb.Layer(wl.shape.as_dict(), dw, batch.num_tokens, pool.shape[0], kv_buf=dpool)
+    try:
+        cb = mb.Batch.of(batch)
+        dx = to_dev(x)
+        ref = torch.empty_like(dx)
+        layer.step(cb, dx, ref, _stream())
+        for cap in caps:
+            mb.mb_layer_set_decode_sms(layer.handle, cap)
+            dy = torch.empty_like(dx)
+            for _ in range(3):
+                layer.step(cb, dx, dy, _stream())
+            mb.mb_device_status(layer.handle, _stream())
+            assert torch.equal(dy.view(torch.int16), ref.view(torch.int16)), f"decode SM cap {cap}"
+        with pytest.raises(mb.MbError):
+            mb.mb_layer_set_decode_sms(layer.handle, -1)
+    finally:
+        layer.close()
