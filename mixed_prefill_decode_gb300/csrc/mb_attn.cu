@@ -772,10 +772,17 @@ __device__ __forceinline__ void decode_worker(const CUtensorMap &tmKV, const CUt
     }
   } else if (warp < 6) {
     // ---------------------------------------------- softmax / accumulation
+    // Per block, one barrier-OR asks whether any logit rose more than 2^8
+    // above its head's reference m; only then do the warps exchange the block
+    // maxima and move m (O and the sums rescaled by alpha).  Softmax does not
+    // depend on the reference, and every exponent stays <= 8, so P < 2^8.
+    // Each thread keeps its own partial sum of P; the 128 partials of a head
+    // are added once, when the item ends.
+    constexpr float kRescaleAbove = 8.f;     // log2 units
     const int q = warp & 3;
     const int t = q * 32 + lane;             // key of the block (S^T lane) and hd row (O^T lane)
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
-    float m[G], l[G], o[G], alpha_prev[G];
+    float m[G], l[G], o[G], alpha_prev[G];   // l: this thread's partial sum
     bool ok = true;
     for (int j = 0;; ++j) {
       const int s = j % C::STAGES;
@@ -785,6 +792,8 @@ __device__ __forceinline__ void decode_worker(const CUtensorMap &tmKV, const CUt
       bad = !mbar_wait(&s_full[j & 1], (j >> 1) & 1, abort_flag, p.err, kErrWaitSoftmax);
       bad = __any_sync(0xffffffffu, bad);
       float sv[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) sv[i] = 0.f;
       if (!bad) {
         tc_fence_after();
         tmem_ld16(tmem + lane_base + (j & 1) * 16, sv);
@@ -800,32 +809,41 @@ __device__ __forceinline__ void decode_worker(const CUtensorMap &tmKV, const CUt
         }
       }
       const bool valid = t < h.nvalid;
-      float sc[G], mx[G];
+      float sc[G], alpha[G];
+      bool grow = false;
 #pragma unroll
       for (int g = 0; g < G; ++g) {
         sc[g] = valid ? sv[g] * p.scale_log2 : -INFINITY;
-        mx[g] = sc[g];
+        grow |= sc[g] > m[g] + kRescaleAbove;   // always at an item's first block
+        alpha[g] = 1.f;
       }
+      if (named_bar_or(1, 128, bad || grow)) {
+        if (named_bar_or(1, 128, bad)) {
+          ok = false;
+          break;
+        }
+        float mx[G];
 #pragma unroll
-      for (int g = 0; g < G; ++g)
+        for (int g = 0; g < G; ++g) {
+          mx[g] = sc[g];
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) mx[g] = fmaxf(mx[g], __shfl_xor_sync(0xffffffffu, mx[g], off));
-      if (lane == 0)
+          for (int off = 16; off > 0; off >>= 1) mx[g] = fmaxf(mx[g], __shfl_xor_sync(0xffffffffu, mx[g], off));
+        }
+        if (lane == 0)
 #pragma unroll
-        for (int g = 0; g < G; ++g) red[q * 16 + g] = mx[g];
-      if (named_bar_or(1, 128, bad)) {
-        ok = false;
-        break;
+          for (int g = 0; g < G; ++g) red[q * 16 + g] = mx[g];
+        named_bar_sync(1, 128);
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          const float bm = fmaxf(fmaxf(red[g], red[16 + g]), fmaxf(red[32 + g], red[48 + g]));
+          const float mn = fmaxf(m[g], bm);
+          alpha[g] = (m[g] == -INFINITY) ? 0.f : ex2_approx(m[g] - mn);
+          m[g] = mn;
+        }
       }
-      float alpha[G], pr[G];
+      float pr[G];
 #pragma unroll
-      for (int g = 0; g < G; ++g) {
-        const float bm = fmaxf(fmaxf(red[g], red[16 + g]), fmaxf(red[32 + g], red[48 + g]));
-        const float mn = fmaxf(m[g], bm);
-        alpha[g] = (m[g] == -INFINITY) ? 0.f : exp2f(m[g] - mn);
-        m[g] = mn;
-        pr[g] = exp2f(sc[g] - mn);   // 0 for masked keys
-      }
+      for (int g = 0; g < G; ++g) pr[g] = ex2_approx(sc[g] - m[g]);   // 0 for masked keys
       // P^T[g][t] into the K-major 128-byte-swizzled B tile (two 64-key chunks)
       uint8_t *pt = sP + (j & 1) * C::PT + (t >> 6) * 2048;
 #pragma unroll
@@ -842,21 +860,8 @@ __device__ __forceinline__ void decode_worker(const CUtensorMap &tmKV, const CUt
       }
       fence_proxy_async_smem();
       mbar_arrive(&p_full[j & 1]);
-      // block sums per head
-      float sm[G];
 #pragma unroll
-      for (int g = 0; g < G; ++g) {
-        sm[g] = pr[g];
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) sm[g] += __shfl_xor_sync(0xffffffffu, sm[g], off);
-      }
-      if (lane == 0)
-#pragma unroll
-        for (int g = 0; g < G; ++g) red[64 + q * 16 + g] = sm[g];
-      named_bar_sync(1, 128);
-#pragma unroll
-      for (int g = 0; g < G; ++g)
-        l[g] = l[g] * alpha[g] + ((red[64 + g] + red[80 + g]) + (red[96 + g] + red[112 + g]));
+      for (int g = 0; g < G; ++g) l[g] = fmaf(l[g], alpha[g], pr[g]);
       // O^T_blk(i): row t = hd element t, column g = head.  Block j-1 is
       // folded in here, after this block's softmax, so that PV(j-1) ran
       // meanwhile; an item's last block is folded at once.
@@ -881,7 +886,19 @@ __device__ __forceinline__ void decode_worker(const CUtensorMap &tmKV, const CUt
       for (int g = 0; g < G; ++g) alpha_prev[g] = alpha[g];
       if (!(h.flags & 2)) continue;
       if (ok && !fold(j, alpha)) ok = false;
-      if (named_bar_or(1, 128, !ok)) break;   // all or none enter the barriers below
+      // the item's sums: the partials of the 128 threads, per head
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        float sw = l[g];
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) sw += __shfl_xor_sync(0xffffffffu, sw, off);
+        if (lane == 0) red[64 + q * 16 + g] = sw;
+      }
+      // all or none enter the barriers below; the barrier also publishes the sums
+      if (named_bar_or(1, 128, !ok)) break;
+      float lsum[G];
+#pragma unroll
+      for (int g = 0; g < G; ++g) lsum[g] = (red[64 + g] + red[80 + g]) + (red[96 + g] + red[112 + g]);
       // ---- the item is done: its output, or its split's partial
       const int32_t *it = p.items + h.item * 8;
       const int req = it[0], hk = it[1], sidx = it[4], n_splits = it[5], grp = it[6];
@@ -890,7 +907,7 @@ __device__ __forceinline__ void decode_worker(const CUtensorMap &tmKV, const CUt
         if (t < HD)
 #pragma unroll
           for (int g = 0; g < G; ++g)
-            p.o[(tok * p.Hq + hk * G + g) * HD + t] = __float2bfloat16_rn(o[g] / l[g]);
+            p.o[(tok * p.Hq + hk * G + g) * HD + t] = __float2bfloat16_rn(o[g] / lsum[g]);
         continue;
       }
       if (t < HD)
@@ -900,7 +917,7 @@ __device__ __forceinline__ void decode_worker(const CUtensorMap &tmKV, const CUt
           dst[t] = o[g];
           if (t == 0) {
             dst[HD] = m[g];
-            dst[HD + 1] = l[g];
+            dst[HD + 1] = lsum[g];
           }
         }
       // The last split of the (request, KV head) to finish merges all of its
