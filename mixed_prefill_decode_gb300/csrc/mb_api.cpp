@@ -113,9 +113,9 @@ static mb_status device_ctx(DeviceCtx **out) {
     cudaDeviceProp prop;
     e = cudaGetDeviceProperties(&prop, dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDeviceProperties");
-    if (prop.major != 10 || (prop.minor != 3 && prop.minor != 0))
-      return fail(MB_EUNSUPPORTED, "device %d is sm_%d%d; these kernels are built for sm_103a", dev, prop.major,
-                  prop.minor);
+    if (prop.major != 10 || prop.minor != 3)
+      return fail(MB_EUNSUPPORTED, "device %d is sm_%d%d; these kernels are built for sm_103a only", dev,
+                  prop.major, prop.minor);
     c.cc_major = prop.major;
     c.cc_minor = prop.minor;
     c.sms = prop.multiProcessorCount;
@@ -134,10 +134,12 @@ static mb_status device_ctx(DeviceCtx **out) {
   return MB_OK;
 }
 
+// SM count of the current device; every entry point has set up its context
+// (device_ctx) before launching, so the fallback is never taken there.
 int device_sm_count() {
   int dev = 0;
-  cudaGetDevice(&dev);
-  return g_dev[dev].sms > 0 ? g_dev[dev].sms : 148;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
+  return g_dev[dev].sms > 0 ? g_dev[dev].sms : 152;
 }
 
 }  // namespace mb
