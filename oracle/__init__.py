@@ -19,9 +19,14 @@ Parity status (what pins each part, tests in ``tests/test_oracle_*.py``):
   rms_norm    torch.nn.functional.rms_norm; scale invariance; constant rows
   linear      one-hot weights select the expected input column
   swiglu      silu closed form at 0 and large |x|; gate/up half order
-  layer       all-zero weights give y = x; composition of the pinned parts
-              (the pages print no worked layer output: beyond that, parity
-              unpinned)
+  layer       all-zero weights give y = x; one key gives h = x + v W_o^T; the
+              FFN half reads only h (two inputs with the same h give the same
+              y); q/k-norm per head before RoPE (closed form at a one-hot
+              row); chunked == unchunked and decode == last prefill row.  The
+              pages print no worked layer output, so no printed value pins it;
+              instead, 28 plausible mistakes planted in a copy of layer.py
+              each fail at least one of these pins
+              (tests/test_oracle_mutations.py)
   packer      the worked example of the pofe.ai page (8 x (64 + 512) at budget
               576) and brute-force invariants
 """

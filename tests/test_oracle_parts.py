@@ -175,3 +175,68 @@ def test_next_tokens_greedy_one_hot_and_ties():
     x2[0, 3] = 5.0
     _, ids2 = next_tokens_greedy(x2, [0], g, W, 1e-6)
     assert ids2[0] == 3             # tie with row 30: the lower index
+
+
+def test_ffn_half_reads_only_h():
+    """Two inputs with the same attention residual h give the same y.
+
+    With V = I, W_o = -1.5 I and one key per request (o = v), h = x - 1.5
+    RMSNorm(x).  For u with rms 1, x = u and x = -2u both give h = -0.5 u, so
+    the FFN half (RMSNorm(h), SwiGLU, down, residual h) must return the same
+    y for both.  An FFN that normalised x, or added x as its residual, would
+    not: the two inputs differ in sign and size."""
+    shape = W.TINY.as_dict()
+    shape["rms_eps"] = 0.0
+    d, Hq, Hkv, hd = shape["d_model"], shape["n_q_heads"], shape["n_kv_heads"], shape["head_dim"]
+    assert Hq == Hkv and Hkv * hd == d
+    w = L.weights_to_f64(W.make_weights(W.TINY, 11))
+    w["g_attn"] = np.ones(d)
+    w["w_qkv"][(Hq + Hkv) * hd:] = np.eye(d)
+    w["w_o"] = -1.5 * np.eye(d)
+    z = np.random.default_rng(12).standard_normal(d)
+    u = z / np.sqrt(np.mean(z * z))
+    x = np.stack([u, -2.0 * u])
+    pool = np.zeros((2, 2, Hkv, 16, hd))
+    r = L.layer_step(shape, w, pool, [0, 1, 2], [1, 1], [0, 1, 2], [0, 1], x)
+    np.testing.assert_allclose(r["h"], np.stack([-0.5 * u, -0.5 * u]), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(r["y"][0], r["y"][1], rtol=0, atol=1e-12)
+    assert np.max(np.abs(r["y"][0] - r["h"][0])) > 1e-3      # the FFN does contribute
+    # the miswirings named above would separate the two rows by this much
+    def ffn(t):
+        gu = L.linear(L.rms_norm(t, w["g_ffn"], 0.0), w["w_gate_up"])
+        return L.linear(L.silu(gu[:, :shape["d_ff"]]) * gu[:, shape["d_ff"]:], w["w_down"])
+    assert np.max(np.abs(ffn(x[:1]) - ffn(x[1:]))) > 1e-3
+
+
+def test_qk_norm_is_per_head_and_precedes_rope():
+    """Qwen3 q/k-norm: RMSNorm over head_dim with its gains, then RoPE.
+
+    x = e_0 and one-hot rows put sqrt(d) (up to eps) in element 0 of q head 0
+    and k head 0 only.  Norm per head gives sqrt(hd) * g[0] there; RoPE at
+    position p then moves it onto the pair (0, hd/2) as (cos p, sin p), both
+    scaled by g[0].  Rotating first would scale the sin term by g[hd/2];
+    normalising over all heads at once would give sqrt(Hq hd) instead."""
+    shape = W.SMALL_G5_QKN.as_dict()
+    d, Hq, Hkv, hd = shape["d_model"], shape["n_q_heads"], shape["n_kv_heads"], shape["head_dim"]
+    eps = shape["rms_eps"]
+    w = L.weights_to_f64(W.make_weights(W.SMALL_G5_QKN, 13))
+    w["g_attn"] = np.ones(d)
+    w["w_qkv"] = np.zeros_like(w["w_qkv"])
+    w["w_qkv"][0, 0] = 1.0               # q head 0, element 0
+    w["w_qkv"][Hq * hd, 0] = 1.0         # k head 0, element 0
+    g_q, g_k = np.ones(hd), np.ones(hd)
+    g_q[0], g_q[hd // 2] = 1.5, 0.5
+    g_k[0], g_k[hd // 2] = 0.75, 2.0
+    w["g_q"], w["g_k"] = g_q, g_k
+    x = np.zeros((1, d))
+    x[0, 0] = 1.0
+    p = 5                                # one decode after 5 cached tokens
+    pool = np.zeros((1, 2, Hkv, 16, hd))
+    r = L.layer_step(shape, w, pool, [0, 1], [p + 1], [0, 1], [0], x)
+    pre = 1.0 / math.sqrt(1.0 / d + eps)                 # element 0 after the input norm
+    mag = pre / math.sqrt(pre * pre / hd + eps)          # after the per-head norm
+    for got, g in ((r["q"][0, 0], g_q[0]), (pool[0, 0, 0, p], g_k[0])):
+        want = np.zeros(hd)
+        want[0], want[hd // 2] = g * mag * math.cos(p), g * mag * math.sin(p)
+        np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-12)
+    assert np.all(r["q"][0, 1:] == 0) and np.all(pool[0, 0, 1:, p] == 0)
