@@ -28,5 +28,8 @@ Parity status (what pins each part, tests in ``tests/test_oracle_*.py``):
               each fail at least one of these pins
               (tests/test_oracle_mutations.py)
   packer      the worked example of the pofe.ai page (8 x (64 + 512) at budget
-              576) and brute-force invariants
+              576), hand traces of the sequence limit, page exhaustion, the
+              free-list order and the adaptive size, and brute-force
+              invariants; 19 planted mistakes each fail one of them
+              (tests/test_oracle_mutations.py)
 """

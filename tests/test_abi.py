@@ -78,6 +78,48 @@ def test_native_packer_matches_oracle_bit_exactly(mb, seed):
         mb.mb_sched_destroy(s)
 
 
+# The hand-traced scripts of test_oracle_packer.py (sequence limit, a decode
+# skipped for want of a page, freed pages at the tail of the free list, the
+# adaptive size under a fixed cap), replayed on the native packer.
+HAND_TRACES = {
+    "max_seqs": ((100, 2, 0, range(64), None),
+                 [("add", 1, 10, 0), ("add", 2, 10, 0), ("add", 3, 10, 0), ("pack",), ("pack",), ("finish", 1),
+                  ("pack",)]),
+    "decode_without_page": ((10, 4, 0, range(2), None),
+                            [("add", 1, 16, 16), ("add", 2, 5, 5), ("pack",), ("finish", 2), ("pack",)]),
+    "free_list_tail": ((16, 4, 0, [2, 0, 1], None),
+                       [("add", 1, 16, 0), ("pack",), ("finish", 1), ("add", 2, 16, 0), ("pack",),
+                        ("add", 3, 32, 0), ("pack",)]),
+    "adaptive_under_cap": ((2048, 8, 100, range(200), (64, 256, 1024, 8)), [("add", 1, 500, 0), ("pack",)]),
+    "adaptive_one_decode": ((2048, 8, 1000, range(200), (64, 256, 1024, 8)),
+                            [("add", 1, 5, 5), ("add", 2, 500, 0), ("pack",)]),
+}
+
+
+@pytest.mark.parametrize("name", list(HAND_TRACES))
+def test_native_packer_hand_traces(mb, name):
+    (budget, max_seqs, cap, order, adaptive), ops = HAND_TRACES[name]
+    order = list(order)
+    py = Packer(budget, max_seqs, cap, order, adaptive=adaptive)
+    s = mb.mb_sched_create(budget, max_seqs, cap, np.asarray(order))
+    if adaptive:
+        mb.mb_sched_set_adaptive(s, *adaptive)
+    try:
+        for op in ops:
+            if op[0] == "add":
+                py.add(*op[1:])
+                mb.mb_sched_add(s, *op[1:])
+            elif op[0] == "finish":
+                py.finish(op[1])
+                mb.mb_sched_finish(s, op[1])
+            else:
+                qo, kv, bti, bt, ids = rows_to_csr(py.pack())
+                c = mb.mb_sched_pack(s)
+                assert [list(x) for x in c] == [qo, kv, bti, bt, ids]
+    finally:
+        mb.mb_sched_destroy(s)
+
+
 def test_native_packer_worked_example(mb):
     s = mb.mb_sched_create(576, 1000, 0, np.arange(20000))
     for i in range(64):

@@ -1,5 +1,5 @@
 """The oracle's pins have power: each plausible mistake planted in a copy of
-oracle/layer.py makes at least one CPU pin fail.
+oracle/layer.py or oracle/packer.py makes at least one CPU pin fail.
 
 Every case writes a scratch tree (the oracle with one edit, the oracle tests,
 a link to the package) under pytest's tmp_path and runs the pins there in a
@@ -14,7 +14,7 @@ import sys
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-PINS = ["test_oracle_attention.py", "test_oracle_parts.py"]
+PINS = {"layer": ["test_oracle_attention.py", "test_oracle_parts.py"], "packer": ["test_oracle_packer.py"]}
 
 # (mistake, text in oracle/layer.py, replacement)
 MUTATIONS = [
@@ -66,34 +66,77 @@ PAIRED = [
     ("attention before the append", [(_APPEND, "    pool0 = pool.copy()\n" + _APPEND),
                                      ("K, V = gather_kv(pool, table, n)", "K, V = gather_kv(pool0, table, n)")]),
 ]
-CASES = [(name, [(a, b)]) for name, a, b in MUTATIONS] + PAIRED
+CASES = [("layer", name, [(a, b)]) for name, a, b in MUTATIONS] + [("layer", n, e) for n, e in PAIRED]
+
+# Packer mistakes.  Not listed: ">" for ">=" at the pressure threshold of the
+# adaptive size, which is no mistake (the line already reaches the minimum
+# there, so both give the same size).
+_DEC_SKIP = "            if need > len(self.free):\n                continue\n            self._take(r, need)\n"
+PACKER = [
+    ("decodes ignore the budget", "            if left < 1:\n                break\n            need = pages_for",
+     "            need = pages_for"),
+    ("decode takes no page at a boundary", "need = pages_for(r.computed + 1) - len(r.pages)",
+     "need = pages_for(r.computed) - len(r.pages)"),
+    ("a decode without a page stops the others", _DEC_SKIP, _DEC_SKIP.replace("continue", "break")),
+    ("partial prefills last in, first out", "for r in list(self.partial):", "for r in reversed(list(self.partial)):"),
+    ("partial prefills ignore the cap",
+     "            n = min(left, r.prompt_len - r.computed)\n            if cap:\n                n = min(n, cap)",
+     "            n = min(left, r.prompt_len - r.computed)"),
+    ("partial prefills ignore their page room", "            n = min(n, room)\n", ""),
+    ("admission ignores the sequence limit",
+     "            if len(self.running) + len(self.partial) >= self.max_seqs:\n                break\n", ""),
+    ("sequence limit off by one", "if len(self.running) + len(self.partial) >= self.max_seqs:",
+     "if len(self.running) + len(self.partial) > self.max_seqs:"),
+    ("admission ignores the cap", "            n = min(left, r.prompt_len)\n            if cap:\n                n = min(n, cap)",
+     "            n = min(left, r.prompt_len)"),
+    ("admission page check off by one", "if pages_for(n) > len(self.free):\n                break",
+     "if pages_for(n) > len(self.free) + 1:\n                break"),
+    ("admission takes an extra page", "self._take(r, pages_for(n))", "self._take(r, pages_for(n + 1))"),
+    ("admission ignores the budget left", "n = min(left, r.prompt_len)", "n = r.prompt_len"),
+    ("adaptive size rounded, not truncated",
+     "chunk = int(base_chunk - (decodes / pressure) * (base_chunk - min_chunk))",
+     "chunk = round(base_chunk - (decodes / pressure) * (base_chunk - min_chunk))"),
+    ("adaptive size and cap combined by max", "cap = min(cap, eff) if cap else eff",
+     "cap = max(cap, eff) if cap else eff"),
+    ("adaptive size idle value is the base", "if decodes == 0:\n        return max_chunk",
+     "if decodes == 0:\n        return base_chunk"),
+    ("freed pages go to the head", "self.free.extend(r.pages)", "self.free.extendleft(reversed(r.pages))"),
+    ("freed pages reversed", "self.free.extend(r.pages)", "self.free.extend(reversed(r.pages))"),
+    ("prompt becomes a decode one step late", "if is_prefill and r.computed >= r.prompt_len:",
+     "if is_prefill and r.computed > r.prompt_len:"),
+    ("free list last in, first out", "r.pages.append(self.free.popleft())", "r.pages.append(self.free.pop())"),
+]
+CASES += [("packer", name, [(a, b)]) for name, a, b in PACKER]
 
 
-def _run_pins(tmp_path, edits):
-    src = open(os.path.join(ROOT, "oracle", "layer.py")).read()
+def _run_pins(tmp_path, module, edits):
+    src = open(os.path.join(ROOT, "oracle", module + ".py")).read()
     for a, b in edits:
         assert src.count(a) == 1, f"edit site not unique or gone: {a!r}"
         src = src.replace(a, b)
     tree = tmp_path / "tree"
     shutil.copytree(os.path.join(ROOT, "oracle"), tree / "oracle", ignore=shutil.ignore_patterns("__pycache__"))
-    (tree / "oracle" / "layer.py").write_text(src)
+    (tree / "oracle" / (module + ".py")).write_text(src)
     (tree / "tests").mkdir()
-    for f in ["conftest.py"] + PINS:
+    for f in ["conftest.py"] + PINS[module]:
         shutil.copy(os.path.join(ROOT, "tests", f), tree / "tests" / f)
+    shutil.copytree(os.path.join(ROOT, "tests", "golden"), tree / "tests" / "golden",
+                    ignore=shutil.ignore_patterns("__pycache__"))
     os.symlink(os.path.join(ROOT, "mixed_prefill_decode_gb300"), tree / "mixed_prefill_decode_gb300")
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider", "-m", "not gpu",
-                        *[os.path.join("tests", f) for f in PINS]], cwd=tree, capture_output=True, text=True,
+                        *[os.path.join("tests", f) for f in PINS[module]]], cwd=tree, capture_output=True, text=True,
                        timeout=600)
     return r
 
 
-def test_unedited_copy_passes(tmp_path):
-    r = _run_pins(tmp_path, [])
+@pytest.mark.parametrize("module", list(PINS))
+def test_unedited_copy_passes(tmp_path, module):
+    r = _run_pins(tmp_path, module, [])
     assert r.returncode == 0, r.stdout[-2000:]
 
 
-@pytest.mark.parametrize("name,edits", CASES, ids=[c[0] for c in CASES])
-def test_planted_mistake_fails_a_pin(tmp_path, name, edits):
-    r = _run_pins(tmp_path, edits)
+@pytest.mark.parametrize("module,name,edits", CASES, ids=[f"{c[0]}: {c[1]}" for c in CASES])
+def test_planted_mistake_fails_a_pin(tmp_path, module, name, edits):
+    r = _run_pins(tmp_path, module, edits)
     tail = r.stdout.strip().splitlines()[-1] if r.stdout.strip() else r.stderr[-500:]
     assert r.returncode == 1 and " failed" in tail, f"{name}: no pin failed ({tail})"

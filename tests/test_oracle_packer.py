@@ -168,3 +168,55 @@ def test_adaptive_cap_bounds_every_prefill_chunk():
         for rid, qo, kv, table in pk.pack():
             if rid not in running:
                 assert qo <= cap
+
+
+def test_max_seqs_alone_stops_admission():
+    # pages and budget to spare: only the sequence limit turns the third away
+    pk = Packer(budget=100, max_seqs=2, chunk_cap=0, free_order=range(64))
+    for rid in (1, 2, 3):
+        pk.add(rid, 10)
+    assert [(r[0], r[1]) for r in pk.pack()] == [(1, 10), (2, 10)]
+    assert [(r[0], r[1]) for r in pk.pack()] == [(1, 1), (2, 1)]      # still two sequences
+    pk.finish(1)
+    assert [(r[0], r[1]) for r in pk.pack()] == [(2, 1), (3, 10)]
+
+
+def test_decode_without_a_page_is_skipped_alone():
+    # request 1 sits on a page boundary (16 cached: its next token needs a
+    # second page), request 2 has room in its page; no page is free
+    pk = Packer(budget=10, max_seqs=4, chunk_cap=0, free_order=range(2))
+    pk.add(1, 16, computed=16)
+    pk.add(2, 5, computed=5)
+    assert len(pk.free) == 0
+    assert [(r[0], r[1], r[2]) for r in pk.pack()] == [(2, 1, 6)]
+    pk.finish(2)                                  # its page frees request 1
+    assert [(r[0], r[1], r[2], r[3]) for r in pk.pack()] == [(1, 1, 17, [0, 1])]
+
+
+def test_freed_pages_go_to_the_tail_of_the_free_list():
+    pk = Packer(budget=16, max_seqs=4, chunk_cap=0, free_order=[2, 0, 1])
+    pk.add(1, 16)
+    assert pk.pack()[0][3] == [2]
+    pk.finish(1)                                   # free list: 0, 1, 2
+    pk.add(2, 16)
+    assert pk.pack()[0][3] == [0]
+    pk.add(3, 32)
+    # 2's first decode crosses into a second page (1), then 3 takes the
+    # remaining 15 tokens of the budget on the last free page (2)
+    assert pk.pack() == [(2, 1, 17, [0, 1]), (3, 15, 15, [2])]
+
+
+def test_adaptive_size_truncates_and_combines_with_the_fixed_cap():
+    from oracle.packer import adaptive_chunk
+    # llm-stack-book 7.8 "Priority and Preemption Policies": the line value is
+    # truncated to an integer; 512 - (4/7) 384 = 292.57 -> 292
+    assert adaptive_chunk(4, 128, 512, 4096, 7) == 292
+    assert adaptive_chunk(2, 128, 512, 4096, 7) == 402     # 402.29
+    # with a fixed per-request cap as well, the smaller of the two applies
+    pk = Packer(budget=2048, max_seqs=8, chunk_cap=100, free_order=range(200), adaptive=(64, 256, 1024, 8))
+    pk.add(1, 500)
+    assert [(r[0], r[1]) for r in pk.pack()] == [(1, 100)]   # no decode: adaptive 1,024, cap 100
+    pk = Packer(budget=2048, max_seqs=8, chunk_cap=1000, free_order=range(200), adaptive=(64, 256, 1024, 8))
+    pk.add(1, 5, computed=5)
+    pk.add(2, 500)
+    assert [(r[0], r[1]) for r in pk.pack()] == [(1, 1), (2, 232)]   # one decode: 256 - 192/8, under cap 1,000
