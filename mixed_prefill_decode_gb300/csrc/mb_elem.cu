@@ -100,8 +100,10 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const __nv_bfloat
 // [Q heads | K heads | V heads].  Rotate-half pairing (i, i + hd/2) with
 // frequency theta^(-2i/hd) at the token's absolute position.  The angle is
 // pos * f with f split into a float head and tail (pos is exact in fp32), and
-// reduced modulo 2 pi with a two-constant Cody-Waite step before sincosf, so
-// it keeps ~1e-6 rad accuracy at positions in the tens of thousands.
+// reduced modulo 2 pi with a two-constant Cody-Waite step (W. J. Cody and
+// W. Waite, "Software Manual for the Elementary Functions", 1980: 2 pi split
+// into its fp32 value and the remainder) before sincosf is called, so it
+// keeps ~1e-6 rad accuracy at positions in the tens of thousands.
 constexpr int kRopeThreads = 256;
 constexpr float kTwoPiHi = 6.28318548202514648f;         // fp32(2 pi)
 constexpr float kTwoPiLo = -1.7484556000744893e-07f;     // 2 pi - kTwoPiHi
