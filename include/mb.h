@@ -318,6 +318,38 @@ mb_status mb_sched_set_adaptive(mb_sched *s, int32_t min_chunk, int32_t base_chu
 mb_status mb_sched_counts(const mb_sched *s, int32_t counts[4]);
 mb_status mb_sched_destroy(mb_sched *s);
 
+/* Checkpoint and resume of the packer.  Chunked prefill adds one piece of
+ * state per request: how many of its prompt tokens are already in the KV
+ * cache (pofe.ai "Chunked prefill", "How it works, step by step"; the
+ * num_computed field of the minimal scheduler in llm-stack-book 7.8, "A
+ * Minimal End-to-End Chunked Prefill Scheduler").  With each request's block
+ * table and the order of the queues and of the free list, that is all the
+ * later batches depend on.
+ *
+ * mb_sched_save writes the state of `s` as int64 words into `buf` (host,
+ * caller-owned, `cap` words) and sets *len to the number of words it needs;
+ * with buf == NULL and cap == 0 it only sets *len.  Layout (version 1):
+ *   0x4D4253434844 (magic), 1 (version), budget, max_seqs, chunk_cap,
+ *   num_pages, adaptive min, base, max and pressure (all 0 when off),
+ *   n_free, the free pages in hand-out order; then the running, partially
+ *   prefilled and waiting queues in turn: the queue's length and, per
+ *   request in queue order, id, prompt_len, computed, n_pages and its pages
+ *   in block-table order.
+ * The output arrays of the last mb_sched_pack are not part of the state.
+ * Errors: MB_EINVAL (null argument), MB_ENOSPACE (cap < *len; nothing written).
+ *
+ * mb_sched_load builds a new scheduler in *out (free it with
+ * mb_sched_destroy) from such words; it packs the same batches as the saved
+ * one would from the same calls on.  The state is checked whole: magic and
+ * version, a valid configuration, every page id in [0, num_pages) exactly
+ * once over the free list and the block tables, unique request ids, each
+ * request holding ceil(computed / 16) pages in the queue its progress implies
+ * (waiting: computed 0; partial: 0 < computed < prompt_len; running: computed
+ * >= prompt_len), and no words left over.  Errors: MB_EINVAL (a check fails;
+ * nothing is built), MB_ENOMEM. */
+mb_status mb_sched_save(const mb_sched *s, int64_t *buf, int64_t cap, int64_t *len);
+mb_status mb_sched_load(const int64_t *buf, int64_t len, mb_sched **out);
+
 const char *mb_last_error(void);
 
 #ifdef __cplusplus

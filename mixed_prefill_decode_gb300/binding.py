@@ -95,6 +95,8 @@ _SIGS = {
     "mb_sample_greedy": (_I32, [_VP, _I32, _VP, _I32, _I32, ctypes.c_float, _VP, _VP, _I32, _VP, _VP, _VP, _VP]),
     "mb_embed": (_I32, [_VP, _I32, _I32, _VP, _I32, _VP, _VP]),
     "mb_sched_counts": (_I32, [_VP, c_int32_p]),
+    "mb_sched_save": (_I32, [_VP, c_int64_p, _I64, c_int64_p]),
+    "mb_sched_load": (_I32, [c_int64_p, _I64, ctypes.POINTER(_VP)]),
     "mb_sched_destroy": (_I32, [_VP]),
     "mb_last_error": (ctypes.c_char_p, []),
 }
@@ -319,6 +321,23 @@ def mb_sched_counts(s: int):
     c = (ctypes.c_int32 * 4)()
     _check(lib().mb_sched_counts(s, c))
     return tuple(c)
+
+
+def mb_sched_save(s: int) -> np.ndarray:
+    """The packer's state as int64 words (layout in include/mb.h)."""
+    n = ctypes.c_int64()
+    _check(lib().mb_sched_save(s, None, 0, ctypes.byref(n)))
+    buf = np.zeros(max(1, n.value), dtype=np.int64)
+    _check(lib().mb_sched_save(s, buf.ctypes.data_as(c_int64_p), n.value, ctypes.byref(n)))
+    return buf[:n.value].copy()
+
+
+def mb_sched_load(words) -> int:
+    """A new scheduler from mb_sched_save's words."""
+    w = np.ascontiguousarray(np.asarray(words, dtype=np.int64))
+    h = _VP()
+    _check(lib().mb_sched_load(w.ctypes.data_as(c_int64_p), len(w), ctypes.byref(h)))
+    return h.value
 
 
 def mb_sched_destroy(s: int) -> None:

@@ -23,6 +23,12 @@ constexpr int32_t kPage = MB_PAGE_TOKENS;
 
 inline int32_t pages_for(int64_t tokens) { return static_cast<int32_t>((tokens + kPage - 1) / kPage); }
 
+// checkpoint words: magic, version, then budget, max_seqs, chunk_cap,
+// num_pages, the four adaptive settings and the free-list length
+constexpr int64_t kStateMagic = 0x4D4253434844;   // "MBSCHD"
+constexpr int64_t kStateVersion = 1;
+constexpr int64_t kStateHeaderWords = 11;
+
 struct Req {
   int64_t id;
   int32_t prompt_len;
@@ -238,6 +244,124 @@ mb_status mb_sched_counts(const mb_sched *s, int32_t counts[4]) {
   counts[1] = static_cast<int32_t>(s->running.size());
   counts[2] = static_cast<int32_t>(s->partial.size());
   counts[3] = static_cast<int32_t>(s->waiting.size());
+  return MB_OK;
+}
+
+// ---------------------------------------------------------------- checkpoint
+// The packer's whole state as int64 words (layout in include/mb.h beside
+// mb_sched_save).  Queue and free-list order are kept: they decide every
+// later batch.
+
+mb_status mb_sched_save(const mb_sched *s, int64_t *buf, int64_t cap, int64_t *len) {
+  if (!s || !len || cap < 0 || (cap > 0 && !buf)) return mb::fail(MB_EINVAL, "mb_sched_save: null argument");
+  int64_t need = kStateHeaderWords + static_cast<int64_t>(s->free_pages.size()) + 3;
+  for (const std::list<Req *> *q : {&s->running, &s->partial, &s->waiting})
+    for (const Req *r : *q) need += 4 + static_cast<int64_t>(r->pages.size());
+  *len = need;
+  if (!buf) return MB_OK;
+  if (cap < need)
+    return mb::fail(MB_ENOSPACE, "mb_sched_save: buffer holds %lld words, the state needs %lld",
+                    static_cast<long long>(cap), static_cast<long long>(need));
+  int64_t *w = buf;
+  *w++ = kStateMagic;
+  *w++ = kStateVersion;
+  *w++ = s->cfg.budget;
+  *w++ = s->cfg.max_seqs;
+  *w++ = s->cfg.chunk_cap;
+  *w++ = s->num_pages;
+  *w++ = s->ad_min;
+  *w++ = s->ad_base;
+  *w++ = s->ad_max;
+  *w++ = s->ad_pressure;
+  *w++ = static_cast<int64_t>(s->free_pages.size());
+  for (int32_t p : s->free_pages) *w++ = p;
+  for (const std::list<Req *> *q : {&s->running, &s->partial, &s->waiting}) {
+    *w++ = static_cast<int64_t>(q->size());
+    for (const Req *r : *q) {
+      *w++ = r->id;
+      *w++ = r->prompt_len;
+      *w++ = r->computed;
+      *w++ = static_cast<int64_t>(r->pages.size());
+      for (int32_t p : r->pages) *w++ = p;
+    }
+  }
+  return MB_OK;
+}
+
+mb_status mb_sched_load(const int64_t *buf, int64_t len, mb_sched **out) {
+  if (!buf || !out || len < kStateHeaderWords) return mb::fail(MB_EINVAL, "mb_sched_load: null or short state");
+  if (buf[0] != kStateMagic || buf[1] != kStateVersion)
+    return mb::fail(MB_EINVAL, "mb_sched_load: not a packer state of this version");
+  int64_t at = 2;
+  auto word = [&](int64_t lo, int64_t hi, int64_t *v) {
+    if (at >= len) return false;
+    *v = buf[at++];
+    return *v >= lo && *v <= hi;
+  };
+  int64_t budget, max_seqs, chunk_cap, num_pages, ad[4], n_free;
+  if (!word(1, INT32_MAX, &budget) || !word(1, INT32_MAX, &max_seqs) || !word(0, INT32_MAX, &chunk_cap) ||
+      !word(0, INT32_MAX, &num_pages) || !word(0, INT32_MAX, &ad[0]) || !word(0, INT32_MAX, &ad[1]) ||
+      !word(0, INT32_MAX, &ad[2]) || !word(0, INT32_MAX, &ad[3]) || !word(0, num_pages, &n_free))
+    return mb::fail(MB_EINVAL, "mb_sched_load: bad configuration words");
+  // every page appears once (free or in a table), so the words bound num_pages
+  if (num_pages > len - kStateHeaderWords - 3) return mb::fail(MB_EINVAL, "mb_sched_load: truncated state");
+  const bool ad_off = ad[0] == 0 && ad[1] == 0 && ad[2] == 0 && ad[3] == 0;
+  if (!ad_off && !(ad[0] >= 1 && ad[1] >= ad[0] && ad[2] >= ad[1] && ad[3] >= 1))
+    return mb::fail(MB_EINVAL, "mb_sched_load: bad adaptive chunk settings");
+  std::vector<char> seen(static_cast<size_t>(num_pages), 0);
+  auto page = [&](int32_t *p) {
+    int64_t v;
+    if (!word(0, num_pages - 1, &v) || seen[static_cast<size_t>(v)]) return false;
+    seen[static_cast<size_t>(v)] = 1;
+    *p = static_cast<int32_t>(v);
+    return true;
+  };
+  mb_sched *s = new (std::nothrow) mb_sched();
+  if (!s) return mb::fail(MB_ENOMEM, "mb_sched_load: out of host memory");
+  s->cfg = {static_cast<int32_t>(budget), static_cast<int32_t>(max_seqs), static_cast<int32_t>(chunk_cap)};
+  s->num_pages = static_cast<int32_t>(num_pages);
+  s->ad_min = static_cast<int32_t>(ad[0]);
+  s->ad_base = static_cast<int32_t>(ad[1]);
+  s->ad_max = static_cast<int32_t>(ad[2]);
+  s->ad_pressure = static_cast<int32_t>(ad[3]);
+  auto reject = [&](const char *what) {
+    delete s;
+    return mb::fail(MB_EINVAL, "mb_sched_load: %s", what);
+  };
+  for (int64_t i = 0; i < n_free; ++i) {
+    int32_t p;
+    if (!page(&p)) return reject("free list holds a page twice or out of range");
+    s->free_pages.push_back(p);
+  }
+  std::list<Req *> *queues[3] = {&s->running, &s->partial, &s->waiting};
+  for (int state = 2; state >= 0; --state) {   // running, partial, waiting
+    int64_t n;
+    if (!word(0, INT32_MAX, &n)) return reject("bad queue length");
+    for (int64_t i = 0; i < n; ++i) {
+      int64_t id, prompt_len, computed, np;
+      if (!word(INT64_MIN, INT64_MAX, &id) || !word(1, INT32_MAX, &prompt_len) ||
+          !word(0, (int64_t{1} << 40), &computed) || !word(0, num_pages, &np))
+        return reject("bad request words");
+      const bool fits = state == 0 ? computed == 0 : state == 1 ? computed > 0 && computed < prompt_len
+                                                                 : computed >= prompt_len;
+      if (!fits) return reject("a request's progress does not match its queue");
+      if (np != pages_for(computed)) return reject("a request does not hold ceil(computed / 16) pages");
+      if (s->by_id.count(id)) return reject("duplicate request id");
+      Req *r = new (std::nothrow) Req{id, static_cast<int32_t>(prompt_len), computed, {}, state};
+      if (!r) return reject("out of host memory");
+      s->by_id[id] = r;
+      queues[2 - state]->push_back(r);
+      for (int64_t k = 0; k < np; ++k) {
+        int32_t p;
+        if (!page(&p)) return reject("a block table holds a page twice or out of range");
+        r->pages.push_back(p);
+      }
+    }
+  }
+  if (at != len) return reject("trailing words after the state");
+  for (char c : seen)
+    if (!c) return reject("a page is neither free nor held by a request");
+  *out = s;
   return MB_OK;
 }
 

@@ -191,6 +191,45 @@ class Packer:
         return rows
 
 
+STATE_MAGIC = 0x4D4253434844
+STATE_VERSION = 1
+
+
+def state_words(pk: Packer) -> List[int]:
+    """The packer's state in the checkpoint layout of the C ABI: what the
+    later batches depend on, per request its id, prompt length, prefilled
+    count and block table (pofe.ai "How it works, step by step": the only new
+    state is the prefilled count; llm-stack-book 7.8's SequenceState keeps
+    num_computed), in queue order, and the free list in hand-out order."""
+    ad = pk.adaptive or (0, 0, 0, 0)
+    w = [STATE_MAGIC, STATE_VERSION, pk.budget, pk.max_seqs, pk.chunk_cap,
+         len(pk.free) + sum(len(r.pages) for r in pk.reqs.values()), *ad, len(pk.free), *pk.free]
+    for queue in (pk.running, pk.partial, list(pk.waiting)):
+        w.append(len(queue))
+        for r in queue:
+            w += [r.rid, r.prompt_len, r.computed, len(r.pages), *r.pages]
+    return [int(v) for v in w]
+
+
+def from_state_words(words: Sequence[int]) -> Packer:
+    """Inverse of state_words (trusted input: the checks live in the C ABI)."""
+    it = iter(int(v) for v in words)
+    assert next(it) == STATE_MAGIC and next(it) == STATE_VERSION
+    budget, max_seqs, chunk_cap, num_pages = next(it), next(it), next(it), next(it)
+    ad = tuple(next(it) for _ in range(4))
+    free = [next(it) for _ in range(next(it))]
+    pk = Packer(budget, max_seqs, chunk_cap, free, adaptive=None if ad == (0, 0, 0, 0) else ad)
+    for queue in (pk.running, pk.partial, pk.waiting):
+        for _ in range(next(it)):
+            rid, prompt_len, computed, n = next(it), next(it), next(it), next(it)
+            r = _Req(rid, prompt_len, computed)
+            r.pages = [next(it) for _ in range(n)]
+            pk.reqs[rid] = r
+            queue.append(r)
+    assert next(it, None) is None
+    return pk
+
+
 def rows_to_csr(rows):
     """(req_id, qo, kv, table) rows -> qo_indptr, kv_len, bt_indptr, bt, req_ids."""
     qo_indptr = [0]

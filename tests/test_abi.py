@@ -120,6 +120,120 @@ def test_native_packer_hand_traces(mb, name):
         mb.mb_sched_destroy(s)
 
 
+@pytest.mark.parametrize("seed", [3, 11, 17, 31, 35])
+def test_native_checkpoint_matches_oracle_and_resumes(mb, seed):
+    """Every 10 steps the native packer is replaced by one loaded from its own
+    checkpoint; the words equal the oracle's state words, and the batches
+    stay bit-identical to the oracle's for the whole stream."""
+    from oracle.packer import state_words
+    rng, P, budget, max_seqs, cap, order = _drive_both(seed)
+    adaptive = (8, 64, 256, 4) if seed >= 30 else None
+    py = Packer(budget, max_seqs, cap, order, adaptive=adaptive)
+    s = mb.mb_sched_create(budget, max_seqs, cap, order)
+    if adaptive:
+        mb.mb_sched_set_adaptive(s, *adaptive)
+    try:
+        nid = 0
+        for step in range(80):
+            if step % 10 == 9:
+                words = mb.mb_sched_save(s)
+                assert list(words) == state_words(py)
+                t = mb.mb_sched_load(words)
+                mb.mb_sched_destroy(s)
+                s = t
+                assert list(mb.mb_sched_save(s)) == list(words)
+            if rng.random() < 0.45:
+                plen = int(rng.integers(1, 500))
+                comp = int(rng.choice([0, 0, 0, int(rng.integers(0, plen + 40))]))
+                try:
+                    py.add(nid, plen, comp)
+                    ok_py = True
+                except Exception:
+                    ok_py = False
+                try:
+                    mb.mb_sched_add(s, nid, plen, comp)
+                    ok_c = True
+                except mb.MbError:
+                    ok_c = False
+                assert ok_py == ok_c
+                nid += 1
+            if py.reqs and rng.random() < 0.25:
+                rid = int(rng.choice(sorted(py.reqs)))
+                py.finish(rid)
+                mb.mb_sched_finish(s, rid)
+            qo, kv, bti, bt, ids = rows_to_csr(py.pack())
+            assert [list(x) for x in mb.mb_sched_pack(s)] == [qo, kv, bti, bt, ids]
+    finally:
+        mb.mb_sched_destroy(s)
+
+
+# A hand-made state: 6 pages; free 3, 4, 5; running request 1 (prompt 10,
+# 20 computed, pages 0, 1); partial request 2 (prompt 40, 16 computed, page
+# 2); waiting request 3 (prompt 9).
+GOOD_STATE = [0x4D4253434844, 1, 100, 4, 0, 6, 0, 0, 0, 0, 3, 3, 4, 5,
+              1, 1, 10, 20, 2, 0, 1,
+              1, 2, 40, 16, 1, 2,
+              1, 3, 9, 0, 0]
+
+
+def _edit(i, v):
+    w = list(GOOD_STATE)
+    w[i] = v
+    return w
+
+
+BAD_STATES = {
+    "magic": _edit(0, 0x4D4253434845),
+    "version": _edit(1, 2),
+    "budget 0": _edit(2, 0),
+    "adaptive half set": _edit(6, 5),
+    "truncated": GOOD_STATE[:-1],
+    "trailing word": GOOD_STATE + [0],
+    "free page twice": _edit(12, 3),
+    "page out of range": _edit(13, 6),
+    "page held by no one": _edit(5, 7),
+    "pages do not match computed": _edit(17, 40),
+    "partial request past its prompt": _edit(24, 40),
+    "waiting request with progress": _edit(30, 1),
+    "duplicate request id": _edit(22, 1),
+    "page in a table and free": _edit(26, 3),
+}
+
+
+def test_sched_load_accepts_a_valid_state_and_round_trips(mb):
+    s = mb.mb_sched_load(GOOD_STATE)
+    try:
+        assert list(mb.mb_sched_save(s)) == GOOD_STATE
+        assert mb.mb_sched_counts(s) == (3, 1, 1, 1)
+        qo, kv, bti, bt, ids = mb.mb_sched_pack(s)
+        # request 1 decodes (page 1 has room), 2 finishes its prompt with 24
+        # tokens (40 need pages 2, 3, 4), 3 is admitted with 9 tokens (page 5)
+        assert list(ids) == [1, 2, 3] and list(qo) == [0, 1, 25, 34] and list(kv) == [21, 40, 9]
+        assert list(bt) == [0, 1, 2, 3, 4, 5]
+    finally:
+        mb.mb_sched_destroy(s)
+
+
+@pytest.mark.parametrize("name", list(BAD_STATES))
+def test_sched_load_rejects_bad_states(mb, name):
+    with pytest.raises(mb.MbError) as e:
+        mb.mb_sched_load(BAD_STATES[name])
+    assert e.value.status == mb.MB_EINVAL
+
+
+def test_sched_save_reports_its_size_and_refuses_a_short_buffer(mb):
+    import ctypes
+    s = mb.mb_sched_load(GOOD_STATE)
+    try:
+        n = ctypes.c_int64()
+        assert mb.lib().mb_sched_save(s, None, 0, ctypes.byref(n)) == mb.MB_OK and n.value == len(GOOD_STATE)
+        buf = np.full(len(GOOD_STATE) - 1, -7, dtype=np.int64)
+        st = mb.lib().mb_sched_save(s, buf.ctypes.data_as(mb.c_int64_p), len(buf), ctypes.byref(n))
+        assert st == mb.MB_ENOSPACE and n.value == len(GOOD_STATE) and np.all(buf == -7)
+    finally:
+        mb.mb_sched_destroy(s)
+
+
 def test_native_packer_worked_example(mb):
     s = mb.mb_sched_create(576, 1000, 0, np.arange(20000))
     for i in range(64):

@@ -220,3 +220,17 @@ def test_adaptive_size_truncates_and_combines_with_the_fixed_cap():
     pk.add(1, 5, computed=5)
     pk.add(2, 500)
     assert [(r[0], r[1]) for r in pk.pack()] == [(1, 1), (2, 232)]   # one decode: 256 - 192/8, under cap 1,000
+
+
+@pytest.mark.parametrize("seed", range(5))
+def test_state_words_round_trip_and_resume(seed):
+    # a packer rebuilt from its state words packs exactly what the original does
+    from oracle.packer import state_words, from_state_words
+    stream = _random_stream(seed, steps=50)
+    for k, (pk, P, rows, before, running_before) in enumerate(stream):
+        if k in (10, 30):
+            words = state_words(pk)
+            twin = from_state_words(words)
+            assert state_words(twin) == words
+            for _ in range(5):
+                assert twin.pack() == pk.pack()
