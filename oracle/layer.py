@@ -55,24 +55,39 @@ def bf16_bits_to_f64(bits) -> np.ndarray:
 # --------------------------------------------------------------------------
 
 def rms_norm(x: np.ndarray, g: np.ndarray, eps: float) -> np.ndarray:
-    """x / sqrt(mean(x^2) + eps) * g over the last axis."""
+    """x / sqrt(mean(x^2) + eps) * g over the last axis.  The pages name the
+    Llama-3 / Qwen3 layers without writing their norm out; this is RMSNorm
+    as published (Zhang and Sennrich, "Root Mean Square Layer
+    Normalization", 2019), with the gain applied after the scaling."""
     ms = np.mean(x * x, axis=-1, keepdims=True)
     return x / np.sqrt(ms + eps) * g
 
 
 def linear(x: np.ndarray, w: np.ndarray) -> np.ndarray:
-    """y = x W^T with W stored row-major [N, K]."""
+    """y = x W^T with W stored row-major [N, K].  Every token of the mixed
+    batch, prefill or decode, is one row of the same product: a linear layer
+    applies the same weights to every token (ConfluxServe, "Why can linear
+    layers be batched but attention cannot?"; pofe.ai, "The bottleneck:
+    prefill-decode interference": the decodes are extra rows of the prefill's
+    matrix multiply)."""
     return x @ w.T
 
 
 def silu(x: np.ndarray) -> np.ndarray:
+    """x * sigmoid(x), the gate of the SwiGLU feed-forward block of Llama-3 /
+    Qwen3 layers (Shazeer, "GLU Variants Improve Transformer", 2020); the
+    pages name the block without writing it out."""
     return x / (1.0 + np.exp(-x))
 
 
 def rope(x: np.ndarray, pos: np.ndarray, theta: float) -> np.ndarray:
     """Rotate-half RoPE: element i pairs with i + hd/2, frequency
     theta^(-2i/hd), angle pos * frequency.  ``x`` is [..., hd]; ``pos``
-    broadcasts against x.shape[:-1]."""
+    broadcasts against x.shape[:-1].  The pages give only the position a
+    chunk's token takes (llm-stack-book 7.8, "Attention on Partial KV
+    Caches": query i of a chunk sits at T_past + i); the rotation is the
+    rotary embedding as published (Su et al., "RoFormer", 2021) in the
+    half-split pairing of Llama-3 / Qwen3 layers."""
     hd = x.shape[-1]
     half = hd // 2
     i = np.arange(half, dtype=np.float64)
@@ -84,13 +99,19 @@ def rope(x: np.ndarray, pos: np.ndarray, theta: float) -> np.ndarray:
 
 
 def page_slot(block_table: np.ndarray, p: int):
-    """Token p of a request lives in page block_table[p // 16], slot p % 16."""
+    """Token p of a request lives in page block_table[p // 16], slot p % 16:
+    the paged KV cache indexed through a per-request block table
+    (llm-stack-book 7.8, "Attention on Partial KV Caches"; pofe.ai, "How it
+    works, step by step": the chunk's keys are read partly from the paged
+    cache), with 16-token pages."""
     return int(block_table[p // PAGE_TOKENS]), p % PAGE_TOKENS
 
 
 def gather_kv(pool: np.ndarray, block_table: np.ndarray, n: int):
     """Keys and values 0..n-1 of one request, read through its block table.
-    pool is [P][2][Hkv][16][hd]; returns K, V as [n, Hkv, hd]."""
+    pool is [P][2][Hkv][16][hd] (heads before slots, the HND order of the
+    Perplexity page, "Gesharcde KV Cache Transfers"); returns K, V as
+    [n, Hkv, hd]."""
     p = np.arange(n)
     pages = block_table[p // PAGE_TOKENS]
     slots = p % PAGE_TOKENS
@@ -104,7 +125,11 @@ def attention_request(q: np.ndarray, K: np.ndarray, V: np.ndarray, cached: int) 
 
     q: [qo, Hq, hd] queries at positions cached + i;  K, V: [kv, Hkv, hd] with
     kv = cached + qo.  Query row i sees keys j <= cached + i.  Scale 1/sqrt(hd).
-    GQA: q head h reads KV head h // (Hq / Hkv).
+    GQA: q head h reads KV head h // (Hq / Hkv).  Follows llm-stack-book 7.8,
+    "Attention on Partial KV Caches" (the mask over the cached prefix plus the
+    chunk, and the scale) and its exercise 5 (GQA by repeating each KV head
+    over its group); a decode row is the case qo = 1 (Perplexity page,
+    "Prefill versus Decode-prestaties": qo_len 1 against a long kv_len).
     """
     qo, Hq, hd = q.shape
     kv, Hkv, _ = K.shape
