@@ -171,7 +171,10 @@ mb_status mb_stack_destroy(mb_stack *stack);
 mb_status mb_batch_validate(const mb_batch *batch, int32_t num_pages, int32_t max_tokens);
 
 /* Synchronise `stream` and report any error word the kernels recorded since
- * the last call (then clears it).  MB_EDEVICE if one was set. */
+ * the last call (then clears it).  MB_EDEVICE if one was set.  layer: that
+ * layer's steps; NULL: the standalone calls on the current device (mb_gemm,
+ * mb_sample_greedy, mb_embed and mb_gemm_noalloc).  With NULL it allocates
+ * nothing, so callers of mb_gemm_noalloc can use it too. */
 mb_status mb_device_status(mb_layer *layer, void *stream);
 
 /* Device pointer and byte size of an intermediate of the last step, for
@@ -219,6 +222,18 @@ mb_status mb_gemm(const void *A, const void *B, void *D, const void *R, int32_t 
                   int32_t K, int32_t epilogue, void *workspace, void *stream);
 int64_t mb_gemm_workspace_bytes(void);
 
+/* The GEMM's bounded wait in a K-split tile, for failure-path tests: the CTA
+ * holding the tile's first piece waits for the other pieces, at most
+ * limit_ns (<= 0: the default, 2 s).  phantom_pieces > 0 makes it also wait
+ * for that many pieces that no CTA writes, so the wait runs out every time
+ * (0, the default, for normal use).  When the limit runs out the kernel
+ * records an error and unwinds instead of waiting on; mb_device_status
+ * reports it as MB_EDEVICE and resets the tile tickets, and the next call
+ * computes normally.  Applies to GEMM launches issued after the call,
+ * process-wide (a stack's CUDA graph keeps what it was captured with).
+ * Errors: MB_EINVAL for phantom_pieces outside [0, 1024]. */
+mb_status mb_gemm_set_split_wait(int64_t limit_ns, int32_t phantom_pieces);
+
 /* The same GEMM for callers that cannot allocate device memory (code inside
  * an allocator's own hooks or out-of-memory path, processes whose device
  * memory is all handed out in advance, plugins limited to the buffers their
@@ -233,7 +248,10 @@ int64_t mb_gemm_workspace_bytes(void);
  * Every call shares the array and clears its tickets on `stream` first, so
  * calls that overlap on the GPU (unordered streams) race.  Shapes whose split
  * would need more scratch than the array holds are rejected with
- * MB_EUNSUPPORTED and a message giving both sizes.  Errors: as mb_gemm. */
+ * MB_EUNSUPPORTED and a message giving both sizes.  Errors: as mb_gemm for
+ * the arguments (sm_103 only); a device-side error (a bounded wait that gave
+ * up) stays in the array until mb_device_status(NULL, stream) reports it as
+ * MB_EDEVICE, clearing it and the tickets, without allocating. */
 mb_status mb_gemm_noalloc(const void *A, const void *B, void *D, const void *R, int32_t M, int32_t N,
                           int32_t K, int32_t epilogue, void *stream);
 

@@ -82,6 +82,7 @@ _SIGS = {
     "mb_gemm": (_I32, [_VP, _VP, _VP, _VP, _I32, _I32, _I32, _I32, _VP, _VP]),
     "mb_gemm_workspace_bytes": (_I64, []),
     "mb_gemm_noalloc": (_I32, [_VP, _VP, _VP, _VP, _I32, _I32, _I32, _I32, _VP]),
+    "mb_gemm_set_split_wait": (_I32, [_I64, _I32]),
     "mb_stack_create": (_I32, [ctypes.POINTER(_VP), _I32, _I32, ctypes.POINTER(_VP)]),
     "mb_stack_step": (_I32, [_VP, ctypes.POINTER(_VP), ctypes.POINTER(mb_batch), _VP, _VP, _VP]),
     "mb_stack_last_launches": (_I32, [_VP]),
@@ -243,6 +244,10 @@ def mb_gemm(A, B, D, R, M: int, N: int, K: int, epilogue: int, workspace=None, s
 
 def mb_gemm_noalloc(A, B, D, R, M: int, N: int, K: int, epilogue: int, stream=None) -> None:
     _check(lib().mb_gemm_noalloc(_ptr(A), _ptr(B), _ptr(D), _ptr(R), M, N, K, epilogue, _ptr(stream)))
+
+
+def mb_gemm_set_split_wait(limit_ns: int, phantom_pieces: int = 0) -> None:
+    _check(lib().mb_gemm_set_split_wait(int(limit_ns), int(phantom_pieces)))
 
 
 def mb_gemm_workspace_bytes() -> int:

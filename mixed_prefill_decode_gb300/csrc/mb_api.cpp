@@ -134,6 +134,15 @@ static mb_status device_ctx(DeviceCtx **out) {
   return MB_OK;
 }
 
+// The current device's context if an entry point has set it up already
+// (nullptr otherwise); allocates nothing.
+static DeviceCtx *device_ctx_if_ready() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  return g_dev[dev].gemm_ws ? &g_dev[dev] : nullptr;
+}
+
 // SM count of the current device; every entry point has set up its context
 // (device_ctx) before launching, so the fallback is never taken there.
 int device_sm_count() {
@@ -818,22 +827,36 @@ mb_status mb_device_status(mb_layer *L, void *stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) return fail(MB_ECUDA, "mb_device_status: %s", cudaGetErrorString(e));
-  int *errp = nullptr;
+  // A layer's context exists (its creation set it up).  Without a layer the
+  // call allocates nothing: it reads the context's word only if some entry
+  // point has set the context up, then the allocation-free GEMM's word.
   mb::DeviceCtx *ctx = nullptr;
-  mb_status st = mb::device_ctx(&ctx);
-  if (st != MB_OK) return st;
-  errp = L ? L->err : ctx->err;
-  int code = 0;
-  e = cudaMemcpy(&code, errp, sizeof code, cudaMemcpyDeviceToHost);
-  if (e != cudaSuccess) return fail(MB_ECUDA, "mb_device_status: %s", cudaGetErrorString(e));
-  if (code != 0) {
-    cudaMemset(errp, 0, 16);
-    // a decode worker that gave up may leave split-merge counters raised
-    if (L && L->part) cudaMemset(L->part, 0, L->part_cap * 4);
-    // a kernel that unwound early may leave stream-K tickets raised
-    cudaMemset(ctx->gemm_ws, 0, mb::gemm_workspace_bytes());
-    return fail(MB_EDEVICE, "mb_device_status: kernel error code %d", code);
+  if (L) {
+    mb_status st = mb::device_ctx(&ctx);
+    if (st != MB_OK) return st;
+  } else {
+    ctx = mb::device_ctx_if_ready();
   }
+  int code = 0;
+  if (ctx) {
+    int *errp = L ? L->err : ctx->err;
+    e = cudaMemcpy(&code, errp, sizeof code, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return fail(MB_ECUDA, "mb_device_status: %s", cudaGetErrorString(e));
+    if (code != 0) {
+      cudaMemset(errp, 0, 16);
+      // a decode worker that gave up may leave split-merge counters raised
+      if (L && L->part) cudaMemset(L->part, 0, L->part_cap * 4);
+      // a kernel that unwound early may leave stream-K tickets raised
+      cudaMemset(ctx->gemm_ws, 0, mb::gemm_workspace_bytes());
+    }
+  }
+  if (!L) {
+    int nc = 0;
+    e = mb::gemm_noalloc_take_error(&nc);
+    if (e != cudaSuccess) return fail(MB_ECUDA, "mb_device_status: %s", cudaGetErrorString(e));
+    if (code == 0) code = nc;
+  }
+  if (code != 0) return fail(MB_EDEVICE, "mb_device_status: kernel error code %d", code);
   return MB_OK;
 }
 

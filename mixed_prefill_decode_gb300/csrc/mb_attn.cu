@@ -1024,12 +1024,8 @@ __global__ void __launch_bounds__(FusedCfg<HD>::THREADS, 1)
 template <int HD, int G>
 cudaError_t launch_attention(const CUtensorMap &tq, const CUtensorMap &tkv, const CUtensorMap &tqd,
                              const ChunkParams &cp, const DecodeParams &dp, int n_tiles, cudaStream_t st) {
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(attention_kernel<HD, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    FusedCfg<HD>::SMEM);
-  });
+  const cudaError_t attr_err =
+      ensure_max_smem(reinterpret_cast<const void *>(attention_kernel<HD, G>), FusedCfg<HD>::SMEM);
   if (attr_err != cudaSuccess) return attr_err;
   return launch_pdl(attention_kernel<HD, G>, dim3(n_tiles + dp.n_workers), dim3(FusedCfg<HD>::THREADS),
                     FusedCfg<HD>::SMEM, st, 1, tq, tkv, tqd, cp, dp, n_tiles);

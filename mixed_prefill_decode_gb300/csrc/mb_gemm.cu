@@ -47,6 +47,7 @@
 
 #include <algorithm>
 #include <cstdint>
+#include <atomic>
 #include <cstdio>
 #include <mutex>
 
@@ -113,9 +114,6 @@ struct TileCfg {
 #define MB_GEMM_PREFETCH 8             // weight k-blocks fetched into L2 ahead of the ring
 #endif
 constexpr int kPrefetchAhead = MB_GEMM_PREFETCH;
-#ifndef MB_GEMM_MULTICAST
-#define MB_GEMM_MULTICAST 1            // 1: a group's CTAs form a cluster and share weight tiles by multicast
-#endif
 // Grouped schedule: split an N-tile along K over several groups only if that
 // takes at least this many K steps off each CTA; below it the stream-K fix-up
 // (partials out, the head piece waiting, partials back in) costs more than the
@@ -130,7 +128,7 @@ struct Params {
   int tiles_m, tiles_n;
   int grouped;          // 1: CTA (g, m) streams weight tiles of group g for M-tile m
   int n_groups;         // grouped: CTA groups (grid = n_groups * tiles_m)
-  int cluster;          // grouped with tiles_m > 1: a group is one cluster; B is multicast
+  int cluster;          // 2: CTA pairs (cluster of two SMs); 1 otherwise
   int dp_tiles, sk_tiles;
   int grid;
   __nv_bfloat16 *D;
@@ -141,6 +139,8 @@ struct Params {
   float *partials;      // [2 grid][NH halves][8 chunks][128 rows][32] fp32
   int *tickets;
   int *err;
+  uint64_t split_wait_ns;   // limit of the head piece's wait for the other pieces of its tile
+  int split_phantom;        // pieces the head also waits for that no CTA writes (failure-path tests; 0)
   // First (unit, k) iteration of each rank; rlo[ranks] = all iterations.
   // Filled on the host (fill_rank_bounds) so that no CTA divides 64-bit
   // numbers before its first load.
@@ -165,6 +165,11 @@ struct Seg {
 
 __host__ __device__ __forceinline__ int sk_ranks(const Params &p) { return p.grouped ? p.n_groups : p.grid; }
 __device__ __forceinline__ int rank_lo(const Params &p, int rank) { return p.rlo[rank]; }
+
+// The split fix-up's wait (mb_gemm_set_split_wait), read at launch: its time
+// limit and the phantom pieces that make it run out in failure-path tests.
+std::atomic<uint64_t> g_split_wait_ns{kWaitLimitNs};
+std::atomic<int> g_split_phantom{0};
 
 // Rank boundaries: rank r covers iterations [total r / R, total (r + 1) / R)
 // of the (unit, k) space.  False if the space does not fit 32-bit indices.
@@ -337,9 +342,8 @@ __global__ void __launch_bounds__(TileCfg<NH, PAIR>::THREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
-      // every CTA of a multicast cluster releases the stage; a pair's one MMA
-      // commit releases both CTAs' stages
-      mbar_init(&empty[s], PAIR ? 1 : p.cluster);
+      // one MMA commit releases the stage (a pair's releases both CTAs' stages)
+      mbar_init(&empty[s], 1);
     }
     for (int a = 0; a < C::NACC; ++a) {
       mbar_init(&tfull[a], 1);
@@ -365,10 +369,10 @@ __global__ void __launch_bounds__(TileCfg<NH, PAIR>::THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  // peers multicast into this CTA's stages and arrive on its barriers
+  // a pair's peer arrives on this CTA's barriers and its MMAs write this
+  // CTA's TMEM: both must be set up first
   if (p.cluster > 1) cluster_sync();
   const uint32_t crank = p.cluster > 1 ? cluster_ctarank() : 0;
-  const uint16_t cmask = static_cast<uint16_t>((1u << p.cluster) - 1u);
   const int sched_b = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
   // a pair's stage-full barriers live in rank 0 (cluster addresses)
   const uint32_t full_r0 = PAIR ? mapa_shared(smem_u32(full), 0) : 0u;
@@ -400,14 +404,8 @@ __global__ void __launch_bounds__(TileCfg<NH, PAIR>::THREADS, 1)
           continue;
         }
         mbar_arrive_expect_tx(&full[pre], stage_bytes(m0f, nh));
-        if (p.cluster == 1) {
-          tma_load_2d(sB + pre * B_STG, &tmB, &full[pre], kb * BK, rows0);
-          tma_load_2d(sB + pre * B_STG + B_STAGE / 2, &tmB, &full[pre], kb * BK, rows1);
-        } else if (crank == 0) {
-          tma_load_2d_mc(sB + pre * B_STG, &tmB, &full[pre], kb * BK, rows0, cmask);
-        } else if (crank == 1) {
-          tma_load_2d_mc(sB + pre * B_STG + B_STAGE / 2, &tmB, &full[pre], kb * BK, rows1, cmask);
-        }
+        tma_load_2d(sB + pre * B_STG, &tmB, &full[pre], kb * BK, rows0);
+        tma_load_2d(sB + pre * B_STG + B_STAGE / 2, &tmB, &full[pre], kb * BK, rows1);
       }
       // then warm L2 with the next k-blocks (a TMA instruction costs ~90
       // cycles to issue: the stage loads go first)
@@ -479,15 +477,9 @@ __global__ void __launch_bounds__(TileCfg<NH, PAIR>::THREADS, 1)
           if (!b_sent) mbar_arrive_expect_tx(&full[s], stage_bytes(m0, nh));
           tma_load_2d(sA + s * A_STAGE, &tmA, &full[s], kb * BK, m0);
           if (nh == 2) tma_load_2d(sA + s * A_STAGE + A_HALF, &tmA, &full[s], kb * BK, m0 + HM);
-          if (b_sent) {
-          } else if (p.cluster == 1) {
+          if (!b_sent) {
             tma_load_2d(sB + s * B_STG, &tmB, &full[s], kb * BK, rows0);
             tma_load_2d(sB + s * B_STG + B_STAGE / 2, &tmB, &full[s], kb * BK, rows1);
-          } else if (crank == 0) {
-            // the group's M-tiles share the weight tile: one read, delivered to all
-            tma_load_2d_mc(sB + s * B_STG, &tmB, &full[s], kb * BK, rows0, cmask);
-          } else if (crank == 1) {
-            tma_load_2d_mc(sB + s * B_STG + B_STAGE / 2, &tmB, &full[s], kb * BK, rows1, cmask);
           }
           issued_mask |= 1u << s;
           issued_ph = (issued_ph & ~(1u << s)) | (ph << s);
@@ -554,8 +546,6 @@ __global__ void __launch_bounds__(TileCfg<NH, PAIR>::THREADS, 1)
           }
           if (PAIR)
             mma_commit_pair(&empty[s], 3);
-          else if (p.cluster > 1)
-            mma_commit_mc(&empty[s], cmask);
           else
             mma_commit(&empty[s]);
           if (++s == STAGES) {
@@ -652,11 +642,11 @@ __global__ void __launch_bounds__(TileCfg<NH, PAIR>::THREADS, 1)
           // the head piece: wait for the other pieces (written early in their
           // ranks' timelines), fold them into the accumulator in TMEM
           if (ep == 0) {
-            const int want = r_last - r_first;
+            const int want = r_last - r_first + p.split_phantom;
             const uint64_t t0 = globaltimer();
             int spins = 0;
             while (ld_acquire_gpu(flag) < want) {
-              if ((++spins & 255) == 0 && globaltimer() - t0 > kWaitLimitNs) {
+              if ((++spins & 255) == 0 && globaltimer() - t0 > p.split_wait_ns) {
                 *abort_flag = 1;
                 atomicExch(p.err, kErrWaitEpilogue);
                 break;
@@ -759,8 +749,8 @@ __global__ void __launch_bounds__(TileCfg<NH, PAIR>::THREADS, 1)
   }
 
   __syncthreads();
-  // no CTA leaves while a peer may still multicast into it or arrive on it
-  // (a pair: rank 0's MMA issuer saw its last MMA complete before this)
+  // no CTA of a pair leaves while its peer may still arrive on it (rank 0's
+  // MMA issuer saw its last MMA complete before this)
   if (p.cluster > 1) cluster_sync();
   if (warp == 1) {
     __syncwarp();
@@ -775,12 +765,8 @@ __global__ void __launch_bounds__(TileCfg<NH, PAIR>::THREADS, 1)
 template <int EPI, int NH, bool PAIR = false>
 cudaError_t launch(const CUtensorMap &tmA, const CUtensorMap &tmB, const Params &p, cudaStream_t st) {
   using C = TileCfg<NH, PAIR>;
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(gemm_kernel<EPI, NH, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    C::SMEM_BYTES);
-  });
+  const cudaError_t attr_err =
+      ensure_max_smem(reinterpret_cast<const void *>(gemm_kernel<EPI, NH, PAIR>), C::SMEM_BYTES);
   if (attr_err != cudaSuccess) return attr_err;
   // a pair schedule's p.grid counts pairs
   return launch_pdl(gemm_kernel<EPI, NH, PAIR>, dim3(PAIR ? 2 * p.grid : p.grid), dim3(C::THREADS), C::SMEM_BYTES,
@@ -826,7 +812,7 @@ int max_clusters(int size) {
   std::lock_guard<std::mutex> lk(mu);
   if (size < 1 || size > 8) return 0;
   if (cache[size] == 0) {
-    cudaFuncSetAttribute(gemm_kernel<EPI, NH, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    ensure_max_smem(reinterpret_cast<const void *>(gemm_kernel<EPI, NH, PAIR>), C::SMEM_BYTES);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(size * 64);
     cfg.blockDim = dim3(C::THREADS);
@@ -843,14 +829,6 @@ int max_clusters(int size) {
     cache[size] = n;
   }
   return cache[size];
-}
-
-int max_clusters_for(int epi, int size) {
-  switch (epi) {
-    case kEpiStore: return max_clusters<kEpiStore, 1>(size);
-    case kEpiResidual: return max_clusters<kEpiResidual, 1>(size);
-    default: return max_clusters<kEpiSwiGLU, 1>(size);
-  }
 }
 
 // CTA pairs of the pair kernel that can be resident at once.
@@ -923,20 +901,6 @@ cudaError_t gemm_run(const void *A, const void *B, const CUtensorMap *tmB_pre, v
       if (p.k_iters - split_iters < kSplitMinSaving) groups = p.tiles_n;   // one whole N-tile per group
     }
     p.cluster = base_cluster;
-    // Multicast pays for 128-row tiles (more CTAs per weight tile), but
-    // clusters of tiles_m CTAs fit fewer groups on the GPCs (5-CTA clusters:
-    // 28 groups = 140 CTAs against 30).  Take it where those groups split the
-    // N-tiles evenly (no stream-K fix-up; Llama-3-8B gate/up at 576 tokens:
-    // 105 against 109 us), otherwise every SM without it (down: 70 against
-    // 74 us).  With 256-row tiles the cluster's lockstep costs more than it saves.
-    if (MB_GEMM_MULTICAST && nh == 1 && p.tiles_m > 1) {
-      const int mc = max_clusters_for(epi, p.tiles_m);
-      const long long mc_groups = groups > mc ? mc : groups;
-      if (mc > 0 && p.tiles_n % mc_groups == 0) {
-        p.cluster = p.tiles_m;
-        groups = mc_groups;
-      }
-    }
     const long long iters = static_cast<long long>(p.tiles_n) * p.k_iters;
     if (iters < 2 * groups) groups = iters / 2 > 0 ? iters / 2 : 1;  // at least two K steps per CTA
     p.grouped = 1;
@@ -971,6 +935,8 @@ cudaError_t gemm_run(const void *A, const void *B, const CUtensorMap *tmB_pre, v
   p.partials = ws.partials;
   p.tickets = ws.tickets;
   p.err = err;
+  p.split_wait_ns = g_split_wait_ns.load(std::memory_order_relaxed);
+  p.split_phantom = g_split_phantom.load(std::memory_order_relaxed);
   if (!fill_rank_bounds(p)) return cudaErrorInvalidValue;
   return launch_for(epi, nh, tmA, tmB, p, st);
 }
@@ -991,8 +957,12 @@ cudaError_t gemm_run(const void *A, const void *B, const CUtensorMap *tmB_pre, v
 // calls that overlap on the GPU (different streams without ordering) race.
 // The tickets are cleared on the call's stream before every launch; the
 // partial tiles need no clearing (every slot is written before it is read).
-// The stream-K part runs on at most kNoAllocGrid CTAs so that its partial
-// tiles fit; problems with at least one tile per SM run without any split.
+// The error word is cleared once, when the array's address is first looked
+// up on a device, and after that only by mb_device_status(NULL, stream),
+// which reports it; so a bounded wait that gave up in one call stays
+// visible after later calls.  The stream-K part runs on at most kNoAllocGrid
+// CTAs so that its partial tiles fit; problems with at least one tile per SM
+// run without any split.
 
 static __device__ __align__(256) uint8_t g_gemm_noalloc_scratch[(2u * 64u * 128u * 256u * 4u) + 4096u];
 
@@ -1002,13 +972,15 @@ namespace {
 constexpr int kNoAllocGrid = 64;
 constexpr size_t kNoAllocPartialBytes = static_cast<size_t>(2 * kNoAllocGrid) * TileCfg<1>::BM * BN * sizeof(float);
 constexpr size_t kNoAllocTailBytes = 4096;  // tickets, then the error word in the last 16 bytes
+constexpr size_t kNoAllocTicketBytes = kNoAllocTailBytes - 16;
 static_assert(sizeof(g_gemm_noalloc_scratch) == kNoAllocPartialBytes + kNoAllocTailBytes, "scratch layout");
 
 std::mutex g_noalloc_mu;
 void *g_noalloc_addr[64] = {};
 
 // Device address of the scratch array on the current device, looked up once
-// per device (host code only has a stand-in for the symbol).
+// per device (host code only has a stand-in for the symbol).  The first
+// lookup also clears the tail (tickets and error word), synchronously.
 cudaError_t noalloc_scratch(void **out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -1019,6 +991,8 @@ cudaError_t noalloc_scratch(void **out) {
     void *p = nullptr;
     e = cudaGetSymbolAddress(&p, g_gemm_noalloc_scratch);
     if (e != cudaSuccess) return e;
+    e = cudaMemset(static_cast<uint8_t *>(p) + kNoAllocPartialBytes, 0, kNoAllocTailBytes);
+    if (e != cudaSuccess) return e;
     g_noalloc_addr[dev] = p;
   }
   *out = g_noalloc_addr[dev];
@@ -1026,6 +1000,34 @@ cudaError_t noalloc_scratch(void **out) {
 }
 
 }  // namespace
+
+// Error code the allocation-free GEMM recorded on the current device since
+// the last call (0: none, or the array was never used here); a non-zero code
+// is cleared together with the tickets a kernel that gave up may have left
+// raised.  The caller has synchronised the streams that used it.
+cudaError_t gemm_noalloc_take_error(int *code) {
+  *code = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  uint8_t *base = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    base = static_cast<uint8_t *>(g_noalloc_addr[dev]);
+  }
+  if (!base) return cudaSuccess;
+  int word = 0;
+  e = cudaMemcpy(&word, base + kNoAllocPartialBytes + kNoAllocTicketBytes, sizeof word, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return e;
+  if (word != 0) {
+    e = cudaMemset(base + kNoAllocPartialBytes, 0, kNoAllocTailBytes);
+    if (e != cudaSuccess) return e;
+  }
+  *code = word;
+  return cudaSuccess;
+}
+
 }  // namespace mb
 
 extern "C" mb_status mb_gemm_noalloc(const void *A, const void *B, void *D, const void *R, int32_t M, int32_t N,
@@ -1047,9 +1049,10 @@ extern "C" mb_status mb_gemm_noalloc(const void *A, const void *B, void *D, cons
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
   if (e != cudaSuccess) return fail(MB_ECUDA, "mb_gemm_noalloc: %s", cudaGetErrorString(e));
-  if (major != 10 || (minor != 3 && minor != 0))
+  if (major != 10 || minor != 3)
     return fail(MB_EUNSUPPORTED, "mb_gemm_noalloc: device is sm_%d%d; these kernels are built for sm_103a", major,
                 minor);
+  if (sms > kMaxGemmGrid) sms = kMaxGemmGrid;
 
   Params p{};
   p.M = M;
@@ -1074,18 +1077,19 @@ extern "C" mb_status mb_gemm_noalloc(const void *A, const void *B, void *D, cons
   }
   const size_t need_partials = p.sk_tiles ? static_cast<size_t>(2 * p.grid) * TileCfg<1>::BM * BN * sizeof(float) : 0;
   const size_t need_tickets = static_cast<size_t>(p.sk_tiles) * sizeof(int);
-  if (need_partials > kNoAllocPartialBytes || need_tickets > kNoAllocTailBytes - 16)
+  if (need_partials > kNoAllocPartialBytes || need_tickets > kNoAllocTicketBytes)
     return fail(MB_EUNSUPPORTED,
                 "mb_gemm_noalloc: this shape needs %zu bytes of partial tiles and %zu of tickets; the static "
                 "scratch holds %zu and %zu",
-                need_partials, need_tickets, kNoAllocPartialBytes, kNoAllocTailBytes - 16);
+                need_partials, need_tickets, kNoAllocPartialBytes, kNoAllocTicketBytes);
 
   void *scratch = nullptr;
   e = noalloc_scratch(&scratch);
   if (e != cudaSuccess) return fail(MB_ECUDA, "mb_gemm_noalloc: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
   uint8_t *base = static_cast<uint8_t *>(scratch);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  e = cudaMemsetAsync(base + kNoAllocPartialBytes, 0, kNoAllocTailBytes, st);
+  // the tickets only: the error word keeps an earlier call's code until it is read
+  e = cudaMemsetAsync(base + kNoAllocPartialBytes, 0, kNoAllocTicketBytes, st);
   if (e != cudaSuccess) return fail(MB_ECUDA, "mb_gemm_noalloc: cudaMemsetAsync: %s", cudaGetErrorString(e));
 
   const int b_rows = epilogue == kEpiSwiGLU ? 2 * N : N;
@@ -1100,9 +1104,20 @@ extern "C" mb_status mb_gemm_noalloc(const void *A, const void *B, void *D, cons
   p.F = epilogue == kEpiSwiGLU ? N : 0;
   p.partials = reinterpret_cast<float *>(base);
   p.tickets = reinterpret_cast<int *>(base + kNoAllocPartialBytes);
-  p.err = reinterpret_cast<int *>(base + kNoAllocPartialBytes + kNoAllocTailBytes - 16);
+  p.err = reinterpret_cast<int *>(base + kNoAllocPartialBytes + kNoAllocTicketBytes);
+  p.split_wait_ns = g_split_wait_ns.load(std::memory_order_relaxed);
+  p.split_phantom = g_split_phantom.load(std::memory_order_relaxed);
   if (!fill_rank_bounds(p)) return fail(MB_EUNSUPPORTED, "mb_gemm_noalloc: too many (tile, K step) pairs");
   e = launch_for(epilogue, 1, tmA, tmB, p, st);   // 128-row tiles: their partials fit the array
   if (e != cudaSuccess) return fail(MB_ECUDA, "mb_gemm_noalloc: launch: %s", cudaGetErrorString(e));
+  return MB_OK;
+}
+
+extern "C" mb_status mb_gemm_set_split_wait(int64_t limit_ns, int32_t phantom_pieces) {
+  if (phantom_pieces < 0 || phantom_pieces > 1024)
+    return mb::fail(MB_EINVAL, "mb_gemm_set_split_wait: phantom_pieces must be in [0, 1024]");
+  mb::g_split_wait_ns.store(limit_ns > 0 ? static_cast<uint64_t>(limit_ns) : mb::dev::kWaitLimitNs,
+                            std::memory_order_relaxed);
+  mb::g_split_phantom.store(phantom_pieces, std::memory_order_relaxed);
   return MB_OK;
 }

@@ -34,6 +34,10 @@ GemmWorkspace gemm_workspace_carve(void *base);
 cudaError_t gemm_run(const void *A, const void *B, const CUtensorMap *tmB, void *D, const void *R, int M, int N,
                      int K, int epi, const GemmWorkspace &ws, int *err, cudaStream_t st);
 
+// Error code recorded by the allocation-free GEMM on the current device since
+// the last call (0 if none); a non-zero code is cleared.  Allocates nothing.
+cudaError_t gemm_noalloc_take_error(int *code);
+
 // ---- element-wise kernels ----
 cudaError_t rmsnorm_run(const void *x, const void *g, void *y, int rows, int d, float eps, cudaStream_t st);
 // y[i] = RMSNorm(x[rows[i]]) g for i < n_rows (rows: device int32, each in [0, n_src))

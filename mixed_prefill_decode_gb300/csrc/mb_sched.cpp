@@ -340,12 +340,13 @@ mb_status mb_sched_load(const int64_t *buf, int64_t len, mb_sched **out) {
     for (int64_t i = 0; i < n; ++i) {
       int64_t id, prompt_len, computed, np;
       if (!word(INT64_MIN, INT64_MAX, &id) || !word(1, INT32_MAX, &prompt_len) ||
-          !word(0, (int64_t{1} << 40), &computed) || !word(0, num_pages, &np))
+          !word(0, INT32_MAX, &computed) || !word(0, num_pages, &np))
         return reject("bad request words");
       const bool fits = state == 0 ? computed == 0 : state == 1 ? computed > 0 && computed < prompt_len
                                                                  : computed >= prompt_len;
       if (!fits) return reject("a request's progress does not match its queue");
-      if (np != pages_for(computed)) return reject("a request does not hold ceil(computed / 16) pages");
+      // in 64 bits: the page count of a large `computed` must not wrap
+      if (np != (computed + kPage - 1) / kPage) return reject("a request does not hold ceil(computed / 16) pages");
       if (s->by_id.count(id)) return reject("duplicate request id");
       Req *r = new (std::nothrow) Req{id, static_cast<int32_t>(prompt_len), computed, {}, state};
       if (!r) return reject("out of host memory");

@@ -197,6 +197,11 @@ BAD_STATES = {
     "waiting request with progress": _edit(30, 1),
     "duplicate request id": _edit(22, 1),
     "page in a table and free": _edit(26, 3),
+    # 2^40 cached tokens with an empty table: a 32-bit page count would wrap to 0
+    "computed past int32 with no pages": [GOOD_STATE[0], 1, 100, 4, 0, 6, 0, 0, 0, 0, 5, 0, 1, 3, 4, 5,
+                                          1, 1, 10, 1 << 40, 0,
+                                          1, 2, 40, 16, 1, 2,
+                                          1, 3, 9, 0, 0],
 }
 
 

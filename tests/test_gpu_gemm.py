@@ -25,6 +25,9 @@ SHAPES = [
     # pairs below 1,024 tokens (M mod 256 > 128): the second CTA of the last pair
     # tile holds 16, 60 and 104 rows
     (400, 768, 512), (700, 1536, 1024), (1000, 512, 256),
+    # grouped schedule with every N-tile split along K (the down projection at
+    # 576 tokens: 224 K steps over two groups)
+    (576, 4096, 14336),
 ]
 
 
@@ -70,3 +73,33 @@ def test_gemm_rejects_bad_shapes(mb):
         mb.mb_gemm(16, 16, 16, None, 128, 128, 60, 0)      # K % 64
     with pytest.raises(mb.MbError):
         mb.mb_gemm(16, 16, 16, None, 128, 100, 64, 2)      # F % 128
+
+
+def test_split_wait_expiry_reports_and_recovers(mb):
+    """The bounded wait of a K-split tile's head piece, made to run out (it
+    also waits for a piece that no CTA writes, with a 1 ms limit): the kernel
+    unwinds instead of hanging, mb_device_status reports MB_EDEVICE and resets
+    the tile tickets, and the GEMMs after it are correct with a clean status.
+    The down projection at 576 tokens splits every N-tile along K."""
+    M, N, K = 576, 4096, 14336
+    A, B, R = _inputs(M, N, K, 4242)
+    dA, dB, dR = to_dev(A), to_dev(B), to_dev(R)
+    dD = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    ref = OL.linear(f64(A), f64(B)) + f64(R)
+    mb.mb_gemm_set_split_wait(1_000_000, 1)
+    try:
+        for rep in range(2):
+            mb.mb_gemm(dA, dB, dD, dR, M, N, K, 1, None, s)
+            with pytest.raises(mb.MbError) as e:
+                mb.mb_device_status(None, s)
+            assert e.value.status == mb.MB_EDEVICE, f"expiry {rep}: status {e.value.status}"
+    finally:
+        mb.mb_gemm_set_split_wait(0, 0)
+    for rep in range(2):
+        dD.fill_(float("nan"))
+        mb.mb_gemm(dA, dB, dD, dR, M, N, K, 1, None, s)
+        mb.mb_device_status(None, s)
+        assert_close(f"after expiry {rep}", f64(from_dev(dD)), ref)
+    with pytest.raises(mb.MbError):
+        mb.mb_gemm_set_split_wait(0, -1)
