@@ -202,7 +202,8 @@ mb_status mb_layer_set_decode_sms(mb_layer *layer, int32_t n);
 mb_status mb_layer_timing(mb_layer *layer, double *ms, int32_t n, int64_t *steps);
 
 /* Number of kernel launches the last mb_step issued, and the bytes it copied
- * host to device (the descriptor and its work lists). */
+ * host to device (the descriptor and its work lists; for a stack, whose one
+ * upload per step goes through its first layer, the last mb_stack_step's). */
 int32_t mb_layer_last_launches(const mb_layer *layer);
 int64_t mb_layer_last_upload_bytes(const mb_layer *layer);
 

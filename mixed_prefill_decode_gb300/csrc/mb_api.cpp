@@ -1082,6 +1082,7 @@ mb_status mb_stack_step(mb_stack *S, mb_kv *const *kvs, const mb_batch *b, const
   }
   S->last_launches = launches;
   S->last_T = static_cast<int32_t>(T);
+  L0->last_upload = plan.upload_bytes;   // the stack's one descriptor upload goes through layer 0
   return MB_OK;
 }
 

@@ -289,6 +289,63 @@ def qwen3_14b_stack(prefix: int = 30720, seed: int = 4000, n_decodes: int = 96):
     return Workload(f"qwen3_14b_stack40_P{prefix}", QWEN3_14B, reqs, seed + prefix), 40
 
 
+@dataclasses.dataclass
+class PromptSweep:
+    """A long prompt fed through an n_layers stack as fixed-size chunks, one
+    chunk per step, beside running decodes (pofe.ai "Chunked prefill": the
+    scheduler gives a partial prompt the budget left after the decodes; the
+    prompt's prefix grows by one chunk per step).  The decodes' positions are
+    held from step to step (each rewrites its own slot), which leaves every
+    step's work unchanged.  ``layout`` places the whole prompt's pages once;
+    ``batch_at(k)`` is step k's descriptor: the decodes, then chunk k of the
+    prompt (qo = chunk, kv = (k + 1) chunk) reading the first pages of the
+    prompt's table."""
+    name: str
+    shape: LayerShape
+    n_layers: int
+    decodes: List[int]     # cached context of each decode
+    prompt: int
+    chunk: int
+    seed: int
+
+    @property
+    def steps(self) -> int:
+        return -(-self.prompt // self.chunk)
+
+    def layout(self, spare_pages: int = 4) -> Tuple[Batch, int]:
+        reqs = [(c, 1) for c in self.decodes] + [(0, self.prompt)]
+        return make_batch(reqs, self.seed + 1, spare_pages=spare_pages)
+
+    def batch_at(self, k: int, full: Batch, with_decodes: bool = True, with_chunk: bool = True) -> Batch:
+        n_dec = len(self.decodes)
+        rows = []
+        if with_decodes:
+            for r in range(n_dec):
+                kv = self.decodes[r] + 1
+                rows.append((1, kv, full.bt[full.bt_indptr[r]:full.bt_indptr[r] + pages_for(kv)]))
+        if with_chunk:
+            q0 = k * self.chunk
+            qo = min(self.chunk, self.prompt - q0)
+            kv = q0 + qo
+            rows.append((qo, kv, full.bt[full.bt_indptr[n_dec]:full.bt_indptr[n_dec] + pages_for(kv)]))
+        qo_indptr = np.cumsum([0] + [r[0] for r in rows]).astype(np.int32)
+        kv_len = np.array([r[1] for r in rows], dtype=np.int32)
+        bt_indptr = np.cumsum([0] + [len(r[2]) for r in rows]).astype(np.int32)
+        bt = np.concatenate([r[2] for r in rows]).astype(np.int32)
+        return Batch(qo_indptr, kv_len, bt_indptr, bt)
+
+
+def qwen3_14b_prompt_sweep(seed: int = 4000, n_decodes: int = 96, prompt: int = 32768, chunk: int = 2048):
+    """The 40-layer Qwen3-14B-shaped stack over a whole 32,768-token prompt fed
+    as 2,048-token chunks (prefix 0, 2,048, ..., 30,720) beside 96 decodes
+    with contexts log-uniform in [1024, 8192] (the same decodes as
+    qwen3_14b_stack)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    ctx = np.exp(rng.uniform(np.log(1024), np.log(8192), size=n_decodes)).astype(np.int64)
+    return PromptSweep(f"qwen3_14b_stack40_prompt{prompt}", QWEN3_14B, 40, [int(c) for c in ctx], prompt, chunk,
+                       seed + 77)
+
+
 def llama3_8b_stack(budget: int, n_decodes: int, seed: int = 5000):
     """32-layer Llama-3-8B-shaped stack for the token-budget sweep: n_decodes
     decodes with contexts log-uniform in [512, 32768] and one prefill chunk of

@@ -5,8 +5,11 @@
   graph replay after the descriptor's block tables changed.
 * A small stack matches the oracle composed over its layers.
 * The 40-layer Qwen3-14B-shaped stack with a 2,048-token chunk at prefix
-  30,720 and 96 decodes: its last layer matches the oracle fed the GPU's input
-  to that layer (per-layer check at full size)."""
+  30,720 and 96 decodes: layers 0, 19 and 39 match the oracle fed the GPU's
+  input to each (per-layer checks at full size), and the graph-replayed stack
+  equals the chained steps bit for bit at that size.
+* The 32-layer Llama-3-8B-shaped stack at the token-budget sweep's smallest
+  point, checked layer by layer."""
 
 import numpy as np
 import pytest
@@ -104,38 +107,76 @@ def test_stack_graph_replay_after_descriptor_change(mb):
             L.close()
 
 
-def test_qwen3_14b_stack40_last_layer_matches_oracle(mb):
-    wl, n_layers = W.qwen3_14b_stack(prefix=30720)
+def _chain_full_size(mb, wl, n_layers, weight_seed, pool_seed, check_layers):
+    """Run an n_layers stack of full-size layers (weights and KV drawn on the
+    device) as chained mb_step calls, keeping the input and output of the
+    layers in check_layers; then the same layers as one stack (CUDA graph)
+    must give the chain's output bit for bit.  Each checked layer is compared
+    with the oracle fed the GPU's bf16 input to that layer."""
     sh = wl.shape
     batch, num_pages = W.make_batch(wl.reqs, wl.seed + 1, spare_pages=4)
     x = W.make_embeddings(batch.num_tokens, sh.d_model, wl.seed + 2)
     layers, dws = [], []
+    errs = {}
     try:
         for l in range(n_layers):
-            dw = W.device_weights(sh, wl.seed + 100 + l)
-            dpool = W.device_kv_pool(sh, num_pages, wl.seed + 200 + l)
+            dw = W.device_weights(sh, weight_seed + l)
+            dpool = W.device_kv_pool(sh, num_pages, pool_seed + l)
             layers.append(mb.Layer(sh.as_dict(), dw, batch.num_tokens, num_pages, kv_buf=dpool))
             dws.append((dw, dpool))
-        last_pool_before = dws[-1][1].clone()
         cb = mb.Batch.of(batch)
-        dx = to_dev(x)
-        # input of the last layer: the first 39 layers as a stack
-        s39 = mb.mb_stack_create([L.handle for L in layers[:-1]], True)
-        s40 = mb.mb_stack_create([L.handle for L in layers], True)
+        cur = to_dev(x)
+        io = {}
+        for l, L in enumerate(layers):
+            out = torch.empty_like(cur)
+            L.step(cb, cur, out, _stream())
+            if l in check_layers:
+                io[l] = (from_dev(cur), None)
+                mb.mb_device_status(L.handle, _stream())
+                io[l] = (io[l][0], from_dev(out))
+            cur = out
+        mb.mb_device_status(layers[0].handle, _stream())
+        chain_out = from_dev(cur)
+        stack = mb.mb_stack_create([L.handle for L in layers], True)
         try:
-            x39 = torch.empty_like(dx)
-            mb.mb_stack_step(s39, [L.kv for L in layers[:-1]], cb, dx, x39, _stream())
-            y40 = torch.empty_like(dx)
-            mb.mb_stack_step(s40, [L.kv for L in layers], cb, dx, y40, _stream())
+            y = torch.empty_like(cur)
+            mb.mb_stack_step(stack, [L.kv for L in layers], cb, to_dev(x), y, _stream())
             mb.mb_device_status(layers[0].handle, _stream())
+            assert np.array_equal(from_dev(y), chain_out), "stack (graph) differs from the chained steps"
         finally:
-            mb.mb_stack_destroy(s39)
-            mb.mb_stack_destroy(s40)
-        wl_bits = {k: from_dev(v) for k, v in dws[-1][0].items()}
-        r = OL.layer_step(sh.as_dict(), OL.weights_to_f64(wl_bits), f64(from_dev(last_pool_before)),
-                          batch.qo_indptr, batch.kv_len, batch.bt_indptr, batch.bt, f64(from_dev(x39)))
-        e = assert_close("stack40 layer 39 y", f64(from_dev(y40)).reshape(r["y"].shape), r["y"])
-        print(f"stack40 last-layer error {e:.2e}, T={batch.num_tokens}")
+            mb.mb_stack_destroy(stack)
+        for l in sorted(check_layers):
+            xin, yout = io[l]
+            wbits = {k: from_dev(v) for k, v in dws[l][0].items()}
+            # the step's own slots are rewritten by the oracle before it attends;
+            # every other slot is as the layer found it
+            pool = f64(from_dev(dws[l][1]))
+            r = OL.layer_step(sh.as_dict(), OL.weights_to_f64(wbits), pool, batch.qo_indptr, batch.kv_len,
+                              batch.bt_indptr, batch.bt, f64(xin))
+            del pool
+            errs[l] = assert_close(f"{wl.name} layer {l} y", f64(yout).reshape(r["y"].shape), r["y"])
+        return batch, errs
     finally:
         for L in layers:
             L.close()
+
+
+def test_qwen3_14b_stack40_layers_match_oracle(mb):
+    """The 40-layer Qwen3-14B-shaped stack, a 2,048-token chunk after 30,720
+    cached tokens plus 96 decodes with contexts log-uniform in [1024, 8192]:
+    layers 0, 19 and 39 each match the oracle fed the GPU's input to that
+    layer, and the stack's graph equals the chained steps bit for bit."""
+    wl, n_layers = W.qwen3_14b_stack(prefix=30720)
+    batch, errs = _chain_full_size(mb, wl, n_layers, wl.seed + 100, wl.seed + 200, {0, 19, 39})
+    print(f"{wl.name}: T={batch.num_tokens}", {l: f"{e:.2e}" for l, e in errs.items()})
+
+
+def test_llama3_8b_stack32_smallest_sweep_point_layer_by_layer(mb):
+    """The 32-layer Llama-3-8B-shaped stack at the sweep's smallest point
+    (budget 256, one decode with a context log-uniform in [512, 32768] and a
+    255-token chunk after a prefix uniform in [0, 16384]): every layer matches
+    the oracle fed the GPU's input to it."""
+    wl, n_layers = W.llama3_8b_stack(256, 1)
+    batch, errs = _chain_full_size(mb, wl, n_layers, 5100, wl.seed + 200, set(range(n_layers)))
+    print(f"{wl.name}: T={batch.num_tokens}, kv={list(batch.kv_len)}",
+          f"max layer error {max(errs.values()):.2e}")
