@@ -1188,6 +1188,81 @@ def run_budget(args):
                           "goodput_rps": g, "points": pts}), flush=True)
 
 
+PROFILE_CASES = {
+    # one layer of the headline stack: the last chunk position (2,048 rows
+    # after 30,720 cached tokens) beside the 96 decodes, the chunk alone, and
+    # the decodes alone
+    "sweep_P30720": dict(k=15, decodes=True, chunk=True),
+    "chunk_P30720": dict(k=15, decodes=False, chunk=True),
+    "chunk_P14336": dict(k=7, decodes=False, chunk=True),
+    "sweep_decodes": dict(k=0, decodes=True, chunk=False),
+    # every position once per step (16 mb_step calls): one layer's share of
+    # each kernel over the whole prompt
+    "sweep_all": dict(k=None, decodes=True, chunk=True),
+}
+
+
+def run_case(args):
+    """One layer of the headline workload on one fixed batch, for profiling
+    (ncu) and quick timing: `--warmup` untimed steps, then `--steps` steps
+    with events around every launch (L2 flushed between steps); prints the
+    per-kernel mean times.  Under ncu, `-s <warmup * launches per step>`
+    skips the warm-up launches."""
+    import torch
+    from mixed_prefill_decode_gb300 import build as B
+    from mixed_prefill_decode_gb300 import binding as mb
+    B.build()
+    peaks, peak_kind = load_peaks()
+    spec = PROFILE_CASES[args.case]
+    sw = W.qwen3_14b_prompt_sweep()
+    sh = sw.shape
+    full, num_pages = sw.layout()
+    ks = range(sw.steps) if spec["k"] is None else [spec["k"]]
+    batches = [sw.batch_at(k, full, with_decodes=spec["decodes"], with_chunk=spec["chunk"]) for k in ks]
+    T = max(b.num_tokens for b in batches)
+    dw = W.device_weights(sh, sw.seed + 100)
+    dpool = W.device_kv_pool(sh, num_pages, sw.seed + 200)
+    layer = mb.Layer(sh.as_dict(), dw, T, num_pages, kv_buf=dpool)
+    cbs = [mb.Batch.of(b) for b in batches]
+    x = torch.randn((T, sh.d_model), device="cuda").to(torch.bfloat16)
+    y = torch.empty_like(x)
+    s = torch.cuda.current_stream().cuda_stream
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+
+    def one(i):
+        for cb in cbs:
+            flush.fill_(i & 0xFF)
+            layer.step(cb, x, y, s)
+
+    for i in range(args.warmup):
+        one(i)
+    mb.mb_device_status(layer.handle, s)
+    mb.mb_layer_set_timing(layer.handle, True)
+    for i in range(args.steps):
+        one(i)
+    torch.cuda.synchronize()
+    km, n = mb.mb_layer_timing(layer.handle)
+    mb.mb_device_status(layer.handle, s)
+    alg = {}
+    for b in batches:   # algorithmic work summed over the positions of one step
+        for name, (bound, wk) in algorithmic(sh, b).items():
+            if name not in alg:
+                alg[name] = (bound, wk)
+            elif bound == "mixed":
+                alg[name] = (bound, (alg[name][1][0] + wk[0], alg[name][1][1] + wk[1]))
+            else:
+                alg[name] = (bound, alg[name][1] + wk)
+    km_step = {k: v * len(batches) for k, v in km.items()}   # per pass over the positions
+    out = {"case": args.case, "tokens": sum(b.num_tokens for b in batches), "positions": len(batches),
+           "launches_per_step": mb.mb_layer_last_launches(layer.handle) * len(batches),
+           "kernels": kernel_table(alg, km_step, n, peaks)}
+    if not spec["decodes"] and spec["chunk"]:
+        fl = alg["attention"][1][0]
+        out["chunk_attention"] = {"flop": fl, "tflops": round(fl / (km_step["attention"] / n / 1e3) / 1e12, 1)}
+    print(json.dumps(out), flush=True)
+    layer.close()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -1204,7 +1279,12 @@ def main():
                     help="decode SM partition: decode-only bandwidth and the mixed step against the decode-SM cap")
     ap.add_argument("--budget", action="store_true",
                     help="budget selection: profile the stack, fit the step time, choose budgets, load-test them")
+    ap.add_argument("--case", choices=sorted(PROFILE_CASES),
+                    help="one layer of the headline workload on one fixed batch (profiling): per-kernel times")
     args = ap.parse_args()
+    if args.case:
+        run_case(args)
+        return
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
     rank, world, local, pg = dist_setup()

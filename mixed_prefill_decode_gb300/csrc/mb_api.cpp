@@ -222,14 +222,20 @@ struct mb_layer {
 
 
 // A stack of layers that share one batch descriptor per step.
+// Everything a captured step's launches take from the batch: the sizes, the
+// descriptor's section offsets (kernel arguments point into the blob) and the
+// buffers.  Batches with equal keys replay one graph; the graph reads the
+// descriptor's contents from the blob at run time.
 struct GraphKey {
   int64_t T;
-  int n_tiles, n_items, n_merge;
+  int n_reqs, n_tiles, n_items, n_merge;
+  size_t offs[8];
   const void *db, *part, *x_in, *x_out, *kv0;
   int dec_sms;
   bool operator==(const GraphKey &o) const {
-    return T == o.T && n_tiles == o.n_tiles && n_items == o.n_items && n_merge == o.n_merge && db == o.db &&
-           part == o.part && x_in == o.x_in && x_out == o.x_out && kv0 == o.kv0 && dec_sms == o.dec_sms;
+    return T == o.T && n_reqs == o.n_reqs && n_tiles == o.n_tiles && n_items == o.n_items &&
+           n_merge == o.n_merge && std::equal(offs, offs + 8, o.offs) && db == o.db && part == o.part &&
+           x_in == o.x_in && x_out == o.x_out && kv0 == o.kv0 && dec_sms == o.dec_sms;
   }
 };
 
@@ -365,16 +371,18 @@ mb_status prepare_step(mb_layer *L, const mb_batch *b, int64_t T, cudaStream_t s
   };
   StepPlan &P = *plan;
   P.T = T;
+  // Section order: everything whose size depends only on (n, T, tiles,
+  // items) first, the block tables (whose length changes with every prefix)
+  // last, so that batches of one geometry share every offset and a captured
+  // graph's kernel arguments stay valid for all of them.
   P.o_qo = sec(n + 1);
   P.o_kv = sec(n);
   P.o_bti = sec(n + 1);
-  P.o_bt = sec(static_cast<size_t>(nb));
   P.o_treq = sec(T);
   P.o_tpos = sec(T);
   std::copy(b->qo_indptr, b->qo_indptr + n + 1, hb.begin() + P.o_qo);
   std::copy(b->kv_len, b->kv_len + n, hb.begin() + P.o_kv);
   std::copy(b->bt_indptr, b->bt_indptr + n + 1, hb.begin() + P.o_bti);
-  std::copy(b->bt, b->bt + nb, hb.begin() + P.o_bt);
   for (int r = 0; r < n; ++r) {
     const int32_t t0 = b->qo_indptr[r], t1 = b->qo_indptr[r + 1];
     const int32_t c = b->kv_len[r] - (t1 - t0);
@@ -438,6 +446,8 @@ mb_status prepare_step(mb_layer *L, const mb_batch *b, int64_t T, cudaStream_t s
   }
   P.o_items = sec(items.size());
   std::copy(items.begin(), items.end(), hb.begin() + P.o_items);
+  P.o_bt = sec(static_cast<size_t>(nb));
+  std::copy(b->bt, b->bt + nb, hb.begin() + P.o_bt);
   P.n_tiles = static_cast<int>(tiles.size());
   P.n_items = static_cast<int>(items.size() / 8);
   P.n_merge = n_groups;
@@ -1031,8 +1041,21 @@ mb_status mb_stack_step(mb_stack *S, mb_kv *const *kvs, const mb_batch *b, const
   // step with the same geometry.
   uint32_t dec_sms_key = 0;   // every layer's decode SM cap (a change re-captures)
   for (mb_layer *Li : S->layers) dec_sms_key = dec_sms_key * 31u + static_cast<uint32_t>(Li->dec_sms);
-  GraphKey key{T,  plan.n_tiles, plan.n_items, plan.n_merge, plan.db,           L0->part,
-               x_in, x_out,      kvs[0],       static_cast<int>(dec_sms_key)};
+  GraphKey key{};
+  key.T = T;
+  key.n_reqs = b->num_reqs;
+  key.n_tiles = plan.n_tiles;
+  key.n_items = plan.n_items;
+  key.n_merge = plan.n_merge;
+  const size_t offs[8] = {plan.o_qo, plan.o_kv, plan.o_bti, plan.o_bt, plan.o_treq, plan.o_tpos, plan.o_tiles,
+                          plan.o_items};
+  std::copy(offs, offs + 8, key.offs);
+  key.db = plan.db;
+  key.part = L0->part;
+  key.x_in = x_in;
+  key.x_out = x_out;
+  key.kv0 = kvs[0];
+  key.dec_sms = static_cast<int>(dec_sms_key);
   auto enqueue = [&](int *launches) -> mb_status {
     for (int i = 0; i < nl; ++i) {
       const void *in = i == 0 ? x_in : S->act[(i - 1) & 1];

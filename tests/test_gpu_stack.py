@@ -107,6 +107,48 @@ def test_stack_graph_replay_after_descriptor_change(mb):
             L.close()
 
 
+def test_stack_graph_replay_over_a_growing_prefix(mb):
+    """A prompt fed chunk by chunk through a graph-replayed stack: every step
+    has the same geometry (decodes plus one 128-row chunk) but a longer block
+    table for the chunk; each step equals the chained mb_step calls on the
+    same descriptor bit for bit, and the last one matches the oracle."""
+    sh = W.SMALL_GQA
+    sw = W.PromptSweep("small_prompt", sh, 2, [40, 333, 900], 512, 128, 901)
+    full, num_pages = sw.layout(spare_pages=4)
+    pools0 = [W.make_kv_pool(sh, num_pages, full, 910 + l) for l in range(sw.n_layers)]
+    wbits = [W.make_weights(sh, 920 + l) for l in range(sw.n_layers)]
+    T = sw.batch_at(0, full).num_tokens
+
+    def make_layers():
+        out = []
+        for l in range(sw.n_layers):
+            dw = {k: to_dev(v) for k, v in wbits[l].items()}
+            out.append((mb.Layer(sh.as_dict(), dw, T, num_pages, kv_buf=to_dev(pools0[l].reshape(-1))), dw))
+        return out
+
+    chained, stacked = make_layers(), make_layers()
+    stack = mb.mb_stack_create([L.handle for L, _ in stacked], True)
+    try:
+        opools = [f64(p) for p in pools0]
+        for k in range(sw.steps):
+            b = sw.batch_at(k, full)
+            x = W.make_embeddings(T, sh.d_model, 930 + k)
+            want = _chain(mb, [L for L, _ in chained], b, x)
+            dy = torch.empty_like(to_dev(x))
+            mb.mb_stack_step(stack, [L.kv for L, _ in stacked], mb.Batch.of(b), to_dev(x), dy, _stream())
+            mb.mb_device_status(stacked[0][0].handle, _stream())
+            assert np.array_equal(from_dev(dy), want), f"graph replay at prefix {k * sw.chunk}"
+            h = f64(x)
+            for l in range(sw.n_layers):
+                h = OL.layer_step(sh.as_dict(), OL.weights_to_f64(wbits[l]), opools[l], b.qo_indptr, b.kv_len,
+                                  b.bt_indptr, b.bt, h)["y"]
+            assert_close(f"stack at prefix {k * sw.chunk}", f64(want).reshape(h.shape), h)
+    finally:
+        mb.mb_stack_destroy(stack)
+        for L, _ in chained + stacked:
+            L.close()
+
+
 def _chain_full_size(mb, wl, n_layers, weight_seed, pool_seed, check_layers):
     """Run an n_layers stack of full-size layers (weights and KV drawn on the
     device) as chained mb_step calls, keeping the input and output of the
