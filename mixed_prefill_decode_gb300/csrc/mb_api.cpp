@@ -12,6 +12,7 @@
 #include <cstring>
 #include <mutex>
 #include <new>
+#include <queue>
 #include <string>
 #include <vector>
 
@@ -202,8 +203,14 @@ struct mb_layer {
   int ring_next = 0;
   int32_t *dblob = nullptr;
   size_t dblob_cap = 0;
+  // Attention scratch: counters first (decode split groups, then split chunk
+  // tiles; every one is zero between launches, since the kernel that raises
+  // a counter lowers it), then the decode and chunk partials.  The counter
+  // region keeps its place and size until it must grow, so no step's
+  // counters ever land on an earlier step's partials.
   float *part = nullptr;
-  size_t part_cap = 0;  // floats
+  size_t part_cap = 0;  // floats, counters included
+  size_t ctr_cap = 0;   // 4-byte words of counters at the start
   // last step
   int32_t last_T = 0;
   int32_t last_launches = 0;
@@ -228,13 +235,15 @@ struct mb_layer {
 // descriptor's contents from the blob at run time.
 struct GraphKey {
   int64_t T;
-  int n_reqs, n_tiles, n_items, n_merge;
+  int n_reqs, n_tiles, n_items, n_merge, n_chunk_slots;
+  size_t ctr_cap;
   size_t offs[8];
   const void *db, *part, *x_in, *x_out, *kv0;
   int dec_sms;
   bool operator==(const GraphKey &o) const {
     return T == o.T && n_reqs == o.n_reqs && n_tiles == o.n_tiles && n_items == o.n_items &&
-           n_merge == o.n_merge && std::equal(offs, offs + 8, o.offs) && db == o.db && part == o.part &&
+           n_merge == o.n_merge && n_chunk_slots == o.n_chunk_slots && ctr_cap == o.ctr_cap &&
+           std::equal(offs, offs + 8, o.offs) && db == o.db && part == o.part &&
            x_in == o.x_in && x_out == o.x_out && kv0 == o.kv0 && dec_sms == o.dec_sms;
   }
 };
@@ -340,13 +349,123 @@ mb_status validate_batch(const mb_batch *b, int32_t num_pages, int32_t max_token
 }
 
 
+// A chunk tile: 256 query rows (qt = 1 or 2 query tiles of 128 rows with
+// rows in them) of one q-head, over nkb key blocks of 128.
+struct ChunkTile {
+  int32_t r, i0, h, nkb, qt;
+};
+// A unit of the attention launch's chunk work: key blocks [j0, j1) of a tile.
+struct ChunkUnit {
+  int32_t r, i0, h, j0, j1, piece, n_pieces, slot;
+  int64_t cost;
+};
+
+constexpr int32_t kMinPieceBlocks = 8;   // a piece covers at least 1,024 keys
+constexpr int64_t kUnitRamp = 2;         // a CTA's set-up, first loads and epilogue, in key blocks
+constexpr int64_t kPieceExtra = 2;       // a piece's partial round trip and share of the merge
+
+// Makespan of list scheduling: each unit, in order, to the processor that
+// frees first.  That is how CTAs launched in that order spread over the SMs
+// (one chunk CTA per SM).
+int64_t list_makespan(const std::vector<int64_t> &costs, int m) {
+  std::priority_queue<int64_t, std::vector<int64_t>, std::greater<int64_t>> q;
+  for (int i = 0; i < m; ++i) q.push(0);
+  int64_t span = 0;
+  for (int64_t c : costs) {
+    const int64_t t = q.top() + c;
+    q.pop();
+    q.push(t);
+    span = std::max(span, t);
+  }
+  return span;
+}
+
+// Chunk tiles cover the GPU in waves of one CTA per SM; when their count is
+// just past a multiple of the SM count, the last wave runs a few tiles on an
+// otherwise idle GPU (320 tiles of a 2,048-row chunk over 40 heads on 152
+// SMs: 2.1 waves).  A tile can be split along its keys into pieces whose
+// partial softmax states are merged by log-sum-exp (every piece but the last
+// covers keys that all of the tile's rows see; the last holds the diagonal).
+// Candidate plans: no split; the tiles of the last partial wave split so that
+// their pieces cover every SM; every tile in 2, 3 or 4 pieces.  The plan with
+// the shortest list-scheduling makespan (in key blocks, with a fixed cost per
+// CTA and per piece) wins; ties keep the plan with fewer units.  Units come
+// out heaviest first; the pieces of a split tile get consecutive partial
+// slots.  Returns the number of slots.
+int plan_chunk_units(std::vector<ChunkTile> tiles, int sms, std::vector<ChunkUnit> *out) {
+  out->clear();
+  if (tiles.empty()) return 0;
+  std::stable_sort(tiles.begin(), tiles.end(),
+                   [](const ChunkTile &x, const ChunkTile &y) { return x.nkb * x.qt > y.nkb * y.qt; });
+  const int n = static_cast<int>(tiles.size());
+  const int m = std::max(1, sms);
+  auto max_pieces = [](const ChunkTile &t) { return std::max(1, std::min(32, t.nkb / kMinPieceBlocks)); };
+  auto piece_lo = [](const ChunkTile &t, int p, int ns) {
+    return static_cast<int32_t>(static_cast<int64_t>(p) * t.nkb / ns);
+  };
+  auto build = [&](const std::vector<int> &ns, std::vector<ChunkUnit> *units) {
+    units->clear();
+    int slot = 0;
+    for (int i = 0; i < n; ++i) {
+      const ChunkTile &t = tiles[i];
+      if (ns[i] == 1) {
+        units->push_back({t.r, t.i0, t.h, 0, t.nkb, 0, 1, 0, static_cast<int64_t>(t.nkb) * t.qt + kUnitRamp});
+        continue;
+      }
+      for (int p = 0; p < ns[i]; ++p) {
+        const int32_t lo = piece_lo(t, p, ns[i]), hi = piece_lo(t, p + 1, ns[i]);
+        units->push_back({t.r, t.i0, t.h, lo, hi, p, ns[i], slot + p,
+                          static_cast<int64_t>(hi - lo) * t.qt + kUnitRamp + kPieceExtra});
+      }
+      slot += ns[i];
+    }
+    std::stable_sort(units->begin(), units->end(),
+                     [](const ChunkUnit &x, const ChunkUnit &y) { return x.cost > y.cost; });
+    return slot;
+  };
+  auto span_of = [&](const std::vector<int> &ns, size_t *count) {
+    std::vector<ChunkUnit> u;
+    build(ns, &u);
+    std::vector<int64_t> costs(u.size());
+    for (size_t i = 0; i < u.size(); ++i) costs[i] = u[i].cost;
+    *count = u.size();
+    return list_makespan(costs, m);
+  };
+  std::vector<std::vector<int>> plans;
+  plans.push_back(std::vector<int>(n, 1));
+  const int first_tail = (n / m) * m;
+  if (first_tail < n) {
+    std::vector<int> ns(n, 1);
+    const int s = (m + (n - first_tail) - 1) / (n - first_tail);
+    for (int i = first_tail; i < n; ++i) ns[i] = std::min(s, max_pieces(tiles[i]));
+    plans.push_back(ns);
+  }
+  for (int k = 2; k <= 4; ++k) {
+    std::vector<int> ns(n);
+    for (int i = 0; i < n; ++i) ns[i] = std::min(k, max_pieces(tiles[i]));
+    plans.push_back(ns);
+  }
+  size_t best = 0, best_count = 0;
+  int64_t best_span = span_of(plans[0], &best_count);
+  for (size_t k = 1; k < plans.size(); ++k) {
+    size_t count = 0;
+    const int64_t sp = span_of(plans[k], &count);
+    if (sp < best_span || (sp == best_span && count < best_count)) {
+      best = k;
+      best_span = sp;
+      best_count = count;
+    }
+  }
+  return build(plans[best], out);
+}
+
 // Device-side plan of one step: where the descriptor, per-token tables and
 // work lists live in the uploaded blob, and their sizes.
 struct StepPlan {
   int64_t T = 0;
   size_t o_qo = 0, o_kv = 0, o_bti = 0, o_bt = 0, o_treq = 0, o_tpos = 0, o_tiles = 0, o_items = 0;
-  int n_tiles = 0, n_items = 0, n_merge = 0;   // n_merge: (request, KV head) groups with several splits
-  size_t merge_off = 0;                        // their counters, in floats from the partials' base
+  int n_tiles = 0, n_items = 0, n_merge = 0;   // n_tiles: chunk units; n_merge: decode split groups
+  int n_chunk_slots = 0;                       // partial slots of split chunk tiles
   const int32_t *db = nullptr;
   int64_t upload_bytes = 0;
 };
@@ -391,30 +510,29 @@ mb_status prepare_step(mb_layer *L, const mb_batch *b, int64_t T, cudaStream_t s
       hb[P.o_tpos + t] = c + (t - t0);
     }
   }
-  // chunk tiles, heaviest first (rows x visible keys)
-  struct Tile {
-    int32_t r, i0, h;
-    int64_t work;
-  };
-  std::vector<Tile> tiles;
+  // chunk tiles: 256 query rows (two 128-row tiles) of one q-head each
+  std::vector<ChunkTile> tiles;
   int64_t dec_pages = 0;
   for (int r = 0; r < n; ++r) {
     const int32_t qo = b->qo_indptr[r + 1] - b->qo_indptr[r];
     if (qo > 1) {
       const int32_t c = b->kv_len[r] - qo;
-      // 256 query rows (two 128-row tiles) per chunk tile
-      for (int32_t i0 = 0; i0 < qo; i0 += 256)
-        for (int32_t hh = 0; hh < Hq; ++hh) tiles.push_back({r, i0, hh, static_cast<int64_t>(c + i0 + 256)});
+      for (int32_t i0 = 0; i0 < qo; i0 += 256) {
+        const int32_t rows = std::min(256, qo - i0);
+        const int32_t nkb = (c + i0 + rows - 1 + 128) / 128;
+        for (int32_t hh = 0; hh < Hq; ++hh) tiles.push_back({r, i0, hh, nkb, rows > 128 ? 2 : 1});
+      }
     } else {
       dec_pages += pages_for(b->kv_len[r]);
     }
   }
-  std::stable_sort(tiles.begin(), tiles.end(), [](const Tile &x, const Tile &y) { return x.work > y.work; });
-  P.o_tiles = sec(tiles.size() * 4);
-  for (size_t i = 0; i < tiles.size(); ++i) {
-    hb[P.o_tiles + 4 * i + 0] = tiles[i].r;
-    hb[P.o_tiles + 4 * i + 1] = tiles[i].i0;
-    hb[P.o_tiles + 4 * i + 2] = tiles[i].h;
+  std::vector<ChunkUnit> units;
+  P.n_chunk_slots = plan_chunk_units(tiles, ctx->sms, &units);
+  P.o_tiles = sec(units.size() * 8);
+  for (size_t i = 0; i < units.size(); ++i) {
+    const ChunkUnit &u = units[i];
+    const int32_t rec[8] = {u.r, u.i0, u.h, u.j0, u.j1, u.piece, u.n_pieces, u.slot};
+    std::copy(rec, rec + 8, hb.begin() + P.o_tiles + 8 * i);
   }
   // decode splits: about MB_DEC_ITEMS_PER_SM items per SM.  A request's
   // 128-key blocks (8 pages) are divided evenly among its splits, so only its
@@ -448,7 +566,7 @@ mb_status prepare_step(mb_layer *L, const mb_batch *b, int64_t T, cudaStream_t s
   std::copy(items.begin(), items.end(), hb.begin() + P.o_items);
   P.o_bt = sec(static_cast<size_t>(nb));
   std::copy(b->bt, b->bt + nb, hb.begin() + P.o_bt);
-  P.n_tiles = static_cast<int>(tiles.size());
+  P.n_tiles = static_cast<int>(units.size());
   P.n_items = static_cast<int>(items.size() / 8);
   P.n_merge = n_groups;
 
@@ -483,23 +601,27 @@ mb_status prepare_step(mb_layer *L, const mb_batch *b, int64_t T, cudaStream_t s
     }
     L->dblob_cap = cap;
   }
-  // decode split partials (rows of hd + 4 floats: o, m, l, pad), then one
-  // merge counter per split group; counters must start at zero
-  const size_t part_need = static_cast<size_t>(P.n_items) * G * (hd + 4) + static_cast<size_t>(P.n_merge);
-  if (L->part_cap < part_need) {
+  // attention scratch: counters (decode split groups, then split chunk
+  // tiles' slots), then decode split partials and chunk tile partials (rows
+  // of hd + 4 floats: o, m, l, pad); counters must start at zero
+  const size_t ctr_need = static_cast<size_t>(P.n_merge) + static_cast<size_t>(P.n_chunk_slots);
+  const size_t part_need = static_cast<size_t>(P.n_items) * G * (hd + 4) +
+                           static_cast<size_t>(P.n_chunk_slots) * 256 * (hd + 4);
+  if (L->ctr_cap < ctr_need || L->part_cap < L->ctr_cap + part_need) {
     cudaStreamSynchronize(s);
     if (L->part) cudaFree(L->part);
     L->part = nullptr;
-    size_t cap = part_need * 2;
-    st = alloc_dev(reinterpret_cast<void **>(&L->part), cap * 4, "decode partials");
+    const size_t ctr_cap = std::max<size_t>(std::max(L->ctr_cap, (ctr_need * 2 + 3) & ~size_t(3)), 64);
+    const size_t cap = ctr_cap + std::max(part_need * 2, L->part_cap > L->ctr_cap ? L->part_cap - L->ctr_cap : 0);
+    st = alloc_dev(reinterpret_cast<void **>(&L->part), cap * 4, "attention partials");
     if (st == MB_OK && cudaMemset(L->part, 0, cap * 4) != cudaSuccess) st = fail(MB_ECUDA, "cudaMemset(partials)");
     if (st != MB_OK) {
-      L->part_cap = 0;
+      L->part_cap = L->ctr_cap = 0;
       return st;
     }
     L->part_cap = cap;
+    L->ctr_cap = ctr_cap;
   }
-  P.merge_off = static_cast<size_t>(P.n_items) * G * (hd + 4);
   std::memcpy(slot.host, hb.data(), hb.size() * 4);
   e = cudaMemcpyAsync(L->dblob, slot.host, hb.size() * 4, cudaMemcpyHostToDevice, s);
   if (e != cudaSuccess) return mb::fail(MB_ECUDA, "step: descriptor upload: %s", cudaGetErrorString(e));
@@ -573,7 +695,6 @@ mb_status launch_layer(mb_layer *L, mb_layer *W, mb_kv *kv, const StepPlan &P, c
   aa.bt = db + P.o_bt;
   aa.tiles = db + P.o_tiles;
   aa.items = db + P.o_items;
-  aa.part = W->part;
   aa.n_tiles = P.n_tiles;
   aa.n_items = P.n_items;
   aa.max_workers = L->dec_sms;
@@ -587,7 +708,10 @@ mb_status launch_layer(mb_layer *L, mb_layer *W, mb_kv *kv, const StepPlan &P, c
   aa.tm_qd = &tm_qd;
   aa.tm_kv = &kv->tmap;
   aa.dec_ctr = W->err + 2;   // words 2-3 of the layer's error block
-  aa.merge_ctr = reinterpret_cast<int *>(W->part + P.merge_off);
+  aa.merge_ctr = reinterpret_cast<int *>(W->part);
+  aa.chunk_ctr = aa.merge_ctr + P.n_merge;
+  aa.part = W->part + W->ctr_cap;
+  aa.chunk_part = aa.part + static_cast<size_t>(P.n_items) * (Hq / Hkv) * (hd + 4);
   if ((st = chk(mb::attention_run(aa, s), "attention")) != MB_OK) return st;
   *launches += (aa.n_tiles + aa.n_items) > 0;
   mark(4);
@@ -1047,6 +1171,8 @@ mb_status mb_stack_step(mb_stack *S, mb_kv *const *kvs, const mb_batch *b, const
   key.n_tiles = plan.n_tiles;
   key.n_items = plan.n_items;
   key.n_merge = plan.n_merge;
+  key.n_chunk_slots = plan.n_chunk_slots;
+  key.ctr_cap = L0->ctr_cap;
   const size_t offs[8] = {plan.o_qo, plan.o_kv, plan.o_bti, plan.o_bt, plan.o_treq, plan.o_tpos, plan.o_tiles,
                           plan.o_items};
   std::copy(offs, offs + 8, key.offs);

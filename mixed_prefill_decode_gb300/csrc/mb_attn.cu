@@ -94,6 +94,8 @@ struct ChunkParams {
   int Hq, Hkv, num_pages;
   float scale_log2;
   int *err;
+  float *part;   // partials of split tiles: [slot][256 rows][hd + 4] (o, m, l, pad)
+  int *ctr;      // one counter per split tile: pieces finished (the merger resets it)
 };
 
 // One chunk tile (up to 256 query rows x one q-head); needs
@@ -118,27 +120,39 @@ __device__ __forceinline__ void chunk_tile(const CUtensorMap &tmQ, const CUtenso
   uint64_t *o_last = o_full + 2;           // every MMA of the tile done (committed once)
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(o_last + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-  static_assert((1 + 2 * C::NK + 2 * C::NV + 7) * 8 + 8 <= 256, "barrier area");
+  volatile int *merge_flag = reinterpret_cast<volatile int *>(tmem_slot + 2);
+  static_assert((1 + 2 * C::NK + 2 * C::NV + 7) * 8 + 12 <= 256, "barrier area");
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  const int req = p.tiles[tile * 4 + 0];
-  const int i0 = p.tiles[tile * 4 + 1];
-  const int h = p.tiles[tile * 4 + 2];
+  // work unit {req, row0, head, j0, j1, piece, n_pieces, slot}: key blocks
+  // [j0, j1) of the tile (all of them when n_pieces == 1)
+  const int32_t *unit = p.tiles + tile * 8;
+  const int req = unit[0];
+  const int i0 = unit[1];
+  const int h = unit[2];
+  const int j0 = unit[3];
+  const int n_pieces = unit[6];
+  const int slot = unit[7];
   const int t0 = p.qo_indptr[req];
   const int qo = p.qo_indptr[req + 1] - t0;
   const int kv = p.kv_len[req];
   const int cached = kv - qo;
   const int rows_valid = min(256, qo - i0);
   const int last_pos = cached + i0 + rows_valid - 1;
-  const int n_kb = (last_pos + 1 + 127) / 128;
-  // blocks each query tile needs (0: the tile has no rows)
-  int nkb_t[2];
+  const int n_kb = (last_pos + 1 + 127) / 128;   // the tile's blocks (all pieces)
+  const int j_end = min(unit[4], n_kb);          // this unit's blocks: [j0, j_end)
+  const int nb = j_end - j0;
+  // blocks each query tile needs (0: the tile has no rows), and where this
+  // unit's part of them ends (every row of a tile sees every key of a piece
+  // that is not the tile's last: only the last piece holds the diagonal)
+  int nkb_t[2], jt_end[2];
 #pragma unroll
   for (int t = 0; t < 2; ++t) {
     const int rows = min(128, rows_valid - 128 * t);
     nkb_t[t] = rows > 0 ? (cached + i0 + 128 * t + rows - 1 + 1 + 127) / 128 : 0;
+    jt_end[t] = min(nkb_t[t], j_end);
   }
   const int hk = h / (p.Hq / p.Hkv);
   const int32_t *table = p.bt + p.bt_indptr[req];
@@ -181,7 +195,7 @@ __device__ __forceinline__ void chunk_tile(const CUtensorMap &tmQ, const CUtenso
     // cycles a copy).  K runs NK - NV blocks ahead of V, the order in which
     // their slots free up.  Page ids: one per lane, loaded a block ahead.
     if (lane == 0) {
-      const int nq = nkb_t[1] > 0 ? 2 : 1;
+      const int nq = jt_end[1] > j0 ? 2 : 1;
       mbar_arrive_expect_tx(q_full, nq * C::QT_BYTES);
       for (int t = 0; t < nq; ++t)
         for (int c = 0; c < C::NH; ++c)
@@ -191,16 +205,18 @@ __device__ __forceinline__ void chunk_tile(const CUtensorMap &tmQ, const CUtenso
     const int n_pages = (last_pos + 1 + 15) / 16;
     auto page_of = [&](int blk) { return lane < 8 && 8 * blk + lane < n_pages ? table[8 * blk + lane] : 0; };
     // one ring: wait for the slot, arm it, 8 copies (lanes 0-7)
+    // blk: the block's index in the tile; rings count from the unit's first
     auto load_block = [&](bool is_v, int blk, int pg) -> bool {
       const int ns = is_v ? C::NV : C::NK;
-      const int st = blk % ns;
+      const int lb = blk - j0;
+      const int st = lb % ns;
       uint64_t *full = (is_v ? v_full : k_full) + st;
       uint64_t *empty = (is_v ? v_empty : k_empty) + st;
       const int key0 = 128 * blk;
       const int np = (min(key0 + 128, last_pos + 1) - key0 + 15) / 16;
       bool ok = true;
       if (lane == 0) {
-        ok = mbar_wait(empty, ((blk / ns) & 1) ^ 1, abort_flag, p.err, kErrWaitProducer);
+        ok = mbar_wait(empty, ((lb / ns) & 1) ^ 1, abort_flag, p.err, kErrWaitProducer);
         if (ok) mbar_arrive_expect_tx(full, np * C::NH * 2048);
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -217,10 +233,10 @@ __device__ __forceinline__ void chunk_tile(const CUtensorMap &tmQ, const CUtenso
     };
     bool ok = true;
     // each ring keeps its own page ids for its current and next block
-    int pk = page_of(0), pk_next = page_of(1), pv = pk, pv_next = pk_next;
-    int kb = 0, vb = 0;   // next K and V block to load
-    while (ok && vb < n_kb) {
-      if (kb < n_kb && kb <= vb + AHEAD) {
+    int pk = page_of(j0), pk_next = page_of(j0 + 1), pv = pk, pv_next = pk_next;
+    int kb = j0, vb = j0;   // next K and V block to load
+    while (ok && vb < j_end) {
+      if (kb < j_end && kb <= vb + AHEAD) {
         ok = load_block(false, kb, pk);
         ++kb;
         pk = pk_next;
@@ -236,10 +252,10 @@ __device__ __forceinline__ void chunk_tile(const CUtensorMap &tmQ, const CUtenso
       // let copies in flight land before the CTA exits (bounded), and the Q load
       const uint64_t t_start = globaltimer();
       if (!ok) {
-        for (int b = max(0, kb - C::NK); b < kb; ++b)
+        for (int b = max(0, kb - j0 - C::NK); b < kb - j0; ++b)
           while (!mbar_try_wait(smem_u32(&k_full[b % C::NK]), (b / C::NK) & 1) && globaltimer() - t_start < kWaitLimitNs) {
           }
-        for (int b = max(0, vb - C::NV); b < vb; ++b)
+        for (int b = max(0, vb - j0 - C::NV); b < vb - j0; ++b)
           while (!mbar_try_wait(smem_u32(&v_full[b % C::NV]), (b / C::NV) & 1) && globaltimer() - t_start < kWaitLimitNs) {
           }
       }
@@ -249,10 +265,11 @@ __device__ __forceinline__ void chunk_tile(const CUtensorMap &tmQ, const CUtenso
   } else if (warp == 1) {
     if (lane == 0) {
       // ------------------------------------------------------- MMA issuer
+      // j: the block's index in the tile; stages and phases count from j0
       auto issue_s = [&](int t, int j) {
         const uint32_t d = tmem + 128 * t;
         const uint32_t q0 = smem_u32(sQ + t * C::QT_BYTES);
-        const uint32_t k0 = smem_u32(sK + (j % C::NK) * C::KV_BYTES);
+        const uint32_t k0 = smem_u32(sK + ((j - j0) % C::NK) * C::KV_BYTES);
 #pragma unroll
         for (int c = 0; c < C::NH; ++c)
 #pragma unroll
@@ -264,46 +281,47 @@ __device__ __forceinline__ void chunk_tile(const CUtensorMap &tmQ, const CUtenso
         mma_commit(&s_full[t]);
       };
       auto issue_pv = [&](int t, int j) {
-        const uint32_t vbase = smem_u32(sV + (j % C::NV) * C::KV_BYTES);
+        const uint32_t vbase = smem_u32(sV + ((j - j0) % C::NV) * C::KV_BYTES);
         // P_t(j) sits in TMEM over S_t(j): 128 keys as 64 columns of bf16 pairs
         const uint32_t pcol = tmem + 128 * t;
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {  // 16 keys (two atoms) per MMA; hd halves 1 KB apart
           const uint64_t bd = sdesc_sw128(vbase + ks * 2 * C::ATOM_STRIDE, 1024, C::ATOM_STRIDE);
-          mma_bf16_ts(tmem + C::O_COL + HD * t, pcol + ks * 8, bd, C::IDESC_PV, (j > 0 || ks > 0) ? 1u : 0u);
+          mma_bf16_ts(tmem + C::O_COL + HD * t, pcol + ks * 8, bd, C::IDESC_PV, (j > j0 || ks > 0) ? 1u : 0u);
         }
         // the last PV of a tile is covered by the o_last commit after the loop
-        if (j + 1 < nkb_t[t]) mma_commit(&o_full[t]);
+        if (j + 1 < jt_end[t]) mma_commit(&o_full[t]);
       };
       auto wait = [&](uint64_t *bar, uint32_t par) { return mbar_wait(bar, par, abort_flag, p.err, kErrWaitMma); };
       // the last tile that reads block j (tile 1 reads every block it needs,
       // and needs at least the blocks of tile 0 when it has rows)
-      auto last_tile = [&](int j) { return j < nkb_t[1] ? 1 : 0; };
+      auto last_tile = [&](int j) { return j < jt_end[1] ? 1 : 0; };
       bool ok = wait(q_full, 0) && wait(&k_full[0], 0);
       if (ok) {
         tc_fence_after();
         for (int t = 0; t < 2; ++t)
-          if (nkb_t[t] > 0) issue_s(t, 0);
-        if (C::NK < n_kb) mma_commit(&k_empty[0]);
+          if (jt_end[t] > j0) issue_s(t, j0);
+        if (C::NK < nb) mma_commit(&k_empty[0]);
       }
       // Block j: PV_0(j), S_0(j+1), PV_1(j), S_1(j+1); a tile that needs no
       // more blocks drops out.  A K block is released after the last S that
       // reads it, a V block after the last PV.
-      for (int j = 0; j < n_kb && ok; ++j) {
-        ok = wait(&v_full[j % C::NV], (j / C::NV) & 1);
+      for (int j = j0; j < j_end && ok; ++j) {
+        const int lj = j - j0;
+        ok = wait(&v_full[lj % C::NV], (lj / C::NV) & 1);
         for (int t = 0; t < 2 && ok; ++t) {
-          if (j >= nkb_t[t]) continue;
-          ok = wait(&p_full[t], j & 1);
+          if (j >= jt_end[t]) continue;
+          ok = wait(&p_full[t], lj & 1);
           if (!ok) break;
           tc_fence_after();
           issue_pv(t, j);
-          if (t == last_tile(j) && j + C::NV < n_kb) mma_commit(&v_empty[j % C::NV]);
-          if (j + 1 < nkb_t[t]) {
-            ok = wait(&k_full[(j + 1) % C::NK], ((j + 1) / C::NK) & 1);
+          if (t == last_tile(j) && lj + C::NV < nb) mma_commit(&v_empty[lj % C::NV]);
+          if (j + 1 < jt_end[t]) {
+            ok = wait(&k_full[(lj + 1) % C::NK], ((lj + 1) / C::NK) & 1);
             if (!ok) break;
             tc_fence_after();
             issue_s(t, j + 1);
-            if (t == last_tile(j + 1) && j + 1 + C::NK < n_kb) mma_commit(&k_empty[(j + 1) % C::NK]);
+            if (t == last_tile(j + 1) && lj + 1 + C::NK < nb) mma_commit(&k_empty[(lj + 1) % C::NK]);
           }
         }
       }
@@ -329,8 +347,9 @@ __device__ __forceinline__ void chunk_tile(const CUtensorMap &tmQ, const CUtenso
     const int zero_t = nkb_t[0] == n_kb ? 0 : 1;   // the tile whose WG zeroes stale V rows
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
-    for (int j = 0; j < nkb_t[t]; ++j) {
-      bool bad = !ok || !mbar_wait(&s_full[t], j & 1, abort_flag, p.err, kErrWaitSoftmax);
+    for (int j = j0; j < jt_end[t]; ++j) {
+      const int lj = j - j0;   // phases and stages count from the unit's first block
+      bool bad = !ok || !mbar_wait(&s_full[t], lj & 1, abort_flag, p.err, kErrWaitSoftmax);
       bad = __any_sync(0xffffffffu, bad);   // tcgen05.ld below is warp-collective
       if (bad) {
         ok = false;
@@ -374,9 +393,9 @@ __device__ __forceinline__ void chunk_tile(const CUtensorMap &tmQ, const CUtenso
       }
       const float mx = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3)) * scale;
       const bool grow = (m_ref == -INFINITY) || (mx > m_ref + kRescaleAbove);
-      if (j > 0 && __any_sync(0xffffffffu, grow)) {
+      if (j > j0 && __any_sync(0xffffffffu, grow)) {
         // O_t holds blocks < j relative to m_ref: finish PV_t(j-1), then rescale
-        bad = !mbar_wait(&o_full[t], (j - 1) & 1, abort_flag, p.err, kErrWaitSoftmax);
+        bad = !mbar_wait(&o_full[t], (lj - 1) & 1, abort_flag, p.err, kErrWaitSoftmax);
         bad = __any_sync(0xffffffffu, bad);
         if (bad) {
           ok = false;
@@ -423,7 +442,7 @@ __device__ __forceinline__ void chunk_tile(const CUtensorMap &tmQ, const CUtenso
       tmem_st32(s_col + 32, pk);
       if (j == n_kb - 1 && t == zero_t) {
         // the block's V copies must have landed before they are patched
-        bad = !mbar_wait(&v_full[j % C::NV], (j / C::NV) & 1, abort_flag, p.err, kErrWaitSoftmax);
+        bad = !mbar_wait(&v_full[lj % C::NV], (lj / C::NV) & 1, abort_flag, p.err, kErrWaitSoftmax);
         if (__any_sync(0xffffffffu, bad)) {
           ok = false;
           break;
@@ -434,7 +453,7 @@ __device__ __forceinline__ void chunk_tile(const CUtensorMap &tmQ, const CUtenso
         // stage: zero their V rows so that P = 0 contributes exactly nothing.
         // One warp group does it (tile 0 if it reads this block), before its
         // P is ready; the other tile's PV is issued after this one's.
-        uint8_t *vrow = sV + (j % C::NV) * C::KV_BYTES + (r >> 3) * C::ATOM_STRIDE + (r & 7) * 128;
+        uint8_t *vrow = sV + (lj % C::NV) * C::KV_BYTES + (r >> 3) * C::ATOM_STRIDE + (r & 7) * 128;
 #pragma unroll
         for (int c = 0; c < C::NH; ++c)
 #pragma unroll
@@ -445,22 +464,91 @@ __device__ __forceinline__ void chunk_tile(const CUtensorMap &tmQ, const CUtenso
       tc_fence_before();
       mbar_arrive(&p_full[t]);
     }
-    if (nkb_t[t] > 0 && ok && mbar_wait(o_last, 0, abort_flag, p.err, kErrWaitSoftmax) && !*abort_flag) {
-      tc_fence_after();
-      const bool valid = i < qo;
-      const float inv = 1.f / l;
-      uint4 *dst = reinterpret_cast<uint4 *>(p.o + static_cast<size_t>(t0 + i) * (p.Hq * HD) + h * HD);
+    const bool have = jt_end[t] > j0;   // this query tile has rows and blocks in this unit
+    bool fin = ok;
+    if (have && fin) fin = mbar_wait(o_last, 0, abort_flag, p.err, kErrWaitSoftmax) && !*abort_flag;
+    fin = __all_sync(0xffffffffu, fin);   // tcgen05.ld below is warp-collective
+    if (n_pieces == 1) {
+      if (have && fin) {
+        tc_fence_after();
+        const bool valid = i < qo;
+        const float inv = 1.f / l;
+        uint4 *dst = reinterpret_cast<uint4 *>(p.o + static_cast<size_t>(t0 + i) * (p.Hq * HD) + h * HD);
 #pragma unroll
-      for (int cc = 0; cc < HD / 32; ++cc) {
-        float v[32];
-        tmem_ld32(o_col + cc * 32, v);
-        if (valid)
+        for (int cc = 0; cc < HD / 32; ++cc) {
+          float v[32];
+          tmem_ld32(o_col + cc * 32, v);
+          if (valid)
 #pragma unroll
-          for (int v8 = 0; v8 < 4; ++v8)
-            dst[cc * 4 + v8] = make_uint4(pack_bf16x2(v[8 * v8] * inv, v[8 * v8 + 1] * inv),
-                                          pack_bf16x2(v[8 * v8 + 2] * inv, v[8 * v8 + 3] * inv),
-                                          pack_bf16x2(v[8 * v8 + 4] * inv, v[8 * v8 + 5] * inv),
-                                          pack_bf16x2(v[8 * v8 + 6] * inv, v[8 * v8 + 7] * inv));
+            for (int v8 = 0; v8 < 4; ++v8)
+              dst[cc * 4 + v8] = make_uint4(pack_bf16x2(v[8 * v8] * inv, v[8 * v8 + 1] * inv),
+                                            pack_bf16x2(v[8 * v8 + 2] * inv, v[8 * v8 + 3] * inv),
+                                            pack_bf16x2(v[8 * v8 + 4] * inv, v[8 * v8 + 5] * inv),
+                                            pack_bf16x2(v[8 * v8 + 6] * inv, v[8 * v8 + 7] * inv));
+        }
+      }
+    } else if (!named_bar_or(2, 256, !fin)) {
+      // A piece of a split tile: its unnormalised o with the row's reference
+      // maximum m and sum l go to its partial slot; the last piece of the tile
+      // to finish merges every piece by log-sum-exp,
+      //   o = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s,  M = max_s m_s.
+      // All eight softmax warps take part (a tile without rows writes nothing).
+      const int first = slot - unit[5];   // the tile's first partial slot
+      if (have) {
+        tc_fence_after();
+        float *row = p.part + (static_cast<size_t>(slot) * 256 + 128 * t + r) * (HD + 4);
+#pragma unroll
+        for (int cc = 0; cc < HD / 32; ++cc) {
+          float v[32];
+          tmem_ld32(o_col + cc * 32, v);
+          float4 *w4 = reinterpret_cast<float4 *>(row + cc * 32);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) w4[k] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+        }
+        row[HD] = m_ref;
+        row[HD + 1] = l;
+      }
+      __threadfence();
+      named_bar_sync(2, 256);
+      if (threadIdx.x == 64) *merge_flag = atomicAdd(&p.ctr[first], 1) == n_pieces - 1;
+      named_bar_sync(2, 256);
+      if (*merge_flag) {
+        __threadfence();
+        // warp w takes rows w, w + 8, ...; lane s holds piece s's (m, l) (at
+        // most 32 pieces) and the hd row is spread over the lanes
+        const int w = warp - 2;
+        constexpr int PER = HD / 32;
+        for (int rr = w; rr < rows_valid; rr += 8) {
+          const float *base = p.part + (static_cast<size_t>(first) * 256 + rr) * (HD + 4);
+          const size_t pstride = static_cast<size_t>(256) * (HD + 4);
+          float mv = -INFINITY, lv = 0.f;
+          if (lane < n_pieces) {
+            mv = base[lane * pstride + HD];
+            lv = base[lane * pstride + HD + 1];
+          }
+          float M = mv;
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+          const float wgt = lane < n_pieces ? exp2f(mv - M) : 0.f;
+          float L = wgt * lv;
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+          float acc[PER];
+#pragma unroll
+          for (int k = 0; k < PER; ++k) acc[k] = 0.f;
+#pragma unroll 4
+          for (int sp = 0; sp < n_pieces; ++sp) {
+            const float ws = __shfl_sync(0xffffffffu, wgt, sp);
+            const float *src = base + sp * pstride;
+#pragma unroll
+            for (int k = 0; k < PER; ++k) acc[k] = fmaf(ws, src[lane + 32 * k], acc[k]);
+          }
+          const float inv = 1.f / L;
+          __nv_bfloat16 *dst = p.o + static_cast<size_t>(t0 + i0 + rr) * (p.Hq * HD) + h * HD;
+#pragma unroll
+          for (int k = 0; k < PER; ++k) dst[lane + 32 * k] = __float2bfloat16_rn(acc[k] * inv);
+        }
+        if (threadIdx.x == 64) p.ctr[first] = 0;   // ready for the next launch
       }
     }
     tc_fence_before();
@@ -1064,6 +1152,8 @@ cudaError_t attention_run(const AttnArgs &a, cudaStream_t st) {
   cp.num_pages = a.num_pages;
   cp.scale_log2 = scale_log2;
   cp.err = a.err;
+  cp.part = a.chunk_part;
+  cp.ctr = a.chunk_ctr;
   DecodeParams dp;
   dp.o = static_cast<__nv_bfloat16 *>(a.o);
   dp.part = a.part;

@@ -66,7 +66,9 @@ cudaError_t rope_append_run(const RopeArgs &a, cudaStream_t st);
 
 // ---- attention ----
 // Work lists (device int32, built on the host per step):
-//   chunk tiles:   {req, q_row0, q_head, 0} x n_tiles   (256 query rows each)
+//   chunk units:   {req, q_row0, q_head, j0, j1, piece, n_pieces, slot} x n_tiles: key blocks [j0, j1)
+//                  of a 256-row tile (n_pieces == 1: the whole tile; otherwise piece `piece`, whose
+//                  partial goes to slot `slot`, the tile's pieces holding consecutive slots)
 //   decode items:  {req, kv_head, page_begin, page_end, split, n_splits, 0, 0} x n_items
 struct AttnArgs {
   const void *q;            // [T][Hq][hd] bf16 (rotated)
@@ -85,6 +87,8 @@ struct AttnArgs {
   const CUtensorMap *tm_kv; // pool map, 5-D view of [P*2*Hkv][16][hd]: one (page, K/V, head) block per copy
   int *dec_ctr;             // two ints, zero between launches: decode work counter
   int *merge_ctr;           // one int per split group, zero between launches
+  float *chunk_part;        // split chunk tiles' partials [slots][256][hd + 4] (o, m, l, pad)
+  int *chunk_ctr;           // one int per slot (the tile's first slot counts its pieces), zero between launches
 };
 // Prefill-chunk tiles and persistent decode workers (both tcgen05) in one launch.
 cudaError_t attention_run(const AttnArgs &a, cudaStream_t st);

@@ -131,6 +131,12 @@ WORKLOADS = {
                                       (0, 2), (15, 129), (0, 300), (127, 2), (1000, 1)], 104),
     "tiny_decode_only": lambda: W.Workload("dec", W.TINY, [(5, 1), (300, 1), (17, 1)], 105),
     "tiny_one_chunk": lambda: W.Workload("chunk", W.TINY, [(0, 256)], 106),
+    # few chunk tiles over long prefixes: each tile's keys are split into
+    # pieces merged by log-sum-exp (a 256-row tile, a tile of 44 rows, and a
+    # 100-row chunk whose second query tile is empty)
+    "gqa4_split_tiles": lambda: W.Workload("split", W.SMALL_GQA, [(3000, 1), (4000, 256), (5000, 1)], 107),
+    "g5_qknorm_split_ragged": lambda: W.Workload("split5", W.SMALL_G5_QKN, [(2500, 300), (777, 1), (3100, 100)],
+                                                 108),
 }
 
 
