@@ -20,9 +20,6 @@
 #include "mb_internal.h"
 #include "mb_kernels.h"
 
-#ifndef MB_DEC_ITEMS_PER_SM
-#define MB_DEC_ITEMS_PER_SM 4
-#endif
 
 namespace mb {
 
@@ -512,7 +509,6 @@ mb_status prepare_step(mb_layer *L, const mb_batch *b, int64_t T, cudaStream_t s
   }
   // chunk tiles: 256 query rows (two 128-row tiles) of one q-head each
   std::vector<ChunkTile> tiles;
-  int64_t dec_pages = 0;
   for (int r = 0; r < n; ++r) {
     const int32_t qo = b->qo_indptr[r + 1] - b->qo_indptr[r];
     if (qo > 1) {
@@ -522,8 +518,6 @@ mb_status prepare_step(mb_layer *L, const mb_batch *b, int64_t T, cudaStream_t s
         const int32_t nkb = (c + i0 + rows - 1 + 128) / 128;
         for (int32_t hh = 0; hh < Hq; ++hh) tiles.push_back({r, i0, hh, nkb, rows > 128 ? 2 : 1});
       }
-    } else {
-      dec_pages += pages_for(b->kv_len[r]);
     }
   }
   std::vector<ChunkUnit> units;
@@ -534,34 +528,86 @@ mb_status prepare_step(mb_layer *L, const mb_batch *b, int64_t T, cudaStream_t s
     const int32_t rec[8] = {u.r, u.i0, u.h, u.j0, u.j1, u.piece, u.n_pieces, u.slot};
     std::copy(rec, rec + 8, hb.begin() + P.o_tiles + 8 * i);
   }
-  // decode splits: about MB_DEC_ITEMS_PER_SM items per SM.  A request's
-  // 128-key blocks (8 pages) are divided evenly among its splits, so only its
-  // last block can be partial.  Workers take items dynamically, so the tail
-  // is about one item long; the splits of one (request, KV head) are
-  // consecutive items {req, kv_head, page_begin, page_end, split, n_splits,
-  // group, 0}, and the last one to finish merges them (group = its counter).
-  const int64_t target_items = static_cast<int64_t>(ctx->sms) * MB_DEC_ITEMS_PER_SM;
-  const int64_t dec_blocks = (dec_pages + 7) / 8;   // upper bound per KV head, summed over requests
-  const int64_t bps = std::max<int64_t>(1, (dec_blocks * Hkv + target_items - 1) / std::max<int64_t>(1, target_items));
-  std::vector<int32_t> items;
-  int32_t n_groups = 0;
+  // Decode splits.  A request's 128-key blocks (8 pages) are divided evenly
+  // among its splits, so only its last block can be partial; the splits of
+  // one (request, KV head) hold consecutive partial slots and the last one to
+  // finish merges them (group = its counter).  Workers take items from a
+  // counter in list order, so the list runs heaviest first (list
+  // scheduling); the split size is the candidate (about 2 to 8 items per
+  // decode worker) whose list-scheduling makespan, at one block per item of
+  // overhead, is shortest (ties: fewer items).
+  std::vector<std::pair<int32_t, int32_t>> decs;   // (request, 128-key blocks)
+  int64_t dec_blocks = 0;
   for (int r = 0; r < n; ++r) {
-    const int32_t qo = b->qo_indptr[r + 1] - b->qo_indptr[r];
-    if (qo != 1) continue;
-    const int32_t np = pages_for(b->kv_len[r]);
-    const int32_t nblk = (np + 7) / 8;
+    if (b->qo_indptr[r + 1] - b->qo_indptr[r] != 1) continue;
+    const int32_t nblk = (pages_for(b->kv_len[r]) + 7) / 8;
+    decs.push_back({r, nblk});
+    dec_blocks += static_cast<int64_t>(nblk) * Hkv;
+  }
+  // planned for one worker per SM whatever the decode SM cap, so that a cap
+  // changes only which worker takes an item, not what the items compute
+  const int workers = std::max(1, ctx->sms);
+  auto splits_of = [](int32_t nblk, int64_t bps) {
     // at most 32 splits: the merge holds one split per lane
-    const int32_t ns = static_cast<int32_t>(
-        std::max<int64_t>(1, std::min<int64_t>({nblk, (nblk + bps / 2) / bps, 32})));
-    for (int32_t hk = 0; hk < Hkv; ++hk) {
-      const int32_t grp = ns > 1 ? n_groups++ : -1;
+    return static_cast<int32_t>(std::max<int64_t>(1, std::min<int64_t>({nblk, (nblk + bps / 2) / bps, 32})));
+  };
+  auto decode_span = [&](int64_t bps, size_t *count) {
+    std::vector<int64_t> costs;
+    for (const auto &d : decs) {
+      const int32_t ns = splits_of(d.second, bps);
       for (int32_t sidx = 0; sidx < ns; ++sidx) {
-        const int32_t pb = 8 * static_cast<int32_t>(static_cast<int64_t>(nblk) * sidx / ns);
-        const int32_t pe = std::min(np, 8 * static_cast<int32_t>(static_cast<int64_t>(nblk) * (sidx + 1) / ns));
-        items.insert(items.end(), {r, hk, pb, pe, sidx, ns, grp, 0});
+        const int64_t nb_item = static_cast<int64_t>(d.second) * (sidx + 1) / ns - static_cast<int64_t>(d.second) * sidx / ns;
+        for (int32_t hk = 0; hk < Hkv; ++hk) costs.push_back(nb_item + 1);
+      }
+    }
+    std::stable_sort(costs.begin(), costs.end(), std::greater<int64_t>());
+    *count = costs.size();
+    return list_makespan(costs, workers);
+  };
+  int64_t bps = 1;
+  if (!decs.empty()) {
+    int64_t best_span = -1;
+    size_t best_count = 0;
+    for (int k : {2, 3, 4, 6, 8}) {
+      const int64_t cand = std::max<int64_t>(1, (dec_blocks + static_cast<int64_t>(workers) * k - 1) /
+                                                    (static_cast<int64_t>(workers) * k));
+      size_t count = 0;
+      const int64_t sp = decode_span(cand, &count);
+      if (best_span < 0 || sp < best_span || (sp == best_span && count < best_count)) {
+        best_span = sp;
+        best_count = count;
+        bps = cand;
       }
     }
   }
+  struct DecItem {
+    int32_t f[8];
+    int32_t blocks;
+  };
+  std::vector<DecItem> ditems;
+  int32_t n_groups = 0, n_slots = 0;
+  for (const auto &d : decs) {
+    const int32_t r = d.first, nblk = d.second;
+    const int32_t np = pages_for(b->kv_len[r]);
+    const int32_t ns = splits_of(nblk, bps);
+    for (int32_t hk = 0; hk < Hkv; ++hk) {
+      const int32_t grp = ns > 1 ? n_groups++ : -1;
+      const int32_t slot0 = ns > 1 ? n_slots : 0;
+      if (ns > 1) n_slots += ns;
+      for (int32_t sidx = 0; sidx < ns; ++sidx) {
+        const int32_t b0 = static_cast<int32_t>(static_cast<int64_t>(nblk) * sidx / ns);
+        const int32_t b1 = static_cast<int32_t>(static_cast<int64_t>(nblk) * (sidx + 1) / ns);
+        const int32_t pb = 8 * b0;
+        const int32_t pe = std::min(np, 8 * b1);
+        ditems.push_back({{r, hk, pb, pe, sidx, ns, grp, slot0}, b1 - b0});
+      }
+    }
+  }
+  std::stable_sort(ditems.begin(), ditems.end(),
+                   [](const DecItem &x, const DecItem &y) { return x.blocks > y.blocks; });
+  std::vector<int32_t> items;
+  items.reserve(ditems.size() * 8);
+  for (const DecItem &it : ditems) items.insert(items.end(), it.f, it.f + 8);
   P.o_items = sec(items.size());
   std::copy(items.begin(), items.end(), hb.begin() + P.o_items);
   P.o_bt = sec(static_cast<size_t>(nb));
@@ -657,7 +703,7 @@ mb_status launch_layer(mb_layer *L, mb_layer *W, mb_kv *kv, const StepPlan &P, c
   if ((st = chk(mb::gemm_run(W->xn, L->w.w_qkv, &L->tm_wqkv, W->qkv, nullptr, Ti, L->qkv_dim, d.d_model,
                              mb::kEpiStore, W->gws, W->err, s), "gemm qkv")) != MB_OK)
     return st;
-  ++*launches;
+  *launches += mb::gemm_launches(Ti);
   mark(2);
   mb::RopeArgs ra;
   ra.qkv = W->qkv;
@@ -720,7 +766,7 @@ mb_status launch_layer(mb_layer *L, mb_layer *W, mb_kv *kv, const StepPlan &P, c
   if ((st = chk(mb::gemm_run(W->o, L->w.w_o, &L->tm_wo, W->h, x_in, Ti, d.d_model, hqd, mb::kEpiResidual, W->gws,
                              W->err, s), "gemm o")) != MB_OK)
     return st;
-  ++*launches;
+  *launches += mb::gemm_launches(Ti);
   mark(6);
   if ((st = chk(mb::rmsnorm_run(W->h, L->w.g_ffn, W->hn, Ti, d.d_model, d.rms_eps, s), "rmsnorm ffn")) != MB_OK)
     return st;
@@ -729,12 +775,12 @@ mb_status launch_layer(mb_layer *L, mb_layer *W, mb_kv *kv, const StepPlan &P, c
   if ((st = chk(mb::gemm_run(W->hn, L->w.w_gate_up, &L->tm_wgu, W->a, nullptr, Ti, d.d_ff, d.d_model,
                              mb::kEpiSwiGLU, W->gws, W->err, s), "gemm gate/up")) != MB_OK)
     return st;
-  ++*launches;
+  *launches += mb::gemm_launches(Ti);
   mark(8);
   if ((st = chk(mb::gemm_run(W->a, L->w.w_down, &L->tm_wd, x_out, W->h, Ti, d.d_model, d.d_ff, mb::kEpiResidual,
                              W->gws, W->err, s), "gemm down")) != MB_OK)
     return st;
-  ++*launches;
+  *launches += mb::gemm_launches(Ti);
   mark(9);
   return MB_OK;
 }

@@ -88,6 +88,29 @@ struct ChunkCfg {
   static constexpr uint32_t O_COL = 256;
 };
 
+// max(a, b, c) in one instruction.
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Probabilities of 64 logits against the reference m (log2 domain, scale
+// folded in): p = 2^(s scale - m) in pairs, packed as bf16 pairs, summed into
+// `sum` (pairwise, packed fp32).
+__device__ __forceinline__ void probs64(const float (&sv)[64], float2 sc2, float m, uint32_t (&pk)[32],
+                                        float2 &sum) {
+  const float2 negm = make_float2(-m, -m);
+#pragma unroll
+  for (int c = 0; c < 64; c += 2) {
+    const float2 x = __ffma2_rn(make_float2(sv[c], sv[c + 1]), sc2, negm);
+    const float p0 = ex2_approx(x.x);
+    const float p1 = ex2_approx(x.y);
+    sum = __fadd2_rn(sum, make_float2(p0, p1));
+    pk[c / 2] = pack_bf16x2(p0, p1);
+  }
+}
+
 struct ChunkParams {
   __nv_bfloat16 *o;
   const int32_t *qo_indptr, *kv_len, *bt_indptr, *bt, *tiles;
@@ -359,87 +382,77 @@ __device__ __forceinline__ void chunk_tile(const CUtensorMap &tmQ, const CUtenso
       const int key0 = 128 * j;
       const bool full = key0 + 127 <= q_pos;   // every key of the block is visible to this row
       const int vis = q_pos - key0;            // else keys key0 .. key0 + vis are (vis < 127)
-      // pass 1: the row's largest visible logit (raw; the scale is positive).
-      // The upper 64 keys are read twice (here and in pass 2) so that only
-      // 64 logits live in registers at a time.
-      float sa[64];
-      float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
-      {
-        float sb[64];
-        tmem_ld64(s_col + 64, sb);
+      // One pass over S while the reference holds: each half of the block's
+      // 128 logits is loaded once, masked, and its probabilities
+      // P = 2^(s scale - m_ref) are kept packed (bf16 pairs) in registers
+      // beside the row's raw maximum.  If a row of the warp rose more than
+      // 2^8 above its reference (always at the unit's first block, where
+      // m_ref = -inf), the warp moves the reference, rescales O and takes the
+      // probabilities again from S, which stays intact in TMEM until P is
+      // stored at the end.  Pairs of logits go through the packed fp32 FMA and
+      // add, and the maximum through 3-input max.
+      uint32_t pk_lo[32], pk_hi[32];
+      float2 lsum = make_float2(0.f, 0.f);
+      float mq0 = -INFINITY, mq1 = -INFINITY, mq2 = -INFINITY, mq3 = -INFINITY;
+      const float2 sc2 = make_float2(scale, scale);
+      const bool have_ref = m_ref != -INFINITY;   // the same for every row of the warp
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        float sv[64];
+        tmem_ld64(s_col + 64 * hh, sv);
         if (!full)
 #pragma unroll
           for (int c = 0; c < 64; ++c)
-            if (c + 64 > vis) sb[c] = -INFINITY;
+            if (64 * hh + c > vis) sv[c] = -INFINITY;
 #pragma unroll
-        for (int c = 0; c < 64; c += 4) {
-          m0 = fmaxf(m0, sb[c]);
-          m1 = fmaxf(m1, sb[c + 1]);
-          m2 = fmaxf(m2, sb[c + 2]);
-          m3 = fmaxf(m3, sb[c + 3]);
+        for (int c = 0; c < 64; c += 8) {
+          mq0 = max3f(mq0, sv[c], sv[c + 1]);
+          mq1 = max3f(mq1, sv[c + 2], sv[c + 3]);
+          mq2 = max3f(mq2, sv[c + 4], sv[c + 5]);
+          mq3 = max3f(mq3, sv[c + 6], sv[c + 7]);
+        }
+        if (have_ref) probs64(sv, sc2, m_ref, hh ? pk_hi : pk_lo, lsum);
+      }
+      const float mx = fmaxf(fmaxf(mq0, mq1), fmaxf(mq2, mq3)) * scale;
+      const bool grow = !have_ref || (mx > m_ref + kRescaleAbove);
+      if (__any_sync(0xffffffffu, grow)) {
+        if (j > j0) {
+          // O_t holds blocks < j relative to m_ref: finish PV_t(j-1), then rescale
+          bad = !mbar_wait(&o_full[t], (lj - 1) & 1, abort_flag, p.err, kErrWaitSoftmax);
+          bad = __any_sync(0xffffffffu, bad);
+          if (bad) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const float alpha = grow ? ex2_approx(m_ref - mx) : 1.f;
+#pragma unroll
+          for (int cc = 0; cc < HD / 32; ++cc) {
+            float v[32];
+            tmem_ld32(o_col + cc * 32, v);
+#pragma unroll
+            for (int k = 0; k < 32; ++k) v[k] *= alpha;
+            tmem_st32(o_col + cc * 32, v);
+          }
+          if (grow) l *= alpha;
+        }
+        if (grow) m_ref = mx;
+        lsum = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          float sv[64];
+          tmem_ld64(s_col + 64 * hh, sv);
+          if (!full)
+#pragma unroll
+            for (int c = 0; c < 64; ++c)
+              if (64 * hh + c > vis) sv[c] = -INFINITY;
+          probs64(sv, sc2, m_ref, hh ? pk_hi : pk_lo, lsum);
         }
       }
-      tmem_ld64(s_col, sa);
-      if (!full)
-#pragma unroll
-        for (int c = 0; c < 64; ++c)
-          if (c > vis) sa[c] = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < 64; c += 4) {
-        m0 = fmaxf(m0, sa[c]);
-        m1 = fmaxf(m1, sa[c + 1]);
-        m2 = fmaxf(m2, sa[c + 2]);
-        m3 = fmaxf(m3, sa[c + 3]);
-      }
-      const float mx = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3)) * scale;
-      const bool grow = (m_ref == -INFINITY) || (mx > m_ref + kRescaleAbove);
-      if (j > j0 && __any_sync(0xffffffffu, grow)) {
-        // O_t holds blocks < j relative to m_ref: finish PV_t(j-1), then rescale
-        bad = !mbar_wait(&o_full[t], (lj - 1) & 1, abort_flag, p.err, kErrWaitSoftmax);
-        bad = __any_sync(0xffffffffu, bad);
-        if (bad) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const float alpha = grow ? ex2_approx(m_ref - mx) : 1.f;
-#pragma unroll
-        for (int cc = 0; cc < HD / 32; ++cc) {
-          float v[32];
-          tmem_ld32(o_col + cc * 32, v);
-#pragma unroll
-          for (int k = 0; k < 32; ++k) v[k] *= alpha;
-          tmem_st32(o_col + cc * 32, v);
-        }
-        if (grow) l *= alpha;
-      }
-      if (grow) m_ref = mx;
-      // pass 2: probabilities relative to m_ref -> bf16 pairs into TMEM over S_t
-      float pk[32];
-#pragma unroll
-      for (int c = 0; c < 64; c += 2) {
-        const float p0 = ex2_approx(fmaf(sa[c], scale, -m_ref));
-        const float p1 = ex2_approx(fmaf(sa[c + 1], scale, -m_ref));
-        l += p0 + p1;
-        pk[c / 2] = __uint_as_float(pack_bf16x2(p0, p1));
-      }
-      tmem_st32(s_col, pk);   // columns 0-31: the upper logits (64-127) are still intact
-      {
-        float sb[64];
-        tmem_ld64(s_col + 64, sb);
-        if (!full)
-#pragma unroll
-          for (int c = 0; c < 64; ++c)
-            if (c + 64 > vis) sb[c] = -INFINITY;
-#pragma unroll
-        for (int c = 0; c < 64; c += 2) {
-          const float p0 = ex2_approx(fmaf(sb[c], scale, -m_ref));
-          const float p1 = ex2_approx(fmaf(sb[c + 1], scale, -m_ref));
-          l += p0 + p1;
-          pk[c / 2] = __uint_as_float(pack_bf16x2(p0, p1));
-        }
-      }
-      tmem_st32(s_col + 32, pk);
+      l += lsum.x + lsum.y;
+      // P over S_t in TMEM: keys 0-63 in columns 0-31, keys 64-127 in 32-63
+      tmem_st32u(s_col, pk_lo);
+      tmem_st32u(s_col + 32, pk_hi);
       if (j == n_kb - 1 && t == zero_t) {
         // the block's V copies must have landed before they are patched
         bad = !mbar_wait(&v_full[lj % C::NV], (lj / C::NV) & 1, abort_flag, p.err, kErrWaitSoftmax);
@@ -989,7 +1002,7 @@ __device__ __forceinline__ void decode_worker(const CUtensorMap &tmKV, const CUt
       for (int g = 0; g < G; ++g) lsum[g] = (red[64 + g] + red[80 + g]) + (red[96 + g] + red[112 + g]);
       // ---- the item is done: its output, or its split's partial
       const int32_t *it = p.items + h.item * 8;
-      const int req = it[0], hk = it[1], sidx = it[4], n_splits = it[5], grp = it[6];
+      const int req = it[0], hk = it[1], sidx = it[4], n_splits = it[5], grp = it[6], pbase = it[7];
       const size_t tok = static_cast<size_t>(p.qo_indptr[req]);
       if (n_splits == 1) {
         if (t < HD)
@@ -1001,7 +1014,7 @@ __device__ __forceinline__ void decode_worker(const CUtensorMap &tmKV, const CUt
       if (t < HD)
 #pragma unroll
         for (int g = 0; g < G; ++g) {
-          float *dst = p.part + (static_cast<size_t>(h.item) * G + g) * part_stride<HD>();
+          float *dst = p.part + (static_cast<size_t>(pbase + sidx) * G + g) * part_stride<HD>();
           dst[t] = o[g];
           if (t == 0) {
             dst[HD] = m[g];
@@ -1020,7 +1033,7 @@ __device__ __forceinline__ void decode_worker(const CUtensorMap &tmKV, const CUt
         // loads of consecutive splits are independent, so a merge costs a few
         // L2 round trips rather than one per split
         __threadfence();
-        const float *first = p.part + static_cast<size_t>(h.item - sidx) * G * part_stride<HD>();
+        const float *first = p.part + static_cast<size_t>(pbase) * G * part_stride<HD>();
         constexpr int PER = HD / 32;
         for (int g = q; g < G; g += 4) {
           float mv = -INFINITY, lv = 0.f;

@@ -33,6 +33,9 @@ GemmWorkspace gemm_workspace_carve(void *base);
 // 64 x 128) or nullptr.
 cudaError_t gemm_run(const void *A, const void *B, const CUtensorMap *tmB, void *D, const void *R, int M, int N,
                      int K, int epi, const GemmWorkspace &ws, int *err, cudaStream_t st);
+// Kernel launches gemm_run issues for M rows (2 when the rows past the last
+// multiple of 256 run as a launch of their own).
+int gemm_launches(int M);
 
 // Error code recorded by the allocation-free GEMM on the current device since
 // the last call (0 if none); a non-zero code is cleared.  Allocates nothing.
@@ -69,7 +72,8 @@ cudaError_t rope_append_run(const RopeArgs &a, cudaStream_t st);
 //   chunk units:   {req, q_row0, q_head, j0, j1, piece, n_pieces, slot} x n_tiles: key blocks [j0, j1)
 //                  of a 256-row tile (n_pieces == 1: the whole tile; otherwise piece `piece`, whose
 //                  partial goes to slot `slot`, the tile's pieces holding consecutive slots)
-//   decode items:  {req, kv_head, page_begin, page_end, split, n_splits, 0, 0} x n_items
+//   decode items:  {req, kv_head, page_begin, page_end, split, n_splits, group, slot0} x n_items: a split
+//                  item writes its partial to slot slot0 + split (the group's splits hold consecutive slots)
 struct AttnArgs {
   const void *q;            // [T][Hq][hd] bf16 (rotated)
   const void *pool;         // [P][2][Hkv][16][hd]
