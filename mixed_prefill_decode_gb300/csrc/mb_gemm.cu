@@ -82,6 +82,7 @@ constexpr int kWideMinRows = 1024;     // from this many tokens on, tiles have t
 #ifndef MB_GEMM_PEEL
 #define MB_GEMM_PEEL 1                 // 1: rows past the last multiple of 256 run as a 128-row-tile launch
 #endif
+constexpr int kPeelMinKSteps = 192;    // ... for GEMMs of at least this many K steps
 
 // Tile configurations: NH halves of 128 rows per tile.
 //  NH = 1: 128 x 256 tiles, 4 stages of 48 KB, two TMEM accumulators, so the
@@ -858,10 +859,13 @@ GemmWorkspace gemm_workspace_carve(void *base) {
   return w;
 }
 
-int gemm_launches(int M) {
+int gemm_launches(int M, int K) {
   const int tail = M % (2 * HM);
   if (M <= 0) return 0;
-  return MB_GEMM_PEEL && MB_GEMM_PAIRS == 1 && M >= kWideMinRows && tail > 0 && tail <= HM ? 2 : 1;
+  return MB_GEMM_PEEL && MB_GEMM_PAIRS == 1 && M >= kWideMinRows && tail > 0 && tail <= HM &&
+                 K / BK >= kPeelMinKSteps
+             ? 2
+             : 1;
 }
 
 cudaError_t gemm_run(const void *A, const void *B, const CUtensorMap *tmB_pre, void *D, const void *R, int M, int N,
@@ -869,12 +873,14 @@ cudaError_t gemm_run(const void *A, const void *B, const CUtensorMap *tmB_pre, v
   if (M <= 0) return cudaSuccess;
   // From kWideMinRows tokens the tiles are 256 rows over CTA pairs.  When M
   // mod 256 is 1..128, the last row of pair tiles is mostly padding and its
-  // tiles cost as much as full ones; the rows past the last multiple of 256
-  // then run as a second launch of 128-row tiles (the same stream; the
-  // second kernel's grid-dependency wait orders its use of the workspace).
-  // Qwen3-14B-shaped down projection at 2,144 tokens on GB300: 326 us as one
-  // launch against 232 us for its first 2,048 rows alone.
-  if (gemm_launches(M) == 2) {
+  // tiles cost as much as full ones; for long K the rows past the last
+  // multiple of 256 then run as a second launch of 128-row tiles (the same
+  // stream; the second kernel's grid-dependency wait orders its use of the
+  // workspace).  Measured on GB300 at 2,144 tokens (Qwen3-14B shapes): the
+  // down projection (272 K steps) 325 -> 301 us; QKV, O and gate/up (80 K
+  // steps) 111 -> 139, 93 -> 126 and 449 -> 492 us, where the tail launch's
+  // split fix-ups cost more than the padding; hence the K threshold.
+  if (gemm_launches(M, K) == 2) {
     const int tail = M % (2 * HM);
     const int Mm = M - tail;
     cudaError_t e = gemm_run(A, B, tmB_pre, D, R, Mm, N, K, epi, ws, err, st);

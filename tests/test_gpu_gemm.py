@@ -28,6 +28,9 @@ SHAPES = [
     # grouped schedule with every N-tile split along K (the down projection at
     # 576 tokens: 224 K steps over two groups)
     (576, 4096, 14336),
+    # at least 192 K steps with M mod 256 in 1..128 from 1,024 tokens: the rows
+    # past the last multiple of 256 run as a launch of their own
+    (1100, 512, 12288), (2144, 768, 12800),
 ]
 
 
@@ -55,7 +58,7 @@ def test_gemm_store_and_residual(mb, M, N, K, epi):
 
 @pytest.mark.parametrize("M,F,K", [(68, 1024, 256), (200, 1536, 512), (576, 14336, 4096), (16, 17408, 5120),
                                    (130, 128, 64), (1040, 1024, 512), (2216, 2048, 1024),
-                                   (700, 1024, 512)])
+                                   (700, 1024, 512), (1030, 256, 12288)])
 def test_gemm_swiglu(mb, M, F, K):
     A, B, _ = _inputs(M, 2 * F, K, M + F + K)
     dA, dB = to_dev(A), to_dev(B)

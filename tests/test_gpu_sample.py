@@ -5,8 +5,10 @@ The argmax is an integer decided by floating point: the kernel decides on the
 bf16 logits it wrote, so the ids are compared bit-exactly with the argmax of
 those same logits (lowest index among equal maxima); the logits themselves
 are compared with the oracle's float64 ones within the acceptance tolerance,
-and where the oracle's own argmax differs, its top two must lie within that
-tolerance of each other."""
+and where the oracle's own argmax differs, the oracle's two logits must lie
+closer than the kernel's bf16 rounding can resolve (a bound computed per row
+from the rounding of the normalised row, the fp32 accumulation and the bf16
+rounding of the logits)."""
 
 import numpy as np
 import pytest
@@ -14,7 +16,7 @@ import torch
 
 from oracle import layer as OL
 from mixed_prefill_decode_gb300 import workload as W
-from gpu_util import to_dev, from_dev, assert_close, f64, TOL
+from gpu_util import to_dev, from_dev, assert_close, f64
 
 pytestmark = pytest.mark.gpu
 
@@ -49,11 +51,26 @@ def test_sample_greedy_matches_oracle(mb, T, d, vocab, n_rows, seed):
     # the logits against the oracle's float64 ones
     ref_logits, ref_ids = OL.next_tokens_greedy(f64(x), rows, f64(g), f64(w), 1e-6)
     assert_close(f"logits {T}x{vocab}", f64(got_logits), ref_logits)
-    scale = np.max(np.abs(ref_logits))
-    for k in np.nonzero(got_ids != ref_ids)[0]:
-        # only a near tie may flip: the oracle's values at both ids agree within the tolerance
-        assert ref_logits[k, ref_ids[k]] - ref_logits[k, got_ids[k]] <= TOL * scale
-    assert np.mean(got_ids == ref_ids) >= 0.9
+    # An id may differ from the oracle's only where the two logits are closer
+    # than the kernel's rounding can tell apart: each GPU logit is the bf16
+    # rounding (half an ulp) of a dot product over the bf16-rounded normalised
+    # row (relative error 2^-9 per element), accumulated in fp32.  So the
+    # oracle's gap between its id o and the kernel's id c must stay within
+    # ulp/2 at both logits plus (2^-9 + d 2^-24 + 1e-6) sum_i |y_i| (|w_o,i| + |w_c,i|).
+    y_ref = OL.rms_norm(f64(x)[rows], f64(g), 1e-6)
+    wf = f64(w)
+
+    def half_ulp(v):
+        return 0.5 * 2.0 ** (np.floor(np.log2(abs(v))) - 7) if v != 0 else 0.0
+
+    flips = np.nonzero(got_ids != ref_ids)[0]
+    for k in flips:
+        o, c = int(ref_ids[k]), int(got_ids[k])
+        absdot = float(np.abs(y_ref[k]) @ (np.abs(wf[o]) + np.abs(wf[c])))
+        bound = half_ulp(ref_logits[k, o]) + half_ulp(ref_logits[k, c]) + (2.0 ** -9 + d * 2.0 ** -24 + 1e-6) * absdot
+        gap = ref_logits[k, o] - ref_logits[k, c]
+        assert gap <= bound, f"row {k}: id {c} instead of {o}, oracle gap {gap:.3e} > rounding bound {bound:.3e}"
+    print(f"{T}x{vocab}: {len(flips)} of {n_rows} ids differ from the oracle's, each within the rounding bound")
 
 
 def test_embed_is_exact_and_checks_ids(mb):
