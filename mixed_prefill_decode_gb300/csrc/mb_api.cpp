@@ -708,7 +708,7 @@ mb_status launch_layer(mb_layer *L, mb_layer *W, mb_kv *kv, const StepPlan &P, c
   if ((st = chk(mb::gemm_run(W->xn, L->w.w_qkv, &L->tm_wqkv, W->qkv, nullptr, Ti, L->qkv_dim, d.d_model,
                              mb::kEpiStore, W->gws, W->err, s), "gemm qkv")) != MB_OK)
     return st;
-  *launches += mb::gemm_launches(Ti, d.d_model);
+  *launches += mb::gemm_launches(Ti, L->qkv_dim, d.d_model, mb::kEpiStore);
   mark(2);
   mb::RopeArgs ra;
   ra.qkv = W->qkv;
@@ -771,7 +771,7 @@ mb_status launch_layer(mb_layer *L, mb_layer *W, mb_kv *kv, const StepPlan &P, c
   if ((st = chk(mb::gemm_run(W->o, L->w.w_o, &L->tm_wo, W->h, x_in, Ti, d.d_model, hqd, mb::kEpiResidual, W->gws,
                              W->err, s), "gemm o")) != MB_OK)
     return st;
-  *launches += mb::gemm_launches(Ti, hqd);
+  *launches += mb::gemm_launches(Ti, d.d_model, hqd, mb::kEpiResidual);
   mark(6);
   if ((st = chk(mb::rmsnorm_run(W->h, L->w.g_ffn, W->hn, Ti, d.d_model, d.rms_eps, s), "rmsnorm ffn")) != MB_OK)
     return st;
@@ -780,12 +780,12 @@ mb_status launch_layer(mb_layer *L, mb_layer *W, mb_kv *kv, const StepPlan &P, c
   if ((st = chk(mb::gemm_run(W->hn, L->w.w_gate_up, &L->tm_wgu, W->a, nullptr, Ti, d.d_ff, d.d_model,
                              mb::kEpiSwiGLU, W->gws, W->err, s), "gemm gate/up")) != MB_OK)
     return st;
-  *launches += mb::gemm_launches(Ti, d.d_model);
+  *launches += mb::gemm_launches(Ti, d.d_ff, d.d_model, mb::kEpiSwiGLU);
   mark(8);
   if ((st = chk(mb::gemm_run(W->a, L->w.w_down, &L->tm_wd, x_out, W->h, Ti, d.d_model, d.d_ff, mb::kEpiResidual,
                              W->gws, W->err, s), "gemm down")) != MB_OK)
     return st;
-  *launches += mb::gemm_launches(Ti, d.d_ff);
+  *launches += mb::gemm_launches(Ti, d.d_model, d.d_ff, mb::kEpiResidual);
   mark(9);
   return MB_OK;
 }

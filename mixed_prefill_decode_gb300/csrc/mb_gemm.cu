@@ -859,13 +859,16 @@ GemmWorkspace gemm_workspace_carve(void *base) {
   return w;
 }
 
-int gemm_launches(int M, int K) {
+int gemm_launches(int M, int N, int K, int epi) {
   const int tail = M % (2 * HM);
   if (M <= 0) return 0;
-  return MB_GEMM_PEEL && MB_GEMM_PAIRS == 1 && M >= kWideMinRows && tail > 0 && tail <= HM &&
-                 K / BK >= kPeelMinKSteps
-             ? 2
-             : 1;
+  if (!(MB_GEMM_PEEL && MB_GEMM_PAIRS == 1 && M >= kWideMinRows && tail > 0 && tail <= HM &&
+        K / BK >= kPeelMinKSteps))
+    return 1;
+  // the rows before the tail must fill at least two waves of CTA pairs
+  const long long tiles_n = epi == kEpiSwiGLU ? N / 128 : (N + BN - 1) / BN;
+  const long long main_tiles = static_cast<long long>(M / (2 * HM)) * tiles_n;
+  return main_tiles >= 2LL * (device_sm_count() / 2) ? 2 : 1;
 }
 
 cudaError_t gemm_run(const void *A, const void *B, const CUtensorMap *tmB_pre, void *D, const void *R, int M, int N,
@@ -879,8 +882,10 @@ cudaError_t gemm_run(const void *A, const void *B, const CUtensorMap *tmB_pre, v
   // workspace).  Measured on GB300 at 2,144 tokens (Qwen3-14B shapes): the
   // down projection (272 K steps) 325 -> 301 us; QKV, O and gate/up (80 K
   // steps) 111 -> 139, 93 -> 126 and 449 -> 492 us, where the tail launch's
-  // split fix-ups cost more than the padding; hence the K threshold.
-  if (gemm_launches(M, K) == 2) {
+  // split fix-ups cost more than the padding; hence the K threshold.  At
+  // 1,040 tokens (1,024 rows: 80 pair tiles for 76 pairs) the peeled down
+  // projection was slower too, hence at least two waves before the tail.
+  if (gemm_launches(M, N, K, epi) == 2) {
     const int tail = M % (2 * HM);
     const int Mm = M - tail;
     cudaError_t e = gemm_run(A, B, tmB_pre, D, R, Mm, N, K, epi, ws, err, st);

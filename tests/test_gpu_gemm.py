@@ -28,9 +28,10 @@ SHAPES = [
     # grouped schedule with every N-tile split along K (the down projection at
     # 576 tokens: 224 K steps over two groups)
     (576, 4096, 14336),
-    # at least 192 K steps with M mod 256 in 1..128 from 1,024 tokens: the rows
-    # past the last multiple of 256 run as a launch of their own
-    (1100, 512, 12288), (2144, 768, 12800),
+    # at least 192 K steps with M mod 256 in 1..128 from 1,024 tokens: with two
+    # waves of pair tiles before them, the rows past the last multiple of 256
+    # run as a launch of their own (2144 x 5120); otherwise they stay (1100)
+    (1100, 512, 12288), (2144, 5120, 12288),
 ]
 
 
