@@ -289,29 +289,33 @@ __device__ __forceinline__ void chunk_tile(const CUtensorMap &tmQ, const CUtenso
     if (lane == 0) {
       // ------------------------------------------------------- MMA issuer
       // j: the block's index in the tile; stages and phases count from j0
+      // Matrix descriptors of the stage bases, built once; an operand at byte
+      // offset `off` from a base is the base descriptor plus off / 16 (the
+      // start-address field; shared-memory addresses stay below 2^18, so the
+      // sum never carries out of it).
+      const uint64_t qd0 = sdesc_sw128(smem_u32(sQ), 16, 1024);
+      const uint64_t kd0 = sdesc_sw128(smem_u32(sK), 16, C::ATOM_STRIDE);
+      const uint64_t vd0 = sdesc_sw128(smem_u32(sV), 1024, C::ATOM_STRIDE);
       auto issue_s = [&](int t, int j) {
         const uint32_t d = tmem + 128 * t;
-        const uint32_t q0 = smem_u32(sQ + t * C::QT_BYTES);
-        const uint32_t k0 = smem_u32(sK + ((j - j0) % C::NK) * C::KV_BYTES);
+        const uint64_t qd = qd0 + static_cast<uint64_t>((t * C::QT_BYTES) >> 4);
+        const uint64_t kd = kd0 + static_cast<uint64_t>((((j - j0) % C::NK) * C::KV_BYTES) >> 4);
 #pragma unroll
         for (int c = 0; c < C::NH; ++c)
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t ad = sdesc_sw128(q0 + c * C::TILE_BYTES + kk * 32, 16, 1024);
-            const uint64_t bd = sdesc_sw128(k0 + c * 1024 + kk * 32, 16, C::ATOM_STRIDE);
-            mma_bf16(d, ad, bd, C::IDESC_S, (c > 0 || kk > 0) ? 1u : 0u);
-          }
+          for (int kk = 0; kk < 4; ++kk)
+            mma_bf16(d, qd + ((c * C::TILE_BYTES + kk * 32) >> 4), kd + ((c * 1024 + kk * 32) >> 4), C::IDESC_S,
+                     (c > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&s_full[t]);
       };
       auto issue_pv = [&](int t, int j) {
-        const uint32_t vbase = smem_u32(sV + ((j - j0) % C::NV) * C::KV_BYTES);
+        const uint64_t vd = vd0 + static_cast<uint64_t>((((j - j0) % C::NV) * C::KV_BYTES) >> 4);
         // P_t(j) sits in TMEM over S_t(j): 128 keys as 64 columns of bf16 pairs
         const uint32_t pcol = tmem + 128 * t;
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {  // 16 keys (two atoms) per MMA; hd halves 1 KB apart
-          const uint64_t bd = sdesc_sw128(vbase + ks * 2 * C::ATOM_STRIDE, 1024, C::ATOM_STRIDE);
-          mma_bf16_ts(tmem + C::O_COL + HD * t, pcol + ks * 8, bd, C::IDESC_PV, (j > j0 || ks > 0) ? 1u : 0u);
-        }
+        for (int ks = 0; ks < 8; ++ks)   // 16 keys (two atoms) per MMA; hd halves 1 KB apart
+          mma_bf16_ts(tmem + C::O_COL + HD * t, pcol + ks * 8, vd + ((ks * 2 * C::ATOM_STRIDE) >> 4), C::IDESC_PV,
+                      (j > j0 || ks > 0) ? 1u : 0u);
         // the last PV of a tile is covered by the o_last commit after the loop
         if (j + 1 < jt_end[t]) mma_commit(&o_full[t]);
       };
