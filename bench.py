@@ -1064,7 +1064,10 @@ def run_partition(args):
     "just enough SMs" for most of its bandwidth).  (1) Decode-only attention
     (Qwen3-14B-shaped, 16 x 8,192 tokens) against the cap on decode-worker
     CTAs; (2) the Llama-3-8B-shaped step (T = 576) with each cap against the
-    one-grid default, where workers take every SM the chunk tiles leave.  One
+    one-grid default, where workers take every SM the chunk tiles leave;
+    (3) the decode and chunk rows as two micro-batches on two streams with
+    SM caps (decode attention beside the other micro-batch's GEMMs), on the
+    Llama-3-8B step and the Qwen3-14B step with 2,200 piggybacked tokens.  One
     JSON line per point."""
     import torch
     from mixed_prefill_decode_gb300 import build as B
@@ -1130,6 +1133,112 @@ def run_partition(args):
                           "ms_per_step": round(ms, 5), "tokens_per_s": round(T / (ms / 1e3), 1),
                           "attention_ms": round(km["attention"] + km["attn_merge"], 5)}), flush=True)
     layer.close()
+    # decode attention beside the GEMMs of another micro-batch, on two streams
+    for wl in (W.llama3_8b_mixed(), W.qwen3_14b_mixed(2200)):
+        for line in two_stream_micro_batches(mb, torch, wl):
+            print(json.dumps(line), flush=True)
+
+
+def two_stream_micro_batches(mb, torch, wl, shares=(6, 4, 3), steps: int = 50) -> list:
+    """Row f1's other half: the decode rows and the chunk rows of one batch as
+    two micro-batches, stepped by two layers (same weights and KV pool, GEMM
+    workspaces of their own) on two streams at once, the decode micro-batch
+    on sms/share SMs (its GEMMs and decode workers) beside the chunk
+    micro-batch's GEMMs on the rest, so that decode attention runs beside the
+    other micro-batch's GEMMs (ConfluxServe's overlap).  Against the one-grid
+    mixed step and the two micro-batches one after the other.  L2 flushed
+    between steps; per-step events on the launching stream."""
+    wb, x, batch, pool = W.materialize(wl, unit_gains=True)
+    sh = wl.shape
+    qo = batch.qo_len()
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+
+    def sub(rs):
+        rows = np.concatenate([np.arange(batch.qo_indptr[r], batch.qo_indptr[r + 1]) for r in rs])
+        q = np.cumsum([0] + [int(qo[r]) for r in rs]).astype(np.int32)
+        tabs = [batch.bt[batch.bt_indptr[r]:batch.bt_indptr[r + 1]] for r in rs]
+        bti = np.cumsum([0] + [len(t) for t in tabs]).astype(np.int32)
+        return rows, W.Batch(q, batch.kv_len[rs].astype(np.int32), bti, np.concatenate(tabs).astype(np.int32))
+
+    parts = {"decode": sub([r for r in range(batch.num_reqs) if qo[r] == 1]),
+             "chunk": sub([r for r in range(batch.num_reqs) if qo[r] > 1])}
+    dw = {k: to_dev(v, torch) for k, v in wb.items()}
+    dpool = to_dev(pool.reshape(-1), torch)
+    main = torch.cuda.current_stream()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    full = mb.Layer(sh.as_dict(), dw, batch.num_tokens, pool.shape[0], kv_buf=dpool)
+    L = {n: mb.Layer(sh.as_dict(), dw, b.num_tokens, pool.shape[0], kv_buf=dpool) for n, (r, b) in parts.items()}
+    ws = {n: torch.zeros(mb.mb_gemm_workspace_bytes(), dtype=torch.uint8, device="cuda") for n in parts}
+    for n in parts:
+        mb.mb_layer_set_gemm_workspace(L[n].handle, ws[n])
+    cb = {n: mb.Batch.of(b) for n, (r, b) in parts.items()}
+    xs = {n: to_dev(x[r], torch) for n, (r, b) in parts.items()}
+    ys = {n: torch.empty_like(xs[n]) for n in parts}
+    st = {n: torch.cuda.Stream() for n in parts}
+    xf, yf, cbf = to_dev(x, torch), None, mb.Batch.of(batch)
+    yf = torch.empty_like(xf)
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        e0 = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        e1 = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        for i in range(steps):
+            flush.fill_(i & 0xFF)
+            e0[i].record(main)
+            fn()
+            e1[i].record(main)
+        torch.cuda.synchronize()
+        return sum(a.elapsed_time(b) for a, b in zip(e0, e1)) / steps
+
+    def one_grid():
+        full.step(cbf, xf, yf, main.cuda_stream)
+
+    def serial():
+        for n in parts:
+            L[n].step(cb[n], xs[n], ys[n], main.cuda_stream)
+
+    def overlapped():
+        start = torch.cuda.Event()
+        start.record(main)
+        ends = []
+        for n in ("decode", "chunk"):
+            st[n].wait_event(start)
+            L[n].step(cb[n], xs[n], ys[n], st[n].cuda_stream)
+            e = torch.cuda.Event()
+            e.record(st[n])
+            ends.append(e)
+        for e in ends:
+            main.wait_event(e)
+
+    out = []
+    T = batch.num_tokens
+    ms = timed(one_grid)
+    out.append({"kind": "micro_batches", "workload": wl.name, "schedule": "one grid (mixed step)", "ms": round(ms, 5),
+                "tokens_per_s": round(T / (ms / 1e3), 1)})
+    for n in parts:
+        mb.mb_layer_set_gemm_sms(L[n].handle, 0)
+        mb.mb_layer_set_decode_sms(L[n].handle, 0)
+    ms = timed(serial)
+    out.append({"kind": "micro_batches", "workload": wl.name, "schedule": "decode then chunk micro-batch, one stream",
+                "ms": round(ms, 5), "tokens_per_s": round(T / (ms / 1e3), 1)})
+    for share in shares:
+        d = sms // share
+        mb.mb_layer_set_gemm_sms(L["decode"].handle, d)
+        mb.mb_layer_set_decode_sms(L["decode"].handle, d)
+        mb.mb_layer_set_gemm_sms(L["chunk"].handle, sms - d)
+        ms = timed(overlapped)
+        out.append({"kind": "micro_batches", "workload": wl.name,
+                    "schedule": f"two streams: decode micro-batch on {d} SMs, chunk micro-batch GEMMs on {sms - d}",
+                    "ms": round(ms, 5), "tokens_per_s": round(T / (ms / 1e3), 1)})
+    for n in parts:
+        mb.mb_device_status(L[n].handle, st[n].cuda_stream)
+    mb.mb_device_status(full.handle, main.cuda_stream)
+    full.close()
+    for n in parts:
+        L[n].close()
+    return out
 
 
 def run_budget(args):
@@ -1199,6 +1308,8 @@ PROFILE_CASES = {
     # every position once per step (16 mb_step calls): one layer's share of
     # each kernel over the whole prompt
     "sweep_all": dict(k=None, decodes=True, chunk=True),
+    # the chunk alone at every position (the roofline's launches)
+    "chunk_all": dict(k=None, decodes=False, chunk=True),
 }
 
 

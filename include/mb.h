@@ -199,6 +199,21 @@ mb_status mb_layer_set_timing(mb_layer *layer, int32_t enable);
  * Takes effect at the next step (stacks re-capture their graphs).  Errors:
  * MB_EINVAL for n < 0. */
 mb_status mb_layer_set_decode_sms(mb_layer *layer, int32_t n);
+/* The other half of the SM partition: the layer's GEMM launches run at most
+ * n CTAs (one per SM; 0, the default, allows one per SM).  With two layers
+ * stepping concurrently on two streams (two micro-batches, the decode
+ * attention of one beside the GEMMs of the other, as ConfluxServe overlaps
+ * them), the caps of the kernels that run at the same time must add up to at
+ * most the SM count: a GEMM's K-split waits on CTAs of its own grid, which
+ * must all be resident.  A stack uses its first layer's setting.  Errors:
+ * MB_EINVAL for n < 0. */
+mb_status mb_layer_set_gemm_sms(mb_layer *layer, int32_t n);
+/* The layer's GEMM workspace (fp32 partial tiles and tile tickets): device
+ * memory of mb_gemm_workspace_bytes() bytes, 256-byte aligned, zero-filled,
+ * owned by the caller; NULL returns to the device's shared one.  Layers that
+ * step concurrently on different streams need workspaces of their own.
+ * Errors: MB_EINVAL, MB_ECUDA, MB_EUNSUPPORTED. */
+mb_status mb_layer_set_gemm_workspace(mb_layer *layer, void *workspace);
 mb_status mb_layer_timing(mb_layer *layer, double *ms, int32_t n, int64_t *steps);
 
 /* Number of kernel launches the last mb_step issued, and the bytes it copied

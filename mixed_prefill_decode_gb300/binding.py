@@ -93,6 +93,8 @@ _SIGS = {
     "mb_sched_finish": (_I32, [_VP, _I64]),
     "mb_sched_set_adaptive": (_I32, [_VP, _I32, _I32, _I32, _I32]),
     "mb_layer_set_decode_sms": (_I32, [_VP, _I32]),
+    "mb_layer_set_gemm_sms": (_I32, [_VP, _I32]),
+    "mb_layer_set_gemm_workspace": (_I32, [_VP, _VP]),
     "mb_sample_greedy": (_I32, [_VP, _I32, _VP, _I32, _I32, ctypes.c_float, _VP, _VP, _I32, _VP, _VP, _VP, _VP]),
     "mb_embed": (_I32, [_VP, _I32, _I32, _VP, _I32, _VP, _VP]),
     "mb_sched_counts": (_I32, [_VP, c_int32_p]),
@@ -221,6 +223,14 @@ def mb_layer_set_timing(layer: int, enable: bool) -> None:
 
 def mb_layer_set_decode_sms(layer: int, n: int) -> None:
     _check(lib().mb_layer_set_decode_sms(layer, n))
+
+
+def mb_layer_set_gemm_sms(layer: int, n: int) -> None:
+    _check(lib().mb_layer_set_gemm_sms(layer, n))
+
+
+def mb_layer_set_gemm_workspace(layer: int, workspace=None) -> None:
+    _check(lib().mb_layer_set_gemm_workspace(layer, _ptr(workspace)))
 
 
 def mb_layer_timing(layer: int):

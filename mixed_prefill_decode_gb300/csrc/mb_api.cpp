@@ -232,14 +232,16 @@ struct mb_layer {
 // descriptor's contents from the blob at run time.
 struct GraphKey {
   int64_t T;
-  int n_reqs, n_tiles, n_items, n_merge, n_chunk_slots;
+  int n_reqs, n_tiles, n_items, n_merge, n_chunk_slots, gemm_ctas;
   size_t ctr_cap;
+  const void *gws;
   size_t offs[8];
   const void *db, *part, *x_in, *x_out, *kv0;
   int dec_sms;
   bool operator==(const GraphKey &o) const {
     return T == o.T && n_reqs == o.n_reqs && n_tiles == o.n_tiles && n_items == o.n_items &&
-           n_merge == o.n_merge && n_chunk_slots == o.n_chunk_slots && ctr_cap == o.ctr_cap &&
+           n_merge == o.n_merge && n_chunk_slots == o.n_chunk_slots && gemm_ctas == o.gemm_ctas &&
+           ctr_cap == o.ctr_cap && gws == o.gws &&
            std::equal(offs, offs + 8, o.offs) && db == o.db && part == o.part &&
            x_in == o.x_in && x_out == o.x_out && kv0 == o.kv0 && dec_sms == o.dec_sms;
   }
@@ -708,7 +710,7 @@ mb_status launch_layer(mb_layer *L, mb_layer *W, mb_kv *kv, const StepPlan &P, c
   if ((st = chk(mb::gemm_run(W->xn, L->w.w_qkv, &L->tm_wqkv, W->qkv, nullptr, Ti, L->qkv_dim, d.d_model,
                              mb::kEpiStore, W->gws, W->err, s), "gemm qkv")) != MB_OK)
     return st;
-  *launches += mb::gemm_launches(Ti, L->qkv_dim, d.d_model, mb::kEpiStore);
+  *launches += mb::gemm_launches(Ti, L->qkv_dim, d.d_model, mb::kEpiStore, W->gws.max_ctas);
   mark(2);
   mb::RopeArgs ra;
   ra.qkv = W->qkv;
@@ -771,7 +773,7 @@ mb_status launch_layer(mb_layer *L, mb_layer *W, mb_kv *kv, const StepPlan &P, c
   if ((st = chk(mb::gemm_run(W->o, L->w.w_o, &L->tm_wo, W->h, x_in, Ti, d.d_model, hqd, mb::kEpiResidual, W->gws,
                              W->err, s), "gemm o")) != MB_OK)
     return st;
-  *launches += mb::gemm_launches(Ti, d.d_model, hqd, mb::kEpiResidual);
+  *launches += mb::gemm_launches(Ti, d.d_model, hqd, mb::kEpiResidual, W->gws.max_ctas);
   mark(6);
   if ((st = chk(mb::rmsnorm_run(W->h, L->w.g_ffn, W->hn, Ti, d.d_model, d.rms_eps, s), "rmsnorm ffn")) != MB_OK)
     return st;
@@ -780,12 +782,12 @@ mb_status launch_layer(mb_layer *L, mb_layer *W, mb_kv *kv, const StepPlan &P, c
   if ((st = chk(mb::gemm_run(W->hn, L->w.w_gate_up, &L->tm_wgu, W->a, nullptr, Ti, d.d_ff, d.d_model,
                              mb::kEpiSwiGLU, W->gws, W->err, s), "gemm gate/up")) != MB_OK)
     return st;
-  *launches += mb::gemm_launches(Ti, d.d_ff, d.d_model, mb::kEpiSwiGLU);
+  *launches += mb::gemm_launches(Ti, d.d_ff, d.d_model, mb::kEpiSwiGLU, W->gws.max_ctas);
   mark(8);
   if ((st = chk(mb::gemm_run(W->a, L->w.w_down, &L->tm_wd, x_out, W->h, Ti, d.d_model, d.d_ff, mb::kEpiResidual,
                              W->gws, W->err, s), "gemm down")) != MB_OK)
     return st;
-  *launches += mb::gemm_launches(Ti, d.d_model, d.d_ff, mb::kEpiResidual);
+  *launches += mb::gemm_launches(Ti, d.d_model, d.d_ff, mb::kEpiResidual, W->gws.max_ctas);
   mark(9);
   return MB_OK;
 }
@@ -978,6 +980,26 @@ mb_status mb_layer_buffer(const mb_layer *L, int32_t which, void **ptr, int64_t 
   return MB_OK;
 }
 
+mb_status mb_layer_set_gemm_sms(mb_layer *L, int32_t n) {
+  if (!L) return fail(MB_EINVAL, "mb_layer_set_gemm_sms: null layer");
+  if (n < 0) return fail(MB_EINVAL, "mb_layer_set_gemm_sms: n must be >= 0");
+  L->gws.max_ctas = n;
+  return MB_OK;
+}
+
+mb_status mb_layer_set_gemm_workspace(mb_layer *L, void *workspace) {
+  if (!L) return fail(MB_EINVAL, "mb_layer_set_gemm_workspace: null layer");
+  if (reinterpret_cast<uintptr_t>(workspace) % 256)
+    return fail(MB_EINVAL, "mb_layer_set_gemm_workspace: workspace must be 256-byte aligned");
+  mb::DeviceCtx *ctx = nullptr;
+  mb_status st = mb::device_ctx(&ctx);
+  if (st != MB_OK) return st;
+  const int cap = L->gws.max_ctas;
+  L->gws = mb::gemm_workspace_carve(workspace ? workspace : ctx->gemm_ws);
+  L->gws.max_ctas = cap;
+  return MB_OK;
+}
+
 mb_status mb_layer_set_decode_sms(mb_layer *L, int32_t n) {
   if (!L) return fail(MB_EINVAL, "mb_layer_set_decode_sms: null layer");
   if (n < 0) return fail(MB_EINVAL, "mb_layer_set_decode_sms: n must be >= 0");
@@ -1031,8 +1053,11 @@ mb_status mb_device_status(mb_layer *L, void *stream) {
       cudaMemset(errp, 0, 16);
       // a decode worker that gave up may leave split-merge counters raised
       if (L && L->part) cudaMemset(L->part, 0, L->part_cap * 4);
-      // a kernel that unwound early may leave stream-K tickets raised
+      // a kernel that unwound early may leave stream-K tickets raised (in the
+      // device's workspace, and in the layer's own if it has one)
       cudaMemset(ctx->gemm_ws, 0, mb::gemm_workspace_bytes());
+      if (L && static_cast<void *>(L->gws.partials) != ctx->gemm_ws)
+        cudaMemset(L->gws.partials, 0, mb::gemm_workspace_bytes());
     }
   }
   if (!L) {
@@ -1224,6 +1249,8 @@ mb_status mb_stack_step(mb_stack *S, mb_kv *const *kvs, const mb_batch *b, const
   key.n_merge = plan.n_merge;
   key.n_chunk_slots = plan.n_chunk_slots;
   key.ctr_cap = L0->ctr_cap;
+  key.gemm_ctas = L0->gws.max_ctas;   // every layer's GEMMs run on layer 0's workspace
+  key.gws = L0->gws.partials;
   const size_t offs[8] = {plan.o_qo, plan.o_kv, plan.o_bti, plan.o_bt, plan.o_treq, plan.o_tpos, plan.o_tiles,
                           plan.o_items};
   std::copy(offs, offs + 8, key.offs);

@@ -859,7 +859,14 @@ GemmWorkspace gemm_workspace_carve(void *base) {
   return w;
 }
 
-int gemm_launches(int M, int N, int K, int epi) {
+// SMs a GEMM may use: the device's, at most kMaxGemmGrid, at most max_ctas.
+static int gemm_sms(int max_ctas) {
+  int sms = device_sm_count() < kMaxGemmGrid ? device_sm_count() : kMaxGemmGrid;
+  if (max_ctas > 0 && max_ctas < sms) sms = max_ctas;
+  return sms;
+}
+
+int gemm_launches(int M, int N, int K, int epi, int max_ctas) {
   const int tail = M % (2 * HM);
   if (M <= 0) return 0;
   if (!(MB_GEMM_PEEL && MB_GEMM_PAIRS == 1 && M >= kWideMinRows && tail > 0 && tail <= HM &&
@@ -868,7 +875,7 @@ int gemm_launches(int M, int N, int K, int epi) {
   // the rows before the tail must fill at least two waves of CTA pairs
   const long long tiles_n = epi == kEpiSwiGLU ? N / 128 : (N + BN - 1) / BN;
   const long long main_tiles = static_cast<long long>(M / (2 * HM)) * tiles_n;
-  return main_tiles >= 2LL * (device_sm_count() / 2) ? 2 : 1;
+  return main_tiles >= 2LL * (gemm_sms(max_ctas) / 2) ? 2 : 1;
 }
 
 cudaError_t gemm_run(const void *A, const void *B, const CUtensorMap *tmB_pre, void *D, const void *R, int M, int N,
@@ -885,7 +892,7 @@ cudaError_t gemm_run(const void *A, const void *B, const CUtensorMap *tmB_pre, v
   // split fix-ups cost more than the padding; hence the K threshold.  At
   // 1,040 tokens (1,024 rows: 80 pair tiles for 76 pairs) the peeled down
   // projection was slower too, hence at least two waves before the tail.
-  if (gemm_launches(M, N, K, epi) == 2) {
+  if (gemm_launches(M, N, K, epi, ws.max_ctas) == 2) {
     const int tail = M % (2 * HM);
     const int Mm = M - tail;
     cudaError_t e = gemm_run(A, B, tmB_pre, D, R, Mm, N, K, epi, ws, err, st);
@@ -910,7 +917,7 @@ cudaError_t gemm_run(const void *A, const void *B, const CUtensorMap *tmB_pre, v
   p.N = N;
   p.K = K;
   p.k_iters = K / BK;
-  const int sm_count = device_sm_count() < kMaxGemmGrid ? device_sm_count() : kMaxGemmGrid;
+  const int sm_count = gemm_sms(ws.max_ctas);
   // Tile shape.  Up to 128 tokens: one 128-row tile per CTA.  From
   // kWideMinRows tokens on: 256-row tiles over CTA pairs.  In between, pairs
   // where they pad M no more than 128-row tiles do (M mod 256 = 0 or > 128):

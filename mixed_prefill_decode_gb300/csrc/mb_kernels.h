@@ -23,6 +23,7 @@ enum GemmEpilogue : int { kEpiStore = 0, kEpiResidual = 1, kEpiSwiGLU = 2 };
 struct GemmWorkspace {
   float *partials;  // [2 * kMaxGemmGrid][256][256] fp32
   int *tickets;     // [2 * kMaxGemmGrid]
+  int max_ctas = 0; // the GEMMs' CTAs at most (0: one per SM)
 };
 constexpr int kMaxGemmGrid = 256;
 size_t gemm_workspace_bytes();
@@ -35,7 +36,7 @@ cudaError_t gemm_run(const void *A, const void *B, const CUtensorMap *tmB, void 
                      int K, int epi, const GemmWorkspace &ws, int *err, cudaStream_t st);
 // Kernel launches gemm_run issues for an M x N x K GEMM with epilogue epi (2
 // when the rows past the last multiple of 256 run as a launch of their own).
-int gemm_launches(int M, int N, int K, int epi);
+int gemm_launches(int M, int N, int K, int epi, int max_ctas);
 
 // Error code recorded by the allocation-free GEMM on the current device since
 // the last call (0 if none); a non-zero code is cleared.  Allocates nothing.

@@ -310,3 +310,68 @@ def test_decode_sm_cap_is_bit_identical(mb, name, caps):
             mb.mb_layer_set_decode_sms(layer.handle, -1)
     finally:
         layer.close()
+
+
+def test_two_micro_batches_on_two_streams(mb):
+    """The decode rows and the chunk rows of one batch as two micro-batches,
+    stepped by two layers over the same weights and KV pool, each with a GEMM
+    workspace of its own, on two streams at once, under SM caps that add up to
+    the SM count (the decode attention of one beside the GEMMs of the other,
+    as ConfluxServe overlaps them): every row matches the oracle's full-batch
+    step, and each micro-batch equals the same micro-batch run alone bit for
+    bit (the schedules depend only on the shapes and caps)."""
+    wl = W.small_mixed(W.SMALL_GQA, seed=121, n_dec=9, chunk=300, prefix=2500)
+    wb, x, batch, pool = W.materialize(wl)
+    sh = wl.shape
+    ref = OL.layer_step(sh.as_dict(), OL.weights_to_f64(wb), f64(pool), batch.qo_indptr, batch.kv_len,
+                        batch.bt_indptr, batch.bt, f64(x))
+    qo = batch.qo_len()
+    dec = [r for r in range(batch.num_reqs) if qo[r] == 1]
+    chk = [r for r in range(batch.num_reqs) if qo[r] > 1]
+
+    def sub(rs):
+        rows = np.concatenate([np.arange(batch.qo_indptr[r], batch.qo_indptr[r + 1]) for r in rs])
+        q = np.cumsum([0] + [int(qo[r]) for r in rs]).astype(np.int32)
+        tabs = [batch.bt[batch.bt_indptr[r]:batch.bt_indptr[r + 1]] for r in rs]
+        bti = np.cumsum([0] + [len(t) for t in tabs]).astype(np.int32)
+        return rows, W.Batch(q, batch.kv_len[rs].astype(np.int32), bti, np.concatenate(tabs).astype(np.int32))
+
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    parts = {"decode": sub(dec), "chunk": sub(chk)}
+    caps = {"decode": (sms // 6, sms // 6), "chunk": (sms - sms // 6, 0)}   # (GEMM CTAs, decode workers)
+    dw = {k: to_dev(v) for k, v in wb.items()}
+    dpool = to_dev(pool.reshape(-1))
+    layers, ws, outs = {}, {}, {}
+    try:
+        for name, (rows, b) in parts.items():
+            L = mb.Layer(sh.as_dict(), dw, b.num_tokens, pool.shape[0], kv_buf=dpool)
+            ws[name] = torch.zeros(mb.mb_gemm_workspace_bytes(), dtype=torch.uint8, device="cuda")
+            mb.mb_layer_set_gemm_workspace(L.handle, ws[name])
+            mb.mb_layer_set_gemm_sms(L.handle, caps[name][0])
+            mb.mb_layer_set_decode_sms(L.handle, caps[name][1])
+            layers[name] = L
+        xs = {name: to_dev(x[rows]) for name, (rows, b) in parts.items()}
+        alone = {}
+        for name, (rows, b) in parts.items():   # each micro-batch alone, one stream
+            y = torch.empty_like(xs[name])
+            layers[name].step(mb.Batch.of(b), xs[name], y, _stream())
+            mb.mb_device_status(layers[name].handle, _stream())
+            alone[name] = from_dev(y)
+        streams = {name: torch.cuda.Stream() for name in parts}
+        start = torch.cuda.Event()
+        start.record()
+        for rep in range(3):
+            for name, (rows, b) in parts.items():
+                s = streams[name]
+                s.wait_event(start)
+                outs[name] = torch.empty_like(xs[name])
+                with torch.cuda.stream(s):
+                    layers[name].step(mb.Batch.of(b), xs[name], outs[name], s.cuda_stream)
+            for name in parts:
+                mb.mb_device_status(layers[name].handle, streams[name].cuda_stream)
+                assert np.array_equal(from_dev(outs[name]), alone[name]), f"{name} on two streams, rep {rep}"
+        for name, (rows, b) in parts.items():
+            assert_close(f"{name} micro-batch y", f64(alone[name]).reshape(len(rows), -1), ref["y"][rows])
+    finally:
+        for L in layers.values():
+            L.close()
