@@ -66,6 +66,11 @@ NCU_TRAFFIC = {
     "gemm_gate_up": {"bytes": 253.111296e6, "sha256_16": "0b09e0cf7d698eff",
                      "sources": ("csrc/mb_gemm.cu", "csrc/mb_ptx.cuh", "csrc/mb_kernels.h"),
                      "capture": "profiles/launches_llama3_8b_T576.md (llama3_8b_T576, second warm-up step)"},
+    # mean over the 16 chunk-alone launches of the prompt sweep (one capture
+    # of each: bench.py --case chunk_all), as the roofline's time is
+    "attention_chunk": {"bytes": 173.722544e6, "sha256_16": "7dc2177f2d536c1d",
+                        "sources": ("csrc/mb_attn.cu", "csrc/mb_ptx.cuh", "csrc/mb_kernels.h", "csrc/mb_api.cpp"),
+                        "capture": "profiles/attention_chunk_qwen3_14b_P30720.md (chunk_all, 16 launches)"},
 }
 
 
