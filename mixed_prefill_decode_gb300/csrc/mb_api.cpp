@@ -232,7 +232,7 @@ struct mb_layer {
 // descriptor's contents from the blob at run time.
 struct GraphKey {
   int64_t T;
-  int n_reqs, n_tiles, n_items, n_merge, n_chunk_slots, gemm_ctas;
+  int n_reqs, n_tiles, n_items, n_merge, n_chunk_slots, gemm_ctas, dec_workers;
   size_t ctr_cap;
   const void *gws;
   size_t offs[8];
@@ -241,6 +241,7 @@ struct GraphKey {
   bool operator==(const GraphKey &o) const {
     return T == o.T && n_reqs == o.n_reqs && n_tiles == o.n_tiles && n_items == o.n_items &&
            n_merge == o.n_merge && n_chunk_slots == o.n_chunk_slots && gemm_ctas == o.gemm_ctas &&
+           dec_workers == o.dec_workers &&
            ctr_cap == o.ctr_cap && gws == o.gws &&
            std::equal(offs, offs + 8, o.offs) && db == o.db && part == o.part &&
            x_in == o.x_in && x_out == o.x_out && kv0 == o.kv0 && dec_sms == o.dec_sms;
@@ -363,6 +364,7 @@ constexpr int32_t kMinPieceBlocks = 8;   // a piece covers at least 1,024 keys
 constexpr int64_t kUnitRamp = 2;         // a CTA's set-up, first loads and epilogue, in key blocks
 constexpr int64_t kPieceExtra = 2;       // a piece's partial round trip and share of the merge
 constexpr int64_t kItemRamp = 3;         // a decode item's Q load, first blocks and output or partial
+constexpr double kDecodeSatFrac = 0.85;  // share of the SMs whose decode workers saturate HBM
 
 // Makespan of list scheduling: each unit, in order, to the processor that
 // frees first.  That is how CTAs launched in that order spread over the SMs
@@ -466,6 +468,7 @@ struct StepPlan {
   size_t o_qo = 0, o_kv = 0, o_bti = 0, o_bt = 0, o_treq = 0, o_tpos = 0, o_tiles = 0, o_items = 0;
   int n_tiles = 0, n_items = 0, n_merge = 0;   // n_tiles: chunk units; n_merge: decode split groups
   int n_chunk_slots = 0;                       // partial slots of split chunk tiles
+  int dec_workers = 0;                         // decode worker CTAs the plan is for
   const int32_t *db = nullptr;
   int64_t upload_bytes = 0;
 };
@@ -551,14 +554,17 @@ mb_status prepare_step(mb_layer *L, const mb_batch *b, int64_t T, cudaStream_t s
     decs.push_back({r, nblk});
     dec_blocks += static_cast<int64_t>(nblk) * Hkv;
   }
-  // planned for one worker per SM whatever the decode SM cap, so that a cap
-  // changes only which worker takes an item, not what the items compute
-  const int workers = std::max(1, ctx->sms);
+  // The worker count is planned too (one per SM at most), whatever the
+  // decode SM cap, so that a cap changes only which worker takes an item,
+  // not what the items compute.  The stream saturates HBM before every SM
+  // takes part (measured: 16 decodes at 8,192 keys, 4.68 TB/s on 128 workers
+  // against 4.50 on 152), so a plan's time is modelled as its makespan in
+  // blocks times W / min(W, kDecodeSatFrac * SMs) for W workers.
   auto splits_of = [](int32_t nblk, int64_t bps) {
     // at most 32 splits: the merge holds one split per lane
     return static_cast<int32_t>(std::max<int64_t>(1, std::min<int64_t>({nblk, (nblk + bps / 2) / bps, 32})));
   };
-  auto decode_span = [&](int64_t bps, size_t *count) {
+  auto decode_span = [&](int64_t bps, int workers, size_t *count) {
     std::vector<int64_t> costs;
     for (const auto &d : decs) {
       const int32_t ns = splits_of(d.second, bps);
@@ -572,18 +578,24 @@ mb_status prepare_step(mb_layer *L, const mb_batch *b, int64_t T, cudaStream_t s
     return list_makespan(costs, workers);
   };
   int64_t bps = 1;
+  P.dec_workers = std::max(1, ctx->sms);
   if (!decs.empty()) {
-    int64_t best_span = -1;
+    const double sat = kDecodeSatFrac * ctx->sms;
+    double best_t = -1.0;
     size_t best_count = 0;
-    for (int k : {2, 3, 4, 6, 8}) {
-      const int64_t cand = std::max<int64_t>(1, (dec_blocks + static_cast<int64_t>(workers) * k - 1) /
-                                                    (static_cast<int64_t>(workers) * k));
-      size_t count = 0;
-      const int64_t sp = decode_span(cand, &count);
-      if (best_span < 0 || sp < best_span || (sp == best_span && count < best_count)) {
-        best_span = sp;
-        best_count = count;
-        bps = cand;
+    for (int w : {ctx->sms, ctx->sms * 7 / 8, ctx->sms * 3 / 4}) {
+      if (w < 1) continue;
+      for (int k : {1, 2, 3, 4, 6, 8}) {
+        const int64_t cand = std::max<int64_t>(1, (dec_blocks + static_cast<int64_t>(w) * k - 1) /
+                                                      (static_cast<int64_t>(w) * k));
+        size_t count = 0;
+        const double t = static_cast<double>(decode_span(cand, w, &count)) * w / std::min<double>(w, sat);
+        if (best_t < 0 || t < best_t - 1e-9 || (std::fabs(t - best_t) <= 1e-9 && count < best_count)) {
+          best_t = t;
+          best_count = count;
+          bps = cand;
+          P.dec_workers = w;
+        }
       }
     }
   }
@@ -750,7 +762,7 @@ mb_status launch_layer(mb_layer *L, mb_layer *W, mb_kv *kv, const StepPlan &P, c
   aa.items = db + P.o_items;
   aa.n_tiles = P.n_tiles;
   aa.n_items = P.n_items;
-  aa.max_workers = L->dec_sms;
+  aa.max_workers = L->dec_sms > 0 ? std::min(L->dec_sms, P.dec_workers) : P.dec_workers;
   aa.T = Ti;
   aa.Hq = Hq;
   aa.Hkv = Hkv;
@@ -1250,6 +1262,7 @@ mb_status mb_stack_step(mb_stack *S, mb_kv *const *kvs, const mb_batch *b, const
   key.n_chunk_slots = plan.n_chunk_slots;
   key.ctr_cap = L0->ctr_cap;
   key.gemm_ctas = L0->gws.max_ctas;   // every layer's GEMMs run on layer 0's workspace
+  key.dec_workers = plan.dec_workers;
   key.gws = L0->gws.partials;
   const size_t offs[8] = {plan.o_qo, plan.o_kv, plan.o_bti, plan.o_bt, plan.o_treq, plan.o_tpos, plan.o_tiles,
                           plan.o_items};
