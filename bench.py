@@ -953,6 +953,8 @@ def run_stack_headline(args, rank: int, world: int, local: int, pg, mb, torch, p
                            "time to first token beside 96 decodes"},
         "roofline": kern["roofline"] if kern else None,
         "kernels": kern["kernels"] if kern else None,
+        "gemm": kern["gemm"] if kern else None,
+        "decode_attn_sweep": kern["decode_attention_alone"] if kern else None,
         "prompt_sweep_per_layer": {k: v for k, v in kern.items() if k not in ("roofline", "kernels")} if kern else None,
         "cpu_baseline": cpu,
         "e2e": {"value": round(e2e_value, 1), "unit": UNIT,
