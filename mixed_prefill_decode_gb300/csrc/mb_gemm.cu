@@ -114,8 +114,17 @@ struct TileCfg {
   static_assert(NACC * NH * BN <= 512, "TMEM holds 512 columns");
   static_assert(NH * FIX_CHUNKS * CHUNK <= SMEM_TILES, "fix-up staging lives in the idle stage buffers");
 };
+// Weight k-blocks warmed into L2 behind the ring's first STAGES, before the
+// grid-dependency wait (while the previous kernel of the stream finishes).
+// Only there: prefetching ahead of the ring inside the main loop as well was
+// slower on GB300 at every shape measured (L2 flushed clean before each
+// call): at 2,144 tokens (Qwen3-14B shapes) QKV 108.5 -> 98.3 us, O 90.1 ->
+// 81.9, gate/up 432 -> 406 and down 287 -> 262 without it; at 16 tokens
+// gate/up 73.7 -> 63.5 and down 55.3 -> 51.2.  A read-only TMA stream of the
+// same boxes, no MMA, shows the same: 59.4 us for 356 MB without prefetch,
+// 67.6 with it 4 blocks ahead.
 #ifndef MB_GEMM_PREFETCH
-#define MB_GEMM_PREFETCH 8             // weight k-blocks fetched into L2 ahead of the ring
+#define MB_GEMM_PREFETCH 8
 #endif
 constexpr int kPrefetchAhead = MB_GEMM_PREFETCH;
 // Grouped schedule: split an N-tile along K over several groups only if that
@@ -125,6 +134,14 @@ constexpr int kPrefetchAhead = MB_GEMM_PREFETCH;
 // and O 39.6 -> 35.5 us unsplit (64 K steps against 51 and 34 split), down
 // 72.3 us split (120 K steps) against 90.8 us unsplit (224).
 constexpr int kSplitMinSaving = 32;
+// Up to this many rows of A (a few decode rows) a split tile's head stages
+// every other piece at once (the partial layout keeps a piece's rows of A
+// contiguous: one bulk copy each) and adds them up with all four epilogue
+// warps before one pass over TMEM, instead of one round trip per piece.
+// Measured on GB300, 16 rows (Qwen3-14B shapes, L2 flushed clean): QKV 30.7
+// -> 26.6 us, O 32.8 -> 26.6, down 51.2 -> 45.1.  At 64 rows the batched
+// code was slower (O 34.8 -> 36.9 us), hence a kernel of its own.
+constexpr int kFoldBatchRows = 32;
 
 struct Params {
   int M, N, K;          // N: output width (F for SwiGLU)
@@ -140,7 +157,7 @@ struct Params {
   const __nv_bfloat16 *R;
   int ldr;
   int F;                // SwiGLU: row offset of the up half in B
-  float *partials;      // [2 grid][NH halves][8 chunks][128 rows][32] fp32
+  float *partials;      // [2 grid][NH halves][8 / FIX groups][128 rows][FIX x 32] fp32 (part_row)
   int *tickets;
   int *err;
   uint64_t split_wait_ns;   // limit of the head piece's wait for the other pieces of its tile
@@ -265,9 +282,14 @@ __device__ __forceinline__ int slot_of(const Params &p, int rank, int mi, int cr
 // serialises the epilogue's 4 warps (measured: ~8 us per 128 x 128 tile).
 __device__ __forceinline__ float silu(float x) { return __fdividef(x, 1.0f + __expf(-x)); }
 
+// Partial tiles: per slot and half, 8 / FIX row groups, each [128 rows][FIX
+// chunks x 32] fp32 (FIX = the chunks a fix-up round stages per half), so
+// that the rows of A in a group are one contiguous block: one bulk copy
+// stages them, however few.
 template <int NH>
-__device__ __forceinline__ float *part_chunk(const Params &p, int slot, int h, int j, int r) {
-  return p.partials + (((static_cast<size_t>(slot) * NH + h) * 8 + j) * 128 + r) * 32;
+__device__ __forceinline__ float *part_row(const Params &p, int slot, int h, int g, int r) {
+  constexpr int FIX = NH == 1 ? 8 : 4;
+  return p.partials + ((((static_cast<size_t>(slot) * NH + h) * (8 / FIX) + g) * 128 + r) * (FIX * 32));
 }
 // Halves of the tile at m0 that hold rows of A.
 template <int NH>
@@ -321,7 +343,10 @@ __device__ __forceinline__ void store_chunk(const Params &p, int row, int col, c
 // a pair issues the pair MMAs, owns the stage-full and accumulator-empty
 // barriers both CTAs' copies and epilogues report to; each CTA loads, drains
 // and fixes up its own 128 rows.
-template <int EPI, int NH, bool PAIR>
+// FOLDB: a split tile's head stages all other pieces at once and adds them
+// up with every epilogue thread before one pass over TMEM (tiles of at most
+// kFoldBatchRows rows of A); otherwise it folds one piece per round.
+template <int EPI, int NH, bool PAIR, bool FOLDB = false>
 __global__ void __launch_bounds__(TileCfg<NH, PAIR>::THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const Params p) {
   using C = TileCfg<NH, PAIR>;
@@ -432,31 +457,13 @@ __global__ void __launch_bounds__(TileCfg<NH, PAIR>::THREADS, 1)
       uint32_t issued_mask = 0, issued_ph = 0;
       int n_issued = 0;   // k steps issued so far (the first `pre` have their weights in flight)
       bool ok = true;
-      bool first_seg = true;
       while (ok && segs.next(sg)) {
         const int m0 = (sg.tile % p.tiles_m) * BM;
         const int nh = halves_of<NH>(p, m0);
         const int nt = sg.tile / p.tiles_m;
         const int rows0 = EPI == kEpiSwiGLU ? nt * 128 : nt * BN;
         const int rows1 = EPI == kEpiSwiGLU ? p.F + nt * 128 : nt * BN + 128;
-        // one CTA per group warms L2 with the weight k-blocks ahead of the ring
-        // (the first segment's first STAGES + kPrefetchAhead blocks were
-        // loaded or prefetched before the grid-dependency wait)
-        const bool prefetcher = (p.grouped ? (sched_b % p.tiles_m) == 0 : true) && crank == 0;
-        const bool warmed = first_seg && pre > 0;
-        const int pf_from = warmed ? sg.k0 + STAGES + kPrefetchAhead : sg.k0 + kPrefetchAhead;
-        first_seg = false;
-        if (prefetcher && !warmed) {
-          for (int kb = sg.k0; kb < sg.k1 && kb < sg.k0 + kPrefetchAhead; ++kb) {
-            tma_prefetch_2d(&tmB, kb * BK, rows0);
-            tma_prefetch_2d(&tmB, kb * BK, rows1);
-          }
-        }
         for (int kb = sg.k0; kb < sg.k1; ++kb) {
-          if (prefetcher && kb + kPrefetchAhead < sg.k1 && kb + kPrefetchAhead >= pf_from) {
-            tma_prefetch_2d(&tmB, (kb + kPrefetchAhead) * BK, rows0);
-            tma_prefetch_2d(&tmB, (kb + kPrefetchAhead) * BK, rows1);
-          }
           if (!mbar_wait(&empty[s], ph ^ 1, abort_flag, p.err, kErrWaitProducer)) {
             ok = false;
             break;
@@ -604,7 +611,12 @@ __global__ void __launch_bounds__(TileCfg<NH, PAIR>::THREADS, 1)
       // this half (a pair: this CTA's 128 rows) holds rows of A
       const bool mine = PAIR ? m0 + static_cast<int>(crank) * HM < p.M : h < halves_of<NH>(p, m0);
       const int nt = sg.tile / p.tiles_m;
-      const int row = m0 + (PAIR ? static_cast<int>(crank) : h) * HM + r;
+      const int hrow0 = m0 + (PAIR ? static_cast<int>(crank) : h) * HM;   // first row of this half
+      const int row = hrow0 + r;
+      // rows of A in this half: only these go through the split fix-up and the
+      // stores (a few decode rows then move a few KB of partials, not 128 KB)
+      const int rv = mine ? min(HM, p.M - hrow0) : 0;
+      const bool wrows = q * 32 < rv;   // this warp's lane quarter holds some (warp-uniform)
       const int col0 = EPI == kEpiSwiGLU ? nt * 128 : nt * BN;
       uint4 rb[16];
       // the residual does not depend on the accumulator: fetch it while the
@@ -627,15 +639,18 @@ __global__ void __launch_bounds__(TileCfg<NH, PAIR>::THREADS, 1)
         if (my_rank != r_first) {
           // a later piece: hand the fp32 partial to the rank that covers the
           // unit's head (for which this unit is its last segment)
-          if (mine) {
+          if (wrows) {
 #pragma unroll 1
             for (int j = 0; j < BN / 32; ++j) {
               float v[32];
               tmem_ld32(tbase + 32 * j, v);
-              float4 *w4 = reinterpret_cast<float4 *>(part_chunk<NH>(p, sg.slot, h, j, r));
+              float4 *w4 = reinterpret_cast<float4 *>(part_row<NH>(p, sg.slot, h, j / C::FIX_CHUNKS, r) +
+                                                      (j % C::FIX_CHUNKS) * 32);
+              if (r < rv) {
 #pragma unroll
-              for (int i = 0; i < 8; ++i)
-                w4[part_swz(i, r)] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+                for (int i = 0; i < 8; ++i)
+                  w4[part_swz(i, r)] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+              }
             }
           }
           release_acc(acc);
@@ -662,50 +677,109 @@ __global__ void __launch_bounds__(TileCfg<NH, PAIR>::THREADS, 1)
           if (named_bar_or(1, EPI_THREADS, *abort_flag != 0)) {
             ok = false;
           } else {
-            // this unit is the rank's last segment: the stage buffers are idle;
-            // each half stages FIX_CHUNKS of its 8 chunks at a time in its own area
+            // this unit is the rank's last segment: the stage buffers are idle.
+            // Each half stages the other pieces' row groups (their rows of A,
+            // one bulk copy each) in its own area, as many per round as fit:
+            // 128 / rv of them, so with a few rows of A every piece lands in
+            // one round.  Item i is group i % G of piece r_first + 1 + i / G;
+            // every element adds, in rank order, the round's pieces to each
+            // other and then their sum to the accumulator.  Both halves of a
+            // 256-row tile size their rounds by half 0's rows, so that they
+            // take the same number of rounds (the named barrier is shared).
+            constexpr int G = 8 / C::FIX_CHUNKS;
+            constexpr uint32_t rbytes = C::FIX_CHUNKS * 128u;   // one row of a group
             uint8_t *stage = smem + h * C::FIX_CHUNKS * CHUNK;
+            const int rv0 = PAIR ? rv : min(HM, p.M - m0);
+            const int per_round = FOLDB && rv0 > 0 ? HM / rv0 : 1;
+            const uint32_t gbytes = static_cast<uint32_t>(rv) * rbytes;
+            const int n_items = (r_last - r_first) * G;
 #pragma unroll 1
-            for (int rk = r_first + 1; rk <= r_last && ok; ++rk) {
-              const int slot = slot_of<PAIR>(p, rk, mi, static_cast<int>(crank), sg.unit);
-#pragma unroll 1
-              for (int rr = 0; rr < 8 / C::FIX_CHUNKS; ++rr) {
-                bool fine = true;
-                if (mine) {
-                  if (q == 0 && lane == 0) {
-                    mbar_arrive_expect_tx(&fixbar[h], C::FIX_CHUNKS * CHUNK);
-                    for (int jj = 0; jj < C::FIX_CHUNKS; ++jj)
-                      bulk_load(stage + jj * CHUNK, part_chunk<NH>(p, slot, h, rr * C::FIX_CHUNKS + jj, 0), CHUNK,
-                                &fixbar[h]);
+            for (int i0 = 0; i0 < n_items && ok; i0 += per_round) {
+              const int i1 = min(n_items, i0 + per_round);
+              bool fine = true;
+              if (mine) {
+                if (q == 0 && lane == 0) {
+                  mbar_arrive_expect_tx(&fixbar[h], static_cast<uint32_t>(i1 - i0) * gbytes);
+                  for (int i = i0; i < i1; ++i) {
+                    const int slot = slot_of<PAIR>(p, r_first + 1 + i / G, mi, static_cast<int>(crank), sg.unit);
+                    bulk_load(stage + (i - i0) * gbytes, part_row<NH>(p, slot, h, i % G, 0), gbytes, &fixbar[h]);
                   }
-                  fine = __all_sync(0xffffffffu, mbar_wait(&fixbar[h], fix_ph, abort_flag, p.err, kErrWaitEpilogue));
-                  fix_ph ^= 1;
                 }
-                // leave together: the barrier at the end of each pass is shared
-                if (named_bar_or(1, EPI_THREADS, !fine)) {
-                  ok = false;
-                  break;
+                fine = __all_sync(0xffffffffu, mbar_wait(&fixbar[h], fix_ph, abort_flag, p.err, kErrWaitEpilogue));
+                fix_ph ^= 1;
+              }
+              // leave together: the barrier at the end of each round is shared
+              if (named_bar_or(1, EPI_THREADS, !fine)) {
+                ok = false;
+                break;
+              }
+              // all threads of the half first add each group's later items into
+              // its first one (consecutive float4 per thread: no bank conflicts),
+              // then the warps that own rows of A add that sum into TMEM
+              if (FOLDB && mine) {
+#pragma unroll 1
+                for (int g = 0; g < G; ++g) {
+                  const int ig = i0 + (g - i0 % G + G) % G;   // first item of group g in this round
+                  if (ig + G >= i1) continue;                 // at most one item of group g
+                  float4 *dst = reinterpret_cast<float4 *>(stage + (ig - i0) * gbytes);
+                  const int n4 = static_cast<int>(gbytes / 16);
+                  auto item4 = [&](int i, int e) {
+                    return reinterpret_cast<const float4 *>(stage + (i - i0) * gbytes)[e];
+                  };
+                  auto add4 = [](float4 &a, const float4 &t) {
+                    a.x += t.x;
+                    a.y += t.y;
+                    a.z += t.z;
+                    a.w += t.w;
+                  };
+#pragma unroll 2
+                  for (int e = r; e < n4; e += HM) {
+                    float4 a = dst[e];
+                    int i = ig + G;
+                    // four items' loads in flight at a time, added in rank order
+#pragma unroll 1
+                    for (; i + 3 * G < i1; i += 4 * G) {
+                      const float4 t0 = item4(i, e), t1 = item4(i + G, e), t2 = item4(i + 2 * G, e),
+                                   t3 = item4(i + 3 * G, e);
+                      add4(a, t0);
+                      add4(a, t1);
+                      add4(a, t2);
+                      add4(a, t3);
+                    }
+#pragma unroll 1
+                    for (; i < i1; i += G) add4(a, item4(i, e));
+                    dst[e] = a;
+                  }
                 }
-                if (mine) {
+              }
+              if (FOLDB) named_bar_sync(1, EPI_THREADS);
+              if (wrows) {
+                const int rs = r < rv ? r : 0;   // the staged row this lane adds
+#pragma unroll 1
+                for (int g = 0; g < G; ++g) {
+                  const int ig = i0 + (g - i0 % G + G) % G;
+                  if (ig >= i1) continue;
 #pragma unroll 1
                   for (int jj = 0; jj < C::FIX_CHUNKS; ++jj) {
-                    const int j = rr * C::FIX_CHUNKS + jj;
                     float v[32];
-                    tmem_ld32(tbase + 32 * j, v);
-                    const float4 *src = reinterpret_cast<const float4 *>(stage + jj * CHUNK + r * 128);
+                    tmem_ld32(tbase + 32 * (g * C::FIX_CHUNKS + jj), v);   // the warp's whole lane quarter
+                    // rows past A's have nothing staged and are never stored: they
+                    // add row 0 (no lane may branch off before the aligned tcgen05.st)
+                    const float4 *src =
+                        reinterpret_cast<const float4 *>(stage + (ig - i0) * gbytes + rs * rbytes + jj * 128);
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                      const float4 t = src[part_swz(i, r)];
-                      v[4 * i] += t.x;
-                      v[4 * i + 1] += t.y;
-                      v[4 * i + 2] += t.z;
-                      v[4 * i + 3] += t.w;
+                    for (int c = 0; c < 8; ++c) {
+                      const float4 t = src[part_swz(c, rs)];
+                      v[4 * c] += t.x;
+                      v[4 * c + 1] += t.y;
+                      v[4 * c + 2] += t.z;
+                      v[4 * c + 3] += t.w;
                     }
-                    tmem_st32(tbase + 32 * j, v);
+                    tmem_st32(tbase + 32 * (g * C::FIX_CHUNKS + jj), v);
                   }
                 }
-                named_bar_sync(1, EPI_THREADS);   // the next copy overwrites the staging
               }
+              named_bar_sync(1, EPI_THREADS);   // the next round overwrites the staging
             }
             finish = ok;
           }
@@ -713,7 +787,7 @@ __global__ void __launch_bounds__(TileCfg<NH, PAIR>::THREADS, 1)
         }
       }
       if (finish) {
-        if (mine) {
+        if (wrows) {
           if (EPI == kEpiSwiGLU) {
 #pragma unroll 1
             for (int j = 0; j < 4; ++j) {
@@ -766,19 +840,21 @@ __global__ void __launch_bounds__(TileCfg<NH, PAIR>::THREADS, 1)
   }
 }
 
-template <int EPI, int NH, bool PAIR = false>
+template <int EPI, int NH, bool PAIR = false, bool FOLDB = false>
 cudaError_t launch(const CUtensorMap &tmA, const CUtensorMap &tmB, const Params &p, cudaStream_t st) {
   using C = TileCfg<NH, PAIR>;
   const cudaError_t attr_err =
-      ensure_max_smem(reinterpret_cast<const void *>(gemm_kernel<EPI, NH, PAIR>), C::SMEM_BYTES);
+      ensure_max_smem(reinterpret_cast<const void *>(gemm_kernel<EPI, NH, PAIR, FOLDB>), C::SMEM_BYTES);
   if (attr_err != cudaSuccess) return attr_err;
   // a pair schedule's p.grid counts pairs
-  return launch_pdl(gemm_kernel<EPI, NH, PAIR>, dim3(PAIR ? 2 * p.grid : p.grid), dim3(C::THREADS), C::SMEM_BYTES,
+  return launch_pdl(gemm_kernel<EPI, NH, PAIR, FOLDB>, dim3(PAIR ? 2 * p.grid : p.grid), dim3(C::THREADS), C::SMEM_BYTES,
                     st, p.cluster, tmA, tmB, p);
 }
 
-// mode: 1 = 128-row tiles, 2 = 256-row tiles, kModePair = 256-row tiles over CTA pairs
+// mode: 1 = 128-row tiles, 2 = 256-row tiles, kModePair = 256-row tiles over CTA pairs,
+// kModeFew = 128-row tiles holding at most kFoldBatchRows rows of A (batched fix-up)
 constexpr int kModePair = 3;
+constexpr int kModeFew = 4;
 
 cudaError_t launch_for(int epi, int nh, const CUtensorMap &tmA, const CUtensorMap &tmB, const Params &p,
                        cudaStream_t st) {
@@ -795,6 +871,14 @@ cudaError_t launch_for(int epi, int nh, const CUtensorMap &tmA, const CUtensorMa
       case kEpiStore: return launch<kEpiStore, 2>(tmA, tmB, p, st);
       case kEpiResidual: return launch<kEpiResidual, 2>(tmA, tmB, p, st);
       case kEpiSwiGLU: return launch<kEpiSwiGLU, 2>(tmA, tmB, p, st);
+      default: return cudaErrorInvalidValue;
+    }
+  }
+  if (nh == kModeFew) {
+    switch (epi) {
+      case kEpiStore: return launch<kEpiStore, 1, false, true>(tmA, tmB, p, st);
+      case kEpiResidual: return launch<kEpiResidual, 1, false, true>(tmA, tmB, p, st);
+      case kEpiSwiGLU: return launch<kEpiSwiGLU, 1, false, true>(tmA, tmB, p, st);
       default: return cudaErrorInvalidValue;
     }
   }
@@ -982,7 +1066,7 @@ cudaError_t gemm_run(const void *A, const void *B, const CUtensorMap *tmB_pre, v
   p.split_wait_ns = g_split_wait_ns.load(std::memory_order_relaxed);
   p.split_phantom = g_split_phantom.load(std::memory_order_relaxed);
   if (!fill_rank_bounds(p)) return cudaErrorInvalidValue;
-  return launch_for(epi, nh, tmA, tmB, p, st);
+  return launch_for(epi, nh == 1 && M <= kFoldBatchRows ? kModeFew : nh, tmA, tmB, p, st);
 }
 
 }  // namespace mb

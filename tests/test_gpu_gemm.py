@@ -32,6 +32,9 @@ SHAPES = [
     # waves of pair tiles before them, the rows past the last multiple of 256
     # run as a launch of their own (2144 x 5120); otherwise they stay (1100)
     (1100, 512, 12288), (2144, 5120, 12288),
+    # at most 32 rows with split tiles: the head stages every piece at once
+    # (7 rows: 18 pieces a round; 32 rows: 4) and sums them before TMEM
+    (7, 5120, 17408), (25, 1536, 4096), (32, 4096, 14336),
 ]
 
 
@@ -59,7 +62,7 @@ def test_gemm_store_and_residual(mb, M, N, K, epi):
 
 @pytest.mark.parametrize("M,F,K", [(68, 1024, 256), (200, 1536, 512), (576, 14336, 4096), (16, 17408, 5120),
                                    (130, 128, 64), (1040, 1024, 512), (2216, 2048, 1024),
-                                   (700, 1024, 512), (1030, 256, 12288)])
+                                   (700, 1024, 512), (1030, 256, 12288), (20, 2048, 8192)])
 def test_gemm_swiglu(mb, M, F, K):
     A, B, _ = _inputs(M, 2 * F, K, M + F + K)
     dA, dB = to_dev(A), to_dev(B)
