@@ -79,10 +79,7 @@ constexpr int kWideMinRows = 1024;     // from this many tokens on, tiles have t
 #ifndef MB_GEMM_PAIR_STAGES
 #define MB_GEMM_PAIR_STAGES 6
 #endif
-#ifndef MB_GEMM_PEEL
-#define MB_GEMM_PEEL 1                 // 1: rows past the last multiple of 256 run as a 128-row-tile launch
-#endif
-constexpr int kPeelMinKSteps = 192;    // ... for GEMMs of at least this many K steps
+constexpr int kLongKSteps = 192;       // stream-K over the last partial wave only from here on
 
 // Tile configurations: NH halves of 128 rows per tile.
 //  NH = 1: 128 x 256 tiles, 4 stages of 48 KB, two TMEM accumulators, so the
@@ -950,42 +947,11 @@ static int gemm_sms(int max_ctas) {
   return sms;
 }
 
-int gemm_launches(int M, int N, int K, int epi, int max_ctas) {
-  const int tail = M % (2 * HM);
-  if (M <= 0) return 0;
-  if (!(MB_GEMM_PEEL && MB_GEMM_PAIRS == 1 && M >= kWideMinRows && tail > 0 && tail <= HM &&
-        K / BK >= kPeelMinKSteps))
-    return 1;
-  // the rows before the tail must fill at least two waves of CTA pairs
-  const long long tiles_n = epi == kEpiSwiGLU ? N / 128 : (N + BN - 1) / BN;
-  const long long main_tiles = static_cast<long long>(M / (2 * HM)) * tiles_n;
-  return main_tiles >= 2LL * (gemm_sms(max_ctas) / 2) ? 2 : 1;
-}
+int gemm_launches(int M, int, int, int, int) { return M > 0 ? 1 : 0; }
 
 cudaError_t gemm_run(const void *A, const void *B, const CUtensorMap *tmB_pre, void *D, const void *R, int M, int N,
                      int K, int epi, const GemmWorkspace &ws, int *err, cudaStream_t st) {
   if (M <= 0) return cudaSuccess;
-  // From kWideMinRows tokens the tiles are 256 rows over CTA pairs.  When M
-  // mod 256 is 1..128, the last row of pair tiles is mostly padding and its
-  // tiles cost as much as full ones; for long K the rows past the last
-  // multiple of 256 then run as a second launch of 128-row tiles (the same
-  // stream; the second kernel's grid-dependency wait orders its use of the
-  // workspace).  Measured on GB300 at 2,144 tokens (Qwen3-14B shapes): the
-  // down projection (272 K steps) 325 -> 301 us; QKV, O and gate/up (80 K
-  // steps) 111 -> 139, 93 -> 126 and 449 -> 492 us, where the tail launch's
-  // split fix-ups cost more than the padding; hence the K threshold.  At
-  // 1,040 tokens (1,024 rows: 80 pair tiles for 76 pairs) the peeled down
-  // projection was slower too, hence at least two waves before the tail.
-  if (gemm_launches(M, N, K, epi, ws.max_ctas) == 2) {
-    const int tail = M % (2 * HM);
-    const int Mm = M - tail;
-    cudaError_t e = gemm_run(A, B, tmB_pre, D, R, Mm, N, K, epi, ws, err, st);
-    if (e != cudaSuccess) return e;
-    const size_t a_off = static_cast<size_t>(Mm) * K, d_off = static_cast<size_t>(Mm) * N;
-    return gemm_run(static_cast<const __nv_bfloat16 *>(A) + a_off, B, tmB_pre,
-                    static_cast<__nv_bfloat16 *>(D) + d_off,
-                    R ? static_cast<const __nv_bfloat16 *>(R) + d_off : nullptr, tail, N, K, epi, ws, err, st);
-  }
   const int b_rows = epi == kEpiSwiGLU ? 2 * N : N;
   CUtensorMap tmA, tmB;
   cudaError_t e = encode_tmap_2d(&tmA, A, K, M, static_cast<uint64_t>(K) * 2, BK, HM);
@@ -1043,10 +1009,22 @@ cudaError_t gemm_run(const void *A, const void *B, const CUtensorMap *tmB_pre, v
     p.grid = sms;
   } else {
     p.cluster = base_cluster;
-    // Whole waves run data-parallel; the last one to two waves are spread
-    // along K over every SM.
+    // Whole waves run data-parallel; the rest is spread along K over every SM
+    // (stream-K).  Short K: the last one to two waves.  Long K: only the last
+    // partial wave.  A rank's stream-K range starts at its own K offset in
+    // its tile, so ranks that share a weight tile read it at different times;
+    // with long K that is more than L2 holds, and the weights come from HBM
+    // once per rank.  Measured on GB300 (down projection, 272 K steps, 5,120
+    // wide): 2,304 tokens (180 pair tiles for 76 pairs) 315 -> 236 us, 2,216
+    // 309 -> 236, 4,100 490 -> 416; at 80 K steps (QKV, O, gate/up at 2,144
+    // tokens) one extra wave of stream-K stays faster (100 against 104 us,
+    // 82 / 86, 412 / 428).  With this, a long-K GEMM whose last pair tiles
+    // are mostly padding (2,144 = 8 x 256 + 96) also needs no second launch
+    // for those rows: 234 us in one launch against 266 with the 96 rows as a
+    // 128-row-tile launch of their own.
     const int waves = tiles / sms;
-    p.dp_tiles = waves >= 2 ? (waves - 1) * sms : 0;
+    const int sk_waves = p.k_iters >= kLongKSteps ? 0 : 1;
+    p.dp_tiles = waves >= 1 + sk_waves ? (waves - sk_waves) * sms : 0;
     p.sk_tiles = tiles - p.dp_tiles;
     const long long sk_iters = static_cast<long long>(p.sk_tiles) * p.k_iters;
     long long g = sms;

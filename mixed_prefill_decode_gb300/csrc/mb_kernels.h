@@ -34,8 +34,8 @@ GemmWorkspace gemm_workspace_carve(void *base);
 // 64 x 128) or nullptr.
 cudaError_t gemm_run(const void *A, const void *B, const CUtensorMap *tmB, void *D, const void *R, int M, int N,
                      int K, int epi, const GemmWorkspace &ws, int *err, cudaStream_t st);
-// Kernel launches gemm_run issues for an M x N x K GEMM with epilogue epi (2
-// when the rows past the last multiple of 256 run as a launch of their own).
+// Kernel launches gemm_run issues for an M x N x K GEMM with epilogue epi
+// (one, or none for M = 0).
 int gemm_launches(int M, int N, int K, int epi, int max_ctas);
 
 // Error code recorded by the allocation-free GEMM on the current device since
