@@ -80,12 +80,12 @@ def workload_by_name(name: str) -> W.Workload:
 # capture, keyed by kernel; each is valid only for the sources it was captured on
 # and reads as null once any of them changes.
 NCU_TRAFFIC = {
-    "gemm_gate_up": {"bytes": 253.111296e6, "sha256_16": "0b09e0cf7d698eff",
+    "gemm_gate_up": {"bytes": 283.514368e6, "sha256_16": "8cd9206735faa4f9",
                      "sources": ("csrc/mb_gemm.cu", "csrc/mb_ptx.cuh", "csrc/mb_kernels.h"),
-                     "capture": "profiles/launches_llama3_8b_T576.md (llama3_8b_T576, second warm-up step)"},
+                     "capture": "profiles/gemm_llama3_8b_T576.md (llama_T576 case, the third GEMM of the fourth step)"},
     # mean over the 16 chunk-alone launches of the prompt sweep (one capture
     # of each: bench.py --case chunk_all), as the roofline's time is
-    "attention_chunk": {"bytes": 173.722544e6, "sha256_16": "7dc2177f2d536c1d",
+    "attention_chunk": {"bytes": 174.162624e6, "sha256_16": "f90f9b67c5edf647",
                         "sources": ("csrc/mb_attn.cu", "csrc/mb_ptx.cuh", "csrc/mb_kernels.h", "csrc/mb_api.cpp"),
                         "capture": "profiles/attention_chunk_qwen3_14b_P30720.md (chunk_all, 16 launches)"},
 }
@@ -1334,6 +1334,9 @@ PROFILE_CASES = {
     "sweep_all": dict(k=None, decodes=True, chunk=True),
     # the chunk alone at every position (the roofline's launches)
     "chunk_all": dict(k=None, decodes=False, chunk=True),
+    # one Llama-3-8B-shaped layer on the 576-token mixed batch (64 decodes +
+    # a 512-token chunk), the auxiliary layer line's batch
+    "llama_T576": dict(workload="llama3_8b_mixed"),
 }
 
 
@@ -1349,14 +1352,22 @@ def run_case(args):
     B.build()
     peaks, peak_kind = load_peaks()
     spec = PROFILE_CASES[args.case]
-    sw = W.qwen3_14b_prompt_sweep()
-    sh = sw.shape
-    full, num_pages = sw.layout()
-    ks = range(sw.steps) if spec["k"] is None else [spec["k"]]
-    batches = [sw.batch_at(k, full, with_decodes=spec["decodes"], with_chunk=spec["chunk"]) for k in ks]
+    if "workload" in spec:   # a fixed batch of a named workload
+        wl = getattr(W, spec["workload"])()
+        sh = wl.shape
+        batch, num_pages = W.make_batch(wl.reqs, wl.seed + 2)   # the layout materialize() gives it
+        batches = [batch]
+        dw = W.device_weights(sh, wl.seed + 100)
+        dpool = W.device_kv_pool(sh, num_pages, wl.seed + 200)
+    else:                    # positions of the prompt sweep
+        sw = W.qwen3_14b_prompt_sweep()
+        sh = sw.shape
+        full, num_pages = sw.layout()
+        ks = range(sw.steps) if spec["k"] is None else [spec["k"]]
+        batches = [sw.batch_at(k, full, with_decodes=spec["decodes"], with_chunk=spec["chunk"]) for k in ks]
+        dw = W.device_weights(sh, sw.seed + 100)
+        dpool = W.device_kv_pool(sh, num_pages, sw.seed + 200)
     T = max(b.num_tokens for b in batches)
-    dw = W.device_weights(sh, sw.seed + 100)
-    dpool = W.device_kv_pool(sh, num_pages, sw.seed + 200)
     layer = mb.Layer(sh.as_dict(), dw, T, num_pages, kv_buf=dpool)
     cbs = [mb.Batch.of(b) for b in batches]
     x = torch.randn((T, sh.d_model), device="cuda").to(torch.bfloat16)
@@ -1391,7 +1402,7 @@ def run_case(args):
     out = {"case": args.case, "tokens": sum(b.num_tokens for b in batches), "positions": len(batches),
            "launches_per_step": mb.mb_layer_last_launches(layer.handle) * len(batches),
            "kernels": kernel_table(alg, km_step, n, peaks)}
-    if not spec["decodes"] and spec["chunk"]:
+    if not spec.get("decodes", True) and spec.get("chunk", True):
         fl = alg["attention"][1][0]
         out["chunk_attention"] = {"flop": fl, "tflops": round(fl / (km_step["attention"] / n / 1e3) / 1e12, 1)}
     print(json.dumps(out), flush=True)
