@@ -210,6 +210,7 @@ __device__ __forceinline__ void chunk_tile(const CUtensorMap &tmQ, const CUtenso
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   pdl_wait();   // q, the KV pool and o belong to earlier kernels of the stream
+  pdl_trigger();
 
   if (warp == 0) {
     // -------------------------------------------------------- TMA producer
@@ -702,6 +703,7 @@ __device__ __forceinline__ void decode_worker(const CUtensorMap &tmKV, const CUt
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   pdl_wait();   // q, the KV pool, o and the work counter belong to earlier kernels
+  pdl_trigger();
 
   if (warp == 0) {
     // -------------------------------------------------------- TMA producer

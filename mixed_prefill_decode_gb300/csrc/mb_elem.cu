@@ -31,6 +31,7 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const __nv_bfloat
                                                                __nv_bfloat16 *__restrict__ y, int d, float eps,
                                                                const int32_t *__restrict__ rows, int n_src, int *err) {
   pdl_wait();
+  pdl_trigger();
   const int row = blockIdx.x;
   const int nv = d / 8;
   int src = row;
@@ -153,6 +154,7 @@ __global__ void __launch_bounds__(kRopeThreads) rope_append_kernel(const RopePar
   __shared__ float cs[HALF], sn[HALF];
   __shared__ int s_page;
   pdl_wait();
+  pdl_trigger();
   const int t = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int heads = p.Hq + 2 * p.Hkv;
@@ -259,6 +261,7 @@ __device__ __forceinline__ bool argmax_better(float v, int i, float bv, int bi) 
 __global__ void __launch_bounds__(kArgmaxThreads) argmax_kernel(const __nv_bfloat16 *__restrict__ logits, int vocab,
                                                                 int32_t *__restrict__ ids) {
   pdl_wait();
+  pdl_trigger();
   const int row = blockIdx.x;
   const uint4 *lr = reinterpret_cast<const uint4 *>(logits + static_cast<size_t>(row) * vocab);
   float bv = -INFINITY;
@@ -299,6 +302,7 @@ __global__ void __launch_bounds__(kEmbedThreads) embed_kernel(const __nv_bfloat1
                                                               const int32_t *__restrict__ ids,
                                                               __nv_bfloat16 *__restrict__ out, int *err) {
   pdl_wait();
+  pdl_trigger();
   const int row = blockIdx.x;
   const int id = ids[row];
   uint4 *o = reinterpret_cast<uint4 *>(out + static_cast<size_t>(row) * d);

@@ -159,6 +159,7 @@ struct Params {
   int *err;
   uint64_t split_wait_ns;   // limit of the head piece's wait for the other pieces of its tile
   int split_phantom;        // pieces the head also waits for that no CTA writes (failure-path tests; 0)
+  int b_const;              // 1: no kernel of the stream writes B (a layer's weights): loaded before the wait
   // First (unit, k) iteration of each rank; rlo[ranks] = all iterations.
   // Filled on the host (fill_rank_bounds) so that no CTA divides 64-bit
   // numbers before its first load.
@@ -409,11 +410,13 @@ __global__ void __launch_bounds__(TileCfg<NH, PAIR>::THREADS, 1)
     return nh * A_HALF + B_STG;
   };
 
-  // The weights are read-only for the whole stream: while earlier kernels
-  // finish, arm the first stages and load their weight tiles (and warm L2
-  // with the next ones); only the activation tiles wait for those kernels.
+  // A layer's weights are read-only for the whole stream: while earlier
+  // kernels finish, arm the first stages and load their weight tiles (and
+  // warm L2 with the next ones); only the activation tiles wait for those
+  // kernels.  Other B operands (standalone calls) may come from the kernel
+  // just before: they wait like A.
   int pre = 0;   // stages whose weight tiles are already on their way
-  if (warp == 0 && lane == 0) {
+  if (warp == 0 && lane == 0 && p.b_const) {
     SegIter first(p, sched_b, blockIdx.x);
     Seg s0;
     if (first.next(s0)) {
@@ -443,6 +446,7 @@ __global__ void __launch_bounds__(TileCfg<NH, PAIR>::THREADS, 1)
     }
   }
   pdl_wait();   // A, R, D, the tickets and partials belong to earlier kernels of the stream
+  pdl_trigger();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -1043,6 +1047,7 @@ cudaError_t gemm_run(const void *A, const void *B, const CUtensorMap *tmB_pre, v
   p.err = err;
   p.split_wait_ns = g_split_wait_ns.load(std::memory_order_relaxed);
   p.split_phantom = g_split_phantom.load(std::memory_order_relaxed);
+  p.b_const = tmB_pre != nullptr;   // the layers' pre-encoded weight maps
   if (!fill_rank_bounds(p)) return cudaErrorInvalidValue;
   return launch_for(epi, nh == 1 && M <= kFoldBatchRows ? kModeFew : nh, tmA, tmB, p, st);
 }

@@ -31,7 +31,9 @@ GemmWorkspace gemm_workspace_carve(void *base);
 
 // D = A B^T (+ R) or SwiGLU; A [M][K], B [Nb][K] (Nb = N, or 2F for SwiGLU
 // where N = F is the output width).  tmB may be a pre-encoded map of B (box
-// 64 x 128) or nullptr.
+// 64 x 128) or nullptr.  A pre-encoded map marks B as a layer's weights, which
+// no kernel of the stream writes: the kernel loads its first weight tiles
+// before its grid-dependency wait.  With nullptr, B waits like A.
 cudaError_t gemm_run(const void *A, const void *B, const CUtensorMap *tmB, void *D, const void *R, int M, int N,
                      int K, int epi, const GemmWorkspace &ws, int *err, cudaStream_t st);
 // Kernel launches gemm_run issues for an M x N x K GEMM with epilogue epi

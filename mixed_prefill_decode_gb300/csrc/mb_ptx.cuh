@@ -63,6 +63,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // Programmatic dependent launch (see mb_launch.cuh): wait until every earlier
 // kernel of the stream has finished and its writes are visible.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Let the next kernel of the stream be scheduled once every CTA of this grid
+// has run this (or exited): its CTAs then take SMs as this grid's free up and
+// run their set-up, and wait in pdl_wait() for this grid to finish.  Every
+// kernel here issues it after its own pdl_wait(), and reads or writes
+// nothing an earlier kernel touches before that wait.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // Non-blocking probe of a phase (try_wait may suspend the thread for a while;
 // a thread that polls two barriers must not sleep on either).
