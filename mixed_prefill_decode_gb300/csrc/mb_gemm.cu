@@ -27,11 +27,12 @@
 //             configuration (NH = 2, not used by the dispatcher) adds warps 6-9
 //   TMEM      all 512 columns
 //   schedule  persistent; whole tiles data-parallel while there are several
-//             waves, the last one to two waves split along K evenly over all
-//             CTAs (stream-K).  A split tile's later pieces go to fp32 partial
-//             slots; the CTA that holds the tile's first piece waits (bounded)
-//             for them, adds them in rank order (deterministic) and runs the
-//             epilogue.  That wait needs every CTA of the grid resident at
+//             waves, the rest split along K evenly over all CTAs (stream-K:
+//             the last one to two waves below 192 K steps, the last partial
+//             wave from there on).  A split tile's later pieces go to fp32
+//             partial slots (the rows of A only); the CTA that holds the
+//             tile's first piece waits (bounded) for them, adds them in rank
+//             order (deterministic) and runs the epilogue.  That wait needs every CTA of the grid resident at
 //             once: the grid never exceeds the SM count, or the number of
 //             clusters the occupancy query says fit.
 //   epilogues store | + residual | SwiGLU (B rows [gate F; up F]: a tile loads

@@ -110,3 +110,21 @@ def test_split_wait_expiry_reports_and_recovers(mb):
         assert_close(f"after expiry {rep}", f64(from_dev(dD)), ref)
     with pytest.raises(mb.MbError):
         mb.mb_gemm_set_split_wait(0, -1)
+
+
+def test_gemm_reads_b_written_by_the_kernel_just_before(mb):
+    """A standalone call's B may come from the kernel just before it on the
+    stream: B waits for that kernel like A does (only a layer's own weights
+    are loaded before the grid-dependency wait).  B is rewritten on the device
+    right before each call, and the result must follow the new B."""
+    M, N, K = 576, 4096, 4096
+    A, B0, _ = _inputs(M, N, K, 11)
+    _, B1, _ = _inputs(M, N, K, 12)
+    s = torch.cuda.current_stream().cuda_stream
+    dA, dB, dB0, dB1 = to_dev(A), to_dev(B0), to_dev(B0), to_dev(B1)
+    dD = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    for src, Bh in ((dB1, B1), (dB0, B0), (dB1, B1)):
+        torch.mul(src, 1, out=dB)   # an elementwise kernel writes B (exactly), then the GEMM at once
+        mb.mb_gemm(dA, dB, dD, None, M, N, K, 0, None, s)
+        mb.mb_device_status(None, s)
+        assert_close(f"gemm after B rewritten {M}x{N}x{K}", f64(from_dev(dD)), OL.linear(f64(A), f64(Bh)))
