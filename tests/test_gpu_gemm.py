@@ -28,9 +28,9 @@ SHAPES = [
     # grouped schedule with every N-tile split along K (the down projection at
     # 576 tokens: 224 K steps over two groups)
     (576, 4096, 14336),
-    # at least 192 K steps with M mod 256 in 1..128 from 1,024 tokens: with two
-    # waves of pair tiles before them, the rows past the last multiple of 256
-    # run as a launch of their own (2144 x 5120); otherwise they stay (1100)
+    # at least 192 K steps: stream-K covers only the last partial wave of pair
+    # tiles (2144 x 5120: 180 tiles, two whole waves on 76 pairs); 1100 x 512
+    # (five M-tiles) takes the grouped schedule, its N-tiles split along K
     (1100, 512, 12288), (2144, 5120, 12288),
     # at most 32 rows with split tiles: the head stages every piece at once
     # (7 rows: 18 pieces a round; 32 rows: 4) and sums them before TMEM
