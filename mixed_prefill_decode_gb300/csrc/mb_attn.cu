@@ -658,9 +658,10 @@ __device__ __forceinline__ void decode_worker(const CUtensorMap &tmKV, const CUt
   float *red = reinterpret_cast<float *>(smem + C::OFF_RED);     // [max | sum][4 warps][16]
   volatile int *merge_flag = reinterpret_cast<volatile int *>(smem + C::OFF_FLAG);
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
-  uint64_t *kv_full = bars;                  // [STAGES]
-  uint64_t *kv_empty = bars + C::STAGES;     // [STAGES]
-  uint64_t *q_full = bars + 2 * C::STAGES;   // [2]
+  uint64_t *k_full = bars;                   // [STAGES]: the block's K landed (and its header is set)
+  uint64_t *v_full = bars + C::STAGES;       // [STAGES]: the block's V landed
+  uint64_t *kv_empty = bars + 2 * C::STAGES; // [STAGES]
+  uint64_t *q_full = bars + 3 * C::STAGES;   // [2]
   uint64_t *q_empty = q_full + 2;            // [2]
   uint64_t *s_full = q_full + 4;             // [2]
   uint64_t *s_empty = q_full + 6;            // [2]
@@ -676,7 +677,8 @@ __device__ __forceinline__ void decode_worker(const CUtensorMap &tmKV, const CUt
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
-      mbar_init(&kv_full[s], 1);
+      mbar_init(&k_full[s], 1);
+      mbar_init(&v_full[s], 1);
       mbar_init(&kv_empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -709,10 +711,12 @@ __device__ __forceinline__ void decode_worker(const CUtensorMap &tmKV, const CUt
     // -------------------------------------------------------- TMA producer
     // The whole warp: lane 0 waits, fetches work and arms each stage, then
     // the block's 8 pages x (K, V) x hd chunks go out as one TMA per lane
-    // (a single thread needs ~90 cycles per copy, which would pace the ring).
-    // Global loads the producer depends on (the next item, the next block's
-    // page ids, one per lane) are issued a block ahead.
-    const int my_pg = lane >> 1, my_kv = lane & 1;   // one copy per (page, K or V): lanes 0-15
+    // (a single thread needs ~90 cycles per copy, which would pace the ring):
+    // the K copies first (lanes 0-7), on a barrier of their own, so that the
+    // block's S can start while its V is still arriving.  Global loads the
+    // producer depends on (the next item, the next block's page ids, one per
+    // lane) are issued a block ahead.
+    const int my_pg = lane & 7, my_kv = lane >> 3;   // one copy per (page, K or V): lanes 0-15
     int seq = 0, k_local = 0;
     bool ok = true;
     int next_item = lane == 0 ? atomicAdd(&p.ctr[0], 1) : 0;
@@ -723,7 +727,7 @@ __device__ __forceinline__ void decode_worker(const CUtensorMap &tmKV, const CUt
           const int s = seq % C::STAGES;
           if (mbar_wait(&kv_empty[s], ((seq / C::STAGES) & 1) ^ 1, abort_flag, p.err, kErrWaitProducer)) {
             hdr[s].item = -1;
-            mbar_arrive(&kv_full[s]);
+            mbar_arrive(&k_full[s]);
           }
         }
         break;
@@ -759,7 +763,8 @@ __device__ __forceinline__ void decode_worker(const CUtensorMap &tmKV, const CUt
             hdr[s].nvalid = min(npg * 16, kv - pg0 * 16);
             hdr[s].flags = (b == 0 ? 1 : 0) | (b == nblk - 1 ? 2 : 0);
             hdr[s].qb = qb;
-            mbar_arrive_expect_tx(&kv_full[s], npg * 2 * C::NH * 2048);
+            mbar_arrive_expect_tx(&k_full[s], npg * C::NH * 2048);
+            mbar_arrive_expect_tx(&v_full[s], npg * C::NH * 2048);
           }
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -771,8 +776,8 @@ __device__ __forceinline__ void decode_worker(const CUtensorMap &tmKV, const CUt
             page = 0;
           }
           const int z = (page * 2 + my_kv) * p.Hkv + hk;
-          tma_load_5d(sKV + s * C::KV_STAGE + my_kv * C::NH * C::TILE + my_pg * C::PAGE_BYTES, &tmKV, &kv_full[s], 0,
-                      0, 0, 0, z);
+          tma_load_5d(sKV + s * C::KV_STAGE + my_kv * C::NH * C::TILE + my_pg * C::PAGE_BYTES, &tmKV,
+                      my_kv ? &v_full[s] : &k_full[s], 0, 0, 0, 0, z);
         }
         ++seq;
       }
@@ -782,7 +787,10 @@ __device__ __forceinline__ void decode_worker(const CUtensorMap &tmKV, const CUt
     if (lane == 0 && (!ok || *abort_flag)) {
       for (int i = max(0, seq - C::STAGES); i < seq; ++i) {
         const uint64_t t0 = globaltimer();
-        while (!mbar_try_wait(smem_u32(&kv_full[i % C::STAGES]), (i / C::STAGES) & 1) &&
+        while (!mbar_try_wait(smem_u32(&k_full[i % C::STAGES]), (i / C::STAGES) & 1) &&
+               globaltimer() - t0 < kWaitLimitNs) {
+        }
+        while (!mbar_try_wait(smem_u32(&v_full[i % C::STAGES]), (i / C::STAGES) & 1) &&
                globaltimer() - t0 < kWaitLimitNs) {
         }
       }
@@ -827,7 +835,7 @@ __device__ __forceinline__ void decode_worker(const CUtensorMap &tmKV, const CUt
         bool progress = false;
         if (!s_end) {
           const int s = ns % C::STAGES;
-          if (mbar_test_wait(smem_u32(&kv_full[s]), (ns / C::STAGES) & 1)) {
+          if (mbar_test_wait(smem_u32(&k_full[s]), (ns / C::STAGES) & 1)) {
             if (hdr[s].item < 0) {
               s_end = progress = true;
             } else {
@@ -848,7 +856,8 @@ __device__ __forceinline__ void decode_worker(const CUtensorMap &tmKV, const CUt
           }
         }
         if (npv < ns && mbar_test_wait(smem_u32(&p_full[npv & 1]), (npv >> 1) & 1) &&
-            mbar_test_wait(smem_u32(&o_empty[npv & 1]), ((npv >> 1) & 1) ^ 1)) {
+            mbar_test_wait(smem_u32(&o_empty[npv & 1]), ((npv >> 1) & 1) ^ 1) &&
+            mbar_test_wait(smem_u32(&v_full[npv % C::STAGES]), (npv / C::STAGES) & 1)) {
           tc_fence_after();
           issue_pv(npv, npv % C::STAGES);
           ++npv;
@@ -893,7 +902,7 @@ __device__ __forceinline__ void decode_worker(const CUtensorMap &tmKV, const CUt
     bool ok = true;
     for (int j = 0;; ++j) {
       const int s = j % C::STAGES;
-      bool bad = !ok || !mbar_wait(&kv_full[s], (j / C::STAGES) & 1, abort_flag, p.err, kErrWaitSoftmax);
+      bool bad = !ok || !mbar_wait(&k_full[s], (j / C::STAGES) & 1, abort_flag, p.err, kErrWaitSoftmax);
       const DecHdr h = hdr[s];
       if (named_bar_or(1, 128, bad) || h.item < 0) break;
       bad = !mbar_wait(&s_full[j & 1], (j >> 1) & 1, abort_flag, p.err, kErrWaitSoftmax);
@@ -956,7 +965,9 @@ __device__ __forceinline__ void decode_worker(const CUtensorMap &tmKV, const CUt
 #pragma unroll
       for (int g = 0; g < G; ++g)
         *reinterpret_cast<__nv_bfloat16 *>(pt + sw128_offset(g, t & 63)) = __float2bfloat16_rn(pr[g]);
-      if (!valid) {
+      if (h.nvalid < 128 && !mbar_wait(&v_full[s], (j / C::STAGES) & 1, abort_flag, p.err, kErrWaitSoftmax))
+        ok = false;   // the V rows below must have landed before they are patched
+      if (!valid && ok) {
         // a key past kv_len: its V row may hold anything; make it exactly 0
         uint8_t *vrow = sKV + s * C::KV_STAGE + C::NH * C::TILE + (t >> 3) * C::ATOM_STRIDE + (t & 7) * 128;
 #pragma unroll
