@@ -85,7 +85,7 @@ NCU_TRAFFIC = {
                      "capture": "profiles/gemm_llama3_8b_T576.md (llama_T576 case, the third GEMM of the fourth step)"},
     # mean over the 16 chunk-alone launches of the prompt sweep (one capture
     # of each: bench.py --case chunk_all), as the roofline's time is
-    "attention_chunk": {"bytes": 174.480864e6, "sha256_16": "92fd3b621d42096f",
+    "attention_chunk": {"bytes": 174.216528e6, "sha256_16": "fbd573b13e2c7b6f",
                         "sources": ("csrc/mb_attn.cu", "csrc/mb_ptx.cuh", "csrc/mb_kernels.h", "csrc/mb_api.cpp"),
                         "capture": "profiles/attention_chunk_qwen3_14b_P30720.md (chunk_all, 16 launches)"},
 }
