@@ -80,14 +80,14 @@ def workload_by_name(name: str) -> W.Workload:
 # capture, keyed by kernel; each is valid only for the sources it was captured on
 # and reads as null once any of them changes.
 NCU_TRAFFIC = {
-    "gemm_gate_up": {"bytes": 283.620864e6, "sha256_16": "24b575e607457959",
+    "gemm_gate_up": {"bytes": 283.620864e6, "sha256_16": "4ac6531ba35ed8ed",
                      "sources": ("csrc/mb_gemm.cu", "csrc/mb_ptx.cuh", "csrc/mb_kernels.h"),
-                     "capture": "profiles/gemm_llama3_8b_T576.md (llama_T576 case, the third GEMM of the fourth step)"},
+                     "capture": "ncu DRAM bytes of bench.py --case llama_T576, the third GEMM of the fourth step"},
     # mean over the 16 chunk-alone launches of the prompt sweep (one capture
     # of each: bench.py --case chunk_all), as the roofline's time is
     "attention_chunk": {"bytes": 174.216528e6, "sha256_16": "fbd573b13e2c7b6f",
                         "sources": ("csrc/mb_attn.cu", "csrc/mb_ptx.cuh", "csrc/mb_kernels.h", "csrc/mb_api.cpp"),
-                        "capture": "profiles/attention_chunk_qwen3_14b_P30720.md (chunk_all, 16 launches)"},
+                        "capture": "ncu DRAM bytes of bench.py --case chunk_all, the 16 launches of the second pass"},
 }
 
 

@@ -721,7 +721,7 @@ __global__ void __launch_bounds__(TileCfg<NH, PAIR>::THREADS, 1)
               if (FOLDB && mine) {
 #pragma unroll 1
                 for (int g = 0; g < G; ++g) {
-                  const int ig = i0 + (g - i0 % G + G) % G;   // first item of group g in this round
+                  const int ig = i0 + (g - i0 % G + G) % G;   // first item of group g staged now
                   if (ig + G >= i1) continue;                 // at most one item of group g
                   float4 *dst = reinterpret_cast<float4 *>(stage + (ig - i0) * gbytes);
                   const int n4 = static_cast<int>(gbytes / 16);
